@@ -1,0 +1,577 @@
+// C-ABI entry points (include/mlp_step.h): argument checks, workspace
+// carving, tensor-map encoding and the enqueue order of each step.  No
+// arithmetic of the method lives here; every computation is a kernel launch.
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+
+using namespace mlp;
+
+namespace mlp {
+
+// ------------------------------------------------------------ device error word
+
+static __device__ int g_device_error = 0;
+
+// Device address of the error word for the current device (looked up once per
+// device; host code cannot use the symbol itself as a device pointer).
+int* device_error_word() {
+  static int* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int*>(p);
+  }
+  return addr[dev];
+}
+
+// ------------------------------------------------------------ bounded waits
+
+static unsigned long long g_wait_limit_ns = 0;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+
+unsigned long long wait_limit_ns() {
+  return g_wait_limit_ns ? g_wait_limit_ns : kDefaultWaitNs;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [outer][inner] with the given row pitch; box
+// [box_outer][box_inner] with 128-byte swizzle; out-of-range elements read 0.
+bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, unsigned long long inner,
+                         unsigned long long outer, unsigned long long row_stride_bytes,
+                         unsigned box_inner, unsigned box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace mlp
+
+namespace {
+
+inline cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline int round8(int x) { return (x + 7) / 8 * 8; }
+
+// ------------------------------------------------------------ GEMM checks
+
+mlp_status check_gemm(const GemmArgs& g, int in_dtype, int c_dtype) {
+  if (g.M < 0 || g.N < 0 || g.K < 0) return MLP_ERR_INVALID_ARG;
+  if (in_dtype != MLP_DTYPE_F32 && in_dtype != MLP_DTYPE_BF16) return MLP_ERR_INVALID_ARG;
+  if (c_dtype != MLP_DTYPE_F32 && c_dtype != MLP_DTYPE_BF16) return MLP_ERR_INVALID_ARG;
+  if (g.act != MLP_ACT_NONE && g.act != MLP_ACT_RELU) return MLP_ERR_INVALID_ARG;
+  if (g.M == 0 || g.N == 0) return MLP_OK;
+  if (!g.C) return MLP_ERR_INVALID_ARG;
+  if (g.K > 0 && (!g.A || !g.B)) return MLP_ERR_INVALID_ARG;
+  // leading dimensions must cover the stored rows
+  const int a_row = g.a_trans ? g.M : g.K;
+  const int b_row = g.b_trans ? g.K : g.N;
+  if (g.K > 0 && (g.lda < a_row || g.ldb < b_row)) return MLP_ERR_INVALID_ARG;
+  if (g.ldc < g.N) return MLP_ERR_INVALID_ARG;
+  if (g.mask && g.ldm < g.N) return MLP_ERR_INVALID_ARG;
+  if (!aligned16(g.C) || (g.K > 0 && (!aligned16(g.A) || !aligned16(g.B))) ||
+      (g.mask && !aligned16(g.mask)) || (g.bias && !aligned16(g.bias)))
+    return MLP_ERR_MISALIGNED;
+  if (in_dtype == MLP_DTYPE_BF16 && g.K > 0) {
+    // TMA: rows must start on 16-byte boundaries
+    if (((long long)g.lda * 2) % 16 != 0 || ((long long)g.ldb * 2) % 16 != 0)
+      return MLP_ERR_MISALIGNED;
+    if ((long long)g.lda * 2 >= (1ll << 40) || (long long)g.ldb * 2 >= (1ll << 40))
+      return MLP_ERR_UNSUPPORTED_SHAPE;
+  }
+  return MLP_OK;
+}
+
+mlp_status run_gemm(const GemmArgs& g, int in_bf16, cudaStream_t st) {
+  if (in_bf16) return launch_gemm_tc(g, wait_limit_ns(), st);
+  return launch_gemm_simt(g, 0, st);
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* mlp_status_string(mlp_status s) {
+  switch (s) {
+    case MLP_OK: return "ok";
+    case MLP_ERR_INVALID_ARG: return "invalid argument";
+    case MLP_ERR_MISALIGNED: return "pointer or leading dimension not 16-byte aligned";
+    case MLP_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MLP_ERR_CUDA: return "CUDA error";
+    case MLP_ERR_DEVICE_TIMEOUT: return "a kernel abandoned a bounded wait";
+    case MLP_ERR_NUMERIC: return "non-finite loss";
+    default: return "unknown status";
+  }
+}
+
+mlp_status mlp_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return MLP_ERR_CUDA;
+  int err = 0;
+  if (cudaMemcpyFromSymbol(&err, g_device_error, sizeof(int)) != cudaSuccess) return MLP_ERR_CUDA;
+  if (err != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return MLP_ERR_CUDA;
+    return MLP_ERR_DEVICE_TIMEOUT;
+  }
+  return MLP_OK;
+}
+
+void mlp_set_wait_limit_ns(long long ns) { g_wait_limit_ns = ns > 0 ? (unsigned long long)ns : 0; }
+
+mlp_status mlp_selftest_wait_timeout(long long limit_ns, void* stream) {
+  if (limit_ns <= 0) return MLP_ERR_INVALID_ARG;
+  return launch_wait_selftest((unsigned long long)limit_ns, S(stream));
+}
+
+// ------------------------------------------------------------ generic kernels
+
+mlp_status mlp_gemm(int M, int N, int K, const void* A, int lda, int a_trans, const void* B,
+                    int ldb, int b_trans, int in_dtype, const float* bias, int act,
+                    const void* mask, int ldm, void* C, int ldc, int c_dtype, void* stream) {
+  GemmArgs g{M, N, K, A, lda, a_trans ? 1 : 0, B, ldb, b_trans ? 1 : 0, bias, act, mask, ldm,
+             C, ldc, c_dtype == MLP_DTYPE_BF16 ? 1 : 0};
+  MLP_CHECK(check_gemm(g, in_dtype, c_dtype));
+  if (M == 0 || N == 0) return MLP_OK;
+  return run_gemm(g, in_dtype == MLP_DTYPE_BF16, S(stream));
+}
+
+size_t mlp_colsum_workspace_bytes(int rows, int cols) {
+  if (rows <= 0 || cols <= 0) return 0;
+  return colsum_workspace_bytes(rows, cols);
+}
+
+mlp_status mlp_colsum(const void* X, int dtype, int rows, int cols, int ld, float* out,
+                      void* workspace, size_t ws_bytes, void* stream) {
+  if (rows < 0 || cols < 0) return MLP_ERR_INVALID_ARG;
+  if (dtype != MLP_DTYPE_F32 && dtype != MLP_DTYPE_BF16) return MLP_ERR_INVALID_ARG;
+  if (cols == 0) return MLP_OK;
+  if (!out || (rows > 0 && !X) || ld < cols) return MLP_ERR_INVALID_ARG;
+  const size_t need = mlp_colsum_workspace_bytes(rows, cols);
+  if (need > 0 && (!workspace || ws_bytes < need)) return MLP_ERR_INVALID_ARG;
+  if ((X && !aligned16(X)) || !aligned16(out) || (workspace && !aligned16(workspace)))
+    return MLP_ERR_MISALIGNED;
+  return launch_colsum(X, dtype == MLP_DTYPE_BF16, rows, cols, ld, out, workspace, S(stream));
+}
+
+size_t softmax_xent_workspace_bytes(int batch, int classes) {
+  (void)classes;
+  return batch > 0 ? xent_workspace_bytes(batch) : 0;
+}
+
+mlp_status softmax_xent_fwd_bwd(const float* logits, int ld_logits, const int32_t* labels,
+                                int batch, int classes, float* loss_out, void* dlogits,
+                                int dlogits_dtype, int ld_dlogits, int32_t* argmax_out,
+                                void* workspace, size_t ws_bytes, void* stream) {
+  if (batch < 0 || classes <= 0) return MLP_ERR_INVALID_ARG;
+  if (batch == 0) return MLP_OK;
+  if (!logits || !labels || ld_logits < classes) return MLP_ERR_INVALID_ARG;
+  if (dlogits && (ld_dlogits < classes ||
+                  (dlogits_dtype != MLP_DTYPE_F32 && dlogits_dtype != MLP_DTYPE_BF16)))
+    return MLP_ERR_INVALID_ARG;
+  const size_t need = softmax_xent_workspace_bytes(batch, classes);
+  if (need > 0 && (!workspace || ws_bytes < need)) return MLP_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(labels) || (dlogits && !aligned16(dlogits)) ||
+      (argmax_out && !aligned16(argmax_out)) || (loss_out && !aligned16(loss_out)) ||
+      (workspace && !aligned16(workspace)))
+    return MLP_ERR_MISALIGNED;
+  return launch_xent(logits, ld_logits, labels, batch, classes, loss_out, dlogits,
+                     dlogits_dtype == MLP_DTYPE_BF16, ld_dlogits, argmax_out, workspace,
+                     S(stream));
+}
+
+mlp_status sgd_momentum_step(float* w, const float* g, float* v, void* w_bf16, size_t n,
+                             float lr, float momentum, void* stream) {
+  if (n == 0) return MLP_OK;
+  if (!w || !g || !v) return MLP_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(g) || !aligned16(v) || (w_bf16 && !aligned16(w_bf16)))
+    return MLP_ERR_MISALIGNED;
+  SgdSegments segs{};
+  segs.n = 1;
+  segs.flat_off[0] = 0;
+  segs.shadow_off[0] = w_bf16 ? 0 : -1;
+  segs.cols[0] = 1;
+  segs.cols_pad[0] = 1;
+  return launch_sgd(w, g, v, static_cast<__nv_bfloat16*>(w_bf16), (long long)n, lr, momentum,
+                    segs, S(stream));
+}
+
+size_t mse_workspace_bytes(size_t n) { return n ? mse_ws_bytes((long long)n) : 0; }
+
+mlp_status mse_loss_fwd_bwd(const void* y, const void* t, size_t n, float* loss_out, void* dy,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  if (n == 0) return MLP_OK;
+  if (!y || !t || !workspace || ws_bytes < mse_workspace_bytes(n)) return MLP_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(t) || (dy && !aligned16(dy)) || !aligned16(workspace) ||
+      (loss_out && !aligned16(loss_out)))
+    return MLP_ERR_MISALIGNED;
+  return launch_mse(y, t, (long long)n, loss_out, dy, workspace, S(stream));
+}
+
+}  // extern "C"
+
+// ====================================================================== MLP handle
+
+struct mlp_handle {
+  std::vector<int> dims;
+  int L = 0;
+  int act = MLP_ACT_RELU;
+  int prec = MLP_PREC_FP32;
+  int max_batch = 0;
+  float* params = nullptr;
+  float* velocity = nullptr;
+  float* grads = nullptr;
+  __nv_bfloat16* shadow = nullptr;
+  long long n_params = 0;
+  std::vector<long long> w_off, b_off, shadow_off;
+  std::vector<int> out_pad;        // shadow row pitch per layer
+  std::vector<int> act_ld;         // leading dimension of H_l buffers (l = 0 is the input)
+  void* x_copy = nullptr;          // [max_batch][act_ld[0]]
+  std::vector<void*> acts;         // acts[l] = H_{l+1}, l = 0..L-2
+  float* logits = nullptr;         // [max_batch][C]
+  void* dlogits = nullptr;         // [max_batch][ldz]
+  int ldz = 0;
+  void* dh[2] = {nullptr, nullptr};
+  int dh_ld = 0;
+  float* loss = nullptr;
+  void* red = nullptr;             // reduction partials
+  size_t red_bytes = 0;
+  SgdSegments segs{};
+  const void* x_used = nullptr;    // operand the last forward read as X
+  int x_ld = 0;
+};
+
+namespace {
+
+int esz(int prec) { return prec == MLP_PREC_BF16 ? 2 : 4; }
+
+bool dims_ok(const int* dims, int n_dims) {
+  if (!dims || n_dims < 2 || n_dims > 9) return false;
+  for (int i = 0; i < n_dims; ++i)
+    if (dims[i] <= 0) return false;
+  return true;
+}
+
+struct Plan {
+  size_t x, acts_total, logits, dlogits, dh, loss, red, total;
+};
+
+Plan plan(const int* dims, int n_dims, int max_batch, int prec) {
+  Plan p{};
+  const int L = n_dims - 1;
+  const size_t B = (size_t)max_batch;
+  const int e = esz(prec);
+  p.x = align256(B * round8(dims[0]) * e);
+  p.acts_total = 0;
+  int maxh = 8;
+  for (int l = 1; l < L; ++l) {
+    p.acts_total += align256(B * round8(dims[l]) * e);
+    if (round8(dims[l]) > maxh) maxh = round8(dims[l]);
+  }
+  if (round8(dims[0]) > maxh) maxh = round8(dims[0]);
+  p.logits = align256(B * dims[L] * sizeof(float));
+  p.dlogits = align256(B * round8(dims[L]) * e);
+  p.dh = align256(B * maxh * e);
+  p.loss = 256;
+  size_t red = xent_workspace_bytes(max_batch);
+  for (int l = 0; l < L; ++l) {
+    const size_t c = colsum_workspace_bytes(max_batch, dims[l + 1]);
+    if (c > red) red = c;
+  }
+  p.red = align256(red > 0 ? red : 256);
+  p.total = p.x + p.acts_total + p.logits + p.dlogits + 2 * p.dh + p.loss + p.red;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mlp_param_count(const int* dims, int n_dims) {
+  if (!dims_ok(dims, n_dims)) return 0;
+  size_t n = 0;
+  for (int l = 0; l + 1 < n_dims; ++l) n += (size_t)dims[l] * dims[l + 1] + dims[l + 1];
+  return n;
+}
+
+size_t mlp_param_offset(const int* dims, int n_dims, int layer, int which) {
+  if (!dims_ok(dims, n_dims) || layer < 0 || layer >= n_dims - 1 || (which != 0 && which != 1))
+    return (size_t)-1;
+  size_t off = 0;
+  for (int l = 0; l < layer; ++l) off += (size_t)dims[l] * dims[l + 1] + dims[l + 1];
+  if (which == 1) off += (size_t)dims[layer] * dims[layer + 1];
+  return off;
+}
+
+size_t mlp_shadow_elems(const int* dims, int n_dims) {
+  if (!dims_ok(dims, n_dims)) return 0;
+  size_t n = 0;
+  for (int l = 0; l + 1 < n_dims; ++l) n += (size_t)dims[l] * round8(dims[l + 1]);
+  return n;
+}
+
+size_t mlp_workspace_bytes(const int* dims, int n_dims, int max_batch, int prec) {
+  if (!dims_ok(dims, n_dims) || max_batch <= 0) return 0;
+  return plan(dims, n_dims, max_batch, prec).total;
+}
+
+mlp_status mlp_create(const int* dims, int n_dims, int hidden_act, int prec, int max_batch,
+                      float* params, float* velocity, float* grads, void* params_bf16,
+                      void* workspace, size_t ws_bytes, mlp_handle** out) {
+  if (!out) return MLP_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!dims_ok(dims, n_dims) || max_batch <= 0) return MLP_ERR_INVALID_ARG;
+  if (prec != MLP_PREC_FP32 && prec != MLP_PREC_BF16) return MLP_ERR_INVALID_ARG;
+  if (hidden_act != MLP_ACT_RELU && hidden_act != MLP_ACT_NONE) return MLP_ERR_INVALID_ARG;
+  if (!params || !velocity || !grads || !workspace) return MLP_ERR_INVALID_ARG;
+  if (prec == MLP_PREC_BF16 && !params_bf16) return MLP_ERR_INVALID_ARG;
+  const Plan pl = plan(dims, n_dims, max_batch, prec);
+  if (ws_bytes < pl.total) return MLP_ERR_INVALID_ARG;
+  if (!aligned16(params) || !aligned16(velocity) || !aligned16(grads) || !aligned16(workspace) ||
+      (params_bf16 && !aligned16(params_bf16)))
+    return MLP_ERR_MISALIGNED;
+
+  mlp_handle* h = new (std::nothrow) mlp_handle();
+  if (!h) return MLP_ERR_INVALID_ARG;
+  h->dims.assign(dims, dims + n_dims);
+  h->L = n_dims - 1;
+  h->act = hidden_act;
+  h->prec = prec;
+  h->max_batch = max_batch;
+  h->params = params;
+  h->velocity = velocity;
+  h->grads = grads;
+  h->shadow = prec == MLP_PREC_BF16 ? static_cast<__nv_bfloat16*>(params_bf16) : nullptr;
+  h->n_params = (long long)mlp_param_count(dims, n_dims);
+  long long off = 0, soff = 0;
+  for (int l = 0; l < h->L; ++l) {
+    h->w_off.push_back(off);
+    off += (long long)dims[l] * dims[l + 1];
+    h->b_off.push_back(off);
+    off += dims[l + 1];
+    h->shadow_off.push_back(soff);
+    h->out_pad.push_back(round8(dims[l + 1]));
+    soff += (long long)dims[l] * round8(dims[l + 1]);
+  }
+  for (int l = 0; l < n_dims; ++l) h->act_ld.push_back(round8(dims[l]));
+  // segment map for the fused SGD + shadow refresh
+  h->segs.n = 2 * h->L;
+  for (int l = 0; l < h->L; ++l) {
+    h->segs.flat_off[2 * l] = h->w_off[l];
+    h->segs.shadow_off[2 * l] = h->shadow ? h->shadow_off[l] : -1;
+    h->segs.cols[2 * l] = dims[l + 1];
+    h->segs.cols_pad[2 * l] = h->out_pad[l];
+    h->segs.flat_off[2 * l + 1] = h->b_off[l];
+    h->segs.shadow_off[2 * l + 1] = -1;
+    h->segs.cols[2 * l + 1] = 1;
+    h->segs.cols_pad[2 * l + 1] = 1;
+  }
+  // workspace carving
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  const int e = esz(prec);
+  const size_t B = (size_t)max_batch;
+  h->x_copy = w;
+  w += pl.x;
+  for (int l = 1; l < h->L; ++l) {
+    h->acts.push_back(w);
+    w += align256(B * h->act_ld[l] * e);
+  }
+  h->logits = reinterpret_cast<float*>(w);
+  w += pl.logits;
+  h->ldz = round8(dims[h->L]);
+  h->dlogits = w;
+  w += pl.dlogits;
+  h->dh_ld = 0;
+  h->dh[0] = w;
+  w += pl.dh;
+  h->dh[1] = w;
+  w += pl.dh;
+  h->loss = reinterpret_cast<float*>(w);
+  w += pl.loss;
+  h->red = w;
+  h->red_bytes = pl.red;
+  *out = h;
+  return MLP_OK;
+}
+
+void mlp_destroy(mlp_handle* h) { delete h; }
+
+mlp_status mlp_refresh_shadow(mlp_handle* h, void* stream) {
+  if (!h) return MLP_ERR_INVALID_ARG;
+  if (!h->shadow) return MLP_OK;
+  return launch_shadow(h->params, h->shadow, h->n_params, h->segs, S(stream));
+}
+
+mlp_status mlp_forward(mlp_handle* h, const void* x, int x_dtype, int batch, float* logits,
+                       void* stream) {
+  if (!h || batch < 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
+  if (x_dtype != MLP_DTYPE_F32 && x_dtype != MLP_DTYPE_BF16 && x_dtype != MLP_DTYPE_U8)
+    return MLP_ERR_INVALID_ARG;
+  if (batch == 0) return MLP_OK;
+  if (!x || !logits) return MLP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(logits)) return MLP_ERR_MISALIGNED;
+  cudaStream_t st = S(stream);
+  const bool bf = h->prec == MLP_PREC_BF16;
+  const int d0 = h->dims[0];
+  // The first GEMM reads X in the path's operand type.  An input already in
+  // that type with 16-byte rows is read in place; otherwise it is converted
+  // into the workspace.
+  const bool in_place = (bf && x_dtype == MLP_DTYPE_BF16 && (d0 * 2) % 16 == 0) ||
+                        (!bf && x_dtype == MLP_DTYPE_F32);
+  if (in_place) {
+    h->x_used = x;
+    h->x_ld = d0;
+  } else {
+    MLP_CHECK(launch_cast(x, x_dtype, h->x_copy, bf ? 1 : 0, (long long)batch * d0, st));
+    h->x_used = h->x_copy;
+    h->x_ld = d0;
+  }
+  if (bf && (h->x_ld * 2) % 16 != 0) return MLP_ERR_UNSUPPORTED_SHAPE;
+  const void* in = h->x_used;
+  int ld_in = h->x_ld;
+  for (int l = 0; l < h->L; ++l) {
+    const bool last = (l == h->L - 1);
+    GemmArgs g{};
+    g.M = batch;
+    g.N = h->dims[l + 1];
+    g.K = h->dims[l];
+    g.A = in;
+    g.lda = ld_in;
+    g.a_trans = 0;
+    if (bf) {
+      g.B = h->shadow + h->shadow_off[l];
+      g.ldb = h->out_pad[l];
+    } else {
+      g.B = h->params + h->w_off[l];
+      g.ldb = h->dims[l + 1];
+    }
+    g.b_trans = 0;
+    g.bias = h->params + h->b_off[l];
+    g.act = last ? MLP_ACT_NONE : h->act;
+    g.mask = nullptr;
+    g.ldm = 0;
+    if (last) {
+      g.C = logits;
+      g.ldc = h->dims[l + 1];
+      g.c_bf16 = 0;
+    } else {
+      g.C = h->acts[l];
+      g.ldc = h->act_ld[l + 1];
+      g.c_bf16 = bf ? 1 : 0;
+    }
+    MLP_CHECK(run_gemm(g, bf, st));
+    in = g.C;
+    ld_in = g.ldc;
+  }
+  return MLP_OK;
+}
+
+mlp_status mlp_backward(mlp_handle* h, const void* dlogits, int ld_dlogits, int batch, void* dx,
+                        void* stream) {
+  if (!h || batch < 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
+  if (batch == 0) return MLP_OK;
+  if (!dlogits || !h->x_used || ld_dlogits < h->dims[h->L]) return MLP_ERR_INVALID_ARG;
+  if (!aligned16(dlogits) || (dx && !aligned16(dx))) return MLP_ERR_MISALIGNED;
+  const bool bf = h->prec == MLP_PREC_BF16;
+  if (bf && (ld_dlogits * 2) % 16 != 0) return MLP_ERR_MISALIGNED;
+  cudaStream_t st = S(stream);
+  const void* dY = dlogits;
+  int ld_dy = ld_dlogits;
+  for (int l = h->L - 1; l >= 0; --l) {
+    const int fi = h->dims[l], fo = h->dims[l + 1];
+    const void* in = l == 0 ? h->x_used : h->acts[l - 1];
+    const int ld_in = l == 0 ? h->x_ld : h->act_ld[l];
+    // dW_l = In_l^T dY_l  (A = In_l read transposed, B = dY_l)
+    GemmArgs gw{};
+    gw.M = fi; gw.N = fo; gw.K = batch;
+    gw.A = in; gw.lda = ld_in; gw.a_trans = 1;
+    gw.B = dY; gw.ldb = ld_dy; gw.b_trans = 0;
+    gw.C = h->grads + h->w_off[l]; gw.ldc = fo; gw.c_bf16 = 0;
+    gw.act = MLP_ACT_NONE;
+    MLP_CHECK(run_gemm(gw, bf, st));
+    // db_l = sum_rows dY_l
+    MLP_CHECK(launch_colsum(dY, bf ? 1 : 0, batch, fo, ld_dy, h->grads + h->b_off[l], h->red, st));
+    if (l == 0 && !dx) break;
+    // dIn = (dY W_l^T) * (H_l > 0)   (B = W_l read transposed)
+    GemmArgs gd{};
+    gd.M = batch; gd.N = fi; gd.K = fo;
+    gd.A = dY; gd.lda = ld_dy; gd.a_trans = 0;
+    if (bf) { gd.B = h->shadow + h->shadow_off[l]; gd.ldb = h->out_pad[l]; }
+    else { gd.B = h->params + h->w_off[l]; gd.ldb = fo; }
+    gd.b_trans = 1;
+    gd.act = MLP_ACT_NONE;
+    if (l > 0) {
+      gd.mask = h->act == MLP_ACT_RELU ? h->acts[l - 1] : nullptr;
+      gd.ldm = h->act_ld[l];
+      gd.C = h->dh[l & 1];
+      gd.ldc = h->act_ld[l];
+      gd.c_bf16 = bf ? 1 : 0;
+    } else {
+      gd.C = dx;
+      gd.ldc = fi;
+      gd.c_bf16 = bf ? 1 : 0;
+    }
+    MLP_CHECK(run_gemm(gd, bf, st));
+    if (l == 0) break;
+    dY = gd.C;
+    ld_dy = gd.ldc;
+  }
+  return MLP_OK;
+}
+
+mlp_status mlp_sgd_step(mlp_handle* h, float lr, float momentum, void* stream) {
+  if (!h) return MLP_ERR_INVALID_ARG;
+  return launch_sgd(h->params, h->grads, h->velocity, h->shadow, h->n_params, lr, momentum,
+                    h->segs, S(stream));
+}
+
+mlp_status mlp_train_step(mlp_handle* h, const void* x, int x_dtype, const int32_t* labels,
+                          int batch, float lr, float momentum, float* loss_out,
+                          int32_t* argmax_out, void* stream) {
+  if (!h || batch < 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
+  if (batch == 0) return MLP_OK;
+  if (!labels) return MLP_ERR_INVALID_ARG;
+  if (!aligned16(labels) || (loss_out && !aligned16(loss_out)) ||
+      (argmax_out && !aligned16(argmax_out)))
+    return MLP_ERR_MISALIGNED;
+  cudaStream_t st = S(stream);
+  const int C = h->dims[h->L];
+  MLP_CHECK(mlp_forward(h, x, x_dtype, batch, h->logits, stream));
+  MLP_CHECK(launch_xent(h->logits, C, labels, batch, C, loss_out ? loss_out : h->loss, h->dlogits,
+                        h->prec == MLP_PREC_BF16, h->ldz, argmax_out, h->red, st));
+  MLP_CHECK(mlp_backward(h, h->dlogits, h->ldz, batch, nullptr, stream));
+  return mlp_sgd_step(h, lr, momentum, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Shared definitions of the CUDA library: status codes, the device error word,
+// bf16 helpers and launch checks.  Nothing here is used by the oracle.
+#pragma once
+
+#include <cstdint>
+#include <cstddef>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/mlp_step.h"
+
+namespace mlp {
+
+// Device-side error word.  Kernels that give up on a bounded wait record a
+// code there instead of trapping; mlp_get_device_status() reads and clears
+// it.  The word lives in api.cu; kernels receive its device address.
+int* device_error_word();
+
+// Error codes written into g_device_error (high bits: where, low bits: what).
+enum : int {
+  DEVERR_NONE = 0,
+  DEVERR_TIMEOUT_PRODUCER = 0x101,
+  DEVERR_TIMEOUT_MMA = 0x102,
+  DEVERR_TIMEOUT_EPILOGUE = 0x103,
+  DEVERR_TIMEOUT_TEARDOWN = 0x104,
+  DEVERR_TIMEOUT_PEER = 0x105,
+};
+
+__device__ __forceinline__ void record_device_error(int* word, int code) {
+  if (word) atomicCAS(word, 0, code);
+}
+
+__device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ __nv_bfloat16 f32_to_bf16(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+// Translate the last launch error into a status.
+inline mlp_status launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MLP_OK : MLP_ERR_CUDA;
+}
+
+#define MLP_CHECK(expr)                      \
+  do {                                       \
+    mlp_status _s = (expr);                  \
+    if (_s != MLP_OK) return _s;             \
+  } while (0)
+
+}  // namespace mlp

@@ -1,0 +1,495 @@
+// Memory-bound kernels of the training step: momentum SGD over the flat
+// parameter buffer (with the bf16 shadow refresh fused in), input casting,
+// stable softmax cross entropy, column-sum bias gradients and the
+// mean-squared loss.  All reductions run in fp32 with a fixed summation order,
+// so results are bitwise reproducible from run to run.
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace mlp {
+
+// ------------------------------------------------------------------ SGD
+//
+// "Capstone 5: train a network with your CUDA kernels", "Read the worked
+// reference": one grid-stride kernel updates every weight and velocity of the
+// flat buffer: v <- m v - lr g;  w <- w + v.  Here the body moves 16 bytes per
+// load/store (float4) with streaming cache hints; each element also writes
+// bf16(w) into the weight shadow the tensor-core GEMMs read, through a
+// per-segment map (row-padded for narrow layers).
+
+__device__ __forceinline__ int find_segment(const SgdSegments& s, long long i) {
+  int k = 0;
+  while (k + 1 < s.n && i >= s.flat_off[k + 1]) ++k;
+  return k;
+}
+
+__device__ __forceinline__ long long shadow_index(const SgdSegments& s, int k, long long i) {
+  const long long j = i - s.flat_off[k];
+  if (s.cols[k] == s.cols_pad[k]) return s.shadow_off[k] + j;
+  const long long r = j / s.cols[k];
+  return s.shadow_off[k] + r * s.cols_pad[k] + (j - r * s.cols[k]);
+}
+
+__device__ __forceinline__ void sgd_scalar(float* w, const float* g, float* v,
+                                           __nv_bfloat16* wb, const SgdSegments& s, long long i,
+                                           float lr, float mom) {
+  const float vel = mom * v[i] - lr * g[i];
+  const float nw = w[i] + vel;
+  v[i] = vel;
+  w[i] = nw;
+  if (wb) {
+    const int k = find_segment(s, i);
+    if (s.shadow_off[k] >= 0) wb[shadow_index(s, k, i)] = f32_to_bf16(nw);
+  }
+}
+
+__global__ void __launch_bounds__(256) sgd_kernel(float* __restrict__ w, const float* __restrict__ g,
+                                                  float* __restrict__ v,
+                                                  __nv_bfloat16* __restrict__ wb, long long n,
+                                                  float lr, float mom, SgdSegments segs) {
+  const long long n4 = n >> 2;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  float4* w4 = reinterpret_cast<float4*>(w);
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  float4* v4 = reinterpret_cast<float4*>(v);
+  for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < n4; q += stride) {
+    const float4 gq = __ldcs(g4 + q);
+    const float4 vq = __ldcs(v4 + q);
+    const float4 wq = __ldcs(w4 + q);
+    float4 nv, nw;
+    nv.x = mom * vq.x - lr * gq.x;  nw.x = wq.x + nv.x;
+    nv.y = mom * vq.y - lr * gq.y;  nw.y = wq.y + nv.y;
+    nv.z = mom * vq.z - lr * gq.z;  nw.z = wq.z + nv.z;
+    nv.w = mom * vq.w - lr * gq.w;  nw.w = wq.w + nv.w;
+    __stcs(v4 + q, nv);
+    __stcs(w4 + q, nw);
+    if (wb) {
+      const long long i = q << 2;
+      const int k = find_segment(segs, i);
+      const bool same = (k + 1 >= segs.n) || (i + 3 < segs.flat_off[k + 1]);
+      if (same && segs.shadow_off[k] >= 0 && segs.cols[k] == segs.cols_pad[k]) {
+        const long long si = segs.shadow_off[k] + (i - segs.flat_off[k]);
+        uint2 pk;
+        pk.x = pack_bf16x2(nw.x, nw.y);
+        pk.y = pack_bf16x2(nw.z, nw.w);
+        if ((si & 3) == 0) {
+          __stcs(reinterpret_cast<uint2*>(wb + si), pk);
+        } else {
+          wb[si] = f32_to_bf16(nw.x); wb[si + 1] = f32_to_bf16(nw.y);
+          wb[si + 2] = f32_to_bf16(nw.z); wb[si + 3] = f32_to_bf16(nw.w);
+        }
+      } else {
+        const float vals[4] = {nw.x, nw.y, nw.z, nw.w};
+        for (int e = 0; e < 4; ++e) {
+          const int ke = find_segment(segs, i + e);
+          if (segs.shadow_off[ke] >= 0) wb[shadow_index(segs, ke, i + e)] = f32_to_bf16(vals[e]);
+        }
+      }
+    }
+  }
+  // scalar tail (n not a multiple of 4)
+  const long long t = (n4 << 2) + (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < n) sgd_scalar(w, g, v, wb, segs, t, lr, mom);
+}
+
+// Shadow refresh alone: wb <- bf16(w) through the segment map.
+__global__ void shadow_kernel(const float* __restrict__ w, __nv_bfloat16* __restrict__ wb,
+                              long long n, SgdSegments segs) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int k = find_segment(segs, i);
+    if (segs.shadow_off[k] >= 0) wb[shadow_index(segs, k, i)] = f32_to_bf16(w[i]);
+  }
+}
+
+int sgd_grid(long long n) {
+  const long long q = (n + 3) / 4;
+  long long blocks = (q + 255) / 256;
+  const long long cap = (long long)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return (int)blocks;
+}
+
+mlp_status launch_sgd(float* w, const float* g, float* v, __nv_bfloat16* wb, long long n,
+                      float lr, float mom, const SgdSegments& segs, cudaStream_t st) {
+  if (n <= 0) return MLP_OK;
+  sgd_kernel<<<sgd_grid(n), 256, 0, st>>>(w, g, v, wb, n, lr, mom, segs);
+  return launch_status();
+}
+
+mlp_status launch_shadow(const float* w, __nv_bfloat16* wb, long long n, const SgdSegments& segs,
+                         cudaStream_t st) {
+  if (n <= 0) return MLP_OK;
+  shadow_kernel<<<sgd_grid(n), 256, 0, st>>>(w, wb, n, segs);
+  return launch_status();
+}
+
+// ------------------------------------------------------------------ casts
+// Inputs arrive as image bytes (value = byte / 255, IEEE division), fp32 or
+// bf16; the tensor-core path wants bf16, the SIMT path fp32.
+
+__global__ void cast_kernel(const void* __restrict__ src, int src_dtype, void* __restrict__ dst,
+                            int dst_bf16, long long n) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    float x;
+    if (src_dtype == MLP_DTYPE_U8) x = (float)static_cast<const uint8_t*>(src)[i] / 255.0f;
+    else if (src_dtype == MLP_DTYPE_BF16) x = bf16_to_f32(static_cast<const __nv_bfloat16*>(src)[i]);
+    else x = static_cast<const float*>(src)[i];
+    if (dst_bf16) static_cast<__nv_bfloat16*>(dst)[i] = f32_to_bf16(x);
+    else static_cast<float*>(dst)[i] = x;
+  }
+}
+
+mlp_status launch_cast(const void* src, int src_dtype, void* dst, int dst_bf16, long long n,
+                       cudaStream_t st) {
+  if (n <= 0) return MLP_OK;
+  long long blocks = (n + 1023) / 1024;
+  if (blocks > (long long)num_sms() * 8) blocks = (long long)num_sms() * 8;
+  cast_kernel<<<(int)blocks, 256, 0, st>>>(src, src_dtype, dst, dst_bf16, n);
+  return launch_status();
+}
+
+// ------------------------------------------------------------------ softmax xent
+//
+// "Capstone 5", "The minimum model" and "Read the worked reference": the loss
+// kernel subtracts each row's maximum before exponentiating, so logits at
+// +/-60 stay finite.  "The Work Moved Down a Layer", "The Debugging Lesson Was
+// Numerical": the reductions run in fp32 with warp shuffles.
+// One warp per row; lanes stride over the classes; the row max (with the
+// lowest index among ties), the sum of exponentials and the loss are reduced
+// with a fixed butterfly, so every lane holds identical values.
+
+struct MaxIdx {
+  float v;
+  int i;
+};
+
+__device__ __forceinline__ MaxIdx warp_argmax(MaxIdx a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, a.v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, a.i, o);
+    if (ov > a.v || (ov == a.v && oi < a.i)) { a.v = ov; a.i = oi; }
+  }
+  return a;
+}
+
+__device__ __forceinline__ float warp_sum(float s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
+
+__device__ __forceinline__ float xent_row(const float* __restrict__ z, int label, int C,
+                                          float inv_norm, void* dlog_row, int dl_bf16, int ldd,
+                                          int* argmax_out, int lane) {
+  label = label < 0 ? 0 : (label >= C ? C - 1 : label);  // keep the read in bounds
+  MaxIdx best{-INFINITY, 0x7fffffff};
+  for (int c = lane; c < C; c += 32) {
+    const float v = z[c];
+    if (v > best.v || (v == best.v && c < best.i)) { best.v = v; best.i = c; }
+  }
+  best = warp_argmax(best);
+  const float m = best.v;
+  float s = 0.f;
+  for (int c = lane; c < C; c += 32) s += expf(z[c] - m);
+  s = warp_sum(s);
+  const float loss = m + logf(s) - z[label];
+  if (dlog_row) {
+    for (int c = lane; c < ldd; c += 32) {
+      float d = 0.f;
+      if (c < C) d = (expf(z[c] - m) / s - (c == label ? 1.f : 0.f)) * inv_norm;
+      if (dl_bf16) static_cast<__nv_bfloat16*>(dlog_row)[c] = f32_to_bf16(d);
+      else static_cast<float*>(dlog_row)[c] = d;
+    }
+  }
+  if (argmax_out && lane == 0) *argmax_out = best.i;
+  return loss;
+}
+
+// Small batches: one block, 8 warps striding over the rows; the block also
+// forms the mean (warp w sums its rows in order, then warp sums in order).
+__global__ void __launch_bounds__(256) xent_single_block_kernel(
+    const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
+    float* __restrict__ loss_out, void* dlog, int dl_bf16, int ldd, int* argmax) {
+  __shared__ float part[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float inv_norm = 1.0f / (float)B;
+  float acc = 0.f;
+  for (int r = warp; r < B; r += 8) {
+    void* drow = nullptr;
+    if (dlog) drow = dl_bf16 ? (void*)(static_cast<__nv_bfloat16*>(dlog) + (size_t)r * ldd)
+                             : (void*)(static_cast<float*>(dlog) + (size_t)r * ldd);
+    acc += xent_row(logits + (size_t)r * ldl, labels[r], C, inv_norm, drow, dl_bf16, ldd,
+                    argmax ? argmax + r : nullptr, lane);
+  }
+  if (lane == 0) part[warp] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < 8; ++w) t += part[w];
+    if (loss_out) *loss_out = t / (float)B;
+  }
+}
+
+// Large batches: one row per warp, one partial per block, then a one-block
+// fixed-order sum.
+__global__ void __launch_bounds__(256) xent_rows_kernel(
+    const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
+    float* __restrict__ partial, void* dlog, int dl_bf16, int ldd, int* argmax) {
+  __shared__ float part[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + warp;
+  float li = 0.f;
+  if (r < B) {
+    void* drow = nullptr;
+    if (dlog) drow = dl_bf16 ? (void*)(static_cast<__nv_bfloat16*>(dlog) + (size_t)r * ldd)
+                             : (void*)(static_cast<float*>(dlog) + (size_t)r * ldd);
+    li = xent_row(logits + (size_t)r * ldl, labels[r], C, 1.0f / (float)B, drow, dl_bf16, ldd,
+                  argmax ? argmax + r : nullptr, lane);
+  }
+  if (lane == 0) part[warp] = li;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < 8; ++w) t += part[w];
+    partial[blockIdx.x] = t;
+  }
+}
+
+// Sum of `n` partials in a fixed order, times `scale`, into *out.
+__global__ void __launch_bounds__(256) sum_partials_kernel(const float* __restrict__ partial,
+                                                           long long n, float divisor,
+                                                           float* __restrict__ out) {
+  __shared__ float red[256];
+  float t = 0.f;
+  for (long long i = threadIdx.x; i < n; i += 256) t += partial[i];
+  red[threadIdx.x] = t;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if ((int)threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *out = red[0] / divisor;
+}
+
+size_t xent_workspace_bytes(int B) {
+  if (B <= 256) return 0;
+  return (size_t)((B + 7) / 8) * sizeof(float);
+}
+
+mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, int C,
+                       float* loss_out, void* dlog, int dl_bf16, int ldd, int* argmax,
+                       void* ws, cudaStream_t st) {
+  if (B <= 0) return MLP_OK;
+  if (B <= 256) {
+    xent_single_block_kernel<<<1, 256, 0, st>>>(logits, ldl, labels, B, C, loss_out, dlog,
+                                                dl_bf16, ldd, argmax);
+    return launch_status();
+  }
+  const int blocks = (B + 7) / 8;
+  float* partial = static_cast<float*>(ws);
+  xent_rows_kernel<<<blocks, 256, 0, st>>>(logits, ldl, labels, B, C, partial, dlog, dl_bf16,
+                                           ldd, argmax);
+  MLP_CHECK(launch_status());
+  if (loss_out) {
+    sum_partials_kernel<<<1, 256, 0, st>>>(partial, blocks, (float)B, loss_out);
+    return launch_status();
+  }
+  return MLP_OK;
+}
+
+// ------------------------------------------------------------------ column sums
+//
+// "Capstone 5", "Check your mapping": each bias gradient is a column
+// reduction across the batch.  Pass 1: block (32 x 8 threads) covers 64
+// columns of one row chunk, each thread two adjacent columns (a warp reads 64
+// consecutive elements of a row); the 8 row-strided partial sums are added in
+// order.  Pass 2 (only when there is more than one chunk) adds the chunk
+// partials in order.
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T* p);
+template <>
+__device__ __forceinline__ float ldf<float>(const float* p) { return __ldg(p); }
+template <>
+__device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return bf16_to_f32(*p);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_pass1_kernel(const T* __restrict__ X, int rows,
+                                                           int cols, int ld, int rows_per_chunk,
+                                                           float* __restrict__ dst) {
+  __shared__ float s[8][65];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int c = blockIdx.x * 64 + 2 * tx;
+  const int r0 = blockIdx.y * rows_per_chunk;
+  const int r1 = min(rows, r0 + rows_per_chunk);
+  float a0 = 0.f, a1 = 0.f;
+  for (int r = r0 + ty; r < r1; r += 8) {
+    const T* row = X + (size_t)r * ld;
+    if (c < cols) a0 += ldf(row + c);
+    if (c + 1 < cols) a1 += ldf(row + c + 1);
+  }
+  s[ty][2 * tx] = a0;
+  s[ty][2 * tx + 1] = a1;
+  __syncthreads();
+  if (ty == 0) {
+    for (int e = 0; e < 2; ++e) {
+      const int cc = c + e;
+      if (cc < cols) {
+        float t = 0.f;
+        for (int k = 0; k < 8; ++k) t += s[k][2 * tx + e];
+        dst[(size_t)blockIdx.y * cols + cc] = t;
+      }
+    }
+  }
+}
+
+__global__ void colsum_pass2_kernel(const float* __restrict__ partial, int chunks, int cols,
+                                    float* __restrict__ out) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  float t = 0.f;
+  for (int k = 0; k < chunks; ++k) t += partial[(size_t)k * cols + c];
+  out[c] = t;
+}
+
+void colsum_plan(int rows, int cols, int* chunks, int* rows_per_chunk) {
+  (void)cols;
+  int ch = (rows + 511) / 512;
+  if (ch > 32) ch = 32;
+  if (ch < 1) ch = 1;
+  int rpc = (rows + ch - 1) / ch;
+  rpc = (rpc + 7) / 8 * 8;
+  ch = rpc > 0 ? (rows + rpc - 1) / rpc : 1;
+  if (ch < 1) ch = 1;
+  *chunks = ch;
+  *rows_per_chunk = rpc > 0 ? rpc : 8;
+}
+
+size_t colsum_workspace_bytes(int rows, int cols) {
+  int ch, rpc;
+  colsum_plan(rows, cols, &ch, &rpc);
+  return ch > 1 ? (size_t)ch * cols * sizeof(float) : 0;
+}
+
+mlp_status launch_colsum(const void* X, int bf16, int rows, int cols, int ld, float* out,
+                         void* ws, cudaStream_t st) {
+  if (cols <= 0) return MLP_OK;
+  int ch, rpc;
+  colsum_plan(rows, cols, &ch, &rpc);
+  dim3 grid((cols + 63) / 64, ch);
+  float* dst = ch > 1 ? static_cast<float*>(ws) : out;
+  if (bf16)
+    colsum_pass1_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(X), rows, cols, ld, rpc, dst);
+  else
+    colsum_pass1_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(X), rows, cols,
+                                                     ld, rpc, dst);
+  MLP_CHECK(launch_status());
+  if (ch > 1) {
+    colsum_pass2_kernel<<<(cols + 255) / 256, 256, 0, st>>>(dst, ch, cols, out);
+    return launch_status();
+  }
+  return MLP_OK;
+}
+
+// ------------------------------------------------------------------ MSE
+// loss = mean((y - t)^2), dy = 2 (y - t) / n; y, t, dy bf16.  Each thread
+// handles 8 consecutive elements per 16-byte load; block partials are summed
+// in a fixed order by sum_partials_kernel.
+
+__global__ void __launch_bounds__(256) mse_kernel(const __nv_bfloat16* __restrict__ y,
+                                                  const __nv_bfloat16* __restrict__ t,
+                                                  long long n, __nv_bfloat16* __restrict__ dy,
+                                                  float* __restrict__ partial) {
+  __shared__ float red[256];
+  const float scale = 2.0f / (float)n;
+  const long long n8 = n >> 3;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  float acc = 0.f;
+  for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < n8; q += stride) {
+    const uint4 yv = __ldcs(reinterpret_cast<const uint4*>(y) + q);
+    const uint4 tv = __ldcs(reinterpret_cast<const uint4*>(t) + q);
+    const __nv_bfloat162* yp = reinterpret_cast<const __nv_bfloat162*>(&yv);
+    const __nv_bfloat162* tp = reinterpret_cast<const __nv_bfloat162*>(&tv);
+    uint4 out;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 a = __bfloat1622float2(yp[e]);
+      const float2 b = __bfloat1622float2(tp[e]);
+      const float d0 = a.x - b.x, d1 = a.y - b.y;
+      acc += d0 * d0;
+      acc += d1 * d1;
+      op[e] = pack_bf16x2(d0 * scale, d1 * scale);
+    }
+    if (dy) __stcs(reinterpret_cast<uint4*>(dy) + q, out);
+  }
+  if (blockIdx.x == 0) {
+    for (long long i = (n8 << 3) + threadIdx.x; i < n; i += blockDim.x) {
+      const float d = bf16_to_f32(y[i]) - bf16_to_f32(t[i]);
+      acc += d * d;
+      if (dy) dy[i] = f32_to_bf16(d * scale);
+    }
+  }
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if ((int)threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) partial[blockIdx.x] = red[0];
+}
+
+int mse_blocks(long long n) {
+  long long q = (n / 8 + 255) / 256;
+  const long long cap = 1024;  // fixed cap: the partition depends only on n
+  if (q > cap) q = cap;
+  if (q < 1) q = 1;
+  return (int)q;
+}
+
+size_t mse_ws_bytes(long long n) { return (size_t)mse_blocks(n) * sizeof(float); }
+
+mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out, void* dy,
+                      void* ws, cudaStream_t st) {
+  if (n <= 0) return MLP_OK;
+  const int blocks = mse_blocks(n);
+  float* partial = static_cast<float*>(ws);
+  mse_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(y),
+                                     static_cast<const __nv_bfloat16*>(t), n,
+                                     static_cast<__nv_bfloat16*>(dy), partial);
+  MLP_CHECK(launch_status());
+  if (loss_out) {
+    sum_partials_kernel<<<1, 256, 0, st>>>(partial, blocks, (float)n, loss_out);
+    return launch_status();
+  }
+  return MLP_OK;
+}
+
+// ------------------------------------------------------------------ wait self-test
+// One thread waits on a barrier that nothing arrives at; the bounded wait
+// gives up after limit_ns, records the timeout and the kernel returns.
+
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+    ptx::mbar_wait_bounded(&bar, 0, limit_ns, err, DEVERR_TIMEOUT_PEER);
+  }
+}
+
+mlp_status launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st) {
+  int* err = device_error_word();
+  if (!err) return MLP_ERR_CUDA;
+  wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, err);
+  return launch_status();
+}
+
+}  // namespace mlp

@@ -1,0 +1,387 @@
+// tcgen05 GEMM for sm_103a: bf16 operands fed by TMA into 128-byte-swizzled
+// shared-memory stages, fp32 accumulation in tensor memory, fp32 epilogue
+// (bias, ReLU, ReLU-mask) and a bf16 or fp32 store.
+//
+// "The Work Moved Down a Layer", "The Debugging Lesson Was Numerical": low
+// precision only for the matrix inputs; the accumulator stays fp32 and bias
+// and activation are applied in fp32 before the final conversion.  "Capstone 5:
+// train a network with your CUDA kernels", "Read the worked reference": bias
+// and ReLU in the epilogue; "Work through the backward pass": dW = X^T dH and
+// dX = dH W^T read an operand transposed -- here the transposition is the
+// operand's major-ness in the MMA descriptors (MN-major tiles), so no copy is
+// ever made.  "Tile the data": operand tiles are reused from shared memory by
+// a 128 x BN output tile.
+//
+// Structure: persistent kernel, one CTA per SM, 6 warps:
+//   warp 0    TMA producer (one lane): fills a STAGES-deep ring of A/B tiles;
+//   warp 1    tensor-memory owner and MMA issuer (one lane): 4 x (128 x BN x 16)
+//             MMAs per 64-wide k-block, commits each stage back to the
+//             producer and each finished tile to the epilogue;
+//   warps 2-5 epilogue: tcgen05.ld of their 32-lane quarter of the
+//             accumulator, fp32 epilogue, vector stores.
+// Two accumulators (2 x BN tensor-memory columns) let the epilogue of tile i
+// overlap the MMAs of tile i+1.  Every mbarrier wait is bounded; a timeout is
+// recorded in the device error word and the CTA winds down cleanly.
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace mlp {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+
+struct TcParams {
+  int M, N, K;
+  int a_mn, b_mn;
+  int tiles_m, tiles_n, num_tiles, k_blocks;
+  const float* bias;
+  int act;
+  const __nv_bfloat16* mask;
+  int ldm;
+  void* C;
+  int ldc;
+  int c_bf16;
+  unsigned long long wait_ns;
+  int* err;
+};
+
+template <int BN, int STAGES>
+struct Layout {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+};
+
+// Grouped raster: 8 tile-rows at a time sweep all tile-columns, so CTAs that
+// run together share A row-blocks and B column-blocks in L2.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
+  constexpr int G = 8;
+  const int group = t / (G * tiles_n);
+  const int first = group * G;
+  const int gm = min(tiles_m - first, G);
+  const int r = t - group * G * tiles_n;
+  tm = first + r % gm;
+  tn = r / gm;
+}
+
+template <int BN>
+__device__ __forceinline__ void epilogue_chunk(const TcParams& p, int m, int n0,
+                                               const uint32_t (&r)[32]) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  const bool full = (n0 + 32 <= p.N);
+  if (p.bias) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (full || n0 + j < p.N) v[j] += __ldg(p.bias + n0 + j);
+  }
+  if (p.act == MLP_ACT_RELU) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j], 0.f);
+  }
+  if (p.mask) {
+    const __nv_bfloat16* mrow = p.mask + (size_t)m * p.ldm + n0;
+    if (full && ((reinterpret_cast<uintptr_t>(mrow) & 15) == 0)) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 mv = __ldg(reinterpret_cast<const uint4*>(mrow) + q);
+        const __nv_bfloat16* mb = reinterpret_cast<const __nv_bfloat16*>(&mv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[q * 8 + e] = bf16_to_f32(mb[e]) > 0.f ? v[q * 8 + e] : 0.f;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n0 + j < p.N) v[j] = bf16_to_f32(mrow[j]) > 0.f ? v[j] : 0.f;
+    }
+  }
+  if (p.c_bf16) {
+    __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(p.C) + (size_t)m * p.ldc + n0;
+    if (full && ((reinterpret_cast<uintptr_t>(crow) & 15) == 0)) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 o;
+        o.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+        o.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+        o.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+        o.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+        reinterpret_cast<uint4*>(crow)[q] = o;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n0 + j < p.N) crow[j] = f32_to_bf16(v[j]);
+    }
+  } else {
+    float* crow = static_cast<float*>(p.C) + (size_t)m * p.ldc + n0;
+    if (full && ((reinterpret_cast<uintptr_t>(crow) & 15) == 0)) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        reinterpret_cast<float4*>(crow)[q] =
+            make_float4(v[q * 4 + 0], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n0 + j < p.N) crow[j] = v[j];
+    }
+  }
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcParams p) {
+  using L = Layout<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * L::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * L::B_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 4);
+    }
+    ptx::mbar_init(done, 1);
+    *s_abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) ptx::tmem_alloc(tmem_slot, L::TMEM_COLS);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // stage bookkeeping of the producer, used to drain copies in flight after
+  // an abort
+  int last_parity[STAGES];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < STAGES; ++s) last_parity[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < p.num_tiles && !*s_abort; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
+                                      DEVERR_TIMEOUT_PRODUCER)) {
+            *s_abort = 1;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+          last_parity[stage] = (int)phase;
+          const int k0 = kb * BK;
+          uint8_t* a_dst = sA + stage * L::A_BYTES;
+          uint8_t* b_dst = sB + stage * L::B_BYTES;
+          if (!p.a_mn) {
+            ptx::tma_load_2d(a_dst, &tmA, &full[stage], k0, tm * BM);
+          } else {
+            ptx::tma_load_2d(a_dst, &tmA, &full[stage], tm * BM, k0);
+            ptx::tma_load_2d(a_dst + 8192, &tmA, &full[stage], tm * BM + 64, k0);
+          }
+          if (!p.b_mn) {
+            ptx::tma_load_2d(b_dst, &tmB, &full[stage], k0, tn * BN);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              ptx::tma_load_2d(b_dst + j * 8192, &tmB, &full[stage], tn * BN + j * 64, k0);
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
+      const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
+      const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
+      const uint32_t a_kstep = p.a_mn ? 2048u : 32u;  // bytes per 16-element k step
+      const uint32_t b_kstep = p.b_mn ? 2048u : 32u;
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = blockIdx.x; t < p.num_tiles && !*s_abort; t += gridDim.x) {
+        if (!ptx::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err, DEVERR_TIMEOUT_MMA)) {
+          *s_abort = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!ptx::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err, DEVERR_TIMEOUT_MMA)) {
+            *s_abort = 1;
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_base = ptx::smem_u32(sA + stage * L::A_BYTES);
+          const uint32_t b_base = ptx::smem_u32(sB + stage * L::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = ptx::sw128_desc(a_base + k * a_kstep, a_lbo, 1024);
+            const uint64_t bd = ptx::sw128_desc(b_base + k * b_kstep, b_lbo, 1024);
+            ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(&empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&tfull[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      // all MMAs issued by this thread have completed once `done` fires
+      ptx::mma_commit(done);
+      ptx::mbar_wait_bounded(done, 0, p.wait_ns, p.err, DEVERR_TIMEOUT_TEARDOWN);
+    }
+  } else {
+    const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter + 32)
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      if (*s_abort) break;
+      if (!ptx::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err, DEVERR_TIMEOUT_EPILOGUE)) {
+        *s_abort = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      int tm, tn;
+      tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
+      const int m = tm * BM + row;
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        const int n0 = tn * BN + c0;
+        if (n0 >= p.N) break;  // warp-uniform
+        uint32_t r[32];
+        __syncwarp();
+        ptx::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                    (uint32_t)(acc * BN + c0),
+                                r);
+        ptx::tmem_ld_wait();
+        if (m < p.M) epilogue_chunk<BN>(p, m, n0, r);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (*s_abort && warp == 0 && lane == 0) {
+    // wait (bounded) for TMA copies that may still be landing in shared memory
+    for (int s = 0; s < STAGES; ++s)
+      if (last_parity[s] >= 0)
+        ptx::mbar_wait_bounded(&full[s], (uint32_t)last_parity[s], p.wait_ns, p.err,
+                               DEVERR_TIMEOUT_TEARDOWN);
+  }
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+template <int BN, int STAGES>
+mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
+                     cudaStream_t st) {
+  using L = Layout<BN, STAGES>;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
+      return MLP_ERR_CUDA;
+    configured = true;
+  }
+  int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  tc_gemm_kernel<BN, STAGES><<<grid, kThreads, L::SMEM, st>>>(ta, tb, p);
+  return launch_status();
+}
+
+}  // namespace
+
+mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStream_t st) {
+  if (g.M <= 0 || g.N <= 0) return MLP_OK;
+  if (g.K <= 0) return launch_gemm_simt(g, 1, st);
+
+  const int tiles_m = (g.M + BM - 1) / BM;
+  // Widest tile that still gives every SM work; narrower tiles for small N.
+  int BN = 256;
+  const int sms = num_sms();
+  auto tiles_for = [&](int bn) { return tiles_m * ((g.N + bn - 1) / bn); };
+  if (g.N <= 64) BN = 64;
+  else if (g.N <= 128) BN = 128;
+  else if (tiles_for(256) < sms) BN = tiles_for(128) < sms ? 64 : 128;
+  if (BN == 128 && tiles_for(128) < sms / 2 && g.N > 64) BN = 64;
+
+  TcParams p;
+  p.M = g.M; p.N = g.N; p.K = g.K;
+  p.a_mn = g.a_trans ? 1 : 0;       // A stored [K][M]  -> M-major tiles
+  p.b_mn = g.b_trans ? 0 : 1;       // B stored [K][N]  -> N-major tiles
+  p.tiles_m = tiles_m;
+  p.tiles_n = (g.N + BN - 1) / BN;
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.k_blocks = (g.K + BK - 1) / BK;
+  p.bias = g.bias;
+  p.act = g.act;
+  p.mask = static_cast<const __nv_bfloat16*>(g.mask);
+  p.ldm = g.ldm;
+  p.C = g.C;
+  p.ldc = g.ldc;
+  p.c_bf16 = g.c_bf16;
+  p.wait_ns = wait_ns;
+  p.err = device_error_word();
+  if (!p.err) return MLP_ERR_CUDA;
+
+  CUtensorMap ta, tb;
+  bool ok;
+  if (!p.a_mn)
+    ok = encode_tmap_bf16_2d(&ta, g.A, g.K, g.M, (unsigned long long)g.lda * 2, 64, BM);
+  else
+    ok = encode_tmap_bf16_2d(&ta, g.A, g.M, g.K, (unsigned long long)g.lda * 2, 64, 64);
+  if (!ok) return MLP_ERR_CUDA;
+  if (!p.b_mn)
+    ok = encode_tmap_bf16_2d(&tb, g.B, g.K, g.N, (unsigned long long)g.ldb * 2, 64, BN);
+  else
+    ok = encode_tmap_bf16_2d(&tb, g.B, g.N, g.K, (unsigned long long)g.ldb * 2, 64, 64);
+  if (!ok) return MLP_ERR_CUDA;
+
+  switch (BN) {
+    case 64: return launch_bn<64, 8>(ta, tb, p, st);
+    case 128: return launch_bn<128, 6>(ta, tb, p, st);
+    default: return launch_bn<256, 4>(ta, tb, p, st);
+  }
+}
+
+}  // namespace mlp

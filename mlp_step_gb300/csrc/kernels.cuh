@@ -1,0 +1,62 @@
+// Host-side launchers of the library's kernels (one translation unit each),
+// called by the C-ABI layer in api.cu.
+#pragma once
+
+#include <cuda.h>
+#include "common.cuh"
+
+namespace mlp {
+
+// Segment map of the flat parameter buffer for the fused SGD + bf16 shadow
+// refresh: segment k covers flat indices [flat_off[k], flat_off[k+1]) (the
+// last one up to n); its elements form rows of `cols` values that land in the
+// shadow at shadow_off[k] with a row pitch of cols_pad (shadow_off < 0: no
+// shadow, e.g. biases).
+struct SgdSegments {
+  int n;
+  long long flat_off[16];
+  long long shadow_off[16];
+  int cols[16];
+  int cols_pad[16];
+};
+
+// k_elementwise.cu
+mlp_status launch_sgd(float* w, const float* g, float* v, __nv_bfloat16* wb, long long n,
+                      float lr, float mom, const SgdSegments& segs, cudaStream_t st);
+mlp_status launch_shadow(const float* w, __nv_bfloat16* wb, long long n, const SgdSegments& segs,
+                         cudaStream_t st);
+mlp_status launch_cast(const void* src, int src_dtype, void* dst, int dst_bf16, long long n,
+                       cudaStream_t st);
+size_t xent_workspace_bytes(int B);
+mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, int C,
+                       float* loss_out, void* dlog, int dl_bf16, int ldd, int* argmax, void* ws,
+                       cudaStream_t st);
+size_t colsum_workspace_bytes(int rows, int cols);
+mlp_status launch_colsum(const void* X, int bf16, int rows, int cols, int ld, float* out,
+                         void* ws, cudaStream_t st);
+size_t mse_ws_bytes(long long n);
+mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out, void* dy,
+                      void* ws, cudaStream_t st);
+mlp_status launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st);
+
+// k_gemm_simt.cu: fp32 (or bf16-input) SIMT GEMM with the fused epilogue.
+struct GemmArgs {
+  int M, N, K;
+  const void* A; int lda; int a_trans;
+  const void* B; int ldb; int b_trans;
+  const float* bias; int act;
+  const void* mask; int ldm;
+  void* C; int ldc; int c_bf16;
+};
+mlp_status launch_gemm_simt(const GemmArgs& g, int in_bf16, cudaStream_t st);
+
+// k_gemm_tc.cu: tcgen05 bf16 GEMM (TMA-fed, fp32 accumulation in tensor memory).
+mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStream_t st);
+
+// Host helpers (api.cu)
+unsigned long long wait_limit_ns();
+bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, unsigned long long inner,
+                         unsigned long long outer, unsigned long long row_stride_bytes,
+                         unsigned box_inner, unsigned box_outer);
+
+}  // namespace mlp

@@ -54,6 +54,8 @@ def lib():
                                        _D, _D, _D, _I]
         L.orc_mlp_backward.argtypes = [_I, ctypes.c_int, _D, _D, ctypes.c_longlong, _D, _D,
                                        ctypes.c_int, _D, _D]
+        L.orc_colsum_f32.argtypes = [_F, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_longlong,
+                                     _D]
         L.orc_sgd_momentum.argtypes = [_D, _D, _D, ctypes.c_longlong, ctypes.c_double,
                                        ctypes.c_double]
         L.orc_mlp_train_step.restype = ctypes.c_double
@@ -173,6 +175,13 @@ def mlp_backward(dims, params, X, hs, dZ, bf16_points=False, want_dx=False):
     lib().orc_mlp_backward(d, n, _p(params, _D), _p(X, _D), B, _p(acts, _D), _p(dZ, _D),
                            int(bf16_points), _p(g, _D), _p(dX, _D))
     return (g, dX) if want_dx else g
+
+
+def colsum(X):
+    X = _f(X)
+    out = np.empty(X.shape[1])
+    lib().orc_colsum_f32(_p(X, _F), X.shape[0], X.shape[1], X.shape[1], _p(out, _D))
+    return out
 
 
 def sgd_momentum(w, g, v, lr, momentum):

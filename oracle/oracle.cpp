@@ -223,6 +223,16 @@ void orc_mlp_backward(const int* dims, int n_dims, const double* params,
   }
 }
 
+// [cap] "Check your mapping": a bias gradient is a column reduction over the
+// batch, out[c] = sum_r X[r][c] (rows in order).  X is float storage.
+void orc_colsum_f32(const float* X, long long rows, long long cols, long long ld, double* out) {
+  for (long long c = 0; c < cols; ++c) {
+    double s = 0.0;
+    for (long long r = 0; r < rows; ++r) s += (double)X[r * ld + c];
+    out[c] = s;
+  }
+}
+
 // [cap] "Read the worked reference": momentum SGD over one flat buffer,
 // v <- momentum * v - lr * g;  w <- w + v.
 void orc_sgd_momentum(double* w, const double* g, double* v, long long n,

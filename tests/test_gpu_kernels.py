@@ -1,0 +1,225 @@
+"""Parity of the single kernels (through the C ABI) with the fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import mlp_step_gb300 as M
+from mlp_step_gb300 import synth
+from helpers import bf16_values, to_dev, rel_to_max, assert_elementwise, near_tie_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    M.load()
+    yield
+    assert M.get_device_status() == M.MLP_OK
+
+
+# ------------------------------------------------------------------ SGD
+
+@pytest.mark.parametrize("n", [203530, 1001, 3, 4 * 1024 * 1024 + 5])
+def test_sgd_matches_oracle(n):
+    lr, m = 0.1, 0.9
+    w = synth.normal_f32((n,), synth.STREAM_GENERIC)
+    g = synth.normal_f32((n,), synth.STREAM_GENERIC + 1)
+    v = synth.normal_f32((n,), synth.STREAM_GENERIC + 2, std=0.01)
+    wd, gd, vd = to_dev(w), to_dev(g), to_dev(v)
+    wb = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    M.sgd_momentum_step(wd, gd, vd, lr, m, w_bf16=wb)
+    w_ref, v_ref = oracle.sgd_momentum(w, g, v, lr, m)
+    # "Stage 2: backward and update" (case 5): |got - ref| <= 1e-6 + 1e-5 |ref|
+    assert_elementwise(wd.cpu().numpy(), w_ref, 1e-5, 1e-6, "w")
+    assert_elementwise(vd.cpu().numpy(), v_ref, 1e-5, 1e-6, "v")
+    # the shadow is bf16 of the updated fp32 weight, element for element
+    assert torch.equal(wb, wd.to(torch.bfloat16))
+
+
+def test_sgd_two_steps_closed_form():
+    n, lr, m = 4099, 0.1, 0.9
+    w0 = synth.normal_f32((n,), synth.STREAM_GENERIC)
+    g0 = synth.normal_f32((n,), synth.STREAM_GENERIC + 1)
+    g1 = synth.normal_f32((n,), synth.STREAM_GENERIC + 2)
+    wd, vd = to_dev(w0), torch.zeros(n, device="cuda")
+    M.sgd_momentum_step(wd, to_dev(g0), vd, lr, m)
+    M.sgd_momentum_step(wd, to_dev(g1), vd, lr, m)
+    w0d, g0d, g1d = (a.astype(np.float64) for a in (w0, g0, g1))
+    assert_elementwise(wd.cpu().numpy(), w0d - lr * g0d * (1 + m) - lr * g1d, 1e-5, 1e-6, "w2")
+
+
+# ------------------------------------------------------------------ softmax xent
+
+def _xent_case(B, C, Z, y, dl_dtype):
+    ld = (C + 7) // 8 * 8
+    Zd = to_dev(Z)
+    yd = to_dev(y)
+    loss = torch.zeros(1, device="cuda")
+    dl = torch.full((B, ld), 7.0, dtype=dl_dtype, device="cuda")
+    am = torch.empty(B, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(M.softmax_xent_workspace_bytes(B, C), 16), dtype=torch.uint8,
+                     device="cuda")
+    M.softmax_xent_fwd_bwd(Zd, yd, loss, dlogits=dl, argmax_out=am, workspace=ws, classes=C)
+    return loss.item(), dl.float().cpu().numpy(), am.cpu().numpy()
+
+
+@pytest.mark.parametrize("B,C", [(128, 10), (112, 10), (1, 10), (300, 10), (16384, 1000),
+                                 (257, 1000)])
+def test_xent_matches_oracle(B, C):
+    Z = synth.normal_f32((B, C), synth.STREAM_GENERIC, std=3.0)
+    y = synth.labels(B, C, seed=17)
+    loss, dl, am = _xent_case(B, C, Z, y, torch.float32)
+    l_ref, _, dZ_ref, am_ref = oracle.softmax_xent(Z.astype(np.float64), y)
+    assert abs(loss - l_ref) <= 2e-6 * max(1.0, abs(l_ref))
+    assert_elementwise(dl[:, :C], dZ_ref, 1e-5, 1e-7 / B, "dZ")
+    assert np.all(dl[:, C:] == 0.0)  # padding columns written as zero
+    ok = ~near_tie_rows(Z)
+    assert np.array_equal(am[ok], am_ref[ok])
+
+
+def test_xent_bf16_dlogits():
+    B, C = 128, 10
+    Z = synth.normal_f32((B, C), synth.STREAM_GENERIC, std=3.0)
+    y = synth.labels(B, C, seed=17)
+    _, dl, _ = _xent_case(B, C, Z, y, torch.bfloat16)
+    _, _, dZ_ref, _ = oracle.softmax_xent(Z.astype(np.float64), y)
+    assert rel_to_max(dl[:, :C], dZ_ref) <= 4e-3
+
+
+def test_xent_extreme_logits_pm60():
+    # "Capstone 5", "Read the worked reference": logits at +/-60 must give
+    # finite loss and gradients; closed forms per row (k entries at +60).
+    B, C = 200, 10
+    Z, k = synth.logits_pm60(B, C)
+    y = synth.labels(B, C, seed=5)
+    loss, dl, am = _xent_case(B, C, Z, y, torch.float32)
+    assert math.isfinite(loss) and np.all(np.isfinite(dl))
+    top = Z[np.arange(B), y] > 0
+    want = np.where(top, np.log(k), 120.0 + np.log(k)).mean()
+    assert abs(loss - want) <= 1e-5 * want
+    p = dl[:, :C] * B + (np.arange(C)[None, :] == y[:, None])
+    pos = Z > 0
+    assert np.allclose(p[pos], np.repeat(1.0 / k, (pos).sum(1)), rtol=1e-5)
+    am_ref = np.argmax(Z, 1)  # first +60
+    assert np.array_equal(am, am_ref)
+
+
+# ------------------------------------------------------------------ column sums
+
+@pytest.mark.parametrize("rows,cols,dtype", [(128, 10, torch.float32), (128, 256, torch.bfloat16),
+                                             (16384, 1000, torch.bfloat16), (3, 5, torch.float32),
+                                             (1, 64, torch.bfloat16), (5000, 333, torch.float32)])
+def test_colsum_matches_oracle(rows, cols, dtype):
+    X = synth.normal_f32((rows, cols), synth.STREAM_GENERIC)
+    Xd = to_dev(X, dtype)
+    out = torch.empty(cols, device="cuda")
+    ws = torch.empty(max(M.mlp_colsum_workspace_bytes(rows, cols), 16), dtype=torch.uint8,
+                     device="cuda")
+    M.mlp_colsum(Xd, out, workspace=ws)
+    ref = oracle.colsum(Xd.float().cpu().numpy())
+    # fp32 accumulation of `rows` terms of magnitude ~1
+    assert_elementwise(out.cpu().numpy(), ref, 1e-5, 1e-6 * math.sqrt(rows), "colsum")
+
+
+# ------------------------------------------------------------------ GEMM (fp32 SIMT)
+
+def _operands(M_, N, K, a_t, b_t, seed=0):
+    A = synth.normal_f32((K, M_) if a_t else (M_, K), synth.STREAM_GENERIC + seed)
+    B = synth.normal_f32((N, K) if b_t else (K, N), synth.STREAM_GENERIC + seed + 1)
+    return A, B
+
+
+@pytest.mark.parametrize("a_t,b_t", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("shape", [(128, 256, 784), (67, 33, 129), (1, 10, 256), (784, 256, 128)])
+def test_gemm_fp32_matches_oracle(shape, a_t, b_t):
+    M_, N, K = shape
+    A, B = _operands(M_, N, K, a_t, b_t)
+    bias = synth.normal_f32((N,), synth.STREAM_GENERIC + 5)
+    C = torch.empty(M_, N, device="cuda")
+    M.mlp_gemm(to_dev(A), to_dev(B), C, M_, N, K, a_trans=a_t, b_trans=b_t, bias=to_dev(bias),
+               act=M.MLP_ACT_RELU)
+    ref = np.maximum(oracle.matmul(A, B, a_t=bool(a_t), b_t=bool(b_t)) + bias, 0.0)
+    assert_elementwise(C.cpu().numpy(), ref, 1e-5, 1e-5 * math.sqrt(K), "C")
+
+
+# ------------------------------------------------------------------ GEMM (bf16 tcgen05)
+
+def _tc_case(M_, N, K, a_t, b_t, bias=False, act=M.MLP_ACT_NONE, mask=False, out_bf16=False,
+             seed=0):
+    A, B = _operands(M_, N, K, a_t, b_t, seed)
+    Ad, Bd = to_dev(A, torch.bfloat16), to_dev(B, torch.bfloat16)
+    bvec = synth.normal_f32((N,), synth.STREAM_GENERIC + 5) if bias else None
+    mk = synth.normal_f32((M_, N), synth.STREAM_GENERIC + 6) if mask else None
+    C = torch.full((M_, N), float("nan"), dtype=torch.bfloat16 if out_bf16 else torch.float32,
+                   device="cuda")
+    M.mlp_gemm(Ad, Bd, C, M_, N, K, a_trans=a_t, b_trans=b_t,
+               bias=to_dev(bvec) if bias else None, act=act,
+               mask=to_dev(mk, torch.bfloat16) if mask else None)
+    ref = oracle.matmul(bf16_values(A), bf16_values(B), a_t=bool(a_t), b_t=bool(b_t))
+    if bias:
+        ref = ref + bvec
+    if act == M.MLP_ACT_RELU:
+        ref = np.maximum(ref, 0.0)
+    if mask:
+        ref = np.where(bf16_values(mk) > 0, ref, 0.0)
+    return C.float().cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("a_t,b_t", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("shape", [(128, 256, 784), (300, 200, 136), (129, 65, 64), (1, 16, 8),
+                                   (256, 10, 128), (128, 256, 10), (2560, 1024, 192),
+                                   (640, 768, 320)])
+def test_gemm_bf16_tc_matches_oracle(shape, a_t, b_t):
+    M_, N, K = shape
+    if (not a_t and K % 8) or (a_t and M_ % 8) or (not b_t and N % 8) or (b_t and K % 8):
+        pytest.skip("bf16 rows must be 16-byte aligned for TMA")
+    got, ref = _tc_case(M_, N, K, a_t, b_t)
+    assert np.all(np.isfinite(got)), "unwritten outputs"
+    assert rel_to_max(got, ref) <= 1e-5, rel_to_max(got, ref)
+
+
+@pytest.mark.parametrize("bias,act,mask,out_bf16", [(True, M.MLP_ACT_RELU, False, True),
+                                                    (False, M.MLP_ACT_NONE, True, True),
+                                                    (True, M.MLP_ACT_NONE, False, False)])
+def test_gemm_bf16_tc_epilogues(bias, act, mask, out_bf16):
+    got, ref = _tc_case(333, 520, 200, 0, 0, bias=bias, act=act, mask=mask, out_bf16=out_bf16)
+    tol = 8e-3 if out_bf16 else 1e-5
+    assert rel_to_max(got, ref) <= tol
+    if act == M.MLP_ACT_RELU:
+        assert np.all(got >= 0)
+    if mask:
+        mk = synth.normal_f32((333, 520), synth.STREAM_GENERIC + 6)
+        assert np.all(got[bf16_values(mk) <= 0] == 0)
+
+
+def test_gemm_bf16_tc_k_zero_gives_bias():
+    N = 24
+    bias = synth.normal_f32((N,), synth.STREAM_GENERIC + 5)
+    C = torch.empty(5, N, device="cuda")
+    A = torch.zeros(5, 8, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(8, N, dtype=torch.bfloat16, device="cuda")
+    M.mlp_gemm(A, B, C, 5, N, 0, bias=to_dev(bias))
+    assert np.array_equal(C.cpu().numpy(), np.tile(bias, (5, 1)))
+
+
+def test_gemm_bf16_tc_deterministic():
+    A, B = _operands(1000, 1000, 1000, 0, 0)
+    Ad, Bd = to_dev(A, torch.bfloat16), to_dev(B, torch.bfloat16)
+    C1 = torch.empty(1000, 1000, device="cuda")
+    C2 = torch.empty(1000, 1000, device="cuda")
+    M.mlp_gemm(Ad, Bd, C1, 1000, 1000, 1000)
+    M.mlp_gemm(Ad, Bd, C2, 1000, 1000, 1000)
+    assert torch.equal(C1, C2)
+
+
+# ------------------------------------------------------------------ bounded wait
+
+def test_bounded_wait_times_out_cleanly():
+    M.selftest_wait_timeout(20_000_000)  # 20 ms
+    assert M.get_device_status() == M.MLP_ERR_DEVICE_TIMEOUT
+    assert M.get_device_status() == M.MLP_OK  # cleared, context still usable
+    x = torch.ones(4, device="cuda")
+    assert x.sum().item() == 4.0

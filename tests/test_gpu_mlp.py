@@ -1,0 +1,157 @@
+"""Parity of the whole MLP training step (through the C ABI) with the fp64 oracle.
+
+The 784-256-10 network of "Capstone 5: train a network with your CUDA
+kernels" ("The minimum model": batch 128, lr 0.1, momentum 0.9, seed
+20260829), on the fp32 SIMT path and on the bf16 tensor-core path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import mlp_step_gb300 as M
+from mlp_step_gb300 import synth
+from helpers import bf16_values, to_dev, rel_to_max, assert_elementwise, near_tie_rows
+
+pytestmark = pytest.mark.gpu
+
+DIMS = [784, 256, 10]
+LR, MOM = 0.1, 0.9
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    M.load()
+    yield
+    assert M.get_device_status() == M.MLP_OK
+
+
+def _x_values(xb):
+    return xb.astype(np.float32) / np.float32(255)   # what the byte input means
+
+
+def _segments(dims, flat):
+    out, off = [], 0
+    for l in range(len(dims) - 1):
+        n = dims[l] * dims[l + 1]
+        out.append(("W%d" % (l + 1), flat[off:off + n]))
+        off += n
+        out.append(("b%d" % (l + 1), flat[off:off + dims[l + 1]]))
+        off += dims[l + 1]
+    return out
+
+
+@pytest.mark.parametrize("B", [128, 112, 1])
+def test_fp32_step_matches_oracle(B):
+    p0 = synth.mlp_flat_params(DIMS)
+    xb = synth.images_u8(B, 784)
+    y = synth.labels(B, 10)
+    net = M.MLP(DIMS, prec=M.MLP_PREC_FP32, max_batch=128, params=torch.from_numpy(p0))
+    loss = torch.zeros(1, device="cuda")
+    am = torch.empty(B, dtype=torch.int32, device="cuda")
+    net.train_step(to_dev(xb), to_dev(y), LR, MOM, loss_out=loss, argmax_out=am)
+    torch.cuda.synchronize()
+    X = _x_values(xb).astype(np.float64)
+    l_ref, p_ref, v_ref, g_ref = oracle.mlp_train_step(DIMS, p0.astype(np.float64),
+                                                       np.zeros(p0.size), X, y, LR, MOM)
+    # weights after one step: max relative error 1e-4 (elementwise, with the
+    # 1e-6 floor of the capstone's step bound)
+    assert_elementwise(net.params.cpu().numpy(), p_ref, 1e-4, 1e-6, "params")
+    assert_elementwise(net.velocity.cpu().numpy(), v_ref, 1e-4, 1e-7, "velocity")
+    assert abs(loss.item() - l_ref) <= 1e-5
+    # argmax of the step's forward is bit-exact against the oracle
+    _, Z = oracle.mlp_forward(DIMS, p0.astype(np.float64), X)
+    ok = ~near_tie_rows(Z)
+    assert np.array_equal(am.cpu().numpy()[ok], np.argmax(Z, 1)[ok])
+
+
+def test_fp32_forward_logits_and_backward_grads():
+    B = 128
+    p0 = synth.mlp_flat_params(DIMS)
+    xb = synth.images_u8(B, 784)
+    net = M.MLP(DIMS, prec=M.MLP_PREC_FP32, max_batch=B, params=torch.from_numpy(p0))
+    X = _x_values(xb)
+    logits = torch.empty(B, 10, device="cuda")
+    net.forward(to_dev(X), logits)
+    hs, Z = oracle.mlp_forward(DIMS, p0.astype(np.float64), X.astype(np.float64))
+    assert_elementwise(logits.cpu().numpy(), Z, 1e-4, 1e-5, "logits")
+    dZ = synth.normal_f32((B, 10), synth.STREAM_GENERIC, std=0.01)
+    dx = torch.empty(B, 784, device="cuda")
+    net.backward(to_dev(dZ), B, dx=dx)
+    g_ref, dX_ref = oracle.mlp_backward(DIMS, p0.astype(np.float64), X.astype(np.float64), hs,
+                                        dZ.astype(np.float64), want_dx=True)
+    for (name, got), (_, ref) in zip(_segments(DIMS, net.grads.cpu().numpy()),
+                                     _segments(DIMS, g_ref)):
+        assert rel_to_max(got, ref) <= 1e-5, name
+    assert rel_to_max(dx.cpu().numpy(), dX_ref) <= 1e-5
+
+
+@pytest.mark.parametrize("B", [128, 112, 1])
+def test_bf16_step_matches_oracle(B):
+    p0 = synth.mlp_flat_params(DIMS)
+    xb = synth.images_u8(B, 784)
+    y = synth.labels(B, 10)
+    net = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=128, params=torch.from_numpy(p0))
+    loss = torch.zeros(1, device="cuda")
+    net.train_step(to_dev(xb), to_dev(y), LR, MOM, loss_out=loss)
+    torch.cuda.synchronize()
+    Xb = bf16_values(_x_values(xb))
+    l_ref, p_ref, v_ref, g_ref = oracle.mlp_train_step(DIMS, p0.astype(np.float64),
+                                                       np.zeros(p0.size), Xb, y, LR, MOM,
+                                                       bf16_points=True)
+    assert abs(loss.item() - l_ref) <= 1e-3
+    for (name, got), (_, ref) in zip(_segments(DIMS, net.grads.cpu().numpy()),
+                                     _segments(DIMS, g_ref)):
+        assert rel_to_max(got, ref) <= 3e-2, name
+    assert rel_to_max(net.params.cpu().numpy() - p0, p_ref - p0) <= 3e-2
+    # the bf16 shadow is the rounded fp32 master weight
+    W1 = net.params[:784 * 256].view(784, 256)
+    S1 = net.shadow[:784 * 256].view(784, 256)
+    assert torch.equal(S1, W1.to(torch.bfloat16))
+    W2 = net.params[200960:200960 + 2560].view(256, 10)
+    S2 = net.shadow[784 * 256:].view(256, 16)
+    assert torch.equal(S2[:, :10], W2.to(torch.bfloat16))
+
+
+def test_bf16_forward_matches_oracle_exact_mode():
+    B = 128
+    p0 = synth.mlp_flat_params(DIMS)
+    xb = synth.images_u8(B, 784)
+    net = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+    logits = torch.empty(B, 10, device="cuda")
+    net.forward(to_dev(xb), logits)
+    _, Z = oracle.mlp_forward(DIMS, p0.astype(np.float64), _x_values(xb).astype(np.float64))
+    assert rel_to_max(logits.cpu().numpy(), Z) <= 3e-2
+
+
+def test_bf16_steps_are_deterministic():
+    B = 128
+    p0 = synth.mlp_flat_params(DIMS)
+    xb = to_dev(synth.images_u8(B, 784))
+    y = to_dev(synth.labels(B, 10))
+    outs = []
+    for _ in range(2):
+        net = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+        for _ in range(3):
+            net.train_step(xb, y, LR, MOM)
+        outs.append(net.params.clone())
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_overfit_32_on_gpu():
+    # "Stage 3: prove that it learns": 32 images, 200 steps, loss below 0.01.
+    n = 32
+    p0 = synth.mlp_flat_params(DIMS)
+    xb = to_dev(synth.images_u8(n, 784))
+    y = to_dev(synth.labels(n, 10))
+    for prec in (M.MLP_PREC_FP32, M.MLP_PREC_BF16):
+        net = M.MLP(DIMS, prec=prec, max_batch=n, params=torch.from_numpy(p0))
+        loss = torch.zeros(1, device="cuda")
+        for _ in range(200):
+            net.train_step(xb, y, LR, MOM, loss_out=loss)
+        logits = torch.empty(n, 10, device="cuda")
+        net.forward(xb, logits)
+        ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+        final = torch.zeros(1, device="cuda")
+        M.softmax_xent_fwd_bwd(logits, y, final, workspace=ws)
+        assert final.item() < 0.01, (prec, final.item())

@@ -53,6 +53,19 @@ def test_matmul_matches_library(a_t, b_t):
     assert np.allclose(ent, want32[ii, jj], rtol=1e-13, atol=1e-13)
 
 
+def test_colsum_matches_library_and_bias_gradient():
+    X = synth.normal(3, synth.STREAM_GENERIC, 37 * 13).reshape(37, 13).astype(np.float32)
+    got = oracle.colsum(X)
+    assert np.allclose(got, X.astype(np.float64).sum(0), rtol=1e-14, atol=1e-14)
+    # it is the bias gradient of the backward pass: db = sum_rows dY
+    dims = [5, 4, 13]
+    p = synth.mlp_flat_params(dims, seed=2).astype(np.float64)
+    X0 = synth.normal(3, synth.STREAM_GENERIC + 1, 37 * 5).reshape(37, 5)
+    hs, _ = oracle.mlp_forward(dims, p, X0)
+    g = oracle.mlp_backward(dims, p, X0, hs, X.astype(np.float64))
+    assert np.allclose(g[-13:], got, rtol=1e-13, atol=1e-14)
+
+
 # ------------------------------------------------------------ forward
 
 def test_forward_all_positive_reduces_to_affine_maps():
