@@ -1,0 +1,497 @@
+#!/usr/bin/env python3
+"""Throughput of the MLP training step on GB300, as one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Workloads (synthetic, seeded inputs; see synth.py):
+  mlp784_epoch  784-256-10 MLP, ReLU hidden, bf16 tensor-core path, one epoch of 6,000
+                images = 46 steps of batch 128 + 1 of 112 (default)
+  mlp784_fp32   same network, fp32 SIMT path, one step of batch 128
+  mlp_wide      1024-8192-8192-1000 MLP, batch 16,384, bf16 operands, fp32 master weights
+  block         one RMSNorm -> gate -> LeakyReLU^2 -> down -> residual block, fwd + bwd,
+                65,536 tokens x 512
+  stack         11 such blocks over 262,144 tokens, MSE loss, fwd + bwd + momentum SGD
+
+A bench "step" is one pass of the whole training step of the workload over its
+batch (for mlp784_epoch: the whole epoch).  The timed region is K steps, each
+bracketed by CUDA events on the launching stream, with an L2 flush (a 256 MiB
+write) between steps outside the events, and a barrier plus device
+synchronisation on both sides; the value is the maximum over ranks.  With N > 1
+every rank runs an independent replica (the step has no data-parallel
+exchange), so scaling is weak.
+
+`--impl reference` times the fp64 CPU oracle (the deliberately slow checker)
+on the same workload, each step a bounded sample, on the host cores of rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "training samples/s (tokens/s) per step on 1 GB300; % of BF16 tensor/HBM roofline"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ environment
+
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.15)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ roofline helpers
+
+def parse_kernel(name):
+    """'gemm_tc_bn256[M,N,K]' -> ('gemm_tc_bn256', (M, N, K))."""
+    if "[" in name:
+        base, rest = name.split("[", 1)
+        return base, tuple(int(v) for v in rest.rstrip("]").split(","))
+    return name, ()
+
+
+def algorithmic_work(name):
+    """(bound, units per launch) from the kernel's recorded shape.
+
+    GEMMs: 2 M N K flops.  Memory-bound kernels: the bytes they must move.
+    """
+    base, sh = parse_kernel(name)
+    if base.startswith("gemm"):
+        M_, N, K = sh
+        return "tensor", 2.0 * M_ * N * K
+    if base.startswith("block_fwd"):
+        T, d, h = sh
+        return "tensor", 4.0 * T * d * h
+    if base.startswith("block_bwd_act"):
+        T, d, h = sh
+        return "tensor", 4.0 * T * d * h
+    if base.startswith("block_bwd_dx"):
+        T, d, h = sh
+        return "tensor", 2.0 * T * d * h
+    if base == "sgd":
+        return "hbm", 22.0 * sh[0]        # read w, g, v; write w, v (fp32) + bf16 shadow
+    if base == "cast":
+        return "hbm", 3.0 * sh[0]         # byte in, bf16 out
+    if base == "xent":
+        B, C = sh
+        return "hbm", B * C * (4.0 + 2.0) + 8.0 * B
+    if base == "colsum":
+        r, c = sh
+        return "hbm", 2.0 * r * c + 4.0 * c
+    if base == "mse":
+        return "hbm", 6.0 * sh[0]
+    return "hbm", 0.0
+
+
+# ------------------------------------------------------------------ workloads
+
+class Workload:
+    name = ""
+    unit = "samples/s"
+    samples_per_step = 1
+    dtype = "bf16"
+    config = {}
+
+    def setup(self):
+        raise NotImplementedError
+
+    def step(self):
+        raise NotImplementedError
+
+    def step_e2e(self):
+        raise NotImplementedError
+
+    h2d_bytes = 0
+    d2h_bytes = 0
+    launches_per_step = 0
+
+    def check(self):
+        pass
+
+
+class MLP784Epoch(Workload):
+    """784-256-10, bf16 tensor-core path, one epoch (6,000 images, 47 steps)."""
+    name = "mlp784_epoch"
+    unit = "samples/s"
+    dtype = "bf16"
+
+    def __init__(self, prec_name="bf16", n_images=6000, batch=128):
+        self.prec_name = prec_name
+        self.n_images = n_images
+        self.batch = batch
+        self.samples_per_step = n_images
+        self.config = {"workload": "784-256-10 MLP, ReLU hidden, %s operands, fp32 accumulation "
+                                   "and master weights; one epoch = %d synthetic images "
+                                   "(%d steps of batch %d, last partial), lr 0.1, momentum 0.9"
+                       % (prec_name, n_images, (n_images + batch - 1) // batch, batch),
+                       "dims": [784, 256, 10], "batch": batch, "images_per_epoch": n_images,
+                       "train_steps_per_bench_step": (n_images + batch - 1) // batch,
+                       "cuda_graph": True, "l2": "flushed between timed steps (256 MiB write)"}
+
+    def setup(self):
+        import torch
+        import mlp_step_gb300 as M
+        from mlp_step_gb300 import synth
+        self.M = M
+        dims = [784, 256, 10]
+        prec = M.MLP_PREC_BF16 if self.prec_name == "bf16" else M.MLP_PREC_FP32
+        p0 = synth.mlp_flat_params(dims)
+        self.net = M.MLP(dims, prec=prec, max_batch=self.batch, params=torch.from_numpy(p0))
+        xb = synth.images_u8(self.n_images, 784)
+        y = synth.labels(self.n_images, 10)
+        self.x_host = torch.from_numpy(xb).pin_memory()
+        self.y_host = torch.from_numpy(y).pin_memory()
+        self.x = self.x_host.cuda()
+        self.y = self.y_host.cuda()
+        self.n_steps = (self.n_images + self.batch - 1) // self.batch
+        self.losses = torch.zeros(self.n_steps, 4, dtype=torch.float32, device="cuda")
+        self.losses_host = torch.zeros(self.n_steps, 4, dtype=torch.float32).pin_memory()
+        self.h2d_bytes = xb.nbytes + y.nbytes
+        self.d2h_bytes = self.n_steps * 4
+        # warm the kernels once eagerly (tensor maps, function attributes), then
+        # capture the epoch into one CUDA graph
+        self._epoch()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        c0 = M.launch_count()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(self.graph, stream=s):
+                self._epoch()
+        torch.cuda.current_stream().wait_stream(s)
+        self.launches_per_step = M.launch_count() - c0
+        torch.cuda.synchronize()
+
+    def _epoch(self):
+        for i in range(self.n_steps):
+            a = i * self.batch
+            b = min(self.n_images, a + self.batch)
+            self.net.train_step(self.x[a:b], self.y[a:b], 0.1, 0.9,
+                                loss_out=self.losses[i])
+
+    def step(self):
+        self.graph.replay()
+
+    def step_eager(self):
+        self._epoch()
+
+    def step_e2e(self):
+        self.x.copy_(self.x_host, non_blocking=True)
+        self.y.copy_(self.y_host, non_blocking=True)
+        self.graph.replay()
+        self.losses_host.copy_(self.losses, non_blocking=True)
+
+    def check(self):
+        import torch
+        torch.cuda.synchronize()
+        last = self.losses[:, 0].cpu().numpy()
+        assert np.all(np.isfinite(last)), "non-finite loss"
+        assert self.M.get_device_status() == self.M.MLP_OK
+
+    # --- reference arm and CPU baseline: the fp64 oracle
+    def oracle_sample(self, budget_s):
+        import oracle
+        from mlp_step_gb300 import synth
+        dims = [784, 256, 10]
+        p = synth.mlp_flat_params(dims).astype(np.float64)
+        v = np.zeros_like(p)
+        xb = synth.images_u8(self.n_images, 784).astype(np.float32) / np.float32(255)
+        y = synth.labels(self.n_images, 10)
+        t0 = time.perf_counter()
+        done = 0
+        steps = 0
+        while True:
+            for i in range(self.n_steps):
+                a = i * self.batch
+                b = min(self.n_images, a + self.batch)
+                _, p, v, _ = oracle.mlp_train_step(dims, p, v, xb[a:b].astype(np.float64),
+                                                   y[a:b], 0.1, 0.9,
+                                                   bf16_points=self.prec_name == "bf16")
+                done += b - a
+                steps += 1
+                if time.perf_counter() - t0 >= budget_s:
+                    break
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return done, dt, "%d oracle training steps (%d images of the epoch's stream), fp64" % (
+            steps, done)
+
+
+WORKLOADS = {
+    "mlp784_epoch": lambda: MLP784Epoch("bf16"),
+    "mlp784_fp32": lambda: MLP784Epoch("fp32", n_images=128),
+}
+
+
+# ------------------------------------------------------------------ measurement
+
+def timed_loop(fn, steps, flush, sync_barrier):
+    """Sum of per-step CUDA-event durations (ms) over `steps` calls of fn."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    sync_barrier()
+    for s, e in evs:
+        flush.zero_()
+        s.record()
+        fn()
+        e.record()
+    sync_barrier()
+    return sum(s.elapsed_time(e) for s, e in evs)
+
+
+def kernel_profile(wl, steps):
+    """Per-kernel average durations from the library's event timing (eager)."""
+    import torch
+    M = wl.M
+    M.timing_enable(True)
+    for _ in range(steps):
+        wl.step_eager()
+    torch.cuda.synchronize()
+    rep = M.timing_report()
+    M.timing_enable(False)
+    return rep
+
+
+def roofline_entry(rep, peaks, peaks_kind, sustained=False):
+    if not rep:
+        return None
+    # dominant kernel kind = largest total time, aggregated over shapes
+    by_base = {}
+    for name, (n, ms) in rep.items():
+        base, _ = parse_kernel(name)
+        by_base.setdefault(base, []).append((name, n, ms))
+    base = max(by_base, key=lambda b: sum(ms for _, _, ms in by_base[b]))
+    entries = by_base[base]
+    launches = sum(n for _, n, _ in entries)
+    total_ms = sum(ms for _, _, ms in entries)
+    work = 0.0
+    bound = "hbm"
+    for name, n, _ in entries:
+        bound, w = algorithmic_work(name)
+        work += w * n
+    avg_ms = total_ms / launches
+    per_launch = work / launches
+    if bound == "tensor":
+        achieved = per_launch / (avg_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        unit = "TFLOP/s"
+    else:
+        achieved = per_launch / (avg_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    share = total_ms / sum(ms for _, ms in rep.values())
+    return {"bound": bound, "kernel": base, "achieved": round(achieved, 3), "peak": peak,
+            "unit": unit, "frac": round(achieved / peak, 5), "traffic": None,
+            "peak_kind": peaks_kind + (" sustained" if sustained and bound == "tensor" else
+                                       (" burst" if bound == "tensor" else "")),
+            "launches_profiled": launches, "avg_launch_ms": round(avg_ms, 6),
+            "share_of_kernel_time": round(share, 4),
+            "work_per_launch": per_launch}
+
+
+def run_ours(args, wl):
+    import torch
+    rank, world, local = rank_info()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    def sync_barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    wl.setup()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    wl.check()
+
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        dev_ms = timed_loop(wl.step, args.steps, flush, sync_barrier)
+        wall = time.perf_counter() - t0
+    wl.check()
+    e2e_ms = timed_loop(wl.step_e2e, args.steps, flush, sync_barrier)
+    wl.check()
+
+    if dist is not None:
+        t = torch.tensor([dev_ms, e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dev_ms, e2e_ms = float(t[0]), float(t[1])
+
+    ms_per_step = dev_ms / args.steps
+    value = wl.samples_per_step * world / (ms_per_step * 1e-3)
+    e2e_value = wl.samples_per_step * world / (e2e_ms / args.steps * 1e-3)
+
+    peaks, peaks_kind = load_peaks()
+    rep = kernel_profile(wl, max(3, min(args.steps, 20)))
+    roof = roofline_entry(rep, peaks, peaks_kind)
+
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": wl.unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic", "config": dict(wl.config, parallelism="replicas" if world > 1
+                                            else "single GPU"),
+        "clocks": clk.summary(),
+        "e2e": {"value": round(e2e_value, 3), "unit": wl.unit,
+                "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
+        "gpu_launches": wl.launches_per_step * args.steps,
+        "roofline": roof,
+        "kernels": {k: [n, round(ms / n, 6)] for k, (n, ms) in sorted(rep.items())},
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        done, dt, sample = wl.oracle_sample(args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(done / dt, 3), "unit": wl.unit,
+                               "cores": os.cpu_count(), "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args, wl):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    per = []
+    done_total = 0
+    sample = ""
+    for i in range(args.warmup + args.steps):
+        done, dt, sample = wl.oracle_sample(args.ref_seconds)
+        if i >= args.warmup:
+            per.append((done, dt))
+            done_total += done
+    secs = sum(dt for _, dt in per)
+    value = done_total / secs
+    out = {"metric": METRIC, "impl": "reference", "value": round(value, 3), "unit": wl.unit,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": wl.config,
+           "cpu_baseline": {"value": round(value, 3), "unit": wl.unit, "cores": os.cpu_count(),
+                            "kind": "oracle", "sample": "each step: " + sample},
+           "e2e": {"value": round(value, 3), "unit": wl.unit, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mlp784_epoch", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    _, world, _ = rank_info()
+    if args.gpus > 1 and world == 1 and "RANK" not in os.environ:
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               "--nproc-per-node", str(args.gpus), "--master-addr", "127.0.0.1",
+               "--master-port", "29517", os.path.abspath(__file__)] + sys.argv[1:]
+        sys.exit(subprocess.call(cmd))
+    wl = WORKLOADS[args.workload]()
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

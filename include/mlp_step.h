@@ -90,6 +90,20 @@ void mlp_set_wait_limit_ns(long long ns);
  * Read the result with mlp_get_device_status(). */
 mlp_status mlp_selftest_wait_timeout(long long limit_ns, void* stream);
 
+/* Number of kernels this library has enqueued (or recorded into a stream
+ * capture) since it was loaded.  Host-side counter. */
+unsigned long long mlp_launch_count(void);
+
+/* Per-kernel timing for measurement: while enabled, every kernel launched on a
+ * stream that is not being captured is bracketed by CUDA events on that
+ * stream.  Enabling clears earlier records. */
+mlp_status mlp_timing_enable(int on);
+
+/* Synchronises the recorded events and writes a JSON object
+ * {"kernel[shape]": [launches, total_ms], ...} into buf (truncated to cap-1
+ * bytes, NUL-terminated).  Returns the bytes the full text needs. */
+size_t mlp_timing_report(char* buf, size_t cap);
+
 /* ---------------------------------------------------------------- MLP ------
  * An MLP with layer widths dims[0..n_dims-1]; every layer but the last applies
  * the hidden activation ([cap] "The minimum model": H = ReLU(X W1 + b1),

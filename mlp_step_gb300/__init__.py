@@ -53,6 +53,9 @@ SIGNATURES = {
     "mlp_get_device_status": (_i, [_vp]),
     "mlp_set_wait_limit_ns": (None, [_ll]),
     "mlp_selftest_wait_timeout": (_i, [_ll, _vp]),
+    "mlp_launch_count": (ctypes.c_ulonglong, []),
+    "mlp_timing_enable": (_i, [_i]),
+    "mlp_timing_report": (_sz, [ctypes.c_char_p, _sz]),
     "mlp_param_count": (_sz, [_vp, _i]),
     "mlp_param_offset": (_sz, [_vp, _i, _i, _i]),
     "mlp_shadow_elems": (_sz, [_vp, _i]),
@@ -157,6 +160,25 @@ def set_wait_limit_ns(ns: int) -> None:
 def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     _check(load().mlp_selftest_wait_timeout(int(limit_ns), _stream(stream)),
            "mlp_selftest_wait_timeout")
+
+
+def launch_count() -> int:
+    """Kernels enqueued (or captured) by the library since it was loaded."""
+    return load().mlp_launch_count()
+
+
+def timing_enable(on: bool) -> None:
+    load().mlp_timing_enable(1 if on else 0)
+
+
+def timing_report() -> dict:
+    """{"kernel[shape]": (launches, total_ms)} for launches since timing_enable(True)."""
+    import json
+    L = load()
+    need = L.mlp_timing_report(None, 0)
+    buf = ctypes.create_string_buffer(need + 16)
+    L.mlp_timing_report(buf, len(buf))
+    return {k: (v[0], v[1]) for k, v in json.loads(buf.value.decode()).items()}
 
 
 # ------------------------------------------------------------------ MLP

@@ -5,6 +5,7 @@
 // so results are bitwise reproducible from run to run.
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace mlp {
 
@@ -114,6 +115,7 @@ int sgd_grid(long long n) {
 mlp_status launch_sgd(float* w, const float* g, float* v, __nv_bfloat16* wb, long long n,
                       float lr, float mom, const SgdSegments& segs, cudaStream_t st) {
   if (n <= 0) return MLP_OK;
+  LaunchScope ls("sgd", st, n);
   sgd_kernel<<<sgd_grid(n), 256, 0, st>>>(w, g, v, wb, n, lr, mom, segs);
   return launch_status();
 }
@@ -121,6 +123,7 @@ mlp_status launch_sgd(float* w, const float* g, float* v, __nv_bfloat16* wb, lon
 mlp_status launch_shadow(const float* w, __nv_bfloat16* wb, long long n, const SgdSegments& segs,
                          cudaStream_t st) {
   if (n <= 0) return MLP_OK;
+  LaunchScope ls("shadow", st, n);
   shadow_kernel<<<sgd_grid(n), 256, 0, st>>>(w, wb, n, segs);
   return launch_status();
 }
@@ -147,6 +150,7 @@ mlp_status launch_cast(const void* src, int src_dtype, void* dst, int dst_bf16, 
   if (n <= 0) return MLP_OK;
   long long blocks = (n + 1023) / 1024;
   if (blocks > (long long)num_sms() * 8) blocks = (long long)num_sms() * 8;
+  LaunchScope ls("cast", st, n);
   cast_kernel<<<(int)blocks, 256, 0, st>>>(src, src_dtype, dst, dst_bf16, n);
   return launch_status();
 }
@@ -285,16 +289,21 @@ mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, i
                        void* ws, cudaStream_t st) {
   if (B <= 0) return MLP_OK;
   if (B <= 256) {
+    LaunchScope ls("xent", st, B, C);
     xent_single_block_kernel<<<1, 256, 0, st>>>(logits, ldl, labels, B, C, loss_out, dlog,
                                                 dl_bf16, ldd, argmax);
     return launch_status();
   }
   const int blocks = (B + 7) / 8;
   float* partial = static_cast<float*>(ws);
+  {
+  LaunchScope ls("xent", st, B, C);
   xent_rows_kernel<<<blocks, 256, 0, st>>>(logits, ldl, labels, B, C, partial, dlog, dl_bf16,
                                            ldd, argmax);
+  }
   MLP_CHECK(launch_status());
   if (loss_out) {
+    LaunchScope ls("sum_partials", st, blocks);
     sum_partials_kernel<<<1, 256, 0, st>>>(partial, blocks, (float)B, loss_out);
     return launch_status();
   }
@@ -384,14 +393,18 @@ mlp_status launch_colsum(const void* X, int bf16, int rows, int cols, int ld, fl
   colsum_plan(rows, cols, &ch, &rpc);
   dim3 grid((cols + 63) / 64, ch);
   float* dst = ch > 1 ? static_cast<float*>(ws) : out;
+  {
+  LaunchScope ls("colsum", st, rows, cols);
   if (bf16)
     colsum_pass1_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(X), rows, cols, ld, rpc, dst);
   else
     colsum_pass1_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(X), rows, cols,
                                                      ld, rpc, dst);
+  }
   MLP_CHECK(launch_status());
   if (ch > 1) {
+    LaunchScope ls("colsum_final", st, ch, cols);
     colsum_pass2_kernel<<<(cols + 255) / 256, 256, 0, st>>>(dst, ch, cols, out);
     return launch_status();
   }
@@ -461,11 +474,15 @@ mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out
   if (n <= 0) return MLP_OK;
   const int blocks = mse_blocks(n);
   float* partial = static_cast<float*>(ws);
+  {
+  LaunchScope ls("mse", st, n);
   mse_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(y),
                                      static_cast<const __nv_bfloat16*>(t), n,
                                      static_cast<__nv_bfloat16*>(dy), partial);
+  }
   MLP_CHECK(launch_status());
   if (loss_out) {
+    LaunchScope ls("sum_partials", st, blocks);
     sum_partials_kernel<<<1, 256, 0, st>>>(partial, blocks, (float)n, loss_out);
     return launch_status();
   }
@@ -488,6 +505,7 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns, int* err) {
 mlp_status launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st) {
   int* err = device_error_word();
   if (!err) return MLP_ERR_CUDA;
+  LaunchScope ls("wait_selftest", st);
   wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, err);
   return launch_status();
 }

@@ -12,6 +12,7 @@
 // steps of 16 staged through shared memory.  Each output sums k in ascending
 // order, so the result is deterministic.
 #include "kernels.cuh"
+#include "trace.cuh"
 
 namespace mlp {
 
@@ -101,6 +102,7 @@ mlp_status launch_gemm_simt(const GemmArgs& g, int in_bf16, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0) return MLP_OK;
   dim3 grid((g.N + 63) / 64, (g.M + 63) / 64);
   if (grid.y > 65535) return MLP_ERR_UNSUPPORTED_SHAPE;
+  LaunchScope ls("gemm_simt", st, g.M, g.N, g.K);
   if (in_bf16) gemm_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(g);
   else gemm_simt_kernel<float><<<grid, 256, 0, st>>>(g);
   return launch_status();

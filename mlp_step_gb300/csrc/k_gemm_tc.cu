@@ -24,6 +24,7 @@
 // recorded in the device error word and the CTA winds down cleanly.
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace mlp {
 
@@ -325,6 +326,8 @@ mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const TcParam
     configured = true;
   }
   int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  static const char* names[3] = {"gemm_tc_bn64", "gemm_tc_bn128", "gemm_tc_bn256"};
+  LaunchScope ls(names[BN == 64 ? 0 : (BN == 128 ? 1 : 2)], st, p.M, p.N, p.K);
   tc_gemm_kernel<BN, STAGES><<<grid, kThreads, L::SMEM, st>>>(ta, tb, p);
   return launch_status();
 }
