@@ -199,6 +199,29 @@ mlp_status softmax_xent_fwd_bwd(const float* logits, int ld_logits, const int32_
                                 int dlogits_dtype, int ld_dlogits, int32_t* argmax_out,
                                 void* workspace, size_t ws_bytes, void* stream);
 
+/* softmax_xent_fwd_bwd without a workspace argument, for callers that cannot
+ * allocate device memory: code that runs inside a host framework owning the
+ * whole device heap, a memory-pool or allocator callback, or a runtime that
+ * forbids allocation after start-up.  The pages have no counterpart; this is a
+ * deployment variant of the loss entry point above, with the same arguments
+ * and results apart from the workspace.
+ * Its scratch (the fixed-order partial sums of the batch mean) is a
+ * file-scope device array of 65,536 floats (256 KiB) that every GPU which
+ * loads the library holds until the process exits; batches above
+ * softmax_xent_noalloc_max_batch() = 524,288 rows return
+ * MLP_ERR_UNSUPPORTED_SHAPE.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture on the device.  The call allocates
+ * nothing.  All calls share the one array and it keeps the last call's
+ * contents (each call writes every partial it reads, so nothing needs
+ * clearing); calls that overlap on the GPU (different streams, or graph
+ * replays in flight together) race on it and must be serialised. */
+int softmax_xent_noalloc_max_batch(void);
+mlp_status softmax_xent_fwd_bwd_noalloc(const float* logits, int ld_logits,
+                                        const int32_t* labels, int batch, int classes,
+                                        float* loss_out, void* dlogits, int dlogits_dtype,
+                                        int ld_dlogits, int32_t* argmax_out, void* stream);
+
 /* ---------------------------------------------------------------- update ---
  * Momentum SGD over one flat buffer ([cap] "Read the worked reference"):
  *   v <- momentum * v - lr * g;  w <- w + v.

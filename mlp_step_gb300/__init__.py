@@ -69,6 +69,8 @@ SIGNATURES = {
     "mlp_train_step": (_i, [_vp, _vp, _i, _vp, _i, _f, _f, _vp, _vp, _vp]),
     "softmax_xent_workspace_bytes": (_sz, [_i, _i]),
     "softmax_xent_fwd_bwd": (_i, [_vp, _i, _vp, _i, _i, _vp, _vp, _i, _i, _vp, _vp, _sz, _vp]),
+    "softmax_xent_noalloc_max_batch": (_i, []),
+    "softmax_xent_fwd_bwd_noalloc": (_i, [_vp, _i, _vp, _i, _i, _vp, _vp, _i, _i, _vp, _vp]),
     "sgd_momentum_step": (_i, [_vp, _vp, _vp, _vp, _sz, _f, _f, _vp]),
     "mlp_gemm": (_i, [_i, _i, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _i, _vp, _i, _vp, _i, _i,
                       _vp]),
@@ -277,6 +279,19 @@ def softmax_xent_fwd_bwd(logits, labels, loss_out, dlogits=None, argmax_out=None
                                        _ptr(loss_out), _ptr(dlogits), dl_dtype, ldd,
                                        _ptr(argmax_out), _ptr(workspace), wsb, _stream(stream)),
            "softmax_xent_fwd_bwd")
+
+
+def softmax_xent_fwd_bwd_noalloc(logits, labels, loss_out, dlogits=None, argmax_out=None,
+                                 classes=None, stream=None):
+    """softmax_xent_fwd_bwd with the library's fixed device scratch (no workspace)."""
+    B = logits.shape[0]
+    C = logits.shape[1] if classes is None else classes
+    dl_dtype = _dtype_code(dlogits) if dlogits is not None else MLP_DTYPE_F32
+    ldd = dlogits.shape[1] if dlogits is not None else C
+    _check(load().softmax_xent_fwd_bwd_noalloc(_ptr(logits), logits.stride(0), _ptr(labels), B,
+                                               C, _ptr(loss_out), _ptr(dlogits), dl_dtype, ldd,
+                                               _ptr(argmax_out), _stream(stream)),
+           "softmax_xent_fwd_bwd_noalloc")
 
 
 def sgd_momentum_step(w, g, v, lr, momentum, w_bf16=None, stream=None):

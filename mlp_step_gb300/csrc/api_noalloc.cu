@@ -1,0 +1,70 @@
+// softmax_xent_fwd_bwd_noalloc: the softmax cross-entropy entry point for
+// callers that cannot allocate device memory.  Its only scratch (the per-block
+// partial losses of the fixed-order mean) lives in a file-scope device array
+// of a fixed size instead of a caller-provided workspace.
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace {
+
+// Partial sums of the batch mean: one float per 8 rows (one block of 8 warps).
+constexpr int kMaxPartials = 65536;  // 256 KiB: batches up to 524,288 rows
+static __device__ __align__(256) float g_xent_scratch[kMaxPartials];
+
+// Device address of g_xent_scratch on the current device.  Host code only
+// sees a host-side stand-in under the array's name, so the address is looked
+// up once per device with cudaGetSymbolAddress (the device must be current).
+float* scratch_address(mlp_status* st) {
+  static float* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *st = MLP_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_xent_scratch) != cudaSuccess || !p) {
+      *st = MLP_ERR_CUDA;
+      return nullptr;
+    }
+    addr[dev] = static_cast<float*>(p);
+  }
+  *st = MLP_OK;
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+int softmax_xent_noalloc_max_batch(void) { return kMaxPartials * 8; }
+
+mlp_status softmax_xent_fwd_bwd_noalloc(const float* logits, int ld_logits,
+                                        const int32_t* labels, int batch, int classes,
+                                        float* loss_out, void* dlogits, int dlogits_dtype,
+                                        int ld_dlogits, int32_t* argmax_out, void* stream) {
+  if (batch < 0 || classes <= 0) return MLP_ERR_INVALID_ARG;
+  if (batch == 0) return MLP_OK;
+  if (batch > kMaxPartials * 8) return MLP_ERR_UNSUPPORTED_SHAPE;
+  if (!logits || !labels || ld_logits < classes) return MLP_ERR_INVALID_ARG;
+  if (dlogits && (ld_dlogits < classes ||
+                  (dlogits_dtype != MLP_DTYPE_F32 && dlogits_dtype != MLP_DTYPE_BF16)))
+    return MLP_ERR_INVALID_ARG;
+  if (!mlp::aligned16(logits) || !mlp::aligned16(labels) ||
+      (dlogits && !mlp::aligned16(dlogits)) || (argmax_out && !mlp::aligned16(argmax_out)) ||
+      (loss_out && !mlp::aligned16(loss_out)))
+    return MLP_ERR_MISALIGNED;
+  mlp_status st = MLP_OK;
+  float* scratch = scratch_address(&st);
+  if (!scratch) return st;
+  // Every partial the mean reads is written by this call first, so nothing
+  // has to be cleared between calls.
+  return mlp::launch_xent(logits, ld_logits, labels, batch, classes, loss_out, dlogits,
+                          dlogits_dtype == MLP_DTYPE_BF16, ld_dlogits, argmax_out, scratch,
+                          static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
