@@ -1,0 +1,735 @@
+// Transformer MLP block kernels for sm_103a ("Full-Depth MLP Megakernel +
+// Fused Attention Preprocessing", "What Worked": RMSNorm -> gate projection ->
+// LeakyReLU^2 -> down projection -> residual, the wide intermediate never
+// written to memory).
+//
+// Forward (block_fwd_kernel): one CTA pair (a 2-CTA cluster) per 128-token
+// tile.  Tensor memory of a CTA holds its half of the 128 x 512 fp32 output
+// (256 columns) and two 128-column gate-chunk accumulators.  The 12 hidden
+// chunks of 128 are split between the pair (CTA r computes chunks c with
+// c % 2 == r): the gate MMA U_c = x W_gate[:, c] runs in tensor memory, the
+// epilogue warps apply RMSNorm's row scale and LeakyReLU^2 in fp32, round to
+// bf16 and write the activation chunk A_c into the operand slot of BOTH CTAs'
+// shared memory (the peer's through distributed shared memory); both CTAs
+// then accumulate y_half += A_c W_down[c, half].  So no FLOP is recomputed and
+// the intermediate stays on chip (the page's design kept it in registers and
+// lost to one large library GEMM; here it lives in tensor memory and shared
+// memory and is fed to the tensor cores directly).
+//
+// RMSNorm with gain 1 is folded into the epilogue: u = r (x W_gate) with
+// r = 1 / sqrt(mean(x^2) + eps) per token, so the gate GEMM reads x as is.
+//
+// Backward (block_bwd_act_kernel): per 128-token x 128-hidden tile, two MMA
+// accumulators U = x W_gate[:, c] and DA = dy W_down[c, :]^T over K = 512;
+// the epilogue writes a = f(r U) and r du = r DA f'(r U) in bf16 for the
+// weight-gradient GEMMs.  rmsnorm_bwd_kernel finishes dx from
+// dn' = (r du) W_gate^T.
+#include "kernels.cuh"
+#include "ptx.cuh"
+#include "trace.cuh"
+
+namespace mlp {
+
+namespace {
+
+constexpr int TM = 128;                 // tokens per tile
+constexpr int DM = 512;                 // model width
+constexpr int HC = 128;                 // hidden chunk
+constexpr int YH = 256;                 // output columns per CTA of the pair
+constexpr int F_STAGES = 4;
+constexpr int F_STAGE_BYTES = 32768;
+constexpr int F_SLOT_BYTES = TM * HC * 2;  // 32 KiB bf16 activation chunk
+constexpr int F_SMEM = 1024 + 2 * F_SLOT_BYTES + F_STAGES * F_STAGE_BYTES + 512;
+constexpr int kThreads = 192;
+
+__device__ __forceinline__ float lrelu_sq(float u, float slope) {
+  const float t = u > 0.f ? u : slope * u;
+  return t * t;
+}
+
+__device__ __forceinline__ float lrelu_sq_grad(float u, float slope) {
+  return u > 0.f ? 2.f * u : 2.f * slope * slope * u;
+}
+
+// RMSNorm scale of one token row of x (bf16 [DM]).
+__device__ __forceinline__ float row_rstd(const __nv_bfloat16* xrow, float eps) {
+  float ss = 0.f;
+  const uint4* p = reinterpret_cast<const uint4*>(xrow);
+#pragma unroll 4
+  for (int q = 0; q < DM / 8; ++q) {
+    const uint4 v = __ldg(p + q);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      ss += f.x * f.x;
+      ss += f.y * f.y;
+    }
+  }
+  return 1.0f / sqrtf(ss / (float)DM + eps);
+}
+
+struct FwdParams {
+  int T, hidden, tiles, n_own;
+  float eps, slope;
+  const __nv_bfloat16* x;
+  __nv_bfloat16* y;
+  float* rstd;
+  unsigned long long wait_ns;
+  int* err;
+};
+
+// MMA issue order of one tile for a CTA that owns n_own gate chunks:
+// G0, then groups (G_g, D_{2g-2}, D_{2g-1}) for g = 1 .. n_own-1, then the last
+// two down chunks -- 3 n_own operations.  op >= 0: gate chunk j = op;
+// op < 0: down chunk c = -op - 1.
+__device__ __forceinline__ int fwd_op(int i, int n_own) {
+  if (i == 0) return 0;
+  const int tail = 3 * n_own - 2;
+  if (i >= tail) return -(2 * n_own - 2 + (i - tail)) - 1;
+  const int g = (i - 1) / 3 + 1;
+  const int r = (i - 1) % 3;
+  if (r == 0) return g;
+  return -(2 * (g - 1) + (r - 1)) - 1;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    block_fwd_kernel(const __grid_constant__ CUtensorMap tmX,
+                     const __grid_constant__ CUtensorMap tmWg,
+                     const __grid_constant__ CUtensorMap tmWd, const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* slots = smem;                                   // 2 x 32 KiB activation chunks
+  uint8_t* stages = smem + 2 * F_SLOT_BYTES;               // F_STAGES x 32 KiB
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + F_STAGES * F_STAGE_BYTES);
+  uint64_t* empty = full + F_STAGES;
+  uint64_t* ufull = empty + F_STAGES;    // [2] gate accumulator ready
+  uint64_t* uempty = ufull + 2;          // [2] gate accumulator drained (128 arrivals)
+  uint64_t* afull = uempty + 2;          // [2] activation slot s written (128 arrivals)
+  uint64_t* aempty = afull + 2;          // [2] slot s consumed by both CTAs (2 arrivals)
+  uint64_t* yfull = aempty + 2;
+  uint64_t* yempty = yfull + 1;          // 128 arrivals
+  uint64_t* done = yempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+  const int cluster = blockIdx.x >> 1;
+  const int n_clusters = gridDim.x >> 1;
+  const int n_ops = 3 * p.n_own;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < F_STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&ufull[b], 1);
+      ptx::mbar_init(&uempty[b], 128);
+      ptx::mbar_init(&afull[b], 128);
+      ptx::mbar_init(&aempty[b], 2);
+    }
+    ptx::mbar_init(yfull, 1);
+    ptx::mbar_init(yempty, 128);
+    ptx::mbar_init(done, 1);
+    *s_abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&tmX);
+    ptx::prefetch_tensormap(&tmWg);
+    ptx::prefetch_tensormap(&tmWd);
+  }
+  if (warp == 1) ptx::tmem_alloc(tmem_slot, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // the peer's barriers are initialised before any remote arrive
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // y half: cols [0,256); U buffers: [256,384), [384,512)
+
+  int last_parity[F_STAGES];
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      for (int s = 0; s < F_STAGES; ++s) last_parity[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = cluster; t < p.tiles && ok && !*s_abort; t += n_clusters) {
+        for (int i = 0; i < n_ops && ok; ++i) {
+          const int op = fwd_op(i, p.n_own);
+          const int nkb = op >= 0 ? DM / 64 : HC / 64;
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
+                                        DEVERR_TIMEOUT_PRODUCER)) {
+              *s_abort = 1;
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&full[stage], F_STAGE_BYTES);
+            last_parity[stage] = (int)phase;
+            uint8_t* st = stages + stage * F_STAGE_BYTES;
+            if (op >= 0) {
+              const int c = 2 * op + (int)rank;
+              ptx::tma_load_2d(st, &tmX, &full[stage], kb * 64, t * TM);
+              ptx::tma_load_2d(st + 16384, &tmWg, &full[stage], c * HC, kb * 64);
+              ptx::tma_load_2d(st + 24576, &tmWg, &full[stage], c * HC + 64, kb * 64);
+            } else {
+              const int c = -op - 1;
+#pragma unroll
+              for (int j = 0; j < YH / 64; ++j)
+                ptx::tma_load_2d(st + j * 8192, &tmWd, &full[stage], (int)rank * YH + j * 64,
+                                 c * HC + kb * 64);
+            }
+            if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_g = ptx::idesc_bf16_f32(TM, HC, 0, 1);
+      const uint32_t idesc_d = ptx::idesc_bf16_f32(TM, YH, 0, 1);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t ucount[2] = {0, 0}, acount[2] = {0, 0}, ycount = 0;
+      bool ok = true;
+      for (int t = cluster; t < p.tiles && ok && !*s_abort; t += n_clusters) {
+        for (int i = 0; i < n_ops && ok; ++i) {
+          const int op = fwd_op(i, p.n_own);
+          if (op >= 0) {
+            const int b = op & 1;
+            if (!ptx::mbar_wait_bounded(&uempty[b], (ucount[b] & 1) ^ 1, p.wait_ns, p.err,
+                                        DEVERR_TIMEOUT_MMA)) { ok = false; break; }
+            ++ucount[b];
+            ptx::tc_fence_after();
+            const uint32_t d = tmem + 256 + b * HC;
+            for (int kb = 0; kb < DM / 64; ++kb) {
+              if (!ptx::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err,
+                                          DEVERR_TIMEOUT_MMA)) { ok = false; break; }
+              ptx::tc_fence_after();
+              const uint32_t sa = ptx::smem_u32(stages + stage * F_STAGE_BYTES);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = ptx::sw128_desc(sa + k * 32, 16, 1024);
+                const uint64_t bd = ptx::sw128_desc(sa + 16384 + k * 2048, 8192, 1024);
+                ptx::mma_bf16(d, ad, bd, idesc_g, (kb > 0 || k > 0) ? 1u : 0u);
+              }
+              ptx::mma_commit(&empty[stage]);
+              if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+            ptx::mma_commit(&ufull[b]);
+          } else {
+            const int c = -op - 1;
+            const int s = c & 1;
+            if (c == 0) {
+              if (!ptx::mbar_wait_bounded(yempty, (ycount & 1) ^ 1, p.wait_ns, p.err,
+                                          DEVERR_TIMEOUT_MMA)) { ok = false; break; }
+              ++ycount;
+            }
+            if (!ptx::mbar_wait_cluster_bounded(&afull[s], acount[s] & 1, p.wait_ns, p.err,
+                                                DEVERR_TIMEOUT_PEER)) { ok = false; break; }
+            ++acount[s];
+            ptx::tc_fence_after();
+            const uint32_t a_base = ptx::smem_u32(slots + s * F_SLOT_BYTES);
+            for (int kb = 0; kb < HC / 64; ++kb) {
+              if (!ptx::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err,
+                                          DEVERR_TIMEOUT_MMA)) { ok = false; break; }
+              ptx::tc_fence_after();
+              const uint32_t sb = ptx::smem_u32(stages + stage * F_STAGE_BYTES);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = ptx::sw128_desc(a_base + kb * 16384 + k * 32, 16, 1024);
+                const uint64_t bd = ptx::sw128_desc(sb + k * 2048, 8192, 1024);
+                ptx::mma_bf16(tmem, ad, bd, idesc_d, (c > 0 || kb > 0 || k > 0) ? 1u : 0u);
+              }
+              ptx::mma_commit(&empty[stage]);
+              if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+            // slot s is reusable once both CTAs' MMAs that read it are done
+            ptx::mma_commit_multicast(&aempty[s], (uint16_t)(1u << s));
+            if (c == 2 * p.n_own - 1) ptx::mma_commit(yfull);
+          }
+        }
+      }
+      if (!ok) *s_abort = 1;
+      ptx::mma_commit(done);
+      ptx::mbar_wait_bounded(done, 0, p.wait_ns, p.err, DEVERR_TIMEOUT_TEARDOWN);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue warps
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    uint32_t uc[2] = {0, 0}, ac = 0, yc = 0;
+    uint8_t* my_slot = slots + rank * F_SLOT_BYTES;
+    const uint32_t my_slot_addr = ptx::smem_u32(my_slot);
+    const uint32_t peer_slot_addr = ptx::mapa_shared(my_slot_addr, peer);
+    const uint32_t afull_peer = ptx::mapa_shared(ptx::smem_u32(&afull[rank]), peer);
+    bool ok = true;
+    for (int t = cluster; t < p.tiles && ok; t += n_clusters) {
+      if (*s_abort) break;
+      const int m = t * TM + row;
+      const bool valid = m < p.T;
+      float r = 0.f;
+      if (valid) {
+        r = row_rstd(p.x + (size_t)m * DM, p.eps);
+        if (rank == 0 && p.rstd) p.rstd[m] = r;
+      }
+      // activation chunks this CTA owns
+      for (int j = 0; j < p.n_own && ok; ++j) {
+        const int b = j & 1;
+        if (!ptx::mbar_wait_bounded(&ufull[b], uc[b] & 1, p.wait_ns, p.err,
+                                    DEVERR_TIMEOUT_EPILOGUE)) { ok = false; break; }
+        ++uc[b];
+        if (!ptx::mbar_wait_bounded(&aempty[rank], (ac & 1) ^ 1, p.wait_ns, p.err,
+                                    DEVERR_TIMEOUT_EPILOGUE)) { ok = false; break; }
+        ++ac;
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < HC / 32; ++cc) {
+          uint32_t v[32];
+          __syncwarp();
+          ptx::tmem_ld_32x32b_x32(tmem + lane_off + 256 + b * HC + cc * 32, v);
+          ptx::tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a0 = lrelu_sq(__uint_as_float(v[2 * e]) * r, p.slope);
+            const float a1 = lrelu_sq(__uint_as_float(v[2 * e + 1]) * r, p.slope);
+            pk[e] = pack_bf16x2(a0, a1);
+          }
+          // K-major 128B-swizzled operand layout: 64-wide k blocks of
+          // [128 rows][128 B]; 16-byte chunk j of row `row` sits at
+          // chunk (j ^ (row & 7)).
+          const int kb = cc >> 1;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int j16 = (cc & 1) * 4 + q;
+            const uint32_t off =
+                (uint32_t)(kb * 16384 + row * 128 + ((j16 ^ (row & 7)) << 4));
+            const uint4 w = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            ptx::st_shared_v4(my_slot_addr + off, w);
+            ptx::st_cluster_v4(peer_slot_addr + off, w);
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&uempty[b]);
+        ptx::fence_proxy_async_cluster();
+        ptx::mbar_arrive(&afull[rank]);
+        ptx::mbar_arrive_remote(afull_peer);
+      }
+      if (!ok) break;
+      // output half: y = x + acc
+      if (!ptx::mbar_wait_bounded(yfull, yc & 1, p.wait_ns, p.err, DEVERR_TIMEOUT_EPILOGUE)) {
+        ok = false;
+        break;
+      }
+      ++yc;
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int cc = 0; cc < YH / 32; ++cc) {
+        uint32_t v[32];
+        __syncwarp();
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + cc * 32, v);
+        ptx::tmem_ld_wait();
+        if (valid) {
+          const int n0 = (int)rank * YH + cc * 32;
+          const uint4* xr = reinterpret_cast<const uint4*>(p.x + (size_t)m * DM + n0);
+          uint4* yr = reinterpret_cast<uint4*>(p.y + (size_t)m * DM + n0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 xv = __ldg(xr + q);
+            const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xv);
+            uint4 o;
+            uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 xf = __bfloat1622float2(xh[e]);
+              op[e] = pack_bf16x2(__uint_as_float(v[q * 8 + 2 * e]) + xf.x,
+                                  __uint_as_float(v[q * 8 + 2 * e + 1]) + xf.y);
+            }
+            yr[q] = o;
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(yempty);
+    }
+    if (!ok) *s_abort = 1;
+  }
+
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (*s_abort && warp == 0 && lane == 0) {
+    for (int s = 0; s < F_STAGES; ++s)
+      if (last_parity[s] >= 0)
+        ptx::mbar_wait_bounded(&full[s], (uint32_t)last_parity[s], p.wait_ns, p.err,
+                               DEVERR_TIMEOUT_TEARDOWN);
+  }
+  __syncwarp();
+  __syncthreads();
+  __syncwarp();
+  // neither CTA leaves while the peer may still write into its shared memory
+  ptx::cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ backward
+
+constexpr int B_STAGES = 3;
+constexpr int B_STAGE_BYTES = 65536;   // x, W_gate, dy, W_down tiles of 16 KiB each
+constexpr int B_SMEM = 1024 + B_STAGES * B_STAGE_BYTES + 512;
+
+struct BwdParams {
+  int T, hidden, tiles_m, tiles_h, num_tiles;
+  float slope;
+  const float* rstd;
+  __nv_bfloat16* a_out;    // [T][hidden]
+  __nv_bfloat16* du_out;   // [T][hidden], r * du
+  unsigned long long wait_ns;
+  int* err;
+};
+
+// 8 token tiles at a time sweep all hidden chunks (the last group may be
+// shorter), so CTAs running together share x / dy rows and weight columns.
+__device__ __forceinline__ void bwd_tile(int t, int tiles_m, int tiles_h, int& tm, int& th) {
+  constexpr int G = 8;
+  const int group = t / (G * tiles_h);
+  const int first = group * G;
+  const int gm = min(tiles_m - first, G);
+  const int r = t - group * G * tiles_h;
+  tm = first + r % gm;
+  th = r / gm;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    block_bwd_act_kernel(const __grid_constant__ CUtensorMap tmX,
+                         const __grid_constant__ CUtensorMap tmWg,
+                         const __grid_constant__ CUtensorMap tmDy,
+                         const __grid_constant__ CUtensorMap tmWd, const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + B_STAGES * B_STAGE_BYTES);
+  uint64_t* empty = full + B_STAGES;
+  uint64_t* tfull = empty + B_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < B_STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&tfull[b], 1);
+      ptx::mbar_init(&tempty[b], 128);
+    }
+    ptx::mbar_init(done, 1);
+    *s_abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&tmX);
+    ptx::prefetch_tensormap(&tmWg);
+    ptx::prefetch_tensormap(&tmDy);
+    ptx::prefetch_tensormap(&tmWd);
+  }
+  if (warp == 1) ptx::tmem_alloc(tmem_slot, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // buffer b: U at b*256, DA at b*256 + 128
+  int last_parity[B_STAGES];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < B_STAGES; ++s) last_parity[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok && !*s_abort; t += gridDim.x) {
+        int tm, th;
+        bwd_tile(t, p.tiles_m, p.tiles_h, tm, th);
+        for (int kb = 0; kb < DM / 64; ++kb) {
+          if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
+                                      DEVERR_TIMEOUT_PRODUCER)) {
+            *s_abort = 1;
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&full[stage], B_STAGE_BYTES);
+          last_parity[stage] = (int)phase;
+          uint8_t* st = stages + stage * B_STAGE_BYTES;
+          ptx::tma_load_2d(st, &tmX, &full[stage], kb * 64, tm * TM);
+          ptx::tma_load_2d(st + 16384, &tmWg, &full[stage], th * HC, kb * 64);
+          ptx::tma_load_2d(st + 24576, &tmWg, &full[stage], th * HC + 64, kb * 64);
+          ptx::tma_load_2d(st + 32768, &tmDy, &full[stage], kb * 64, tm * TM);
+          ptx::tma_load_2d(st + 49152, &tmWd, &full[stage], kb * 64, th * HC);
+          if (++stage == B_STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc_u = ptx::idesc_bf16_f32(TM, HC, 0, 1);   // B = W_gate, N-major
+      const uint32_t idesc_a = ptx::idesc_bf16_f32(TM, HC, 0, 0);   // B = W_down rows, K-major
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok && !*s_abort; t += gridDim.x) {
+        if (!ptx::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err,
+                                    DEVERR_TIMEOUT_MMA)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t du = tmem + acc * 256;
+        const uint32_t da = du + 128;
+        for (int kb = 0; kb < DM / 64; ++kb) {
+          if (!ptx::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err,
+                                      DEVERR_TIMEOUT_MMA)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t sb = ptx::smem_u32(stages + stage * B_STAGE_BYTES);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t en = (kb > 0 || k > 0) ? 1u : 0u;
+            ptx::mma_bf16(du, ptx::sw128_desc(sb + k * 32, 16, 1024),
+                          ptx::sw128_desc(sb + 16384 + k * 2048, 8192, 1024), idesc_u, en);
+            ptx::mma_bf16(da, ptx::sw128_desc(sb + 32768 + k * 32, 16, 1024),
+                          ptx::sw128_desc(sb + 49152 + k * 32, 16, 1024), idesc_a, en);
+          }
+          ptx::mma_commit(&empty[stage]);
+          if (++stage == B_STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&tfull[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      if (!ok) *s_abort = 1;
+      ptx::mma_commit(done);
+      ptx::mbar_wait_bounded(done, 0, p.wait_ns, p.err, DEVERR_TIMEOUT_TEARDOWN);
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      if (*s_abort) break;
+      if (!ptx::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err,
+                                  DEVERR_TIMEOUT_EPILOGUE)) {
+        *s_abort = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      int tm, th;
+      bwd_tile(t, p.tiles_m, p.tiles_h, tm, th);
+      const int m = tm * TM + row;
+      const bool valid = m < p.T;
+      const float r = valid ? __ldg(p.rstd + m) : 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < HC / 32; ++cc) {
+        uint32_t vu[32], va[32];
+        __syncwarp();
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + acc * 256 + cc * 32, vu);
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + acc * 256 + 128 + cc * 32, va);
+        ptx::tmem_ld_wait();
+        if (valid) {
+          uint32_t pa[16], pd[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float u0 = __uint_as_float(vu[2 * e]) * r;
+            const float u1 = __uint_as_float(vu[2 * e + 1]) * r;
+            pa[e] = pack_bf16x2(lrelu_sq(u0, p.slope), lrelu_sq(u1, p.slope));
+            const float d0 = __uint_as_float(va[2 * e]) * lrelu_sq_grad(u0, p.slope) * r;
+            const float d1 = __uint_as_float(va[2 * e + 1]) * lrelu_sq_grad(u1, p.slope) * r;
+            pd[e] = pack_bf16x2(d0, d1);
+          }
+          const size_t off = (size_t)m * p.hidden + th * HC + cc * 32;
+          uint4* ao = reinterpret_cast<uint4*>(p.a_out + off);
+          uint4* dd = reinterpret_cast<uint4*>(p.du_out + off);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            ao[q] = make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
+            dd[q] = make_uint4(pd[4 * q], pd[4 * q + 1], pd[4 * q + 2], pd[4 * q + 3]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tempty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (*s_abort && warp == 0 && lane == 0) {
+    for (int s = 0; s < B_STAGES; ++s)
+      if (last_parity[s] >= 0)
+        ptx::mbar_wait_bounded(&full[s], (uint32_t)last_parity[s], p.wait_ns, p.err,
+                               DEVERR_TIMEOUT_TEARDOWN);
+  }
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// dx = dy + dn' - r^2 x s, s = mean_i(dn'_i x_i), with dn' = (r du) W_gate^T.
+// One warp per token row; lanes hold 16 of the 512 columns.
+__global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const float* __restrict__ dnp,
+                                                          const __nv_bfloat16* __restrict__ x,
+                                                          const __nv_bfloat16* __restrict__ dy,
+                                                          const float* __restrict__ rstd, int T,
+                                                          __nv_bfloat16* __restrict__ dx) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const size_t base = (size_t)t * DM;
+  float dn[16], xv[16];
+  // lane owns columns [lane*8, lane*8+8) and [256 + lane*8, 256 + lane*8 + 8)
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c0 = h * 256 + lane * 8;
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(dnp + base + c0));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(dnp + base + c0 + 4));
+    dn[h * 8 + 0] = a.x; dn[h * 8 + 1] = a.y; dn[h * 8 + 2] = a.z; dn[h * 8 + 3] = a.w;
+    dn[h * 8 + 4] = b.x; dn[h * 8 + 5] = b.y; dn[h * 8 + 6] = b.z; dn[h * 8 + 7] = b.w;
+    const uint4 xq = __ldg(reinterpret_cast<const uint4*>(x + base + c0));
+    const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xq);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(xh[e]);
+      xv[h * 8 + 2 * e] = f.x;
+      xv[h * 8 + 2 * e + 1] = f.y;
+    }
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) s += dn[i] * xv[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  s /= (float)DM;
+  const float r = rstd[t];
+  const float k = r * r * s;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c0 = h * 256 + lane * 8;
+    const uint4 dq = __ldg(reinterpret_cast<const uint4*>(dy + base + c0));
+    const __nv_bfloat162* dh = reinterpret_cast<const __nv_bfloat162*>(&dq);
+    uint4 o;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(dh[e]);
+      const int i0 = h * 8 + 2 * e;
+      op[e] = pack_bf16x2(f.x + dn[i0] - k * xv[i0], f.y + dn[i0 + 1] - k * xv[i0 + 1]);
+    }
+    *reinterpret_cast<uint4*>(dx + base + c0) = o;
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+
+mlp_status launch_block_fwd(const void* x, const void* wg, const void* wd, int T, int hidden,
+                            float eps, float slope, void* y, float* rstd, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(block_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             F_SMEM) != cudaSuccess)
+      return MLP_ERR_CUDA;
+    configured = true;
+  }
+  CUtensorMap tx, tg, td;
+  if (!encode_tmap_bf16_2d(&tx, x, DM, T, DM * 2, 64, TM)) return MLP_ERR_CUDA;
+  if (!encode_tmap_bf16_2d(&tg, wg, hidden, DM, (unsigned long long)hidden * 2, 64, 64))
+    return MLP_ERR_CUDA;
+  if (!encode_tmap_bf16_2d(&td, wd, DM, hidden, DM * 2, 64, 64)) return MLP_ERR_CUDA;
+  FwdParams p;
+  p.T = T;
+  p.hidden = hidden;
+  p.tiles = (T + TM - 1) / TM;
+  p.n_own = hidden / (2 * HC);
+  p.eps = eps;
+  p.slope = slope;
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.rstd = rstd;
+  p.wait_ns = wait_limit_ns();
+  p.err = device_error_word();
+  if (!p.err) return MLP_ERR_CUDA;
+  int clusters = num_sms() / 2;
+  if (clusters > p.tiles) clusters = p.tiles;
+  if (clusters < 1) clusters = 1;
+  LaunchScope ls("block_fwd", st, T, DM, hidden);
+  block_fwd_kernel<<<2 * clusters, kThreads, F_SMEM, st>>>(tx, tg, td, p);
+  return launch_status();
+}
+
+mlp_status launch_block_bwd_act(const void* x, const void* wg, const void* wd, const void* dy,
+                                const float* rstd, int T, int hidden, float slope, void* a_out,
+                                void* du_out, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(block_bwd_act_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             B_SMEM) != cudaSuccess)
+      return MLP_ERR_CUDA;
+    configured = true;
+  }
+  CUtensorMap tx, tg, tdy, twd;
+  if (!encode_tmap_bf16_2d(&tx, x, DM, T, DM * 2, 64, TM)) return MLP_ERR_CUDA;
+  if (!encode_tmap_bf16_2d(&tg, wg, hidden, DM, (unsigned long long)hidden * 2, 64, 64))
+    return MLP_ERR_CUDA;
+  if (!encode_tmap_bf16_2d(&tdy, dy, DM, T, DM * 2, 64, TM)) return MLP_ERR_CUDA;
+  if (!encode_tmap_bf16_2d(&twd, wd, DM, hidden, DM * 2, 64, HC)) return MLP_ERR_CUDA;
+  BwdParams p;
+  p.T = T;
+  p.hidden = hidden;
+  p.tiles_m = (T + TM - 1) / TM;
+  p.tiles_h = hidden / HC;
+  p.num_tiles = p.tiles_m * p.tiles_h;
+  p.slope = slope;
+  p.rstd = rstd;
+  p.a_out = static_cast<__nv_bfloat16*>(a_out);
+  p.du_out = static_cast<__nv_bfloat16*>(du_out);
+  p.wait_ns = wait_limit_ns();
+  p.err = device_error_word();
+  if (!p.err) return MLP_ERR_CUDA;
+  int grid = num_sms();
+  if (grid > p.num_tiles) grid = p.num_tiles;
+  LaunchScope ls("block_bwd_act", st, T, DM, hidden);
+  block_bwd_act_kernel<<<grid, kThreads, B_SMEM, st>>>(tx, tg, tdy, twd, p);
+  return launch_status();
+}
+
+mlp_status launch_rmsnorm_bwd(const float* dnp, const void* x, const void* dy, const float* rstd,
+                              int T, void* dx, cudaStream_t st) {
+  if (T <= 0) return MLP_OK;
+  LaunchScope ls("rmsnorm_bwd", st, T);
+  rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(dnp, static_cast<const __nv_bfloat16*>(x),
+                                                  static_cast<const __nv_bfloat16*>(dy), rstd, T,
+                                                  static_cast<__nv_bfloat16*>(dx));
+  return launch_status();
+}
+
+}  // namespace mlp

@@ -53,6 +53,15 @@ mlp_status launch_gemm_simt(const GemmArgs& g, int in_bf16, cudaStream_t st);
 // k_gemm_tc.cu: tcgen05 bf16 GEMM (TMA-fed, fp32 accumulation in tensor memory).
 mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStream_t st);
 
+// k_block.cu: the MLP block (d = 512).
+mlp_status launch_block_fwd(const void* x, const void* wg, const void* wd, int T, int hidden,
+                            float eps, float slope, void* y, float* rstd, cudaStream_t st);
+mlp_status launch_block_bwd_act(const void* x, const void* wg, const void* wd, const void* dy,
+                                const float* rstd, int T, int hidden, float slope, void* a_out,
+                                void* du_out, cudaStream_t st);
+mlp_status launch_rmsnorm_bwd(const float* dnp, const void* x, const void* dy, const float* rstd,
+                              int T, void* dx, cudaStream_t st);
+
 // Host helpers (api.cu)
 unsigned long long wait_limit_ns();
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, unsigned long long inner,
