@@ -146,10 +146,9 @@ def algorithmic_work(name):
         return "tensor", 4.0 * T * d * h
     if base.startswith("block_bwd_act"):
         T, d, h = sh
-        return "tensor", 4.0 * T * d * h
-    if base.startswith("block_bwd_dx"):
-        T, d, h = sh
-        return "tensor", 2.0 * T * d * h
+        return "tensor", 2.0 * T * d * h      # dA = dY W_down^T; the u recompute is not credited
+    if base == "rmsnorm_bwd":
+        return "hbm", 5124.0 * sh[0]          # per token: dn' fp32 + x, dy, dx bf16 + rstd
     if base == "sgd":
         return "hbm", 22.0 * sh[0]        # read w, g, v; write w, v (fp32) + bf16 shadow
     if base == "cast":
@@ -301,9 +300,298 @@ class MLP784Epoch(Workload):
             steps, done)
 
 
+class WideMLP(Workload):
+    """1024-8192-8192-1000, batch 16,384, bf16 operands, fp32 master weights."""
+    name = "mlp_wide"
+    unit = "samples/s"
+    dtype = "bf16"
+
+    def __init__(self):
+        self.dims = [1024, 8192, 8192, 1000]
+        self.batch = 16384
+        self.samples_per_step = self.batch
+        self.config = {"workload": "1024-8192-8192-1000 MLP, ReLU, bf16 weights/activations, "
+                                   "fp32 master weights and accumulation, batch 16384, inputs "
+                                   "N(0,1), labels uniform 0..999, SGD momentum lr 0.01 m 0.9; "
+                                   "one full fwd + bwd + update step",
+                       "dims": self.dims, "batch": self.batch, "cuda_graph": True,
+                       "l2": "flushed between timed steps (256 MiB write); working set > L2"}
+
+    def setup(self):
+        import torch
+        import mlp_step_gb300 as M
+        from mlp_step_gb300 import synth
+        self.M = M
+        p0 = synth.mlp_flat_params(self.dims)
+        self.net = M.MLP(self.dims, prec=M.MLP_PREC_BF16, max_batch=self.batch,
+                         params=torch.from_numpy(p0))
+        X = synth.normal_f32((self.batch, self.dims[0]), synth.STREAM_X)
+        y = synth.labels(self.batch, self.dims[-1])
+        self.x_host = torch.from_numpy(X).to(torch.bfloat16).pin_memory()
+        self.y_host = torch.from_numpy(y).pin_memory()
+        self.x = self.x_host.cuda()
+        self.y = self.y_host.cuda()
+        self.loss = torch.zeros(4, device="cuda")
+        self.loss_host = torch.zeros(4).pin_memory()
+        self.h2d_bytes = self.x_host.numel() * 2 + self.y_host.numel() * 4
+        self.d2h_bytes = 4
+        self.step_eager()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        c0 = M.launch_count()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(self.graph, stream=s):
+                self.step_eager()
+        torch.cuda.current_stream().wait_stream(s)
+        self.launches_per_step = M.launch_count() - c0
+        torch.cuda.synchronize()
+
+    def step_eager(self):
+        self.net.train_step(self.x, self.y, 0.01, 0.9, loss_out=self.loss)
+
+    def step(self):
+        self.graph.replay()
+
+    def step_e2e(self):
+        self.x.copy_(self.x_host, non_blocking=True)
+        self.y.copy_(self.y_host, non_blocking=True)
+        self.graph.replay()
+        self.loss_host.copy_(self.loss, non_blocking=True)
+
+    def check(self):
+        import torch
+        torch.cuda.synchronize()
+        assert np.isfinite(self.loss[0].item()), "non-finite loss"
+        assert self.M.get_device_status() == self.M.MLP_OK
+
+    def oracle_sample(self, budget_s):
+        import oracle
+        from mlp_step_gb300 import synth
+        p = synth.mlp_flat_params(self.dims).astype(np.float64)
+        v = np.zeros_like(p)
+        rows = 4
+        X = synth.normal_f32((rows, self.dims[0]), synth.STREAM_X).astype(np.float64)
+        y = synth.labels(rows, self.dims[-1])
+        t0 = time.perf_counter()
+        done = 0
+        steps = 0
+        while True:
+            _, p, v, _ = oracle.mlp_train_step(self.dims, p, v, X, y, 0.01, 0.9)
+            done += rows
+            steps += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return done, dt, ("%d oracle training steps of batch %d (fp64; the full-batch step "
+                          "would take hours)" % (steps, rows))
+
+
+class BlockStep(Workload):
+    """One MLP block forward + backward over 65,536 tokens (d 512, hidden 1536)."""
+    name = "block"
+    unit = "tokens/s"
+    dtype = "bf16"
+
+    def __init__(self, T=65536):
+        self.T, self.d, self.h = T, 512, 1536
+        self.samples_per_step = T
+        self.config = {"workload": "transformer MLP block fwd+bwd: x[%d tokens, 512] bf16 "
+                                   "N(0,1), RMSNorm (eps 1e-6, gain 1) -> W_gate 512x1536 -> "
+                                   "LeakyReLU(0.5)^2 -> W_down 1536x512 -> residual, weights "
+                                   "N(0,0.02), upstream grad N(0,1); the 1536-wide "
+                                   "intermediate stays on chip in the forward" % T,
+                       "tokens": T, "d": 512, "hidden": 1536, "cuda_graph": True,
+                       "l2": "flushed between timed steps (256 MiB write)"}
+
+    def setup(self):
+        import torch
+        import mlp_step_gb300 as M
+        from mlp_step_gb300 import synth
+        self.M = M
+        T, d, h = self.T, self.d, self.h
+        bf = torch.bfloat16
+        self.x_host = torch.from_numpy(synth.normal_f32((T, d), synth.STREAM_BLOCK_X)).to(bf)
+        self.x_host = self.x_host.pin_memory()
+        self.dy_host = torch.from_numpy(synth.normal_f32((T, d), synth.STREAM_BLOCK_DY)).to(bf)
+        self.dy_host = self.dy_host.pin_memory()
+        self.x = self.x_host.cuda()
+        self.dy = self.dy_host.cuda()
+        self.wg = torch.from_numpy(synth.normal_f32((d, h), synth.STREAM_BLOCK_WG,
+                                                    std=0.02)).to(bf).cuda()
+        self.wd = torch.from_numpy(synth.normal_f32((h, d), synth.STREAM_BLOCK_WD,
+                                                    std=0.02)).to(bf).cuda()
+        self.y = torch.empty(T, d, dtype=bf, device="cuda")
+        self.r = torch.empty(T, device="cuda")
+        self.dx = torch.empty(T, d, dtype=bf, device="cuda")
+        self.dwg = torch.empty(d, h, device="cuda")
+        self.dwd = torch.empty(h, d, device="cuda")
+        self.ws = torch.empty(M.mlp_block_workspace_bytes(T, d, h), dtype=torch.uint8,
+                              device="cuda")
+        self.dx_host = torch.empty(4, dtype=bf).pin_memory()
+        self.h2d_bytes = 2 * T * d * 2
+        self.d2h_bytes = 8
+        self.step_eager()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        c0 = M.launch_count()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(self.graph, stream=s):
+                self.step_eager()
+        torch.cuda.current_stream().wait_stream(s)
+        self.launches_per_step = M.launch_count() - c0
+        torch.cuda.synchronize()
+
+    def step_eager(self):
+        M = self.M
+        M.mlp_block_fwd(self.x, self.wg, self.wd, self.y, self.r)
+        M.mlp_block_bwd(self.x, self.r, self.wg, self.wd, self.dy, self.dx, self.dwg, self.dwd,
+                        self.ws)
+
+    def step(self):
+        self.graph.replay()
+
+    def step_e2e(self):
+        self.x.copy_(self.x_host, non_blocking=True)
+        self.dy.copy_(self.dy_host, non_blocking=True)
+        self.graph.replay()
+        self.dx_host.copy_(self.dx[0, :4], non_blocking=True)
+
+    def check(self):
+        import torch
+        torch.cuda.synchronize()
+        assert torch.isfinite(self.dwg).all(), "non-finite gradient"
+        assert self.M.get_device_status() == self.M.MLP_OK
+
+    def oracle_sample(self, budget_s):
+        import oracle
+        from mlp_step_gb300 import synth
+        T = 64
+        x = synth.normal_f32((T, self.d), synth.STREAM_BLOCK_X).astype(np.float64)
+        dy = synth.normal_f32((T, self.d), synth.STREAM_BLOCK_DY).astype(np.float64)
+        wg = synth.normal_f32((self.d, self.h), synth.STREAM_BLOCK_WG, std=0.02)
+        wd = synth.normal_f32((self.h, self.d), synth.STREAM_BLOCK_WD, std=0.02)
+        t0 = time.perf_counter()
+        done = 0
+        n = 0
+        while True:
+            oracle.block_fwd(x, wg, wd, 1e-6, 0.5)
+            oracle.block_bwd(x, wg, wd, dy, 1e-6, 0.5)
+            done += T
+            n += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return done, dt, "%d oracle block fwd+bwd passes over %d tokens (fp64)" % (n, T)
+
+
+class StackStep(Workload):
+    """11 blocks over 262,144 tokens, MSE loss, full fwd + bwd + momentum SGD."""
+    name = "stack"
+    unit = "tokens/s"
+    dtype = "bf16"
+
+    def __init__(self, n_blocks=11, T=262144):
+        self.nb, self.T, self.d, self.h = n_blocks, T, 512, 1536
+        self.samples_per_step = T
+        self.config = {"workload": "stack of %d MLP blocks (d 512, hidden 1536, "
+                                   "LeakyReLU(0.5)^2, RMSNorm pre-norm, residual) over %d tokens "
+                                   "bf16, MSE loss vs N(0,1) targets, full fwd + bwd + "
+                                   "flat-buffer SGD-momentum step (lr 0.02, m 0.95)"
+                                   % (n_blocks, T),
+                       "blocks": n_blocks, "tokens": T, "d": 512, "hidden": 1536,
+                       "cuda_graph": True, "l2": "working set far above L2; flushed as well"}
+
+    def setup(self):
+        import torch
+        import mlp_step_gb300 as M
+        from mlp_step_gb300 import synth
+        self.M = M
+        nb, T, d, h = self.nb, self.T, self.d, self.h
+        bf = torch.bfloat16
+        self.x_host = torch.from_numpy(synth.normal_f32((T, d), synth.STREAM_BLOCK_X)).to(bf)
+        self.x_host = self.x_host.pin_memory()
+        self.t_host = torch.from_numpy(synth.normal_f32((T, d), synth.STREAM_TARGET)).to(bf)
+        self.t_host = self.t_host.pin_memory()
+        self.x = self.x_host.cuda()
+        self.t = self.t_host.cuda()
+        P = M.mlp_stack_param_count(nb, d, h)
+        self.params = torch.from_numpy(synth.normal_f32((P,), synth.STREAM_BLOCK_WG,
+                                                        std=0.02)).cuda()
+        self.vel = torch.zeros_like(self.params)
+        self.grads = torch.zeros_like(self.params)
+        self.shadow = self.params.to(bf)
+        self.ws = torch.empty(M.mlp_stack_workspace_bytes(nb, T, d, h), dtype=torch.uint8,
+                              device="cuda")
+        self.loss = torch.zeros(4, device="cuda")
+        self.loss_host = torch.zeros(4).pin_memory()
+        self.h2d_bytes = 2 * T * d * 2
+        self.d2h_bytes = 4
+        self.step_eager()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        c0 = M.launch_count()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(self.graph, stream=s):
+                self.step_eager()
+        torch.cuda.current_stream().wait_stream(s)
+        self.launches_per_step = M.launch_count() - c0
+        torch.cuda.synchronize()
+
+    def step_eager(self):
+        self.M.mlp_stack_train_step(self.nb, self.T, self.d, self.h, self.x, self.t, self.params,
+                                    self.vel, self.grads, self.shadow, 0.02, 0.95, self.loss,
+                                    self.ws)
+
+    def step(self):
+        self.graph.replay()
+
+    def step_e2e(self):
+        self.x.copy_(self.x_host, non_blocking=True)
+        self.t.copy_(self.t_host, non_blocking=True)
+        self.graph.replay()
+        self.loss_host.copy_(self.loss, non_blocking=True)
+
+    def check(self):
+        import torch
+        torch.cuda.synchronize()
+        assert np.isfinite(self.loss[0].item()), "non-finite loss"
+        assert self.M.get_device_status() == self.M.MLP_OK
+
+    def oracle_sample(self, budget_s):
+        import oracle
+        from mlp_step_gb300 import synth
+        T = 16
+        x = synth.normal_f32((T, self.d), synth.STREAM_BLOCK_X).astype(np.float64)
+        t = synth.normal_f32((T, self.d), synth.STREAM_TARGET).astype(np.float64)
+        P = self.nb * 2 * self.d * self.h
+        p = synth.normal_f32((P,), synth.STREAM_BLOCK_WG, std=0.02).astype(np.float64)
+        t0 = time.perf_counter()
+        done = 0
+        n = 0
+        while True:
+            _, g, _ = oracle.stack_fwd_bwd(x, p, self.nb, self.d, self.h, 1e-6, 0.5, t)
+            p, _ = oracle.sgd_momentum(p, g, np.zeros_like(p), 0.02, 0.95)
+            done += T
+            n += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return done, dt, ("%d oracle stack steps over %d tokens (%d blocks, fp64)"
+                          % (n, T, self.nb))
+
+
 WORKLOADS = {
     "mlp784_epoch": lambda: MLP784Epoch("bf16"),
     "mlp784_fp32": lambda: MLP784Epoch("fp32", n_images=128),
+    "mlp_wide": WideMLP,
+    "block": BlockStep,
+    "stack": StackStep,
 }
 
 

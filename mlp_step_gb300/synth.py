@@ -122,6 +122,14 @@ def mlp_flat_params(dims, seed: int = SEED) -> np.ndarray:
     return np.concatenate(parts)
 
 
+def uniform_f32(shape, stream: int, lo: float = -1.0, hi: float = 1.0,
+                seed: int = SEED) -> np.ndarray:
+    """float32 uniforms in [lo, hi) (cheaper than normals for very large tensors)."""
+    n = int(np.prod(shape))
+    u = uniform01(seed, stream, n)
+    return (lo + (hi - lo) * u).astype(np.float32).reshape(shape)
+
+
 def normal_f32(shape, stream: int, std: float = 1.0, seed: int = SEED) -> np.ndarray:
     n = int(np.prod(shape))
     return (normal(seed, stream, n) * std).astype(np.float32).reshape(shape)
