@@ -306,14 +306,15 @@ class WideMLP(Workload):
     unit = "samples/s"
     dtype = "bf16"
 
-    def __init__(self):
+    def __init__(self, batch=16384):
         self.dims = [1024, 8192, 8192, 1000]
-        self.batch = 16384
+        self.batch = batch
         self.samples_per_step = self.batch
         self.config = {"workload": "1024-8192-8192-1000 MLP, ReLU, bf16 weights/activations, "
                                    "fp32 master weights and accumulation, batch 16384, inputs "
                                    "N(0,1), labels uniform 0..999, SGD momentum lr 0.01 m 0.9; "
-                                   "one full fwd + bwd + update step",
+                                   "one full fwd + bwd + update step" + (
+                                       "" if batch == 16384 else " (batch %d)" % batch),
                        "dims": self.dims, "batch": self.batch, "cuda_graph": True,
                        "l2": "flushed between timed steps (256 MiB write); working set > L2"}
 
@@ -593,6 +594,8 @@ WORKLOADS = {
     "block": BlockStep,
     "stack": StackStep,
 }
+SIZED = {"block": lambda T: BlockStep(T=T), "stack": lambda T: StackStep(T=T),
+         "mlp_wide": lambda B: WideMLP(batch=B)}
 
 
 # ------------------------------------------------------------------ measurement
@@ -765,6 +768,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="tokens (block, stack) or batch (mlp_wide): smaller profiling cases")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -774,7 +779,10 @@ def main():
                "--nproc-per-node", str(args.gpus), "--master-addr", "127.0.0.1",
                "--master-port", "29517", os.path.abspath(__file__)] + sys.argv[1:]
         sys.exit(subprocess.call(cmd))
-    wl = WORKLOADS[args.workload]()
+    if args.tokens and args.workload in SIZED:
+        wl = SIZED[args.workload](args.tokens)
+    else:
+        wl = WORKLOADS[args.workload]()
     if args.impl == "reference":
         run_reference(args, wl)
     else:

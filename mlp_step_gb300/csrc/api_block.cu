@@ -14,7 +14,7 @@ bool block_shape_ok(int T, int d, int hidden) {
 }
 
 struct BlockWs {
-  size_t a, du, dn, total;
+  size_t a, du, dn, split, total;
 };
 
 BlockWs block_ws(int T, int d, int hidden) {
@@ -22,13 +22,19 @@ BlockWs block_ws(int T, int d, int hidden) {
   w.a = align256((size_t)T * hidden * 2);
   w.du = align256((size_t)T * hidden * 2);
   w.dn = align256((size_t)T * d * 4);
-  w.total = w.a + w.du + w.dn;
+  // split-K partial sums of the two weight-gradient GEMMs (K = T)
+  size_t s1 = gemm_tc_splitk_bytes(hidden, d, T), s2 = gemm_tc_splitk_bytes(d, hidden, T);
+  w.split = align256(s1 > s2 ? s1 : s2);
+  w.total = w.a + w.du + w.dn + w.split;
   return w;
 }
 
 mlp_status gemm(int M, int N, int K, const void* A, int lda, int a_trans, const void* B, int ldb,
-                int b_trans, void* C, int ldc, cudaStream_t st) {
+                int b_trans, void* C, int ldc, cudaStream_t st, void* ws = nullptr,
+                size_t ws_bytes = 0) {
   GemmArgs g{};
+  g.ws = ws;
+  g.ws_bytes = ws_bytes;
   g.M = M; g.N = N; g.K = K;
   g.A = A; g.lda = lda; g.a_trans = a_trans;
   g.B = B; g.ldb = ldb; g.b_trans = b_trans;
@@ -45,12 +51,13 @@ mlp_status block_bwd_impl(const void* x, const float* rstd, const void* wg, cons
   void* a_ws = base;
   void* du_ws = base + w.a;
   float* dn_ws = reinterpret_cast<float*>(base + w.a + w.du);
+  void* split_ws = base + w.a + w.du + w.dn;
   // a = f(u), r du, with u recomputed from x and rstd
   MLP_CHECK(launch_block_bwd_act(x, wg, wd, dy, rstd, T, hidden, slope, a_ws, du_ws, st));
   // dW_down = a^T dy   [hidden][d]
-  MLP_CHECK(gemm(hidden, d, T, a_ws, hidden, 1, dy, d, 0, dwd, d, st));
+  MLP_CHECK(gemm(hidden, d, T, a_ws, hidden, 1, dy, d, 0, dwd, d, st, split_ws, w.split));
   // dW_gate = x^T (r du) = n^T du   [d][hidden]
-  MLP_CHECK(gemm(d, hidden, T, x, d, 1, du_ws, hidden, 0, dwg, hidden, st));
+  MLP_CHECK(gemm(d, hidden, T, x, d, 1, du_ws, hidden, 0, dwg, hidden, st, split_ws, w.split));
   // dn' = (r du) W_gate^T   [T][d]
   MLP_CHECK(gemm(T, d, hidden, du_ws, hidden, 0, wg, hidden, 1, dn_ws, d, st));
   // dx = dy + dn' - r^2 x mean(dn' x)

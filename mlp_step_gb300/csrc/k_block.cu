@@ -36,10 +36,11 @@ constexpr int TM = 128;                 // tokens per tile
 constexpr int DM = 512;                 // model width
 constexpr int HC = 128;                 // hidden chunk
 constexpr int YH = 256;                 // output columns per CTA of the pair
-constexpr int F_STAGES = 4;
+constexpr int F_STAGES = 3;
+constexpr int F_SLOTS = 4;                // two activation slots per CTA of the pair
 constexpr int F_STAGE_BYTES = 32768;
 constexpr int F_SLOT_BYTES = TM * HC * 2;  // 32 KiB bf16 activation chunk
-constexpr int F_SMEM = 1024 + 2 * F_SLOT_BYTES + F_STAGES * F_STAGE_BYTES + 512;
+constexpr int F_SMEM = 1024 + F_SLOTS * F_SLOT_BYTES + F_STAGES * F_STAGE_BYTES + 2 * TM * 4 + 512;
 constexpr int kThreads = 192;
 
 __device__ __forceinline__ float lrelu_sq(float u, float slope) {
@@ -51,24 +52,6 @@ __device__ __forceinline__ float lrelu_sq_grad(float u, float slope) {
   return u > 0.f ? 2.f * u : 2.f * slope * slope * u;
 }
 
-// RMSNorm scale of one token row of x (bf16 [DM]).
-__device__ __forceinline__ float row_rstd(const __nv_bfloat16* xrow, float eps) {
-  float ss = 0.f;
-  const uint4* p = reinterpret_cast<const uint4*>(xrow);
-#pragma unroll 4
-  for (int q = 0; q < DM / 8; ++q) {
-    const uint4 v = __ldg(p + q);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(h[e]);
-      ss += f.x * f.x;
-      ss += f.y * f.y;
-    }
-  }
-  return 1.0f / sqrtf(ss / (float)DM + eps);
-}
-
 struct FwdParams {
   int T, hidden, tiles, n_own;
   float eps, slope;
@@ -78,6 +61,8 @@ struct FwdParams {
   unsigned long long wait_ns;
   int* err;
 };
+
+constexpr int F_THREADS = 320;  // 10 warps
 
 // MMA issue order of one tile for a CTA that owns n_own gate chunks:
 // G0, then groups (G_g, D_{2g-2}, D_{2g-1}) for g = 1 .. n_own-1, then the last
@@ -93,22 +78,70 @@ __device__ __forceinline__ int fwd_op(int i, int n_own) {
   return -(2 * (g - 1) + (r - 1)) - 1;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ float sumsq_bf16x8(const uint4& v) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(h[e]);
+    s += f.x * f.x;
+    s += f.y * f.y;
+  }
+  return s;
+}
+
+// RMSNorm scale of the 32 token rows [row0, row0 + 32) of a tile, computed by
+// one warp with coalesced loads (each row: lanes read 2 x 16 B); lane i
+// returns the scale of row row0 + i (0 for rows past T).
+__device__ __forceinline__ float warp_rows_rstd(const __nv_bfloat16* x, int row0, int T, float eps,
+                                                int lane) {
+  float mine = 0.f;
+#pragma unroll 1
+  for (int rr = 0; rr < 32; rr += 8) {
+    uint4 v[8][2];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int m = row0 + rr + q;
+      if (m < T) {
+        const uint4* p = reinterpret_cast<const uint4*>(x + (size_t)m * DM);
+        v[q][0] = __ldg(p + lane);
+        v[q][1] = __ldg(p + 32 + lane);
+      } else {
+        v[q][0] = make_uint4(0, 0, 0, 0);
+        v[q][1] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float ss = sumsq_bf16x8(v[q][0]) + sumsq_bf16x8(v[q][1]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == rr + q) mine = ss;
+    }
+  }
+  return row0 + lane < T ? 1.0f / sqrtf(mine / (float)DM + eps) : 0.f;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
     block_fwd_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmWg,
                      const __grid_constant__ CUtensorMap tmWd, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* slots = smem;                                   // 2 x 32 KiB activation chunks
-  uint8_t* stages = smem + 2 * F_SLOT_BYTES;               // F_STAGES x 32 KiB
-  uint64_t* full = reinterpret_cast<uint64_t*>(stages + F_STAGES * F_STAGE_BYTES);
+  // activation slots: chunk c lives in slot 2 * (c % 2) + (c / 2) % 2, i.e.
+  // each CTA of the pair owns two slots (its chunks alternate between them)
+  uint8_t* slots = smem;                                   // F_SLOTS x 32 KiB
+  uint8_t* stages = smem + F_SLOTS * F_SLOT_BYTES;         // F_STAGES x 32 KiB
+  float* rbuf = reinterpret_cast<float*>(stages + F_STAGES * F_STAGE_BYTES);  // [2][TM]
+  uint64_t* full = reinterpret_cast<uint64_t*>(rbuf + 2 * TM);
   uint64_t* empty = full + F_STAGES;
   uint64_t* ufull = empty + F_STAGES;    // [2] gate accumulator ready
   uint64_t* uempty = ufull + 2;          // [2] gate accumulator drained (128 arrivals)
-  uint64_t* afull = uempty + 2;          // [2] activation slot s written (128 arrivals)
-  uint64_t* aempty = afull + 2;          // [2] slot s consumed by both CTAs (2 arrivals)
-  uint64_t* yfull = aempty + 2;
+  uint64_t* afull = uempty + 2;          // [4] activation slot written (128 arrivals)
+  uint64_t* aempty = afull + F_SLOTS;    // [4] slot consumed by both CTAs (2 arrivals)
+  uint64_t* rready = aempty + F_SLOTS;   // [2] row scales of a tile in rbuf (128 arrivals)
+  uint64_t* yfull = rready + 2;
   uint64_t* yempty = yfull + 1;          // 128 arrivals
   uint64_t* done = yempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
@@ -129,8 +162,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ufull[b], 1);
       ptx::mbar_init(&uempty[b], 128);
-      ptx::mbar_init(&afull[b], 128);
-      ptx::mbar_init(&aempty[b], 2);
+      ptx::mbar_init(&rready[b], 128);
+    }
+    for (int s2 = 0; s2 < F_SLOTS; ++s2) {
+      ptx::mbar_init(&afull[s2], 128);
+      ptx::mbar_init(&aempty[s2], 2);
     }
     ptx::mbar_init(yfull, 1);
     ptx::mbar_init(yempty, 128);
@@ -195,7 +231,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t idesc_d = ptx::idesc_bf16_f32(TM, YH, 0, 1);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t ucount[2] = {0, 0}, acount[2] = {0, 0}, ycount = 0;
+      uint32_t ucount[2] = {0, 0}, acount[F_SLOTS] = {0, 0, 0, 0}, ycount = 0;
       bool ok = true;
       for (int t = cluster; t < p.tiles && ok && !*s_abort; t += n_clusters) {
         for (int i = 0; i < n_ops && ok; ++i) {
@@ -225,7 +261,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::mma_commit(&ufull[b]);
           } else {
             const int c = -op - 1;
-            const int s = c & 1;
+            const int s = 2 * (c & 1) + ((c >> 1) & 1);
             if (c == 0) {
               if (!ptx::mbar_wait_bounded(yempty, (ycount & 1) ^ 1, p.wait_ns, p.err,
                                           DEVERR_TIMEOUT_MMA)) { ok = false; break; }
@@ -251,8 +287,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
-            // slot s is reusable once both CTAs' MMAs that read it are done
-            ptx::mma_commit_multicast(&aempty[s], (uint16_t)(1u << s));
+            // slot s is reusable once both CTAs' MMAs that read it are done;
+            // its owner (CTA c % 2) waits for that
+            ptx::mma_commit_multicast(&aempty[s], (uint16_t)(1u << (c & 1)));
             if (c == 2 * p.n_own - 1) ptx::mma_commit(yfull);
           }
         }
@@ -261,35 +298,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mma_commit(done);
       ptx::mbar_wait_bounded(done, 0, p.wait_ns, p.err, DEVERR_TIMEOUT_TEARDOWN);
     }
-  } else {
-    // ---------------------------------------------------------------- epilogue warps
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- activation warps
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    uint32_t uc[2] = {0, 0}, ac = 0, yc = 0;
-    uint8_t* my_slot = slots + rank * F_SLOT_BYTES;
-    const uint32_t my_slot_addr = ptx::smem_u32(my_slot);
-    const uint32_t peer_slot_addr = ptx::mapa_shared(my_slot_addr, peer);
-    const uint32_t afull_peer = ptx::mapa_shared(ptx::smem_u32(&afull[rank]), peer);
+    uint32_t uc[2] = {0, 0}, ac[2] = {0, 0};
     bool ok = true;
-    for (int t = cluster; t < p.tiles && ok; t += n_clusters) {
+    int it = 0;
+    for (int t = cluster; t < p.tiles && ok; t += n_clusters, ++it) {
       if (*s_abort) break;
-      const int m = t * TM + row;
-      const bool valid = m < p.T;
-      float r = 0.f;
-      if (valid) {
-        r = row_rstd(p.x + (size_t)m * DM, p.eps);
-        if (rank == 0 && p.rstd) p.rstd[m] = r;
-      }
-      // activation chunks this CTA owns
+      if (!ptx::mbar_wait_bounded(&rready[it & 1], (it >> 1) & 1, p.wait_ns, p.err,
+                                  DEVERR_TIMEOUT_EPILOGUE)) { ok = false; break; }
+      const float r = rbuf[(it & 1) * TM + row];
       for (int j = 0; j < p.n_own && ok; ++j) {
         const int b = j & 1;
         if (!ptx::mbar_wait_bounded(&ufull[b], uc[b] & 1, p.wait_ns, p.err,
                                     DEVERR_TIMEOUT_EPILOGUE)) { ok = false; break; }
         ++uc[b];
-        if (!ptx::mbar_wait_bounded(&aempty[rank], (ac & 1) ^ 1, p.wait_ns, p.err,
+        // own chunk c = 2 j + rank goes to slot 2 rank + (j % 2)
+        const int sub = j & 1;
+        const int sl = 2 * (int)rank + sub;
+        if (!ptx::mbar_wait_bounded(&aempty[sl], (ac[sub] & 1) ^ 1, p.wait_ns, p.err,
                                     DEVERR_TIMEOUT_EPILOGUE)) { ok = false; break; }
-        ++ac;
+        ++ac[sub];
+        const uint32_t my_slot_addr = ptx::smem_u32(slots + sl * F_SLOT_BYTES);
+        const uint32_t peer_slot_addr = ptx::mapa_shared(my_slot_addr, peer);
         ptx::tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < HC / 32; ++cc) {
@@ -321,31 +355,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         ptx::mbar_arrive(&uempty[b]);
         ptx::fence_proxy_async_cluster();
-        ptx::mbar_arrive(&afull[rank]);
-        ptx::mbar_arrive_remote(afull_peer);
+        ptx::mbar_arrive(&afull[sl]);
+        ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(&afull[sl]), peer));
       }
-      if (!ok) break;
-      // output half: y = x + acc
+    }
+    if (!ok) *s_abort = 1;
+  } else {
+    // ---------------------------------------------------------------- output warps
+    // Row scales for the next tile are computed one tile ahead.  The residual
+    // half-row of x streams through a ring of four 32-column chunks in
+    // registers, the first four in flight while the tile's MMAs run.  (Ten
+    // warps put three on some SM sub-partitions, which caps a thread at 168
+    // registers, so the whole half-row cannot be held at once.)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    uint4 xq[4][4];
+    uint32_t yc = 0;
+    bool ok = true;
+    int it = 0;
+    auto publish_rstd = [&](int tile, int buf) {
+      const float r = warp_rows_rstd(p.x, tile * TM + quarter * 32, p.T, p.eps, lane);
+      rbuf[buf * TM + row] = r;
+      const int m = tile * TM + row;
+      if (rank == 0 && p.rstd && m < p.T) p.rstd[m] = r;
+      ptx::mbar_arrive(&rready[buf]);
+    };
+    if (cluster < p.tiles) publish_rstd(cluster, 0);
+    for (int t = cluster; t < p.tiles && ok; t += n_clusters, ++it) {
+      if (*s_abort) break;
+      const int tn = t + n_clusters;
+      if (tn < p.tiles) publish_rstd(tn, (it + 1) & 1);
+      const int m = t * TM + row;
+      const bool valid = m < p.T;
+      const uint4* xsrc = reinterpret_cast<const uint4*>(p.x + (size_t)m * DM + rank * YH);
+      if (valid) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) xq[c][q] = __ldg(xsrc + c * 4 + q);
+      }
       if (!ptx::mbar_wait_bounded(yfull, yc & 1, p.wait_ns, p.err, DEVERR_TIMEOUT_EPILOGUE)) {
         ok = false;
         break;
       }
       ++yc;
       ptx::tc_fence_after();
-#pragma unroll 1
+      uint4* yr = reinterpret_cast<uint4*>(p.y + (size_t)m * DM + rank * YH);
+#pragma unroll
       for (int cc = 0; cc < YH / 32; ++cc) {
         uint32_t v[32];
         __syncwarp();
         ptx::tmem_ld_32x32b_x32(tmem + lane_off + cc * 32, v);
         ptx::tmem_ld_wait();
         if (valid) {
-          const int n0 = (int)rank * YH + cc * 32;
-          const uint4* xr = reinterpret_cast<const uint4*>(p.x + (size_t)m * DM + n0);
-          uint4* yr = reinterpret_cast<uint4*>(p.y + (size_t)m * DM + n0);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint4 xv = __ldg(xr + q);
-            const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xv);
+            const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xq[cc & 3][q]);
             uint4 o;
             uint32_t* op = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
@@ -354,7 +420,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               op[e] = pack_bf16x2(__uint_as_float(v[q * 8 + 2 * e]) + xf.x,
                                   __uint_as_float(v[q * 8 + 2 * e + 1]) + xf.y);
             }
-            yr[q] = o;
+            yr[cc * 4 + q] = o;
+          }
+          if (cc + 4 < YH / 32) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xq[cc & 3][q] = __ldg(xsrc + (cc + 4) * 4 + q);
           }
         }
       }
@@ -682,7 +752,7 @@ mlp_status launch_block_fwd(const void* x, const void* wg, const void* wd, int T
   if (clusters > p.tiles) clusters = p.tiles;
   if (clusters < 1) clusters = 1;
   LaunchScope ls("block_fwd", st, T, DM, hidden);
-  block_fwd_kernel<<<2 * clusters, kThreads, F_SMEM, st>>>(tx, tg, td, p);
+  block_fwd_kernel<<<2 * clusters, F_THREADS, F_SMEM, st>>>(tx, tg, td, p);
   return launch_status();
 }
 

@@ -213,6 +213,105 @@ __device__ __forceinline__ float xent_row(const float* __restrict__ z, int label
   return loss;
 }
 
+// Rows of up to 1024 classes whose logits start on 16-byte boundaries: the
+// warp reads the row once (float4 per lane per 128-class segment), keeps the
+// values and their exponentials in registers, and writes dZ from them.
+template <int NSEG>
+__device__ __forceinline__ float xent_row_regs(const float* __restrict__ z, int label, int C,
+                                               float inv_norm, void* dlog_row, int dl_bf16,
+                                               int ldd, int* argmax_out, int lane) {
+  label = label < 0 ? 0 : (label >= C ? C - 1 : label);
+  float v[NSEG][4];
+  MaxIdx best{-INFINITY, 0x7fffffff};
+#pragma unroll
+  for (int g = 0; g < NSEG; ++g) {
+    const int c0 = g * 128 + lane * 4;
+    if (c0 + 3 < C) {
+      const float4 q = __ldcs(reinterpret_cast<const float4*>(z + c0));
+      v[g][0] = q.x; v[g][1] = q.y; v[g][2] = q.z; v[g][3] = q.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[g][e] = c0 + e < C ? z[c0 + e] : -INFINITY;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (v[g][e] > best.v || (v[g][e] == best.v && c0 + e < best.i)) {
+        best.v = v[g][e];
+        best.i = c0 + e;
+      }
+  }
+  best = warp_argmax(best);
+  const float m = best.v;
+  float s = 0.f;
+#pragma unroll
+  for (int g = 0; g < NSEG; ++g)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = g * 128 + lane * 4 + e;
+      v[g][e] = c < C ? expf(v[g][e] - m) : 0.f;
+      s += v[g][e];
+    }
+  s = warp_sum(s);
+  const float loss = m + logf(s) - z[label];
+  if (dlog_row) {
+#pragma unroll
+    for (int g = 0; g < NSEG; ++g) {
+      const int c0 = g * 128 + lane * 4;
+      float d[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        d[e] = c0 + e < C ? (v[g][e] / s - (c0 + e == label ? 1.f : 0.f)) * inv_norm : 0.f;
+      if (c0 + 3 < ldd) {
+        if (dl_bf16) {
+          uint2 o;
+          o.x = pack_bf16x2(d[0], d[1]);
+          o.y = pack_bf16x2(d[2], d[3]);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dlog_row) + c0) = o;
+        } else {
+          *reinterpret_cast<float4*>(static_cast<float*>(dlog_row) + c0) =
+              make_float4(d[0], d[1], d[2], d[3]);
+        }
+      } else {
+        for (int e = 0; e < 4 && c0 + e < ldd; ++e) {
+          if (dl_bf16) static_cast<__nv_bfloat16*>(dlog_row)[c0 + e] = f32_to_bf16(d[e]);
+          else static_cast<float*>(dlog_row)[c0 + e] = d[e];
+        }
+      }
+    }
+    // padding columns beyond the last 128-class segment
+    for (int c = NSEG * 128 + lane; c < ldd; c += 32) {
+      if (dl_bf16) static_cast<__nv_bfloat16*>(dlog_row)[c] = f32_to_bf16(0.f);
+      else static_cast<float*>(dlog_row)[c] = 0.f;
+    }
+  }
+  if (argmax_out && lane == 0) *argmax_out = best.i;
+  return loss;
+}
+
+template <int NSEG>
+__global__ void __launch_bounds__(256) xent_rows_regs_kernel(
+    const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
+    float* __restrict__ partial, void* dlog, int dl_bf16, int ldd, int* argmax) {
+  __shared__ float part[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + warp;
+  float li = 0.f;
+  if (r < B) {
+    void* drow = nullptr;
+    if (dlog) drow = dl_bf16 ? (void*)(static_cast<__nv_bfloat16*>(dlog) + (size_t)r * ldd)
+                             : (void*)(static_cast<float*>(dlog) + (size_t)r * ldd);
+    li = xent_row_regs<NSEG>(logits + (size_t)r * ldl, labels[r], C, 1.0f / (float)B, drow,
+                             dl_bf16, ldd, argmax ? argmax + r : nullptr, lane);
+  }
+  if (lane == 0) part[warp] = li;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < 8; ++w) t += part[w];
+    partial[blockIdx.x] = t;
+  }
+}
+
 // Small batches: one block, 8 warps striding over the rows; the block also
 // forms the mean (warp w sums its rows in order, then warp sums in order).
 __global__ void __launch_bounds__(256) xent_single_block_kernel(
@@ -296,10 +395,19 @@ mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, i
   }
   const int blocks = (B + 7) / 8;
   float* partial = static_cast<float*>(ws);
+  const bool vec = C <= 1024 && (ldl % 4) == 0 && aligned16(logits) &&
+                   (!dlog || ((ldd % 4) == 0 && aligned16(dlog)));
   {
   LaunchScope ls("xent", st, B, C);
-  xent_rows_kernel<<<blocks, 256, 0, st>>>(logits, ldl, labels, B, C, partial, dlog, dl_bf16,
-                                           ldd, argmax);
+  if (vec && C <= 256)
+    xent_rows_regs_kernel<2><<<blocks, 256, 0, st>>>(logits, ldl, labels, B, C, partial, dlog,
+                                                     dl_bf16, ldd, argmax);
+  else if (vec)
+    xent_rows_regs_kernel<8><<<blocks, 256, 0, st>>>(logits, ldl, labels, B, C, partial, dlog,
+                                                     dl_bf16, ldd, argmax);
+  else
+    xent_rows_kernel<<<blocks, 256, 0, st>>>(logits, ldl, labels, B, C, partial, dlog, dl_bf16,
+                                             ldd, argmax);
   }
   MLP_CHECK(launch_status());
   if (loss_out) {
@@ -322,7 +430,7 @@ mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, i
 template <typename T>
 __device__ __forceinline__ float ldf(const T* p);
 template <>
-__device__ __forceinline__ float ldf<float>(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float ldf<float>(const float* p) { return *p; }
 template <>
 __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p) {
   return bf16_to_f32(*p);
@@ -354,6 +462,56 @@ __global__ void __launch_bounds__(256) colsum_pass1_kernel(const T* __restrict__
         for (int k = 0; k < 8; ++k) t += s[k][2 * tx + e];
         dst[(size_t)blockIdx.y * cols + cc] = t;
       }
+    }
+  }
+}
+
+// Vector form: each lane reads 16 bytes of a row (8 bf16 or 4 fp32 columns),
+// a warp covers 512 contiguous bytes, 8 warps stride over the rows of the
+// chunk (4 rows in flight per lane), then the warps' sums are added in order.
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_vec_kernel(const T* __restrict__ X, int rows,
+                                                         int cols, int ld, int rows_per_chunk,
+                                                         float* __restrict__ dst) {
+  constexpr int V = 16 / sizeof(T);          // columns per lane
+  constexpr int BC = 32 * V;                 // columns per block
+  __shared__ float s[8][BC + 1];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c0 = blockIdx.x * BC + lane * V;
+  const int r0 = blockIdx.y * rows_per_chunk;
+  const int r1 = min(rows, r0 + rows_per_chunk);
+  float acc[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) acc[e] = 0.f;
+  if (c0 < cols) {
+    int r = r0 + w;
+    for (; r + 24 < r1; r += 32) {
+      uint4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q[u] = __ldcs(reinterpret_cast<const uint4*>(X + (size_t)(r + 8 * u) * ld + c0));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const T* t = reinterpret_cast<const T*>(&q[u]);
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] += ldf(t + e);
+      }
+    }
+    for (; r < r1; r += 8) {
+      const uint4 q = __ldcs(reinterpret_cast<const uint4*>(X + (size_t)r * ld + c0));
+      const T* t = reinterpret_cast<const T*>(&q);
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] += ldf(t + e);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < V; ++e) s[w][lane * V + e] = acc[e];
+  __syncthreads();
+  for (int c = threadIdx.x; c < BC; c += 256) {
+    const int cc = blockIdx.x * BC + c;
+    if (cc < cols) {
+      float t = 0.f;
+      for (int k = 0; k < 8; ++k) t += s[k][c];
+      dst[(size_t)blockIdx.y * cols + cc] = t;
     }
   }
 }
@@ -393,7 +551,19 @@ mlp_status launch_colsum(const void* X, int bf16, int rows, int cols, int ld, fl
   colsum_plan(rows, cols, &ch, &rpc);
   dim3 grid((cols + 63) / 64, ch);
   float* dst = ch > 1 ? static_cast<float*>(ws) : out;
-  {
+  const bool vec = aligned16(X) && (bf16 ? (cols % 8 == 0 && ld % 8 == 0)
+                                         : (cols % 4 == 0 && ld % 4 == 0));
+  if (vec) {
+    LaunchScope ls("colsum", st, rows, cols);
+    const int bc = bf16 ? 256 : 128;
+    dim3 g((cols + bc - 1) / bc, ch);
+    if (bf16)
+      colsum_vec_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(X),
+                                                         rows, cols, ld, rpc, dst);
+    else
+      colsum_vec_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(X), rows, cols, ld,
+                                                  rpc, dst);
+  } else {
   LaunchScope ls("colsum", st, rows, cols);
   if (bf16)
     colsum_pass1_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(

@@ -47,6 +47,10 @@ struct TcParams {
   int c_bf16;
   unsigned long long wait_ns;
   int* err;
+  // split-K: each work unit covers k-blocks [s*kb_per_split, (s+1)*kb_per_split)
+  // of one tile and stores raw fp32 sums into partial[s][M][ldp]
+  int splits, kb_per_split, ldp;
+  float* partial;
 };
 
 template <int BN, int STAGES>
@@ -186,10 +190,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < STAGES; ++s) last_parity[s] = -1;
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < p.num_tiles && !*s_abort; t += gridDim.x) {
+      for (int u = blockIdx.x; u < p.num_tiles * p.splits && !*s_abort; u += gridDim.x) {
         int tm, tn;
-        tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        tile_coords(u / p.splits, p.tiles_m, p.tiles_n, tm, tn);
+        const int kb0 = (u % p.splits) * p.kb_per_split;
+        const int kb1 = min(p.k_blocks, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
                                       DEVERR_TIMEOUT_PRODUCER)) {
             *s_abort = 1;
@@ -228,15 +234,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int t = blockIdx.x; t < p.num_tiles && !*s_abort; t += gridDim.x) {
+      for (int u = blockIdx.x; u < p.num_tiles * p.splits && !*s_abort; u += gridDim.x) {
         if (!ptx::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err, DEVERR_TIMEOUT_MMA)) {
           *s_abort = 1;
           break;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        const int kb0 = (u % p.splits) * p.kb_per_split;
+        const int kb1 = min(p.k_blocks, kb0 + p.kb_per_split);
         bool ok = true;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err, DEVERR_TIMEOUT_MMA)) {
             *s_abort = 1;
             ok = false;
@@ -249,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = ptx::sw128_desc(a_base + k * a_kstep, a_lbo, 1024);
             const uint64_t bd = ptx::sw128_desc(b_base + k * b_kstep, b_lbo, 1024);
-            ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           ptx::mma_commit(&empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -267,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    for (int u = blockIdx.x; u < p.num_tiles * p.splits; u += gridDim.x) {
       if (*s_abort) break;
       if (!ptx::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err, DEVERR_TIMEOUT_EPILOGUE)) {
         *s_abort = 1;
@@ -275,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_after();
       int tm, tn;
-      tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
+      tile_coords(u / p.splits, p.tiles_m, p.tiles_n, tm, tn);
+      float* part = p.splits > 1 ? p.partial + (size_t)(u % p.splits) * p.M * p.ldp : nullptr;
       const int m = tm * BM + row;
       for (int c0 = 0; c0 < BN; c0 += 32) {
         const int n0 = tn * BN + c0;
@@ -286,7 +295,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (uint32_t)(acc * BN + c0),
                                 r);
         ptx::tmem_ld_wait();
-        if (m < p.M) epilogue_chunk<BN>(p, m, n0, r);
+        if (m < p.M) {
+          if (part) {
+            float* prow = part + (size_t)m * p.ldp + n0;
+            if (n0 + 32 <= p.N) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(prow)[q] =
+                    make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            } else {
+              for (int j = 0; j < 32 && n0 + j < p.N; ++j) prow[j] = __uint_as_float(r[j]);
+            }
+          } else {
+            epilogue_chunk<BN>(p, m, n0, r);
+          }
+        }
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -314,6 +338,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Split-K finish: out = epilogue(sum_s partial[s]) in a fixed order, four
+// consecutive columns per thread.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const TcParams p) {
+  const long long quads = (long long)p.M * (p.ldp / 4);
+  const size_t plane = (size_t)p.M * p.ldp;
+  for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < quads;
+       q += (long long)gridDim.x * blockDim.x) {
+    const int m = (int)(q / (p.ldp / 4));
+    const int n0 = (int)(q % (p.ldp / 4)) * 4;
+    if (n0 >= p.N) continue;
+    float4 acc = __ldcs(reinterpret_cast<const float4*>(p.partial + (size_t)m * p.ldp + n0));
+    for (int s = 1; s < p.splits; ++s) {
+      const float4 v =
+          __ldcs(reinterpret_cast<const float4*>(p.partial + s * plane + (size_t)m * p.ldp + n0));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    float v[4] = {acc.x, acc.y, acc.z, acc.w};
+    for (int j = 0; j < 4 && n0 + j < p.N; ++j) {
+      const int n = n0 + j;
+      float o = v[j];
+      if (p.bias) o += p.bias[n];
+      if (p.act == MLP_ACT_RELU) o = fmaxf(o, 0.f);
+      if (p.mask) o = bf16_to_f32(p.mask[(size_t)m * p.ldm + n]) > 0.f ? o : 0.f;
+      if (p.c_bf16) static_cast<__nv_bfloat16*>(p.C)[(size_t)m * p.ldc + n] = f32_to_bf16(o);
+      else static_cast<float*>(p.C)[(size_t)m * p.ldc + n] = o;
+    }
+  }
+}
+
 template <int BN, int STAGES>
 mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
                      cudaStream_t st) {
@@ -325,28 +378,74 @@ mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const TcParam
       return MLP_ERR_CUDA;
     configured = true;
   }
-  int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  static const char* names[3] = {"gemm_tc_bn64", "gemm_tc_bn128", "gemm_tc_bn256"};
-  LaunchScope ls(names[BN == 64 ? 0 : (BN == 128 ? 1 : 2)], st, p.M, p.N, p.K);
-  tc_gemm_kernel<BN, STAGES><<<grid, kThreads, L::SMEM, st>>>(ta, tb, p);
-  return launch_status();
+  const int units = p.num_tiles * p.splits;
+  int grid = units < num_sms() ? units : num_sms();
+  {
+    static const char* names[3] = {"gemm_tc_bn64", "gemm_tc_bn128", "gemm_tc_bn256"};
+    static const char* split_names[3] = {"gemm_tc_splitk_bn64", "gemm_tc_splitk_bn128",
+                                         "gemm_tc_splitk_bn256"};
+    const int which = BN == 64 ? 0 : (BN == 128 ? 1 : 2);
+    LaunchScope ls(p.splits > 1 ? split_names[which] : names[which], st, p.M, p.N, p.K);
+    tc_gemm_kernel<BN, STAGES><<<grid, kThreads, L::SMEM, st>>>(ta, tb, p);
+  }
+  MLP_CHECK(launch_status());
+  if (p.splits > 1) {
+    const long long quads = (long long)p.M * (p.ldp / 4);
+    long long blocks = (quads + 255) / 256;
+    if (blocks > (long long)num_sms() * 8) blocks = (long long)num_sms() * 8;
+    LaunchScope ls("splitk_reduce", st, p.M, p.N, p.splits);
+    splitk_reduce_kernel<<<(int)blocks, 256, 0, st>>>(p);
+    return launch_status();
+  }
+  return MLP_OK;
+}
+
+// Split-K plan from the shape alone (so workspace sizes do not depend on the
+// device): only when 128x256 tiles leave most of ~144 SMs idle and K is long.
+void splitk_plan(int M, int N, int K, int* splits, int* kb_per_split) {
+  const int tiles = ((M + BM - 1) / BM) * ((N + 255) / 256);
+  const int kblocks = (K + BK - 1) / BK;
+  int s = 1;
+  if (tiles < 72 && kblocks >= 64) {
+    s = 144 / tiles;
+    if (s > 16) s = 16;
+    if (s > kblocks / 16) s = kblocks / 16;
+    if (s < 1) s = 1;
+  }
+  int per = (kblocks + s - 1) / s;
+  s = (kblocks + per - 1) / per;
+  *splits = s;
+  *kb_per_split = per;
 }
 
 }  // namespace
 
+size_t gemm_tc_splitk_bytes(int M, int N, int K) {
+  int s, per;
+  splitk_plan(M, N, K, &s, &per);
+  if (s <= 1) return 0;
+  return (size_t)s * M * ((N + 3) / 4 * 4) * sizeof(float);
+}
+
 mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0) return MLP_OK;
   if (g.K <= 0) return launch_gemm_simt(g, 1, st);
+
+  int splits = 1, kb_per_split = (g.K + BK - 1) / BK;
+  const size_t split_bytes = gemm_tc_splitk_bytes(g.M, g.N, g.K);
+  if (split_bytes > 0 && g.ws && g.ws_bytes >= split_bytes && aligned16(g.ws))
+    splitk_plan(g.M, g.N, g.K, &splits, &kb_per_split);
 
   const int tiles_m = (g.M + BM - 1) / BM;
   // Widest tile that still gives every SM work; narrower tiles for small N.
   int BN = 256;
   const int sms = num_sms();
   auto tiles_for = [&](int bn) { return tiles_m * ((g.N + bn - 1) / bn); };
-  if (g.N <= 64) BN = 64;
+  if (splits > 1) BN = 256;
+  else if (g.N <= 64) BN = 64;
   else if (g.N <= 128) BN = 128;
   else if (tiles_for(256) < sms) BN = tiles_for(128) < sms ? 64 : 128;
-  if (BN == 128 && tiles_for(128) < sms / 2 && g.N > 64) BN = 64;
+  if (splits == 1 && BN == 128 && tiles_for(128) < sms / 2 && g.N > 64) BN = 64;
 
   TcParams p;
   p.M = g.M; p.N = g.N; p.K = g.K;
@@ -364,6 +463,10 @@ mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStr
   p.ldc = g.ldc;
   p.c_bf16 = g.c_bf16;
   p.wait_ns = wait_ns;
+  p.splits = splits;
+  p.kb_per_split = kb_per_split;
+  p.ldp = (g.N + 3) / 4 * 4;
+  p.partial = splits > 1 ? static_cast<float*>(g.ws) : nullptr;
   p.err = device_error_word();
   if (!p.err) return MLP_ERR_CUDA;
 

@@ -47,11 +47,16 @@ struct GemmArgs {
   const float* bias; int act;
   const void* mask; int ldm;
   void* C; int ldc; int c_bf16;
+  // optional scratch for split-K partial sums (tensor-core path only)
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
 };
 mlp_status launch_gemm_simt(const GemmArgs& g, int in_bf16, cudaStream_t st);
 
 // k_gemm_tc.cu: tcgen05 bf16 GEMM (TMA-fed, fp32 accumulation in tensor memory).
 mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStream_t st);
+// Scratch bytes a split-K launch of this shape would use (0: no split).
+size_t gemm_tc_splitk_bytes(int M, int N, int K);
 
 // k_block.cu: the MLP block (d = 512).
 mlp_status launch_block_fwd(const void* x, const void* wg, const void* wd, int T, int hidden,
