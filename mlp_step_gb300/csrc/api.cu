@@ -256,20 +256,23 @@ struct mlp_handle {
   long long n_params = 0;
   std::vector<long long> w_off, b_off, shadow_off;
   std::vector<int> out_pad;        // shadow row pitch per layer
-  std::vector<int> act_ld;         // leading dimension of H_l buffers (l = 0 is the input)
+  // Layer inputs (X and every hidden activation) are stored with one extra
+  // column of ones after the features (ld = round8(width + 1)): the
+  // weight-gradient GEMM over [In | 1] then yields [dW; db], which is exactly
+  // the flat layout of W followed by b.
+  std::vector<int> act_ld;         // act_ld[l]: pitch of layer l's input buffer
   void* x_copy = nullptr;          // [max_batch][act_ld[0]]
   std::vector<void*> acts;         // acts[l] = H_{l+1}, l = 0..L-2
   float* logits = nullptr;         // [max_batch][C]
   void* dlogits = nullptr;         // [max_batch][ldz]
   int ldz = 0;
   void* dh[2] = {nullptr, nullptr};
-  int dh_ld = 0;
   float* loss = nullptr;
   void* red = nullptr;             // reduction partials
   size_t red_bytes = 0;
   SgdSegments segs{};
-  const void* x_used = nullptr;    // operand the last forward read as X
-  int x_ld = 0;
+  bool ones_ready = false;
+  bool have_forward = false;
 };
 
 namespace {
@@ -292,26 +295,165 @@ Plan plan(const int* dims, int n_dims, int max_batch, int prec) {
   const int L = n_dims - 1;
   const size_t B = (size_t)max_batch;
   const int e = esz(prec);
-  p.x = align256(B * round8(dims[0]) * e);
+  p.x = align256(B * round8(dims[0] + 1) * e);
   p.acts_total = 0;
   int maxh = 8;
   for (int l = 1; l < L; ++l) {
-    p.acts_total += align256(B * round8(dims[l]) * e);
-    if (round8(dims[l]) > maxh) maxh = round8(dims[l]);
+    p.acts_total += align256(B * round8(dims[l] + 1) * e);
+    if (round8(dims[l] + 1) > maxh) maxh = round8(dims[l] + 1);
   }
-  if (round8(dims[0]) > maxh) maxh = round8(dims[0]);
+  if (round8(dims[0] + 1) > maxh) maxh = round8(dims[0] + 1);
   p.logits = align256(B * dims[L] * sizeof(float));
   p.dlogits = align256(B * round8(dims[L]) * e);
   p.dh = align256(B * maxh * e);
   p.loss = 256;
   size_t red = xent_workspace_bytes(max_batch);
-  for (int l = 0; l < L; ++l) {
-    const size_t c = colsum_workspace_bytes(max_batch, dims[l + 1]);
-    if (c > red) red = c;
-  }
   p.red = align256(red > 0 ? red : 256);
   p.total = p.x + p.acts_total + p.logits + p.dlogits + 2 * p.dh + p.loss + p.red;
   return p;
+}
+
+// ones columns of every layer input buffer, for all max_batch rows (once per
+// handle: the forward GEMMs never write them)
+mlp_status ensure_ones(mlp_handle* h, cudaStream_t st) {
+  if (h->ones_ready) return MLP_OK;
+  OnesCols oc{};
+  oc.n = h->L;
+  oc.ptr[0] = h->x_copy;
+  oc.ld[0] = h->act_ld[0];
+  oc.col[0] = h->dims[0];
+  for (int l = 1; l < h->L; ++l) {
+    oc.ptr[l] = h->acts[l - 1];
+    oc.ld[l] = h->act_ld[l];
+    oc.col[l] = h->dims[l];
+  }
+  MLP_CHECK(launch_ones_cols(oc, h->max_batch, h->prec == MLP_PREC_BF16, st));
+  h->ones_ready = true;
+  return MLP_OK;
+}
+
+// Hidden layers 0 .. L-2 of the forward (bias + activation in the epilogue).
+mlp_status forward_hidden(mlp_handle* h, int batch, cudaStream_t st) {
+  const bool bf = h->prec == MLP_PREC_BF16;
+  for (int l = 0; l + 1 < h->L; ++l) {
+    GemmArgs g{};
+    g.M = batch;
+    g.N = h->dims[l + 1];
+    g.K = h->dims[l];
+    g.A = l == 0 ? h->x_copy : h->acts[l - 1];
+    g.lda = h->act_ld[l];
+    g.a_trans = 0;
+    if (bf) {
+      g.B = h->shadow + h->shadow_off[l];
+      g.ldb = h->out_pad[l];
+    } else {
+      g.B = h->params + h->w_off[l];
+      g.ldb = h->dims[l + 1];
+    }
+    g.b_trans = 0;
+    g.bias = h->params + h->b_off[l];
+    g.act = h->act;
+    g.C = h->acts[l];
+    g.ldc = h->act_ld[l + 1];
+    g.c_bf16 = bf ? 1 : 0;
+    MLP_CHECK(run_gemm(g, bf, st));
+  }
+  return MLP_OK;
+}
+
+// The output layer's GEMM operands (logits = In W_L + b_L).
+GemmArgs logits_gemm(mlp_handle* h, int batch, float* logits) {
+  const bool bf = h->prec == MLP_PREC_BF16;
+  const int l = h->L - 1;
+  GemmArgs g{};
+  g.M = batch;
+  g.N = h->dims[l + 1];
+  g.K = h->dims[l];
+  g.A = l == 0 ? h->x_copy : h->acts[l - 1];
+  g.lda = h->act_ld[l];
+  if (bf) {
+    g.B = h->shadow + h->shadow_off[l];
+    g.ldb = h->out_pad[l];
+  } else {
+    g.B = h->params + h->w_off[l];
+    g.ldb = h->dims[l + 1];
+  }
+  g.bias = h->params + h->b_off[l];
+  g.act = MLP_ACT_NONE;
+  g.C = logits;
+  g.ldc = h->dims[l + 1];
+  g.c_bf16 = 0;
+  return g;
+}
+
+mlp_status load_input(mlp_handle* h, const void* x, int x_dtype, int batch, cudaStream_t st) {
+  MLP_CHECK(ensure_ones(h, st));
+  // X goes into the workspace copy with the ones column, in the path's type
+  const bool bf = h->prec == MLP_PREC_BF16;
+  const int d0 = h->dims[0];
+  // rows of d0 values into rows of pitch act_ld[0]
+  return launch_cast_rows(x, x_dtype, h->x_copy, bf ? 1 : 0, batch, d0, h->act_ld[0], st);
+}
+
+// Backward from dY = dlogits.  With fuse_sgd, each layer's weight-gradient
+// GEMM also applies momentum SGD to that layer's weights and bias (after the
+// layer's input gradient has read the old weights).
+mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int batch, void* dx,
+                         bool fuse_sgd, float lr, float mom, cudaStream_t st) {
+  const bool bf = h->prec == MLP_PREC_BF16;
+  const void* dY = dlogits;
+  int ld_dy = ld_dlogits;
+  for (int l = h->L - 1; l >= 0; --l) {
+    const int fi = h->dims[l], fo = h->dims[l + 1];
+    const void* in = l == 0 ? h->x_copy : h->acts[l - 1];
+    const int ld_in = h->act_ld[l];
+    // dIn = (dY W_l^T) * (H_l > 0)   (B = W_l read transposed); reads the
+    // layer's weights before any update
+    GemmArgs gd{};
+    const bool want_din = l > 0 || dx;
+    if (want_din) {
+      gd.M = batch; gd.N = fi; gd.K = fo;
+      gd.A = dY; gd.lda = ld_dy; gd.a_trans = 0;
+      if (bf) { gd.B = h->shadow + h->shadow_off[l]; gd.ldb = h->out_pad[l]; }
+      else { gd.B = h->params + h->w_off[l]; gd.ldb = fo; }
+      gd.b_trans = 1;
+      gd.act = MLP_ACT_NONE;
+      if (l > 0) {
+        gd.mask = h->act == MLP_ACT_RELU ? h->acts[l - 1] : nullptr;
+        gd.ldm = h->act_ld[l];
+        gd.C = h->dh[l & 1];
+        gd.ldc = h->act_ld[l];
+      } else {
+        gd.C = dx;
+        gd.ldc = fi;
+      }
+      gd.c_bf16 = bf ? 1 : 0;
+      MLP_CHECK(run_gemm(gd, bf, st));
+    }
+    // [dW_l; db_l] = [In_l | 1]^T dY_l   (A = In_l read transposed), written
+    // over the layer's flat slice of grads
+    GemmArgs gw{};
+    gw.M = fi + 1; gw.N = fo; gw.K = batch;
+    gw.A = in; gw.lda = ld_in; gw.a_trans = 1;
+    gw.B = dY; gw.ldb = ld_dy; gw.b_trans = 0;
+    gw.C = h->grads + h->w_off[l]; gw.ldc = fo; gw.c_bf16 = 0;
+    gw.act = MLP_ACT_NONE;
+    if (fuse_sgd) {
+      gw.sgd_w = h->params + h->w_off[l];
+      gw.sgd_v = h->velocity + h->w_off[l];
+      gw.sgd_lr = lr;
+      gw.sgd_mom = mom;
+      gw.sgd_shadow = h->shadow ? h->shadow + h->shadow_off[l] : nullptr;
+      gw.sgd_ld_shadow = h->out_pad[l];
+      gw.sgd_shadow_rows = fi;
+    }
+    MLP_CHECK(run_gemm(gw, bf, st));
+    if (l > 0) {
+      dY = gd.C;
+      ld_dy = gd.ldc;
+    }
+  }
+  return MLP_OK;
 }
 
 }  // namespace
@@ -384,7 +526,7 @@ mlp_status mlp_create(const int* dims, int n_dims, int hidden_act, int prec, int
     h->out_pad.push_back(round8(dims[l + 1]));
     soff += (long long)dims[l] * round8(dims[l + 1]);
   }
-  for (int l = 0; l < n_dims; ++l) h->act_ld.push_back(round8(dims[l]));
+  for (int l = 0; l < h->L; ++l) h->act_ld.push_back(round8(dims[l] + 1));
   // segment map for the fused SGD + shadow refresh
   h->segs.n = 2 * h->L;
   for (int l = 0; l < h->L; ++l) {
@@ -412,7 +554,6 @@ mlp_status mlp_create(const int* dims, int n_dims, int hidden_act, int prec, int
   h->ldz = round8(dims[h->L]);
   h->dlogits = w;
   w += pl.dlogits;
-  h->dh_ld = 0;
   h->dh[0] = w;
   w += pl.dh;
   h->dh[1] = w;
@@ -442,58 +583,10 @@ mlp_status mlp_forward(mlp_handle* h, const void* x, int x_dtype, int batch, flo
   if (!x || !logits) return MLP_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(logits)) return MLP_ERR_MISALIGNED;
   cudaStream_t st = S(stream);
-  const bool bf = h->prec == MLP_PREC_BF16;
-  const int d0 = h->dims[0];
-  // The first GEMM reads X in the path's operand type.  An input already in
-  // that type with 16-byte rows is read in place; otherwise it is converted
-  // into the workspace.
-  const bool in_place = (bf && x_dtype == MLP_DTYPE_BF16 && (d0 * 2) % 16 == 0) ||
-                        (!bf && x_dtype == MLP_DTYPE_F32);
-  if (in_place) {
-    h->x_used = x;
-    h->x_ld = d0;
-  } else {
-    MLP_CHECK(launch_cast(x, x_dtype, h->x_copy, bf ? 1 : 0, (long long)batch * d0, st));
-    h->x_used = h->x_copy;
-    h->x_ld = d0;
-  }
-  if (bf && (h->x_ld * 2) % 16 != 0) return MLP_ERR_UNSUPPORTED_SHAPE;
-  const void* in = h->x_used;
-  int ld_in = h->x_ld;
-  for (int l = 0; l < h->L; ++l) {
-    const bool last = (l == h->L - 1);
-    GemmArgs g{};
-    g.M = batch;
-    g.N = h->dims[l + 1];
-    g.K = h->dims[l];
-    g.A = in;
-    g.lda = ld_in;
-    g.a_trans = 0;
-    if (bf) {
-      g.B = h->shadow + h->shadow_off[l];
-      g.ldb = h->out_pad[l];
-    } else {
-      g.B = h->params + h->w_off[l];
-      g.ldb = h->dims[l + 1];
-    }
-    g.b_trans = 0;
-    g.bias = h->params + h->b_off[l];
-    g.act = last ? MLP_ACT_NONE : h->act;
-    g.mask = nullptr;
-    g.ldm = 0;
-    if (last) {
-      g.C = logits;
-      g.ldc = h->dims[l + 1];
-      g.c_bf16 = 0;
-    } else {
-      g.C = h->acts[l];
-      g.ldc = h->act_ld[l + 1];
-      g.c_bf16 = bf ? 1 : 0;
-    }
-    MLP_CHECK(run_gemm(g, bf, st));
-    in = g.C;
-    ld_in = g.ldc;
-  }
+  MLP_CHECK(load_input(h, x, x_dtype, batch, st));
+  MLP_CHECK(forward_hidden(h, batch, st));
+  MLP_CHECK(run_gemm(logits_gemm(h, batch, logits), h->prec == MLP_PREC_BF16, st));
+  h->have_forward = true;
   return MLP_OK;
 }
 
@@ -501,53 +594,11 @@ mlp_status mlp_backward(mlp_handle* h, const void* dlogits, int ld_dlogits, int 
                         void* stream) {
   if (!h || batch < 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
   if (batch == 0) return MLP_OK;
-  if (!dlogits || !h->x_used || ld_dlogits < h->dims[h->L]) return MLP_ERR_INVALID_ARG;
+  if (!dlogits || !h->have_forward || ld_dlogits < h->dims[h->L]) return MLP_ERR_INVALID_ARG;
   if (!aligned16(dlogits) || (dx && !aligned16(dx))) return MLP_ERR_MISALIGNED;
   const bool bf = h->prec == MLP_PREC_BF16;
   if (bf && (ld_dlogits * 2) % 16 != 0) return MLP_ERR_MISALIGNED;
-  cudaStream_t st = S(stream);
-  const void* dY = dlogits;
-  int ld_dy = ld_dlogits;
-  for (int l = h->L - 1; l >= 0; --l) {
-    const int fi = h->dims[l], fo = h->dims[l + 1];
-    const void* in = l == 0 ? h->x_used : h->acts[l - 1];
-    const int ld_in = l == 0 ? h->x_ld : h->act_ld[l];
-    // dW_l = In_l^T dY_l  (A = In_l read transposed, B = dY_l)
-    GemmArgs gw{};
-    gw.M = fi; gw.N = fo; gw.K = batch;
-    gw.A = in; gw.lda = ld_in; gw.a_trans = 1;
-    gw.B = dY; gw.ldb = ld_dy; gw.b_trans = 0;
-    gw.C = h->grads + h->w_off[l]; gw.ldc = fo; gw.c_bf16 = 0;
-    gw.act = MLP_ACT_NONE;
-    MLP_CHECK(run_gemm(gw, bf, st));
-    // db_l = sum_rows dY_l
-    MLP_CHECK(launch_colsum(dY, bf ? 1 : 0, batch, fo, ld_dy, h->grads + h->b_off[l], h->red, st));
-    if (l == 0 && !dx) break;
-    // dIn = (dY W_l^T) * (H_l > 0)   (B = W_l read transposed)
-    GemmArgs gd{};
-    gd.M = batch; gd.N = fi; gd.K = fo;
-    gd.A = dY; gd.lda = ld_dy; gd.a_trans = 0;
-    if (bf) { gd.B = h->shadow + h->shadow_off[l]; gd.ldb = h->out_pad[l]; }
-    else { gd.B = h->params + h->w_off[l]; gd.ldb = fo; }
-    gd.b_trans = 1;
-    gd.act = MLP_ACT_NONE;
-    if (l > 0) {
-      gd.mask = h->act == MLP_ACT_RELU ? h->acts[l - 1] : nullptr;
-      gd.ldm = h->act_ld[l];
-      gd.C = h->dh[l & 1];
-      gd.ldc = h->act_ld[l];
-      gd.c_bf16 = bf ? 1 : 0;
-    } else {
-      gd.C = dx;
-      gd.ldc = fi;
-      gd.c_bf16 = bf ? 1 : 0;
-    }
-    MLP_CHECK(run_gemm(gd, bf, st));
-    if (l == 0) break;
-    dY = gd.C;
-    ld_dy = gd.ldc;
-  }
-  return MLP_OK;
+  return backward_impl(h, dlogits, ld_dlogits, batch, dx, false, 0.f, 0.f, S(stream));
 }
 
 mlp_status mlp_sgd_step(mlp_handle* h, float lr, float momentum, void* stream) {
@@ -560,17 +611,37 @@ mlp_status mlp_train_step(mlp_handle* h, const void* x, int x_dtype, const int32
                           int batch, float lr, float momentum, float* loss_out,
                           int32_t* argmax_out, void* stream) {
   if (!h || batch < 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
+  if (x_dtype != MLP_DTYPE_F32 && x_dtype != MLP_DTYPE_BF16 && x_dtype != MLP_DTYPE_U8)
+    return MLP_ERR_INVALID_ARG;
   if (batch == 0) return MLP_OK;
-  if (!labels) return MLP_ERR_INVALID_ARG;
-  if (!aligned16(labels) || (loss_out && !aligned16(loss_out)) ||
+  if (!x || !labels) return MLP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(labels) || (loss_out && !aligned16(loss_out)) ||
       (argmax_out && !aligned16(argmax_out)))
     return MLP_ERR_MISALIGNED;
   cudaStream_t st = S(stream);
   const int C = h->dims[h->L];
-  MLP_CHECK(mlp_forward(h, x, x_dtype, batch, h->logits, stream));
-  MLP_CHECK(launch_xent(h->logits, C, labels, batch, C, loss_out ? loss_out : h->loss, h->dlogits,
-                        h->prec == MLP_PREC_BF16, h->ldz, argmax_out, h->red, st));
-  MLP_CHECK(mlp_backward(h, h->dlogits, h->ldz, batch, nullptr, stream));
+  const bool bf = h->prec == MLP_PREC_BF16;
+  float* loss = loss_out ? loss_out : h->loss;
+  MLP_CHECK(load_input(h, x, x_dtype, batch, st));
+  MLP_CHECK(forward_hidden(h, batch, st));
+  GemmArgs gz = logits_gemm(h, batch, h->logits);
+  if (bf && batch <= 128 && C <= 32) {
+    // one tile holds the whole head: softmax cross entropy in its epilogue
+    gz.xent_labels = labels;
+    gz.xent_dlog = h->dlogits;
+    gz.xent_ldd = h->ldz;
+    gz.xent_loss = loss;
+    gz.xent_argmax = argmax_out;
+    gz.xent_norm = batch;
+    MLP_CHECK(run_gemm(gz, true, st));
+  } else {
+    MLP_CHECK(run_gemm(gz, bf, st));
+    MLP_CHECK(launch_xent(h->logits, C, labels, batch, C, loss, h->dlogits, bf, h->ldz,
+                          argmax_out, h->red, st));
+  }
+  h->have_forward = true;
+  if (bf) return backward_impl(h, h->dlogits, h->ldz, batch, nullptr, true, lr, momentum, st);
+  MLP_CHECK(backward_impl(h, h->dlogits, h->ldz, batch, nullptr, false, 0.f, 0.f, st));
   return mlp_sgd_step(h, lr, momentum, stream);
 }
 

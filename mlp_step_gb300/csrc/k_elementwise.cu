@@ -130,28 +130,54 @@ mlp_status launch_shadow(const float* w, __nv_bfloat16* wb, long long n, const S
 
 // ------------------------------------------------------------------ casts
 // Inputs arrive as image bytes (value = byte / 255, IEEE division), fp32 or
-// bf16; the tensor-core path wants bf16, the SIMT path fp32.
+// bf16; the tensor-core path wants bf16, the SIMT path fp32.  Source rows of
+// `cols` values land in destination rows of pitch ld_dst.
 
-__global__ void cast_kernel(const void* __restrict__ src, int src_dtype, void* __restrict__ dst,
-                            int dst_bf16, long long n) {
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-    float x;
-    if (src_dtype == MLP_DTYPE_U8) x = (float)static_cast<const uint8_t*>(src)[i] / 255.0f;
-    else if (src_dtype == MLP_DTYPE_BF16) x = bf16_to_f32(static_cast<const __nv_bfloat16*>(src)[i]);
-    else x = static_cast<const float*>(src)[i];
-    if (dst_bf16) static_cast<__nv_bfloat16*>(dst)[i] = f32_to_bf16(x);
-    else static_cast<float*>(dst)[i] = x;
+__device__ __forceinline__ float load_in(const void* src, int src_dtype, size_t i) {
+  if (src_dtype == MLP_DTYPE_U8) return (float)static_cast<const uint8_t*>(src)[i] / 255.0f;
+  if (src_dtype == MLP_DTYPE_BF16) return bf16_to_f32(static_cast<const __nv_bfloat16*>(src)[i]);
+  return static_cast<const float*>(src)[i];
+}
+
+__global__ void __launch_bounds__(256) cast_rows_kernel(const void* __restrict__ src,
+                                                        int src_dtype, void* __restrict__ dst,
+                                                        int dst_bf16, int rows, int cols,
+                                                        int ld_dst) {
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const size_t si = (size_t)r * cols, di = (size_t)r * ld_dst;
+    if (dst_bf16 && src_dtype == MLP_DTYPE_U8 && (cols & 7) == 0 && (ld_dst & 7) == 0) {
+      // 8 bytes in, 8 bf16 (16 bytes) out per thread
+      const uint2* s8 = reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(src) + si);
+      uint4* d16 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + di);
+      for (int q = threadIdx.x; q < cols / 8; q += blockDim.x) {
+        const uint2 b = s8[q];
+        const uint8_t* u = reinterpret_cast<const uint8_t*>(&b);
+        uint4 o;
+        o.x = pack_bf16x2((float)u[0] / 255.0f, (float)u[1] / 255.0f);
+        o.y = pack_bf16x2((float)u[2] / 255.0f, (float)u[3] / 255.0f);
+        o.z = pack_bf16x2((float)u[4] / 255.0f, (float)u[5] / 255.0f);
+        o.w = pack_bf16x2((float)u[6] / 255.0f, (float)u[7] / 255.0f);
+        d16[q] = o;
+      }
+    } else {
+      for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+        const float v = load_in(src, src_dtype, si + c);
+        if (dst_bf16) static_cast<__nv_bfloat16*>(dst)[di + c] = f32_to_bf16(v);
+        else static_cast<float*>(dst)[di + c] = v;
+      }
+    }
   }
 }
 
-mlp_status launch_cast(const void* src, int src_dtype, void* dst, int dst_bf16, long long n,
-                       cudaStream_t st) {
-  if (n <= 0) return MLP_OK;
-  long long blocks = (n + 1023) / 1024;
-  if (blocks > (long long)num_sms() * 8) blocks = (long long)num_sms() * 8;
-  LaunchScope ls("cast", st, n);
-  cast_kernel<<<(int)blocks, 256, 0, st>>>(src, src_dtype, dst, dst_bf16, n);
+mlp_status launch_cast_rows(const void* src, int src_dtype, void* dst, int dst_bf16, int rows,
+                            int cols, int ld_dst, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return MLP_OK;
+  // the vector path of the kernel needs 8-byte source rows and 16-byte
+  // destination rows, which the row-size checks there and 16-byte base
+  // pointers (checked by the callers) guarantee
+  int blocks = rows < num_sms() * 16 ? rows : num_sms() * 16;
+  LaunchScope ls("cast", st, (long long)rows * cols);
+  cast_rows_kernel<<<blocks, 256, 0, st>>>(src, src_dtype, dst, dst_bf16, rows, cols, ld_dst);
   return launch_status();
 }
 
@@ -657,6 +683,28 @@ mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out
     return launch_status();
   }
   return MLP_OK;
+}
+
+// ------------------------------------------------------------------ ones columns
+
+__global__ void ones_cols_kernel(OnesCols oc, int rows, int bf16) {
+  const int k = blockIdx.y;
+  const int col = oc.col[k], ld = oc.ld[k];
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
+    for (int c = col; c < ld; ++c) {
+      const float v = c == col ? 1.f : 0.f;
+      if (bf16) static_cast<__nv_bfloat16*>(oc.ptr[k])[(size_t)r * ld + c] = f32_to_bf16(v);
+      else static_cast<float*>(oc.ptr[k])[(size_t)r * ld + c] = v;
+    }
+  }
+}
+
+mlp_status launch_ones_cols(const OnesCols& oc, int rows, int bf16, cudaStream_t st) {
+  if (oc.n <= 0 || rows <= 0) return MLP_OK;
+  LaunchScope ls("ones_cols", st, rows, oc.n);
+  dim3 grid((rows + 255) / 256, oc.n);
+  ones_cols_kernel<<<grid, 256, 0, st>>>(oc, rows, bf16);
+  return launch_status();
 }
 
 // ------------------------------------------------------------------ wait self-test

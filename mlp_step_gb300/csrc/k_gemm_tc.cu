@@ -51,6 +51,18 @@ struct TcParams {
   // of one tile and stores raw fp32 sums into partial[s][M][ldp]
   int splits, kb_per_split, ldp;
   float* partial;
+  // fused softmax cross entropy (single tile) and momentum SGD epilogues
+  const int* xent_labels;
+  __nv_bfloat16* xent_dlog;
+  int xent_ldd;
+  float* xent_loss;
+  int* xent_argmax;
+  int xent_norm;
+  float* sgd_w;
+  float* sgd_v;
+  float sgd_lr, sgd_mom;
+  __nv_bfloat16* sgd_shadow;
+  int sgd_ld_shadow, sgd_shadow_rows;
 };
 
 template <int BN, int STAGES>
@@ -139,12 +151,114 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, int m, int n0,
   }
 }
 
+// Momentum SGD on one 32-column piece of the fp32 gradient row m ("Capstone 5:
+// train a network with your CUDA kernels", "Read the worked reference":
+// v <- m v - lr g, w <- w + v), also storing g and bf16(w).
+__device__ __forceinline__ void sgd_epilogue_chunk(const TcParams& p, int m, int n0,
+                                                   const uint32_t (&r)[32]) {
+  const size_t off = (size_t)m * p.ldc + n0;
+  float* gr = static_cast<float*>(p.C) + off;
+  float* wr = p.sgd_w + off;
+  float* vr = p.sgd_v + off;
+  __nv_bfloat16* sr =
+      m < p.sgd_shadow_rows ? p.sgd_shadow + (size_t)m * p.sgd_ld_shadow + n0 : nullptr;
+  const bool vec = (n0 + 32 <= p.N) && ((reinterpret_cast<uintptr_t>(gr) & 15) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(wr) & 15) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(vr) & 15) == 0) &&
+                   (!sr || (reinterpret_cast<uintptr_t>(sr) & 15) == 0);
+  if (vec) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 w4 = reinterpret_cast<const float4*>(wr)[q];
+      const float4 v4 = reinterpret_cast<const float4*>(vr)[q];
+      const float g0 = __uint_as_float(r[4 * q]), g1 = __uint_as_float(r[4 * q + 1]);
+      const float g2 = __uint_as_float(r[4 * q + 2]), g3 = __uint_as_float(r[4 * q + 3]);
+      float4 nv, nw;
+      nv.x = p.sgd_mom * v4.x - p.sgd_lr * g0;  nw.x = w4.x + nv.x;
+      nv.y = p.sgd_mom * v4.y - p.sgd_lr * g1;  nw.y = w4.y + nv.y;
+      nv.z = p.sgd_mom * v4.z - p.sgd_lr * g2;  nw.z = w4.z + nv.z;
+      nv.w = p.sgd_mom * v4.w - p.sgd_lr * g3;  nw.w = w4.w + nv.w;
+      reinterpret_cast<float4*>(gr)[q] = make_float4(g0, g1, g2, g3);
+      reinterpret_cast<float4*>(vr)[q] = nv;
+      reinterpret_cast<float4*>(wr)[q] = nw;
+      if (sr) {
+        uint2 o;
+        o.x = pack_bf16x2(nw.x, nw.y);
+        o.y = pack_bf16x2(nw.z, nw.w);
+        reinterpret_cast<uint2*>(sr)[q] = o;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (n0 + j < p.N) {
+        const float g = __uint_as_float(r[j]);
+        const float nv = p.sgd_mom * vr[j] - p.sgd_lr * g;
+        const float nw = wr[j] + nv;
+        gr[j] = g;
+        vr[j] = nv;
+        wr[j] = nw;
+        if (sr) sr[j] = f32_to_bf16(nw);
+      }
+    }
+  }
+}
+
+// Stable softmax cross entropy of one row of at most 32 logits held by one
+// thread ("Capstone 5", "The minimum model" and "Read the worked reference":
+// subtract the row maximum before exponentiating; fp32 throughout).  Writes
+// the fp32 logits (if C is set), bf16 dZ = (softmax - onehot) / norm padded
+// with zeros to xent_ldd, and the argmax (lowest index among ties); returns
+// the row loss m + ln(sum exp(z - m)) - z_label.
+__device__ __forceinline__ float xent_epilogue_row(const TcParams& p, int m,
+                                                   const uint32_t (&r)[32]) {
+  int y = __ldg(p.xent_labels + m);
+  y = y < 0 ? 0 : (y >= p.N ? p.N - 1 : y);
+  float z[32];
+  float mx = -INFINITY, zy = 0.f;
+  int am = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    z[j] = -INFINITY;
+    if (j < p.N) {
+      z[j] = __uint_as_float(r[j]) + (p.bias ? __ldg(p.bias + j) : 0.f);
+      if (z[j] > mx) { mx = z[j]; am = j; }
+      if (j == y) zy = z[j];
+    }
+  }
+  if (p.C) {
+    float* lrow = static_cast<float*>(p.C) + (size_t)m * p.ldc;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < p.N) lrow[j] = z[j];
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    z[j] = j < p.N ? expf(z[j] - mx) : 0.f;  // z now holds exp(z - max)
+    s += z[j];
+  }
+  const float inv = 1.0f / (float)p.xent_norm;
+  __nv_bfloat16* drow = p.xent_dlog + (size_t)m * p.xent_ldd;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j < p.xent_ldd) {
+      float d = 0.f;
+      if (j < p.N) d = (z[j] / s - (j == y ? 1.f : 0.f)) * inv;
+      drow[j] = f32_to_bf16(d);
+    }
+  }
+  if (p.xent_argmax) p.xent_argmax[m] = am;
+  return mx + logf(s) - zy;
+}
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
   using L = Layout<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
+  __shared__ float xent_part[4];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -285,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tm, tn;
       tile_coords(u / p.splits, p.tiles_m, p.tiles_n, tm, tn);
       float* part = p.splits > 1 ? p.partial + (size_t)(u % p.splits) * p.M * p.ldp : nullptr;
+      float row_loss = 0.f;
       const int m = tm * BM + row;
       for (int c0 = 0; c0 < BN; c0 += 32) {
         const int n0 = tn * BN + c0;
@@ -307,10 +422,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               for (int j = 0; j < 32 && n0 + j < p.N; ++j) prow[j] = __uint_as_float(r[j]);
             }
+          } else if (p.xent_labels) {
+            row_loss = xent_epilogue_row(p, m, r);
+          } else if (p.sgd_w) {
+            sgd_epilogue_chunk(p, m, n0, r);
           } else {
             epilogue_chunk<BN>(p, m, n0, r);
           }
         }
+      }
+      if (p.xent_labels) {
+        // mean loss of the (single) tile: butterfly sum within each warp,
+        // then the four warps in lane-quarter order
+        float v = m < p.M ? row_loss : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) xent_part[quarter] = v;
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (warp == 2 && lane == 0)
+          *p.xent_loss = (((xent_part[0] + xent_part[1]) + xent_part[2]) + xent_part[3]) /
+                         (float)p.xent_norm;
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -429,7 +560,10 @@ size_t gemm_tc_splitk_bytes(int M, int N, int K) {
 
 mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0) return MLP_OK;
-  if (g.K <= 0) return launch_gemm_simt(g, 1, st);
+  if (g.K <= 0) {
+    if (g.xent_labels || g.sgd_w) return MLP_ERR_UNSUPPORTED_SHAPE;
+    return launch_gemm_simt(g, 1, st);
+  }
 
   int splits = 1, kb_per_split = (g.K + BK - 1) / BK;
   const size_t split_bytes = gemm_tc_splitk_bytes(g.M, g.N, g.K);
@@ -467,6 +601,22 @@ mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStr
   p.kb_per_split = kb_per_split;
   p.ldp = (g.N + 3) / 4 * 4;
   p.partial = splits > 1 ? static_cast<float*>(g.ws) : nullptr;
+  p.xent_labels = g.xent_labels;
+  p.xent_dlog = static_cast<__nv_bfloat16*>(g.xent_dlog);
+  p.xent_ldd = g.xent_ldd;
+  p.xent_loss = g.xent_loss;
+  p.xent_argmax = g.xent_argmax;
+  p.xent_norm = g.xent_norm;
+  p.sgd_w = g.sgd_w;
+  p.sgd_v = g.sgd_v;
+  p.sgd_lr = g.sgd_lr;
+  p.sgd_mom = g.sgd_mom;
+  p.sgd_shadow = g.sgd_shadow;
+  p.sgd_ld_shadow = g.sgd_ld_shadow;
+  p.sgd_shadow_rows = g.sgd_shadow_rows;
+  if (p.xent_labels && (p.num_tiles != 1 || g.N > 32 || !p.xent_dlog || !p.xent_loss))
+    return MLP_ERR_UNSUPPORTED_SHAPE;
+  if ((p.xent_labels || p.sgd_w) && splits > 1) return MLP_ERR_UNSUPPORTED_SHAPE;
   p.err = device_error_word();
   if (!p.err) return MLP_ERR_CUDA;
 

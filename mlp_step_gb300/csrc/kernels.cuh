@@ -25,8 +25,8 @@ mlp_status launch_sgd(float* w, const float* g, float* v, __nv_bfloat16* wb, lon
                       float lr, float mom, const SgdSegments& segs, cudaStream_t st);
 mlp_status launch_shadow(const float* w, __nv_bfloat16* wb, long long n, const SgdSegments& segs,
                          cudaStream_t st);
-mlp_status launch_cast(const void* src, int src_dtype, void* dst, int dst_bf16, long long n,
-                       cudaStream_t st);
+mlp_status launch_cast_rows(const void* src, int src_dtype, void* dst, int dst_bf16, int rows,
+                            int cols, int ld_dst, cudaStream_t st);
 size_t xent_workspace_bytes(int B);
 mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, int C,
                        float* loss_out, void* dlog, int dl_bf16, int ldd, int* argmax, void* ws,
@@ -38,6 +38,16 @@ size_t mse_ws_bytes(long long n);
 mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out, void* dy,
                       void* ws, cudaStream_t st);
 mlp_status launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st);
+// Sets column `col` of rows [0, rows) of each listed bf16 or fp32 matrix to 1
+// (and the columns after it, up to ld, to 0): the ones column that lets a
+// weight-gradient GEMM produce the bias gradient as its last row.
+struct OnesCols {
+  int n;
+  void* ptr[8];
+  int ld[8];
+  int col[8];
+};
+mlp_status launch_ones_cols(const OnesCols& oc, int rows, int bf16, cudaStream_t st);
 
 // k_gemm_simt.cu: fp32 (or bf16-input) SIMT GEMM with the fused epilogue.
 struct GemmArgs {
@@ -50,6 +60,26 @@ struct GemmArgs {
   // optional scratch for split-K partial sums (tensor-core path only)
   void* ws = nullptr;
   size_t ws_bytes = 0;
+  // Fused softmax cross entropy (tensor-core path; the whole problem must be
+  // one tile: M <= 128, N <= 32): C receives the fp32 logits (nullable),
+  // xent_dlog the bf16 dZ [M][xent_ldd], xent_loss the mean loss over
+  // xent_norm rows, xent_argmax (nullable) the predictions.
+  const int* xent_labels = nullptr;
+  void* xent_dlog = nullptr;
+  int xent_ldd = 0;
+  float* xent_loss = nullptr;
+  int* xent_argmax = nullptr;
+  int xent_norm = 0;
+  // Fused momentum SGD on the fp32 result g (tensor-core path): with w and v
+  // laid out like C, v <- mom v - lr g, w <- w + v, and bf16(w) into
+  // sgd_shadow[m][sgd_ld_shadow] for rows m < sgd_shadow_rows.  C still
+  // receives g.
+  float* sgd_w = nullptr;
+  float* sgd_v = nullptr;
+  float sgd_lr = 0.f, sgd_mom = 0.f;
+  __nv_bfloat16* sgd_shadow = nullptr;
+  int sgd_ld_shadow = 0;
+  int sgd_shadow_rows = 0;
 };
 mlp_status launch_gemm_simt(const GemmArgs& g, int in_bf16, cudaStream_t st);
 

@@ -113,6 +113,41 @@ def test_bf16_step_matches_oracle(B):
     assert torch.equal(S2[:, :10], W2.to(torch.bfloat16))
 
 
+def test_bf16_fused_step_matches_unfused_sequence():
+    """The train step fuses softmax cross entropy into the logits GEMM and the
+    momentum update into the weight-gradient GEMMs; the separate calls
+    (forward, loss, backward, SGD) must give the same step."""
+    B = 128
+    p0 = synth.mlp_flat_params(DIMS)
+    p0[200704:200960] = synth.normal_f32((256,), synth.STREAM_GENERIC, std=0.1)  # nonzero b1
+    xb = to_dev(synth.images_u8(B, 784))
+    y = to_dev(synth.labels(B, 10))
+    fused = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+    loss_f = torch.zeros(4, device="cuda")
+    am_f = torch.empty(B, dtype=torch.int32, device="cuda")
+    for _ in range(2):   # second step also exercises a nonzero velocity
+        fused.train_step(xb, y, LR, MOM, loss_out=loss_f, argmax_out=am_f)
+    seq = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+    logits = torch.empty(B, 10, device="cuda")
+    dl = torch.empty(B, 16, dtype=torch.bfloat16, device="cuda")
+    loss_s = torch.zeros(4, device="cuda")
+    am_s = torch.empty(B, dtype=torch.int32, device="cuda")
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        seq.forward(xb, logits)
+        M.softmax_xent_fwd_bwd(logits, y, loss_s, dlogits=dl, argmax_out=am_s, workspace=ws)
+        seq.backward(dl, B)
+        seq.sgd_step(LR, MOM)
+    torch.cuda.synchronize()
+    assert abs(loss_f[0].item() - loss_s[0].item()) <= 1e-6 * abs(loss_s[0].item())
+    assert torch.equal(am_f, am_s)
+    assert torch.allclose(fused.grads, seq.grads, rtol=1e-5, atol=1e-9)
+    assert torch.allclose(fused.params, seq.params, rtol=1e-6, atol=1e-8)
+    assert torch.allclose(fused.velocity, seq.velocity, rtol=1e-5, atol=1e-9)
+    assert torch.equal(fused.shadow, seq.shadow) or \
+        (fused.shadow.float() - seq.shadow.float()).abs().max().item() <= 2 ** -7
+
+
 def test_bf16_forward_matches_oracle_exact_mode():
     B = 128
     p0 = synth.mlp_flat_params(DIMS)
