@@ -1,6 +1,7 @@
 // C-ABI entry points (include/mlp_step.h): argument checks, workspace
 // carving, tensor-map encoding and the enqueue order of each step.  No
 // arithmetic of the method lives here; every computation is a kernel launch.
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -31,6 +32,19 @@ int* device_error_word() {
     addr[dev] = static_cast<int*>(p);
   }
   return addr[dev];
+}
+
+// ------------------------------------------------------------ launch options
+
+// Programmatic dependent launch is on unless MLP_STEP_PDL=0 is set in the
+// environment (read once).
+bool pdl_enabled() {
+  static int on = -1;
+  if (on < 0) {
+    const char* e = getenv("MLP_STEP_PDL");
+    on = (e && e[0] == '0') ? 0 : 1;
+  }
+  return on == 1;
 }
 
 // ------------------------------------------------------------ bounded waits
@@ -438,7 +452,12 @@ mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int
     gw.B = dY; gw.ldb = ld_dy; gw.b_trans = 0;
     gw.C = h->grads + h->w_off[l]; gw.ldc = fo; gw.c_bf16 = 0;
     gw.act = MLP_ACT_NONE;
-    if (fuse_sgd) {
+    // The update rides in the GEMM epilogue only for small weight matrices:
+    // there it saves a launch; on large ones the epilogue's per-row accesses
+    // to w and v compete with the MMA operand traffic and the flat SGD kernel
+    // (which streams at HBM speed) is faster.
+    const bool fuse_here = fuse_sgd && (long long)(fi + 1) * fo <= (1ll << 18);
+    if (fuse_here) {
       gw.sgd_w = h->params + h->w_off[l];
       gw.sgd_v = h->velocity + h->w_off[l];
       gw.sgd_lr = lr;
@@ -448,6 +467,23 @@ mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int
       gw.sgd_shadow_rows = fi;
     }
     MLP_CHECK(run_gemm(gw, bf, st));
+    if (fuse_sgd && !fuse_here) {
+      // flat SGD over this layer's W and b (and its shadow rows)
+      SgdSegments seg{};
+      seg.n = 2;
+      seg.flat_off[0] = 0;
+      seg.shadow_off[0] = h->shadow ? 0 : -1;
+      seg.cols[0] = fo;
+      seg.cols_pad[0] = h->out_pad[l];
+      seg.flat_off[1] = (long long)fi * fo;
+      seg.shadow_off[1] = -1;
+      seg.cols[1] = 1;
+      seg.cols_pad[1] = 1;
+      MLP_CHECK(launch_sgd(h->params + h->w_off[l], h->grads + h->w_off[l],
+                           h->velocity + h->w_off[l],
+                           h->shadow ? h->shadow + h->shadow_off[l] : nullptr,
+                           (long long)(fi + 1) * fo, lr, mom, seg, st));
+    }
     if (l > 0) {
       dY = gd.C;
       ld_dy = gd.ldc;

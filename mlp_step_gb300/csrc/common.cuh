@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cstddef>
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -36,6 +37,36 @@ __device__ __forceinline__ __nv_bfloat16 f32_to_bf16(float v) { return __float2b
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// Programmatic dependent launch: kernels launched through launch_k may start
+// (their prologue: barriers, tensor memory, tensor-map prefetch) while the
+// previous kernel on the stream finishes; each kernel calls pdl_wait() before
+// its first global-memory access, which waits for the previous grid to
+// complete and its writes to be visible, and pdl_launch_dependents() so that
+// the next kernel may be scheduled.  Without the launch attribute both are
+// no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -183,6 +183,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
   ptx::cluster_sync();  // the peer's barriers are initialised before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // y half: cols [0,256); U buffers: [256,384), [384,512)
+  pdl_wait();
+  pdl_launch_dependents();
 
   int last_parity[F_STAGES];
 
@@ -523,6 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // buffer b: U at b*256, DA at b*256 + 128
+  pdl_wait();
+  pdl_launch_dependents();
   int last_parity[B_STAGES];
 
   if (warp == 0) {
@@ -670,6 +674,8 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const float* __restric
                                                           const __nv_bfloat16* __restrict__ dy,
                                                           const float* __restrict__ rstd, int T,
                                                           __nv_bfloat16* __restrict__ dx) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -752,7 +758,7 @@ mlp_status launch_block_fwd(const void* x, const void* wg, const void* wd, int T
   if (clusters > p.tiles) clusters = p.tiles;
   if (clusters < 1) clusters = 1;
   LaunchScope ls("block_fwd", st, T, DM, hidden);
-  block_fwd_kernel<<<2 * clusters, F_THREADS, F_SMEM, st>>>(tx, tg, td, p);
+  launch_k(block_fwd_kernel, dim3(2 * clusters), dim3(F_THREADS), F_SMEM, st, tx, tg, td, p);
   return launch_status();
 }
 
@@ -788,7 +794,7 @@ mlp_status launch_block_bwd_act(const void* x, const void* wg, const void* wd, c
   int grid = num_sms();
   if (grid > p.num_tiles) grid = p.num_tiles;
   LaunchScope ls("block_bwd_act", st, T, DM, hidden);
-  block_bwd_act_kernel<<<grid, kThreads, B_SMEM, st>>>(tx, tg, tdy, twd, p);
+  launch_k(block_bwd_act_kernel, dim3(grid), dim3(kThreads), B_SMEM, st, tx, tg, tdy, twd, p);
   return launch_status();
 }
 
@@ -796,7 +802,7 @@ mlp_status launch_rmsnorm_bwd(const float* dnp, const void* x, const void* dy, c
                               int T, void* dx, cudaStream_t st) {
   if (T <= 0) return MLP_OK;
   LaunchScope ls("rmsnorm_bwd", st, T);
-  rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(dnp, static_cast<const __nv_bfloat16*>(x),
+  launch_k(rmsnorm_bwd_kernel, dim3((T + 7) / 8), dim3(256), 0, st, dnp, static_cast<const __nv_bfloat16*>(x),
                                                   static_cast<const __nv_bfloat16*>(dy), rstd, T,
                                                   static_cast<__nv_bfloat16*>(dx));
   return launch_status();

@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(256) sgd_kernel(float* __restrict__ w, const f
                                                   float* __restrict__ v,
                                                   __nv_bfloat16* __restrict__ wb, long long n,
                                                   float lr, float mom, SgdSegments segs) {
+  pdl_wait();
+  pdl_launch_dependents();
   const long long n4 = n >> 2;
   const long long stride = (long long)gridDim.x * blockDim.x;
   float4* w4 = reinterpret_cast<float4*>(w);
@@ -96,6 +98,8 @@ __global__ void __launch_bounds__(256) sgd_kernel(float* __restrict__ w, const f
 // Shadow refresh alone: wb <- bf16(w) through the segment map.
 __global__ void shadow_kernel(const float* __restrict__ w, __nv_bfloat16* __restrict__ wb,
                               long long n, SgdSegments segs) {
+  pdl_wait();
+  pdl_launch_dependents();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     const int k = find_segment(segs, i);
@@ -116,7 +120,7 @@ mlp_status launch_sgd(float* w, const float* g, float* v, __nv_bfloat16* wb, lon
                       float lr, float mom, const SgdSegments& segs, cudaStream_t st) {
   if (n <= 0) return MLP_OK;
   LaunchScope ls("sgd", st, n);
-  sgd_kernel<<<sgd_grid(n), 256, 0, st>>>(w, g, v, wb, n, lr, mom, segs);
+  launch_k(sgd_kernel, dim3(sgd_grid(n)), dim3(256), 0, st, w, g, v, wb, n, lr, mom, segs);
   return launch_status();
 }
 
@@ -124,7 +128,7 @@ mlp_status launch_shadow(const float* w, __nv_bfloat16* wb, long long n, const S
                          cudaStream_t st) {
   if (n <= 0) return MLP_OK;
   LaunchScope ls("shadow", st, n);
-  shadow_kernel<<<sgd_grid(n), 256, 0, st>>>(w, wb, n, segs);
+  launch_k(shadow_kernel, dim3(sgd_grid(n)), dim3(256), 0, st, w, wb, n, segs);
   return launch_status();
 }
 
@@ -143,6 +147,8 @@ __global__ void __launch_bounds__(256) cast_rows_kernel(const void* __restrict__
                                                         int src_dtype, void* __restrict__ dst,
                                                         int dst_bf16, int rows, int cols,
                                                         int ld_dst) {
+  pdl_wait();
+  pdl_launch_dependents();
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const size_t si = (size_t)r * cols, di = (size_t)r * ld_dst;
     if (dst_bf16 && src_dtype == MLP_DTYPE_U8 && (cols & 7) == 0 && (ld_dst & 7) == 0) {
@@ -177,7 +183,7 @@ mlp_status launch_cast_rows(const void* src, int src_dtype, void* dst, int dst_b
   // pointers (checked by the callers) guarantee
   int blocks = rows < num_sms() * 16 ? rows : num_sms() * 16;
   LaunchScope ls("cast", st, (long long)rows * cols);
-  cast_rows_kernel<<<blocks, 256, 0, st>>>(src, src_dtype, dst, dst_bf16, rows, cols, ld_dst);
+  launch_k(cast_rows_kernel, dim3(blocks), dim3(256), 0, st, src, src_dtype, dst, dst_bf16, rows, cols, ld_dst);
   return launch_status();
 }
 
@@ -318,6 +324,8 @@ template <int NSEG>
 __global__ void __launch_bounds__(256) xent_rows_regs_kernel(
     const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
     float* __restrict__ partial, void* dlog, int dl_bf16, int ldd, int* argmax) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float part[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + warp;
@@ -343,6 +351,8 @@ __global__ void __launch_bounds__(256) xent_rows_regs_kernel(
 __global__ void __launch_bounds__(256) xent_single_block_kernel(
     const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
     float* __restrict__ loss_out, void* dlog, int dl_bf16, int ldd, int* argmax) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float part[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float inv_norm = 1.0f / (float)B;
@@ -368,6 +378,8 @@ __global__ void __launch_bounds__(256) xent_single_block_kernel(
 __global__ void __launch_bounds__(256) xent_rows_kernel(
     const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
     float* __restrict__ partial, void* dlog, int dl_bf16, int ldd, int* argmax) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float part[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + warp;
@@ -392,6 +404,8 @@ __global__ void __launch_bounds__(256) xent_rows_kernel(
 __global__ void __launch_bounds__(256) sum_partials_kernel(const float* __restrict__ partial,
                                                            long long n, float divisor,
                                                            float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float red[256];
   float t = 0.f;
   for (long long i = threadIdx.x; i < n; i += 256) t += partial[i];
@@ -415,7 +429,7 @@ mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, i
   if (B <= 0) return MLP_OK;
   if (B <= 256) {
     LaunchScope ls("xent", st, B, C);
-    xent_single_block_kernel<<<1, 256, 0, st>>>(logits, ldl, labels, B, C, loss_out, dlog,
+    launch_k(xent_single_block_kernel, dim3(1), dim3(256), 0, st, logits, ldl, labels, B, C, loss_out, dlog,
                                                 dl_bf16, ldd, argmax);
     return launch_status();
   }
@@ -426,19 +440,19 @@ mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, i
   {
   LaunchScope ls("xent", st, B, C);
   if (vec && C <= 256)
-    xent_rows_regs_kernel<2><<<blocks, 256, 0, st>>>(logits, ldl, labels, B, C, partial, dlog,
+    launch_k(xent_rows_regs_kernel<2>, dim3(blocks), dim3(256), 0, st, logits, ldl, labels, B, C, partial, dlog,
                                                      dl_bf16, ldd, argmax);
   else if (vec)
-    xent_rows_regs_kernel<8><<<blocks, 256, 0, st>>>(logits, ldl, labels, B, C, partial, dlog,
+    launch_k(xent_rows_regs_kernel<8>, dim3(blocks), dim3(256), 0, st, logits, ldl, labels, B, C, partial, dlog,
                                                      dl_bf16, ldd, argmax);
   else
-    xent_rows_kernel<<<blocks, 256, 0, st>>>(logits, ldl, labels, B, C, partial, dlog, dl_bf16,
+    launch_k(xent_rows_kernel, dim3(blocks), dim3(256), 0, st, logits, ldl, labels, B, C, partial, dlog, dl_bf16,
                                              ldd, argmax);
   }
   MLP_CHECK(launch_status());
   if (loss_out) {
     LaunchScope ls("sum_partials", st, blocks);
-    sum_partials_kernel<<<1, 256, 0, st>>>(partial, blocks, (float)B, loss_out);
+    launch_k(sum_partials_kernel, dim3(1), dim3(256), 0, st, partial, blocks, (float)B, loss_out);
     return launch_status();
   }
   return MLP_OK;
@@ -466,6 +480,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) colsum_pass1_kernel(const T* __restrict__ X, int rows,
                                                            int cols, int ld, int rows_per_chunk,
                                                            float* __restrict__ dst) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float s[8][65];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int c = blockIdx.x * 64 + 2 * tx;
@@ -499,6 +515,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) colsum_vec_kernel(const T* __restrict__ X, int rows,
                                                          int cols, int ld, int rows_per_chunk,
                                                          float* __restrict__ dst) {
+  pdl_wait();
+  pdl_launch_dependents();
   constexpr int V = 16 / sizeof(T);          // columns per lane
   constexpr int BC = 32 * V;                 // columns per block
   __shared__ float s[8][BC + 1];
@@ -544,6 +562,8 @@ __global__ void __launch_bounds__(256) colsum_vec_kernel(const T* __restrict__ X
 
 __global__ void colsum_pass2_kernel(const float* __restrict__ partial, int chunks, int cols,
                                     float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= cols) return;
   float t = 0.f;
@@ -584,24 +604,24 @@ mlp_status launch_colsum(const void* X, int bf16, int rows, int cols, int ld, fl
     const int bc = bf16 ? 256 : 128;
     dim3 g((cols + bc - 1) / bc, ch);
     if (bf16)
-      colsum_vec_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(X),
+      launch_k(colsum_vec_kernel<__nv_bfloat16>, dim3(g), dim3(256), 0, st, static_cast<const __nv_bfloat16*>(X),
                                                          rows, cols, ld, rpc, dst);
     else
-      colsum_vec_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(X), rows, cols, ld,
+      launch_k(colsum_vec_kernel<float>, dim3(g), dim3(256), 0, st, static_cast<const float*>(X), rows, cols, ld,
                                                   rpc, dst);
   } else {
   LaunchScope ls("colsum", st, rows, cols);
   if (bf16)
-    colsum_pass1_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+    launch_k(colsum_pass1_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st, 
         static_cast<const __nv_bfloat16*>(X), rows, cols, ld, rpc, dst);
   else
-    colsum_pass1_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(X), rows, cols,
+    launch_k(colsum_pass1_kernel<float>, dim3(grid), dim3(256), 0, st, static_cast<const float*>(X), rows, cols,
                                                      ld, rpc, dst);
   }
   MLP_CHECK(launch_status());
   if (ch > 1) {
     LaunchScope ls("colsum_final", st, ch, cols);
-    colsum_pass2_kernel<<<(cols + 255) / 256, 256, 0, st>>>(dst, ch, cols, out);
+    launch_k(colsum_pass2_kernel, dim3((cols + 255) / 256), dim3(256), 0, st, dst, ch, cols, out);
     return launch_status();
   }
   return MLP_OK;
@@ -616,6 +636,8 @@ __global__ void __launch_bounds__(256) mse_kernel(const __nv_bfloat16* __restric
                                                   const __nv_bfloat16* __restrict__ t,
                                                   long long n, __nv_bfloat16* __restrict__ dy,
                                                   float* __restrict__ partial) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float red[256];
   const float scale = 2.0f / (float)n;
   const long long n8 = n >> 3;
@@ -672,14 +694,14 @@ mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out
   float* partial = static_cast<float*>(ws);
   {
   LaunchScope ls("mse", st, n);
-  mse_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(y),
+  launch_k(mse_kernel, dim3(blocks), dim3(256), 0, st, static_cast<const __nv_bfloat16*>(y),
                                      static_cast<const __nv_bfloat16*>(t), n,
                                      static_cast<__nv_bfloat16*>(dy), partial);
   }
   MLP_CHECK(launch_status());
   if (loss_out) {
     LaunchScope ls("sum_partials", st, blocks);
-    sum_partials_kernel<<<1, 256, 0, st>>>(partial, blocks, (float)n, loss_out);
+    launch_k(sum_partials_kernel, dim3(1), dim3(256), 0, st, partial, blocks, (float)n, loss_out);
     return launch_status();
   }
   return MLP_OK;
@@ -688,6 +710,8 @@ mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out
 // ------------------------------------------------------------------ ones columns
 
 __global__ void ones_cols_kernel(OnesCols oc, int rows, int bf16) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int k = blockIdx.y;
   const int col = oc.col[k], ld = oc.ld[k];
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
@@ -703,7 +727,7 @@ mlp_status launch_ones_cols(const OnesCols& oc, int rows, int bf16, cudaStream_t
   if (oc.n <= 0 || rows <= 0) return MLP_OK;
   LaunchScope ls("ones_cols", st, rows, oc.n);
   dim3 grid((rows + 255) / 256, oc.n);
-  ones_cols_kernel<<<grid, 256, 0, st>>>(oc, rows, bf16);
+  launch_k(ones_cols_kernel, dim3(grid), dim3(256), 0, st, oc, rows, bf16);
   return launch_status();
 }
 
@@ -712,6 +736,8 @@ mlp_status launch_ones_cols(const OnesCols& oc, int rows, int bf16, cudaStream_t
 // gives up after limit_ns, records the timeout and the kernel returns.
 
 __global__ void wait_selftest_kernel(unsigned long long limit_ns, int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bar, 1);
@@ -724,7 +750,7 @@ mlp_status launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st) {
   int* err = device_error_word();
   if (!err) return MLP_ERR_CUDA;
   LaunchScope ls("wait_selftest", st);
-  wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, err);
+  launch_k(wait_selftest_kernel, dim3(1), dim3(32), 0, st, limit_ns, err);
   return launch_status();
 }
 

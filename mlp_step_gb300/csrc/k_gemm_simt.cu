@@ -27,6 +27,8 @@ __device__ __forceinline__ float ld_in<__nv_bfloat16>(const __nv_bfloat16* p) {
 
 template <typename T>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float As[16][64 + 4];
   __shared__ float Bs[16][64 + 4];
   const T* A = static_cast<const T*>(g.A);
@@ -103,8 +105,8 @@ mlp_status launch_gemm_simt(const GemmArgs& g, int in_bf16, cudaStream_t st) {
   dim3 grid((g.N + 63) / 64, (g.M + 63) / 64);
   if (grid.y > 65535) return MLP_ERR_UNSUPPORTED_SHAPE;
   LaunchScope ls("gemm_simt", st, g.M, g.N, g.K);
-  if (in_bf16) gemm_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(g);
-  else gemm_simt_kernel<float><<<grid, 256, 0, st>>>(g);
+  if (in_bf16) launch_k(gemm_simt_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st, g);
+  else launch_k(gemm_simt_kernel<float>, dim3(grid), dim3(256), 0, st, g);
   return launch_status();
 }
 

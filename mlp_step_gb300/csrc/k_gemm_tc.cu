@@ -294,6 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // prologue done: from here on global memory is touched
+  pdl_wait();
+  pdl_launch_dependents();
 
   // stage bookkeeping of the producer, used to drain copies in flight after
   // an abort
@@ -472,6 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Split-K finish: out = epilogue(sum_s partial[s]) in a fixed order, four
 // consecutive columns per thread.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const TcParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const long long quads = (long long)p.M * (p.ldp / 4);
   const size_t plane = (size_t)p.M * p.ldp;
   for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < quads;
@@ -517,7 +522,7 @@ mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const TcParam
                                          "gemm_tc_splitk_bn256"};
     const int which = BN == 64 ? 0 : (BN == 128 ? 1 : 2);
     LaunchScope ls(p.splits > 1 ? split_names[which] : names[which], st, p.M, p.N, p.K);
-    tc_gemm_kernel<BN, STAGES><<<grid, kThreads, L::SMEM, st>>>(ta, tb, p);
+    launch_k(tc_gemm_kernel<BN, STAGES>, dim3(grid), dim3(kThreads), L::SMEM, st, ta, tb, p);
   }
   MLP_CHECK(launch_status());
   if (p.splits > 1) {
@@ -525,7 +530,7 @@ mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const TcParam
     long long blocks = (quads + 255) / 256;
     if (blocks > (long long)num_sms() * 8) blocks = (long long)num_sms() * 8;
     LaunchScope ls("splitk_reduce", st, p.M, p.N, p.splits);
-    splitk_reduce_kernel<<<(int)blocks, 256, 0, st>>>(p);
+    launch_k(splitk_reduce_kernel, dim3((int)blocks), dim3(256), 0, st, p);
     return launch_status();
   }
   return MLP_OK;
