@@ -96,6 +96,7 @@ namespace {
 inline cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline int round8(int x) { return (x + 7) / 8 * 8; }
+inline int round64(int x) { return (x + 63) / 64 * 64; }
 
 // ------------------------------------------------------------ GEMM checks
 
@@ -271,7 +272,8 @@ struct mlp_handle {
   std::vector<long long> w_off, b_off, shadow_off;
   std::vector<int> out_pad;        // shadow row pitch per layer
   // Layer inputs (X and every hidden activation) are stored with one extra
-  // column of ones after the features (ld = round8(width + 1)): the
+  // column of ones after the features (ld = width + 1 rounded up to 64
+  // elements, so rows start on 128-byte lines for the TMA tiles): the
   // weight-gradient GEMM over [In | 1] then yields [dW; db], which is exactly
   // the flat layout of W followed by b.
   std::vector<int> act_ld;         // act_ld[l]: pitch of layer l's input buffer
@@ -309,14 +311,14 @@ Plan plan(const int* dims, int n_dims, int max_batch, int prec) {
   const int L = n_dims - 1;
   const size_t B = (size_t)max_batch;
   const int e = esz(prec);
-  p.x = align256(B * round8(dims[0] + 1) * e);
+  p.x = align256(B * round64(dims[0] + 1) * e);
   p.acts_total = 0;
   int maxh = 8;
   for (int l = 1; l < L; ++l) {
-    p.acts_total += align256(B * round8(dims[l] + 1) * e);
-    if (round8(dims[l] + 1) > maxh) maxh = round8(dims[l] + 1);
+    p.acts_total += align256(B * round64(dims[l] + 1) * e);
+    if (round64(dims[l] + 1) > maxh) maxh = round64(dims[l] + 1);
   }
-  if (round8(dims[0] + 1) > maxh) maxh = round8(dims[0] + 1);
+  if (round64(dims[0] + 1) > maxh) maxh = round64(dims[0] + 1);
   p.logits = align256(B * dims[L] * sizeof(float));
   p.dlogits = align256(B * round8(dims[L]) * e);
   p.dh = align256(B * maxh * e);
@@ -562,7 +564,7 @@ mlp_status mlp_create(const int* dims, int n_dims, int hidden_act, int prec, int
     h->out_pad.push_back(round8(dims[l + 1]));
     soff += (long long)dims[l] * round8(dims[l + 1]);
   }
-  for (int l = 0; l < h->L; ++l) h->act_ld.push_back(round8(dims[l] + 1));
+  for (int l = 0; l < h->L; ++l) h->act_ld.push_back(round64(dims[l] + 1));
   // segment map for the fused SGD + shadow refresh
   h->segs.n = 2 * h->L;
   for (int l = 0; l < h->L; ++l) {

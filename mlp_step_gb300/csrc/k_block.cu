@@ -37,8 +37,8 @@ constexpr int DM = 512;                 // model width
 constexpr int HC = 128;                 // hidden chunk
 constexpr int YH = 256;                 // output columns per CTA of the pair
 constexpr int F_STAGES = 3;
-constexpr int F_SLOTS = 4;                // two activation slots per CTA of the pair
-constexpr int F_STAGE_BYTES = 32768;
+constexpr int F_SLOTS = 2;                // one activation slot per CTA of the pair
+constexpr int F_STAGE_BYTES = 49152;      // x k-block + two W_gate chunks' k-blocks
 constexpr int F_SLOT_BYTES = TM * HC * 2;  // 32 KiB bf16 activation chunk
 constexpr int F_SMEM = 1024 + F_SLOTS * F_SLOT_BYTES + F_STAGES * F_STAGE_BYTES + 2 * TM * 4 + 512;
 constexpr int kThreads = 192;
@@ -64,18 +64,27 @@ struct FwdParams {
 
 constexpr int F_THREADS = 320;  // 10 warps
 
-// MMA issue order of one tile for a CTA that owns n_own gate chunks:
-// G0, then groups (G_g, D_{2g-2}, D_{2g-1}) for g = 1 .. n_own-1, then the last
-// two down chunks -- 3 n_own operations.  op >= 0: gate chunk j = op;
-// op < 0: down chunk c = -op - 1.
-__device__ __forceinline__ int fwd_op(int i, int n_own) {
-  if (i == 0) return 0;
-  const int tail = 3 * n_own - 2;
-  if (i >= tail) return -(2 * n_own - 2 + (i - tail)) - 1;
-  const int g = (i - 1) / 3 + 1;
-  const int r = (i - 1) % 3;
-  if (r == 0) return g;
-  return -(2 * (g - 1) + (r - 1)) - 1;
+// MMA issue order of one tile for a CTA that owns n_own gate chunks (its
+// chunks c = 2 j + rank, j = 0 .. n_own-1).  Gate chunks go in pairs: one
+// N = 256 pass computes chunks j = 2p and 2p+1 into the two adjacent gate
+// accumulators (operand reads per FLOP halve against two N = 128 passes),
+// followed by the four down chunks c = 4p .. 4p+3 that those pairs of both
+// CTAs feed.  An odd last chunk runs alone (N = 128).
+enum : int { OP_GATE_PAIR = 0, OP_GATE = 1, OP_DOWN = 2 };
+struct FwdOp {
+  int kind, idx;
+};
+__device__ __forceinline__ int fwd_n_ops(int n_own) { return 5 * (n_own / 2) + 3 * (n_own & 1); }
+__device__ __forceinline__ FwdOp fwd_op(int i, int n_own) {
+  const int n_gp = n_own / 2;
+  if (i < 5 * n_gp) {
+    const int pr = i / 5, r = i % 5;
+    if (r == 0) return {OP_GATE_PAIR, pr};
+    return {OP_DOWN, 4 * pr + r - 1};
+  }
+  const int r = i - 5 * n_gp;
+  if (r == 0) return {OP_GATE, n_own - 1};
+  return {OP_DOWN, 2 * (n_own - 1) + r - 1};
 }
 
 __device__ __forceinline__ float sumsq_bf16x8(const uint4& v) {
@@ -129,22 +138,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  // activation slots: chunk c lives in slot 2 * (c % 2) + (c / 2) % 2, i.e.
-  // each CTA of the pair owns two slots (its chunks alternate between them)
+  // activation slots: chunk c lives in slot c % 2, the slot of its owner
   uint8_t* slots = smem;                                   // F_SLOTS x 32 KiB
-  uint8_t* stages = smem + F_SLOTS * F_SLOT_BYTES;         // F_STAGES x 32 KiB
+  uint8_t* stages = smem + F_SLOTS * F_SLOT_BYTES;         // F_STAGES x 48 KiB
   float* rbuf = reinterpret_cast<float*>(stages + F_STAGES * F_STAGE_BYTES);  // [2][TM]
   uint64_t* full = reinterpret_cast<uint64_t*>(rbuf + 2 * TM);
   uint64_t* empty = full + F_STAGES;
   uint64_t* ufull = empty + F_STAGES;    // [2] gate accumulator ready
   uint64_t* uempty = ufull + 2;          // [2] gate accumulator drained (128 arrivals)
-  uint64_t* afull = uempty + 2;          // [4] activation slot written (128 arrivals)
-  uint64_t* aempty = afull + F_SLOTS;    // [4] slot consumed by both CTAs (2 arrivals)
+  uint64_t* afull = uempty + 2;          // [2] activation slot filled (1 arrival + copy bytes)
+  uint64_t* aempty = afull + F_SLOTS;    // [2] slot consumed by both CTAs (2 arrivals)
   uint64_t* rready = aempty + F_SLOTS;   // [2] row scales of a tile in rbuf (128 arrivals)
   uint64_t* yfull = rready + 2;
   uint64_t* yempty = yfull + 1;          // 128 arrivals
   uint64_t* done = yempty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* awritten = done + 1;         // chunk stored in this CTA's slot (128 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(awritten + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -152,7 +161,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
   const uint32_t peer = rank ^ 1u;
   const int cluster = blockIdx.x >> 1;
   const int n_clusters = gridDim.x >> 1;
-  const int n_ops = 3 * p.n_own;
+  const int n_ops = fwd_n_ops(p.n_own);
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < F_STAGES; ++s) {
@@ -165,12 +174,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
       ptx::mbar_init(&rready[b], 128);
     }
     for (int s2 = 0; s2 < F_SLOTS; ++s2) {
-      ptx::mbar_init(&afull[s2], 128);
+      ptx::mbar_init(&afull[s2], 1);
       ptx::mbar_init(&aempty[s2], 2);
     }
     ptx::mbar_init(yfull, 1);
     ptx::mbar_init(yempty, 128);
     ptx::mbar_init(done, 1);
+    ptx::mbar_init(awritten, 128);
     *s_abort = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tensormap(&tmX);
@@ -197,8 +207,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
       bool ok = true;
       for (int t = cluster; t < p.tiles && ok && !*s_abort; t += n_clusters) {
         for (int i = 0; i < n_ops && ok; ++i) {
-          const int op = fwd_op(i, p.n_own);
-          const int nkb = op >= 0 ? DM / 64 : HC / 64;
+          const FwdOp op = fwd_op(i, p.n_own);
+          const int nkb = op.kind == OP_DOWN ? HC / 64 : DM / 64;
+          const uint32_t bytes = op.kind == OP_GATE_PAIR ? 49152u : 32768u;
           for (int kb = 0; kb < nkb; ++kb) {
             if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
                                         DEVERR_TIMEOUT_PRODUCER)) {
@@ -206,20 +217,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
               ok = false;
               break;
             }
-            ptx::mbar_arrive_expect_tx(&full[stage], F_STAGE_BYTES);
+            ptx::mbar_arrive_expect_tx(&full[stage], bytes);
             last_parity[stage] = (int)phase;
             uint8_t* st = stages + stage * F_STAGE_BYTES;
-            if (op >= 0) {
-              const int c = 2 * op + (int)rank;
-              ptx::tma_load_2d(st, &tmX, &full[stage], kb * 64, t * TM);
-              ptx::tma_load_2d(st + 16384, &tmWg, &full[stage], c * HC, kb * 64);
-              ptx::tma_load_2d(st + 24576, &tmWg, &full[stage], c * HC + 64, kb * 64);
-            } else {
-              const int c = -op - 1;
+            if (op.kind == OP_DOWN) {
+              const int c = op.idx;
 #pragma unroll
               for (int j = 0; j < YH / 64; ++j)
                 ptx::tma_load_2d(st + j * 8192, &tmWd, &full[stage], (int)rank * YH + j * 64,
                                  c * HC + kb * 64);
+            } else {
+              ptx::tma_load_2d(st, &tmX, &full[stage], kb * 64, t * TM);
+              // chunk(s) c = 2 j + rank: one for a single gate, j = 2p, 2p+1 for a pair
+              const int j0 = op.kind == OP_GATE_PAIR ? 2 * op.idx : op.idx;
+              const int nch = op.kind == OP_GATE_PAIR ? 2 : 1;
+              for (int q = 0; q < nch; ++q) {
+                const int c = 2 * (j0 + q) + (int)rank;
+                ptx::tma_load_2d(st + 16384 + q * 16384, &tmWg, &full[stage], c * HC, kb * 64);
+                ptx::tma_load_2d(st + 24576 + q * 16384, &tmWg, &full[stage], c * HC + 64,
+                                 kb * 64);
+              }
             }
             if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
           }
@@ -230,21 +247,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc_g = ptx::idesc_bf16_f32(TM, HC, 0, 1);
+      const uint32_t idesc_gp = ptx::idesc_bf16_f32(TM, 2 * HC, 0, 1);
       const uint32_t idesc_d = ptx::idesc_bf16_f32(TM, YH, 0, 1);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t ucount[2] = {0, 0}, acount[F_SLOTS] = {0, 0, 0, 0}, ycount = 0;
+      uint32_t ucount[2] = {0, 0}, acount[F_SLOTS] = {0, 0}, ycount = 0;
       bool ok = true;
       for (int t = cluster; t < p.tiles && ok && !*s_abort; t += n_clusters) {
         for (int i = 0; i < n_ops && ok; ++i) {
-          const int op = fwd_op(i, p.n_own);
-          if (op >= 0) {
-            const int b = op & 1;
-            if (!ptx::mbar_wait_bounded(&uempty[b], (ucount[b] & 1) ^ 1, p.wait_ns, p.err,
-                                        DEVERR_TIMEOUT_MMA)) { ok = false; break; }
-            ++ucount[b];
+          const FwdOp op = fwd_op(i, p.n_own);
+          if (op.kind != OP_DOWN) {
+            // gate accumulators: a pair fills both, a single gate fills j % 2
+            const bool pair = op.kind == OP_GATE_PAIR;
+            const int b0 = pair ? 0 : (op.idx & 1);
+            const int nb = pair ? 2 : 1;
+            for (int q = 0; q < nb && ok; ++q) {
+              const int b = b0 + q;
+              if (!ptx::mbar_wait_bounded(&uempty[b], (ucount[b] & 1) ^ 1, p.wait_ns, p.err,
+                                          DEVERR_TIMEOUT_MMA)) { ok = false; break; }
+              ++ucount[b];
+            }
+            if (!ok) break;
             ptx::tc_fence_after();
-            const uint32_t d = tmem + 256 + b * HC;
+            const uint32_t d = tmem + 256 + b0 * HC;
+            const uint32_t idesc = pair ? idesc_gp : idesc_g;
             for (int kb = 0; kb < DM / 64; ++kb) {
               if (!ptx::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err,
                                           DEVERR_TIMEOUT_MMA)) { ok = false; break; }
@@ -254,16 +280,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
               for (int k = 0; k < 4; ++k) {
                 const uint64_t ad = ptx::sw128_desc(sa + k * 32, 16, 1024);
                 const uint64_t bd = ptx::sw128_desc(sa + 16384 + k * 2048, 8192, 1024);
-                ptx::mma_bf16(d, ad, bd, idesc_g, (kb > 0 || k > 0) ? 1u : 0u);
+                ptx::mma_bf16(d, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
               }
               ptx::mma_commit(&empty[stage]);
               if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
-            ptx::mma_commit(&ufull[b]);
+            for (int q = 0; q < nb; ++q) ptx::mma_commit(&ufull[b0 + q]);
           } else {
-            const int c = -op - 1;
-            const int s = 2 * (c & 1) + ((c >> 1) & 1);
+            const int c = op.idx;
+            const int s = c & 1;
             if (c == 0) {
               if (!ptx::mbar_wait_bounded(yempty, (ycount & 1) ^ 1, p.wait_ns, p.err,
                                           DEVERR_TIMEOUT_MMA)) { ok = false; break; }
@@ -290,8 +316,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
             }
             if (!ok) break;
             // slot s is reusable once both CTAs' MMAs that read it are done;
-            // its owner (CTA c % 2) waits for that
-            ptx::mma_commit_multicast(&aempty[s], (uint16_t)(1u << (c & 1)));
+            // its owner (CTA s) waits for that
+            ptx::mma_commit_multicast(&aempty[s], (uint16_t)(1u << s));
             if (c == 2 * p.n_own - 1) ptx::mma_commit(yfull);
           }
         }
@@ -305,7 +331,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    uint32_t uc[2] = {0, 0}, ac[2] = {0, 0};
+    uint32_t uc[2] = {0, 0}, ac = 0, wc = 0;
     bool ok = true;
     int it = 0;
     for (int t = cluster; t < p.tiles && ok; t += n_clusters, ++it) {
@@ -318,14 +344,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
         if (!ptx::mbar_wait_bounded(&ufull[b], uc[b] & 1, p.wait_ns, p.err,
                                     DEVERR_TIMEOUT_EPILOGUE)) { ok = false; break; }
         ++uc[b];
-        // own chunk c = 2 j + rank goes to slot 2 rank + (j % 2)
-        const int sub = j & 1;
-        const int sl = 2 * (int)rank + sub;
-        if (!ptx::mbar_wait_bounded(&aempty[sl], (ac[sub] & 1) ^ 1, p.wait_ns, p.err,
+        // own chunk c = 2 j + rank goes to this CTA's slot
+        const int sl = (int)rank;
+        if (!ptx::mbar_wait_bounded(&aempty[sl], (ac & 1) ^ 1, p.wait_ns, p.err,
                                     DEVERR_TIMEOUT_EPILOGUE)) { ok = false; break; }
-        ++ac[sub];
+        ++ac;
         const uint32_t my_slot_addr = ptx::smem_u32(slots + sl * F_SLOT_BYTES);
-        const uint32_t peer_slot_addr = ptx::mapa_shared(my_slot_addr, peer);
         ptx::tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < HC / 32; ++cc) {
@@ -349,16 +373,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
             const int j16 = (cc & 1) * 4 + q;
             const uint32_t off =
                 (uint32_t)(kb * 16384 + row * 128 + ((j16 ^ (row & 7)) << 4));
-            const uint4 w = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            ptx::st_shared_v4(my_slot_addr + off, w);
-            ptx::st_cluster_v4(peer_slot_addr + off, w);
+            ptx::st_shared_v4(my_slot_addr + off,
+                              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
           }
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(&uempty[b]);
-        ptx::fence_proxy_async_cluster();
-        ptx::mbar_arrive(&afull[sl]);
-        ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(&afull[sl]), peer));
+        // the chunk is complete in this CTA once all 128 writers are past
+        // this point; one thread then publishes it locally and sends a copy
+        // to the peer's slot (the copy's bytes complete the peer's barrier)
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(awritten);
+        if (warp == 2 && lane == 0) {
+          // on a timeout the chunk is not published; the peer and the MMA
+          // warp then give up on their own bounded waits
+          if (!ptx::mbar_wait_bounded(awritten, wc & 1, p.wait_ns, p.err,
+                                      DEVERR_TIMEOUT_EPILOGUE)) {
+            *s_abort = 1;
+          } else {
+          ptx::mbar_arrive(&afull[sl]);
+          const uint32_t peer_bar = ptx::mapa_shared(ptx::smem_u32(&afull[sl]), peer);
+          ptx::mbar_arrive_expect_tx_remote(peer_bar, (uint32_t)F_SLOT_BYTES);
+          ptx::bulk_copy_to_peer(ptx::mapa_shared(my_slot_addr, peer), my_slot_addr,
+                                 (uint32_t)F_SLOT_BYTES, peer_bar);
+          }
+        }
+        ++wc;
       }
     }
     if (!ok) *s_abort = 1;

@@ -268,7 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* xent_bar = done + 1;   // the four epilogue warps' loss partials are in xent_part
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xent_bar + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -284,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&tempty[a], 4);
     }
     ptx::mbar_init(done, 1);
+    ptx::mbar_init(xent_bar, 4);
     *s_abort = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tensormap(&tmA);
@@ -440,9 +442,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v = m < p.M ? row_loss : 0.f;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) xent_part[quarter] = v;
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (warp == 2 && lane == 0)
+        if (lane == 0) {
+          xent_part[quarter] = v;
+          ptx::mbar_arrive(xent_bar);
+        }
+        if (warp == 2 && lane == 0 &&
+            ptx::mbar_wait_bounded(xent_bar, 0, p.wait_ns, p.err, DEVERR_TIMEOUT_EPILOGUE))
           *p.xent_loss = (((xent_part[0] + xent_part[1]) + xent_part[2]) + xent_part[3]) /
                          (float)p.xent_norm;
       }

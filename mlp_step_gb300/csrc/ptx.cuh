@@ -138,6 +138,27 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Arrive on a peer CTA's mbarrier and raise its expected transaction bytes.
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_addr, uint32_t tx) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+          cluster_addr),
+      "r"(tx)
+      : "memory");
+}
+
+// Asynchronous bulk copy of `bytes` (multiple of 16) from this CTA's shared
+// memory into another CTA's shared memory; completes as transaction bytes on
+// the destination CTA's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster_addr, uint32_t src_addr,
+                                                  uint32_t bytes, uint32_t mbar_cluster_addr) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cluster_addr),
+      "r"(src_addr), "r"(bytes), "r"(mbar_cluster_addr)
+      : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
