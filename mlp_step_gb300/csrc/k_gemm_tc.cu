@@ -22,6 +22,9 @@
 // Two accumulators (2 x BN tensor-memory columns) let the epilogue of tile i
 // overlap the MMAs of tile i+1.  Every mbarrier wait is bounded; a timeout is
 // recorded in the device error word and the CTA winds down cleanly.
+#include <cstdlib>
+#include <cstring>
+
 #include "kernels.cuh"
 #include "ptx.cuh"
 #include "trace.cuh"
@@ -63,6 +66,7 @@ struct TcParams {
   float sgd_lr, sgd_mom;
   __nv_bfloat16* sgd_shadow;
   int sgd_ld_shadow, sgd_shadow_rows;
+  int tma_store;  // epilogue writes C through the tmC tensor map
 };
 
 template <int BN, int STAGES>
@@ -70,8 +74,14 @@ struct Layout {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  // barriers (256 B, padded to keep what follows 1024-aligned), then the
+  // optional epilogue staging for TMA stores: per epilogue warp two 32 x 32
+  // buffers of up to 4 KiB (fp32); launches without TMA stores do not
+  // allocate it, which leaves more of the SM's memory to L1.
+  static constexpr int BAR_BYTES = 1024;
+  static constexpr int STG_BYTES = 4 * 2 * 4096;
+  static constexpr int SMEM_BASE = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int SMEM = SMEM_BASE + STG_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
 };
 
@@ -87,10 +97,10 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = r / gm;
 }
 
-template <int BN>
-__device__ __forceinline__ void epilogue_chunk(const TcParams& p, int m, int n0,
-                                               const uint32_t (&r)[32]) {
-  float v[32];
+// Epilogue arithmetic of one 32-column piece of row m in fp32: + bias,
+// ReLU, ReLU mask (keep where the stored activation is > 0).
+__device__ __forceinline__ void epilogue_values(const TcParams& p, int m, int n0,
+                                                const uint32_t (&r)[32], float (&v)[32]) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
   const bool full = (n0 + 32 <= p.N);
@@ -103,7 +113,7 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, int m, int n0,
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j], 0.f);
   }
-  if (p.mask) {
+  if (p.mask && m < p.M) {
     const __nv_bfloat16* mrow = p.mask + (size_t)m * p.ldm + n0;
     if (full && ((reinterpret_cast<uintptr_t>(mrow) & 15) == 0)) {
 #pragma unroll
@@ -119,6 +129,12 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, int m, int n0,
         if (n0 + j < p.N) v[j] = bf16_to_f32(mrow[j]) > 0.f ? v[j] : 0.f;
     }
   }
+}
+
+// Register store of one piece (outputs whose rows are not 16-byte aligned).
+__device__ __forceinline__ void epilogue_store_regs(const TcParams& p, int m, int n0,
+                                                    const float (&v)[32]) {
+  const bool full = (n0 + 32 <= p.N);
   if (p.c_bf16) {
     __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(p.C) + (size_t)m * p.ldc + n0;
     if (full && ((reinterpret_cast<uintptr_t>(crow) & 15) == 0)) {
@@ -148,6 +164,32 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, int m, int n0,
       for (int j = 0; j < 32; ++j)
         if (n0 + j < p.N) crow[j] = v[j];
     }
+  }
+}
+
+// Row `lane` of a warp's 32 x 32 staging box, in the swizzled layout the
+// output tensor map uses: 16-byte chunk q of a row is stored at chunk
+// q ^ (lane & 7) for fp32 (128-byte rows, 128-byte swizzle) and at
+// q ^ ((lane >> 1) & 3) for bf16 (64-byte rows, 64-byte swizzle).
+__device__ __forceinline__ void epilogue_stage_row(uint8_t* box, int c_bf16, int lane,
+                                                   const float (&v)[32]) {
+  if (c_bf16) {
+    uint8_t* row = box + lane * 64;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 o;
+      o.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+      o.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+      o.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+      o.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+      *reinterpret_cast<uint4*>(row + ((q ^ ((lane >> 1) & 3)) << 4)) = o;
+    }
+  } else {
+    uint8_t* row = box + lane * 128;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float4*>(row + ((q ^ (lane & 7)) << 4)) =
+          make_float4(v[q * 4 + 0], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
   }
 }
 
@@ -255,7 +297,7 @@ __device__ __forceinline__ float xent_epilogue_row(const TcParams& p, int m,
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   using L = Layout<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ float xent_part[4];
@@ -264,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * L::A_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * L::B_BYTES);
+  uint8_t* stg = sB + STAGES * L::B_BYTES + L::BAR_BYTES;  // epilogue staging (1024-aligned)
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -290,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
     ptx::prefetch_tensormap(&tmA);
     ptx::prefetch_tensormap(&tmB);
+    if (p.tma_store) ptx::prefetch_tensormap(&tmC);
   }
   if (warp == 1) ptx::tmem_alloc(tmem_slot, L::TMEM_COLS);
   ptx::tc_fence_before();
@@ -394,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    int stg_count = 0;  // staged boxes issued by this warp
     for (int u = blockIdx.x; u < p.num_tiles * p.splits; u += gridDim.x) {
       if (*s_abort) break;
       if (!ptx::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err, DEVERR_TIMEOUT_EPILOGUE)) {
@@ -431,9 +476,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             row_loss = xent_epilogue_row(p, m, r);
           } else if (p.sgd_w) {
             sgd_epilogue_chunk(p, m, n0, r);
-          } else {
-            epilogue_chunk<BN>(p, m, n0, r);
+          } else if (!p.tma_store) {
+            float v[32];
+            epilogue_values(p, m, n0, r, v);
+            epilogue_store_regs(p, m, n0, v);
           }
+        }
+        if (p.tma_store) {
+          // all lanes take part: rows past M are staged too and clipped by TMA
+          float v[32];
+          epilogue_values(p, m, n0, r, v);
+          uint8_t* box = stg + (warp - 2) * 8192 + (stg_count & 1) * 4096;
+          if (stg_count >= 2) {
+            if (lane == 0) ptx::bulk_wait_group_read<1>();
+            __syncwarp();
+          }
+          epilogue_stage_row(box, p.c_bf16, lane, v);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&tmC, box, n0, tm * BM + quarter * 32);
+            ptx::bulk_commit_group();
+          }
+          ++stg_count;
         }
       }
       if (p.xent_labels) {
@@ -456,6 +521,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
+    // the bulk stores must finish before the CTA (and its shared memory) ends
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
   }
 
   __syncwarp();
@@ -509,8 +577,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const TcParams p) {
 }
 
 template <int BN, int STAGES>
-mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
-                     cudaStream_t st) {
+mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                     const TcParams& p, cudaStream_t st) {
   using L = Layout<BN, STAGES>;
   static bool configured = false;
   if (!configured) {
@@ -527,7 +595,8 @@ mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const TcParam
                                          "gemm_tc_splitk_bn256"};
     const int which = BN == 64 ? 0 : (BN == 128 ? 1 : 2);
     LaunchScope ls(p.splits > 1 ? split_names[which] : names[which], st, p.M, p.N, p.K);
-    launch_k(tc_gemm_kernel<BN, STAGES>, dim3(grid), dim3(kThreads), L::SMEM, st, ta, tb, p);
+    launch_k(tc_gemm_kernel<BN, STAGES>, dim3(grid), dim3(kThreads),
+             p.tma_store ? L::SMEM : L::SMEM_BASE, st, ta, tb, tc, p);
   }
   MLP_CHECK(launch_status());
   if (p.splits > 1) {
@@ -643,10 +712,26 @@ mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStr
     ok = encode_tmap_bf16_2d(&tb, g.B, g.N, g.K, (unsigned long long)g.ldb * 2, 64, 64);
   if (!ok) return MLP_ERR_CUDA;
 
+  // Output through TMA stores when the output is large (for small outputs the
+  // staging round trip costs more latency than it saves), rows are 16-byte
+  // aligned and no fused epilogue writes extra tensors.
+  CUtensorMap tc;
+  memset(&tc, 0, sizeof(tc));
+  const int esz = g.c_bf16 ? 2 : 4;
+  p.tma_store = 0;
+  if (!p.xent_labels && !p.sgd_w && splits == 1 && (long long)g.M * g.N >= (1ll << 20) &&
+      ((long long)g.ldc * esz) % 16 == 0 && aligned16(g.C)) {
+    if (!encode_tmap_out_2d(&tc, g.C, g.c_bf16 ? 0 : 1, g.N, g.M,
+                            (unsigned long long)g.ldc * esz, 32, 32))
+      return MLP_ERR_CUDA;
+    p.tma_store = 1;
+  }
+  // short, narrow problems (the 784-256-10 step) need few stages
+  if (BN == 64 && p.k_blocks <= 16) return launch_bn<64, 4>(ta, tb, tc, p, st);
   switch (BN) {
-    case 64: return launch_bn<64, 8>(ta, tb, p, st);
-    case 128: return launch_bn<128, 6>(ta, tb, p, st);
-    default: return launch_bn<256, 4>(ta, tb, p, st);
+    case 64: return launch_bn<64, 8>(ta, tb, tc, p, st);
+    case 128: return launch_bn<128, 6>(ta, tb, tc, p, st);
+    default: return launch_bn<256, 4>(ta, tb, tc, p, st);
   }
 }
 

@@ -102,5 +102,10 @@ unsigned long long wait_limit_ns();
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, unsigned long long inner,
                          unsigned long long outer, unsigned long long row_stride_bytes,
                          unsigned box_inner, unsigned box_outer);
+// Same for an output tile map: bf16 (64-byte swizzle) or fp32 (128-byte
+// swizzle) elements, box [box_outer][box_inner].
+bool encode_tmap_out_2d(CUtensorMap* map, const void* base, int fp32, unsigned long long inner,
+                        unsigned long long outer, unsigned long long row_stride_bytes,
+                        unsigned box_inner, unsigned box_outer);
 
 }  // namespace mlp
