@@ -195,6 +195,17 @@ def test_gemm_bf16_tc_epilogues(bias, act, mask, out_bf16):
         assert np.all(got[bf16_values(mk) <= 0] == 0)
 
 
+@pytest.mark.parametrize("out_bf16", [False, True])
+@pytest.mark.parametrize("shape", [(1100, 1000, 136), (1029, 1032, 64)])
+def test_gemm_bf16_tc_large_ragged_outputs(shape, out_bf16):
+    # outputs of a million elements or more leave through TMA bulk stores;
+    # the ragged last tiles must be clipped exactly
+    M_, N, K = shape
+    got, ref = _tc_case(M_, N, K, 0, 0, bias=True, act=M.MLP_ACT_RELU, out_bf16=out_bf16)
+    assert np.all(np.isfinite(got)), "unwritten outputs"
+    assert rel_to_max(got, ref) <= (8e-3 if out_bf16 else 1e-5)
+
+
 def test_gemm_bf16_tc_k_zero_gives_bias():
     N = 24
     bias = synth.normal_f32((N,), synth.STREAM_GENERIC + 5)
