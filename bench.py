@@ -628,6 +628,26 @@ def kernel_profile(wl, steps):
     return rep
 
 
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary under profiles/, if it
+    was captured on the kernel source that is built now (else None)."""
+    import glob
+    import hashlib
+    src = os.path.join(ROOT, "mlp_step_gb300", "csrc", "k_gemm_tc.cu" if kernel.startswith("gemm")
+                       else "k_block.cu")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    for f in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        for line in open(f):
+            parts = line.split()
+            if len(parts) == 5 and parts[0] == "traffic:" and parts[1] == kernel and \
+                    parts[2] == workload and parts[4] == sha:
+                return float(parts[3])
+    return None
+
+
 def roofline_entry(rep, peaks, peaks_kind, sustained=False):
     if not rep:
         return None
@@ -707,6 +727,8 @@ def run_ours(args, wl):
     peaks, peaks_kind = load_peaks()
     rep = kernel_profile(wl, max(3, min(args.steps, 20)))
     roof = roofline_entry(rep, peaks, peaks_kind)
+    if roof is not None:
+        roof["traffic"] = recorded_traffic(roof["kernel"], wl.name)
 
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": wl.unit, "n_gpus": world,
