@@ -200,6 +200,7 @@ class MLP784Epoch(Workload):
         self.prec_name = prec_name
         self.n_images = n_images
         self.batch = batch
+        self.n_steps = (n_images + batch - 1) // batch
         self.samples_per_step = n_images
         self.config = {"workload": "784-256-10 MLP, ReLU hidden, %s operands, fp32 accumulation "
                                    "and master weights; one epoch = %d synthetic images "
@@ -685,6 +686,17 @@ def roofline_entry(rep, peaks, peaks_kind, sustained=False):
             "work_per_launch": per_launch}
 
 
+def max_over_ranks(dist, values, device="cpu"):
+    """Element-wise maximum of a list of floats over all ranks (the timing
+    contract takes the slowest replica); identity without a process group."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def run_ours(args, wl):
     import torch
     rank, world, local = rank_info()
@@ -715,10 +727,9 @@ def run_ours(args, wl):
     e2e_ms = timed_loop(wl.step_e2e, args.steps, flush, sync_barrier)
     wl.check()
 
-    if dist is not None:
-        t = torch.tensor([dev_ms, e2e_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dev_ms, e2e_ms = float(t[0]), float(t[1])
+    dev_ms, e2e_ms = max_over_ranks(dist, [dev_ms, e2e_ms],
+                                    device="cuda" if dist is not None and
+                                    dist.get_backend() == "nccl" else "cpu")
 
     ms_per_step = dev_ms / args.steps
     value = wl.samples_per_step * world / (ms_per_step * 1e-3)
@@ -788,7 +799,8 @@ def main():
     ap.add_argument("--workload", default="mlp784_epoch", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--ref-seconds", type=float, default=2.0)
+    ap.add_argument("--ref-seconds", type=float, default=1.0,
+                    help="CPU seconds of oracle work per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens (block, stack) or batch (mlp_wide): smaller profiling cases")
