@@ -97,17 +97,54 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = r / gm;
 }
 
-// Epilogue arithmetic of one 32-column piece of row m in fp32: + bias,
-// ReLU, ReLU mask (keep where the stored activation is > 0).
+// Bias of columns [n0, n0 + 32) staged in a warp's 32-float shared-memory
+// slot (0 past N): one coalesced load per piece instead of 32 broadcast
+// loads per thread.  Called by the whole warp at a warp-uniform point.
+__device__ __forceinline__ const float* stage_bias(const TcParams& p, int n0, float* slot,
+                                                   int lane) {
+  if (!p.bias) return nullptr;
+  __syncwarp();  // the previous piece's readers are done with the slot
+  slot[lane] = n0 + lane < p.N ? __ldg(p.bias + n0 + lane) : 0.f;
+  __syncwarp();
+  return slot;
+}
+
+// The ReLU-mask piece of row m, columns [n0, n0 + 32), loaded ahead of the
+// accumulator read so that its latency overlaps the tensor-memory load
+// (vector form only for whole, 16-byte aligned pieces).
+struct MaskPiece {
+  uint4 q[4];
+  int vec;
+};
+
+__device__ __forceinline__ void load_mask(const TcParams& p, int m, int n0, MaskPiece& mp) {
+  mp.vec = 0;
+  if (!p.mask || m >= p.M) return;
+  const __nv_bfloat16* mrow = p.mask + (size_t)m * p.ldm + n0;
+  if (n0 + 32 <= p.N && ((reinterpret_cast<uintptr_t>(mrow) & 15) == 0)) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mp.q[q] = __ldg(reinterpret_cast<const uint4*>(mrow) + q);
+    mp.vec = 1;
+  }
+}
+
+// Epilogue arithmetic of one 32-column piece of row m in fp32: + bias (from
+// the staged slot, if any), ReLU, ReLU mask (keep where the stored
+// activation is > 0).
 __device__ __forceinline__ void epilogue_values(const TcParams& p, int m, int n0,
-                                                const uint32_t (&r)[32], float (&v)[32]) {
+                                                const uint32_t (&r)[32], const float* sb,
+                                                const MaskPiece& mp, float (&v)[32]) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  const bool full = (n0 + 32 <= p.N);
-  if (p.bias) {
+  if (sb) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (full || n0 + j < p.N) v[j] += __ldg(p.bias + n0 + j);
+    for (int q = 0; q < 8; ++q) {
+      const float4 b4 = reinterpret_cast<const float4*>(sb)[q];
+      v[4 * q] += b4.x;
+      v[4 * q + 1] += b4.y;
+      v[4 * q + 2] += b4.z;
+      v[4 * q + 3] += b4.w;
+    }
   }
   if (p.act == MLP_ACT_RELU) {
 #pragma unroll
@@ -115,11 +152,10 @@ __device__ __forceinline__ void epilogue_values(const TcParams& p, int m, int n0
   }
   if (p.mask && m < p.M) {
     const __nv_bfloat16* mrow = p.mask + (size_t)m * p.ldm + n0;
-    if (full && ((reinterpret_cast<uintptr_t>(mrow) & 15) == 0)) {
+    if (mp.vec) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint4 mv = __ldg(reinterpret_cast<const uint4*>(mrow) + q);
-        const __nv_bfloat16* mb = reinterpret_cast<const __nv_bfloat16*>(&mv);
+        const __nv_bfloat16* mb = reinterpret_cast<const __nv_bfloat16*>(&mp.q[q]);
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[q * 8 + e] = bf16_to_f32(mb[e]) > 0.f ? v[q * 8 + e] : 0.f;
       }
@@ -314,6 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* xent_bar = done + 1;   // the four epilogue warps' loss partials are in xent_part
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xent_bar + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // per epilogue warp 32 staged bias values, in the upper half of the barrier area
+  float* sbias = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -454,12 +492,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 0; c0 < BN; c0 += 32) {
         const int n0 = tn * BN + c0;
         if (n0 >= p.N) break;  // warp-uniform
+        MaskPiece mp;
+        load_mask(p, m, n0, mp);
         uint32_t r[32];
         __syncwarp();
         ptx::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                     (uint32_t)(acc * BN + c0),
                                 r);
         ptx::tmem_ld_wait();
+        const float* sb = stage_bias(p, n0, sbias + (warp - 2) * 32, lane);
         if (m < p.M) {
           if (part) {
             float* prow = part + (size_t)m * p.ldp + n0;
@@ -470,7 +511,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
             } else {
-              for (int j = 0; j < 32 && n0 + j < p.N; ++j) prow[j] = __uint_as_float(r[j]);
+              // fully unrolled with a predicate: a loop with a data-dependent
+              // trip count would index r[] dynamically and put the whole
+              // accumulator piece in local memory on every path
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (n0 + j < p.N) prow[j] = __uint_as_float(r[j]);
             }
           } else if (p.xent_labels) {
             row_loss = xent_epilogue_row(p, m, r);
@@ -478,14 +524,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             sgd_epilogue_chunk(p, m, n0, r);
           } else if (!p.tma_store) {
             float v[32];
-            epilogue_values(p, m, n0, r, v);
+            epilogue_values(p, m, n0, r, sb, mp, v);
             epilogue_store_regs(p, m, n0, v);
           }
         }
         if (p.tma_store) {
           // all lanes take part: rows past M are staged too and clipped by TMA
           float v[32];
-          epilogue_values(p, m, n0, r, v);
+          epilogue_values(p, m, n0, r, sb, mp, v);
           uint8_t* box = stg + (warp - 2) * 8192 + (stg_count & 1) * 4096;
           if (stg_count >= 2) {
             if (lane == 0) ptx::bulk_wait_group_read<1>();
@@ -542,6 +588,286 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     __syncwarp();
     ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ CTA-pair kernel
+//
+// A 256 x 256 output tile per CTA pair (cluster of 2) with tcgen05.mma.cta_group::2:
+// CTA r of the pair stages rows [128 r, 128 r + 128) of the A tile and columns
+// [128 r, 128 r + 128) of the B tile; the even CTA issues the M = 256, N = 256
+// MMAs, whose operands come from both CTAs' shared memory and whose
+// accumulator rows land in each CTA's own tensor memory (its 128 rows x 256
+// columns, two such buffers).  Per SM that is 32 KiB of operands per 64-wide
+// k-block for 2 x 128 x 256 x 64 flops, a third less shared-memory traffic
+// per flop than a 128 x 256 single-CTA tile, whose operand streams (TMA
+// writes plus MMA reads) otherwise bound the tensor pipe.
+//
+// Barriers: the even CTA's full[s] collects both CTAs' TMA bytes (the odd
+// CTA's loads signal it across the pair); the MMA completions of a stage
+// arrive on empty[s] in both CTAs; tfull[a] in both CTAs tells the epilogues
+// an accumulator is ready; the even CTA's tempty[a] counts the eight
+// epilogue warps of the pair that drained it.
+constexpr int BN2 = 256;
+
+template <int STAGES>
+struct Layout2 {
+  static constexpr int A_BYTES = 128 * BK * 2;
+  static constexpr int B_BYTES = 128 * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BAR_BYTES = 1024;
+  static constexpr int STG_BYTES = 4 * 2 * 4096;
+  static constexpr int SMEM_BASE = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int SMEM = SMEM_BASE + STG_BYTES;
+};
+
+template <int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+  using L = Layout2<STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * L::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * L::B_BYTES);
+  uint8_t* stg = sB + STAGES * L::B_BYTES + L::BAR_BYTES;
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* sbias = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+  const int units = p.num_tiles * p.splits;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 8);
+    }
+    ptx::mbar_init(done, 1);
+    *s_abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB);
+    if (p.tma_store) ptx::prefetch_tensormap(&tmC);
+  }
+  if (warp == 1) ptx::tmem_alloc_pair(tmem_slot, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  int last_parity[STAGES];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < STAGES; ++s) last_parity[s] = -1;
+      const uint32_t full0 = ptx::mapa_shared(ptx::smem_u32(full), 0);  // the even CTA's full[]
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int u = pair; u < units && !*s_abort; u += n_pairs) {
+        int tm, tn;
+        tile_coords(u / p.splits, p.tiles_m, p.tiles_n, tm, tn);
+        const int kb0 = (u % p.splits) * p.kb_per_split;
+        const int kb1 = min(p.k_blocks, kb0 + p.kb_per_split);
+        const int m0 = tm * 256 + (int)rank * 128;
+        const int n0 = tn * BN2 + (int)rank * 128;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!ptx::mbar_wait_cluster_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
+                                              DEVERR_TIMEOUT_PRODUCER)) {
+            *s_abort = 1;
+            break;
+          }
+          if (rank == 0) {
+            ptx::mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
+            last_parity[stage] = (int)phase;
+          }
+          const uint32_t bar = full0 + (uint32_t)stage * 8u;
+          const int k0 = kb * BK;
+          uint8_t* a_dst = sA + stage * L::A_BYTES;
+          uint8_t* b_dst = sB + stage * L::B_BYTES;
+          if (!p.a_mn) {
+            ptx::tma_load_2d_pair(a_dst, &tmA, bar, k0, m0);
+          } else {
+            ptx::tma_load_2d_pair(a_dst, &tmA, bar, m0, k0);
+            ptx::tma_load_2d_pair(a_dst + 8192, &tmA, bar, m0 + 64, k0);
+          }
+          if (!p.b_mn) {
+            ptx::tma_load_2d_pair(b_dst, &tmB, bar, k0, n0);
+          } else {
+            ptx::tma_load_2d_pair(b_dst, &tmB, bar, n0, k0);
+            ptx::tma_load_2d_pair(b_dst + 8192, &tmB, bar, n0 + 64, k0);
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = ptx::idesc_bf16_f32(256, BN2, p.a_mn, p.b_mn);
+      const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
+      const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
+      const uint32_t a_kstep = p.a_mn ? 2048u : 32u;
+      const uint32_t b_kstep = p.b_mn ? 2048u : 32u;
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int u = pair; u < units && !*s_abort; u += n_pairs) {
+        if (!ptx::mbar_wait_cluster_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err,
+                                            DEVERR_TIMEOUT_MMA)) {
+          *s_abort = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN2);
+        const int kb0 = (u % p.splits) * p.kb_per_split;
+        const int kb1 = min(p.k_blocks, kb0 + p.kb_per_split);
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!ptx::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err, DEVERR_TIMEOUT_MMA)) {
+            *s_abort = 1;
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_base = ptx::smem_u32(sA + stage * L::A_BYTES);
+          const uint32_t b_base = ptx::smem_u32(sB + stage * L::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = ptx::sw128_desc(a_base + k * a_kstep, a_lbo, 1024);
+            const uint64_t bd = ptx::sw128_desc(b_base + k * b_kstep, b_lbo, 1024);
+            ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit_pair_multicast(&empty[stage], 3);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair_multicast(&tfull[acc], 3);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      ptx::mma_commit_pair_multicast(done, 1);
+      ptx::mbar_wait_bounded(done, 0, p.wait_ns, p.err, DEVERR_TIMEOUT_TEARDOWN);
+    }
+  } else {
+    const int quarter = warp & 3;
+    const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_u32(tempty), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int stg_count = 0;
+    for (int u = pair; u < units; u += n_pairs) {
+      if (*s_abort) break;
+      if (!ptx::mbar_wait_cluster_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err,
+                                          DEVERR_TIMEOUT_EPILOGUE)) {
+        *s_abort = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      int tm, tn;
+      tile_coords(u / p.splits, p.tiles_m, p.tiles_n, tm, tn);
+      float* part = p.splits > 1 ? p.partial + (size_t)(u % p.splits) * p.M * p.ldp : nullptr;
+      const int row0 = tm * 256 + (int)rank * 128 + quarter * 32;  // this warp's first row
+      const int m = row0 + lane;
+      for (int c0 = 0; c0 < BN2; c0 += 32) {
+        const int n0 = tn * BN2 + c0;
+        if (n0 >= p.N) break;  // warp-uniform
+        MaskPiece mp;
+        load_mask(p, m, n0, mp);
+        uint32_t r[32];
+        __syncwarp();
+        ptx::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                    (uint32_t)(acc * BN2 + c0),
+                                r);
+        ptx::tmem_ld_wait();
+        const float* sb = stage_bias(p, n0, sbias + (warp - 2) * 32, lane);
+        if (part) {
+          if (m < p.M) {
+            float* prow = part + (size_t)m * p.ldp + n0;
+            if (n0 + 32 <= p.N) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(prow)[q] =
+                    make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            } else {
+              // fully unrolled with a predicate: a loop with a data-dependent
+              // trip count would index r[] dynamically and put the whole
+              // accumulator piece in local memory on every path
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (n0 + j < p.N) prow[j] = __uint_as_float(r[j]);
+            }
+          }
+        } else if (!p.tma_store) {
+          if (m < p.M) {
+            float v[32];
+            epilogue_values(p, m, n0, r, sb, mp, v);
+            epilogue_store_regs(p, m, n0, v);
+          }
+        } else if (row0 < p.M) {  // warp-uniform; rows past M are clipped by TMA
+          float v[32];
+          epilogue_values(p, m, n0, r, sb, mp, v);
+          uint8_t* box = stg + (warp - 2) * 8192 + (stg_count & 1) * 4096;
+          if (stg_count >= 2) {
+            if (lane == 0) ptx::bulk_wait_group_read<1>();
+            __syncwarp();
+          }
+          epilogue_stage_row(box, p.c_bf16, lane, v);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&tmC, box, n0, row0);
+            ptx::bulk_commit_group();
+          }
+          ++stg_count;
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0) ptx::mbar_arrive(&tempty[acc]);
+        else ptx::mbar_arrive_remote(tempty0 + (uint32_t)acc * 8u);
+      }
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (*s_abort && warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s)
+      if (last_parity[s] >= 0)
+        ptx::mbar_wait_bounded(&full[s], (uint32_t)last_parity[s], p.wait_ns, p.err,
+                               DEVERR_TIMEOUT_TEARDOWN);
+  }
+  __syncwarp();
+  __syncthreads();
+  // neither CTA frees its tensor memory or leaves while the pair's MMAs or
+  // signals may still reach it
+  ptx::cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tmem_dealloc_pair(tmem_base, 512);
   }
 }
 
@@ -610,31 +936,98 @@ mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
   return MLP_OK;
 }
 
-// Split-K plan from the shape alone (so workspace sizes do not depend on the
-// device): only when 128x256 tiles leave most of ~144 SMs idle and K is long.
-void splitk_plan(int M, int N, int K, int* splits, int* kb_per_split) {
-  const int tiles = ((M + BM - 1) / BM) * ((N + 255) / 256);
+template <int STAGES>
+mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                       const TcParams& p, cudaStream_t st) {
+  using L = Layout2<STAGES>;
+  static bool configured = false;
+  static int max_pairs = 0;
+  if (!configured) {
+    if (cudaFuncSetAttribute(tc_gemm_pair_kernel<STAGES>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
+      return MLP_ERR_CUDA;
+    // pairs that fit at once (a GPC with an odd number of free SMs leaves one over)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::SMEM;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<STAGES>, &cfg) != cudaSuccess ||
+        n < 1) {
+      cudaGetLastError();
+      n = num_sms() / 2;
+    }
+    max_pairs = n;
+    configured = true;
+  }
+  const int units = p.num_tiles * p.splits;
+  const int pairs = units < max_pairs ? units : max_pairs;
+  {
+    LaunchScope ls(p.splits > 1 ? "gemm_tc_pair_splitk" : "gemm_tc_pair", st, p.M, p.N, p.K);
+    launch_k(tc_gemm_pair_kernel<STAGES>, dim3(2 * pairs), dim3(kThreads),
+             p.tma_store ? L::SMEM : L::SMEM_BASE, st, ta, tb, tc, p);
+  }
+  MLP_CHECK(launch_status());
+  if (p.splits > 1) {
+    const long long quads = (long long)p.M * (p.ldp / 4);
+    long long blocks = (quads + 255) / 256;
+    if (blocks > (long long)num_sms() * 8) blocks = (long long)num_sms() * 8;
+    LaunchScope ls("splitk_reduce", st, p.M, p.N, p.splits);
+    launch_k(splitk_reduce_kernel, dim3((int)blocks), dim3(256), 0, st, p);
+    return launch_status();
+  }
+  return MLP_OK;
+}
+
+// Kernel choice and split-K plan from the shape alone (so workspace sizes do
+// not depend on the device).  CTA pairs with 256 x 256 tiles whenever both
+// output dimensions exceed 128 and there are enough pair tiles for ~76 pairs,
+// or K is long enough to split; otherwise single-CTA 128 x BN tiles, split
+// only when 128 x 256 tiles leave most of ~144 SMs idle and K is long.
+struct GemmPlan {
+  bool pair;
+  int splits, kb_per_split;
+};
+
+GemmPlan gemm_plan(int M, int N, int K, bool fused) {
+  GemmPlan pl;
   const int kblocks = (K + BK - 1) / BK;
+  pl.pair = false;
   int s = 1;
-  if (tiles < 72 && kblocks >= 64) {
-    s = 144 / tiles;
-    if (s > 16) s = 16;
-    if (s > kblocks / 16) s = kblocks / 16;
-    if (s < 1) s = 1;
+  if (!fused && M > 128 && N > 128) {
+    const int pair_tiles = ((M + 255) / 256) * ((N + BN2 - 1) / BN2);
+    if (pair_tiles >= 48) {
+      pl.pair = true;
+    } else if (kblocks >= 64) {
+      s = 76 / pair_tiles;
+      if (s > 16) s = 16;
+      if (s > kblocks / 16) s = kblocks / 16;
+      if (s >= 2) pl.pair = true;
+      else s = 1;
+    }
+  }
+  if (!pl.pair && !fused) {
+    const int tiles = ((M + BM - 1) / BM) * ((N + 255) / 256);
+    if (tiles < 72 && kblocks >= 64) {
+      s = 144 / tiles;
+      if (s > 16) s = 16;
+      if (s > kblocks / 16) s = kblocks / 16;
+      if (s < 1) s = 1;
+    }
   }
   int per = (kblocks + s - 1) / s;
   s = (kblocks + per - 1) / per;
-  *splits = s;
-  *kb_per_split = per;
+  pl.splits = s;
+  pl.kb_per_split = per;
+  return pl;
 }
 
 }  // namespace
 
 size_t gemm_tc_splitk_bytes(int M, int N, int K) {
-  int s, per;
-  splitk_plan(M, N, K, &s, &per);
-  if (s <= 1) return 0;
-  return (size_t)s * M * ((N + 3) / 4 * 4) * sizeof(float);
+  const GemmPlan pl = gemm_plan(M, N, K, false);
+  if (pl.splits <= 1) return 0;
+  return (size_t)pl.splits * M * ((N + 3) / 4 * 4) * sizeof(float);
 }
 
 mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStream_t st) {
@@ -644,21 +1037,28 @@ mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStr
     return launch_gemm_simt(g, 1, st);
   }
 
-  int splits = 1, kb_per_split = (g.K + BK - 1) / BK;
-  const size_t split_bytes = gemm_tc_splitk_bytes(g.M, g.N, g.K);
-  if (split_bytes > 0 && g.ws && g.ws_bytes >= split_bytes && aligned16(g.ws))
-    splitk_plan(g.M, g.N, g.K, &splits, &kb_per_split);
+  const bool fused = g.xent_labels || g.sgd_w;
+  GemmPlan pl = gemm_plan(g.M, g.N, g.K, fused);
+  if (pl.splits > 1 && !(g.ws && g.ws_bytes >= gemm_tc_splitk_bytes(g.M, g.N, g.K) &&
+                         aligned16(g.ws))) {
+    // no workspace for partial sums: one pass over K (single-CTA tiles when
+    // the pair grid would be too small)
+    pl.splits = 1;
+    pl.kb_per_split = (g.K + BK - 1) / BK;
+    if (((g.M + 255) / 256) * ((g.N + BN2 - 1) / BN2) < 48) pl.pair = false;
+  }
+  const int splits = pl.splits, kb_per_split = pl.kb_per_split;
 
-  const int tiles_m = (g.M + BM - 1) / BM;
+  const int tiles_m = pl.pair ? (g.M + 255) / 256 : (g.M + BM - 1) / BM;
   // Widest tile that still gives every SM work; narrower tiles for small N.
   int BN = 256;
   const int sms = num_sms();
   auto tiles_for = [&](int bn) { return tiles_m * ((g.N + bn - 1) / bn); };
-  if (splits > 1) BN = 256;
+  if (pl.pair || splits > 1) BN = 256;
   else if (g.N <= 64) BN = 64;
   else if (g.N <= 128) BN = 128;
   else if (tiles_for(256) < sms) BN = tiles_for(128) < sms ? 64 : 128;
-  if (splits == 1 && BN == 128 && tiles_for(128) < sms / 2 && g.N > 64) BN = 64;
+  if (!pl.pair && splits == 1 && BN == 128 && tiles_for(128) < sms / 2 && g.N > 64) BN = 64;
 
   TcParams p;
   p.M = g.M; p.N = g.N; p.K = g.K;
@@ -706,8 +1106,10 @@ mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStr
   else
     ok = encode_tmap_bf16_2d(&ta, g.A, g.M, g.K, (unsigned long long)g.lda * 2, 64, 64);
   if (!ok) return MLP_ERR_CUDA;
+  // K-major B boxes: BN rows, or each pair CTA's 128 of the tile's 256
   if (!p.b_mn)
-    ok = encode_tmap_bf16_2d(&tb, g.B, g.K, g.N, (unsigned long long)g.ldb * 2, 64, BN);
+    ok = encode_tmap_bf16_2d(&tb, g.B, g.K, g.N, (unsigned long long)g.ldb * 2, 64,
+                             pl.pair ? 128 : BN);
   else
     ok = encode_tmap_bf16_2d(&tb, g.B, g.N, g.K, (unsigned long long)g.ldb * 2, 64, 64);
   if (!ok) return MLP_ERR_CUDA;
@@ -726,6 +1128,7 @@ mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStr
       return MLP_ERR_CUDA;
     p.tma_store = 1;
   }
+  if (pl.pair) return launch_pair<6>(ta, tb, tc, p, st);
   // short, narrow problems (the 784-256-10 step) need few stages
   if (BN == 64 && p.k_blocks <= 16) return launch_bn<64, 4>(ta, tb, tc, p, st);
   switch (BN) {

@@ -171,7 +171,11 @@ def _tc_case(M_, N, K, a_t, b_t, bias=False, act=M.MLP_ACT_NONE, mask=False, out
 @pytest.mark.parametrize("a_t,b_t", [(0, 0), (1, 0), (0, 1), (1, 1)])
 @pytest.mark.parametrize("shape", [(128, 256, 784), (300, 200, 136), (129, 65, 64), (1, 16, 8),
                                    (256, 10, 128), (128, 256, 10), (2560, 1024, 192),
-                                   (640, 768, 320)])
+                                   (640, 768, 320),
+                                   # CTA-pair 256 x 256 tiles: whole tiles, ragged M / N / K
+                                   # (the last pair tile's odd CTA entirely past M), and
+                                   # an output row pitch that rules out TMA stores
+                                   (2304, 1536, 200), (2100, 1800, 72), (2100, 1803, 72)])
 def test_gemm_bf16_tc_matches_oracle(shape, a_t, b_t):
     M_, N, K = shape
     if (not a_t and K % 8) or (a_t and M_ % 8) or (not b_t and N % 8) or (b_t and K % 8):
@@ -196,7 +200,7 @@ def test_gemm_bf16_tc_epilogues(bias, act, mask, out_bf16):
 
 
 @pytest.mark.parametrize("out_bf16", [False, True])
-@pytest.mark.parametrize("shape", [(1100, 1000, 136), (1029, 1032, 64)])
+@pytest.mark.parametrize("shape", [(1100, 1000, 136), (1029, 1032, 64), (2100, 1800, 72)])
 def test_gemm_bf16_tc_large_ragged_outputs(shape, out_bf16):
     # outputs of a million elements or more leave through TMA bulk stores;
     # the ragged last tiles must be clipped exactly
