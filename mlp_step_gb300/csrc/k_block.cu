@@ -19,10 +19,12 @@
 // RMSNorm with gain 1 is folded into the epilogue: u = r (x W_gate) with
 // r = 1 / sqrt(mean(x^2) + eps) per token, so the gate GEMM reads x as is.
 //
-// Backward (block_bwd_act_kernel): per 128-token x 128-hidden tile, two MMA
-// accumulators U = x W_gate[:, c] and DA = dy W_down[c, :]^T over K = 512;
+// Backward (block_bwd_act_kernel): per 256-token x 128-hidden tile, two MMA
+// accumulators U = x W_gate[:, c] and DA = dy W_down[c, :]^T over K = 512,
+// computed by a CTA pair with tcgen05.mma.cta_group::2 (each CTA stages its
+// own 128 token rows of x and dy and half of the chunk's weight columns);
 // the epilogue writes a = f(r U) and r du = r DA f'(r U) in bf16 for the
-// weight-gradient GEMMs.  rmsnorm_bwd_kernel finishes dx from
+// weight-gradient GEMMs, through TMA bulk stores.  rmsnorm_bwd_kernel finishes dx from
 // dn' = (r du) W_gate^T.
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -499,42 +501,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
 
 // ------------------------------------------------------------------ backward
 
-constexpr int B_STAGES = 3;
-constexpr int B_STAGE_BYTES = 65536;   // x, W_gate, dy, W_down tiles of 16 KiB each
-constexpr int B_SMEM = 1024 + B_STAGES * B_STAGE_BYTES + 512;
+// Per CTA and 64-wide k-block: x rows (16 KiB), this CTA's 64 W_gate
+// columns (8 KiB), dy rows (16 KiB), this CTA's 64 W_down rows (8 KiB).
+constexpr int B_STAGES = 4;
+constexpr int B_X = 0, B_WG = 16384, B_DY = 24576, B_WD = 40960;
+constexpr int B_STAGE_BYTES = 49152;
+constexpr int B_BAR_BYTES = 1024;
+constexpr int B_STG_BYTES = 4 * 8192;  // per epilogue warp: {a, du} x 2 buffers x 2 KiB
+constexpr int B_SMEM = 1024 + B_STAGES * B_STAGE_BYTES + B_BAR_BYTES + B_STG_BYTES;
 
 struct BwdParams {
-  int T, hidden, tiles_m, tiles_h, num_tiles;
+  int T, hidden, pairs_m, tiles_h, num_tiles;
   float slope;
   const float* rstd;
-  __nv_bfloat16* a_out;    // [T][hidden]
-  __nv_bfloat16* du_out;   // [T][hidden], r * du
   unsigned long long wait_ns;
   int* err;
 };
 
-// 8 token tiles at a time sweep all hidden chunks (the last group may be
-// shorter), so CTAs running together share x / dy rows and weight columns.
-__device__ __forceinline__ void bwd_tile(int t, int tiles_m, int tiles_h, int& tm, int& th) {
-  constexpr int G = 8;
+// Tile t covers token rows [256 pm, 256 pm + 256) and hidden chunk th.  Four
+// token pairs at a time sweep all hidden chunks (the last group may be
+// shorter), so pairs running together share x / dy rows and weight columns
+// in L2.
+__device__ __forceinline__ void bwd_tile(int t, int pairs_m, int tiles_h, int& pm, int& th) {
+  constexpr int G = 4;
   const int group = t / (G * tiles_h);
   const int first = group * G;
-  const int gm = min(tiles_m - first, G);
+  const int gm = min(pairs_m - first, G);
   const int r = t - group * G * tiles_h;
-  tm = first + r % gm;
+  pm = first + r % gm;
   th = r / gm;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Row `lane` of a warp's 32 x 32 bf16 staging box in the 64-byte-swizzled
+// layout of the output tensor maps: 16-byte chunk q at q ^ ((lane >> 1) & 3).
+__device__ __forceinline__ void stage_row_bf16(uint8_t* box, int lane, const uint32_t (&pk)[16]) {
+  uint8_t* row = box + lane * 64;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(row + ((q ^ ((lane >> 1) & 3)) << 4)) =
+        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     block_bwd_act_kernel(const __grid_constant__ CUtensorMap tmX,
                          const __grid_constant__ CUtensorMap tmWg,
                          const __grid_constant__ CUtensorMap tmDy,
-                         const __grid_constant__ CUtensorMap tmWd, const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tmWd,
+                         const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmDu, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(stages + B_STAGES * B_STAGE_BYTES);
+  uint8_t* stg = stages + B_STAGES * B_STAGE_BYTES + B_BAR_BYTES;
   uint64_t* empty = full + B_STAGES;
   uint64_t* tfull = empty + B_STAGES;
   uint64_t* tempty = tfull + 2;
@@ -542,6 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < B_STAGES; ++s) {
@@ -550,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&tfull[b], 1);
-      ptx::mbar_init(&tempty[b], 128);
+      ptx::mbar_init(&tempty[b], 8);  // the pair's eight epilogue warps
     }
     ptx::mbar_init(done, 1);
     *s_abort = 0;
@@ -559,10 +581,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tensormap(&tmWg);
     ptx::prefetch_tensormap(&tmDy);
     ptx::prefetch_tensormap(&tmWd);
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmDu);
   }
-  if (warp == 1) ptx::tmem_alloc(tmem_slot, 512);
+  if (warp == 1) ptx::tmem_alloc_pair(tmem_slot, 512);
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // buffer b: U at b*256, DA at b*256 + 128
   pdl_wait();
@@ -572,43 +597,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       for (int s = 0; s < B_STAGES; ++s) last_parity[s] = -1;
+      const uint32_t full0 = ptx::mapa_shared(ptx::smem_u32(full), 0);  // the even CTA's full[]
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok && !*s_abort; t += gridDim.x) {
-        int tm, th;
-        bwd_tile(t, p.tiles_m, p.tiles_h, tm, th);
+      for (int t = pair; t < p.num_tiles && ok && !*s_abort; t += n_pairs) {
+        int pm, th;
+        bwd_tile(t, p.pairs_m, p.tiles_h, pm, th);
+        const int m0 = pm * 2 * TM + (int)rank * TM;
+        const int h0 = th * HC + (int)rank * (HC / 2);
         for (int kb = 0; kb < DM / 64; ++kb) {
-          if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
-                                      DEVERR_TIMEOUT_PRODUCER)) {
+          if (!ptx::mbar_wait_cluster_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
+                                              DEVERR_TIMEOUT_PRODUCER)) {
             *s_abort = 1;
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&full[stage], B_STAGE_BYTES);
-          last_parity[stage] = (int)phase;
+          if (rank == 0) {
+            ptx::mbar_arrive_expect_tx(&full[stage], 2 * B_STAGE_BYTES);
+            last_parity[stage] = (int)phase;
+          }
+          const uint32_t bar = full0 + (uint32_t)stage * 8u;
           uint8_t* st = stages + stage * B_STAGE_BYTES;
-          ptx::tma_load_2d(st, &tmX, &full[stage], kb * 64, tm * TM);
-          ptx::tma_load_2d(st + 16384, &tmWg, &full[stage], th * HC, kb * 64);
-          ptx::tma_load_2d(st + 24576, &tmWg, &full[stage], th * HC + 64, kb * 64);
-          ptx::tma_load_2d(st + 32768, &tmDy, &full[stage], kb * 64, tm * TM);
-          ptx::tma_load_2d(st + 49152, &tmWd, &full[stage], kb * 64, th * HC);
+          ptx::tma_load_2d_pair(st + B_X, &tmX, bar, kb * 64, m0);
+          ptx::tma_load_2d_pair(st + B_WG, &tmWg, bar, h0, kb * 64);
+          ptx::tma_load_2d_pair(st + B_DY, &tmDy, bar, kb * 64, m0);
+          ptx::tma_load_2d_pair(st + B_WD, &tmWd, bar, kb * 64, h0);
           if (++stage == B_STAGES) { stage = 0; phase ^= 1; }
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc_u = ptx::idesc_bf16_f32(TM, HC, 0, 1);   // B = W_gate, N-major
-      const uint32_t idesc_a = ptx::idesc_bf16_f32(TM, HC, 0, 0);   // B = W_down rows, K-major
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc_u = ptx::idesc_bf16_f32(2 * TM, HC, 0, 1);  // B = W_gate, N-major
+      const uint32_t idesc_a = ptx::idesc_bf16_f32(2 * TM, HC, 0, 0);  // B = W_down rows
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok && !*s_abort; t += gridDim.x) {
-        if (!ptx::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err,
-                                    DEVERR_TIMEOUT_MMA)) { ok = false; break; }
+      for (int t = pair; t < p.num_tiles && ok && !*s_abort; t += n_pairs) {
+        if (!ptx::mbar_wait_cluster_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err,
+                                            DEVERR_TIMEOUT_MMA)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t du = tmem + acc * 256;
         const uint32_t da = du + 128;
@@ -620,73 +650,87 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t en = (kb > 0 || k > 0) ? 1u : 0u;
-            ptx::mma_bf16(du, ptx::sw128_desc(sb + k * 32, 16, 1024),
-                          ptx::sw128_desc(sb + 16384 + k * 2048, 8192, 1024), idesc_u, en);
-            ptx::mma_bf16(da, ptx::sw128_desc(sb + 32768 + k * 32, 16, 1024),
-                          ptx::sw128_desc(sb + 49152 + k * 32, 16, 1024), idesc_a, en);
+            ptx::mma_bf16_pair(du, ptx::sw128_desc(sb + B_X + k * 32, 16, 1024),
+                               ptx::sw128_desc(sb + B_WG + k * 2048, 8192, 1024), idesc_u, en);
+            ptx::mma_bf16_pair(da, ptx::sw128_desc(sb + B_DY + k * 32, 16, 1024),
+                               ptx::sw128_desc(sb + B_WD + k * 32, 16, 1024), idesc_a, en);
           }
-          ptx::mma_commit(&empty[stage]);
+          ptx::mma_commit_pair_multicast(&empty[stage], 3);
           if (++stage == B_STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        ptx::mma_commit(&tfull[acc]);
+        ptx::mma_commit_pair_multicast(&tfull[acc], 3);
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
       if (!ok) *s_abort = 1;
-      ptx::mma_commit(done);
+      ptx::mma_commit_pair_multicast(done, 1);
       ptx::mbar_wait_bounded(done, 0, p.wait_ns, p.err, DEVERR_TIMEOUT_TEARDOWN);
     }
   } else {
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_u32(tempty), 0);
+    uint8_t* wstg = stg + (warp - 2) * 8192;  // [buffer][a | du] boxes of 2 KiB
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    int stg_count = 0;
+    for (int t = pair; t < p.num_tiles; t += n_pairs) {
       if (*s_abort) break;
-      if (!ptx::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err,
-                                  DEVERR_TIMEOUT_EPILOGUE)) {
+      if (!ptx::mbar_wait_cluster_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err,
+                                          DEVERR_TIMEOUT_EPILOGUE)) {
         *s_abort = 1;
         break;
       }
       ptx::tc_fence_after();
-      int tm, th;
-      bwd_tile(t, p.tiles_m, p.tiles_h, tm, th);
-      const int m = tm * TM + row;
-      const bool valid = m < p.T;
-      const float r = valid ? __ldg(p.rstd + m) : 0.f;
-#pragma unroll 1
+      int pm, th;
+      bwd_tile(t, p.pairs_m, p.tiles_h, pm, th);
+      const int row0 = pm * 2 * TM + (int)rank * TM + quarter * 32;  // this warp's first row
+      const int m = row0 + lane;
+      const float r = m < p.T ? __ldg(p.rstd + m) : 0.f;
       for (int cc = 0; cc < HC / 32; ++cc) {
         uint32_t vu[32], va[32];
         __syncwarp();
         ptx::tmem_ld_32x32b_x32(tmem + lane_off + acc * 256 + cc * 32, vu);
         ptx::tmem_ld_32x32b_x32(tmem + lane_off + acc * 256 + 128 + cc * 32, va);
         ptx::tmem_ld_wait();
-        if (valid) {
-          uint32_t pa[16], pd[16];
+        if (row0 >= p.T) continue;  // warp-uniform: the whole box is past the last token
+        uint32_t pa[16], pd[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float u0 = __uint_as_float(vu[2 * e]) * r;
-            const float u1 = __uint_as_float(vu[2 * e + 1]) * r;
-            pa[e] = pack_bf16x2(lrelu_sq(u0, p.slope), lrelu_sq(u1, p.slope));
-            const float d0 = __uint_as_float(va[2 * e]) * lrelu_sq_grad(u0, p.slope) * r;
-            const float d1 = __uint_as_float(va[2 * e + 1]) * lrelu_sq_grad(u1, p.slope) * r;
-            pd[e] = pack_bf16x2(d0, d1);
-          }
-          const size_t off = (size_t)m * p.hidden + th * HC + cc * 32;
-          uint4* ao = reinterpret_cast<uint4*>(p.a_out + off);
-          uint4* dd = reinterpret_cast<uint4*>(p.du_out + off);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            ao[q] = make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
-            dd[q] = make_uint4(pd[4 * q], pd[4 * q + 1], pd[4 * q + 2], pd[4 * q + 3]);
-          }
+        for (int e = 0; e < 16; ++e) {
+          const float u0 = __uint_as_float(vu[2 * e]) * r;
+          const float u1 = __uint_as_float(vu[2 * e + 1]) * r;
+          pa[e] = pack_bf16x2(lrelu_sq(u0, p.slope), lrelu_sq(u1, p.slope));
+          const float d0 = __uint_as_float(va[2 * e]) * lrelu_sq_grad(u0, p.slope) * r;
+          const float d1 = __uint_as_float(va[2 * e + 1]) * lrelu_sq_grad(u1, p.slope) * r;
+          pd[e] = pack_bf16x2(d0, d1);
         }
+        uint8_t* box = wstg + (stg_count & 1) * 4096;
+        if (stg_count >= 2) {
+          if (lane == 0) ptx::bulk_wait_group_read<1>();
+          __syncwarp();
+        }
+        stage_row_bf16(box, lane, pa);
+        stage_row_bf16(box + 2048, lane, pd);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          // rows past T are clipped by the tensor maps
+          ptx::tma_store_2d(&tmA, box, th * HC + cc * 32, row0);
+          ptx::tma_store_2d(&tmDu, box + 2048, th * HC + cc * 32, row0);
+          ptx::bulk_commit_group();
+        }
+        ++stg_count;
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&tempty[acc]);
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0) ptx::mbar_arrive(&tempty[acc]);
+        else ptx::mbar_arrive_remote(tempty0 + (uint32_t)acc * 8u);
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
   }
 
   __syncwarp();
@@ -701,9 +745,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
   __syncthreads();
+  // neither CTA frees its tensor memory or leaves while the pair's MMAs or
+  // signals may still reach it
+  ptx::cluster_sync();
   if (warp == 1) {
     __syncwarp();
-    ptx::tmem_dealloc(tmem, 512);
+    ptx::tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -806,35 +853,48 @@ mlp_status launch_block_bwd_act(const void* x, const void* wg, const void* wd, c
                                 const float* rstd, int T, int hidden, float slope, void* a_out,
                                 void* du_out, cudaStream_t st) {
   static bool configured = false;
+  static int max_pairs = 0;
   if (!configured) {
     if (cudaFuncSetAttribute(block_bwd_act_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              B_SMEM) != cudaSuccess)
       return MLP_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = B_SMEM;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, block_bwd_act_kernel, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = num_sms() / 2;
+    }
+    max_pairs = n;
     configured = true;
   }
-  CUtensorMap tx, tg, tdy, twd;
+  CUtensorMap tx, tg, tdy, twd, ta, tdu;
   if (!encode_tmap_bf16_2d(&tx, x, DM, T, DM * 2, 64, TM)) return MLP_ERR_CUDA;
   if (!encode_tmap_bf16_2d(&tg, wg, hidden, DM, (unsigned long long)hidden * 2, 64, 64))
     return MLP_ERR_CUDA;
   if (!encode_tmap_bf16_2d(&tdy, dy, DM, T, DM * 2, 64, TM)) return MLP_ERR_CUDA;
-  if (!encode_tmap_bf16_2d(&twd, wd, DM, hidden, DM * 2, 64, HC)) return MLP_ERR_CUDA;
+  if (!encode_tmap_bf16_2d(&twd, wd, DM, hidden, DM * 2, 64, HC / 2)) return MLP_ERR_CUDA;
+  if (!encode_tmap_out_2d(&ta, a_out, 0, hidden, T, (unsigned long long)hidden * 2, 32, 32))
+    return MLP_ERR_CUDA;
+  if (!encode_tmap_out_2d(&tdu, du_out, 0, hidden, T, (unsigned long long)hidden * 2, 32, 32))
+    return MLP_ERR_CUDA;
   BwdParams p;
   p.T = T;
   p.hidden = hidden;
-  p.tiles_m = (T + TM - 1) / TM;
+  p.pairs_m = (T + 2 * TM - 1) / (2 * TM);
   p.tiles_h = hidden / HC;
-  p.num_tiles = p.tiles_m * p.tiles_h;
+  p.num_tiles = p.pairs_m * p.tiles_h;
   p.slope = slope;
   p.rstd = rstd;
-  p.a_out = static_cast<__nv_bfloat16*>(a_out);
-  p.du_out = static_cast<__nv_bfloat16*>(du_out);
   p.wait_ns = wait_limit_ns();
   p.err = device_error_word();
   if (!p.err) return MLP_ERR_CUDA;
-  int grid = num_sms();
-  if (grid > p.num_tiles) grid = p.num_tiles;
+  const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
   LaunchScope ls("block_bwd_act", st, T, DM, hidden);
-  launch_k(block_bwd_act_kernel, dim3(grid), dim3(kThreads), B_SMEM, st, tx, tg, tdy, twd, p);
+  launch_k(block_bwd_act_kernel, dim3(2 * pairs), dim3(kThreads), B_SMEM, st, tx, tg, tdy, twd, ta,
+           tdu, p);
   return launch_status();
 }
 
