@@ -784,11 +784,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float* part = p.splits > 1 ? p.partial + (size_t)(u % p.splits) * p.M * p.ldp : nullptr;
       const int row0 = tm * 256 + (int)rank * 128 + quarter * 32;  // this warp's first row
       const int m = row0 + lane;
+      // ReLU-mask pieces are fetched one piece ahead of their use
+      MaskPiece mp_next;
+      load_mask(p, m, tn * BN2, mp_next);
       for (int c0 = 0; c0 < BN2; c0 += 32) {
         const int n0 = tn * BN2 + c0;
         if (n0 >= p.N) break;  // warp-uniform
-        MaskPiece mp;
-        load_mask(p, m, n0, mp);
+        const MaskPiece mp = mp_next;
+        if (c0 + 32 < BN2 && n0 + 32 < p.N) load_mask(p, m, n0 + 32, mp_next);
         uint32_t r[32];
         __syncwarp();
         ptx::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) +
@@ -981,9 +984,11 @@ mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
 
 // Kernel choice and split-K plan from the shape alone (so workspace sizes do
 // not depend on the device).  CTA pairs with 256 x 256 tiles whenever both
-// output dimensions exceed 128 and there are enough pair tiles for ~76 pairs,
-// or K is long enough to split; otherwise single-CTA 128 x BN tiles, split
-// only when 128 x 256 tiles leave most of ~144 SMs idle and K is long.
+// output dimensions exceed 128 and there are enough pair tiles for ~76 pairs
+// (unless their last round is so ragged that single-CTA tiles finish first,
+// e.g. M = 1025), or K is long enough to split; otherwise single-CTA
+// 128 x BN tiles, split only when 128 x 256 tiles leave most of ~144 SMs idle
+// and K is long.
 struct GemmPlan {
   bool pair;
   int splits, kb_per_split;
@@ -996,9 +1001,14 @@ GemmPlan gemm_plan(int M, int N, int K, bool fused) {
   int s = 1;
   if (!fused && M > 128 && N > 128) {
     const int pair_tiles = ((M + 255) / 256) * ((N + BN2 - 1) / BN2);
-    if (pair_tiles >= 48) {
+    const int single_tiles = ((M + BM - 1) / BM) * ((N + 255) / 256);
+    // rounds of tiles over ~76 pairs vs ~152 single CTAs; a pair round does
+    // about 1.25x the work per SM of a single-CTA round in the same time
+    const int pair_rounds = (pair_tiles + 75) / 76;
+    const int single_rounds = (single_tiles + 151) / 152;
+    if (pair_tiles >= 48 && 4 * pair_rounds <= 5 * single_rounds) {
       pl.pair = true;
-    } else if (kblocks >= 64) {
+    } else if (pair_tiles < 48 && kblocks >= 64) {
       s = 76 / pair_tiles;
       if (s > 16) s = 16;
       if (s > kblocks / 16) s = kblocks / 16;
