@@ -174,10 +174,33 @@ mlp_status mlp_sgd_step(mlp_handle* h, float lr, float momentum, void* stream);
 /* One full training step on the stream: forward, softmax cross entropy
  * (mean over the batch), backward, momentum SGD.  labels int32[batch] in
  * [0, dims[-1]).  loss_out (nullable): device fp32 scalar.  argmax_out
- * (nullable): device int32[batch] predictions of this step's forward. */
+ * (nullable): device int32[batch] predictions of this step's forward.
+ * For MLP_PREC_BF16 networks with batch <= 128, at most 32 classes and small
+ * layers (every GEMM of the step fits one round of CTAs and every weight
+ * update rides in its gradient GEMM) the step is ONE cooperative kernel
+ * launch whose phases are separated by grid barriers; results are the same
+ * as with one launch per GEMM ([cap] "Capstone 5: train a network with your
+ * CUDA kernels": the training loop of the minimum model). */
 mlp_status mlp_train_step(mlp_handle* h, const void* x, int x_dtype, const int32_t* labels,
                           int batch, float lr, float momentum, float* loss_out,
                           int32_t* argmax_out, void* stream);
+
+/* One epoch of training steps in sequence ([cap] "The minimum model": the
+ * data set is visited in order in mini-batches): step s takes rows
+ * [s * batch, min(n_samples, (s + 1) * batch)) of x ([n_samples][dims[0]],
+ * dtype x_dtype) and of labels (int32[n_samples]); the last step takes the
+ * remainder.  losses_out (nullable): device fp32[ceil(n_samples / batch)],
+ * the mean loss of each step, 4-byte aligned.  argmax_out (nullable): device
+ * int32[n_samples] predictions.  Exactly the results of calling
+ * mlp_train_step on each step's slices in order; where a step is one
+ * cooperative launch (see mlp_train_step) all full-size steps run in ONE
+ * launch with a grid barrier between steps.  Each step's slice of x,
+ * labels and argmax_out must start on 16 bytes (batch * dims[0] * element
+ * size and batch * 4 multiples of 16, base pointers 16-byte aligned), else
+ * MLP_ERR_MISALIGNED.  batch in [1, max_batch]. */
+mlp_status mlp_train_epoch(mlp_handle* h, const void* x, int x_dtype, const int32_t* labels,
+                           int n_samples, int batch, float lr, float momentum, float* losses_out,
+                           int32_t* argmax_out, void* stream);
 
 /* ---------------------------------------------------------------- loss -----
  * Stable softmax cross entropy, forward and backward ([cap] "The minimum

@@ -67,6 +67,7 @@ SIGNATURES = {
     "mlp_backward": (_i, [_vp, _vp, _i, _i, _vp, _vp]),
     "mlp_sgd_step": (_i, [_vp, _f, _f, _vp]),
     "mlp_train_step": (_i, [_vp, _vp, _i, _vp, _i, _f, _f, _vp, _vp, _vp]),
+    "mlp_train_epoch": (_i, [_vp, _vp, _i, _vp, _i, _i, _f, _f, _vp, _vp, _vp]),
     "softmax_xent_workspace_bytes": (_sz, [_i, _i]),
     "softmax_xent_fwd_bwd": (_i, [_vp, _i, _vp, _i, _i, _vp, _vp, _i, _i, _vp, _vp, _sz, _vp]),
     "softmax_xent_noalloc_max_batch": (_i, []),
@@ -260,6 +261,15 @@ class MLP:
         _check(load().mlp_train_step(self.handle, _ptr(x), _dtype_code(x), _ptr(labels), b, lr,
                                      momentum, _ptr(loss_out), _ptr(argmax_out),
                                      _stream(stream)), "mlp_train_step")
+
+    def train_epoch(self, x, labels, lr, momentum, batch, losses_out=None, argmax_out=None,
+                    n_samples=None, stream=None):
+        """Training steps over x / labels in order, `batch` rows at a time (the
+        last step takes the remainder); losses_out: fp32[n_steps]."""
+        n = x.shape[0] if n_samples is None else n_samples
+        _check(load().mlp_train_epoch(self.handle, _ptr(x), _dtype_code(x), _ptr(labels), n,
+                                      batch, lr, momentum, _ptr(losses_out), _ptr(argmax_out),
+                                      _stream(stream)), "mlp_train_epoch")
 
 
 # ------------------------------------------------------------------ single kernels

@@ -149,6 +149,17 @@ mlp_status run_gemm(const GemmArgs& g, int in_bf16, cudaStream_t st) {
   return launch_gemm_simt(g, 0, st);
 }
 
+// Launches the GEMM now, or (rec set) appends it to a step program in the
+// given phase.
+mlp_status issue_gemm(const GemmArgs& g, int in_bf16, cudaStream_t st, StepSpec* rec, int phase) {
+  if (!rec) return run_gemm(g, in_bf16, st);
+  if (rec->n_gemm >= kStepMaxGemms || !step_gemm_supported(g)) return MLP_ERR_UNSUPPORTED_SHAPE;
+  rec->gemm[rec->n_gemm] = g;
+  rec->phase[rec->n_gemm] = phase;
+  ++rec->n_gemm;
+  return MLP_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -301,6 +312,7 @@ struct mlp_handle {
   int ldz = 0;
   void* dh[2] = {nullptr, nullptr};
   float* loss = nullptr;
+  unsigned* step_bar = nullptr;    // grid barrier words of the step program (in the loss block)
   void* red = nullptr;             // reduction partials
   size_t red_bytes = 0;
   SgdSegments segs{};
@@ -365,8 +377,9 @@ mlp_status ensure_ones(mlp_handle* h, cudaStream_t st) {
   return MLP_OK;
 }
 
-// Hidden layers 0 .. L-2 of the forward (bias + activation in the epilogue).
-mlp_status forward_hidden(mlp_handle* h, int batch, cudaStream_t st) {
+// Hidden layers 0 .. L-2 of the forward (bias + activation in the epilogue);
+// in a step program, layer l is phase 1 + l.
+mlp_status forward_hidden(mlp_handle* h, int batch, cudaStream_t st, StepSpec* rec = nullptr) {
   const bool bf = h->prec == MLP_PREC_BF16;
   for (int l = 0; l + 1 < h->L; ++l) {
     GemmArgs g{};
@@ -389,7 +402,7 @@ mlp_status forward_hidden(mlp_handle* h, int batch, cudaStream_t st) {
     g.C = h->acts[l];
     g.ldc = h->act_ld[l + 1];
     g.c_bf16 = bf ? 1 : 0;
-    MLP_CHECK(run_gemm(g, bf, st));
+    MLP_CHECK(issue_gemm(g, bf, st, rec, 1 + l));
   }
   return MLP_OK;
 }
@@ -430,9 +443,14 @@ mlp_status load_input(mlp_handle* h, const void* x, int x_dtype, int batch, cuda
 
 // Backward from dY = dlogits.  With fuse_sgd, each layer's weight-gradient
 // GEMM also applies momentum SGD to that layer's weights and bias (after the
-// layer's input gradient has read the old weights).
+// layer's input gradient has read the old weights).  In a step program
+// (after the forward's phases 1 .. L), layer l's input gradient is phase
+// 2L - l and its weight gradient the phase after (or, without an input
+// gradient, the phase after its dY's): each reads only earlier phases'
+// outputs and the weights it reads are updated in a later phase.
 mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int batch, void* dx,
-                         bool fuse_sgd, float lr, float mom, cudaStream_t st) {
+                         bool fuse_sgd, float lr, float mom, cudaStream_t st,
+                         StepSpec* rec = nullptr) {
   const bool bf = h->prec == MLP_PREC_BF16;
   const void* dY = dlogits;
   int ld_dy = ld_dlogits;
@@ -461,7 +479,7 @@ mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int
         gd.ldc = fi;
       }
       gd.c_bf16 = bf ? 1 : 0;
-      MLP_CHECK(run_gemm(gd, bf, st));
+      MLP_CHECK(issue_gemm(gd, bf, st, rec, 2 * h->L - l));
     }
     // [dW_l; db_l] = [In_l | 1]^T dY_l   (A = In_l read transposed), written
     // over the layer's flat slice of grads
@@ -485,7 +503,8 @@ mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int
       gw.sgd_ld_shadow = h->out_pad[l];
       gw.sgd_shadow_rows = fi;
     }
-    MLP_CHECK(run_gemm(gw, bf, st));
+    if (rec && fuse_sgd && !fuse_here) return MLP_ERR_UNSUPPORTED_SHAPE;
+    MLP_CHECK(issue_gemm(gw, bf, st, rec, 2 * h->L - l + (want_din ? 1 : 0)));
     if (fuse_sgd && !fuse_here) {
       // flat SGD over this layer's W and b (and its shadow rows)
       SgdSegments seg{};
@@ -509,6 +528,75 @@ mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int
     }
   }
   return MLP_OK;
+}
+
+// The step program of one training step (bf16 path, one-tile head): input
+// cast (phase 0), forward, logits with the softmax cross entropy, backward
+// with momentum SGD in every weight-gradient GEMM -- the same kernels'
+// arithmetic in the same order as the launch-per-GEMM path.  False when some
+// GEMM does not fit one round of CTAs or a layer's update cannot ride in its
+// gradient GEMM.
+bool build_step_spec(mlp_handle* h, const void* x, int x_dtype, const int32_t* labels, int batch,
+                     float lr, float momentum, float* loss, int32_t* argmax_out, cudaStream_t st,
+                     StepSpec* spec) {
+  const int C = h->dims[h->L];
+  if (h->prec != MLP_PREC_BF16 || batch > 128 || C > 32) return false;
+  spec->cast_src = x;
+  spec->cast_dtype = x_dtype;
+  spec->cast_dst = h->x_copy;
+  spec->cast_rows = batch;
+  spec->cast_cols = h->dims[0];
+  spec->cast_ld = h->act_ld[0];
+  if (forward_hidden(h, batch, st, spec) != MLP_OK) return false;
+  GemmArgs gz = logits_gemm(h, batch, h->logits);
+  gz.xent_labels = labels;
+  gz.xent_dlog = h->dlogits;
+  gz.xent_ldd = h->ldz;
+  gz.xent_loss = loss;
+  gz.xent_argmax = argmax_out;
+  gz.xent_norm = batch;
+  if (issue_gemm(gz, true, st, spec, h->L) != MLP_OK) return false;
+  return backward_impl(h, h->dlogits, h->ldz, batch, nullptr, true, lr, momentum, st, spec) ==
+         MLP_OK;
+}
+
+mlp_status train_step_impl(mlp_handle* h, const void* x, int x_dtype, const int32_t* labels,
+                           int batch, float lr, float momentum, float* loss_out,
+                           int32_t* argmax_out, cudaStream_t st) {
+  const int C = h->dims[h->L];
+  const bool bf = h->prec == MLP_PREC_BF16;
+  float* loss = loss_out ? loss_out : h->loss;
+  {
+    // the whole step as one cooperative launch where it fits
+    StepSpec spec;
+    if (build_step_spec(h, x, x_dtype, labels, batch, lr, momentum, loss, argmax_out, st, &spec)) {
+      MLP_CHECK(ensure_ones(h, st));
+      MLP_CHECK(launch_step_program(spec, h->step_bar, wait_limit_ns(), st));
+      h->have_forward = true;
+      return MLP_OK;
+    }
+  }
+  MLP_CHECK(load_input(h, x, x_dtype, batch, st));
+  MLP_CHECK(forward_hidden(h, batch, st));
+  GemmArgs gz = logits_gemm(h, batch, h->logits);
+  if (bf && batch <= 128 && C <= 32) {
+    // one tile holds the whole head: softmax cross entropy in its epilogue
+    gz.xent_labels = labels;
+    gz.xent_dlog = h->dlogits;
+    gz.xent_ldd = h->ldz;
+    gz.xent_loss = loss;
+    gz.xent_argmax = argmax_out;
+    gz.xent_norm = batch;
+    MLP_CHECK(run_gemm(gz, true, st));
+  } else {
+    MLP_CHECK(run_gemm(gz, bf, st));
+    MLP_CHECK(launch_xent(h->logits, C, labels, batch, C, loss, h->dlogits, bf, h->ldz,
+                          argmax_out, h->red, st));
+  }
+  h->have_forward = true;
+  if (bf) return backward_impl(h, h->dlogits, h->ldz, batch, nullptr, true, lr, momentum, st);
+  MLP_CHECK(backward_impl(h, h->dlogits, h->ldz, batch, nullptr, false, 0.f, 0.f, st));
+  return mlp_sgd_step(h, lr, momentum, st);
 }
 
 }  // namespace
@@ -614,6 +702,7 @@ mlp_status mlp_create(const int* dims, int n_dims, int hidden_act, int prec, int
   h->dh[1] = w;
   w += pl.dh;
   h->loss = reinterpret_cast<float*>(w);
+  h->step_bar = reinterpret_cast<unsigned*>(w + 128);
   w += pl.loss;
   h->red = w;
   h->red_bytes = pl.red;
@@ -673,31 +762,51 @@ mlp_status mlp_train_step(mlp_handle* h, const void* x, int x_dtype, const int32
   if (!aligned16(x) || !aligned16(labels) || (loss_out && !aligned16(loss_out)) ||
       (argmax_out && !aligned16(argmax_out)))
     return MLP_ERR_MISALIGNED;
+  return train_step_impl(h, x, x_dtype, labels, batch, lr, momentum, loss_out, argmax_out,
+                         S(stream));
+}
+
+mlp_status mlp_train_epoch(mlp_handle* h, const void* x, int x_dtype, const int32_t* labels,
+                           int n_samples, int batch, float lr, float momentum, float* losses_out,
+                           int32_t* argmax_out, void* stream) {
+  if (!h || n_samples < 0 || batch <= 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
+  if (x_dtype != MLP_DTYPE_F32 && x_dtype != MLP_DTYPE_BF16 && x_dtype != MLP_DTYPE_U8)
+    return MLP_ERR_INVALID_ARG;
+  if (n_samples == 0) return MLP_OK;
+  if (!x || !labels) return MLP_ERR_INVALID_ARG;
+  const int xsz = x_dtype == MLP_DTYPE_U8 ? 1 : (x_dtype == MLP_DTYPE_BF16 ? 2 : 4);
+  const long long x_step = (long long)batch * h->dims[0] * xsz;
+  // every step's input rows, labels and predictions start on 16 bytes
+  if (!aligned16(x) || !aligned16(labels) || (argmax_out && !aligned16(argmax_out)) ||
+      x_step % 16 != 0 || ((long long)batch * 4) % 16 != 0 ||
+      (losses_out && (reinterpret_cast<uintptr_t>(losses_out) & 3)))
+    return MLP_ERR_MISALIGNED;
   cudaStream_t st = S(stream);
-  const int C = h->dims[h->L];
-  const bool bf = h->prec == MLP_PREC_BF16;
-  float* loss = loss_out ? loss_out : h->loss;
-  MLP_CHECK(load_input(h, x, x_dtype, batch, st));
-  MLP_CHECK(forward_hidden(h, batch, st));
-  GemmArgs gz = logits_gemm(h, batch, h->logits);
-  if (bf && batch <= 128 && C <= 32) {
-    // one tile holds the whole head: softmax cross entropy in its epilogue
-    gz.xent_labels = labels;
-    gz.xent_dlog = h->dlogits;
-    gz.xent_ldd = h->ldz;
-    gz.xent_loss = loss;
-    gz.xent_argmax = argmax_out;
-    gz.xent_norm = batch;
-    MLP_CHECK(run_gemm(gz, true, st));
-  } else {
-    MLP_CHECK(run_gemm(gz, bf, st));
-    MLP_CHECK(launch_xent(h->logits, C, labels, batch, C, loss, h->dlogits, bf, h->ldz,
-                          argmax_out, h->red, st));
+  const int full = n_samples / batch, rem = n_samples % batch;
+  int done = 0;
+  if (full > 0) {
+    StepSpec spec;
+    float* loss = losses_out ? losses_out : h->loss;
+    if (build_step_spec(h, x, x_dtype, labels, batch, lr, momentum, loss, argmax_out, st, &spec)) {
+      spec.n_steps = full;
+      spec.cast_stride = x_step;
+      spec.label_stride = batch;
+      spec.loss_stride = losses_out ? 1 : 0;
+      spec.argmax_stride = batch;
+      MLP_CHECK(ensure_ones(h, st));
+      MLP_CHECK(launch_step_program(spec, h->step_bar, wait_limit_ns(), st));
+      h->have_forward = true;
+      done = full;
+    }
   }
-  h->have_forward = true;
-  if (bf) return backward_impl(h, h->dlogits, h->ldz, batch, nullptr, true, lr, momentum, st);
-  MLP_CHECK(backward_impl(h, h->dlogits, h->ldz, batch, nullptr, false, 0.f, 0.f, st));
-  return mlp_sgd_step(h, lr, momentum, stream);
+  for (int s = done; s < full + (rem > 0 ? 1 : 0); ++s) {
+    const int b = s < full ? batch : rem;
+    MLP_CHECK(train_step_impl(h, static_cast<const uint8_t*>(x) + s * x_step, x_dtype,
+                              labels + (size_t)s * batch, b, lr, momentum,
+                              losses_out ? losses_out + s : nullptr,
+                              argmax_out ? argmax_out + (size_t)s * batch : nullptr, st));
+  }
+  return MLP_OK;
 }
 
 }  // extern "C"

@@ -25,6 +25,7 @@ enum : int {
   DEVERR_TIMEOUT_EPILOGUE = 0x103,
   DEVERR_TIMEOUT_TEARDOWN = 0x104,
   DEVERR_TIMEOUT_PEER = 0x105,
+  DEVERR_TIMEOUT_GRID = 0x106,
 };
 
 __device__ __forceinline__ void record_device_error(int* word, int code) {

@@ -373,6 +373,59 @@ __global__ void __launch_bounds__(256) xent_single_block_kernel(
   }
 }
 
+// Small heads (C <= 32) of small batches (B <= 512): one row per thread of
+// a single block, so every row's max, sum and dZ come out of one pass with
+// one round trip to memory; the batch mean is a fixed-order tree sum.
+__global__ void __launch_bounds__(512) xent_lane_rows_kernel(
+    const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
+    float* __restrict__ loss_out, void* dlog, int dl_bf16, int ldd, int* argmax) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ float red[512];
+  const int r = threadIdx.x;
+  float li = 0.f;
+  if (r < B) {
+    const float* z = logits + (size_t)r * ldl;
+    int y = labels[r];
+    y = y < 0 ? 0 : (y >= C ? C - 1 : y);  // keep the read in bounds
+    float v[32];
+    float mx = -INFINITY, zy = 0.f;
+    int am = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] = j < C ? z[j] : -INFINITY;
+      if (v[j] > mx) { mx = v[j]; am = j; }  // first maximum: lowest index among ties
+      if (j == y) zy = v[j];
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] = j < C ? expf(v[j] - mx) : 0.f;  // v now holds exp(z - max)
+      s += v[j];
+    }
+    li = mx + logf(s) - zy;
+    if (dlog) {
+      const float inv = 1.0f / (float)B;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (j < ldd) {
+          const float d = j < C ? (v[j] / s - (j == y ? 1.f : 0.f)) * inv : 0.f;
+          if (dl_bf16) static_cast<__nv_bfloat16*>(dlog)[(size_t)r * ldd + j] = f32_to_bf16(d);
+          else static_cast<float*>(dlog)[(size_t)r * ldd + j] = d;
+        }
+      }
+    }
+    if (argmax) argmax[r] = am;
+  }
+  red[r] = li;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (r < w) red[r] += red[r + w];
+    __syncthreads();
+  }
+  if (r == 0 && loss_out) *loss_out = red[0] / (float)B;
+}
+
 // Large batches: one row per warp, one partial per block, then a one-block
 // fixed-order sum.
 __global__ void __launch_bounds__(256) xent_rows_kernel(
@@ -427,6 +480,14 @@ mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, i
                        float* loss_out, void* dlog, int dl_bf16, int ldd, int* argmax,
                        void* ws, cudaStream_t st) {
   if (B <= 0) return MLP_OK;
+  if (C <= 32 && ldd <= 32 && B <= 512) {
+    int threads = 32;
+    while (threads < B) threads *= 2;  // a power of two for the tree sum
+    LaunchScope ls("xent", st, B, C);
+    launch_k(xent_lane_rows_kernel, dim3(1), dim3(threads), 0, st, logits, ldl, labels, B, C,
+             loss_out, dlog, dl_bf16, ldd, argmax);
+    return launch_status();
+  }
   if (B <= 256) {
     LaunchScope ls("xent", st, B, C);
     launch_k(xent_single_block_kernel, dim3(1), dim3(256), 0, st, logits, ldl, labels, B, C, loss_out, dlog,

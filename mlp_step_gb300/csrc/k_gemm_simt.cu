@@ -10,7 +10,11 @@
 //
 // 64x64 output tile per block, 256 threads each owning a 4x4 micro-tile, K in
 // steps of 16 staged through shared memory.  Each output sums k in ascending
-// order, so the result is deterministic.
+// order, so the result is deterministic.  For fp32 operands the K steps
+// stream through a 4-deep ring of cp.async copies (zero-filled past the
+// edges), so a block waits on one global-memory round trip per four steps
+// rather than per step: at the batch sizes of the minimum model the grid has
+// a handful of blocks and the loop is latency-bound.
 #include "kernels.cuh"
 #include "trace.cuh"
 
@@ -100,13 +104,136 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
   }
 }
 
+constexpr int SIMT_STAGES = 4;
+constexpr int SIMT_SLOT = 64 * 20;  // floats per operand slot: [64][16 + 4] or [16][64 + 4]
+
+__device__ __forceinline__ void cp_async_f32(float* smem_dst, const float* src, bool valid) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  // src-size 0 writes zeros (and reads nothing) for elements past the edges
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(float* smem_dst, const float* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+
+// Four consecutive elements of a row of a row-major operand (row `r`, column
+// `c0`, leading dimension ld) into 16 contiguous bytes of shared memory:
+// one 16-byte copy when the four are in range and aligned, else element-wise
+// (zero-filled past the edges).
+__device__ __forceinline__ void stage_quad(float* dst, const float* base, int ld, int r, int c0,
+                                           int rows, int cols, bool vec) {
+  if (vec && r < rows && c0 + 3 < cols) {
+    cp_async_16(dst, base + (size_t)r * ld + c0);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const bool ok = r < rows && c0 + e < cols;
+      cp_async_f32(dst + e, ok ? base + (size_t)r * ld + c0 + e : base, ok);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) gemm_simt_f32_pipelined_kernel(GemmArgs g) {
+  pdl_wait();
+  pdl_launch_dependents();
+  // A slot: [64 m][20] (A stored [M][K]) or [16 k][68] (stored [K][M]);
+  // B slot: [16 k][68] (B stored [K][N]) or [64 n][20] (stored [N][K]).
+  __shared__ __align__(16) float As[SIMT_STAGES][SIMT_SLOT];
+  __shared__ __align__(16) float Bs[SIMT_STAGES][SIMT_SLOT];
+  const float* A = static_cast<const float*>(g.A);
+  const float* B = static_cast<const float*>(g.B);
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int nk = (g.K + 15) / 16;
+  const bool a_vec = (reinterpret_cast<uintptr_t>(A) & 15) == 0 && (g.lda & 3) == 0;
+  const bool b_vec = (reinterpret_cast<uintptr_t>(B) & 15) == 0 && (g.ldb & 3) == 0;
+  float acc[4][4] = {};
+
+  // each thread stages one quad of each operand per step
+  auto issue = [&](int kt) {
+    const int st = kt % SIMT_STAGES, k0 = kt * 16;
+    if (!g.a_trans) {
+      const int m = tid >> 2, kq = (tid & 3) * 4;
+      stage_quad(&As[st][m * 20 + kq], A, g.lda, m0 + m, k0 + kq, g.M, g.K, a_vec);
+    } else {
+      const int k = tid >> 4, mq = (tid & 15) * 4;
+      stage_quad(&As[st][k * 68 + mq], A, g.lda, k0 + k, m0 + mq, g.K, g.M, a_vec);
+    }
+    if (!g.b_trans) {
+      const int k = tid >> 4, nq = (tid & 15) * 4;
+      stage_quad(&Bs[st][k * 68 + nq], B, g.ldb, k0 + k, n0 + nq, g.K, g.N, b_vec);
+    } else {
+      const int n = tid >> 2, kq = (tid & 3) * 4;
+      stage_quad(&Bs[st][n * 20 + kq], B, g.ldb, n0 + n, k0 + kq, g.N, g.K, b_vec);
+    }
+  };
+
+  // prologue: the first STAGES - 1 steps in flight (one commit group each,
+  // empty groups past the end keep the group count uniform)
+#pragma unroll
+  for (int kt = 0; kt < SIMT_STAGES - 1; ++kt) {
+    if (kt < nk) issue(kt);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int kt = 0; kt < nk; ++kt) {
+    // step kt has landed once at most STAGES - 2 newer groups are pending
+    asm volatile("cp.async.wait_group %0;" ::"n"(SIMT_STAGES - 2) : "memory");
+    __syncthreads();
+    // refill the slot the previous step used (all threads are past it)
+    if (kt + SIMT_STAGES - 1 < nk) issue(kt + SIMT_STAGES - 1);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const float* as = As[kt % SIMT_STAGES];
+    const float* bs = Bs[kt % SIMT_STAGES];
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        a[i] = g.a_trans ? as[kk * 68 + ty * 4 + i] : as[(ty * 4 + i) * 20 + kk];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        b[j] = g.b_trans ? bs[(tx * 4 + j) * 20 + kk] : bs[kk * 68 + tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] += a[i] * b[j];
+    }
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= g.M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n >= g.N) continue;
+      float v = acc[i][j];
+      if (g.bias) v += g.bias[n];
+      if (g.act == MLP_ACT_RELU) v = fmaxf(v, 0.f);
+      if (g.mask) {
+        const float mk = ld_in(static_cast<const float*>(g.mask) + (size_t)m * g.ldm + n);
+        v = mk > 0.f ? v : 0.f;
+      }
+      if (g.c_bf16) static_cast<__nv_bfloat16*>(g.C)[(size_t)m * g.ldc + n] = f32_to_bf16(v);
+      else static_cast<float*>(g.C)[(size_t)m * g.ldc + n] = v;
+    }
+  }
+}
+
 mlp_status launch_gemm_simt(const GemmArgs& g, int in_bf16, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0) return MLP_OK;
   dim3 grid((g.N + 63) / 64, (g.M + 63) / 64);
   if (grid.y > 65535) return MLP_ERR_UNSUPPORTED_SHAPE;
   LaunchScope ls("gemm_simt", st, g.M, g.N, g.K);
   if (in_bf16) launch_k(gemm_simt_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st, g);
-  else launch_k(gemm_simt_kernel<float>, dim3(grid), dim3(256), 0, st, g);
+  else launch_k(gemm_simt_f32_pipelined_kernel, dim3(grid), dim3(256), 0, st, g);
   return launch_status();
 }
 

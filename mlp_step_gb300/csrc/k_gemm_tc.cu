@@ -229,54 +229,48 @@ __device__ __forceinline__ void epilogue_stage_row(uint8_t* box, int c_bf16, int
   }
 }
 
-// Momentum SGD on one 32-column piece of the fp32 gradient row m ("Capstone 5:
-// train a network with your CUDA kernels", "Read the worked reference":
-// v <- m v - lr g, w <- w + v), also storing g and bf16(w).
-__device__ __forceinline__ void sgd_epilogue_chunk(const TcParams& p, int m, int n0,
-                                                   const uint32_t (&r)[32]) {
-  const size_t off = (size_t)m * p.ldc + n0;
-  float* gr = static_cast<float*>(p.C) + off;
-  float* wr = p.sgd_w + off;
-  float* vr = p.sgd_v + off;
-  __nv_bfloat16* sr =
-      m < p.sgd_shadow_rows ? p.sgd_shadow + (size_t)m * p.sgd_ld_shadow + n0 : nullptr;
-  const bool vec = (n0 + 32 <= p.N) && ((reinterpret_cast<uintptr_t>(gr) & 15) == 0) &&
-                   ((reinterpret_cast<uintptr_t>(wr) & 15) == 0) &&
-                   ((reinterpret_cast<uintptr_t>(vr) & 15) == 0) &&
-                   (!sr || (reinterpret_cast<uintptr_t>(sr) & 15) == 0);
-  if (vec) {
+// Momentum SGD ("Capstone 5: train a network with your CUDA kernels", "Read
+// the worked reference": v <- m v - lr g, w <- w + v, also storing g and
+// bf16(w)) on the 32 x 32 piece rows [row0, row0 + 32), columns
+// [n0, n0 + 32) of a warp.  The fp32
+// gradient piece goes through the warp's shared-memory slot (32 x 33 floats,
+// conflict-free both ways) so that g, w, v and the bf16 shadow are read and
+// written one row at a time across the lanes: 128-byte accesses instead of
+// 32 rows touched by every instruction.  Called by the whole warp.
+__device__ __forceinline__ void sgd_epilogue_staged(const TcParams& p, int row0, int n0,
+                                                    const uint32_t (&r)[32], float* slot,
+                                                    int lane) {
+  __syncwarp();
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 w4 = reinterpret_cast<const float4*>(wr)[q];
-      const float4 v4 = reinterpret_cast<const float4*>(vr)[q];
-      const float g0 = __uint_as_float(r[4 * q]), g1 = __uint_as_float(r[4 * q + 1]);
-      const float g2 = __uint_as_float(r[4 * q + 2]), g3 = __uint_as_float(r[4 * q + 3]);
-      float4 nv, nw;
-      nv.x = p.sgd_mom * v4.x - p.sgd_lr * g0;  nw.x = w4.x + nv.x;
-      nv.y = p.sgd_mom * v4.y - p.sgd_lr * g1;  nw.y = w4.y + nv.y;
-      nv.z = p.sgd_mom * v4.z - p.sgd_lr * g2;  nw.z = w4.z + nv.z;
-      nv.w = p.sgd_mom * v4.w - p.sgd_lr * g3;  nw.w = w4.w + nv.w;
-      reinterpret_cast<float4*>(gr)[q] = make_float4(g0, g1, g2, g3);
-      reinterpret_cast<float4*>(vr)[q] = nv;
-      reinterpret_cast<float4*>(wr)[q] = nw;
-      if (sr) {
-        uint2 o;
-        o.x = pack_bf16x2(nw.x, nw.y);
-        o.y = pack_bf16x2(nw.z, nw.w);
-        reinterpret_cast<uint2*>(sr)[q] = o;
-      }
+  for (int j = 0; j < 32; ++j) slot[lane * 33 + j] = __uint_as_float(r[j]);
+  __syncwarp();
+  const int n = n0 + lane;
+  const bool col_ok = n < p.N;
+  // half a piece at a time: its 32 loads in flight at once, then the updates
+#pragma unroll
+  for (int h = 0; h < 32; h += 16) {
+    float wv[16], vv[16];
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+      const int m = row0 + h + rr;
+      const size_t off = (size_t)m * p.ldc + n;
+      const bool ok = col_ok && m < p.M;
+      wv[rr] = ok ? p.sgd_w[off] : 0.f;
+      vv[rr] = ok ? p.sgd_v[off] : 0.f;
     }
-  } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (n0 + j < p.N) {
-        const float g = __uint_as_float(r[j]);
-        const float nv = p.sgd_mom * vr[j] - p.sgd_lr * g;
-        const float nw = wr[j] + nv;
-        gr[j] = g;
-        vr[j] = nv;
-        wr[j] = nw;
-        if (sr) sr[j] = f32_to_bf16(nw);
+    for (int rr = 0; rr < 16; ++rr) {
+      const int m = row0 + h + rr;
+      if (col_ok && m < p.M) {
+        const float g = slot[(h + rr) * 33 + lane];
+        const size_t off = (size_t)m * p.ldc + n;
+        const float nv = p.sgd_mom * vv[rr] - p.sgd_lr * g;
+        const float nw = wv[rr] + nv;
+        static_cast<float*>(p.C)[off] = g;
+        p.sgd_v[off] = nv;
+        p.sgd_w[off] = nw;
+        if (p.sgd_shadow && m < p.sgd_shadow_rows)
+          p.sgd_shadow[(size_t)m * p.sgd_ld_shadow + n] = f32_to_bf16(nw);
       }
     }
   }
@@ -289,8 +283,9 @@ __device__ __forceinline__ void sgd_epilogue_chunk(const TcParams& p, int m, int
 // with zeros to xent_ldd, and the argmax (lowest index among ties); returns
 // the row loss m + ln(sum exp(z - m)) - z_label.
 __device__ __forceinline__ float xent_epilogue_row(const TcParams& p, int m,
-                                                   const uint32_t (&r)[32]) {
-  int y = __ldg(p.xent_labels + m);
+                                                   const uint32_t (&r)[32], const int* labels,
+                                                   int* argmax) {
+  int y = __ldg(labels + m);
   y = y < 0 ? 0 : (y >= p.N ? p.N - 1 : y);
   float z[32];
   float mx = -INFINITY, zy = 0.f;
@@ -306,9 +301,17 @@ __device__ __forceinline__ float xent_epilogue_row(const TcParams& p, int m,
   }
   if (p.C) {
     float* lrow = static_cast<float*>(p.C) + (size_t)m * p.ldc;
+    if ((reinterpret_cast<uintptr_t>(lrow) & 7) == 0) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < p.N) lrow[j] = z[j];
+      for (int j = 0; j < 32; j += 2) {
+        if (j + 1 < p.N) *reinterpret_cast<float2*>(lrow + j) = make_float2(z[j], z[j + 1]);
+        else if (j < p.N) lrow[j] = z[j];
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < p.N) lrow[j] = z[j];
+    }
   }
   float s = 0.f;
 #pragma unroll
@@ -318,16 +321,45 @@ __device__ __forceinline__ float xent_epilogue_row(const TcParams& p, int m,
   }
   const float inv = 1.0f / (float)p.xent_norm;
   __nv_bfloat16* drow = p.xent_dlog + (size_t)m * p.xent_ldd;
+  float d[32];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    if (j < p.xent_ldd) {
-      float d = 0.f;
-      if (j < p.N) d = (z[j] / s - (j == y ? 1.f : 0.f)) * inv;
-      drow[j] = f32_to_bf16(d);
-    }
+  for (int j = 0; j < 32; ++j)
+    d[j] = j < p.N ? (z[j] / s - (j == y ? 1.f : 0.f)) * inv : 0.f;
+  if ((p.xent_ldd & 7) == 0 && (reinterpret_cast<uintptr_t>(drow) & 15) == 0) {
+    // rows of a multiple of 8 bf16: 16-byte stores
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (8 * q < p.xent_ldd)
+        reinterpret_cast<uint4*>(drow)[q] =
+            make_uint4(pack_bf16x2(d[8 * q], d[8 * q + 1]), pack_bf16x2(d[8 * q + 2], d[8 * q + 3]),
+                       pack_bf16x2(d[8 * q + 4], d[8 * q + 5]),
+                       pack_bf16x2(d[8 * q + 6], d[8 * q + 7]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < p.xent_ldd) drow[j] = f32_to_bf16(d[j]);
   }
-  if (p.xent_argmax) p.xent_argmax[m] = am;
+  if (argmax) argmax[m] = am;
   return mx + logf(s) - zy;
+}
+
+// L1 prefetch of what the epilogue of row m, columns [n0, n0 + bn) will
+// read (bias, labels, ReLU mask, the SGD state), issued while the MMAs of
+// the tile still run so the epilogue does not wait on L2 or HBM latency.
+__device__ __forceinline__ void epilogue_prefetch(const TcParams& p, int m, int n0, int bn,
+                                                  int lane, const int* labels) {
+  if (p.bias && lane == 0)
+    for (int c = 0; c < bn && n0 + c < p.N; c += 32) ptx::prefetch_l1(p.bias + n0 + c);
+  if (m >= p.M) return;
+  if (labels) ptx::prefetch_l1(labels + m);
+  if (p.mask)
+    for (int c = 0; c < bn && n0 + c < p.N; c += 64)
+      ptx::prefetch_l1(static_cast<const __nv_bfloat16*>(p.mask) + (size_t)m * p.ldm + n0 + c);
+  if (p.sgd_w)
+    for (int c = 0; c < bn && n0 + c < p.N; c += 32) {
+      ptx::prefetch_l1(p.sgd_w + (size_t)m * p.ldc + n0 + c);
+      ptx::prefetch_l1(p.sgd_v + (size_t)m * p.ldc + n0 + c);
+    }
 }
 
 template <int BN, int STAGES>
@@ -479,16 +511,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stg_count = 0;  // staged boxes issued by this warp
     for (int u = blockIdx.x; u < p.num_tiles * p.splits; u += gridDim.x) {
       if (*s_abort) break;
+      int tm, tn;
+      tile_coords(u / p.splits, p.tiles_m, p.tiles_n, tm, tn);
+      const int m = tm * BM + row;
+      epilogue_prefetch(p, m, tn * BN, BN, lane, p.xent_labels);
       if (!ptx::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err, DEVERR_TIMEOUT_EPILOGUE)) {
         *s_abort = 1;
         break;
       }
       ptx::tc_fence_after();
-      int tm, tn;
-      tile_coords(u / p.splits, p.tiles_m, p.tiles_n, tm, tn);
       float* part = p.splits > 1 ? p.partial + (size_t)(u % p.splits) * p.M * p.ldp : nullptr;
       float row_loss = 0.f;
-      const int m = tm * BM + row;
       for (int c0 = 0; c0 < BN; c0 += 32) {
         const int n0 = tn * BN + c0;
         if (n0 >= p.N) break;  // warp-uniform
@@ -501,7 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 r);
         ptx::tmem_ld_wait();
         const float* sb = stage_bias(p, n0, sbias + (warp - 2) * 32, lane);
-        if (m < p.M) {
+        if (p.sgd_w) {
+          sgd_epilogue_staged(p, tm * BM + quarter * 32, n0, r,
+                              reinterpret_cast<float*>(stg + (warp - 2) * 8192), lane);
+        } else if (m < p.M) {
           if (part) {
             float* prow = part + (size_t)m * p.ldp + n0;
             if (n0 + 32 <= p.N) {
@@ -519,9 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n0 + j < p.N) prow[j] = __uint_as_float(r[j]);
             }
           } else if (p.xent_labels) {
-            row_loss = xent_epilogue_row(p, m, r);
-          } else if (p.sgd_w) {
-            sgd_epilogue_chunk(p, m, n0, r);
+            row_loss = xent_epilogue_row(p, m, r, p.xent_labels, p.xent_argmax);
           } else if (!p.tma_store) {
             float v[32];
             epilogue_values(p, m, n0, r, sb, mp, v);
@@ -581,6 +615,378 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < STAGES; ++s)
       if (last_parity[s] >= 0)
         ptx::mbar_wait_bounded(&full[s], (uint32_t)last_parity[s], p.wait_ns, p.err,
+                               DEVERR_TIMEOUT_TEARDOWN);
+  }
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ step programs
+//
+// A training step of a small MLP is a chain of small GEMMs, each of which is
+// latency-bound (microseconds of TMA round trips and epilogue for a few
+// MFLOP).  A step program runs the whole chain in ONE cooperative launch:
+// the same warp roles as tc_gemm_kernel, a persistent CTA per SM, and the
+// GEMMs of each phase spread over the CTAs by tile; a grid-wide barrier
+// separates phases (a phase only reads what earlier phases wrote).  Phase 0
+// may cast the input batch to bf16.  The tensor memory, the mbarrier rings
+// and their phase bits live across phases.
+
+constexpr int kStepMaxPhases = kStepMaxGemms + 1;
+constexpr int STEP_BN = 64;
+constexpr int STEP_STAGES = 8;
+
+struct StepPhaseDev {
+  int kind;  // 0: GEMM tiles, 1: input cast
+  int g0, n_gemm, tiles;
+};
+
+struct StepProgram {
+  CUtensorMap ta[kStepMaxGemms];
+  CUtensorMap tb[kStepMaxGemms];
+  TcParams gp[kStepMaxGemms];
+  int tile_base[kStepMaxGemms];  // first tile of GEMM g within its phase
+  StepPhaseDev ph[kStepMaxPhases];
+  int n_phases;
+  const void* cast_src;
+  int cast_dtype;
+  __nv_bfloat16* cast_dst;
+  int cast_rows, cast_cols, cast_ld;
+  unsigned* bar;  // [arrivals, generation]
+  unsigned long long wait_ns;
+  int* err;
+  int n_steps;
+  long long cast_stride, label_stride, loss_stride, argmax_stride;
+  int xent_g;  // the GEMM with the fused loss (-1: none)
+};
+
+// passed by value as the kernel's parameter block (limit 32,764 bytes)
+static_assert(sizeof(StepProgram) <= 32000, "step program exceeds the kernel parameter limit");
+
+// Grid-wide barrier of the step program (all threads of every CTA call it).
+// Writers' global stores are ordered before the arrival by the CTA barrier
+// and a device-scope fence; the proxy fences let the next phase's TMA loads
+// (async proxy) see data written with ordinary stores.  Bounded: on a
+// timeout the error word is set and the CTA's abort flag raised.
+__device__ __forceinline__ void step_grid_sync(const StepProgram& prog, volatile int* s_abort) {
+  asm volatile("fence.proxy.async;" ::: "memory");
+  __syncthreads();
+  if (threadIdx.x == 0 && !*s_abort) {
+    unsigned* count = prog.bar;
+    unsigned* gen = prog.bar + 1;
+    unsigned g0, prev;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g0) : "l"(gen) : "memory");
+    // the arrival releases this CTA's writes (ordered before it by the CTA
+    // barrier above) at device scope
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(count) : "memory");
+    if (prev == gridDim.x - 1) {
+      asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(count) : "memory");
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(gen), "r"(g0 + 1u) : "memory");
+    } else {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (true) {
+        unsigned gv;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(gv) : "l"(gen) : "memory");
+        if (gv != g0) break;
+        if (ptx::globaltimer_ns() - t0 > prog.wait_ns) {
+          record_device_error(prog.err, DEVERR_TIMEOUT_GRID);
+          *s_abort = 1;
+          break;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  asm volatile("fence.proxy.async;" ::: "memory");
+}
+
+__device__ __forceinline__ float step_load_in(const void* src, int dtype, size_t i) {
+  if (dtype == MLP_DTYPE_U8) return (float)static_cast<const uint8_t*>(src)[i] / 255.0f;
+  if (dtype == MLP_DTYPE_BF16) return bf16_to_f32(static_cast<const __nv_bfloat16*>(src)[i]);
+  return static_cast<const float*>(src)[i];
+}
+
+// GEMM g of phase ph that owns the phase's tile u, and u's index within it.
+__device__ __forceinline__ int step_gemm_of(const StepProgram& prog, const StepPhaseDev& ph, int u,
+                                            int& local) {
+  int g = ph.g0;
+  for (int k = 1; k < ph.n_gemm; ++k)
+    if (u >= prog.tile_base[ph.g0 + k]) g = ph.g0 + k;
+  local = u - prog.tile_base[g];
+  return g;
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_step_kernel(const __grid_constant__ StepProgram prog) {
+  using L = Layout<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ float xent_part[4];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * L::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * L::B_BYTES);
+  uint8_t* stg = sB + STAGES * L::B_BYTES + L::BAR_BYTES;  // per epilogue warp 8 KiB
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint64_t* xent_bar = done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xent_bar + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* sbias = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 4);
+    }
+    ptx::mbar_init(done, 1);
+    ptx::mbar_init(xent_bar, 4);
+    *s_abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    // the operand descriptors of every GEMM this CTA will load, ahead of use
+    for (int phi = 0; phi < prog.n_phases; ++phi) {
+      const StepPhaseDev ph = prog.ph[phi];
+      if (ph.kind != 0 || (int)blockIdx.x >= ph.tiles) continue;
+      for (int g = ph.g0 + lane; g < ph.g0 + ph.n_gemm; g += 32) {
+        ptx::prefetch_tensormap(&prog.ta[g]);
+        ptx::prefetch_tensormap(&prog.tb[g]);
+      }
+    }
+  }
+  if (warp == 1) ptx::tmem_alloc(tmem_slot, L::TMEM_COLS);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // pipeline positions of the producer and the MMA issuer, and the
+  // accumulator hand-off of the MMA issuer and the epilogue, across phases
+  int stage = 0;
+  uint32_t phase = 0;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  int last_parity[STAGES];
+  for (int s = 0; s < STAGES; ++s) last_parity[s] = -1;
+  int xent_uses = 0;
+
+  const int n_total = prog.n_steps * prog.n_phases;
+  for (int it = 0; it < n_total && !*s_abort; ++it) {
+    const int step = it / prog.n_phases, phi = it % prog.n_phases;
+    const StepPhaseDev ph = prog.ph[phi];
+    if (ph.kind == 1) {
+      // input rows -> bf16 rows of pitch cast_ld (image bytes are byte / 255)
+      const long long stride = (long long)gridDim.x * blockDim.x;
+      const long long first = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+      const void* src = static_cast<const uint8_t*>(prog.cast_src) + step * prog.cast_stride;
+      if (prog.cast_dtype == MLP_DTYPE_U8 && (prog.cast_cols & 7) == 0 &&
+          (prog.cast_ld & 7) == 0 && (reinterpret_cast<uintptr_t>(src) & 7) == 0) {
+        // 8 bytes in, 8 bf16 (16 bytes) out per thread and step
+        const int vpr = prog.cast_cols / 8;
+        const long long n = (long long)prog.cast_rows * vpr;
+        for (long long i = first; i < n; i += stride) {
+          const int r = (int)(i / vpr), q = (int)(i % vpr);
+          const uint2 b = reinterpret_cast<const uint2*>(src)[i];
+          const uint8_t* u8 = reinterpret_cast<const uint8_t*>(&b);
+          uint4 o;
+          o.x = pack_bf16x2((float)u8[0] / 255.0f, (float)u8[1] / 255.0f);
+          o.y = pack_bf16x2((float)u8[2] / 255.0f, (float)u8[3] / 255.0f);
+          o.z = pack_bf16x2((float)u8[4] / 255.0f, (float)u8[5] / 255.0f);
+          o.w = pack_bf16x2((float)u8[6] / 255.0f, (float)u8[7] / 255.0f);
+          reinterpret_cast<uint4*>(prog.cast_dst + (size_t)r * prog.cast_ld)[q] = o;
+        }
+      } else {
+        const long long n = (long long)prog.cast_rows * prog.cast_cols;
+        for (long long i = first; i < n; i += stride) {
+          const int r = (int)(i / prog.cast_cols), c = (int)(i % prog.cast_cols);
+          prog.cast_dst[(size_t)r * prog.cast_ld + c] =
+              f32_to_bf16(step_load_in(src, prog.cast_dtype, (size_t)i));
+        }
+      }
+    } else if (warp == 0) {
+      if (lane == 0) {
+        // ---------------------------------------------------------- producer
+        for (int u = blockIdx.x; u < ph.tiles && !*s_abort; u += gridDim.x) {
+          int t;
+          const int g = step_gemm_of(prog, ph, u, t);
+          const TcParams& p = prog.gp[g];
+          int tm, tn;
+          tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1, prog.wait_ns, prog.err,
+                                        DEVERR_TIMEOUT_PRODUCER)) {
+              *s_abort = 1;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+            last_parity[stage] = (int)phase;
+            const int k0 = kb * BK;
+            uint8_t* a_dst = sA + stage * L::A_BYTES;
+            uint8_t* b_dst = sB + stage * L::B_BYTES;
+            if (!p.a_mn) {
+              ptx::tma_load_2d(a_dst, &prog.ta[g], &full[stage], k0, tm * BM);
+            } else {
+              ptx::tma_load_2d(a_dst, &prog.ta[g], &full[stage], tm * BM, k0);
+              ptx::tma_load_2d(a_dst + 8192, &prog.ta[g], &full[stage], tm * BM + 64, k0);
+            }
+            if (!p.b_mn) {
+              ptx::tma_load_2d(b_dst, &prog.tb[g], &full[stage], k0, tn * BN);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                ptx::tma_load_2d(b_dst + j * 8192, &prog.tb[g], &full[stage], tn * BN + j * 64,
+                                 k0);
+            }
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          }
+        }
+      }
+    } else if (warp == 1) {
+      if (lane == 0) {
+        // ---------------------------------------------------------- MMA issuer
+        for (int u = blockIdx.x; u < ph.tiles && !*s_abort; u += gridDim.x) {
+          int t;
+          const int g = step_gemm_of(prog, ph, u, t);
+          const TcParams& p = prog.gp[g];
+          const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
+          const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
+          const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
+          const uint32_t a_kstep = p.a_mn ? 2048u : 32u;
+          const uint32_t b_kstep = p.b_mn ? 2048u : 32u;
+          if (!ptx::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, prog.wait_ns, prog.err,
+                                      DEVERR_TIMEOUT_MMA)) {
+            *s_abort = 1;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+          bool ok = true;
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!ptx::mbar_wait_bounded(&full[stage], phase, prog.wait_ns, prog.err,
+                                        DEVERR_TIMEOUT_MMA)) {
+              *s_abort = 1;
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t a_base = ptx::smem_u32(sA + stage * L::A_BYTES);
+            const uint32_t b_base = ptx::smem_u32(sB + stage * L::B_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint64_t ad = ptx::sw128_desc(a_base + k * a_kstep, a_lbo, 1024);
+              const uint64_t bd = ptx::sw128_desc(b_base + k * b_kstep, b_lbo, 1024);
+              ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(&empty[stage]);
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          ptx::mma_commit(&tfull[acc]);
+          if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+      }
+    } else {
+      // ------------------------------------------------------------ epilogue
+      const int quarter = warp & 3;
+      const int row = quarter * 32 + lane;
+      for (int u = blockIdx.x; u < ph.tiles; u += gridDim.x) {
+        if (*s_abort) break;
+        int t;
+        const int g = step_gemm_of(prog, ph, u, t);
+        const TcParams& p = prog.gp[g];
+        // the loss GEMM's labels and outputs of this step
+        const int* labels = p.xent_labels ? p.xent_labels + step * prog.label_stride : nullptr;
+        int* argmax = p.xent_argmax ? p.xent_argmax + step * prog.argmax_stride : nullptr;
+        float* loss_out = p.xent_loss ? p.xent_loss + step * prog.loss_stride : nullptr;
+        int tm, tn;
+        tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
+        const int m = tm * BM + row;
+        epilogue_prefetch(p, m, tn * BN, BN, lane, labels);
+        if (!ptx::mbar_wait_bounded(&tfull[acc], acc_phase, prog.wait_ns, prog.err,
+                                    DEVERR_TIMEOUT_EPILOGUE)) {
+          *s_abort = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+        float row_loss = 0.f;
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          const int n0 = tn * BN + c0;
+          if (n0 >= p.N) break;  // warp-uniform
+          MaskPiece mp;
+          load_mask(p, m, n0, mp);
+          uint32_t r[32];
+          __syncwarp();
+          ptx::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                      (uint32_t)(acc * BN + c0),
+                                  r);
+          ptx::tmem_ld_wait();
+          const float* sb = stage_bias(p, n0, sbias + (warp - 2) * 32, lane);
+          if (p.sgd_w) {
+            sgd_epilogue_staged(p, tm * BM + quarter * 32, n0, r,
+                                reinterpret_cast<float*>(stg + (warp - 2) * 8192), lane);
+          } else if (m < p.M) {
+            if (p.xent_labels) {
+              row_loss = xent_epilogue_row(p, m, r, labels, argmax);
+            } else {
+              float v[32];
+              epilogue_values(p, m, n0, r, sb, mp, v);
+              epilogue_store_regs(p, m, n0, v);
+            }
+          }
+        }
+        if (p.xent_labels) {
+          float v = m < p.M ? row_loss : 0.f;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) {
+            xent_part[quarter] = v;
+            ptx::mbar_arrive(xent_bar);
+          }
+          if (warp == 2 && lane == 0 &&
+              ptx::mbar_wait_bounded(xent_bar, (uint32_t)(xent_uses & 1), prog.wait_ns, prog.err,
+                                     DEVERR_TIMEOUT_EPILOGUE))
+            *loss_out = (((xent_part[0] + xent_part[1]) + xent_part[2]) + xent_part[3]) /
+                        (float)p.xent_norm;
+          ++xent_uses;
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+    }
+    if (it + 1 < n_total) step_grid_sync(prog, s_abort);
+  }
+
+  // teardown: the MMA issuer's last MMAs are complete before the tensor
+  // memory is freed; after an abort, copies still in flight land first
+  if (warp == 1 && lane == 0) {
+    ptx::mma_commit(done);
+    ptx::mbar_wait_bounded(done, 0, prog.wait_ns, prog.err, DEVERR_TIMEOUT_TEARDOWN);
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (*s_abort && warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s)
+      if (last_parity[s] >= 0)
+        ptx::mbar_wait_bounded(&full[s], (uint32_t)last_parity[s], prog.wait_ns, prog.err,
                                DEVERR_TIMEOUT_TEARDOWN);
   }
   __syncwarp();
@@ -925,7 +1331,7 @@ mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
     const int which = BN == 64 ? 0 : (BN == 128 ? 1 : 2);
     LaunchScope ls(p.splits > 1 ? split_names[which] : names[which], st, p.M, p.N, p.K);
     launch_k(tc_gemm_kernel<BN, STAGES>, dim3(grid), dim3(kThreads),
-             p.tma_store ? L::SMEM : L::SMEM_BASE, st, ta, tb, tc, p);
+             p.tma_store || p.sgd_w ? L::SMEM : L::SMEM_BASE, st, ta, tb, tc, p);
   }
   MLP_CHECK(launch_status());
   if (p.splits > 1) {
@@ -1032,7 +1438,154 @@ GemmPlan gemm_plan(int M, int N, int K, bool fused) {
   return pl;
 }
 
+// Kernel parameters and operand tensor maps of one GEMM for a tile grid of
+// tiles_m x ceil(N / BN) (K-major B boxes of b_box_rows rows).
+mlp_status prepare_tc(const GemmArgs& g, int tiles_m, int BN, int splits, int kb_per_split,
+                      int b_box_rows, unsigned long long wait_ns, TcParams* pp, CUtensorMap* ta,
+                      CUtensorMap* tb) {
+  TcParams& p = *pp;
+  p.M = g.M; p.N = g.N; p.K = g.K;
+  p.a_mn = g.a_trans ? 1 : 0;       // A stored [K][M]  -> M-major tiles
+  p.b_mn = g.b_trans ? 0 : 1;       // B stored [K][N]  -> N-major tiles
+  p.tiles_m = tiles_m;
+  p.tiles_n = (g.N + BN - 1) / BN;
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.k_blocks = (g.K + BK - 1) / BK;
+  p.bias = g.bias;
+  p.act = g.act;
+  p.mask = static_cast<const __nv_bfloat16*>(g.mask);
+  p.ldm = g.ldm;
+  p.C = g.C;
+  p.ldc = g.ldc;
+  p.c_bf16 = g.c_bf16;
+  p.wait_ns = wait_ns;
+  p.splits = splits;
+  p.kb_per_split = kb_per_split;
+  p.ldp = (g.N + 3) / 4 * 4;
+  p.partial = splits > 1 ? static_cast<float*>(g.ws) : nullptr;
+  p.xent_labels = g.xent_labels;
+  p.xent_dlog = static_cast<__nv_bfloat16*>(g.xent_dlog);
+  p.xent_ldd = g.xent_ldd;
+  p.xent_loss = g.xent_loss;
+  p.xent_argmax = g.xent_argmax;
+  p.xent_norm = g.xent_norm;
+  p.sgd_w = g.sgd_w;
+  p.sgd_v = g.sgd_v;
+  p.sgd_lr = g.sgd_lr;
+  p.sgd_mom = g.sgd_mom;
+  p.sgd_shadow = g.sgd_shadow;
+  p.sgd_ld_shadow = g.sgd_ld_shadow;
+  p.sgd_shadow_rows = g.sgd_shadow_rows;
+  p.tma_store = 0;
+  if (p.xent_labels && (p.num_tiles != 1 || g.N > 32 || !p.xent_dlog || !p.xent_loss))
+    return MLP_ERR_UNSUPPORTED_SHAPE;
+  if ((p.xent_labels || p.sgd_w) && splits > 1) return MLP_ERR_UNSUPPORTED_SHAPE;
+  p.err = device_error_word();
+  if (!p.err) return MLP_ERR_CUDA;
+
+  bool ok;
+  if (!p.a_mn)
+    ok = encode_tmap_bf16_2d(ta, g.A, g.K, g.M, (unsigned long long)g.lda * 2, 64, BM);
+  else
+    ok = encode_tmap_bf16_2d(ta, g.A, g.M, g.K, (unsigned long long)g.lda * 2, 64, 64);
+  if (!ok) return MLP_ERR_CUDA;
+  if (!p.b_mn)
+    ok = encode_tmap_bf16_2d(tb, g.B, g.K, g.N, (unsigned long long)g.ldb * 2, 64, b_box_rows);
+  else
+    ok = encode_tmap_bf16_2d(tb, g.B, g.N, g.K, (unsigned long long)g.ldb * 2, 64, 64);
+  if (!ok) return MLP_ERR_CUDA;
+  return MLP_OK;
+}
+
 }  // namespace
+
+bool step_gemm_supported(const GemmArgs& g) {
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0) return false;
+  const int tiles = ((g.M + BM - 1) / BM) * ((g.N + STEP_BN - 1) / STEP_BN);
+  if (tiles > num_sms()) return false;
+  if (g.xent_labels && (g.M > BM || g.N > 32)) return false;
+  // one pass over K, accumulator in tensor memory: no split-K
+  return true;
+}
+
+mlp_status launch_step_program(const StepSpec& s, unsigned* bar_words, unsigned long long wait_ns,
+                               cudaStream_t st) {
+  using L = Layout<STEP_BN, STEP_STAGES>;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(tc_step_kernel<STEP_BN, STEP_STAGES>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
+      return MLP_ERR_CUDA;
+    configured = true;
+  }
+  if (s.n_gemm < 0 || s.n_gemm > kStepMaxGemms || !bar_words) return MLP_ERR_INVALID_ARG;
+  StepProgram prog;  // ~12 KiB of kernel parameters
+  memset(&prog, 0, sizeof(prog));
+  int np = 0;
+  if (s.cast_src && s.cast_rows > 0 && s.cast_cols > 0) {
+    prog.ph[np++] = StepPhaseDev{1, 0, 0, 0};
+    prog.cast_src = s.cast_src;
+    prog.cast_dtype = s.cast_dtype;
+    prog.cast_dst = static_cast<__nv_bfloat16*>(s.cast_dst);
+    prog.cast_rows = s.cast_rows;
+    prog.cast_cols = s.cast_cols;
+    prog.cast_ld = s.cast_ld;
+  }
+  int grid = 1;
+  for (int g = 0; g < s.n_gemm; ++g) {
+    const GemmArgs& a = s.gemm[g];
+    if (!step_gemm_supported(a)) return MLP_ERR_UNSUPPORTED_SHAPE;
+    if (g > 0 && s.phase[g] < s.phase[g - 1]) return MLP_ERR_INVALID_ARG;
+    MLP_CHECK(prepare_tc(a, (a.M + BM - 1) / BM, STEP_BN, 1, (a.K + BK - 1) / BK, STEP_BN, wait_ns,
+                         &prog.gp[g], &prog.ta[g], &prog.tb[g]));
+    if (g == 0 || s.phase[g] != s.phase[g - 1]) {
+      if (np >= kStepMaxPhases) return MLP_ERR_INVALID_ARG;
+      prog.ph[np++] = StepPhaseDev{0, g, 0, 0};
+    }
+    StepPhaseDev& ph = prog.ph[np - 1];
+    prog.tile_base[g] = ph.tiles;
+    ph.tiles += prog.gp[g].num_tiles;
+    ph.n_gemm += 1;
+    if (ph.tiles > grid) grid = ph.tiles;
+  }
+  if (np == 0) return MLP_OK;
+  if (grid > num_sms()) return MLP_ERR_UNSUPPORTED_SHAPE;
+  if (s.n_steps < 1) return MLP_ERR_INVALID_ARG;
+  prog.n_phases = np;
+  prog.n_steps = s.n_steps;
+  prog.cast_stride = s.cast_stride;
+  prog.label_stride = s.label_stride;
+  prog.loss_stride = s.loss_stride;
+  prog.argmax_stride = s.argmax_stride;
+  prog.xent_g = -1;
+  for (int g = 0; g < s.n_gemm; ++g)
+    if (s.gemm[g].xent_labels) prog.xent_g = g;
+  prog.bar = bar_words;
+  prog.wait_ns = wait_ns;
+  prog.err = device_error_word();
+  if (!prog.err) return MLP_ERR_CUDA;
+  // a clean barrier for this launch, even after an abandoned one
+  if (cudaMemsetAsync(bar_words, 0, 2 * sizeof(unsigned), st) != cudaSuccess) return MLP_ERR_CUDA;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::SMEM;  // with the epilogue staging (fused SGD)
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident: the grid barrier needs it
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // recorded shape: steps, GEMM flops per step (2 M N K summed), GEMMs
+  long long flops = 0;
+  for (int g = 0; g < s.n_gemm; ++g)
+    flops += 2ll * s.gemm[g].M * s.gemm[g].N * s.gemm[g].K;
+  LaunchScope ls("step_program", st, s.n_steps, flops, s.n_gemm);
+  if (cudaLaunchKernelEx(&cfg, tc_step_kernel<STEP_BN, STEP_STAGES>, prog) != cudaSuccess)
+    return MLP_ERR_CUDA;
+  return launch_status();
+}
 
 size_t gemm_tc_splitk_bytes(int M, int N, int K) {
   const GemmPlan pl = gemm_plan(M, N, K, false);
@@ -1070,59 +1623,10 @@ mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStr
   else if (tiles_for(256) < sms) BN = tiles_for(128) < sms ? 64 : 128;
   if (!pl.pair && splits == 1 && BN == 128 && tiles_for(128) < sms / 2 && g.N > 64) BN = 64;
 
-  TcParams p;
-  p.M = g.M; p.N = g.N; p.K = g.K;
-  p.a_mn = g.a_trans ? 1 : 0;       // A stored [K][M]  -> M-major tiles
-  p.b_mn = g.b_trans ? 0 : 1;       // B stored [K][N]  -> N-major tiles
-  p.tiles_m = tiles_m;
-  p.tiles_n = (g.N + BN - 1) / BN;
-  p.num_tiles = p.tiles_m * p.tiles_n;
-  p.k_blocks = (g.K + BK - 1) / BK;
-  p.bias = g.bias;
-  p.act = g.act;
-  p.mask = static_cast<const __nv_bfloat16*>(g.mask);
-  p.ldm = g.ldm;
-  p.C = g.C;
-  p.ldc = g.ldc;
-  p.c_bf16 = g.c_bf16;
-  p.wait_ns = wait_ns;
-  p.splits = splits;
-  p.kb_per_split = kb_per_split;
-  p.ldp = (g.N + 3) / 4 * 4;
-  p.partial = splits > 1 ? static_cast<float*>(g.ws) : nullptr;
-  p.xent_labels = g.xent_labels;
-  p.xent_dlog = static_cast<__nv_bfloat16*>(g.xent_dlog);
-  p.xent_ldd = g.xent_ldd;
-  p.xent_loss = g.xent_loss;
-  p.xent_argmax = g.xent_argmax;
-  p.xent_norm = g.xent_norm;
-  p.sgd_w = g.sgd_w;
-  p.sgd_v = g.sgd_v;
-  p.sgd_lr = g.sgd_lr;
-  p.sgd_mom = g.sgd_mom;
-  p.sgd_shadow = g.sgd_shadow;
-  p.sgd_ld_shadow = g.sgd_ld_shadow;
-  p.sgd_shadow_rows = g.sgd_shadow_rows;
-  if (p.xent_labels && (p.num_tiles != 1 || g.N > 32 || !p.xent_dlog || !p.xent_loss))
-    return MLP_ERR_UNSUPPORTED_SHAPE;
-  if ((p.xent_labels || p.sgd_w) && splits > 1) return MLP_ERR_UNSUPPORTED_SHAPE;
-  p.err = device_error_word();
-  if (!p.err) return MLP_ERR_CUDA;
-
   CUtensorMap ta, tb;
-  bool ok;
-  if (!p.a_mn)
-    ok = encode_tmap_bf16_2d(&ta, g.A, g.K, g.M, (unsigned long long)g.lda * 2, 64, BM);
-  else
-    ok = encode_tmap_bf16_2d(&ta, g.A, g.M, g.K, (unsigned long long)g.lda * 2, 64, 64);
-  if (!ok) return MLP_ERR_CUDA;
-  // K-major B boxes: BN rows, or each pair CTA's 128 of the tile's 256
-  if (!p.b_mn)
-    ok = encode_tmap_bf16_2d(&tb, g.B, g.K, g.N, (unsigned long long)g.ldb * 2, 64,
-                             pl.pair ? 128 : BN);
-  else
-    ok = encode_tmap_bf16_2d(&tb, g.B, g.N, g.K, (unsigned long long)g.ldb * 2, 64, 64);
-  if (!ok) return MLP_ERR_CUDA;
+  TcParams p;
+  MLP_CHECK(prepare_tc(g, tiles_m, BN, splits, kb_per_split, pl.pair ? 128 : BN, wait_ns, &p, &ta,
+                       &tb));
 
   // Output through TMA stores when the output is large (for small outputs the
   // staging round trip costs more latency than it saves), rows are 16-byte

@@ -88,6 +88,34 @@ mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStr
 // Scratch bytes a split-K launch of this shape would use (0: no split).
 size_t gemm_tc_splitk_bytes(int M, int N, int K);
 
+// k_gemm_tc.cu: one training step of a small MLP as ONE cooperative launch.
+// Phase 0 optionally casts the input rows to bf16; then phases of mutually
+// independent tensor-core GEMMs (bf16 operands, single-CTA 128 x 64 tiles,
+// no split-K, fused epilogues as in launch_gemm_tc) run one after another,
+// separated by grid-wide barriers, on one persistent CTA per SM.
+constexpr int kStepMaxGemms = 24;
+struct StepSpec {
+  const void* cast_src = nullptr;
+  int cast_dtype = 0;
+  void* cast_dst = nullptr;  // bf16 rows of pitch cast_ld
+  int cast_rows = 0, cast_cols = 0, cast_ld = 0;
+  int n_gemm = 0;
+  GemmArgs gemm[kStepMaxGemms];
+  int phase[kStepMaxGemms];  // >= 1, non-decreasing; equal phases run together
+  // The program may run n_steps times back to back in the same launch (one
+  // grid barrier between steps); step s reads the cast source at
+  // cast_src + s * cast_stride bytes and its loss GEMM uses labels +
+  // s * label_stride, loss + s * loss_stride, argmax + s * argmax_stride.
+  int n_steps = 1;
+  long long cast_stride = 0, label_stride = 0, loss_stride = 0, argmax_stride = 0;
+};
+// Whether launch_step_program can run this GEMM inside a step program.
+bool step_gemm_supported(const GemmArgs& g);
+// bar_words: two zero-initialised unsigned words of device memory owned by
+// the caller (the grid barrier's arrival count and generation).
+mlp_status launch_step_program(const StepSpec& s, unsigned* bar_words, unsigned long long wait_ns,
+                               cudaStream_t st);
+
 // k_block.cu: the MLP block (d = 512).
 mlp_status launch_block_fwd(const void* x, const void* wg, const void* wd, int T, int hidden,
                             float eps, float slope, void* y, float* rstd, cudaStream_t st);

@@ -148,6 +148,70 @@ def test_bf16_fused_step_matches_unfused_sequence():
         (fused.shadow.float() - seq.shadow.float()).abs().max().item() <= 2 ** -7
 
 
+def test_bf16_epoch_matches_step_sequence():
+    """mlp_train_epoch runs the full-size steps as one launch (a grid barrier
+    between steps) and the remainder as an ordinary step: every result must
+    equal the step-by-step sequence bit for bit."""
+    B, n = 128, 3 * 128 + 40
+    p0 = synth.mlp_flat_params(DIMS)
+    xb = to_dev(synth.images_u8(n, 784))
+    y = to_dev(synth.labels(n, 10))
+    ep = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+    losses = torch.zeros(4, device="cuda")
+    am_e = torch.empty(n, dtype=torch.int32, device="cuda")
+    ep.train_epoch(xb, y, LR, MOM, B, losses_out=losses, argmax_out=am_e)
+    sq = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+    loss_s = torch.zeros(4, 4, device="cuda")
+    am_s = torch.empty(n, dtype=torch.int32, device="cuda")
+    for s in range(4):
+        a, b = s * B, min(n, (s + 1) * B)
+        sq.train_step(xb[a:b], y[a:b], LR, MOM, loss_out=loss_s[s], argmax_out=am_s[a:b])
+    torch.cuda.synchronize()
+    assert torch.equal(losses, loss_s[:, 0])
+    assert torch.equal(am_e, am_s)
+    for name in ("params", "velocity", "grads", "shadow"):
+        assert torch.equal(getattr(ep, name), getattr(sq, name)), name
+    assert M.get_device_status() == M.MLP_OK
+
+
+def test_bf16_epoch_rejects_misaligned_steps():
+    net = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=128)
+    xb = torch.zeros(12, 784, dtype=torch.uint8, device="cuda")
+    y = torch.zeros(12, dtype=torch.int32, device="cuda")
+    with pytest.raises(M.MlpError) as e:
+        net.train_epoch(xb, y, LR, MOM, 6)   # each step's labels would start on 24-byte steps
+    assert e.value.status == M.MLP_ERR_MISALIGNED
+
+
+def test_bf16_three_layer_step_program_matches_unfused_sequence():
+    """A three-layer net's step program merges each layer's update into the
+    next layer's input-gradient phase; it must equal the separate calls."""
+    dims = [200, 96, 48, 10]
+    B = 100
+    p0 = synth.mlp_flat_params(dims)
+    xb = to_dev(synth.normal_f32((B, 200), synth.STREAM_GENERIC + 3))
+    y = to_dev(synth.labels(B, 10))
+    fused = M.MLP(dims, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+    loss_f = torch.zeros(4, device="cuda")
+    for _ in range(2):
+        fused.train_step(xb, y, LR, MOM, loss_out=loss_f)
+    seq = M.MLP(dims, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+    logits = torch.empty(B, 10, device="cuda")
+    dl = torch.empty(B, 16, dtype=torch.bfloat16, device="cuda")
+    loss_s = torch.zeros(4, device="cuda")
+    ws = torch.empty(M.softmax_xent_workspace_bytes(B, 10) + 16, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        seq.forward(xb, logits)
+        M.softmax_xent_fwd_bwd(logits, y, loss_s, dlogits=dl, workspace=ws)
+        seq.backward(dl, B)
+        seq.sgd_step(LR, MOM)
+    torch.cuda.synchronize()
+    assert abs(loss_f[0].item() - loss_s[0].item()) <= 1e-6 * abs(loss_s[0].item())
+    assert torch.allclose(fused.params, seq.params, rtol=1e-6, atol=1e-8)
+    assert torch.allclose(fused.velocity, seq.velocity, rtol=1e-5, atol=1e-9)
+    assert M.get_device_status() == M.MLP_OK
+
+
 def test_bf16_forward_matches_oracle_exact_mode():
     B = 128
     p0 = synth.mlp_flat_params(DIMS)
