@@ -128,6 +128,20 @@ __device__ __forceinline__ void load_mask(const TcParams& p, int m, int n0, Mask
   }
 }
 
+// Bias value for lane `lane` of the 32-column piece at n0, loaded before the
+// accumulator is ready; stage_bias_reg publishes it in the warp's slot.
+__device__ __forceinline__ float load_bias_lane(const TcParams& p, int n0, int lane) {
+  return (p.bias && n0 + lane < p.N) ? __ldg(p.bias + n0 + lane) : 0.f;
+}
+__device__ __forceinline__ const float* stage_bias_reg(const TcParams& p, float b, float* slot,
+                                                       int lane) {
+  if (!p.bias) return nullptr;
+  __syncwarp();
+  slot[lane] = b;
+  __syncwarp();
+  return slot;
+}
+
 // Epilogue arithmetic of one 32-column piece of row m in fp32: + bias (from
 // the staged slot, if any), ReLU, ReLU mask (keep where the stored
 // activation is > 0).
@@ -272,6 +286,75 @@ __device__ __forceinline__ void sgd_epilogue_staged(const TcParams& p, int row0,
         if (p.sgd_shadow && m < p.sgd_shadow_rows)
           p.sgd_shadow[(size_t)m * p.sgd_ld_shadow + n] = f32_to_bf16(nw);
       }
+    }
+  }
+}
+
+// The SGD state (w, v) of a warp's 32 rows x 64 columns of a tile, copied
+// into shared memory ([32][64] floats each) with cp.async while the tile's
+// MMAs run; 16-byte copies where a row segment is whole and aligned, else
+// per element (zero-filled outside the matrix).  Completed by cp.async.wait_all.
+__device__ __forceinline__ void sgd_state_prefetch(const TcParams& p, int row0, int n_base,
+                                                   float* w_s, float* v_s, int lane) {
+  const int m = row0 + lane;
+  const bool vec = (p.ldc & 3) == 0 && (reinterpret_cast<uintptr_t>(p.sgd_w) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(p.sgd_v) & 15) == 0;
+  float* wr = w_s + lane * 64;
+  float* vr = v_s + lane * 64;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int n = n_base + 4 * q;
+    if (n >= p.N || m >= p.M) break;  // rows past M and columns past N are never read
+    const size_t off = (size_t)m * p.ldc + n;
+    if (vec && m < p.M && n + 3 < p.N) {
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ptx::smem_u32(wr + 4 * q)),
+                   "l"(p.sgd_w + off)
+                   : "memory");
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ptx::smem_u32(vr + 4 * q)),
+                   "l"(p.sgd_v + off)
+                   : "memory");
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool ok = m < p.M && n + e < p.N;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                         ptx::smem_u32(wr + 4 * q + e)),
+                     "l"(ok ? p.sgd_w + off + e : p.sgd_w), "r"(ok ? 4 : 0)
+                     : "memory");
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                         ptx::smem_u32(vr + 4 * q + e)),
+                     "l"(ok ? p.sgd_v + off + e : p.sgd_v), "r"(ok ? 4 : 0)
+                     : "memory");
+      }
+    }
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Momentum SGD as in sgd_epilogue_staged, with w and v of the piece taken
+// from the shared-memory copy (columns c0 .. c0 + 31 of the warp's rows).
+__device__ __forceinline__ void sgd_epilogue_smem(const TcParams& p, int row0, int n0, int c0,
+                                                  const uint32_t (&r)[32], float* slot,
+                                                  const float* w_s, const float* v_s, int lane) {
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) slot[lane * 33 + j] = __uint_as_float(r[j]);
+  __syncwarp();
+  const int n = n0 + lane;
+  const bool col_ok = n < p.N;
+#pragma unroll 8
+  for (int rr = 0; rr < 32; ++rr) {
+    const int m = row0 + rr;
+    if (col_ok && m < p.M) {
+      const float g = slot[rr * 33 + lane];
+      const size_t off = (size_t)m * p.ldc + n;
+      const float nv = p.sgd_mom * v_s[rr * 64 + c0 + lane] - p.sgd_lr * g;
+      const float nw = w_s[rr * 64 + c0 + lane] + nv;
+      static_cast<float*>(p.C)[off] = g;
+      p.sgd_v[off] = nv;
+      p.sgd_w[off] = nw;
+      if (p.sgd_shadow && m < p.sgd_shadow_rows)
+        p.sgd_shadow[(size_t)m * p.sgd_ld_shadow + n] = f32_to_bf16(nw);
     }
   }
 }
@@ -434,7 +517,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             *s_abort = 1;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+          // 64-wide boxes entirely past M (A M-major) or N (B N-major) are
+          // not loaded: they only feed accumulator rows / columns that are
+          // never stored, and a box of nothing but fill is slow to deliver
+          const bool a_hi = !p.a_mn || tm * BM + 64 < p.M;
+          uint32_t bytes = L::STAGE_BYTES - (a_hi ? 0u : 8192u);
+          if (p.b_mn) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              if (tn * BN + j * 64 >= p.N) bytes -= 8192u;
+          }
+          ptx::mbar_arrive_expect_tx(&full[stage], bytes);
           last_parity[stage] = (int)phase;
           const int k0 = kb * BK;
           uint8_t* a_dst = sA + stage * L::A_BYTES;
@@ -443,14 +536,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_load_2d(a_dst, &tmA, &full[stage], k0, tm * BM);
           } else {
             ptx::tma_load_2d(a_dst, &tmA, &full[stage], tm * BM, k0);
-            ptx::tma_load_2d(a_dst + 8192, &tmA, &full[stage], tm * BM + 64, k0);
+            if (a_hi) ptx::tma_load_2d(a_dst + 8192, &tmA, &full[stage], tm * BM + 64, k0);
           }
           if (!p.b_mn) {
             ptx::tma_load_2d(b_dst, &tmB, &full[stage], k0, tn * BN);
           } else {
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
-              ptx::tma_load_2d(b_dst + j * 8192, &tmB, &full[stage], tn * BN + j * 64, k0);
+              if (tn * BN + j * 64 < p.N)
+                ptx::tma_load_2d(b_dst + j * 8192, &tmB, &full[stage], tn * BN + j * 64, k0);
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -638,7 +732,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 constexpr int kStepMaxPhases = kStepMaxGemms + 1;
 constexpr int STEP_BN = 64;
-constexpr int STEP_STAGES = 8;
+constexpr int STEP_STAGES = 4;
+// per epilogue warp: the SGD state copy, w and v of 32 rows x 64 columns
+constexpr int STEP_SGD_BYTES = 4 * 2 * 32 * 64 * 4;
 
 struct StepPhaseDev {
   int kind;  // 0: GEMM tiles, 1: input cast
@@ -656,7 +752,7 @@ struct StepProgram {
   int cast_dtype;
   __nv_bfloat16* cast_dst;
   int cast_rows, cast_cols, cast_ld;
-  unsigned* bar;  // [arrivals, generation]
+  unsigned* bar;  // arrival count of the grid barriers (zeroed before each launch)
   unsigned long long wait_ns;
   int* err;
   int n_steps;
@@ -667,31 +763,31 @@ struct StepProgram {
 // passed by value as the kernel's parameter block (limit 32,764 bytes)
 static_assert(sizeof(StepProgram) <= 32000, "step program exceeds the kernel parameter limit");
 
-// Grid-wide barrier of the step program (all threads of every CTA call it).
-// Writers' global stores are ordered before the arrival by the CTA barrier
-// and a device-scope fence; the proxy fences let the next phase's TMA loads
-// (async proxy) see data written with ordinary stores.  Bounded: on a
-// timeout the error word is set and the CTA's abort flag raised.
-__device__ __forceinline__ void step_grid_sync(const StepProgram& prog, volatile int* s_abort) {
+// Grid-wide barrier of the step program (all threads of every CTA call it):
+// one device-scope atomic arrival per CTA and polling of the same counter.
+// The proxy fences let the next phase's TMA loads (async proxy) see data
+// written with ordinary stores.  Bounded: on a timeout the error word is set
+// and the CTA's abort flag raised.
+__device__ __forceinline__ void step_grid_sync(const StepProgram& prog, volatile int* s_abort,
+                                               unsigned& passed) {
   asm volatile("fence.proxy.async;" ::: "memory");
   __syncthreads();
+  ++passed;  // barriers of this launch so far, the same count in every CTA
   if (threadIdx.x == 0 && !*s_abort) {
+    // the arrival count only grows during a launch (zeroed before it): this
+    // barrier is complete once it reaches passed * gridDim.x.  The arrival
+    // releases this CTA's writes (ordered before it by the CTA barrier
+    // above) at device scope; the polls acquire the other CTAs' writes.
     unsigned* count = prog.bar;
-    unsigned* gen = prog.bar + 1;
-    unsigned g0, prev;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g0) : "l"(gen) : "memory");
-    // the arrival releases this CTA's writes (ordered before it by the CTA
-    // barrier above) at device scope
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(count) : "memory");
-    if (prev == gridDim.x - 1) {
-      asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(count) : "memory");
-      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(gen), "r"(g0 + 1u) : "memory");
-    } else {
+    const unsigned target = passed * gridDim.x;
+    unsigned seen;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(seen) : "l"(count) : "memory");
+    ++seen;
+    if (seen < target) {
       const uint64_t t0 = ptx::globaltimer_ns();
       while (true) {
-        unsigned gv;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(gv) : "l"(gen) : "memory");
-        if (gv != g0) break;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(count) : "memory");
+        if (seen >= target) break;
         if (ptx::globaltimer_ns() - t0 > prog.wait_ns) {
           record_device_error(prog.err, DEVERR_TIMEOUT_GRID);
           *s_abort = 1;
@@ -732,6 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sB = smem + STAGES * L::A_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * L::B_BYTES);
   uint8_t* stg = sB + STAGES * L::B_BYTES + L::BAR_BYTES;  // per epilogue warp 8 KiB
+  float* sgd_state = reinterpret_cast<float*>(stg + L::STG_BYTES);  // per warp w, v [32][64]
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -784,6 +881,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int last_parity[STAGES];
   for (int s = 0; s < STAGES; ++s) last_parity[s] = -1;
   int xent_uses = 0;
+  unsigned barriers_passed = 0;
 
   const int n_total = prog.n_steps * prog.n_phases;
   for (int it = 0; it < n_total && !*s_abort; ++it) {
@@ -824,7 +922,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = blockIdx.x; u < ph.tiles && !*s_abort; u += gridDim.x) {
           int t;
           const int g = step_gemm_of(prog, ph, u, t);
-          const TcParams& p = prog.gp[g];
+          // a private copy: fields read from the parameter block through a
+          // computed index are slow loads, re-issued after every store
+          const TcParams p = prog.gp[g];
           int tm, tn;
           tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
           for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -833,7 +933,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               *s_abort = 1;
               break;
             }
-            ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+            // boxes entirely past M / N are not loaded (see tc_gemm_kernel)
+            const bool a_hi = !p.a_mn || tm * BM + 64 < p.M;
+            uint32_t bytes = L::STAGE_BYTES - (a_hi ? 0u : 8192u);
+            if (p.b_mn) {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                if (tn * BN + j * 64 >= p.N) bytes -= 8192u;
+            }
+            ptx::mbar_arrive_expect_tx(&full[stage], bytes);
             last_parity[stage] = (int)phase;
             const int k0 = kb * BK;
             uint8_t* a_dst = sA + stage * L::A_BYTES;
@@ -842,15 +950,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tma_load_2d(a_dst, &prog.ta[g], &full[stage], k0, tm * BM);
             } else {
               ptx::tma_load_2d(a_dst, &prog.ta[g], &full[stage], tm * BM, k0);
-              ptx::tma_load_2d(a_dst + 8192, &prog.ta[g], &full[stage], tm * BM + 64, k0);
+              if (a_hi)
+                ptx::tma_load_2d(a_dst + 8192, &prog.ta[g], &full[stage], tm * BM + 64, k0);
             }
             if (!p.b_mn) {
               ptx::tma_load_2d(b_dst, &prog.tb[g], &full[stage], k0, tn * BN);
             } else {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j)
-                ptx::tma_load_2d(b_dst + j * 8192, &prog.tb[g], &full[stage], tn * BN + j * 64,
-                                 k0);
+                if (tn * BN + j * 64 < p.N)
+                  ptx::tma_load_2d(b_dst + j * 8192, &prog.tb[g], &full[stage], tn * BN + j * 64,
+                                   k0);
             }
             if (++stage == STAGES) { stage = 0; phase ^= 1; }
           }
@@ -862,7 +972,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = blockIdx.x; u < ph.tiles && !*s_abort; u += gridDim.x) {
           int t;
           const int g = step_gemm_of(prog, ph, u, t);
-          const TcParams& p = prog.gp[g];
+          // a private copy: fields read from the parameter block through a
+          // computed index are slow loads, re-issued after every store
+          const TcParams p = prog.gp[g];
           const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
           const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
           const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
@@ -908,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*s_abort) break;
         int t;
         const int g = step_gemm_of(prog, ph, u, t);
-        const TcParams& p = prog.gp[g];
+        const TcParams p = prog.gp[g];  // private copy, as in the other roles
         // the loss GEMM's labels and outputs of this step
         const int* labels = p.xent_labels ? p.xent_labels + step * prog.label_stride : nullptr;
         int* argmax = p.xent_argmax ? p.xent_argmax + step * prog.argmax_stride : nullptr;
@@ -916,14 +1028,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tm, tn;
         tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
         const int m = tm * BM + row;
+        const int row0 = tm * BM + quarter * 32;
+        float* w_s = sgd_state + (warp - 2) * (2 * 32 * 64);
+        float* v_s = w_s + 32 * 64;
+        // everything the epilogue reads besides the accumulator is requested
+        // now, while the tile's MMAs still run
         epilogue_prefetch(p, m, tn * BN, BN, lane, labels);
+        if (p.sgd_w) sgd_state_prefetch(p, row0, tn * BN, w_s, v_s, lane);
+        float bias_r[BN / 32];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) bias_r[c] = load_bias_lane(p, tn * BN + 32 * c, lane);
         if (!ptx::mbar_wait_bounded(&tfull[acc], acc_phase, prog.wait_ns, prog.err,
                                     DEVERR_TIMEOUT_EPILOGUE)) {
           *s_abort = 1;
           break;
         }
         ptx::tc_fence_after();
+        if (p.sgd_w) {
+          asm volatile("cp.async.wait_all;" ::: "memory");
+          __syncwarp();
+        }
         float row_loss = 0.f;
+#pragma unroll
         for (int c0 = 0; c0 < BN; c0 += 32) {
           const int n0 = tn * BN + c0;
           if (n0 >= p.N) break;  // warp-uniform
@@ -935,14 +1061,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       (uint32_t)(acc * BN + c0),
                                   r);
           ptx::tmem_ld_wait();
-          const float* sb = stage_bias(p, n0, sbias + (warp - 2) * 32, lane);
           if (p.sgd_w) {
-            sgd_epilogue_staged(p, tm * BM + quarter * 32, n0, r,
-                                reinterpret_cast<float*>(stg + (warp - 2) * 8192), lane);
-          } else if (m < p.M) {
-            if (p.xent_labels) {
-              row_loss = xent_epilogue_row(p, m, r, labels, argmax);
-            } else {
+            sgd_epilogue_smem(p, row0, n0, c0, r,
+                              reinterpret_cast<float*>(stg + (warp - 2) * 8192), w_s, v_s, lane);
+          } else if (p.xent_labels) {
+            if (m < p.M) row_loss = xent_epilogue_row(p, m, r, labels, argmax);
+          } else {
+            const float* sb = stage_bias_reg(p, bias_r[c0 / 32], sbias + (warp - 2) * 32, lane);
+            if (m < p.M) {
               float v[32];
               epilogue_values(p, m, n0, r, sb, mp, v);
               epilogue_store_regs(p, m, n0, v);
@@ -970,7 +1096,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
     }
-    if (it + 1 < n_total) step_grid_sync(prog, s_abort);
+    if (it + 1 < n_total) step_grid_sync(prog, s_abort, barriers_passed);
   }
 
   // teardown: the MMA issuer's last MMAs are complete before the tensor
@@ -1514,7 +1640,8 @@ mlp_status launch_step_program(const StepSpec& s, unsigned* bar_words, unsigned 
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(tc_step_kernel<STEP_BN, STEP_STAGES>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::SMEM + STEP_SGD_BYTES) != cudaSuccess)
       return MLP_ERR_CUDA;
     configured = true;
   }
@@ -1564,13 +1691,13 @@ mlp_status launch_step_program(const StepSpec& s, unsigned* bar_words, unsigned 
   prog.wait_ns = wait_ns;
   prog.err = device_error_word();
   if (!prog.err) return MLP_ERR_CUDA;
-  // a clean barrier for this launch, even after an abandoned one
-  if (cudaMemsetAsync(bar_words, 0, 2 * sizeof(unsigned), st) != cudaSuccess) return MLP_ERR_CUDA;
+  // a clean barrier count for this launch, even after an abandoned one
+  if (cudaMemsetAsync(bar_words, 0, sizeof(unsigned), st) != cudaSuccess) return MLP_ERR_CUDA;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = L::SMEM;  // with the epilogue staging (fused SGD)
+  cfg.dynamicSmemBytes = L::SMEM + STEP_SGD_BYTES;  // epilogue staging and SGD state
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident: the grid barrier needs it

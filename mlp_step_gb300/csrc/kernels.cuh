@@ -111,8 +111,8 @@ struct StepSpec {
 };
 // Whether launch_step_program can run this GEMM inside a step program.
 bool step_gemm_supported(const GemmArgs& g);
-// bar_words: two zero-initialised unsigned words of device memory owned by
-// the caller (the grid barrier's arrival count and generation).
+// bar_words: one unsigned word of device memory owned by the caller (the
+// grid barrier's arrival count, zeroed on the stream before each launch).
 mlp_status launch_step_program(const StepSpec& s, unsigned* bar_words, unsigned long long wait_ns,
                                cudaStream_t st);
 
