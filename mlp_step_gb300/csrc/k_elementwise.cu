@@ -6,6 +6,7 @@
 #include "kernels.cuh"
 #include "ptx.cuh"
 #include "trace.cuh"
+#include "xent_row.cuh"
 
 namespace mlp {
 
@@ -375,7 +376,31 @@ __global__ void __launch_bounds__(256) xent_single_block_kernel(
 
 // Small heads (C <= 32) of small batches (B <= 512): one row per thread of
 // a single block, so every row's max, sum and dZ come out of one pass with
-// one round trip to memory; the batch mean is a fixed-order tree sum.
+// one round trip to memory (the row routine of xent_row.cuh, shared with the
+// loss epilogue of the logits GEMM); the batch mean is a fixed-order tree sum.
+template <int NC>
+__device__ __forceinline__ float xent_lane_row(const float* __restrict__ z_row, int label, int C,
+                                               float inv, void* dlog_row, int dl_bf16, int ldd,
+                                               int* argmax) {
+  float z[NC], d[NC];
+#pragma unroll
+  for (int j = 0; j < NC; ++j) z[j] = j < C ? z_row[j] : 0.f;
+  int am;
+  const float li = xent_row_small<NC>(z, C, label, inv, d, am);
+  if (dlog_row) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < ldd) {
+        const float v = j < NC ? d[j % NC] : 0.f;
+        if (dl_bf16) static_cast<__nv_bfloat16*>(dlog_row)[j] = f32_to_bf16(v);
+        else static_cast<float*>(dlog_row)[j] = v;
+      }
+    }
+  }
+  if (argmax) *argmax = am;
+  return li;
+}
+
 __global__ void __launch_bounds__(512) xent_lane_rows_kernel(
     const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
     float* __restrict__ loss_out, void* dlog, int dl_bf16, int ldd, int* argmax) {
@@ -385,37 +410,15 @@ __global__ void __launch_bounds__(512) xent_lane_rows_kernel(
   const int r = threadIdx.x;
   float li = 0.f;
   if (r < B) {
-    const float* z = logits + (size_t)r * ldl;
-    int y = labels[r];
-    y = y < 0 ? 0 : (y >= C ? C - 1 : y);  // keep the read in bounds
-    float v[32];
-    float mx = -INFINITY, zy = 0.f;
-    int am = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      v[j] = j < C ? z[j] : -INFINITY;
-      if (v[j] > mx) { mx = v[j]; am = j; }  // first maximum: lowest index among ties
-      if (j == y) zy = v[j];
-    }
-    float s = 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      v[j] = j < C ? expf(v[j] - mx) : 0.f;  // v now holds exp(z - max)
-      s += v[j];
-    }
-    li = mx + logf(s) - zy;
-    if (dlog) {
-      const float inv = 1.0f / (float)B;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (j < ldd) {
-          const float d = j < C ? (v[j] / s - (j == y ? 1.f : 0.f)) * inv : 0.f;
-          if (dl_bf16) static_cast<__nv_bfloat16*>(dlog)[(size_t)r * ldd + j] = f32_to_bf16(d);
-          else static_cast<float*>(dlog)[(size_t)r * ldd + j] = d;
-        }
-      }
-    }
-    if (argmax) argmax[r] = am;
+    const float inv = 1.0f / (float)B;
+    void* drow = nullptr;
+    if (dlog) drow = dl_bf16 ? (void*)(static_cast<__nv_bfloat16*>(dlog) + (size_t)r * ldd)
+                             : (void*)(static_cast<float*>(dlog) + (size_t)r * ldd);
+    int* am = argmax ? argmax + r : nullptr;
+    li = C <= 16 ? xent_lane_row<16>(logits + (size_t)r * ldl, labels[r], C, inv, drow, dl_bf16,
+                                     ldd, am)
+                 : xent_lane_row<32>(logits + (size_t)r * ldl, labels[r], C, inv, drow, dl_bf16,
+                                     ldd, am);
   }
   red[r] = li;
   __syncthreads();

@@ -28,6 +28,7 @@
 #include "kernels.cuh"
 #include "ptx.cuh"
 #include "trace.cuh"
+#include "xent_row.cuh"
 
 namespace mlp {
 
@@ -342,88 +343,97 @@ __device__ __forceinline__ void sgd_epilogue_smem(const TcParams& p, int row0, i
   __syncwarp();
   const int n = n0 + lane;
   const bool col_ok = n < p.N;
-#pragma unroll 8
-  for (int rr = 0; rr < 32; ++rr) {
-    const int m = row0 + rr;
-    if (col_ok && m < p.M) {
-      const float g = slot[rr * 33 + lane];
-      const size_t off = (size_t)m * p.ldc + n;
-      const float nv = p.sgd_mom * v_s[rr * 64 + c0 + lane] - p.sgd_lr * g;
-      const float nw = w_s[rr * 64 + c0 + lane] + nv;
-      static_cast<float*>(p.C)[off] = g;
-      p.sgd_v[off] = nv;
-      p.sgd_w[off] = nw;
-      if (p.sgd_shadow && m < p.sgd_shadow_rows)
-        p.sgd_shadow[(size_t)m * p.sgd_ld_shadow + n] = f32_to_bf16(nw);
+  // eight rows at a time: all shared-memory reads of the batch before any of
+  // its global stores (the compiler cannot move a load past a store through
+  // a pointer it cannot tell apart), so the row chains overlap
+#pragma unroll 1
+  for (int r0 = 0; r0 < 32; r0 += 8) {
+    float g[8], nv[8], nw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = r0 + i;
+      g[i] = slot[rr * 33 + lane];
+      nv[i] = v_s[rr * 64 + c0 + lane];
+      nw[i] = w_s[rr * 64 + c0 + lane];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      nv[i] = p.sgd_mom * nv[i] - p.sgd_lr * g[i];
+      nw[i] = nw[i] + nv[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int m = row0 + r0 + i;
+      if (col_ok && m < p.M) {
+        const size_t off = (size_t)m * p.ldc + n;
+        static_cast<float*>(p.C)[off] = g[i];
+        p.sgd_v[off] = nv[i];
+        p.sgd_w[off] = nw[i];
+        if (p.sgd_shadow && m < p.sgd_shadow_rows)
+          p.sgd_shadow[(size_t)m * p.sgd_ld_shadow + n] = f32_to_bf16(nw[i]);
+      }
     }
   }
 }
 
-// Stable softmax cross entropy of one row of at most 32 logits held by one
-// thread ("Capstone 5", "The minimum model" and "Read the worked reference":
-// subtract the row maximum before exponentiating; fp32 throughout).  Writes
-// the fp32 logits (if C is set), bf16 dZ = (softmax - onehot) / norm padded
-// with zeros to xent_ldd, and the argmax (lowest index among ties); returns
-// the row loss m + ln(sum exp(z - m)) - z_label.
-__device__ __forceinline__ float xent_epilogue_row(const TcParams& p, int m,
-                                                   const uint32_t (&r)[32], const int* labels,
-                                                   int* argmax) {
-  int y = __ldg(labels + m);
-  y = y < 0 ? 0 : (y >= p.N ? p.N - 1 : y);
-  float z[32];
-  float mx = -INFINITY, zy = 0.f;
-  int am = 0;
+// Softmax cross entropy of one row of at most 32 logits held by one thread
+// (the row routine of xent_row.cuh, shared with the one-row-per-thread loss
+// kernel).  Writes the fp32 logits (if C is set), bf16 dZ = (softmax -
+// onehot) / norm padded with zeros to xent_ldd, and the argmax (lowest index
+// among ties); returns the row loss.
+template <int NC>
+__device__ __forceinline__ float xent_epilogue_row_nc(const TcParams& p, int m,
+                                                      const uint32_t (&r)[32], const int* labels,
+                                                      int* argmax) {
+  const int y = __ldg(labels + m);
+  float z[NC];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    z[j] = -INFINITY;
-    if (j < p.N) {
-      z[j] = __uint_as_float(r[j]) + (p.bias ? __ldg(p.bias + j) : 0.f);
-      if (z[j] > mx) { mx = z[j]; am = j; }
-      if (j == y) zy = z[j];
-    }
-  }
+  for (int j = 0; j < NC; ++j)
+    z[j] = j < p.N ? __uint_as_float(r[j]) + (p.bias ? __ldg(p.bias + j) : 0.f) : 0.f;
   if (p.C) {
     float* lrow = static_cast<float*>(p.C) + (size_t)m * p.ldc;
     if ((reinterpret_cast<uintptr_t>(lrow) & 7) == 0) {
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
+      for (int j = 0; j < NC; j += 2) {
         if (j + 1 < p.N) *reinterpret_cast<float2*>(lrow + j) = make_float2(z[j], z[j + 1]);
         else if (j < p.N) lrow[j] = z[j];
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
+      for (int j = 0; j < NC; ++j)
         if (j < p.N) lrow[j] = z[j];
     }
   }
-  float s = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    z[j] = j < p.N ? expf(z[j] - mx) : 0.f;  // z now holds exp(z - max)
-    s += z[j];
-  }
-  const float inv = 1.0f / (float)p.xent_norm;
+  float d[NC];
+  int am;
+  const float loss = xent_row_small<NC>(z, p.N, y, 1.0f / (float)p.xent_norm, d, am);
   __nv_bfloat16* drow = p.xent_dlog + (size_t)m * p.xent_ldd;
-  float d[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j)
-    d[j] = j < p.N ? (z[j] / s - (j == y ? 1.f : 0.f)) * inv : 0.f;
   if ((p.xent_ldd & 7) == 0 && (reinterpret_cast<uintptr_t>(drow) & 15) == 0) {
     // rows of a multiple of 8 bf16: 16-byte stores
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      if (8 * q < p.xent_ldd)
+      if (8 * q < p.xent_ldd) {
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = 8 * q + e < NC ? d[(8 * q + e) % NC] : 0.f;
         reinterpret_cast<uint4*>(drow)[q] =
-            make_uint4(pack_bf16x2(d[8 * q], d[8 * q + 1]), pack_bf16x2(d[8 * q + 2], d[8 * q + 3]),
-                       pack_bf16x2(d[8 * q + 4], d[8 * q + 5]),
-                       pack_bf16x2(d[8 * q + 6], d[8 * q + 7]));
+            make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                       pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+      }
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (j < p.xent_ldd) drow[j] = f32_to_bf16(d[j]);
+      if (j < p.xent_ldd) drow[j] = f32_to_bf16(j < NC ? d[j % NC] : 0.f);
   }
   if (argmax) argmax[m] = am;
-  return mx + logf(s) - zy;
+  return loss;
+}
+
+__device__ __forceinline__ float xent_epilogue_row(const TcParams& p, int m,
+                                                   const uint32_t (&r)[32], const int* labels,
+                                                   int* argmax) {
+  return p.N <= 16 ? xent_epilogue_row_nc<16>(p, m, r, labels, argmax)
+                   : xent_epilogue_row_nc<32>(p, m, r, labels, argmax);
 }
 
 // L1 prefetch of what the epilogue of row m, columns [n0, n0 + bn) will
@@ -732,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 constexpr int kStepMaxPhases = kStepMaxGemms + 1;
 constexpr int STEP_BN = 64;
-constexpr int STEP_STAGES = 4;
+constexpr int STEP_STAGES = 5;
 // per epilogue warp: the SGD state copy, w and v of 32 rows x 64 columns
 constexpr int STEP_SGD_BYTES = 4 * 2 * 32 * 64 * 4;
 
