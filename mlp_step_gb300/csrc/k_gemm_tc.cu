@@ -768,9 +768,11 @@ struct StepProgram {
   int n_steps;
   long long cast_stride, label_stride, loss_stride, argmax_stride;
   int xent_g;  // the GEMM with the fused loss (-1: none)
+  int n_gemm;
 };
 
 // passed by value as the kernel's parameter block (limit 32,764 bytes)
+static_assert(sizeof(TcParams) % 4 == 0, "copied as words");
 static_assert(sizeof(StepProgram) <= 32000, "step program exceeds the kernel parameter limit");
 
 // Grid-wide barrier of the step program (all threads of every CTA call it):
@@ -817,12 +819,12 @@ __device__ __forceinline__ float step_load_in(const void* src, int dtype, size_t
 }
 
 // GEMM g of phase ph that owns the phase's tile u, and u's index within it.
-__device__ __forceinline__ int step_gemm_of(const StepProgram& prog, const StepPhaseDev& ph, int u,
+__device__ __forceinline__ int step_gemm_of(const int* tile_base, const StepPhaseDev& ph, int u,
                                             int& local) {
   int g = ph.g0;
   for (int k = 1; k < ph.n_gemm; ++k)
-    if (u >= prog.tile_base[ph.g0 + k]) g = ph.g0 + k;
-  local = u - prog.tile_base[g];
+    if (u >= tile_base[ph.g0 + k]) g = ph.g0 + k;
+  local = u - tile_base[g];
   return g;
 }
 
@@ -832,6 +834,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Layout<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ float xent_part[4];
+  // the program's per-GEMM parameters, tile bases and phases, copied once:
+  // reading them from the parameter block through a computed index is a
+  // slow load on every use
+  __shared__ TcParams s_gp[kStepMaxGemms];
+  __shared__ int s_tile_base[kStepMaxGemms];
+  __shared__ StepPhaseDev s_ph[kStepMaxPhases];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -876,6 +884,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  {
+    const int words = prog.n_gemm * (int)(sizeof(TcParams) / 4);
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(prog.gp);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(s_gp);
+    for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+    for (int i = threadIdx.x; i < prog.n_gemm; i += blockDim.x) s_tile_base[i] = prog.tile_base[i];
+    for (int i = threadIdx.x; i < prog.n_phases; i += blockDim.x) s_ph[i] = prog.ph[i];
+  }
   if (warp == 1) ptx::tmem_alloc(tmem_slot, L::TMEM_COLS);
   ptx::tc_fence_before();
   __syncthreads();
@@ -896,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_total = prog.n_steps * prog.n_phases;
   for (int it = 0; it < n_total && !*s_abort; ++it) {
     const int step = it / prog.n_phases, phi = it % prog.n_phases;
-    const StepPhaseDev ph = prog.ph[phi];
+    const StepPhaseDev ph = s_ph[phi];
     if (ph.kind == 1) {
       // input rows -> bf16 rows of pitch cast_ld (image bytes are byte / 255)
       const long long stride = (long long)gridDim.x * blockDim.x;
@@ -931,10 +947,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- producer
         for (int u = blockIdx.x; u < ph.tiles && !*s_abort; u += gridDim.x) {
           int t;
-          const int g = step_gemm_of(prog, ph, u, t);
-          // a private copy: fields read from the parameter block through a
-          // computed index are slow loads, re-issued after every store
-          const TcParams p = prog.gp[g];
+          const int g = step_gemm_of(s_tile_base, ph, u, t);
+          // a private copy: a reference would be re-read after every store
+          const TcParams p = s_gp[g];
           int tm, tn;
           tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
           for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -975,16 +990,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (++stage == STAGES) { stage = 0; phase ^= 1; }
           }
         }
+        // the next phase's operand descriptors, so its first loads do not
+        // wait for a descriptor fetch
+        const StepPhaseDev nx = s_ph[(phi + 1) % prog.n_phases];
+        if (nx.kind == 0 && (int)blockIdx.x < nx.tiles)
+          for (int g = nx.g0; g < nx.g0 + nx.n_gemm; ++g) {
+            ptx::prefetch_tensormap(&prog.ta[g]);
+            ptx::prefetch_tensormap(&prog.tb[g]);
+          }
       }
     } else if (warp == 1) {
       if (lane == 0) {
         // ---------------------------------------------------------- MMA issuer
         for (int u = blockIdx.x; u < ph.tiles && !*s_abort; u += gridDim.x) {
           int t;
-          const int g = step_gemm_of(prog, ph, u, t);
-          // a private copy: fields read from the parameter block through a
-          // computed index are slow loads, re-issued after every store
-          const TcParams p = prog.gp[g];
+          const int g = step_gemm_of(s_tile_base, ph, u, t);
+          // a private copy: a reference would be re-read after every store
+          const TcParams p = s_gp[g];
           const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
           const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
           const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
@@ -1029,8 +1051,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = blockIdx.x; u < ph.tiles; u += gridDim.x) {
         if (*s_abort) break;
         int t;
-        const int g = step_gemm_of(prog, ph, u, t);
-        const TcParams p = prog.gp[g];  // private copy, as in the other roles
+        const int g = step_gemm_of(s_tile_base, ph, u, t);
+        const TcParams p = s_gp[g];  // private copy, as in the other roles
         // the loss GEMM's labels and outputs of this step
         const int* labels = p.xent_labels ? p.xent_labels + step * prog.label_stride : nullptr;
         int* argmax = p.xent_argmax ? p.xent_argmax + step * prog.argmax_stride : nullptr;
@@ -1695,6 +1717,7 @@ mlp_status launch_step_program(const StepSpec& s, unsigned* bar_words, unsigned 
   prog.loss_stride = s.loss_stride;
   prog.argmax_stride = s.argmax_stride;
   prog.xent_g = -1;
+  prog.n_gemm = s.n_gemm;
   for (int g = 0; g < s.n_gemm; ++g)
     if (s.gemm[g].xent_labels) prog.xent_g = g;
   prog.bar = bar_words;
