@@ -138,6 +138,9 @@ def algorithmic_work(name):
     GEMMs: 2 M N K flops.  Memory-bound kernels: the bytes they must move.
     """
     base, sh = parse_kernel(name)
+    if base == "gemm_simt":
+        M_, N, K = sh
+        return "alu", 2.0 * M_ * N * K   # fp32 FMA on the CUDA cores, not the tensor cores
     if base.startswith("gemm"):
         M_, N, K = sh
         return "tensor", 2.0 * M_ * N * K
@@ -655,6 +658,17 @@ def recorded_traffic(kernel, workload):
     return None
 
 
+def fp32_alu_tflops():
+    """Peak fp32 FMA rate of the CUDA cores: SMs x 128 fp32 lanes x 2 flops per
+    clock at the maximum SM clock (2070 MHz on the GB300)."""
+    try:
+        import torch
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+    except Exception:
+        sms = 152
+    return sms * 128 * 2 * 2.070e9 / 1e12
+
+
 def roofline_entry(rep, peaks, peaks_kind, sustained=False):
     if not rep:
         return None
@@ -678,6 +692,10 @@ def roofline_entry(rep, peaks, peaks_kind, sustained=False):
         achieved = per_launch / (avg_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
         unit = "TFLOP/s"
+    elif bound == "alu":
+        achieved = per_launch / (avg_ms * 1e-3) / 1e12
+        peak = round(fp32_alu_tflops(), 2)
+        unit = "TFLOP/s"
     else:
         achieved = per_launch / (avg_ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
@@ -685,8 +703,9 @@ def roofline_entry(rep, peaks, peaks_kind, sustained=False):
     share = total_ms / sum(ms for _, ms in rep.values())
     return {"bound": bound, "kernel": base, "achieved": round(achieved, 3), "peak": peak,
             "unit": unit, "frac": round(achieved / peak, 5), "traffic": None,
-            "peak_kind": peaks_kind + (" sustained" if sustained and bound == "tensor" else
-                                       (" burst" if bound == "tensor" else "")),
+            "peak_kind": ("derived: SMs x 128 fp32 lanes x 2 flops x 2070 MHz" if bound == "alu" else
+                          peaks_kind + (" sustained" if sustained and bound == "tensor" else
+                                        (" burst" if bound == "tensor" else ""))),
             "launches_profiled": launches, "avg_launch_ms": round(avg_ms, 6),
             "share_of_kernel_time": round(share, 4),
             "work_per_launch": per_launch}
