@@ -5,6 +5,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 #include <cudaTypedefs.h>
 
@@ -306,6 +307,7 @@ struct mlp_handle {
   // the flat layout of W followed by b.
   std::vector<int> act_ld;         // act_ld[l]: pitch of layer l's input buffer
   void* x_copy = nullptr;          // [max_batch][act_ld[0]]
+  void* x_copy_alt = nullptr;      // second input buffer of multi-step programs (bf16 only)
   std::vector<void*> acts;         // acts[l] = H_{l+1}, l = 0..L-2
   float* logits = nullptr;         // [max_batch][C]
   void* dlogits = nullptr;         // [max_batch][ldz]
@@ -332,7 +334,7 @@ bool dims_ok(const int* dims, int n_dims) {
 }
 
 struct Plan {
-  size_t x, acts_total, logits, dlogits, dh, loss, red, total;
+  size_t x, x_alt, acts_total, logits, dlogits, dh, loss, red, total;
 };
 
 Plan plan(const int* dims, int n_dims, int max_batch, int prec) {
@@ -341,6 +343,7 @@ Plan plan(const int* dims, int n_dims, int max_batch, int prec) {
   const size_t B = (size_t)max_batch;
   const int e = esz(prec);
   p.x = align256(B * round64(dims[0] + 1) * e);
+  p.x_alt = prec == MLP_PREC_BF16 ? p.x : 0;
   p.acts_total = 0;
   int maxh = 8;
   for (int l = 1; l < L; ++l) {
@@ -354,7 +357,7 @@ Plan plan(const int* dims, int n_dims, int max_batch, int prec) {
   p.loss = 256;
   size_t red = xent_workspace_bytes(max_batch);
   p.red = align256(red > 0 ? red : 256);
-  p.total = p.x + p.acts_total + p.logits + p.dlogits + 2 * p.dh + p.loss + p.red;
+  p.total = p.x + p.x_alt + p.acts_total + p.logits + p.dlogits + 2 * p.dh + p.loss + p.red;
   return p;
 }
 
@@ -371,6 +374,12 @@ mlp_status ensure_ones(mlp_handle* h, cudaStream_t st) {
     oc.ptr[l] = h->acts[l - 1];
     oc.ld[l] = h->act_ld[l];
     oc.col[l] = h->dims[l];
+  }
+  if (h->x_copy_alt) {
+    oc.ptr[oc.n] = h->x_copy_alt;
+    oc.ld[oc.n] = h->act_ld[0];
+    oc.col[oc.n] = h->dims[0];
+    ++oc.n;
   }
   MLP_CHECK(launch_ones_cols(oc, h->max_batch, h->prec == MLP_PREC_BF16, st));
   h->ones_ready = true;
@@ -688,6 +697,10 @@ mlp_status mlp_create(const int* dims, int n_dims, int hidden_act, int prec, int
   const size_t B = (size_t)max_batch;
   h->x_copy = w;
   w += pl.x;
+  if (pl.x_alt) {
+    h->x_copy_alt = w;
+    w += pl.x_alt;
+  }
   for (int l = 1; l < h->L; ++l) {
     h->acts.push_back(w);
     w += align256(B * h->act_ld[l] * e);
@@ -793,8 +806,12 @@ mlp_status mlp_train_epoch(mlp_handle* h, const void* x, int x_dtype, const int3
       spec.label_stride = batch;
       spec.loss_stride = losses_out ? 1 : 0;
       spec.argmax_stride = batch;
+      if (full > 1) spec.cast_dst_alt = h->x_copy_alt;
       MLP_CHECK(ensure_ones(h, st));
       MLP_CHECK(launch_step_program(spec, h->step_bar, wait_limit_ns(), st));
+      // with two input buffers the last step (index full - 1) read the second
+      // one when full is even: keep x_copy naming the latest input
+      if (spec.cast_dst_alt && full % 2 == 0) std::swap(h->x_copy, h->x_copy_alt);
       h->have_forward = true;
       done = full;
     }

@@ -68,6 +68,7 @@ struct TcParams {
   __nv_bfloat16* sgd_shadow;
   int sgd_ld_shadow, sgd_shadow_rows;
   int tma_store;  // epilogue writes C through the tmC tensor map
+  int a_alt;      // step programs: odd steps read A through the alternate tensor map
 };
 
 template <int BN, int STAGES>
@@ -754,6 +755,7 @@ struct StepPhaseDev {
 struct StepProgram {
   CUtensorMap ta[kStepMaxGemms];
   CUtensorMap tb[kStepMaxGemms];
+  CUtensorMap ta_alt[kStepMaxGemms];  // A over the second input buffer (GEMMs with a_alt)
   TcParams gp[kStepMaxGemms];
   int tile_base[kStepMaxGemms];  // first tile of GEMM g within its phase
   StepPhaseDev ph[kStepMaxPhases];
@@ -761,6 +763,8 @@ struct StepProgram {
   const void* cast_src;
   int cast_dtype;
   __nv_bfloat16* cast_dst;
+  __nv_bfloat16* cast_dst_alt;
+  int cast_ahead_phase;  // phase whose idle CTAs cast the next step's input (-1: none)
   int cast_rows, cast_cols, cast_ld;
   unsigned* bar;  // arrival count of the grid barriers (zeroed before each launch)
   unsigned long long wait_ns;
@@ -774,6 +778,46 @@ struct StepProgram {
 // passed by value as the kernel's parameter block (limit 32,764 bytes)
 static_assert(sizeof(TcParams) % 4 == 0, "copied as words");
 static_assert(sizeof(StepProgram) <= 32000, "step program exceeds the kernel parameter limit");
+
+// Element i of a step's input rows as a float (image bytes scaled to [0, 1]).
+__device__ __forceinline__ float step_load_in(const void* src, int dtype, size_t i) {
+  if (dtype == MLP_DTYPE_U8) return (float)static_cast<const uint8_t*>(src)[i] / 255.0f;
+  if (dtype == MLP_DTYPE_BF16) return bf16_to_f32(static_cast<const __nv_bfloat16*>(src)[i]);
+  return static_cast<const float*>(src)[i];
+}
+
+// Input rows of step `step` -> bf16 rows of pitch cast_ld at dst (image
+// bytes become byte / 255), spread over CTAs [0, n_cta) of those calling it
+// (cta = this CTA's index among them); all threads of the CTA take part.
+__device__ __forceinline__ void step_cast(const StepProgram& prog, int step, __nv_bfloat16* dst,
+                                          int cta, int n_cta) {
+  const long long stride = (long long)n_cta * blockDim.x;
+  const long long first = (long long)cta * blockDim.x + threadIdx.x;
+  const void* src = static_cast<const uint8_t*>(prog.cast_src) + step * prog.cast_stride;
+  if (prog.cast_dtype == MLP_DTYPE_U8 && (prog.cast_cols & 7) == 0 && (prog.cast_ld & 7) == 0 &&
+      (reinterpret_cast<uintptr_t>(src) & 7) == 0) {
+    // 8 bytes in, 8 bf16 (16 bytes) out per thread and step
+    const int vpr = prog.cast_cols / 8;
+    const long long n = (long long)prog.cast_rows * vpr;
+    for (long long i = first; i < n; i += stride) {
+      const int r = (int)(i / vpr), q = (int)(i % vpr);
+      const uint2 b = reinterpret_cast<const uint2*>(src)[i];
+      const uint8_t* u8 = reinterpret_cast<const uint8_t*>(&b);
+      uint4 o;
+      o.x = pack_bf16x2((float)u8[0] / 255.0f, (float)u8[1] / 255.0f);
+      o.y = pack_bf16x2((float)u8[2] / 255.0f, (float)u8[3] / 255.0f);
+      o.z = pack_bf16x2((float)u8[4] / 255.0f, (float)u8[5] / 255.0f);
+      o.w = pack_bf16x2((float)u8[6] / 255.0f, (float)u8[7] / 255.0f);
+      reinterpret_cast<uint4*>(dst + (size_t)r * prog.cast_ld)[q] = o;
+    }
+  } else {
+    const long long n = (long long)prog.cast_rows * prog.cast_cols;
+    for (long long i = first; i < n; i += stride) {
+      const int r = (int)(i / prog.cast_cols), c = (int)(i % prog.cast_cols);
+      dst[(size_t)r * prog.cast_ld + c] = f32_to_bf16(step_load_in(src, prog.cast_dtype, (size_t)i));
+    }
+  }
+}
 
 // Grid-wide barrier of the step program (all threads of every CTA call it):
 // one device-scope atomic arrival per CTA and polling of the same counter.
@@ -810,12 +854,6 @@ __device__ __forceinline__ void step_grid_sync(const StepProgram& prog, volatile
   }
   __syncthreads();
   asm volatile("fence.proxy.async;" ::: "memory");
-}
-
-__device__ __forceinline__ float step_load_in(const void* src, int dtype, size_t i) {
-  if (dtype == MLP_DTYPE_U8) return (float)static_cast<const uint8_t*>(src)[i] / 255.0f;
-  if (dtype == MLP_DTYPE_BF16) return bf16_to_f32(static_cast<const __nv_bfloat16*>(src)[i]);
-  return static_cast<const float*>(src)[i];
 }
 
 // GEMM g of phase ph that owns the phase's tile u, and u's index within it.
@@ -881,6 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int g = ph.g0 + lane; g < ph.g0 + ph.n_gemm; g += 32) {
         ptx::prefetch_tensormap(&prog.ta[g]);
         ptx::prefetch_tensormap(&prog.tb[g]);
+        if (prog.gp[g].a_alt) ptx::prefetch_tensormap(&prog.ta_alt[g]);
       }
     }
   }
@@ -910,38 +949,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned barriers_passed = 0;
 
   const int n_total = prog.n_steps * prog.n_phases;
+  const bool dbuf = prog.cast_ahead_phase >= 0;
   for (int it = 0; it < n_total && !*s_abort; ++it) {
     const int step = it / prog.n_phases, phi = it % prog.n_phases;
     const StepPhaseDev ph = s_ph[phi];
+    bool sync_after = true;
     if (ph.kind == 1) {
-      // input rows -> bf16 rows of pitch cast_ld (image bytes are byte / 255)
-      const long long stride = (long long)gridDim.x * blockDim.x;
-      const long long first = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-      const void* src = static_cast<const uint8_t*>(prog.cast_src) + step * prog.cast_stride;
-      if (prog.cast_dtype == MLP_DTYPE_U8 && (prog.cast_cols & 7) == 0 &&
-          (prog.cast_ld & 7) == 0 && (reinterpret_cast<uintptr_t>(src) & 7) == 0) {
-        // 8 bytes in, 8 bf16 (16 bytes) out per thread and step
-        const int vpr = prog.cast_cols / 8;
-        const long long n = (long long)prog.cast_rows * vpr;
-        for (long long i = first; i < n; i += stride) {
-          const int r = (int)(i / vpr), q = (int)(i % vpr);
-          const uint2 b = reinterpret_cast<const uint2*>(src)[i];
-          const uint8_t* u8 = reinterpret_cast<const uint8_t*>(&b);
-          uint4 o;
-          o.x = pack_bf16x2((float)u8[0] / 255.0f, (float)u8[1] / 255.0f);
-          o.y = pack_bf16x2((float)u8[2] / 255.0f, (float)u8[3] / 255.0f);
-          o.z = pack_bf16x2((float)u8[4] / 255.0f, (float)u8[5] / 255.0f);
-          o.w = pack_bf16x2((float)u8[6] / 255.0f, (float)u8[7] / 255.0f);
-          reinterpret_cast<uint4*>(prog.cast_dst + (size_t)r * prog.cast_ld)[q] = o;
-        }
-      } else {
-        const long long n = (long long)prog.cast_rows * prog.cast_cols;
-        for (long long i = first; i < n; i += stride) {
-          const int r = (int)(i / prog.cast_cols), c = (int)(i % prog.cast_cols);
-          prog.cast_dst[(size_t)r * prog.cast_ld + c] =
-              f32_to_bf16(step_load_in(src, prog.cast_dtype, (size_t)i));
-        }
-      }
+      // with two input buffers only the first step casts in a phase of its
+      // own; the later ones were cast during the step before
+      if (!dbuf || step == 0) step_cast(prog, step, prog.cast_dst, blockIdx.x, gridDim.x);
+      else sync_after = false;
     } else if (warp == 0) {
       if (lane == 0) {
         // ---------------------------------------------------------- producer
@@ -971,12 +988,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int k0 = kb * BK;
             uint8_t* a_dst = sA + stage * L::A_BYTES;
             uint8_t* b_dst = sB + stage * L::B_BYTES;
+            const CUtensorMap* tma = (p.a_alt && (step & 1)) ? &prog.ta_alt[g] : &prog.ta[g];
             if (!p.a_mn) {
-              ptx::tma_load_2d(a_dst, &prog.ta[g], &full[stage], k0, tm * BM);
+              ptx::tma_load_2d(a_dst, tma, &full[stage], k0, tm * BM);
             } else {
-              ptx::tma_load_2d(a_dst, &prog.ta[g], &full[stage], tm * BM, k0);
-              if (a_hi)
-                ptx::tma_load_2d(a_dst + 8192, &prog.ta[g], &full[stage], tm * BM + 64, k0);
+              ptx::tma_load_2d(a_dst, tma, &full[stage], tm * BM, k0);
+              if (a_hi) ptx::tma_load_2d(a_dst + 8192, tma, &full[stage], tm * BM + 64, k0);
             }
             if (!p.b_mn) {
               ptx::tma_load_2d(b_dst, &prog.tb[g], &full[stage], k0, tn * BN);
@@ -997,6 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int g = nx.g0; g < nx.g0 + nx.n_gemm; ++g) {
             ptx::prefetch_tensormap(&prog.ta[g]);
             ptx::prefetch_tensormap(&prog.tb[g]);
+            if (s_gp[g].a_alt) ptx::prefetch_tensormap(&prog.ta_alt[g]);
           }
       }
     } else if (warp == 1) {
@@ -1128,7 +1146,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
     }
-    if (it + 1 < n_total) step_grid_sync(prog, s_abort, barriers_passed);
+    // the next step's input, cast by the CTAs without a tile in this phase
+    if (dbuf && phi == prog.cast_ahead_phase && step + 1 < prog.n_steps &&
+        (int)blockIdx.x >= ph.tiles)
+      step_cast(prog, step + 1, ((step + 1) & 1) ? prog.cast_dst_alt : prog.cast_dst,
+                (int)blockIdx.x - ph.tiles, (int)gridDim.x - ph.tiles);
+    if (it + 1 < n_total && sync_after) step_grid_sync(prog, s_abort, barriers_passed);
   }
 
   // teardown: the MMA issuer's last MMAs are complete before the tensor
@@ -1603,6 +1626,7 @@ mlp_status prepare_tc(const GemmArgs& g, int tiles_m, int BN, int splits, int kb
                       CUtensorMap* tb) {
   TcParams& p = *pp;
   p.M = g.M; p.N = g.N; p.K = g.K;
+  p.a_alt = 0;
   p.a_mn = g.a_trans ? 1 : 0;       // A stored [K][M]  -> M-major tiles
   p.b_mn = g.b_trans ? 0 : 1;       // B stored [K][N]  -> N-major tiles
   p.tiles_m = tiles_m;
@@ -1710,6 +1734,28 @@ mlp_status launch_step_program(const StepSpec& s, unsigned* bar_words, unsigned 
   if (np == 0) return MLP_OK;
   if (grid > num_sms()) return MLP_ERR_UNSUPPORTED_SHAPE;
   if (s.n_steps < 1) return MLP_ERR_INVALID_ARG;
+  // Two input buffers: the next step's input is cast by the CTAs idle in the
+  // GEMM phase with the fewest tiles; GEMMs reading the input alternate.
+  prog.cast_ahead_phase = -1;
+  if (s.cast_dst_alt && s.n_steps > 1 && prog.ph[0].kind == 1) {
+    int best = -1;
+    for (int i = 1; i < np; ++i)
+      if (prog.ph[i].tiles < grid && (best < 0 || prog.ph[i].tiles < prog.ph[best].tiles)) best = i;
+    if (best > 0) {
+      for (int g = 0; g < s.n_gemm; ++g) {
+        if (s.gemm[g].A != s.cast_dst) continue;
+        GemmArgs a2 = s.gemm[g];
+        a2.A = s.cast_dst_alt;
+        TcParams p2;
+        CUtensorMap tb2;
+        MLP_CHECK(prepare_tc(a2, (a2.M + BM - 1) / BM, STEP_BN, 1, (a2.K + BK - 1) / BK, STEP_BN,
+                             wait_ns, &p2, &prog.ta_alt[g], &tb2));
+        prog.gp[g].a_alt = 1;
+      }
+      prog.cast_ahead_phase = best;
+      prog.cast_dst_alt = static_cast<__nv_bfloat16*>(s.cast_dst_alt);
+    }
+  }
   prog.n_phases = np;
   prog.n_steps = s.n_steps;
   prog.cast_stride = s.cast_stride;

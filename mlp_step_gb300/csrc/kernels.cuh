@@ -43,9 +43,9 @@ mlp_status launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st);
 // weight-gradient GEMM produce the bias gradient as its last row.
 struct OnesCols {
   int n;
-  void* ptr[8];
-  int ld[8];
-  int col[8];
+  void* ptr[9];
+  int ld[9];
+  int col[9];
 };
 mlp_status launch_ones_cols(const OnesCols& oc, int rows, int bf16, cudaStream_t st);
 
@@ -98,6 +98,11 @@ struct StepSpec {
   const void* cast_src = nullptr;
   int cast_dtype = 0;
   void* cast_dst = nullptr;  // bf16 rows of pitch cast_ld
+  // Optional second input buffer (same shape) for programs of several steps:
+  // step s then reads buffer s % 2, and step s + 1's input is cast during
+  // step s (by the CTAs idle in its smallest GEMM phase) instead of in a
+  // phase of its own.  GEMMs whose A operand is cast_dst follow the buffer.
+  void* cast_dst_alt = nullptr;
   int cast_rows = 0, cast_cols = 0, cast_ld = 0;
   int n_gemm = 0;
   GemmArgs gemm[kStepMaxGemms];
