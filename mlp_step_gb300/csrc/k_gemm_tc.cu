@@ -841,10 +841,11 @@ __device__ __forceinline__ void step_grid_sync(const StepProgram& prog, volatile
     ++seen;
     if (seen < target) {
       const uint64_t t0 = ptx::globaltimer_ns();
-      while (true) {
+      for (int polls = 1;; ++polls) {
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(count) : "memory");
         if (seen >= target) break;
-        if (ptx::globaltimer_ns() - t0 > prog.wait_ns) {
+        // the timer is read now and then, not on every poll
+        if ((polls & 15) == 0 && ptx::globaltimer_ns() - t0 > prog.wait_ns) {
           record_device_error(prog.err, DEVERR_TIMEOUT_GRID);
           *s_abort = 1;
           break;
