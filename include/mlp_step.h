@@ -120,9 +120,10 @@ size_t mlp_param_count(const int* dims, int n_dims);
 size_t mlp_param_offset(const int* dims, int n_dims, int layer, int which);
 
 /* Elements of the bf16 weight shadow used by MLP_PREC_BF16: each W_l stored
- * [in][out_pad] with out_pad = out rounded up to a multiple of 8 (16-byte
- * rows), layers back to back.  Biases have no shadow (the epilogue reads the
- * fp32 bias). */
+ * [in][out_pad] with out_pad = out rounded up to a multiple of 8 when out <= 16
+ * (16-byte rows), else to a multiple of 64 (whole 128-byte lines, which the
+ * tensor-core tiles read fastest), layers back to back.  Biases have no shadow
+ * (the epilogue reads the fp32 bias). */
 size_t mlp_shadow_elems(const int* dims, int n_dims);
 
 /* Bytes of device workspace mlp_create needs for batches up to max_batch. */

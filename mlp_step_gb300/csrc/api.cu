@@ -115,6 +115,12 @@ inline cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline int round8(int x) { return (x + 7) / 8 * 8; }
 inline int round64(int x) { return (x + 63) / 64 * 64; }
+// Row pitch (elements) of bf16 matrices with n columns that TMA tiles read:
+// compact for small heads, else whole 128-byte lines, so no box row of the
+// tiles straddles two lines.
+inline int bf16_pitch(int n) { return n <= 16 ? round8(n) : round64(n); }
+// Row pitch of the handle's fp32 logits.
+inline int f32_pitch(int n) { return n <= 16 ? n : (n + 31) / 32 * 32; }
 
 // ------------------------------------------------------------ GEMM checks
 
@@ -312,6 +318,7 @@ struct mlp_handle {
   float* logits = nullptr;         // [max_batch][C]
   void* dlogits = nullptr;         // [max_batch][ldz]
   int ldz = 0;
+  int ldl = 0;                     // row pitch of logits
   void* dh[2] = {nullptr, nullptr};
   float* loss = nullptr;
   unsigned* step_bar = nullptr;    // grid barrier words of the step program (in the loss block)
@@ -351,8 +358,8 @@ Plan plan(const int* dims, int n_dims, int max_batch, int prec) {
     if (round64(dims[l] + 1) > maxh) maxh = round64(dims[l] + 1);
   }
   if (round64(dims[0] + 1) > maxh) maxh = round64(dims[0] + 1);
-  p.logits = align256(B * dims[L] * sizeof(float));
-  p.dlogits = align256(B * round8(dims[L]) * e);
+  p.logits = align256(B * f32_pitch(dims[L]) * sizeof(float));
+  p.dlogits = align256(B * bf16_pitch(dims[L]) * e);
   p.dh = align256(B * maxh * e);
   p.loss = 256;
   size_t red = xent_workspace_bytes(max_batch);
@@ -417,7 +424,7 @@ mlp_status forward_hidden(mlp_handle* h, int batch, cudaStream_t st, StepSpec* r
 }
 
 // The output layer's GEMM operands (logits = In W_L + b_L).
-GemmArgs logits_gemm(mlp_handle* h, int batch, float* logits) {
+GemmArgs logits_gemm(mlp_handle* h, int batch, float* logits, int ld_logits) {
   const bool bf = h->prec == MLP_PREC_BF16;
   const int l = h->L - 1;
   GemmArgs g{};
@@ -436,7 +443,7 @@ GemmArgs logits_gemm(mlp_handle* h, int batch, float* logits) {
   g.bias = h->params + h->b_off[l];
   g.act = MLP_ACT_NONE;
   g.C = logits;
-  g.ldc = h->dims[l + 1];
+  g.ldc = ld_logits;
   g.c_bf16 = 0;
   return g;
 }
@@ -557,7 +564,7 @@ bool build_step_spec(mlp_handle* h, const void* x, int x_dtype, const int32_t* l
   spec->cast_cols = h->dims[0];
   spec->cast_ld = h->act_ld[0];
   if (forward_hidden(h, batch, st, spec) != MLP_OK) return false;
-  GemmArgs gz = logits_gemm(h, batch, h->logits);
+  GemmArgs gz = logits_gemm(h, batch, h->logits, h->ldl);
   gz.xent_labels = labels;
   gz.xent_dlog = h->dlogits;
   gz.xent_ldd = h->ldz;
@@ -587,7 +594,7 @@ mlp_status train_step_impl(mlp_handle* h, const void* x, int x_dtype, const int3
   }
   MLP_CHECK(load_input(h, x, x_dtype, batch, st));
   MLP_CHECK(forward_hidden(h, batch, st));
-  GemmArgs gz = logits_gemm(h, batch, h->logits);
+  GemmArgs gz = logits_gemm(h, batch, h->logits, h->ldl);
   if (bf && batch <= 128 && C <= 32) {
     // one tile holds the whole head: softmax cross entropy in its epilogue
     gz.xent_labels = labels;
@@ -599,7 +606,7 @@ mlp_status train_step_impl(mlp_handle* h, const void* x, int x_dtype, const int3
     MLP_CHECK(run_gemm(gz, true, st));
   } else {
     MLP_CHECK(run_gemm(gz, bf, st));
-    MLP_CHECK(launch_xent(h->logits, C, labels, batch, C, loss, h->dlogits, bf, h->ldz,
+    MLP_CHECK(launch_xent(h->logits, h->ldl, labels, batch, C, loss, h->dlogits, bf, h->ldz,
                           argmax_out, h->red, st));
   }
   h->have_forward = true;
@@ -631,7 +638,7 @@ size_t mlp_param_offset(const int* dims, int n_dims, int layer, int which) {
 size_t mlp_shadow_elems(const int* dims, int n_dims) {
   if (!dims_ok(dims, n_dims)) return 0;
   size_t n = 0;
-  for (int l = 0; l + 1 < n_dims; ++l) n += (size_t)dims[l] * round8(dims[l + 1]);
+  for (int l = 0; l + 1 < n_dims; ++l) n += (size_t)dims[l] * bf16_pitch(dims[l + 1]);
   return n;
 }
 
@@ -675,8 +682,8 @@ mlp_status mlp_create(const int* dims, int n_dims, int hidden_act, int prec, int
     h->b_off.push_back(off);
     off += dims[l + 1];
     h->shadow_off.push_back(soff);
-    h->out_pad.push_back(round8(dims[l + 1]));
-    soff += (long long)dims[l] * round8(dims[l + 1]);
+    h->out_pad.push_back(bf16_pitch(dims[l + 1]));
+    soff += (long long)dims[l] * bf16_pitch(dims[l + 1]);
   }
   for (int l = 0; l < h->L; ++l) h->act_ld.push_back(round64(dims[l] + 1));
   // segment map for the fused SGD + shadow refresh
@@ -707,7 +714,8 @@ mlp_status mlp_create(const int* dims, int n_dims, int hidden_act, int prec, int
   }
   h->logits = reinterpret_cast<float*>(w);
   w += pl.logits;
-  h->ldz = round8(dims[h->L]);
+  h->ldz = bf16_pitch(dims[h->L]);
+  h->ldl = f32_pitch(dims[h->L]);
   h->dlogits = w;
   w += pl.dlogits;
   h->dh[0] = w;
@@ -742,7 +750,7 @@ mlp_status mlp_forward(mlp_handle* h, const void* x, int x_dtype, int batch, flo
   cudaStream_t st = S(stream);
   MLP_CHECK(load_input(h, x, x_dtype, batch, st));
   MLP_CHECK(forward_hidden(h, batch, st));
-  MLP_CHECK(run_gemm(logits_gemm(h, batch, logits), h->prec == MLP_PREC_BF16, st));
+  MLP_CHECK(run_gemm(logits_gemm(h, batch, logits, h->dims[h->L]), h->prec == MLP_PREC_BF16, st));
   h->have_forward = true;
   return MLP_OK;
 }

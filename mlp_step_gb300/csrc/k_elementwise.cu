@@ -71,8 +71,19 @@ __global__ void __launch_bounds__(256) sgd_kernel(float* __restrict__ w, const f
       const long long i = q << 2;
       const int k = find_segment(segs, i);
       const bool same = (k + 1 >= segs.n) || (i + 3 < segs.flat_off[k + 1]);
-      if (same && segs.shadow_off[k] >= 0 && segs.cols[k] == segs.cols_pad[k]) {
-        const long long si = segs.shadow_off[k] + (i - segs.flat_off[k]);
+      // the group's shadow position when its four elements share one row
+      long long si = -1;
+      if (same && segs.shadow_off[k] >= 0) {
+        const long long local = i - segs.flat_off[k];
+        if (segs.cols[k] == segs.cols_pad[k]) {
+          si = segs.shadow_off[k] + local;
+        } else if (local < (1ll << 31)) {
+          const unsigned cols = (unsigned)segs.cols[k];
+          const unsigned r = (unsigned)local / cols, c = (unsigned)local - r * cols;
+          if (c + 3 < cols) si = segs.shadow_off[k] + (long long)r * segs.cols_pad[k] + c;
+        }
+      }
+      if (si >= 0) {
         uint2 pk;
         pk.x = pack_bf16x2(nw.x, nw.y);
         pk.y = pack_bf16x2(nw.z, nw.w);

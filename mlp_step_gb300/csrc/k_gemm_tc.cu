@@ -1198,19 +1198,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // epilogue warps of the pair that drained it.
 constexpr int BN2 = 256;
 
+// 10 warps: TMA producer, MMA issuer, 8 epilogue warps (two per tensor-memory
+// lane quadrant, each draining 128 of the 256 accumulator columns)
+constexpr int kPairThreads = 320;
+
 template <int STAGES>
 struct Layout2 {
   static constexpr int A_BYTES = 128 * BK * 2;
   static constexpr int B_BYTES = 128 * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int BAR_BYTES = 1024;
-  static constexpr int STG_BYTES = 4 * 2 * 4096;
+  static constexpr int BAR_BYTES = 2048;        // barriers, then 8 x 32 bias floats at 512
+  static constexpr int STG_BYTES = 8 * 4096;    // per epilogue warp: 2 x 2 KiB (bf16) / 4 KiB (fp32)
   static constexpr int SMEM_BASE = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
   static constexpr int SMEM = SMEM_BASE + STG_BYTES;
 };
 
 template <int STAGES>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -1243,7 +1247,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], 8);
+      ptx::mbar_init(&tempty[a], 16);  // the pair's 16 epilogue warps
     }
     ptx::mbar_init(done, 1);
     *s_abort = 0;
@@ -1355,6 +1359,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     const int quarter = warp & 3;
+    const int c_half = ((warp - 2) >> 2) * (BN2 / 2);  // this warp's 128 accumulator columns
     const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_u32(tempty), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -1374,12 +1379,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int m = row0 + lane;
       // ReLU-mask pieces are fetched one piece ahead of their use
       MaskPiece mp_next;
-      load_mask(p, m, tn * BN2, mp_next);
-      for (int c0 = 0; c0 < BN2; c0 += 32) {
+      load_mask(p, m, tn * BN2 + c_half, mp_next);
+      for (int c0 = c_half; c0 < c_half + BN2 / 2; c0 += 32) {
         const int n0 = tn * BN2 + c0;
         if (n0 >= p.N) break;  // warp-uniform
         const MaskPiece mp = mp_next;
-        if (c0 + 32 < BN2 && n0 + 32 < p.N) load_mask(p, m, n0 + 32, mp_next);
+        if (c0 + 32 < c_half + BN2 / 2 && n0 + 32 < p.N) load_mask(p, m, n0 + 32, mp_next);
         uint32_t r[32];
         __syncwarp();
         ptx::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) +
@@ -1414,9 +1419,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else if (row0 < p.M) {  // warp-uniform; rows past M are clipped by TMA
           float v[32];
           epilogue_values(p, m, n0, r, sb, mp, v);
-          uint8_t* box = stg + (warp - 2) * 8192 + (stg_count & 1) * 4096;
-          if (stg_count >= 2) {
-            if (lane == 0) ptx::bulk_wait_group_read<1>();
+          // per warp 4 KiB: two 2 KiB bf16 boxes in turn, or one fp32 box
+          uint8_t* box = stg + (warp - 2) * 4096 + (p.c_bf16 ? (stg_count & 1) * 2048 : 0);
+          if (p.c_bf16 ? stg_count >= 2 : stg_count >= 1) {
+            if (lane == 0) {
+              if (p.c_bf16) ptx::bulk_wait_group_read<1>();
+              else ptx::bulk_wait_group_read<0>();
+            }
             __syncwarp();
           }
           epilogue_stage_row(box, p.c_bf16, lane, v);
@@ -1540,7 +1549,7 @@ mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
     // pairs that fit at once (a GPC with an odd number of free SMs leaves one over)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms() / 2));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kPairThreads);
     cfg.dynamicSmemBytes = L::SMEM;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<STAGES>, &cfg) != cudaSuccess ||
@@ -1555,7 +1564,7 @@ mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
   const int pairs = units < max_pairs ? units : max_pairs;
   {
     LaunchScope ls(p.splits > 1 ? "gemm_tc_pair_splitk" : "gemm_tc_pair", st, p.M, p.N, p.K);
-    launch_k(tc_gemm_pair_kernel<STAGES>, dim3(2 * pairs), dim3(kThreads),
+    launch_k(tc_gemm_pair_kernel<STAGES>, dim3(2 * pairs), dim3(kPairThreads),
              p.tma_store ? L::SMEM : L::SMEM_BASE, st, ta, tb, tc, p);
   }
   MLP_CHECK(launch_status());

@@ -209,7 +209,26 @@ def test_bf16_three_layer_step_program_matches_unfused_sequence():
     assert abs(loss_f[0].item() - loss_s[0].item()) <= 1e-6 * abs(loss_s[0].item())
     assert torch.allclose(fused.params, seq.params, rtol=1e-6, atol=1e-8)
     assert torch.allclose(fused.velocity, seq.velocity, rtol=1e-5, atol=1e-9)
+    # shadow rows of the wider layers are padded to whole 128-byte lines
+    # (96 -> 128 and 48 -> 64 columns): each row holds bf16 of the updated
+    # weight row, the padding stays zero, through both update paths
+    for net in (fused, seq):
+        assert_shadow_layout(dims, net)
     assert M.get_device_status() == M.MLP_OK
+
+
+def assert_shadow_layout(dims, net):
+    pitch = lambda n: (n + 7) // 8 * 8 if n <= 16 else (n + 63) // 64 * 64
+    assert net.shadow.numel() == sum(dims[l] * pitch(dims[l + 1]) for l in range(len(dims) - 1))
+    off = soff = 0
+    for l in range(len(dims) - 1):
+        fi, fo = dims[l], dims[l + 1]
+        W = net.params[off:off + fi * fo].view(fi, fo)
+        S = net.shadow[soff:soff + fi * pitch(fo)].view(fi, pitch(fo))
+        assert torch.equal(S[:, :fo], W.to(torch.bfloat16)), l
+        assert not S[:, fo:].float().abs().any(), l
+        off += fi * fo + fo
+        soff += fi * pitch(fo)
 
 
 def test_bf16_forward_matches_oracle_exact_mode():
