@@ -154,7 +154,7 @@ def algorithmic_work(name):
         T, d, h = sh
         return "tensor", 2.0 * T * d * h      # dA = dY W_down^T; the u recompute is not credited
     if base == "rmsnorm_bwd":
-        return "hbm", 5124.0 * sh[0]          # per token: dn' fp32 + x, dy, dx bf16 + rstd
+        return "hbm", 4100.0 * sh[0]          # per token: dn', x, dy, dx bf16 + rstd
     if base == "sgd":
         return "hbm", 22.0 * sh[0]        # read w, g, v; write w, v (fp32) + bf16 shadow
     if base == "cast":

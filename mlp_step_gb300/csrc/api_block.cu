@@ -21,7 +21,7 @@ BlockWs block_ws(int T, int d, int hidden) {
   BlockWs w;
   w.a = align256((size_t)T * hidden * 2);
   w.du = align256((size_t)T * hidden * 2);
-  w.dn = align256((size_t)T * d * 4);
+  w.dn = align256((size_t)T * d * 2);  // dn' in bf16
   // split-K partial sums of the two weight-gradient GEMMs (K = T)
   size_t s1 = gemm_tc_splitk_bytes(hidden, d, T), s2 = gemm_tc_splitk_bytes(d, hidden, T);
   w.split = align256(s1 > s2 ? s1 : s2);
@@ -31,7 +31,7 @@ BlockWs block_ws(int T, int d, int hidden) {
 
 mlp_status gemm(int M, int N, int K, const void* A, int lda, int a_trans, const void* B, int ldb,
                 int b_trans, void* C, int ldc, cudaStream_t st, void* ws = nullptr,
-                size_t ws_bytes = 0) {
+                size_t ws_bytes = 0, int c_bf16 = 0) {
   GemmArgs g{};
   g.ws = ws;
   g.ws_bytes = ws_bytes;
@@ -39,7 +39,7 @@ mlp_status gemm(int M, int N, int K, const void* A, int lda, int a_trans, const 
   g.A = A; g.lda = lda; g.a_trans = a_trans;
   g.B = B; g.ldb = ldb; g.b_trans = b_trans;
   g.act = MLP_ACT_NONE;
-  g.C = C; g.ldc = ldc; g.c_bf16 = 0;
+  g.C = C; g.ldc = ldc; g.c_bf16 = c_bf16;
   return launch_gemm_tc(g, wait_limit_ns(), st);
 }
 
@@ -50,7 +50,7 @@ mlp_status block_bwd_impl(const void* x, const float* rstd, const void* wg, cons
   uint8_t* base = static_cast<uint8_t*>(ws);
   void* a_ws = base;
   void* du_ws = base + w.a;
-  float* dn_ws = reinterpret_cast<float*>(base + w.a + w.du);
+  void* dn_ws = base + w.a + w.du;
   void* split_ws = base + w.a + w.du + w.dn;
   // a = f(u), r du, with u recomputed from x and rstd
   MLP_CHECK(launch_block_bwd_act(x, wg, wd, dy, rstd, T, hidden, slope, a_ws, du_ws, st));
@@ -58,8 +58,8 @@ mlp_status block_bwd_impl(const void* x, const float* rstd, const void* wg, cons
   MLP_CHECK(gemm(hidden, d, T, a_ws, hidden, 1, dy, d, 0, dwd, d, st, split_ws, w.split));
   // dW_gate = x^T (r du) = n^T du   [d][hidden]
   MLP_CHECK(gemm(d, hidden, T, x, d, 1, du_ws, hidden, 0, dwg, hidden, st, split_ws, w.split));
-  // dn' = (r du) W_gate^T   [T][d]
-  MLP_CHECK(gemm(T, d, hidden, du_ws, hidden, 0, wg, hidden, 1, dn_ws, d, st));
+  // dn' = (r du) W_gate^T   [T][d], rounded to bf16 (it only feeds dx)
+  MLP_CHECK(gemm(T, d, hidden, du_ws, hidden, 0, wg, hidden, 1, dn_ws, d, st, nullptr, 0, 1));
   // dx = dy + dn' - r^2 x mean(dn' x)
   return launch_rmsnorm_bwd(dn_ws, x, dy, rstd, T, dx, st);
 }

@@ -756,7 +756,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // dx = dy + dn' - r^2 x s, s = mean_i(dn'_i x_i), with dn' = (r du) W_gate^T.
 // One warp per token row; lanes hold 16 of the 512 columns.
-__global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const float* __restrict__ dnp,
+__global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ dnp,
                                                           const __nv_bfloat16* __restrict__ x,
                                                           const __nv_bfloat16* __restrict__ dy,
                                                           const float* __restrict__ rstd, int T,
@@ -772,10 +772,14 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const float* __restric
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int c0 = h * 256 + lane * 8;
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(dnp + base + c0));
-    const float4 b = __ldcs(reinterpret_cast<const float4*>(dnp + base + c0 + 4));
-    dn[h * 8 + 0] = a.x; dn[h * 8 + 1] = a.y; dn[h * 8 + 2] = a.z; dn[h * 8 + 3] = a.w;
-    dn[h * 8 + 4] = b.x; dn[h * 8 + 5] = b.y; dn[h * 8 + 6] = b.z; dn[h * 8 + 7] = b.w;
+    const uint4 dq = __ldcs(reinterpret_cast<const uint4*>(dnp + base + c0));
+    const __nv_bfloat162* dnh = reinterpret_cast<const __nv_bfloat162*>(&dq);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(dnh[e]);
+      dn[h * 8 + 2 * e] = f.x;
+      dn[h * 8 + 2 * e + 1] = f.y;
+    }
     const uint4 xq = __ldg(reinterpret_cast<const uint4*>(x + base + c0));
     const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xq);
 #pragma unroll
@@ -898,13 +902,13 @@ mlp_status launch_block_bwd_act(const void* x, const void* wg, const void* wd, c
   return launch_status();
 }
 
-mlp_status launch_rmsnorm_bwd(const float* dnp, const void* x, const void* dy, const float* rstd,
+mlp_status launch_rmsnorm_bwd(const void* dnp, const void* x, const void* dy, const float* rstd,
                               int T, void* dx, cudaStream_t st) {
   if (T <= 0) return MLP_OK;
   LaunchScope ls("rmsnorm_bwd", st, T);
-  launch_k(rmsnorm_bwd_kernel, dim3((T + 7) / 8), dim3(256), 0, st, dnp, static_cast<const __nv_bfloat16*>(x),
-                                                  static_cast<const __nv_bfloat16*>(dy), rstd, T,
-                                                  static_cast<__nv_bfloat16*>(dx));
+  launch_k(rmsnorm_bwd_kernel, dim3((T + 7) / 8), dim3(256), 0, st,
+           static_cast<const __nv_bfloat16*>(dnp), static_cast<const __nv_bfloat16*>(x),
+           static_cast<const __nv_bfloat16*>(dy), rstd, T, static_cast<__nv_bfloat16*>(dx));
   return launch_status();
 }
 

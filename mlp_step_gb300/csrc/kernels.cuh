@@ -127,7 +127,8 @@ mlp_status launch_block_fwd(const void* x, const void* wg, const void* wd, int T
 mlp_status launch_block_bwd_act(const void* x, const void* wg, const void* wd, const void* dy,
                                 const float* rstd, int T, int hidden, float slope, void* a_out,
                                 void* du_out, cudaStream_t st);
-mlp_status launch_rmsnorm_bwd(const float* dnp, const void* x, const void* dy, const float* rstd,
+// dnp: bf16 [T][512]
+mlp_status launch_rmsnorm_bwd(const void* dnp, const void* x, const void* dy, const float* rstd,
                               int T, void* dx, cudaStream_t st);
 
 // Host helpers (api.cu)
