@@ -174,6 +174,43 @@ def test_bf16_epoch_matches_step_sequence():
     assert M.get_device_status() == M.MLP_OK
 
 
+@pytest.mark.parametrize("rem", [0, 40])
+def test_bf16_epochs_with_even_step_counts_match_step_sequence(rem):
+    """Epoch programs alternate two input buffers; after an even number of
+    full steps the handle's input names the second one.  Two epochs in a row
+    (2 full steps each, with or without a remainder) and a forward afterwards
+    must still equal the step-by-step sequence bit for bit."""
+    B = 128
+    n = 2 * B + rem
+    p0 = synth.mlp_flat_params(DIMS)
+    xb = to_dev(synth.images_u8(2 * n, 784))
+    y = to_dev(synth.labels(2 * n, 10))
+    ep = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+    sq = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+    steps = (n + B - 1) // B
+    losses = torch.zeros(2 * steps, device="cuda")
+    loss_s = torch.zeros(2 * steps, 4, device="cuda")
+    for e in range(2):
+        a0 = e * n
+        ep.train_epoch(xb[a0:a0 + n], y[a0:a0 + n], LR, MOM, B,
+                       losses_out=losses[e * steps:(e + 1) * steps])
+        for s in range(steps):
+            a, b = a0 + s * B, a0 + min(n, (s + 1) * B)
+            sq.train_step(xb[a:b], y[a:b], LR, MOM, loss_out=loss_s[e * steps + s])
+    torch.cuda.synchronize()
+    assert torch.equal(losses, loss_s[:, 0])
+    for name in ("params", "velocity", "grads", "shadow"):
+        assert torch.equal(getattr(ep, name), getattr(sq, name)), name
+    # the handle's own input buffer is usable afterwards
+    lg_e = torch.empty(B, 10, device="cuda")
+    lg_s = torch.empty(B, 10, device="cuda")
+    ep.forward(xb[:B], lg_e)
+    sq.forward(xb[:B], lg_s)
+    torch.cuda.synchronize()
+    assert torch.equal(lg_e, lg_s)
+    assert M.get_device_status() == M.MLP_OK
+
+
 def test_bf16_epoch_rejects_misaligned_steps():
     net = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=128)
     xb = torch.zeros(12, 784, dtype=torch.uint8, device="cuda")
