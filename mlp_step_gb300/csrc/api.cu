@@ -314,6 +314,7 @@ struct mlp_handle {
   std::vector<int> act_ld;         // act_ld[l]: pitch of layer l's input buffer
   void* x_copy = nullptr;          // [max_batch][act_ld[0]]
   void* x_copy_alt = nullptr;      // second input buffer of multi-step programs (bf16 only)
+  void* simt_ws = nullptr;         // split-K scratch of the fp32 GEMMs (fp32 only)
   std::vector<void*> acts;         // acts[l] = H_{l+1}, l = 0..L-2
   float* logits = nullptr;         // [max_batch][C]
   void* dlogits = nullptr;         // [max_batch][ldz]
@@ -341,7 +342,7 @@ bool dims_ok(const int* dims, int n_dims) {
 }
 
 struct Plan {
-  size_t x, x_alt, acts_total, logits, dlogits, dh, loss, red, total;
+  size_t x, x_alt, acts_total, logits, dlogits, dh, loss, red, simt, total;
 };
 
 Plan plan(const int* dims, int n_dims, int max_batch, int prec) {
@@ -364,7 +365,9 @@ Plan plan(const int* dims, int n_dims, int max_batch, int prec) {
   p.loss = 256;
   size_t red = xent_workspace_bytes(max_batch);
   p.red = align256(red > 0 ? red : 256);
-  p.total = p.x + p.x_alt + p.acts_total + p.logits + p.dlogits + 2 * p.dh + p.loss + p.red;
+  p.simt = prec == MLP_PREC_BF16 ? 0 : align256(gemm_simt_scratch_bytes());
+  p.total = p.x + p.x_alt + p.acts_total + p.logits + p.dlogits + 2 * p.dh + p.loss + p.red +
+            p.simt;
   return p;
 }
 
@@ -389,8 +392,20 @@ mlp_status ensure_ones(mlp_handle* h, cudaStream_t st) {
     ++oc.n;
   }
   MLP_CHECK(launch_ones_cols(oc, h->max_batch, h->prec == MLP_PREC_BF16, st));
+  // the split-K counters of the fp32 GEMMs start at zero (each launch leaves
+  // them so)
+  if (h->simt_ws && cudaMemsetAsync(h->simt_ws, 0, 4096, st) != cudaSuccess) return MLP_ERR_CUDA;
   h->ones_ready = true;
   return MLP_OK;
+}
+
+// fp32 GEMMs of the handle get its split-K scratch
+GemmArgs& with_simt_ws(const mlp_handle* h, GemmArgs& g) {
+  if (h->prec != MLP_PREC_BF16 && h->simt_ws) {
+    g.ws = h->simt_ws;
+    g.ws_bytes = gemm_simt_scratch_bytes();
+  }
+  return g;
 }
 
 // Hidden layers 0 .. L-2 of the forward (bias + activation in the epilogue);
@@ -418,7 +433,7 @@ mlp_status forward_hidden(mlp_handle* h, int batch, cudaStream_t st, StepSpec* r
     g.C = h->acts[l];
     g.ldc = h->act_ld[l + 1];
     g.c_bf16 = bf ? 1 : 0;
-    MLP_CHECK(issue_gemm(g, bf, st, rec, 1 + l));
+    MLP_CHECK(issue_gemm(with_simt_ws(h, g), bf, st, rec, 1 + l));
   }
   return MLP_OK;
 }
@@ -495,7 +510,7 @@ mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int
         gd.ldc = fi;
       }
       gd.c_bf16 = bf ? 1 : 0;
-      MLP_CHECK(issue_gemm(gd, bf, st, rec, 2 * h->L - l));
+      MLP_CHECK(issue_gemm(with_simt_ws(h, gd), bf, st, rec, 2 * h->L - l));
     }
     // [dW_l; db_l] = [In_l | 1]^T dY_l   (A = In_l read transposed), written
     // over the layer's flat slice of grads
@@ -520,7 +535,7 @@ mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int
       gw.sgd_shadow_rows = fi;
     }
     if (rec && fuse_sgd && !fuse_here) return MLP_ERR_UNSUPPORTED_SHAPE;
-    MLP_CHECK(issue_gemm(gw, bf, st, rec, 2 * h->L - l + (want_din ? 1 : 0)));
+    MLP_CHECK(issue_gemm(with_simt_ws(h, gw), bf, st, rec, 2 * h->L - l + (want_din ? 1 : 0)));
     if (fuse_sgd && !fuse_here) {
       // flat SGD over this layer's W and b (and its shadow rows)
       SgdSegments seg{};
@@ -605,7 +620,7 @@ mlp_status train_step_impl(mlp_handle* h, const void* x, int x_dtype, const int3
     gz.xent_norm = batch;
     MLP_CHECK(run_gemm(gz, true, st));
   } else {
-    MLP_CHECK(run_gemm(gz, bf, st));
+    MLP_CHECK(run_gemm(with_simt_ws(h, gz), bf, st));
     MLP_CHECK(launch_xent(h->logits, h->ldl, labels, batch, C, loss, h->dlogits, bf, h->ldz,
                           argmax_out, h->red, st));
   }
@@ -727,6 +742,8 @@ mlp_status mlp_create(const int* dims, int n_dims, int hidden_act, int prec, int
   w += pl.loss;
   h->red = w;
   h->red_bytes = pl.red;
+  w += pl.red;
+  if (pl.simt) h->simt_ws = w;
   *out = h;
   return MLP_OK;
 }
@@ -750,7 +767,8 @@ mlp_status mlp_forward(mlp_handle* h, const void* x, int x_dtype, int batch, flo
   cudaStream_t st = S(stream);
   MLP_CHECK(load_input(h, x, x_dtype, batch, st));
   MLP_CHECK(forward_hidden(h, batch, st));
-  MLP_CHECK(run_gemm(logits_gemm(h, batch, logits, h->dims[h->L]), h->prec == MLP_PREC_BF16, st));
+  GemmArgs gl = logits_gemm(h, batch, logits, h->dims[h->L]);
+  MLP_CHECK(run_gemm(with_simt_ws(h, gl), h->prec == MLP_PREC_BF16, st));
   h->have_forward = true;
   return MLP_OK;
 }

@@ -137,9 +137,19 @@ __device__ __forceinline__ void stage_quad(float* dst, const float* base, int ld
   }
 }
 
+// Split-K scratch (in the caller's workspace g.ws): per-tile arrival counters,
+// then the raw 64 x 64 partial sums of every (tile, split).
+constexpr int kSimtCounters = 512;
+constexpr int kSimtMaxParts = 304;
+
 __global__ void __launch_bounds__(256) gemm_simt_f32_pipelined_kernel(GemmArgs g) {
   pdl_wait();
   pdl_launch_dependents();
+  // split z of gridDim.z sums k-steps [kt0, kt1); with splits the last split
+  // of a tile to finish adds the partials in split order (deterministic) and
+  // runs the epilogue
+  const int splits = gridDim.z, z = blockIdx.z;
+  __shared__ int s_last;
   // A slot: [64 m][20] (A stored [M][K]) or [16 k][68] (stored [K][M]);
   // B slot: [16 k][68] (B stored [K][N]) or [64 n][20] (stored [N][K]).
   __shared__ __align__(16) float As[SIMT_STAGES][SIMT_SLOT];
@@ -149,14 +159,17 @@ __global__ void __launch_bounds__(256) gemm_simt_f32_pipelined_kernel(GemmArgs g
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
   const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
-  const int nk = (g.K + 15) / 16;
+  const int nk_all = (g.K + 15) / 16;
+  const int per = (nk_all + splits - 1) / splits;
+  const int kt0 = z * per < nk_all ? z * per : nk_all;
+  const int nk = (kt0 + per < nk_all ? kt0 + per : nk_all) - kt0;  // k-steps of this split
   const bool a_vec = (reinterpret_cast<uintptr_t>(A) & 15) == 0 && (g.lda & 3) == 0;
   const bool b_vec = (reinterpret_cast<uintptr_t>(B) & 15) == 0 && (g.ldb & 3) == 0;
   float acc[4][4] = {};
 
   // each thread stages one quad of each operand per step
   auto issue = [&](int kt) {
-    const int st = kt % SIMT_STAGES, k0 = kt * 16;
+    const int st = kt % SIMT_STAGES, k0 = (kt0 + kt) * 16;
     if (!g.a_trans) {
       const int m = tid >> 2, kq = (tid & 3) * 4;
       stage_quad(&As[st][m * 20 + kq], A, g.lda, m0 + m, k0 + kq, g.M, g.K, a_vec);
@@ -206,6 +219,36 @@ __global__ void __launch_bounds__(256) gemm_simt_f32_pipelined_kernel(GemmArgs g
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 
+  if (splits > 1) {
+    const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+    unsigned* counters = static_cast<unsigned*>(g.ws);
+    float* parts = reinterpret_cast<float*>(static_cast<uint8_t*>(g.ws) + kSimtCounters * 4);
+    float* mine = parts + ((size_t)tile * splits + z) * 4096;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(mine + (ty * 4 + i) * 64 + tx * 4) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&counters[tile], 1u) == (unsigned)(splits - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int z2 = 0; z2 < splits; ++z2) {
+      const float* pz = parts + ((size_t)tile * splits + z2) * 4096;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 q = __ldcg(reinterpret_cast<const float4*>(pz + (ty * 4 + i) * 64 + tx * 4));
+        acc[i][0] += q.x; acc[i][1] += q.y; acc[i][2] += q.z; acc[i][3] += q.w;
+      }
+    }
+    if (tid == 0) counters[tile] = 0;  // ready for the next launch
+  }
+
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int m = m0 + ty * 4 + i;
@@ -227,13 +270,35 @@ __global__ void __launch_bounds__(256) gemm_simt_f32_pipelined_kernel(GemmArgs g
   }
 }
 
+size_t gemm_simt_scratch_bytes() {
+  return (size_t)kSimtCounters * 4 + (size_t)kSimtMaxParts * 64 * 64 * 4;
+}
+
+// K splits of an fp32 GEMM: when its tiles leave most SMs idle, K is cut so
+// that about one CTA per SM runs (each split at least two 16-deep steps);
+// needs the split-K scratch in g.ws (counters zero between launches).
+static int simt_splits(const GemmArgs& g, int tiles) {
+  if (!g.ws || g.ws_bytes < gemm_simt_scratch_bytes() || (reinterpret_cast<uintptr_t>(g.ws) & 15))
+    return 1;
+  if (tiles >= num_sms() || tiles > kSimtCounters) return 1;
+  const int nk = (g.K + 15) / 16;
+  int s = (num_sms() + tiles - 1) / tiles;
+  if (s > nk / 2) s = nk / 2;
+  if (s * tiles > kSimtMaxParts) s = kSimtMaxParts / tiles;
+  return s < 1 ? 1 : s;
+}
+
 mlp_status launch_gemm_simt(const GemmArgs& g, int in_bf16, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0) return MLP_OK;
   dim3 grid((g.N + 63) / 64, (g.M + 63) / 64);
   if (grid.y > 65535) return MLP_ERR_UNSUPPORTED_SHAPE;
   LaunchScope ls("gemm_simt", st, g.M, g.N, g.K);
-  if (in_bf16) launch_k(gemm_simt_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st, g);
-  else launch_k(gemm_simt_f32_pipelined_kernel, dim3(grid), dim3(256), 0, st, g);
+  if (in_bf16) {
+    launch_k(gemm_simt_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st, g);
+  } else {
+    grid.z = simt_splits(g, (int)(grid.x * grid.y));
+    launch_k(gemm_simt_f32_pipelined_kernel, dim3(grid), dim3(256), 0, st, g);
+  }
   return launch_status();
 }
 

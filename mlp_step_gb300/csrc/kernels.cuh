@@ -81,7 +81,11 @@ struct GemmArgs {
   int sgd_ld_shadow = 0;
   int sgd_shadow_rows = 0;
 };
+// fp32 operands (in_bf16 = 0) with g.ws holding gemm_simt_scratch_bytes()
+// (16-byte aligned, its first 2 KiB zero before the first launch): small
+// problems split K over more CTAs.
 mlp_status launch_gemm_simt(const GemmArgs& g, int in_bf16, cudaStream_t st);
+size_t gemm_simt_scratch_bytes();
 
 // k_gemm_tc.cu: tcgen05 bf16 GEMM (TMA-fed, fp32 accumulation in tensor memory).
 mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStream_t st);
