@@ -191,9 +191,84 @@ class Workload:
     h2d_bytes = 0
     d2h_bytes = 0
     launches_per_step = 0
+    # End to end with the next step's input copies overlapping the current
+    # step (a data loader's prefetch): (host attribute, device attribute) of
+    # every input the step reads, and the result read back after each step.
+    # Only for workloads whose inputs and working set are far above L2.
+    e2e_inputs = ()
+
+    def e2e_result(self):
+        """(device tensor, pinned host tensor) of the per-step result."""
+        raise NotImplementedError
 
     def check(self):
         pass
+
+
+def capture_graph(wl):
+    """A CUDA graph of one eager step of the workload (its current buffers)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            wl.step_eager()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g
+
+
+def e2e_slots(wl):
+    """Two input-buffer sets, each with a graph of the step over it: slot 0 is
+    the workload's own, slot 1 a second copy of every input."""
+    import torch
+    own = {d: getattr(wl, d) for _, d in wl.e2e_inputs}
+    slots = [(own, wl.graph)]
+    second = {d: torch.empty_like(t).copy_(t) for d, t in own.items()}
+    for d, t in second.items():
+        setattr(wl, d, t)
+    wl.step_eager()  # warm the second buffers' tensor maps outside the capture
+    torch.cuda.synchronize()
+    slots.append((second, capture_graph(wl)))
+    for d, t in own.items():
+        setattr(wl, d, t)
+    return slots
+
+
+def timed_e2e_pipelined(wl, slots, steps, sync_barrier):
+    """Wall time (ms, CUDA events) of `steps` end-to-end steps: every step
+    copies its inputs from pinned host memory (a second stream, into the slot
+    the step before last has released), runs the step's graph once its copies
+    have landed, and reads its result back; step k + 1's copies overlap step
+    k's kernels."""
+    import torch
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    ready = [torch.cuda.Event(), torch.cuda.Event()]
+    freed = [torch.cuda.Event(), torch.cuda.Event()]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    dev_out, host_out = wl.e2e_result()
+    sync_barrier()
+    start.record(comp)
+    copy.wait_event(start)
+    for k in range(steps):
+        i = k & 1
+        bufs, graph = slots[i]
+        with torch.cuda.stream(copy):
+            if k >= 2:
+                copy.wait_event(freed[i])
+            for h, d in wl.e2e_inputs:
+                bufs[d].copy_(getattr(wl, h), non_blocking=True)
+            ready[i].record(copy)
+        comp.wait_event(ready[i])
+        graph.replay()
+        freed[i].record(comp)
+        host_out.copy_(dev_out, non_blocking=True)
+    end.record(comp)
+    sync_barrier()
+    return start.elapsed_time(end)
 
 
 class MLP784Epoch(Workload):
@@ -366,6 +441,11 @@ class WideMLP(Workload):
         self.graph.replay()
         self.loss_host.copy_(self.loss, non_blocking=True)
 
+    e2e_inputs = (("x_host", "x"), ("y_host", "y"))
+
+    def e2e_result(self):
+        return self.loss, self.loss_host
+
     def check(self):
         import torch
         torch.cuda.synchronize()
@@ -466,6 +546,11 @@ class BlockStep(Workload):
         self.graph.replay()
         self.dx_host.copy_(self.dx[0, :4], non_blocking=True)
 
+    e2e_inputs = (("x_host", "x"), ("dy_host", "dy"))
+
+    def e2e_result(self):
+        return self.dx[0, :4], self.dx_host
+
     def check(self):
         import torch
         torch.cuda.synchronize()
@@ -562,6 +647,11 @@ class StackStep(Workload):
         self.t.copy_(self.t_host, non_blocking=True)
         self.graph.replay()
         self.loss_host.copy_(self.loss, non_blocking=True)
+
+    e2e_inputs = (("x_host", "x"), ("t_host", "t"))
+
+    def e2e_result(self):
+        return self.loss, self.loss_host
 
     def check(self):
         import torch
@@ -749,7 +839,16 @@ def run_ours(args, wl):
         dev_ms = timed_loop(wl.step, args.steps, flush, sync_barrier)
         wall = time.perf_counter() - t0
     wl.check()
-    e2e_ms = timed_loop(wl.step_e2e, args.steps, flush, sync_barrier)
+    if wl.e2e_inputs:
+        slots = e2e_slots(wl)
+        for _ in range(2):  # warm-up of the pipelined form
+            timed_e2e_pipelined(wl, slots, 2, sync_barrier)
+        e2e_ms = timed_e2e_pipelined(wl, slots, args.steps, sync_barrier)
+        e2e_mode = ("pipelined: step k+1's host-to-device copies overlap step k on a second "
+                    "stream (inputs and working set far above L2, no flush)")
+    else:
+        e2e_ms = timed_loop(wl.step_e2e, args.steps, flush, sync_barrier)
+        e2e_mode = "serial: copies, step, read-back per step; L2 flushed between steps"
     wl.check()
 
     dev_ms, e2e_ms = max_over_ranks(dist, [dev_ms, e2e_ms],
@@ -774,7 +873,8 @@ def run_ours(args, wl):
                                             else "single GPU"),
         "clocks": clk.summary(),
         "e2e": {"value": round(e2e_value, 3), "unit": wl.unit,
-                "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
+                "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes,
+                "mode": e2e_mode},
         "gpu_launches": wl.launches_per_step * args.steps,
         "roofline": roof,
         "kernels": {k: [n, round(ms / n, 6)] for k, (n, ms) in sorted(rep.items())},
