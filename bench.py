@@ -279,6 +279,9 @@ class MLP784Epoch(Workload):
 
     def __init__(self, prec_name="bf16", n_images=6000, batch=128):
         self.prec_name = prec_name
+        if prec_name == "fp32":
+            self.name = "mlp784_fp32"
+            self.dtype = "f32"
         self.n_images = n_images
         self.batch = batch
         self.n_steps = (n_images + batch - 1) // batch
@@ -707,8 +710,9 @@ SIZED = {"block": lambda T: BlockStep(T=T), "stack": lambda T: StackStep(T=T),
 
 # ------------------------------------------------------------------ measurement
 
-def timed_loop(fn, steps, flush, sync_barrier):
-    """Sum of per-step CUDA-event durations (ms) over `steps` calls of fn."""
+def timed_loop(fn, steps, flush, sync_barrier, per_step=None):
+    """Sum of per-step CUDA-event durations (ms) over `steps` calls of fn
+    (the durations themselves appended to per_step when given)."""
     import torch
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
@@ -719,7 +723,10 @@ def timed_loop(fn, steps, flush, sync_barrier):
         fn()
         e.record()
     sync_barrier()
-    return sum(s.elapsed_time(e) for s, e in evs)
+    ts = [s.elapsed_time(e) for s, e in evs]
+    if per_step is not None:
+        per_step.extend(ts)
+    return sum(ts)
 
 
 def kernel_profile(wl, steps):
@@ -848,7 +855,8 @@ def run_ours(args, wl):
 
     with ClockSampler(local) as clk:
         t0 = time.perf_counter()
-        dev_ms = timed_loop(wl.step, args.steps, flush, sync_barrier)
+        step_ms = []
+        dev_ms = timed_loop(wl.step, args.steps, flush, sync_barrier, step_ms)
         wall = time.perf_counter() - t0
     wl.check()
     if wl.e2e_inputs:
@@ -877,9 +885,12 @@ def run_ours(args, wl):
     if roof is not None:
         roof["traffic"] = recorded_traffic(roof["kernel"], wl.name)
 
+    med = float(np.median(step_ms))
+    cv = float(np.std(step_ms) / np.mean(step_ms)) if len(step_ms) > 1 else 0.0
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": wl.unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "ms_per_step_median": round(med, 6), "ms_per_step_cv": round(cv, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic", "config": dict(wl.config, parallelism="replicas" if world > 1
                                             else "single GPU"),
@@ -893,9 +904,18 @@ def run_ours(args, wl):
         "wall_s_timed_region": round(wall, 4),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.set_threads(os.cpu_count())
         done, dt, sample = wl.oracle_sample(args.cpu_seconds)
         out["cpu_baseline"] = {"value": round(done / dt, 3), "unit": wl.unit,
                                "cores": os.cpu_count(), "kind": "oracle", "sample": sample}
+        if wl.name == "mlp784_fp32":
+            # the single-step configuration is also timed on one host thread
+            oracle.set_threads(1)
+            done, dt, sample = wl.oracle_sample(args.cpu_seconds)
+            out["cpu_baseline_1thread"] = {"value": round(done / dt, 3), "unit": wl.unit,
+                                           "cores": 1, "kind": "oracle", "sample": sample}
+            oracle.set_threads(os.cpu_count())
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist is not None:

@@ -39,6 +39,8 @@ def lib():
         build()
         _lib = ctypes.CDLL(_LIB)
         L = _lib
+        L.orc_set_threads.argtypes = [ctypes.c_int]
+        L.orc_max_threads.restype = ctypes.c_int
         L.orc_round_bf16.restype = ctypes.c_double
         L.orc_round_bf16.argtypes = [ctypes.c_double]
         L.orc_param_count.restype = ctypes.c_longlong
@@ -100,6 +102,15 @@ def _p(a, t):
 
 def _dims(dims):
     return (ctypes.c_int * len(dims))(*dims), len(dims)
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's OpenMP loops (for timing)."""
+    lib().orc_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return lib().orc_max_threads()
 
 
 def round_bf16(v: float) -> float:

@@ -40,8 +40,14 @@
 #include <cstring>
 #include <vector>
 #include <algorithm>
+#include <omp.h>
 
 extern "C" {
+
+// Threads of the OpenMP loops below (timing runs only; results do not
+// depend on it: every reduction sums in a fixed order within one thread).
+void orc_set_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
+int orc_max_threads() { return omp_get_max_threads(); }
 
 // ---------------------------------------------------------------- helpers
 
