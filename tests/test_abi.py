@@ -97,3 +97,77 @@ def test_other_entry_points_reject_bad_arguments(lib):
     assert lib.mlp_colsum(fake, 7, 4, 4, 4, fake, None, 0, None) == 1
     assert lib.mse_loss_fwd_bwd(fake, fake, 100, fake, fake, None, 0, None) == 1
     assert lib.mlp_selftest_wait_timeout(0, None) == 1
+
+
+def test_block_and_stack_entry_points_check_shapes_and_pointers(lib):
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)  # 8-byte aligned only
+    f = ctypes.c_float
+    # forward: negative T, unsupported width / hidden size, negative eps
+    assert lib.mlp_block_fwd(fake, fake, fake, -1, 512, 1536, f(1e-6), f(0.5), fake, fake,
+                             None) == 1
+    assert lib.mlp_block_fwd(fake, fake, fake, 8, 256, 1536, f(1e-6), f(0.5), fake, fake,
+                             None) == 3
+    assert lib.mlp_block_fwd(fake, fake, fake, 8, 512, 1000, f(1e-6), f(0.5), fake, fake,
+                             None) == 3
+    assert lib.mlp_block_fwd(fake, fake, fake, 8, 512, 1536, f(-1.0), f(0.5), fake, fake,
+                             None) == 1
+    # empty: nothing to do; null pointers are fine then
+    assert lib.mlp_block_fwd(None, None, None, 0, 512, 1536, f(1e-6), f(0.5), None, None,
+                             None) == 0
+    assert lib.mlp_block_fwd(None, fake, fake, 8, 512, 1536, f(1e-6), f(0.5), fake, fake,
+                             None) == 1
+    assert lib.mlp_block_fwd(odd, fake, fake, 8, 512, 1536, f(1e-6), f(0.5), fake, fake,
+                             None) == 2
+    # backward: workspace too small, empty, misaligned
+    need = M.mlp_block_workspace_bytes(8, 512, 1536)
+    assert need > 0 and M.mlp_block_workspace_bytes(8, 512, 1000) == 0
+    args = [fake, fake, fake, fake, fake, 8, 512, 1536, f(1e-6), f(0.5), fake, fake, fake, fake]
+    assert lib.mlp_block_bwd(*args, need - 1, None) == 1
+    assert lib.mlp_block_bwd(*args[:5], 0, *args[6:], 0, None) == 0
+    assert lib.mlp_block_bwd(odd, *args[1:], need, None) == 2
+    # stack: no blocks, empty, workspace too small
+    P = M.mlp_stack_param_count(2, 512, 1536)
+    assert P == 2 * 2 * 512 * 1536
+    ws = M.mlp_stack_workspace_bytes(2, 8, 512, 1536)
+    st = [fake, fake, fake, fake, fake, fake, f(0.02), f(0.95), fake, fake]
+    assert lib.mlp_stack_train_step(0, 8, 512, 1536, f(1e-6), f(0.5), *st, ws, None) == 1
+    assert lib.mlp_stack_train_step(2, 0, 512, 1536, f(1e-6), f(0.5), *st, ws, None) == 0
+    assert lib.mlp_stack_train_step(2, 8, 512, 1536, f(1e-6), f(0.5), *st, ws - 1, None) == 1
+    assert lib.mlp_stack_train_step(2, 8, 512, 1000, f(1e-6), f(0.5), *st, ws, None) == 3
+
+
+def test_loss_and_update_entry_points_check_arguments(lib):
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10004)
+    f = ctypes.c_float
+    # softmax cross entropy: no classes, leading dimensions below the width,
+    # unknown dZ type
+    assert lib.softmax_xent_fwd_bwd(fake, 10, fake, 4, 0, None, None, 0, 10, None, None, 0,
+                                    None) == 1
+    assert lib.softmax_xent_fwd_bwd(fake, 8, fake, 4, 10, None, None, 0, 10, None, None, 0,
+                                    None) == 1
+    assert lib.softmax_xent_fwd_bwd(fake, 10, fake, 4, 10, None, fake, 0, 8, None, None, 0,
+                                    None) == 1
+    assert lib.softmax_xent_fwd_bwd(fake, 10, fake, 4, 10, None, fake, 9, 16, None, None, 0,
+                                    None) == 1
+    # MSE: empty, misaligned input
+    assert lib.mse_loss_fwd_bwd(None, None, 0, None, None, None, 0, None) == 0
+    ws = M.mse_workspace_bytes(100)
+    assert lib.mse_loss_fwd_bwd(odd, fake, 100, fake, fake, fake, ws, None) == 2
+    # column sums: negative rows, nothing to sum, ld below the width
+    assert lib.mlp_colsum(fake, 0, -1, 4, 4, fake, None, 0, None) == 1
+    assert lib.mlp_colsum(None, 0, 4, 0, 4, None, None, 0, None) == 0
+    assert lib.mlp_colsum(fake, 0, 4, 8, 4, fake, None, 0, None) == 1
+    # GEMM: negative sizes, empty output, unknown activation
+    g = [fake, 8, 0, fake, 8, 0, 0, None, 0, None, 0, fake, 8, 0, None]
+    assert lib.mlp_gemm(-1, 8, 8, *g) == 1
+    assert lib.mlp_gemm(0, 8, 8, *g) == 0
+    assert lib.mlp_gemm(8, 0, 8, *g) == 0
+    assert lib.mlp_gemm(8, 8, 8, fake, 8, 0, fake, 8, 0, 0, None, 5, None, 0, fake, 8, 0,
+                        None) == 1
+    # training entry points without a handle
+    assert lib.mlp_train_step(None, fake, 2, fake, 128, f(0.1), f(0.9), None, None, None) == 1
+    assert lib.mlp_train_epoch(None, fake, 2, fake, 256, 128, f(0.1), f(0.9), None, None,
+                               None) == 1
+    assert lib.mlp_forward(None, fake, 2, 128, fake, None) == 1
