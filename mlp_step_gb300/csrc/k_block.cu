@@ -19,13 +19,14 @@
 // RMSNorm with gain 1 is folded into the epilogue: u = r (x W_gate) with
 // r = 1 / sqrt(mean(x^2) + eps) per token, so the gate GEMM reads x as is.
 //
-// Backward (block_bwd_act_kernel): per 256-token x 128-hidden tile, two MMA
+// Backward (block_bwd_act_kernel): per 256-token x 256-hidden tile, two MMA
 // accumulators U = x W_gate[:, c] and DA = dy W_down[c, :]^T over K = 512,
-// computed by a CTA pair with tcgen05.mma.cta_group::2 (each CTA stages its
-// own 128 token rows of x and dy and half of the chunk's weight columns);
-// the epilogue writes a = f(r U) and r du = r DA f'(r U) in bf16 for the
-// weight-gradient GEMMs, through TMA bulk stores.  rmsnorm_bwd_kernel finishes dx from
-// dn' = (r du) W_gate^T.
+// computed one after the other by a CTA pair with tcgen05.mma.cta_group::2
+// (each CTA stages its own 128 token rows of x and dy and half of the tile's
+// weight columns); the epilogue converts each accumulator while the other is
+// being computed and writes a = f(r U) and r du = DA r f'(r U) in bf16 for
+// the weight-gradient GEMMs, through TMA bulk stores.  rmsnorm_bwd_kernel
+// finishes dx from dn' = (r du) W_gate^T.
 #include "kernels.cuh"
 #include "ptx.cuh"
 #include "trace.cuh"
@@ -43,7 +44,6 @@ constexpr int F_SLOTS = 2;                // one activation slot per CTA of the 
 constexpr int F_STAGE_BYTES = 49152;      // x k-block + two W_gate chunks' k-blocks
 constexpr int F_SLOT_BYTES = TM * HC * 2;  // 32 KiB bf16 activation chunk
 constexpr int F_SMEM = 1024 + F_SLOTS * F_SLOT_BYTES + F_STAGES * F_STAGE_BYTES + 2 * TM * 4 + 512;
-constexpr int kThreads = 192;
 
 __device__ __forceinline__ float lrelu_sq(float u, float slope) {
   const float t = u > 0.f ? u : slope * u;
@@ -501,14 +501,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
 
 // ------------------------------------------------------------------ backward
 
-// Per CTA and 64-wide k-block: x rows (16 KiB), this CTA's 64 W_gate
-// columns (8 KiB), dy rows (16 KiB), this CTA's 64 W_down rows (8 KiB).
-constexpr int B_STAGES = 4;
-constexpr int B_X = 0, B_WG = 16384, B_DY = 24576, B_WD = 40960;
-constexpr int B_STAGE_BYTES = 49152;
+// Each pair tile covers 256 tokens x BH = 256 hidden columns and runs as two
+// halves: U = x W_gate[:, tile] (K = 512) into tensor-memory columns
+// [0, 256), then DA = dy W_down[tile, :]^T into columns [256, 512).  Stage
+// one of the epilogue converts U (writes a = f(r U), keeps g = r f'(r U) as
+// packed bf16 in registers) while the MMA computes DA; stage two forms
+// r du = DA g while the MMA computes the next tile's U.  So the MMA never
+// waits for a whole-tile epilogue, and every x / dy k-block feeds 256 hidden
+// columns (the kernel is bound by how fast TMA fills one SM's shared memory
+// from L2, ~89 GB/s per SM on this part).
+//
+// A stage holds one half's operands for one 64-wide k-block: x or dy rows
+// (16 KiB) and this CTA's 128 W_gate columns (two 8 KiB boxes) or 128 W_down
+// rows (16 KiB).
+constexpr int BH = 256;
+constexpr int B_STAGES = 6;
+constexpr int B_A = 0, B_B = 16384;
+constexpr int B_STAGE_BYTES = 32768;
 constexpr int B_BAR_BYTES = 1024;
-constexpr int B_STG_BYTES = 4 * 8192;  // per epilogue warp: {a, du} x 2 buffers x 2 KiB
+constexpr int B_THREADS = 320;        // producer, MMA, 8 epilogue warps
+constexpr int B_STG_BYTES = 8 * 4096;  // per epilogue warp: 2 buffers x 2 KiB
 constexpr int B_SMEM = 1024 + B_STAGES * B_STAGE_BYTES + B_BAR_BYTES + B_STG_BYTES;
+static_assert(B_SMEM <= 232448, "backward kernel shared memory");
 
 struct BwdParams {
   int T, hidden, pairs_m, tiles_h, num_tiles;
@@ -518,10 +532,10 @@ struct BwdParams {
   int* err;
 };
 
-// Tile t covers token rows [256 pm, 256 pm + 256) and hidden chunk th.  Four
-// token pairs at a time sweep all hidden chunks (the last group may be
-// shorter), so pairs running together share x / dy rows and weight columns
-// in L2.
+// Tile t covers token rows [256 pm, 256 pm + 256) and hidden columns
+// [256 th, 256 th + 256).  Four token pairs at a time sweep all hidden
+// chunks (the last group may be shorter), so pairs running together share
+// x / dy rows and weight columns in L2.
 __device__ __forceinline__ void bwd_tile(int t, int pairs_m, int tiles_h, int& pm, int& th) {
   constexpr int G = 4;
   const int group = t / (G * tiles_h);
@@ -542,7 +556,27 @@ __device__ __forceinline__ void stage_row_bf16(uint8_t* box, int lane, const uin
         make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// One epilogue warp's 32 x 32 bf16 box through its double-buffered staging
+// area and a TMA store (rows past the last token are clipped by the map).
+__device__ __forceinline__ void store_box_bf16(const CUtensorMap* map, uint8_t* wstg,
+                                               int& stg_count, int lane,
+                                               const uint32_t (&pk)[16], int col, int row) {
+  uint8_t* box = wstg + (stg_count & 1) * 2048;
+  if (stg_count >= 2) {
+    if (lane == 0) ptx::bulk_wait_group_read<1>();
+    __syncwarp();
+  }
+  stage_row_bf16(box, lane, pk);
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    ptx::tma_store_2d(map, box, col, row);
+    ptx::bulk_commit_group();
+  }
+  ++stg_count;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(B_THREADS, 1)
     block_bwd_act_kernel(const __grid_constant__ CUtensorMap tmX,
                          const __grid_constant__ CUtensorMap tmWg,
                          const __grid_constant__ CUtensorMap tmDy,
@@ -556,8 +590,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(stages + B_STAGES * B_STAGE_BYTES);
   uint8_t* stg = stages + B_STAGES * B_STAGE_BYTES + B_BAR_BYTES;
   uint64_t* empty = full + B_STAGES;
-  uint64_t* tfull = empty + B_STAGES;
-  uint64_t* tempty = tfull + 2;
+  uint64_t* tfull = empty + B_STAGES;  // [half]: accumulator ready
+  uint64_t* tempty = tfull + 2;        // [half]: accumulator read out
   uint64_t* done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -570,9 +604,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&tfull[b], 1);
-      ptx::mbar_init(&tempty[b], 8);  // the pair's eight epilogue warps
+    for (int h = 0; h < 2; ++h) {
+      ptx::mbar_init(&tfull[h], 1);
+      ptx::mbar_init(&tempty[h], 16);  // the pair's sixteen epilogue warps
     }
     ptx::mbar_init(done, 1);
     *s_abort = 0;
@@ -589,7 +623,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
   ptx::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // buffer b: U at b*256, DA at b*256 + 128
+  const uint32_t tmem = *tmem_slot;  // U at column 0, DA at column BH
   pdl_wait();
   pdl_launch_dependents();
   int last_parity[B_STAGES];
@@ -605,129 +639,140 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int pm, th;
         bwd_tile(t, p.pairs_m, p.tiles_h, pm, th);
         const int m0 = pm * 2 * TM + (int)rank * TM;
-        const int h0 = th * HC + (int)rank * (HC / 2);
-        for (int kb = 0; kb < DM / 64; ++kb) {
-          if (!ptx::mbar_wait_cluster_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
-                                              DEVERR_TIMEOUT_PRODUCER)) {
-            *s_abort = 1;
-            ok = false;
-            break;
+        const int h0 = th * BH + (int)rank * (BH / 2);
+        for (int half = 0; half < 2 && ok; ++half) {
+          for (int kb = 0; kb < DM / 64; ++kb) {
+            if (!ptx::mbar_wait_cluster_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
+                                                DEVERR_TIMEOUT_PRODUCER)) {
+              *s_abort = 1;
+              ok = false;
+              break;
+            }
+            if (rank == 0) {
+              ptx::mbar_arrive_expect_tx(&full[stage], 2 * B_STAGE_BYTES);
+              last_parity[stage] = (int)phase;
+            }
+            const uint32_t bar = full0 + (uint32_t)stage * 8u;
+            uint8_t* st = stages + stage * B_STAGE_BYTES;
+            if (half == 0) {
+              ptx::tma_load_2d_pair(st + B_A, &tmX, bar, kb * 64, m0);
+              ptx::tma_load_2d_pair(st + B_B, &tmWg, bar, h0, kb * 64);
+              ptx::tma_load_2d_pair(st + B_B + 8192, &tmWg, bar, h0 + 64, kb * 64);
+            } else {
+              ptx::tma_load_2d_pair(st + B_A, &tmDy, bar, kb * 64, m0);
+              ptx::tma_load_2d_pair(st + B_B, &tmWd, bar, kb * 64, h0);
+            }
+            if (++stage == B_STAGES) { stage = 0; phase ^= 1; }
           }
-          if (rank == 0) {
-            ptx::mbar_arrive_expect_tx(&full[stage], 2 * B_STAGE_BYTES);
-            last_parity[stage] = (int)phase;
-          }
-          const uint32_t bar = full0 + (uint32_t)stage * 8u;
-          uint8_t* st = stages + stage * B_STAGE_BYTES;
-          ptx::tma_load_2d_pair(st + B_X, &tmX, bar, kb * 64, m0);
-          ptx::tma_load_2d_pair(st + B_WG, &tmWg, bar, h0, kb * 64);
-          ptx::tma_load_2d_pair(st + B_DY, &tmDy, bar, kb * 64, m0);
-          ptx::tma_load_2d_pair(st + B_WD, &tmWd, bar, kb * 64, h0);
-          if (++stage == B_STAGES) { stage = 0; phase ^= 1; }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
-      const uint32_t idesc_u = ptx::idesc_bf16_f32(2 * TM, HC, 0, 1);  // B = W_gate, N-major
-      const uint32_t idesc_a = ptx::idesc_bf16_f32(2 * TM, HC, 0, 0);  // B = W_down rows
+      // half 0: B = W_gate columns (N-major); half 1: B = W_down rows (K-major)
+      const uint32_t idesc[2] = {ptx::idesc_bf16_f32(2 * TM, BH, 0, 1),
+                                 ptx::idesc_bf16_f32(2 * TM, BH, 0, 0)};
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = pair; t < p.num_tiles && ok && !*s_abort; t += n_pairs) {
-        if (!ptx::mbar_wait_cluster_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err,
-                                            DEVERR_TIMEOUT_MMA)) { ok = false; break; }
-        ptx::tc_fence_after();
-        const uint32_t du = tmem + acc * 256;
-        const uint32_t da = du + 128;
-        for (int kb = 0; kb < DM / 64; ++kb) {
-          if (!ptx::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err,
-                                      DEVERR_TIMEOUT_MMA)) { ok = false; break; }
+        for (int half = 0; half < 2; ++half) {
+          if (!ptx::mbar_wait_cluster_bounded(&tempty[half], acc_phase ^ 1, p.wait_ns, p.err,
+                                              DEVERR_TIMEOUT_MMA)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t sb = ptx::smem_u32(stages + stage * B_STAGE_BYTES);
+          const uint32_t d = tmem + (uint32_t)(half * BH);
+          for (int kb = 0; kb < DM / 64; ++kb) {
+            if (!ptx::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err,
+                                        DEVERR_TIMEOUT_MMA)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t sb = ptx::smem_u32(stages + stage * B_STAGE_BYTES);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t en = (kb > 0 || k > 0) ? 1u : 0u;
-            ptx::mma_bf16_pair(du, ptx::sw128_desc(sb + B_X + k * 32, 16, 1024),
-                               ptx::sw128_desc(sb + B_WG + k * 2048, 8192, 1024), idesc_u, en);
-            ptx::mma_bf16_pair(da, ptx::sw128_desc(sb + B_DY + k * 32, 16, 1024),
-                               ptx::sw128_desc(sb + B_WD + k * 32, 16, 1024), idesc_a, en);
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t bd = half == 0 ? ptx::sw128_desc(sb + B_B + k * 2048, 8192, 1024)
+                                            : ptx::sw128_desc(sb + B_B + k * 32, 16, 1024);
+              ptx::mma_bf16_pair(d, ptx::sw128_desc(sb + B_A + k * 32, 16, 1024), bd,
+                                 idesc[half], (kb > 0 || k > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit_pair_multicast(&empty[stage], 3);
+            if (++stage == B_STAGES) { stage = 0; phase ^= 1; }
           }
-          ptx::mma_commit_pair_multicast(&empty[stage], 3);
-          if (++stage == B_STAGES) { stage = 0; phase ^= 1; }
+          if (!ok) break;
+          ptx::mma_commit_pair_multicast(&tfull[half], 3);
         }
-        if (!ok) break;
-        ptx::mma_commit_pair_multicast(&tfull[acc], 3);
-        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        acc_phase ^= 1;
       }
       if (!ok) *s_abort = 1;
       ptx::mma_commit_pair_multicast(done, 1);
       ptx::mbar_wait_bounded(done, 0, p.wait_ns, p.err, DEVERR_TIMEOUT_TEARDOWN);
     }
   } else {
+    // Warps 2-9: TMEM lane quarter warp % 4, columns [c_half, c_half + 128)
+    // of the tile.
     const int quarter = warp & 3;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int c_half = ((warp - 2) >> 2) * (BH / 2);
     const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_u32(tempty), 0);
-    uint8_t* wstg = stg + (warp - 2) * 8192;  // [buffer][a | du] boxes of 2 KiB
-    int acc = 0;
+    uint8_t* wstg = stg + (warp - 2) * 4096;
     uint32_t acc_phase = 0;
     int stg_count = 0;
-    for (int t = pair; t < p.num_tiles; t += n_pairs) {
-      if (*s_abort) break;
-      if (!ptx::mbar_wait_cluster_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err,
-                                          DEVERR_TIMEOUT_EPILOGUE)) {
-        *s_abort = 1;
-        break;
-      }
-      ptx::tc_fence_after();
+    bool ok = true;
+    for (int t = pair; t < p.num_tiles && ok; t += n_pairs) {
       int pm, th;
       bwd_tile(t, p.pairs_m, p.tiles_h, pm, th);
       const int row0 = pm * 2 * TM + (int)rank * TM + quarter * 32;  // this warp's first row
       const int m = row0 + lane;
       const float r = m < p.T ? __ldg(p.rstd + m) : 0.f;
-      for (int cc = 0; cc < HC / 32; ++cc) {
-        uint32_t vu[32], va[32];
-        __syncwarp();
-        ptx::tmem_ld_32x32b_x32(tmem + lane_off + acc * 256 + cc * 32, vu);
-        ptx::tmem_ld_32x32b_x32(tmem + lane_off + acc * 256 + 128 + cc * 32, va);
-        ptx::tmem_ld_wait();
-        if (row0 >= p.T) continue;  // warp-uniform: the whole box is past the last token
-        uint32_t pa[16], pd[16];
+      const int col0 = th * BH + c_half;
+      uint32_t g[BH / 4];  // r f'(r U) as packed bf16 pairs, 128 columns
+      for (int half = 0; half < 2; ++half) {
+        if (*s_abort) { ok = false; break; }
+        if (!ptx::mbar_wait_cluster_bounded(&tfull[half], acc_phase, p.wait_ns, p.err,
+                                            DEVERR_TIMEOUT_EPILOGUE)) {
+          *s_abort = 1;
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float u0 = __uint_as_float(vu[2 * e]) * r;
-          const float u1 = __uint_as_float(vu[2 * e + 1]) * r;
-          pa[e] = pack_bf16x2(lrelu_sq(u0, p.slope), lrelu_sq(u1, p.slope));
-          const float d0 = __uint_as_float(va[2 * e]) * lrelu_sq_grad(u0, p.slope) * r;
-          const float d1 = __uint_as_float(va[2 * e + 1]) * lrelu_sq_grad(u1, p.slope) * r;
-          pd[e] = pack_bf16x2(d0, d1);
-        }
-        uint8_t* box = wstg + (stg_count & 1) * 4096;
-        if (stg_count >= 2) {
-          if (lane == 0) ptx::bulk_wait_group_read<1>();
+        for (int cc = 0; cc < BH / 64; ++cc) {
+          uint32_t v[32];
           __syncwarp();
+          ptx::tmem_ld_32x32b_x32(tmem + lane_off + (uint32_t)(half * BH + c_half + cc * 32), v);
+          ptx::tmem_ld_wait();
+          if (cc + 1 == BH / 64) {
+            // this half's accumulator is in registers: the MMA may reuse it
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (rank == 0) ptx::mbar_arrive(&tempty[half]);
+              else ptx::mbar_arrive_remote(tempty0 + (uint32_t)half * 8u);
+            }
+          }
+          uint32_t pk[16];
+          if (half == 0) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float u0 = __uint_as_float(v[2 * e]) * r;
+              const float u1 = __uint_as_float(v[2 * e + 1]) * r;
+              pk[e] = pack_bf16x2(lrelu_sq(u0, p.slope), lrelu_sq(u1, p.slope));
+              g[cc * 16 + e] =
+                  pack_bf16x2(lrelu_sq_grad(u0, p.slope) * r, lrelu_sq_grad(u1, p.slope) * r);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const uint32_t w = g[cc * 16 + e];
+              pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * __uint_as_float(w << 16),
+                                  __uint_as_float(v[2 * e + 1]) * __uint_as_float(w & 0xffff0000u));
+            }
+          }
+          if (row0 < p.T)  // warp-uniform: boxes wholly past the last token are skipped
+            store_box_bf16(half == 0 ? &tmA : &tmDu, wstg, stg_count, lane, pk, col0 + cc * 32,
+                           row0);
         }
-        stage_row_bf16(box, lane, pa);
-        stage_row_bf16(box + 2048, lane, pd);
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          // rows past T are clipped by the tensor maps
-          ptx::tma_store_2d(&tmA, box, th * HC + cc * 32, row0);
-          ptx::tma_store_2d(&tmDu, box + 2048, th * HC + cc * 32, row0);
-          ptx::bulk_commit_group();
-        }
-        ++stg_count;
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (rank == 0) ptx::mbar_arrive(&tempty[acc]);
-        else ptx::mbar_arrive_remote(tempty0 + (uint32_t)acc * 8u);
-      }
-      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      acc_phase ^= 1;
     }
     if (lane == 0) ptx::bulk_wait_group<0>();
     __syncwarp();
@@ -864,7 +909,7 @@ mlp_status launch_block_bwd_act(const void* x, const void* wg, const void* wd, c
       return MLP_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms() / 2));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(B_THREADS);
     cfg.dynamicSmemBytes = B_SMEM;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, block_bwd_act_kernel, &cfg) != cudaSuccess || n < 1) {
@@ -879,7 +924,7 @@ mlp_status launch_block_bwd_act(const void* x, const void* wg, const void* wd, c
   if (!encode_tmap_bf16_2d(&tg, wg, hidden, DM, (unsigned long long)hidden * 2, 64, 64))
     return MLP_ERR_CUDA;
   if (!encode_tmap_bf16_2d(&tdy, dy, DM, T, DM * 2, 64, TM)) return MLP_ERR_CUDA;
-  if (!encode_tmap_bf16_2d(&twd, wd, DM, hidden, DM * 2, 64, HC / 2)) return MLP_ERR_CUDA;
+  if (!encode_tmap_bf16_2d(&twd, wd, DM, hidden, DM * 2, 64, BH / 2)) return MLP_ERR_CUDA;
   if (!encode_tmap_out_2d(&ta, a_out, 0, hidden, T, (unsigned long long)hidden * 2, 32, 32))
     return MLP_ERR_CUDA;
   if (!encode_tmap_out_2d(&tdu, du_out, 0, hidden, T, (unsigned long long)hidden * 2, 32, 32))
@@ -888,7 +933,7 @@ mlp_status launch_block_bwd_act(const void* x, const void* wg, const void* wd, c
   p.T = T;
   p.hidden = hidden;
   p.pairs_m = (T + 2 * TM - 1) / (2 * TM);
-  p.tiles_h = hidden / HC;
+  p.tiles_h = hidden / BH;
   p.num_tiles = p.pairs_m * p.tiles_h;
   p.slope = slope;
   p.rstd = rstd;
@@ -897,7 +942,7 @@ mlp_status launch_block_bwd_act(const void* x, const void* wg, const void* wd, c
   if (!p.err) return MLP_ERR_CUDA;
   const int pairs = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
   LaunchScope ls("block_bwd_act", st, T, DM, hidden);
-  launch_k(block_bwd_act_kernel, dim3(2 * pairs), dim3(kThreads), B_SMEM, st, tx, tg, tdy, twd, ta,
+  launch_k(block_bwd_act_kernel, dim3(2 * pairs), dim3(B_THREADS), B_SMEM, st, tx, tg, tdy, twd, ta,
            tdu, p);
   return launch_status();
 }
