@@ -8,6 +8,8 @@ Workloads (synthetic, seeded inputs; see synth.py):
                 images = 46 steps of batch 128 + 1 of 112 (default)
   mlp784_fp32   same network, fp32 SIMT path, one step of batch 128
   mlp_wide      1024-8192-8192-1000 MLP, batch 16,384, bf16 operands, fp32 master weights
+  mlp784_epoch_f16, mlp_wide_f16
+                the same two workloads with fp16 operands (FP16 in, FP32 accumulate)
   block         one RMSNorm -> gate -> LeakyReLU^2 -> down -> residual block, fwd + bwd,
                 65,536 tokens x 512
   stack         11 such blocks over 262,144 tokens, MSE loss, fwd + bwd + momentum SGD
@@ -272,7 +274,8 @@ def timed_e2e_pipelined(wl, slots, steps, sync_barrier):
 
 
 class MLP784Epoch(Workload):
-    """784-256-10, bf16 tensor-core path, one epoch (6,000 images, 47 steps)."""
+    """784-256-10, bf16 (or fp16) tensor-core path, one epoch (6,000 images,
+    47 steps); the fp32 form is one step of 128 on the SIMT path."""
     name = "mlp784_epoch"
     unit = "samples/s"
     dtype = "bf16"
@@ -282,6 +285,9 @@ class MLP784Epoch(Workload):
         if prec_name == "fp32":
             self.name = "mlp784_fp32"
             self.dtype = "f32"
+        elif prec_name == "fp16":
+            self.name = "mlp784_epoch_f16"
+            self.dtype = "f16"
         self.n_images = n_images
         self.batch = batch
         self.n_steps = (n_images + batch - 1) // batch
@@ -300,7 +306,8 @@ class MLP784Epoch(Workload):
         from mlp_step_gb300 import synth
         self.M = M
         dims = [784, 256, 10]
-        prec = M.MLP_PREC_BF16 if self.prec_name == "bf16" else M.MLP_PREC_FP32
+        prec = {"bf16": M.MLP_PREC_BF16, "fp16": M.MLP_PREC_FP16}.get(self.prec_name,
+                                                                      M.MLP_PREC_FP32)
         p0 = synth.mlp_flat_params(dims)
         self.net = M.MLP(dims, prec=prec, max_batch=self.batch, params=torch.from_numpy(p0))
         xb = synth.images_u8(self.n_images, 784)
@@ -383,7 +390,8 @@ class MLP784Epoch(Workload):
                 b = min(self.n_images, a + self.batch)
                 _, p, v, _ = oracle.mlp_train_step(dims, p, v, xb[a:b].astype(np.float64),
                                                    y[a:b], 0.1, 0.9,
-                                                   bf16_points=self.prec_name == "bf16")
+                                                   points={"bf16": 1, "fp16": 2}.get(
+                                                       self.prec_name, 0))
                 done += b - a
                 steps += 1
                 if time.perf_counter() - t0 >= budget_s:
@@ -396,16 +404,22 @@ class MLP784Epoch(Workload):
 
 
 class WideMLP(Workload):
-    """1024-8192-8192-1000, batch 16,384, bf16 operands, fp32 master weights."""
+    """1024-8192-8192-1000, batch 16,384, bf16 (or fp16) operands, fp32 master
+    weights."""
     name = "mlp_wide"
     unit = "samples/s"
     dtype = "bf16"
 
-    def __init__(self, batch=16384):
+    def __init__(self, batch=16384, prec_name="bf16"):
         self.dims = [1024, 8192, 8192, 1000]
         self.batch = batch
+        self.prec_name = prec_name
+        if prec_name == "fp16":
+            self.name = "mlp_wide_f16"
+            self.dtype = "f16"
         self.samples_per_step = self.batch
-        self.config = {"workload": "1024-8192-8192-1000 MLP, ReLU, bf16 weights/activations, "
+        self.config = {"workload": "1024-8192-8192-1000 MLP, ReLU, " + prec_name +
+                                   " weights/activations, "
                                    "fp32 master weights and accumulation, batch 16384, inputs "
                                    "N(0,1), labels uniform 0..999, SGD momentum lr 0.01 m 0.9; "
                                    "one full fwd + bwd + update step" + (
@@ -419,11 +433,12 @@ class WideMLP(Workload):
         from mlp_step_gb300 import synth
         self.M = M
         p0 = synth.mlp_flat_params(self.dims)
-        self.net = M.MLP(self.dims, prec=M.MLP_PREC_BF16, max_batch=self.batch,
-                         params=torch.from_numpy(p0))
+        f16 = self.prec_name == "fp16"
+        self.net = M.MLP(self.dims, prec=M.MLP_PREC_FP16 if f16 else M.MLP_PREC_BF16,
+                         max_batch=self.batch, params=torch.from_numpy(p0))
         X = synth.normal_f32((self.batch, self.dims[0]), synth.STREAM_X)
         y = synth.labels(self.batch, self.dims[-1])
-        self.x_host = torch.from_numpy(X).to(torch.bfloat16).pin_memory()
+        self.x_host = torch.from_numpy(X).to(torch.float16 if f16 else torch.bfloat16).pin_memory()
         self.y_host = torch.from_numpy(y).pin_memory()
         self.x = self.x_host.cuda()
         self.y = self.y_host.cuda()
@@ -700,7 +715,9 @@ class StackStep(Workload):
 WORKLOADS = {
     "mlp784_epoch": lambda: MLP784Epoch("bf16"),
     "mlp784_fp32": lambda: MLP784Epoch("fp32", n_images=128),
+    "mlp784_epoch_f16": lambda: MLP784Epoch("fp16"),
     "mlp_wide": WideMLP,
+    "mlp_wide_f16": lambda: WideMLP(prec_name="fp16"),
     "block": BlockStep,
     "stack": StackStep,
 }
@@ -778,7 +795,10 @@ def fp32_alu_tflops():
     return sms * 128 * 2 * 2.070e9 / 1e12
 
 
-def roofline_entry(rep, peaks, peaks_kind, sustained=False):
+def roofline_entry(rep, peaks, peaks_kind, sustained=False, f16=False):
+    """Roofline of the dominant kernel.  f16: the contraction runs on fp16
+    operands, whose nominal dense rate equals bf16's, so the measured bf16
+    peak is its denominator (times 1.0)."""
     if not rep:
         return None
     # dominant kernel kind = largest total time, aggregated over shapes
@@ -814,7 +834,9 @@ def roofline_entry(rep, peaks, peaks_kind, sustained=False):
             "unit": unit, "frac": round(achieved / peak, 5), "traffic": None,
             "peak_kind": ("derived: SMs x 128 fp32 lanes x 2 flops x 2070 MHz" if bound == "alu" else
                           peaks_kind + (" sustained" if sustained and bound == "tensor" else
-                                        (" burst" if bound == "tensor" else ""))),
+                                        (" burst" if bound == "tensor" else "")) +
+                          (" bf16 x 1.0 (nominal dense fp16 = bf16 rate)"
+                           if bound == "tensor" and f16 else "")),
             "launches_profiled": launches, "avg_launch_ms": round(avg_ms, 6),
             "share_of_kernel_time": round(share, 4),
             "work_per_launch": per_launch}
@@ -881,7 +903,7 @@ def run_ours(args, wl):
 
     peaks, peaks_kind = load_peaks()
     rep = kernel_profile(wl, max(3, min(args.steps, 20)))
-    roof = roofline_entry(rep, peaks, peaks_kind)
+    roof = roofline_entry(rep, peaks, peaks_kind, f16=wl.dtype == "f16")
     if roof is not None:
         roof["traffic"] = recorded_traffic(roof["kernel"], wl.name)
 

@@ -64,10 +64,16 @@ typedef int mlp_status;
 #define MLP_PREC_BF16 1              /* bf16 operands, fp32 accumulation in tensor
                                         memory, fp32 epilogue ([vk] "The Debugging
                                         Lesson Was Numerical"), fp32 master weights  */
+#define MLP_PREC_FP16 2              /* the same tensor-core path with fp16 operands
+                                        (the FP16-in / FP32-accumulate choice of [vk]
+                                        "The Debugging Lesson Was Numerical"): fp16
+                                        input copy, weight shadow, hidden
+                                        activations and gradients fed to the GEMMs */
 
 #define MLP_DTYPE_F32 0
 #define MLP_DTYPE_BF16 1
 #define MLP_DTYPE_U8 2               /* image bytes; the value used is byte / 255    */
+#define MLP_DTYPE_F16 3              /* IEEE binary16                                */
 
 typedef struct mlp_handle mlp_handle;
 
@@ -119,7 +125,8 @@ size_t mlp_param_count(const int* dims, int n_dims);
  * inside the flat buffer.  Returns (size_t)-1 for a bad layer or which. */
 size_t mlp_param_offset(const int* dims, int n_dims, int layer, int which);
 
-/* Elements of the bf16 weight shadow used by MLP_PREC_BF16: each W_l stored
+/* Elements of the 16-bit weight shadow used by MLP_PREC_BF16 (bf16) and
+ * MLP_PREC_FP16 (fp16): each W_l stored
  * [in][out_pad] with out_pad = out rounded up to a multiple of 8 when out <= 16
  * (16-byte rows), else to a multiple of 64 (whole 128-byte lines, which the
  * tensor-core tiles read fastest), layers back to back.  Biases have no shadow
@@ -131,7 +138,9 @@ size_t mlp_workspace_bytes(const int* dims, int n_dims, int max_batch, int prec)
 
 /* Builds a host-side handle over caller-owned device buffers.
  *   params, velocity, grads: fp32[mlp_param_count], flat layout above.
- *   params_bf16: bf16[mlp_shadow_elems] for MLP_PREC_BF16, else NULL.
+ *   params_bf16: the 16-bit weight shadow, 16-byte aligned:
+ *   bf16[mlp_shadow_elems] for MLP_PREC_BF16, fp16[mlp_shadow_elems] for
+ *   MLP_PREC_FP16, NULL for MLP_PREC_FP32.
  *   workspace: ws_bytes >= mlp_workspace_bytes(...), holds saved activations,
  *   dZ/dH buffers and reduction partials between calls.
  *   hidden_act: MLP_ACT_RELU or MLP_ACT_NONE.
@@ -146,12 +155,12 @@ mlp_status mlp_create(const int* dims, int n_dims, int hidden_act, int prec, int
 /* Frees the host-side handle only. */
 void mlp_destroy(mlp_handle* h);
 
-/* Rewrites the bf16 shadow from the fp32 parameters (after the caller changed
- * them).  No-op for MLP_PREC_FP32. */
+/* Rewrites the 16-bit shadow from the fp32 parameters (after the caller
+ * changed them).  No-op for MLP_PREC_FP32. */
 mlp_status mlp_refresh_shadow(mlp_handle* h, void* stream);
 
-/* Forward of `batch` rows of x ([batch][dims[0]], dtype x_dtype: F32, BF16 or
- * U8).  Writes logits fp32 [batch][dims[-1]] and keeps the input copy and the
+/* Forward of `batch` rows of x ([batch][dims[0]], dtype x_dtype: F32, BF16,
+ * F16 or U8; converted to the network's operand type).  Writes logits fp32 [batch][dims[-1]] and keeps the input copy and the
  * hidden activations in the workspace for mlp_backward.
  * ([cap] "The minimum model"; bias and ReLU live in the GEMM epilogue per
  * [cap] "Read the worked reference".)  batch <= max_batch. */
@@ -161,22 +170,23 @@ mlp_status mlp_forward(mlp_handle* h, const void* x, int x_dtype, int batch, flo
 /* Backward of the last mlp_forward, given dlogits = dL/dZ:
  *   dW_l = In_l^T dY_l,  db_l = sum_rows dY_l,  dY_{l-1} = (dY_l W_l^T) * (H_l > 0)
  * ([cap] "Work through the backward pass", "Check your mapping").
- * dlogits: [batch][ld_dlogits], fp32 for MLP_PREC_FP32, bf16 for MLP_PREC_BF16
- * (for bf16, ld_dlogits * 2 must be a multiple of 16).
+ * dlogits: [batch][ld_dlogits], fp32 for MLP_PREC_FP32, bf16 for MLP_PREC_BF16,
+ * fp16 for MLP_PREC_FP16 (for 16-bit, ld_dlogits * 2 must be a multiple of 16).
  * Overwrites the handle's grads (no accumulation).  dx (nullable): [batch][dims[0]]
- * fp32 (FP32) or bf16 (BF16), receives dX = dY_0 W_1^T. */
+ * in the same type as dlogits, receives dX = dY_0 W_1^T. */
 mlp_status mlp_backward(mlp_handle* h, const void* dlogits, int ld_dlogits, int batch, void* dx,
                         void* stream);
 
-/* Momentum SGD over the handle's flat buffers, then (BF16) the shadow refresh,
- * in one kernel. */
+/* Momentum SGD over the handle's flat buffers, then (BF16, FP16) the shadow
+ * refresh, in one kernel. */
 mlp_status mlp_sgd_step(mlp_handle* h, float lr, float momentum, void* stream);
 
 /* One full training step on the stream: forward, softmax cross entropy
  * (mean over the batch), backward, momentum SGD.  labels int32[batch] in
  * [0, dims[-1]).  loss_out (nullable): device fp32 scalar.  argmax_out
  * (nullable): device int32[batch] predictions of this step's forward.
- * For MLP_PREC_BF16 networks with batch <= 128, at most 32 classes and small
+ * For MLP_PREC_BF16 and MLP_PREC_FP16 networks with batch <= 128, at most 32
+ * classes and small
  * layers (every GEMM of the step fits one round of CTAs and every weight
  * update rides in its gradient GEMM) the step is ONE cooperative kernel
  * launch whose phases are separated by grid barriers; results are the same
@@ -211,7 +221,7 @@ mlp_status mlp_train_epoch(mlp_handle* h, const void* x, int x_dtype, const int3
  *   dZ_ic = (exp(z_c - m) / s - [c == y_i]) / batch.
  * loss_out: device fp32 scalar = mean_i loss_i (fixed-order reduction, so the
  * result is bitwise reproducible).  logits fp32 [batch][ld_logits];
- * dlogits (nullable) [batch][ld_dlogits] fp32 or bf16 (dlogits_dtype); when
+ * dlogits (nullable) [batch][ld_dlogits] fp32, bf16 or fp16 (dlogits_dtype); when
  * ld_dlogits > classes the padding columns are written as zero.  argmax_out
  * (nullable) int32[batch]: lowest index among equal maxima.
  * workspace: softmax_xent_workspace_bytes(batch, classes) bytes of scratch.
@@ -260,12 +270,13 @@ mlp_status sgd_momentum_step(float* w, const float* g, float* v, void* w_bf16, s
  *   b_trans = 0: B stored [K][ldb];  b_trans = 1: B stored [N][ldb] (B = S^T).
  * ([cap] "Work through the backward pass": the weight and input gradients are
  * multiplies with one transposed input; no transpose copy is made.)
- * in_dtype F32 runs the fp32 SIMT kernel; BF16 runs the tcgen05 kernel (bf16
- * operands from TMA, fp32 accumulation in tensor memory).
+ * in_dtype F32 runs the fp32 SIMT kernel; BF16 and F16 run the tcgen05 kernel
+ * (bf16 or fp16 operands from TMA, fp32 accumulation in tensor memory).
  * Epilogue, in fp32, in this order ([cap] "Read the worked reference"; [vk]):
  *   + bias[n] (nullable, fp32);  act (NONE or RELU);
  *   mask (nullable, dtype = in_dtype, [M][ldm]): keep where mask > 0, else 0;
- *   store as c_dtype (F32 or BF16) into C [M][ldc].
+ *   store as c_dtype into C [M][ldc]: F32, or the 16-bit type of the operands
+ *   (BF16 for in_dtype F32 or BF16, F16 for in_dtype F16).
  * K = 0 gives the epilogue of a zero sum. */
 mlp_status mlp_gemm(int M, int N, int K, const void* A, int lda, int a_trans, const void* B,
                     int ldb, int b_trans, int in_dtype, const float* bias, int act,
@@ -273,7 +284,7 @@ mlp_status mlp_gemm(int M, int N, int K, const void* A, int lda, int a_trans, co
 
 /* Column reduction: out[c] = sum_r X[r][c] in fp32 (bias gradient, [cap]
  * "Check your mapping": one bias per unit, summed over the batch).  X dtype
- * F32 or BF16, [rows][ld].  Fixed-order two-pass reduction (bitwise
+ * F32, BF16 or F16, [rows][ld].  Fixed-order two-pass reduction (bitwise
  * reproducible); workspace: mlp_colsum_workspace_bytes(rows, cols). */
 size_t mlp_colsum_workspace_bytes(int rows, int cols);
 mlp_status mlp_colsum(const void* X, int dtype, int rows, int cols, int ld, float* out,

@@ -17,7 +17,8 @@ import os
 __all__ = [
     "MlpError", "load", "lib_path",
     "MLP_ACT_NONE", "MLP_ACT_RELU", "MLP_ACT_LEAKY_RELU_SQ",
-    "MLP_PREC_FP32", "MLP_PREC_BF16", "MLP_DTYPE_F32", "MLP_DTYPE_BF16", "MLP_DTYPE_U8",
+    "MLP_PREC_FP32", "MLP_PREC_BF16", "MLP_PREC_FP16", "MLP_DTYPE_F32", "MLP_DTYPE_BF16",
+    "MLP_DTYPE_U8", "MLP_DTYPE_F16",
 ]
 
 MLP_OK = 0
@@ -33,9 +34,11 @@ MLP_ACT_RELU = 1
 MLP_ACT_LEAKY_RELU_SQ = 2
 MLP_PREC_FP32 = 0
 MLP_PREC_BF16 = 1
+MLP_PREC_FP16 = 2
 MLP_DTYPE_F32 = 0
 MLP_DTYPE_BF16 = 1
 MLP_DTYPE_U8 = 2
+MLP_DTYPE_F16 = 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_HERE, "libmlp_step.so")
@@ -143,6 +146,8 @@ def _dtype_code(t):
         return MLP_DTYPE_BF16
     if t.dtype == torch.uint8:
         return MLP_DTYPE_U8
+    if t.dtype == torch.float16:
+        return MLP_DTYPE_F16
     raise TypeError("unsupported dtype %s" % t.dtype)
 
 
@@ -208,7 +213,8 @@ def mlp_workspace_bytes(dims, max_batch: int, prec: int) -> int:
 
 class MLP:
     """Owner of the device buffers of one MLP (flat params, velocity, grads,
-    bf16 shadow, workspace) and of the library handle over them."""
+    the 16-bit weight shadow of the tensor-core precisions, workspace) and of
+    the library handle over them."""
 
     def __init__(self, dims, prec=MLP_PREC_BF16, max_batch=128, params=None,
                  hidden_act=MLP_ACT_RELU, device="cuda"):
@@ -223,9 +229,10 @@ class MLP:
         self.velocity = torch.zeros_like(self.params)
         self.grads = torch.zeros_like(self.params)
         self.shadow = None
-        if prec == MLP_PREC_BF16:
-            self.shadow = torch.zeros(mlp_shadow_elems(self.dims), dtype=torch.bfloat16,
-                                      device=device)
+        if prec in (MLP_PREC_BF16, MLP_PREC_FP16):
+            self.shadow = torch.zeros(mlp_shadow_elems(self.dims),
+                                      dtype=torch.bfloat16 if prec == MLP_PREC_BF16
+                                      else torch.float16, device=device)
         wsb = mlp_workspace_bytes(self.dims, max_batch, prec)
         self.workspace = torch.empty(wsb, dtype=torch.uint8, device=device)
         d, nd = _dims(self.dims)

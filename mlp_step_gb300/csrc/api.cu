@@ -126,8 +126,11 @@ inline int f32_pitch(int n) { return n <= 16 ? n : (n + 31) / 32 * 32; }
 
 mlp_status check_gemm(const GemmArgs& g, int in_dtype, int c_dtype) {
   if (g.M < 0 || g.N < 0 || g.K < 0) return MLP_ERR_INVALID_ARG;
-  if (in_dtype != MLP_DTYPE_F32 && in_dtype != MLP_DTYPE_BF16) return MLP_ERR_INVALID_ARG;
-  if (c_dtype != MLP_DTYPE_F32 && c_dtype != MLP_DTYPE_BF16) return MLP_ERR_INVALID_ARG;
+  if (in_dtype != MLP_DTYPE_F32 && in_dtype != MLP_DTYPE_BF16 && in_dtype != MLP_DTYPE_F16)
+    return MLP_ERR_INVALID_ARG;
+  // 16-bit outputs take the operands' 16-bit type (bf16 for fp32 operands)
+  const int c16 = in_dtype == MLP_DTYPE_F16 ? MLP_DTYPE_F16 : MLP_DTYPE_BF16;
+  if (c_dtype != MLP_DTYPE_F32 && c_dtype != c16) return MLP_ERR_INVALID_ARG;
   if (g.act != MLP_ACT_NONE && g.act != MLP_ACT_RELU) return MLP_ERR_INVALID_ARG;
   if (g.M == 0 || g.N == 0) return MLP_OK;
   if (!g.C) return MLP_ERR_INVALID_ARG;
@@ -141,7 +144,7 @@ mlp_status check_gemm(const GemmArgs& g, int in_dtype, int c_dtype) {
   if (!aligned16(g.C) || (g.K > 0 && (!aligned16(g.A) || !aligned16(g.B))) ||
       (g.mask && !aligned16(g.mask)) || (g.bias && !aligned16(g.bias)))
     return MLP_ERR_MISALIGNED;
-  if (in_dtype == MLP_DTYPE_BF16 && g.K > 0) {
+  if (in_dtype != MLP_DTYPE_F32 && g.K > 0) {
     // TMA: rows must start on 16-byte boundaries
     if (((long long)g.lda * 2) % 16 != 0 || ((long long)g.ldb * 2) % 16 != 0)
       return MLP_ERR_MISALIGNED;
@@ -211,10 +214,11 @@ mlp_status mlp_gemm(int M, int N, int K, const void* A, int lda, int a_trans, co
                     int ldb, int b_trans, int in_dtype, const float* bias, int act,
                     const void* mask, int ldm, void* C, int ldc, int c_dtype, void* stream) {
   GemmArgs g{M, N, K, A, lda, a_trans ? 1 : 0, B, ldb, b_trans ? 1 : 0, bias, act, mask, ldm,
-             C, ldc, c_dtype == MLP_DTYPE_BF16 ? 1 : 0};
+             C, ldc, c_dtype != MLP_DTYPE_F32 ? 1 : 0};
+  g.f16 = in_dtype == MLP_DTYPE_F16 ? 1 : 0;
   MLP_CHECK(check_gemm(g, in_dtype, c_dtype));
   if (M == 0 || N == 0) return MLP_OK;
-  return run_gemm(g, in_dtype == MLP_DTYPE_BF16, S(stream));
+  return run_gemm(g, in_dtype != MLP_DTYPE_F32, S(stream));
 }
 
 size_t mlp_colsum_workspace_bytes(int rows, int cols) {
@@ -225,14 +229,15 @@ size_t mlp_colsum_workspace_bytes(int rows, int cols) {
 mlp_status mlp_colsum(const void* X, int dtype, int rows, int cols, int ld, float* out,
                       void* workspace, size_t ws_bytes, void* stream) {
   if (rows < 0 || cols < 0) return MLP_ERR_INVALID_ARG;
-  if (dtype != MLP_DTYPE_F32 && dtype != MLP_DTYPE_BF16) return MLP_ERR_INVALID_ARG;
+  if (dtype != MLP_DTYPE_F32 && dtype != MLP_DTYPE_BF16 && dtype != MLP_DTYPE_F16)
+    return MLP_ERR_INVALID_ARG;
   if (cols == 0) return MLP_OK;
   if (!out || (rows > 0 && !X) || ld < cols) return MLP_ERR_INVALID_ARG;
   const size_t need = mlp_colsum_workspace_bytes(rows, cols);
   if (need > 0 && (!workspace || ws_bytes < need)) return MLP_ERR_INVALID_ARG;
   if ((X && !aligned16(X)) || !aligned16(out) || (workspace && !aligned16(workspace)))
     return MLP_ERR_MISALIGNED;
-  return launch_colsum(X, dtype == MLP_DTYPE_BF16, rows, cols, ld, out, workspace, S(stream));
+  return launch_colsum(X, dtype, rows, cols, ld, out, workspace, S(stream));
 }
 
 size_t softmax_xent_workspace_bytes(int batch, int classes) {
@@ -248,7 +253,8 @@ mlp_status softmax_xent_fwd_bwd(const float* logits, int ld_logits, const int32_
   if (batch == 0) return MLP_OK;
   if (!logits || !labels || ld_logits < classes) return MLP_ERR_INVALID_ARG;
   if (dlogits && (ld_dlogits < classes ||
-                  (dlogits_dtype != MLP_DTYPE_F32 && dlogits_dtype != MLP_DTYPE_BF16)))
+                  (dlogits_dtype != MLP_DTYPE_F32 && dlogits_dtype != MLP_DTYPE_BF16 &&
+                   dlogits_dtype != MLP_DTYPE_F16)))
     return MLP_ERR_INVALID_ARG;
   const size_t need = softmax_xent_workspace_bytes(batch, classes);
   if (need > 0 && (!workspace || ws_bytes < need)) return MLP_ERR_INVALID_ARG;
@@ -257,7 +263,7 @@ mlp_status softmax_xent_fwd_bwd(const float* logits, int ld_logits, const int32_
       (workspace && !aligned16(workspace)))
     return MLP_ERR_MISALIGNED;
   return launch_xent(logits, ld_logits, labels, batch, classes, loss_out, dlogits,
-                     dlogits_dtype == MLP_DTYPE_BF16, ld_dlogits, argmax_out, workspace,
+                     dlogits ? dlogits_dtype : MLP_DTYPE_F32, ld_dlogits, argmax_out, workspace,
                      S(stream));
 }
 
@@ -273,8 +279,8 @@ mlp_status sgd_momentum_step(float* w, const float* g, float* v, void* w_bf16, s
   segs.shadow_off[0] = w_bf16 ? 0 : -1;
   segs.cols[0] = 1;
   segs.cols_pad[0] = 1;
-  return launch_sgd(w, g, v, static_cast<__nv_bfloat16*>(w_bf16), (long long)n, lr, momentum,
-                    segs, S(stream));
+  return launch_sgd(w, g, v, w_bf16, MLP_DTYPE_BF16, (long long)n, lr, momentum, segs,
+                    S(stream));
 }
 
 size_t mse_workspace_bytes(size_t n) { return n ? mse_ws_bytes((long long)n) : 0; }
@@ -302,7 +308,7 @@ struct mlp_handle {
   float* params = nullptr;
   float* velocity = nullptr;
   float* grads = nullptr;
-  __nv_bfloat16* shadow = nullptr;
+  __nv_bfloat16* shadow = nullptr;  // 16-bit weight shadow (bf16 bits, or fp16 for MLP_PREC_FP16)
   long long n_params = 0;
   std::vector<long long> w_off, b_off, shadow_off;
   std::vector<int> out_pad;        // shadow row pitch per layer
@@ -313,7 +319,7 @@ struct mlp_handle {
   // the flat layout of W followed by b.
   std::vector<int> act_ld;         // act_ld[l]: pitch of layer l's input buffer
   void* x_copy = nullptr;          // [max_batch][act_ld[0]]
-  void* x_copy_alt = nullptr;      // second input buffer of multi-step programs (bf16 only)
+  void* x_copy_alt = nullptr;      // second input buffer of multi-step programs (16-bit only)
   void* simt_ws = nullptr;         // split-K scratch of the fp32 GEMMs (fp32 only)
   std::vector<void*> acts;         // acts[l] = H_{l+1}, l = 0..L-2
   float* logits = nullptr;         // [max_batch][C]
@@ -332,7 +338,17 @@ struct mlp_handle {
 
 namespace {
 
-int esz(int prec) { return prec == MLP_PREC_BF16 ? 2 : 4; }
+int esz(int prec) { return prec == MLP_PREC_FP32 ? 4 : 2; }
+
+// The tensor-core path (bf16 or fp16 operands)?
+bool tc_prec(int prec) { return prec == MLP_PREC_BF16 || prec == MLP_PREC_FP16; }
+
+// MLP_DTYPE_* code of the handle's operand buffers (input copy, hidden
+// activations, dZ / dH, weight shadow).
+int buf_dtype(const mlp_handle* h) {
+  return h->prec == MLP_PREC_FP16 ? MLP_DTYPE_F16
+                                  : (h->prec == MLP_PREC_BF16 ? MLP_DTYPE_BF16 : MLP_DTYPE_F32);
+}
 
 bool dims_ok(const int* dims, int n_dims) {
   if (!dims || n_dims < 2 || n_dims > 9) return false;
@@ -351,7 +367,7 @@ Plan plan(const int* dims, int n_dims, int max_batch, int prec) {
   const size_t B = (size_t)max_batch;
   const int e = esz(prec);
   p.x = align256(B * round64(dims[0] + 1) * e);
-  p.x_alt = prec == MLP_PREC_BF16 ? p.x : 0;
+  p.x_alt = tc_prec(prec) ? p.x : 0;
   p.acts_total = 0;
   int maxh = 8;
   for (int l = 1; l < L; ++l) {
@@ -365,7 +381,7 @@ Plan plan(const int* dims, int n_dims, int max_batch, int prec) {
   p.loss = 256;
   size_t red = xent_workspace_bytes(max_batch);
   p.red = align256(red > 0 ? red : 256);
-  p.simt = prec == MLP_PREC_BF16 ? 0 : align256(gemm_simt_scratch_bytes());
+  p.simt = tc_prec(prec) ? 0 : align256(gemm_simt_scratch_bytes());
   p.total = p.x + p.x_alt + p.acts_total + p.logits + p.dlogits + 2 * p.dh + p.loss + p.red +
             p.simt;
   return p;
@@ -391,7 +407,7 @@ mlp_status ensure_ones(mlp_handle* h, cudaStream_t st) {
     oc.col[oc.n] = h->dims[0];
     ++oc.n;
   }
-  MLP_CHECK(launch_ones_cols(oc, h->max_batch, h->prec == MLP_PREC_BF16, st));
+  MLP_CHECK(launch_ones_cols(oc, h->max_batch, buf_dtype(h), st));
   // the split-K counters of the fp32 GEMMs start at zero (each launch leaves
   // them so)
   if (h->simt_ws && cudaMemsetAsync(h->simt_ws, 0, 4096, st) != cudaSuccess) return MLP_ERR_CUDA;
@@ -401,7 +417,7 @@ mlp_status ensure_ones(mlp_handle* h, cudaStream_t st) {
 
 // fp32 GEMMs of the handle get its split-K scratch
 GemmArgs& with_simt_ws(const mlp_handle* h, GemmArgs& g) {
-  if (h->prec != MLP_PREC_BF16 && h->simt_ws) {
+  if (!tc_prec(h->prec) && h->simt_ws) {
     g.ws = h->simt_ws;
     g.ws_bytes = gemm_simt_scratch_bytes();
   }
@@ -411,9 +427,10 @@ GemmArgs& with_simt_ws(const mlp_handle* h, GemmArgs& g) {
 // Hidden layers 0 .. L-2 of the forward (bias + activation in the epilogue);
 // in a step program, layer l is phase 1 + l.
 mlp_status forward_hidden(mlp_handle* h, int batch, cudaStream_t st, StepSpec* rec = nullptr) {
-  const bool bf = h->prec == MLP_PREC_BF16;
+  const bool bf = tc_prec(h->prec);
   for (int l = 0; l + 1 < h->L; ++l) {
     GemmArgs g{};
+    g.f16 = h->prec == MLP_PREC_FP16 ? 1 : 0;
     g.M = batch;
     g.N = h->dims[l + 1];
     g.K = h->dims[l];
@@ -440,9 +457,10 @@ mlp_status forward_hidden(mlp_handle* h, int batch, cudaStream_t st, StepSpec* r
 
 // The output layer's GEMM operands (logits = In W_L + b_L).
 GemmArgs logits_gemm(mlp_handle* h, int batch, float* logits, int ld_logits) {
-  const bool bf = h->prec == MLP_PREC_BF16;
+  const bool bf = tc_prec(h->prec);
   const int l = h->L - 1;
   GemmArgs g{};
+  g.f16 = h->prec == MLP_PREC_FP16 ? 1 : 0;
   g.M = batch;
   g.N = h->dims[l + 1];
   g.K = h->dims[l];
@@ -466,10 +484,9 @@ GemmArgs logits_gemm(mlp_handle* h, int batch, float* logits, int ld_logits) {
 mlp_status load_input(mlp_handle* h, const void* x, int x_dtype, int batch, cudaStream_t st) {
   MLP_CHECK(ensure_ones(h, st));
   // X goes into the workspace copy with the ones column, in the path's type
-  const bool bf = h->prec == MLP_PREC_BF16;
   const int d0 = h->dims[0];
   // rows of d0 values into rows of pitch act_ld[0]
-  return launch_cast_rows(x, x_dtype, h->x_copy, bf ? 1 : 0, batch, d0, h->act_ld[0], st);
+  return launch_cast_rows(x, x_dtype, h->x_copy, buf_dtype(h), batch, d0, h->act_ld[0], st);
 }
 
 // Backward from dY = dlogits.  With fuse_sgd, each layer's weight-gradient
@@ -482,7 +499,8 @@ mlp_status load_input(mlp_handle* h, const void* x, int x_dtype, int batch, cuda
 mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int batch, void* dx,
                          bool fuse_sgd, float lr, float mom, cudaStream_t st,
                          StepSpec* rec = nullptr) {
-  const bool bf = h->prec == MLP_PREC_BF16;
+  const bool bf = tc_prec(h->prec);
+  const int f16 = h->prec == MLP_PREC_FP16 ? 1 : 0;
   const void* dY = dlogits;
   int ld_dy = ld_dlogits;
   for (int l = h->L - 1; l >= 0; --l) {
@@ -492,6 +510,7 @@ mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int
     // dIn = (dY W_l^T) * (H_l > 0)   (B = W_l read transposed); reads the
     // layer's weights before any update
     GemmArgs gd{};
+    gd.f16 = f16;
     const bool want_din = l > 0 || dx;
     if (want_din) {
       gd.M = batch; gd.N = fi; gd.K = fo;
@@ -515,6 +534,7 @@ mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int
     // [dW_l; db_l] = [In_l | 1]^T dY_l   (A = In_l read transposed), written
     // over the layer's flat slice of grads
     GemmArgs gw{};
+    gw.f16 = f16;
     gw.M = fi + 1; gw.N = fo; gw.K = batch;
     gw.A = in; gw.lda = ld_in; gw.a_trans = 1;
     gw.B = dY; gw.ldb = ld_dy; gw.b_trans = 0;
@@ -550,7 +570,7 @@ mlp_status backward_impl(mlp_handle* h, const void* dlogits, int ld_dlogits, int
       seg.cols_pad[1] = 1;
       MLP_CHECK(launch_sgd(h->params + h->w_off[l], h->grads + h->w_off[l],
                            h->velocity + h->w_off[l],
-                           h->shadow ? h->shadow + h->shadow_off[l] : nullptr,
+                           h->shadow ? h->shadow + h->shadow_off[l] : nullptr, buf_dtype(h),
                            (long long)(fi + 1) * fo, lr, mom, seg, st));
     }
     if (l > 0) {
@@ -571,7 +591,8 @@ bool build_step_spec(mlp_handle* h, const void* x, int x_dtype, const int32_t* l
                      float lr, float momentum, float* loss, int32_t* argmax_out, cudaStream_t st,
                      StepSpec* spec) {
   const int C = h->dims[h->L];
-  if (h->prec != MLP_PREC_BF16 || batch > 128 || C > 32) return false;
+  if (!tc_prec(h->prec) || batch > 128 || C > 32) return false;
+  spec->f16 = h->prec == MLP_PREC_FP16 ? 1 : 0;
   spec->cast_src = x;
   spec->cast_dtype = x_dtype;
   spec->cast_dst = h->x_copy;
@@ -595,7 +616,7 @@ mlp_status train_step_impl(mlp_handle* h, const void* x, int x_dtype, const int3
                            int batch, float lr, float momentum, float* loss_out,
                            int32_t* argmax_out, cudaStream_t st) {
   const int C = h->dims[h->L];
-  const bool bf = h->prec == MLP_PREC_BF16;
+  const bool bf = tc_prec(h->prec);
   float* loss = loss_out ? loss_out : h->loss;
   {
     // the whole step as one cooperative launch where it fits
@@ -621,8 +642,8 @@ mlp_status train_step_impl(mlp_handle* h, const void* x, int x_dtype, const int3
     MLP_CHECK(run_gemm(gz, true, st));
   } else {
     MLP_CHECK(run_gemm(with_simt_ws(h, gz), bf, st));
-    MLP_CHECK(launch_xent(h->logits, h->ldl, labels, batch, C, loss, h->dlogits, bf, h->ldz,
-                          argmax_out, h->red, st));
+    MLP_CHECK(launch_xent(h->logits, h->ldl, labels, batch, C, loss, h->dlogits, buf_dtype(h),
+                          h->ldz, argmax_out, h->red, st));
   }
   h->have_forward = true;
   if (bf) return backward_impl(h, h->dlogits, h->ldz, batch, nullptr, true, lr, momentum, st);
@@ -668,10 +689,11 @@ mlp_status mlp_create(const int* dims, int n_dims, int hidden_act, int prec, int
   if (!out) return MLP_ERR_INVALID_ARG;
   *out = nullptr;
   if (!dims_ok(dims, n_dims) || max_batch <= 0) return MLP_ERR_INVALID_ARG;
-  if (prec != MLP_PREC_FP32 && prec != MLP_PREC_BF16) return MLP_ERR_INVALID_ARG;
+  if (prec != MLP_PREC_FP32 && prec != MLP_PREC_BF16 && prec != MLP_PREC_FP16)
+    return MLP_ERR_INVALID_ARG;
   if (hidden_act != MLP_ACT_RELU && hidden_act != MLP_ACT_NONE) return MLP_ERR_INVALID_ARG;
   if (!params || !velocity || !grads || !workspace) return MLP_ERR_INVALID_ARG;
-  if (prec == MLP_PREC_BF16 && !params_bf16) return MLP_ERR_INVALID_ARG;
+  if (tc_prec(prec) && !params_bf16) return MLP_ERR_INVALID_ARG;
   const Plan pl = plan(dims, n_dims, max_batch, prec);
   if (ws_bytes < pl.total) return MLP_ERR_INVALID_ARG;
   if (!aligned16(params) || !aligned16(velocity) || !aligned16(grads) || !aligned16(workspace) ||
@@ -688,7 +710,7 @@ mlp_status mlp_create(const int* dims, int n_dims, int hidden_act, int prec, int
   h->params = params;
   h->velocity = velocity;
   h->grads = grads;
-  h->shadow = prec == MLP_PREC_BF16 ? static_cast<__nv_bfloat16*>(params_bf16) : nullptr;
+  h->shadow = tc_prec(prec) ? static_cast<__nv_bfloat16*>(params_bf16) : nullptr;
   h->n_params = (long long)mlp_param_count(dims, n_dims);
   long long off = 0, soff = 0;
   for (int l = 0; l < h->L; ++l) {
@@ -753,13 +775,14 @@ void mlp_destroy(mlp_handle* h) { delete h; }
 mlp_status mlp_refresh_shadow(mlp_handle* h, void* stream) {
   if (!h) return MLP_ERR_INVALID_ARG;
   if (!h->shadow) return MLP_OK;
-  return launch_shadow(h->params, h->shadow, h->n_params, h->segs, S(stream));
+  return launch_shadow(h->params, h->shadow, buf_dtype(h), h->n_params, h->segs, S(stream));
 }
 
 mlp_status mlp_forward(mlp_handle* h, const void* x, int x_dtype, int batch, float* logits,
                        void* stream) {
   if (!h || batch < 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
-  if (x_dtype != MLP_DTYPE_F32 && x_dtype != MLP_DTYPE_BF16 && x_dtype != MLP_DTYPE_U8)
+  if (x_dtype != MLP_DTYPE_F32 && x_dtype != MLP_DTYPE_BF16 && x_dtype != MLP_DTYPE_U8 &&
+      x_dtype != MLP_DTYPE_F16)
     return MLP_ERR_INVALID_ARG;
   if (batch == 0) return MLP_OK;
   if (!x || !logits) return MLP_ERR_INVALID_ARG;
@@ -768,7 +791,7 @@ mlp_status mlp_forward(mlp_handle* h, const void* x, int x_dtype, int batch, flo
   MLP_CHECK(load_input(h, x, x_dtype, batch, st));
   MLP_CHECK(forward_hidden(h, batch, st));
   GemmArgs gl = logits_gemm(h, batch, logits, h->dims[h->L]);
-  MLP_CHECK(run_gemm(with_simt_ws(h, gl), h->prec == MLP_PREC_BF16, st));
+  MLP_CHECK(run_gemm(with_simt_ws(h, gl), tc_prec(h->prec), st));
   h->have_forward = true;
   return MLP_OK;
 }
@@ -779,22 +802,23 @@ mlp_status mlp_backward(mlp_handle* h, const void* dlogits, int ld_dlogits, int 
   if (batch == 0) return MLP_OK;
   if (!dlogits || !h->have_forward || ld_dlogits < h->dims[h->L]) return MLP_ERR_INVALID_ARG;
   if (!aligned16(dlogits) || (dx && !aligned16(dx))) return MLP_ERR_MISALIGNED;
-  const bool bf = h->prec == MLP_PREC_BF16;
+  const bool bf = tc_prec(h->prec);
   if (bf && (ld_dlogits * 2) % 16 != 0) return MLP_ERR_MISALIGNED;
   return backward_impl(h, dlogits, ld_dlogits, batch, dx, false, 0.f, 0.f, S(stream));
 }
 
 mlp_status mlp_sgd_step(mlp_handle* h, float lr, float momentum, void* stream) {
   if (!h) return MLP_ERR_INVALID_ARG;
-  return launch_sgd(h->params, h->grads, h->velocity, h->shadow, h->n_params, lr, momentum,
-                    h->segs, S(stream));
+  return launch_sgd(h->params, h->grads, h->velocity, h->shadow, buf_dtype(h), h->n_params, lr,
+                    momentum, h->segs, S(stream));
 }
 
 mlp_status mlp_train_step(mlp_handle* h, const void* x, int x_dtype, const int32_t* labels,
                           int batch, float lr, float momentum, float* loss_out,
                           int32_t* argmax_out, void* stream) {
   if (!h || batch < 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
-  if (x_dtype != MLP_DTYPE_F32 && x_dtype != MLP_DTYPE_BF16 && x_dtype != MLP_DTYPE_U8)
+  if (x_dtype != MLP_DTYPE_F32 && x_dtype != MLP_DTYPE_BF16 && x_dtype != MLP_DTYPE_U8 &&
+      x_dtype != MLP_DTYPE_F16)
     return MLP_ERR_INVALID_ARG;
   if (batch == 0) return MLP_OK;
   if (!x || !labels) return MLP_ERR_INVALID_ARG;
@@ -809,11 +833,12 @@ mlp_status mlp_train_epoch(mlp_handle* h, const void* x, int x_dtype, const int3
                            int n_samples, int batch, float lr, float momentum, float* losses_out,
                            int32_t* argmax_out, void* stream) {
   if (!h || n_samples < 0 || batch <= 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
-  if (x_dtype != MLP_DTYPE_F32 && x_dtype != MLP_DTYPE_BF16 && x_dtype != MLP_DTYPE_U8)
+  if (x_dtype != MLP_DTYPE_F32 && x_dtype != MLP_DTYPE_BF16 && x_dtype != MLP_DTYPE_U8 &&
+      x_dtype != MLP_DTYPE_F16)
     return MLP_ERR_INVALID_ARG;
   if (n_samples == 0) return MLP_OK;
   if (!x || !labels) return MLP_ERR_INVALID_ARG;
-  const int xsz = x_dtype == MLP_DTYPE_U8 ? 1 : (x_dtype == MLP_DTYPE_BF16 ? 2 : 4);
+  const int xsz = x_dtype == MLP_DTYPE_U8 ? 1 : (x_dtype == MLP_DTYPE_F32 ? 4 : 2);
   const long long x_step = (long long)batch * h->dims[0] * xsz;
   // every step's input rows, labels and predictions start on 16 bytes
   if (!aligned16(x) || !aligned16(labels) || (argmax_out && !aligned16(argmax_out)) ||

@@ -185,7 +185,7 @@ mlp_status mlp_stack_train_step(int n_blocks, int T, int d, int hidden, float ep
   segs.shadow_off[0] = 0;
   segs.cols[0] = 1;
   segs.cols_pad[0] = 1;
-  return launch_sgd(params, grads, velocity, static_cast<__nv_bfloat16*>(params_bf16),
+  return launch_sgd(params, grads, velocity, params_bf16, MLP_DTYPE_BF16,
                     (long long)(per * n_blocks), lr, momentum, segs, st);
 }
 

@@ -51,7 +51,8 @@ mlp_status softmax_xent_fwd_bwd_noalloc(const float* logits, int ld_logits,
   if (batch > kMaxPartials * 8) return MLP_ERR_UNSUPPORTED_SHAPE;
   if (!logits || !labels || ld_logits < classes) return MLP_ERR_INVALID_ARG;
   if (dlogits && (ld_dlogits < classes ||
-                  (dlogits_dtype != MLP_DTYPE_F32 && dlogits_dtype != MLP_DTYPE_BF16)))
+                  (dlogits_dtype != MLP_DTYPE_F32 && dlogits_dtype != MLP_DTYPE_BF16 &&
+                   dlogits_dtype != MLP_DTYPE_F16)))
     return MLP_ERR_INVALID_ARG;
   if (!mlp::aligned16(logits) || !mlp::aligned16(labels) ||
       (dlogits && !mlp::aligned16(dlogits)) || (argmax_out && !mlp::aligned16(argmax_out)) ||
@@ -63,7 +64,8 @@ mlp_status softmax_xent_fwd_bwd_noalloc(const float* logits, int ld_logits,
   // Every partial the mean reads is written by this call first, so nothing
   // has to be cleared between calls.
   return mlp::launch_xent(logits, ld_logits, labels, batch, classes, loss_out, dlogits,
-                          dlogits_dtype == MLP_DTYPE_BF16, ld_dlogits, argmax_out, scratch,
+                          dlogits ? dlogits_dtype : MLP_DTYPE_F32, ld_dlogits, argmax_out,
+                          scratch,
                           static_cast<cudaStream_t>(stream));
 }
 

@@ -1,5 +1,5 @@
 // Shared definitions of the CUDA library: status codes, the device error word,
-// bf16 helpers and launch checks.  Nothing here is used by the oracle.
+// bf16 / fp16 helpers and launch checks.  Nothing here is used by the oracle.
 #pragma once
 
 #include <cstdint>
@@ -7,6 +7,7 @@
 #include <utility>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "../../include/mlp_step.h"
 
@@ -38,6 +39,42 @@ __device__ __forceinline__ __nv_bfloat16 f32_to_bf16(float v) { return __float2b
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 p = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// The tensor-core path's 16-bit operand format: H16 = 0 for bf16, 1 for fp16
+// (the same storage size and the same sign / zero encoding, so 16-bit
+// buffers travel as raw bits and ReLU masks read either format).
+template <int H16>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
+  if constexpr (H16) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
+}
+
+template <int H16>
+__device__ __forceinline__ uint16_t f32_to_16(float v) {
+  if constexpr (H16) return __half_as_ushort(__float2half_rn(v));
+  else return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+// Runtime-format forms for the bandwidth-bound kernels.  fmt: MLP_DTYPE_BF16
+// or MLP_DTYPE_F16.
+__device__ __forceinline__ uint32_t pack16x2_fmt(float lo, float hi, int fmt) {
+  return fmt == MLP_DTYPE_F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
+__device__ __forceinline__ uint16_t f32_to_16_fmt(float v, int fmt) {
+  return fmt == MLP_DTYPE_F16 ? __half_as_ushort(__float2half_rn(v))
+                              : __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ float f16bits_to_f32(uint16_t b, int fmt) {
+  return fmt == MLP_DTYPE_F16 ? __half2float(__ushort_as_half(b))
+                              : __bfloat162float(__ushort_as_bfloat16(b));
 }
 
 // Programmatic dependent launch: kernels launched through launch_k may start

@@ -33,22 +33,23 @@ __device__ __forceinline__ long long shadow_index(const SgdSegments& s, int k, l
 }
 
 __device__ __forceinline__ void sgd_scalar(float* w, const float* g, float* v,
-                                           __nv_bfloat16* wb, const SgdSegments& s, long long i,
-                                           float lr, float mom) {
+                                           uint16_t* wb, int wb_fmt, const SgdSegments& s,
+                                           long long i, float lr, float mom) {
   const float vel = mom * v[i] - lr * g[i];
   const float nw = w[i] + vel;
   v[i] = vel;
   w[i] = nw;
   if (wb) {
     const int k = find_segment(s, i);
-    if (s.shadow_off[k] >= 0) wb[shadow_index(s, k, i)] = f32_to_bf16(nw);
+    if (s.shadow_off[k] >= 0) wb[shadow_index(s, k, i)] = f32_to_16_fmt(nw, wb_fmt);
   }
 }
 
 __global__ void __launch_bounds__(256) sgd_kernel(float* __restrict__ w, const float* __restrict__ g,
                                                   float* __restrict__ v,
-                                                  __nv_bfloat16* __restrict__ wb, long long n,
-                                                  float lr, float mom, SgdSegments segs) {
+                                                  uint16_t* __restrict__ wb, int wb_fmt,
+                                                  long long n, float lr, float mom,
+                                                  SgdSegments segs) {
   pdl_wait();
   pdl_launch_dependents();
   const long long n4 = n >> 2;
@@ -85,37 +86,38 @@ __global__ void __launch_bounds__(256) sgd_kernel(float* __restrict__ w, const f
       }
       if (si >= 0) {
         uint2 pk;
-        pk.x = pack_bf16x2(nw.x, nw.y);
-        pk.y = pack_bf16x2(nw.z, nw.w);
+        pk.x = pack16x2_fmt(nw.x, nw.y, wb_fmt);
+        pk.y = pack16x2_fmt(nw.z, nw.w, wb_fmt);
         if ((si & 3) == 0) {
           __stcs(reinterpret_cast<uint2*>(wb + si), pk);
         } else {
-          wb[si] = f32_to_bf16(nw.x); wb[si + 1] = f32_to_bf16(nw.y);
-          wb[si + 2] = f32_to_bf16(nw.z); wb[si + 3] = f32_to_bf16(nw.w);
+          wb[si] = (uint16_t)(pk.x & 0xffffu); wb[si + 1] = (uint16_t)(pk.x >> 16);
+          wb[si + 2] = (uint16_t)(pk.y & 0xffffu); wb[si + 3] = (uint16_t)(pk.y >> 16);
         }
       } else {
         const float vals[4] = {nw.x, nw.y, nw.z, nw.w};
         for (int e = 0; e < 4; ++e) {
           const int ke = find_segment(segs, i + e);
-          if (segs.shadow_off[ke] >= 0) wb[shadow_index(segs, ke, i + e)] = f32_to_bf16(vals[e]);
+          if (segs.shadow_off[ke] >= 0)
+            wb[shadow_index(segs, ke, i + e)] = f32_to_16_fmt(vals[e], wb_fmt);
         }
       }
     }
   }
   // scalar tail (n not a multiple of 4)
   const long long t = (n4 << 2) + (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t < n) sgd_scalar(w, g, v, wb, segs, t, lr, mom);
+  if (t < n) sgd_scalar(w, g, v, wb, wb_fmt, segs, t, lr, mom);
 }
 
-// Shadow refresh alone: wb <- bf16(w) through the segment map.
-__global__ void shadow_kernel(const float* __restrict__ w, __nv_bfloat16* __restrict__ wb,
-                              long long n, SgdSegments segs) {
+// Shadow refresh alone: wb <- bf16(w) or fp16(w) through the segment map.
+__global__ void shadow_kernel(const float* __restrict__ w, uint16_t* __restrict__ wb,
+                              int wb_fmt, long long n, SgdSegments segs) {
   pdl_wait();
   pdl_launch_dependents();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     const int k = find_segment(segs, i);
-    if (segs.shadow_off[k] >= 0) wb[shadow_index(segs, k, i)] = f32_to_bf16(w[i]);
+    if (segs.shadow_off[k] >= 0) wb[shadow_index(segs, k, i)] = f32_to_16_fmt(w[i], wb_fmt);
   }
 }
 
@@ -128,66 +130,71 @@ int sgd_grid(long long n) {
   return (int)blocks;
 }
 
-mlp_status launch_sgd(float* w, const float* g, float* v, __nv_bfloat16* wb, long long n,
+mlp_status launch_sgd(float* w, const float* g, float* v, void* wb, int wb_fmt, long long n,
                       float lr, float mom, const SgdSegments& segs, cudaStream_t st) {
   if (n <= 0) return MLP_OK;
   LaunchScope ls("sgd", st, n);
-  launch_k(sgd_kernel, dim3(sgd_grid(n)), dim3(256), 0, st, w, g, v, wb, n, lr, mom, segs);
+  launch_k(sgd_kernel, dim3(sgd_grid(n)), dim3(256), 0, st, w, g, v, static_cast<uint16_t*>(wb),
+           wb_fmt, n, lr, mom, segs);
   return launch_status();
 }
 
-mlp_status launch_shadow(const float* w, __nv_bfloat16* wb, long long n, const SgdSegments& segs,
-                         cudaStream_t st) {
+mlp_status launch_shadow(const float* w, void* wb, int wb_fmt, long long n,
+                         const SgdSegments& segs, cudaStream_t st) {
   if (n <= 0) return MLP_OK;
   LaunchScope ls("shadow", st, n);
-  launch_k(shadow_kernel, dim3(sgd_grid(n)), dim3(256), 0, st, w, wb, n, segs);
+  launch_k(shadow_kernel, dim3(sgd_grid(n)), dim3(256), 0, st, w, static_cast<uint16_t*>(wb),
+           wb_fmt, n, segs);
   return launch_status();
 }
 
 // ------------------------------------------------------------------ casts
-// Inputs arrive as image bytes (value = byte / 255, IEEE division), fp32 or
-// bf16; the tensor-core path wants bf16, the SIMT path fp32.  Source rows of
-// `cols` values land in destination rows of pitch ld_dst.
+// Inputs arrive as image bytes (value = byte / 255, IEEE division), fp32,
+// bf16 or fp16; the tensor-core path wants bf16 or fp16, the SIMT path fp32.
+// Source rows of `cols` values land in destination rows of pitch ld_dst.
 
 __device__ __forceinline__ float load_in(const void* src, int src_dtype, size_t i) {
   if (src_dtype == MLP_DTYPE_U8) return (float)static_cast<const uint8_t*>(src)[i] / 255.0f;
-  if (src_dtype == MLP_DTYPE_BF16) return bf16_to_f32(static_cast<const __nv_bfloat16*>(src)[i]);
+  if (src_dtype == MLP_DTYPE_BF16 || src_dtype == MLP_DTYPE_F16)
+    return f16bits_to_f32(static_cast<const uint16_t*>(src)[i], src_dtype);
   return static_cast<const float*>(src)[i];
 }
 
+// dst_dtype: MLP_DTYPE_F32, MLP_DTYPE_BF16 or MLP_DTYPE_F16.
 __global__ void __launch_bounds__(256) cast_rows_kernel(const void* __restrict__ src,
                                                         int src_dtype, void* __restrict__ dst,
-                                                        int dst_bf16, int rows, int cols,
+                                                        int dst_dtype, int rows, int cols,
                                                         int ld_dst) {
   pdl_wait();
   pdl_launch_dependents();
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const size_t si = (size_t)r * cols, di = (size_t)r * ld_dst;
-    if (dst_bf16 && src_dtype == MLP_DTYPE_U8 && (cols & 7) == 0 && (ld_dst & 7) == 0) {
-      // 8 bytes in, 8 bf16 (16 bytes) out per thread
+    const bool d16 = dst_dtype != MLP_DTYPE_F32;
+    if (d16 && src_dtype == MLP_DTYPE_U8 && (cols & 7) == 0 && (ld_dst & 7) == 0) {
+      // 8 bytes in, 8 16-bit values (16 bytes) out per thread
       const uint2* s8 = reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(src) + si);
-      uint4* d16 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + di);
+      uint4* dq = reinterpret_cast<uint4*>(static_cast<uint16_t*>(dst) + di);
       for (int q = threadIdx.x; q < cols / 8; q += blockDim.x) {
         const uint2 b = s8[q];
         const uint8_t* u = reinterpret_cast<const uint8_t*>(&b);
         uint4 o;
-        o.x = pack_bf16x2((float)u[0] / 255.0f, (float)u[1] / 255.0f);
-        o.y = pack_bf16x2((float)u[2] / 255.0f, (float)u[3] / 255.0f);
-        o.z = pack_bf16x2((float)u[4] / 255.0f, (float)u[5] / 255.0f);
-        o.w = pack_bf16x2((float)u[6] / 255.0f, (float)u[7] / 255.0f);
-        d16[q] = o;
+        o.x = pack16x2_fmt((float)u[0] / 255.0f, (float)u[1] / 255.0f, dst_dtype);
+        o.y = pack16x2_fmt((float)u[2] / 255.0f, (float)u[3] / 255.0f, dst_dtype);
+        o.z = pack16x2_fmt((float)u[4] / 255.0f, (float)u[5] / 255.0f, dst_dtype);
+        o.w = pack16x2_fmt((float)u[6] / 255.0f, (float)u[7] / 255.0f, dst_dtype);
+        dq[q] = o;
       }
     } else {
       for (int c = threadIdx.x; c < cols; c += blockDim.x) {
         const float v = load_in(src, src_dtype, si + c);
-        if (dst_bf16) static_cast<__nv_bfloat16*>(dst)[di + c] = f32_to_bf16(v);
+        if (d16) static_cast<uint16_t*>(dst)[di + c] = f32_to_16_fmt(v, dst_dtype);
         else static_cast<float*>(dst)[di + c] = v;
       }
     }
   }
 }
 
-mlp_status launch_cast_rows(const void* src, int src_dtype, void* dst, int dst_bf16, int rows,
+mlp_status launch_cast_rows(const void* src, int src_dtype, void* dst, int dst_dtype, int rows,
                             int cols, int ld_dst, cudaStream_t st) {
   if (rows <= 0 || cols <= 0) return MLP_OK;
   // the vector path of the kernel needs 8-byte source rows and 16-byte
@@ -195,7 +202,8 @@ mlp_status launch_cast_rows(const void* src, int src_dtype, void* dst, int dst_b
   // pointers (checked by the callers) guarantee
   int blocks = rows < num_sms() * 16 ? rows : num_sms() * 16;
   LaunchScope ls("cast", st, (long long)rows * cols);
-  launch_k(cast_rows_kernel, dim3(blocks), dim3(256), 0, st, src, src_dtype, dst, dst_bf16, rows, cols, ld_dst);
+  launch_k(cast_rows_kernel, dim3(blocks), dim3(256), 0, st, src, src_dtype, dst, dst_dtype, rows,
+           cols, ld_dst);
   return launch_status();
 }
 
@@ -231,7 +239,7 @@ __device__ __forceinline__ float warp_sum(float s) {
 }
 
 __device__ __forceinline__ float xent_row(const float* __restrict__ z, int label, int C,
-                                          float inv_norm, void* dlog_row, int dl_bf16, int ldd,
+                                          float inv_norm, void* dlog_row, int dl_dtype, int ldd,
                                           int* argmax_out, int lane) {
   label = label < 0 ? 0 : (label >= C ? C - 1 : label);  // keep the read in bounds
   MaxIdx best{-INFINITY, 0x7fffffff};
@@ -249,7 +257,7 @@ __device__ __forceinline__ float xent_row(const float* __restrict__ z, int label
     for (int c = lane; c < ldd; c += 32) {
       float d = 0.f;
       if (c < C) d = (expf(z[c] - m) / s - (c == label ? 1.f : 0.f)) * inv_norm;
-      if (dl_bf16) static_cast<__nv_bfloat16*>(dlog_row)[c] = f32_to_bf16(d);
+      if (dl_dtype) static_cast<uint16_t*>(dlog_row)[c] = f32_to_16_fmt(d, dl_dtype);
       else static_cast<float*>(dlog_row)[c] = d;
     }
   }
@@ -262,7 +270,7 @@ __device__ __forceinline__ float xent_row(const float* __restrict__ z, int label
 // values and their exponentials in registers, and writes dZ from them.
 template <int NSEG>
 __device__ __forceinline__ float xent_row_regs(const float* __restrict__ z, int label, int C,
-                                               float inv_norm, void* dlog_row, int dl_bf16,
+                                               float inv_norm, void* dlog_row, int dl_dtype,
                                                int ldd, int* argmax_out, int lane) {
   label = label < 0 ? 0 : (label >= C ? C - 1 : label);
   float v[NSEG][4];
@@ -306,25 +314,25 @@ __device__ __forceinline__ float xent_row_regs(const float* __restrict__ z, int 
       for (int e = 0; e < 4; ++e)
         d[e] = c0 + e < C ? (v[g][e] / s - (c0 + e == label ? 1.f : 0.f)) * inv_norm : 0.f;
       if (c0 + 3 < ldd) {
-        if (dl_bf16) {
+        if (dl_dtype) {
           uint2 o;
-          o.x = pack_bf16x2(d[0], d[1]);
-          o.y = pack_bf16x2(d[2], d[3]);
-          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dlog_row) + c0) = o;
+          o.x = pack16x2_fmt(d[0], d[1], dl_dtype);
+          o.y = pack16x2_fmt(d[2], d[3], dl_dtype);
+          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(dlog_row) + c0) = o;
         } else {
           *reinterpret_cast<float4*>(static_cast<float*>(dlog_row) + c0) =
               make_float4(d[0], d[1], d[2], d[3]);
         }
       } else {
         for (int e = 0; e < 4 && c0 + e < ldd; ++e) {
-          if (dl_bf16) static_cast<__nv_bfloat16*>(dlog_row)[c0 + e] = f32_to_bf16(d[e]);
+          if (dl_dtype) static_cast<uint16_t*>(dlog_row)[c0 + e] = f32_to_16_fmt(d[e], dl_dtype);
           else static_cast<float*>(dlog_row)[c0 + e] = d[e];
         }
       }
     }
     // padding columns beyond the last 128-class segment
     for (int c = NSEG * 128 + lane; c < ldd; c += 32) {
-      if (dl_bf16) static_cast<__nv_bfloat16*>(dlog_row)[c] = f32_to_bf16(0.f);
+      if (dl_dtype) static_cast<uint16_t*>(dlog_row)[c] = 0;
       else static_cast<float*>(dlog_row)[c] = 0.f;
     }
   }
@@ -335,7 +343,7 @@ __device__ __forceinline__ float xent_row_regs(const float* __restrict__ z, int 
 template <int NSEG>
 __global__ void __launch_bounds__(256) xent_rows_regs_kernel(
     const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
-    float* __restrict__ partial, void* dlog, int dl_bf16, int ldd, int* argmax) {
+    float* __restrict__ partial, void* dlog, int dl_dtype, int ldd, int* argmax) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float part[8];
@@ -344,10 +352,10 @@ __global__ void __launch_bounds__(256) xent_rows_regs_kernel(
   float li = 0.f;
   if (r < B) {
     void* drow = nullptr;
-    if (dlog) drow = dl_bf16 ? (void*)(static_cast<__nv_bfloat16*>(dlog) + (size_t)r * ldd)
+    if (dlog) drow = dl_dtype ? (void*)(static_cast<uint16_t*>(dlog) + (size_t)r * ldd)
                              : (void*)(static_cast<float*>(dlog) + (size_t)r * ldd);
     li = xent_row_regs<NSEG>(logits + (size_t)r * ldl, labels[r], C, 1.0f / (float)B, drow,
-                             dl_bf16, ldd, argmax ? argmax + r : nullptr, lane);
+                             dl_dtype, ldd, argmax ? argmax + r : nullptr, lane);
   }
   if (lane == 0) part[warp] = li;
   __syncthreads();
@@ -362,7 +370,7 @@ __global__ void __launch_bounds__(256) xent_rows_regs_kernel(
 // forms the mean (warp w sums its rows in order, then warp sums in order).
 __global__ void __launch_bounds__(256) xent_single_block_kernel(
     const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
-    float* __restrict__ loss_out, void* dlog, int dl_bf16, int ldd, int* argmax) {
+    float* __restrict__ loss_out, void* dlog, int dl_dtype, int ldd, int* argmax) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float part[8];
@@ -371,9 +379,9 @@ __global__ void __launch_bounds__(256) xent_single_block_kernel(
   float acc = 0.f;
   for (int r = warp; r < B; r += 8) {
     void* drow = nullptr;
-    if (dlog) drow = dl_bf16 ? (void*)(static_cast<__nv_bfloat16*>(dlog) + (size_t)r * ldd)
+    if (dlog) drow = dl_dtype ? (void*)(static_cast<uint16_t*>(dlog) + (size_t)r * ldd)
                              : (void*)(static_cast<float*>(dlog) + (size_t)r * ldd);
-    acc += xent_row(logits + (size_t)r * ldl, labels[r], C, inv_norm, drow, dl_bf16, ldd,
+    acc += xent_row(logits + (size_t)r * ldl, labels[r], C, inv_norm, drow, dl_dtype, ldd,
                     argmax ? argmax + r : nullptr, lane);
   }
   if (lane == 0) part[warp] = acc;
@@ -391,7 +399,7 @@ __global__ void __launch_bounds__(256) xent_single_block_kernel(
 // loss epilogue of the logits GEMM); the batch mean is a fixed-order tree sum.
 template <int NC>
 __device__ __forceinline__ float xent_lane_row(const float* __restrict__ z_row, int label, int C,
-                                               float inv, void* dlog_row, int dl_bf16, int ldd,
+                                               float inv, void* dlog_row, int dl_dtype, int ldd,
                                                int* argmax) {
   float z[NC], d[NC];
 #pragma unroll
@@ -403,7 +411,7 @@ __device__ __forceinline__ float xent_lane_row(const float* __restrict__ z_row, 
     for (int j = 0; j < 32; ++j) {
       if (j < ldd) {
         const float v = j < NC ? d[j % NC] : 0.f;
-        if (dl_bf16) static_cast<__nv_bfloat16*>(dlog_row)[j] = f32_to_bf16(v);
+        if (dl_dtype) static_cast<uint16_t*>(dlog_row)[j] = f32_to_16_fmt(v, dl_dtype);
         else static_cast<float*>(dlog_row)[j] = v;
       }
     }
@@ -414,7 +422,7 @@ __device__ __forceinline__ float xent_lane_row(const float* __restrict__ z_row, 
 
 __global__ void __launch_bounds__(512) xent_lane_rows_kernel(
     const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
-    float* __restrict__ loss_out, void* dlog, int dl_bf16, int ldd, int* argmax) {
+    float* __restrict__ loss_out, void* dlog, int dl_dtype, int ldd, int* argmax) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float red[512];
@@ -423,12 +431,12 @@ __global__ void __launch_bounds__(512) xent_lane_rows_kernel(
   if (r < B) {
     const float inv = 1.0f / (float)B;
     void* drow = nullptr;
-    if (dlog) drow = dl_bf16 ? (void*)(static_cast<__nv_bfloat16*>(dlog) + (size_t)r * ldd)
+    if (dlog) drow = dl_dtype ? (void*)(static_cast<uint16_t*>(dlog) + (size_t)r * ldd)
                              : (void*)(static_cast<float*>(dlog) + (size_t)r * ldd);
     int* am = argmax ? argmax + r : nullptr;
-    li = C <= 16 ? xent_lane_row<16>(logits + (size_t)r * ldl, labels[r], C, inv, drow, dl_bf16,
+    li = C <= 16 ? xent_lane_row<16>(logits + (size_t)r * ldl, labels[r], C, inv, drow, dl_dtype,
                                      ldd, am)
-                 : xent_lane_row<32>(logits + (size_t)r * ldl, labels[r], C, inv, drow, dl_bf16,
+                 : xent_lane_row<32>(logits + (size_t)r * ldl, labels[r], C, inv, drow, dl_dtype,
                                      ldd, am);
   }
   red[r] = li;
@@ -444,7 +452,7 @@ __global__ void __launch_bounds__(512) xent_lane_rows_kernel(
 // fixed-order sum.
 __global__ void __launch_bounds__(256) xent_rows_kernel(
     const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
-    float* __restrict__ partial, void* dlog, int dl_bf16, int ldd, int* argmax) {
+    float* __restrict__ partial, void* dlog, int dl_dtype, int ldd, int* argmax) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float part[8];
@@ -453,9 +461,9 @@ __global__ void __launch_bounds__(256) xent_rows_kernel(
   float li = 0.f;
   if (r < B) {
     void* drow = nullptr;
-    if (dlog) drow = dl_bf16 ? (void*)(static_cast<__nv_bfloat16*>(dlog) + (size_t)r * ldd)
+    if (dlog) drow = dl_dtype ? (void*)(static_cast<uint16_t*>(dlog) + (size_t)r * ldd)
                              : (void*)(static_cast<float*>(dlog) + (size_t)r * ldd);
-    li = xent_row(logits + (size_t)r * ldl, labels[r], C, 1.0f / (float)B, drow, dl_bf16, ldd,
+    li = xent_row(logits + (size_t)r * ldl, labels[r], C, 1.0f / (float)B, drow, dl_dtype, ldd,
                   argmax ? argmax + r : nullptr, lane);
   }
   if (lane == 0) part[warp] = li;
@@ -491,7 +499,7 @@ size_t xent_workspace_bytes(int B) {
 }
 
 mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, int C,
-                       float* loss_out, void* dlog, int dl_bf16, int ldd, int* argmax,
+                       float* loss_out, void* dlog, int dl_dtype, int ldd, int* argmax,
                        void* ws, cudaStream_t st) {
   if (B <= 0) return MLP_OK;
   if (C <= 32 && ldd <= 32 && B <= 512) {
@@ -499,13 +507,13 @@ mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, i
     while (threads < B) threads *= 2;  // a power of two for the tree sum
     LaunchScope ls("xent", st, B, C);
     launch_k(xent_lane_rows_kernel, dim3(1), dim3(threads), 0, st, logits, ldl, labels, B, C,
-             loss_out, dlog, dl_bf16, ldd, argmax);
+             loss_out, dlog, dl_dtype, ldd, argmax);
     return launch_status();
   }
   if (B <= 256) {
     LaunchScope ls("xent", st, B, C);
     launch_k(xent_single_block_kernel, dim3(1), dim3(256), 0, st, logits, ldl, labels, B, C, loss_out, dlog,
-                                                dl_bf16, ldd, argmax);
+                                                dl_dtype, ldd, argmax);
     return launch_status();
   }
   const int blocks = (B + 7) / 8;
@@ -516,12 +524,12 @@ mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, i
   LaunchScope ls("xent", st, B, C);
   if (vec && C <= 256)
     launch_k(xent_rows_regs_kernel<2>, dim3(blocks), dim3(256), 0, st, logits, ldl, labels, B, C, partial, dlog,
-                                                     dl_bf16, ldd, argmax);
+                                                     dl_dtype, ldd, argmax);
   else if (vec)
     launch_k(xent_rows_regs_kernel<8>, dim3(blocks), dim3(256), 0, st, logits, ldl, labels, B, C, partial, dlog,
-                                                     dl_bf16, ldd, argmax);
+                                                     dl_dtype, ldd, argmax);
   else
-    launch_k(xent_rows_kernel, dim3(blocks), dim3(256), 0, st, logits, ldl, labels, B, C, partial, dlog, dl_bf16,
+    launch_k(xent_rows_kernel, dim3(blocks), dim3(256), 0, st, logits, ldl, labels, B, C, partial, dlog, dl_dtype,
                                              ldd, argmax);
   }
   MLP_CHECK(launch_status());
@@ -549,6 +557,10 @@ __device__ __forceinline__ float ldf<float>(const float* p) { return *p; }
 template <>
 __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p) {
   return bf16_to_f32(*p);
+}
+template <>
+__device__ __forceinline__ float ldf<__half>(const __half* p) {
+  return __half2float(*p);
 }
 
 template <typename T>
@@ -583,7 +595,7 @@ __global__ void __launch_bounds__(256) colsum_pass1_kernel(const T* __restrict__
   }
 }
 
-// Vector form: each lane reads 16 bytes of a row (8 bf16 or 4 fp32 columns),
+// Vector form: each lane reads 16 bytes of a row (8 bf16 / fp16 or 4 fp32 columns),
 // a warp covers 512 contiguous bytes, 8 warps stride over the rows of the
 // chunk (4 rows in flight per lane), then the warps' sums are added in order.
 template <typename T>
@@ -665,34 +677,36 @@ size_t colsum_workspace_bytes(int rows, int cols) {
   return ch > 1 ? (size_t)ch * cols * sizeof(float) : 0;
 }
 
-mlp_status launch_colsum(const void* X, int bf16, int rows, int cols, int ld, float* out,
+// dtype: MLP_DTYPE_F32, MLP_DTYPE_BF16 or MLP_DTYPE_F16.
+template <typename T>
+void launch_colsum_t(const T* X, int rows, int cols, int ld, int ch, int rpc, float* dst,
+                     bool vec, cudaStream_t st) {
+  LaunchScope ls("colsum", st, rows, cols);
+  if (vec) {
+    constexpr int bc = 32 * (16 / (int)sizeof(T));
+    dim3 g((cols + bc - 1) / bc, ch);
+    launch_k(colsum_vec_kernel<T>, g, dim3(256), 0, st, X, rows, cols, ld, rpc, dst);
+  } else {
+    dim3 grid((cols + 63) / 64, ch);
+    launch_k(colsum_pass1_kernel<T>, grid, dim3(256), 0, st, X, rows, cols, ld, rpc, dst);
+  }
+}
+
+mlp_status launch_colsum(const void* X, int dtype, int rows, int cols, int ld, float* out,
                          void* ws, cudaStream_t st) {
   if (cols <= 0) return MLP_OK;
   int ch, rpc;
   colsum_plan(rows, cols, &ch, &rpc);
-  dim3 grid((cols + 63) / 64, ch);
   float* dst = ch > 1 ? static_cast<float*>(ws) : out;
-  const bool vec = aligned16(X) && (bf16 ? (cols % 8 == 0 && ld % 8 == 0)
-                                         : (cols % 4 == 0 && ld % 4 == 0));
-  if (vec) {
-    LaunchScope ls("colsum", st, rows, cols);
-    const int bc = bf16 ? 256 : 128;
-    dim3 g((cols + bc - 1) / bc, ch);
-    if (bf16)
-      launch_k(colsum_vec_kernel<__nv_bfloat16>, dim3(g), dim3(256), 0, st, static_cast<const __nv_bfloat16*>(X),
-                                                         rows, cols, ld, rpc, dst);
-    else
-      launch_k(colsum_vec_kernel<float>, dim3(g), dim3(256), 0, st, static_cast<const float*>(X), rows, cols, ld,
-                                                  rpc, dst);
-  } else {
-  LaunchScope ls("colsum", st, rows, cols);
-  if (bf16)
-    launch_k(colsum_pass1_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st, 
-        static_cast<const __nv_bfloat16*>(X), rows, cols, ld, rpc, dst);
+  const bool h16 = dtype != MLP_DTYPE_F32;
+  const bool vec = aligned16(X) && (h16 ? (cols % 8 == 0 && ld % 8 == 0)
+                                        : (cols % 4 == 0 && ld % 4 == 0));
+  if (dtype == MLP_DTYPE_BF16)
+    launch_colsum_t(static_cast<const __nv_bfloat16*>(X), rows, cols, ld, ch, rpc, dst, vec, st);
+  else if (dtype == MLP_DTYPE_F16)
+    launch_colsum_t(static_cast<const __half*>(X), rows, cols, ld, ch, rpc, dst, vec, st);
   else
-    launch_k(colsum_pass1_kernel<float>, dim3(grid), dim3(256), 0, st, static_cast<const float*>(X), rows, cols,
-                                                     ld, rpc, dst);
-  }
+    launch_colsum_t(static_cast<const float*>(X), rows, cols, ld, ch, rpc, dst, vec, st);
   MLP_CHECK(launch_status());
   if (ch > 1) {
     LaunchScope ls("colsum_final", st, ch, cols);
@@ -784,7 +798,8 @@ mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out
 
 // ------------------------------------------------------------------ ones columns
 
-__global__ void ones_cols_kernel(OnesCols oc, int rows, int bf16) {
+// dtype: MLP_DTYPE_F32, MLP_DTYPE_BF16 or MLP_DTYPE_F16.
+__global__ void ones_cols_kernel(OnesCols oc, int rows, int dtype) {
   pdl_wait();
   pdl_launch_dependents();
   const int k = blockIdx.y;
@@ -792,17 +807,18 @@ __global__ void ones_cols_kernel(OnesCols oc, int rows, int bf16) {
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
     for (int c = col; c < ld; ++c) {
       const float v = c == col ? 1.f : 0.f;
-      if (bf16) static_cast<__nv_bfloat16*>(oc.ptr[k])[(size_t)r * ld + c] = f32_to_bf16(v);
+      if (dtype != MLP_DTYPE_F32)
+        static_cast<uint16_t*>(oc.ptr[k])[(size_t)r * ld + c] = f32_to_16_fmt(v, dtype);
       else static_cast<float*>(oc.ptr[k])[(size_t)r * ld + c] = v;
     }
   }
 }
 
-mlp_status launch_ones_cols(const OnesCols& oc, int rows, int bf16, cudaStream_t st) {
+mlp_status launch_ones_cols(const OnesCols& oc, int rows, int dtype, cudaStream_t st) {
   if (oc.n <= 0 || rows <= 0) return MLP_OK;
   LaunchScope ls("ones_cols", st, rows, oc.n);
   dim3 grid((rows + 255) / 256, oc.n);
-  launch_k(ones_cols_kernel, dim3(grid), dim3(256), 0, st, oc, rows, bf16);
+  launch_k(ones_cols_kernel, dim3(grid), dim3(256), 0, st, oc, rows, dtype);
   return launch_status();
 }
 

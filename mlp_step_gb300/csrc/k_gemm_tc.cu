@@ -48,7 +48,8 @@ struct TcParams {
   int ldm;
   void* C;
   int ldc;
-  int c_bf16;
+  int c_bf16;  // C is 16-bit (bf16, or fp16 when f16 is set)
+  int f16;     // operands and 16-bit outputs are fp16 rather than bf16
   unsigned long long wait_ns;
   int* err;
   // split-K: each work unit covers k-blocks [s*kb_per_split, (s+1)*kb_per_split)
@@ -184,6 +185,7 @@ __device__ __forceinline__ void epilogue_values(const TcParams& p, int m, int n0
 }
 
 // Register store of one piece (outputs whose rows are not 16-byte aligned).
+template <int H16>
 __device__ __forceinline__ void epilogue_store_regs(const TcParams& p, int m, int n0,
                                                     const float (&v)[32]) {
   const bool full = (n0 + 32 <= p.N);
@@ -193,16 +195,19 @@ __device__ __forceinline__ void epilogue_store_regs(const TcParams& p, int m, in
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 o;
-        o.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-        o.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-        o.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-        o.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+        o.x = pack16x2<H16>(v[q * 8 + 0], v[q * 8 + 1]);
+        o.y = pack16x2<H16>(v[q * 8 + 2], v[q * 8 + 3]);
+        o.z = pack16x2<H16>(v[q * 8 + 4], v[q * 8 + 5]);
+        o.w = pack16x2<H16>(v[q * 8 + 6], v[q * 8 + 7]);
         reinterpret_cast<uint4*>(crow)[q] = o;
       }
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (n0 + j < p.N) crow[j] = f32_to_bf16(v[j]);
+        if (n0 + j < p.N) {
+          if constexpr (H16) reinterpret_cast<uint16_t*>(crow)[j] = f32_to_16<1>(v[j]);
+          else crow[j] = f32_to_bf16(v[j]);
+        }
     }
   } else {
     float* crow = static_cast<float*>(p.C) + (size_t)m * p.ldc + n0;
@@ -223,6 +228,7 @@ __device__ __forceinline__ void epilogue_store_regs(const TcParams& p, int m, in
 // output tensor map uses: 16-byte chunk q of a row is stored at chunk
 // q ^ (lane & 7) for fp32 (128-byte rows, 128-byte swizzle) and at
 // q ^ ((lane >> 1) & 3) for bf16 (64-byte rows, 64-byte swizzle).
+template <int H16>
 __device__ __forceinline__ void epilogue_stage_row(uint8_t* box, int c_bf16, int lane,
                                                    const float (&v)[32]) {
   if (c_bf16) {
@@ -230,10 +236,10 @@ __device__ __forceinline__ void epilogue_stage_row(uint8_t* box, int c_bf16, int
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       uint4 o;
-      o.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-      o.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-      o.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-      o.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+      o.x = pack16x2<H16>(v[q * 8 + 0], v[q * 8 + 1]);
+      o.y = pack16x2<H16>(v[q * 8 + 2], v[q * 8 + 3]);
+      o.z = pack16x2<H16>(v[q * 8 + 4], v[q * 8 + 5]);
+      o.w = pack16x2<H16>(v[q * 8 + 6], v[q * 8 + 7]);
       *reinterpret_cast<uint4*>(row + ((q ^ ((lane >> 1) & 3)) << 4)) = o;
     }
   } else {
@@ -253,6 +259,7 @@ __device__ __forceinline__ void epilogue_stage_row(uint8_t* box, int c_bf16, int
 // conflict-free both ways) so that g, w, v and the bf16 shadow are read and
 // written one row at a time across the lanes: 128-byte accesses instead of
 // 32 rows touched by every instruction.  Called by the whole warp.
+template <int H16>
 __device__ __forceinline__ void sgd_epilogue_staged(const TcParams& p, int row0, int n0,
                                                     const uint32_t (&r)[32], float* slot,
                                                     int lane) {
@@ -285,8 +292,12 @@ __device__ __forceinline__ void sgd_epilogue_staged(const TcParams& p, int row0,
         static_cast<float*>(p.C)[off] = g;
         p.sgd_v[off] = nv;
         p.sgd_w[off] = nw;
-        if (p.sgd_shadow && m < p.sgd_shadow_rows)
-          p.sgd_shadow[(size_t)m * p.sgd_ld_shadow + n] = f32_to_bf16(nw);
+        if (p.sgd_shadow && m < p.sgd_shadow_rows) {
+          if constexpr (H16)
+            reinterpret_cast<uint16_t*>(p.sgd_shadow)[(size_t)m * p.sgd_ld_shadow + n] =
+                f32_to_16<1>(nw);
+          else p.sgd_shadow[(size_t)m * p.sgd_ld_shadow + n] = f32_to_bf16(nw);
+        }
       }
     }
   }
@@ -335,6 +346,7 @@ __device__ __forceinline__ void sgd_state_prefetch(const TcParams& p, int row0, 
 
 // Momentum SGD as in sgd_epilogue_staged, with w and v of the piece taken
 // from the shared-memory copy (columns c0 .. c0 + 31 of the warp's rows).
+template <int H16>
 __device__ __forceinline__ void sgd_epilogue_smem(const TcParams& p, int row0, int n0, int c0,
                                                   const uint32_t (&r)[32], float* slot,
                                                   const float* w_s, const float* v_s, int lane) {
@@ -370,8 +382,12 @@ __device__ __forceinline__ void sgd_epilogue_smem(const TcParams& p, int row0, i
         static_cast<float*>(p.C)[off] = g[i];
         p.sgd_v[off] = nv[i];
         p.sgd_w[off] = nw[i];
-        if (p.sgd_shadow && m < p.sgd_shadow_rows)
-          p.sgd_shadow[(size_t)m * p.sgd_ld_shadow + n] = f32_to_bf16(nw[i]);
+        if (p.sgd_shadow && m < p.sgd_shadow_rows) {
+          if constexpr (H16)
+            reinterpret_cast<uint16_t*>(p.sgd_shadow)[(size_t)m * p.sgd_ld_shadow + n] =
+                f32_to_16<1>(nw[i]);
+          else p.sgd_shadow[(size_t)m * p.sgd_ld_shadow + n] = f32_to_bf16(nw[i]);
+        }
       }
     }
   }
@@ -379,10 +395,10 @@ __device__ __forceinline__ void sgd_epilogue_smem(const TcParams& p, int row0, i
 
 // Softmax cross entropy of one row of at most 32 logits held by one thread
 // (the row routine of xent_row.cuh, shared with the one-row-per-thread loss
-// kernel).  Writes the fp32 logits (if C is set), bf16 dZ = (softmax -
+// kernel).  Writes the fp32 logits (if C is set), 16-bit dZ = (softmax -
 // onehot) / norm padded with zeros to xent_ldd, and the argmax (lowest index
 // among ties); returns the row loss.
-template <int NC>
+template <int NC, int H16>
 __device__ __forceinline__ float xent_epilogue_row_nc(const TcParams& p, int m,
                                                       const uint32_t (&r)[32], const int* labels,
                                                       int* argmax) {
@@ -418,23 +434,28 @@ __device__ __forceinline__ float xent_epilogue_row_nc(const TcParams& p, int m,
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = 8 * q + e < NC ? d[(8 * q + e) % NC] : 0.f;
         reinterpret_cast<uint4*>(drow)[q] =
-            make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                       pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+            make_uint4(pack16x2<H16>(v[0], v[1]), pack16x2<H16>(v[2], v[3]),
+                       pack16x2<H16>(v[4], v[5]), pack16x2<H16>(v[6], v[7]));
       }
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (j < p.xent_ldd) drow[j] = f32_to_bf16(j < NC ? d[j % NC] : 0.f);
+      if (j < p.xent_ldd) {
+        if constexpr (H16)
+          reinterpret_cast<uint16_t*>(drow)[j] = f32_to_16<1>(j < NC ? d[j % NC] : 0.f);
+        else drow[j] = f32_to_bf16(j < NC ? d[j % NC] : 0.f);
+      }
   }
   if (argmax) argmax[m] = am;
   return loss;
 }
 
+template <int H16>
 __device__ __forceinline__ float xent_epilogue_row(const TcParams& p, int m,
                                                    const uint32_t (&r)[32], const int* labels,
                                                    int* argmax) {
-  return p.N <= 16 ? xent_epilogue_row_nc<16>(p, m, r, labels, argmax)
-                   : xent_epilogue_row_nc<32>(p, m, r, labels, argmax);
+  return p.N <= 16 ? xent_epilogue_row_nc<16, H16>(p, m, r, labels, argmax)
+                   : xent_epilogue_row_nc<32, H16>(p, m, r, labels, argmax);
 }
 
 // L1 prefetch of what the epilogue of row m, columns [n0, n0 + bn) will
@@ -456,7 +477,7 @@ __device__ __forceinline__ void epilogue_prefetch(const TcParams& p, int m, int 
     }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int H16>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -563,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
+      const uint32_t idesc = ptx::idesc_16_f32<H16>(BM, BN, p.a_mn, p.b_mn);
       const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
       const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
       const uint32_t a_kstep = p.a_mn ? 2048u : 32u;  // bytes per 16-element k step
@@ -640,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_ld_wait();
         const float* sb = stage_bias(p, n0, sbias + (warp - 2) * 32, lane);
         if (p.sgd_w) {
-          sgd_epilogue_staged(p, tm * BM + quarter * 32, n0, r,
+          sgd_epilogue_staged<H16>(p, tm * BM + quarter * 32, n0, r,
                               reinterpret_cast<float*>(stg + (warp - 2) * 8192), lane);
         } else if (m < p.M) {
           if (part) {
@@ -660,11 +681,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n0 + j < p.N) prow[j] = __uint_as_float(r[j]);
             }
           } else if (p.xent_labels) {
-            row_loss = xent_epilogue_row(p, m, r, p.xent_labels, p.xent_argmax);
+            row_loss = xent_epilogue_row<H16>(p, m, r, p.xent_labels, p.xent_argmax);
           } else if (!p.tma_store) {
             float v[32];
             epilogue_values(p, m, n0, r, sb, mp, v);
-            epilogue_store_regs(p, m, n0, v);
+            epilogue_store_regs<H16>(p, m, n0, v);
           }
         }
         if (p.tma_store) {
@@ -676,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) ptx::bulk_wait_group_read<1>();
             __syncwarp();
           }
-          epilogue_stage_row(box, p.c_bf16, lane, v);
+          epilogue_stage_row<H16>(box, p.c_bf16, lane, v);
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -783,12 +804,14 @@ static_assert(sizeof(StepProgram) <= 32000, "step program exceeds the kernel par
 __device__ __forceinline__ float step_load_in(const void* src, int dtype, size_t i) {
   if (dtype == MLP_DTYPE_U8) return (float)static_cast<const uint8_t*>(src)[i] / 255.0f;
   if (dtype == MLP_DTYPE_BF16) return bf16_to_f32(static_cast<const __nv_bfloat16*>(src)[i]);
+  if (dtype == MLP_DTYPE_F16) return __half2float(static_cast<const __half*>(src)[i]);
   return static_cast<const float*>(src)[i];
 }
 
-// Input rows of step `step` -> bf16 rows of pitch cast_ld at dst (image
+// Input rows of step `step` -> 16-bit rows of pitch cast_ld at dst (image
 // bytes become byte / 255), spread over CTAs [0, n_cta) of those calling it
 // (cta = this CTA's index among them); all threads of the CTA take part.
+template <int H16>
 __device__ __forceinline__ void step_cast(const StepProgram& prog, int step, __nv_bfloat16* dst,
                                           int cta, int n_cta) {
   const long long stride = (long long)n_cta * blockDim.x;
@@ -804,17 +827,21 @@ __device__ __forceinline__ void step_cast(const StepProgram& prog, int step, __n
       const uint2 b = reinterpret_cast<const uint2*>(src)[i];
       const uint8_t* u8 = reinterpret_cast<const uint8_t*>(&b);
       uint4 o;
-      o.x = pack_bf16x2((float)u8[0] / 255.0f, (float)u8[1] / 255.0f);
-      o.y = pack_bf16x2((float)u8[2] / 255.0f, (float)u8[3] / 255.0f);
-      o.z = pack_bf16x2((float)u8[4] / 255.0f, (float)u8[5] / 255.0f);
-      o.w = pack_bf16x2((float)u8[6] / 255.0f, (float)u8[7] / 255.0f);
+      o.x = pack16x2<H16>((float)u8[0] / 255.0f, (float)u8[1] / 255.0f);
+      o.y = pack16x2<H16>((float)u8[2] / 255.0f, (float)u8[3] / 255.0f);
+      o.z = pack16x2<H16>((float)u8[4] / 255.0f, (float)u8[5] / 255.0f);
+      o.w = pack16x2<H16>((float)u8[6] / 255.0f, (float)u8[7] / 255.0f);
       reinterpret_cast<uint4*>(dst + (size_t)r * prog.cast_ld)[q] = o;
     }
   } else {
     const long long n = (long long)prog.cast_rows * prog.cast_cols;
     for (long long i = first; i < n; i += stride) {
       const int r = (int)(i / prog.cast_cols), c = (int)(i % prog.cast_cols);
-      dst[(size_t)r * prog.cast_ld + c] = f32_to_bf16(step_load_in(src, prog.cast_dtype, (size_t)i));
+      if constexpr (H16)
+        reinterpret_cast<uint16_t*>(dst)[(size_t)r * prog.cast_ld + c] =
+            f32_to_16<1>(step_load_in(src, prog.cast_dtype, (size_t)i));
+      else
+        dst[(size_t)r * prog.cast_ld + c] = f32_to_bf16(step_load_in(src, prog.cast_dtype, (size_t)i));
     }
   }
 }
@@ -869,7 +896,7 @@ __device__ __forceinline__ int step_gemm_of(const int* tile_base, const StepPhas
   return g;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int H16>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_step_kernel(const __grid_constant__ StepProgram prog) {
   using L = Layout<BN, STAGES>;
@@ -960,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ph.kind == 1) {
       // with two input buffers only the first step casts in a phase of its
       // own; the later ones were cast during the step before
-      if (!dbuf || step == 0) step_cast(prog, step, prog.cast_dst, blockIdx.x, gridDim.x);
+      if (!dbuf || step == 0) step_cast<H16>(prog, step, prog.cast_dst, blockIdx.x, gridDim.x);
       else sync_after = false;
     } else if (warp == 0) {
       if (lane == 0) {
@@ -1028,7 +1055,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int g = step_gemm_of(s_tile_base, ph, u, t);
           // a private copy: a reference would be re-read after every store
           const TcParams p = s_gp[g];
-          const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
+          const uint32_t idesc = ptx::idesc_16_f32<H16>(BM, BN, p.a_mn, p.b_mn);
           const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
           const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
           const uint32_t a_kstep = p.a_mn ? 2048u : 32u;
@@ -1115,16 +1142,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   r);
           ptx::tmem_ld_wait();
           if (p.sgd_w) {
-            sgd_epilogue_smem(p, row0, n0, c0, r,
+            sgd_epilogue_smem<H16>(p, row0, n0, c0, r,
                               reinterpret_cast<float*>(stg + (warp - 2) * 8192), w_s, v_s, lane);
           } else if (p.xent_labels) {
-            if (m < p.M) row_loss = xent_epilogue_row(p, m, r, labels, argmax);
+            if (m < p.M) row_loss = xent_epilogue_row<H16>(p, m, r, labels, argmax);
           } else {
             const float* sb = stage_bias_reg(p, bias_r[c0 / 32], sbias + (warp - 2) * 32, lane);
             if (m < p.M) {
               float v[32];
               epilogue_values(p, m, n0, r, sb, mp, v);
-              epilogue_store_regs(p, m, n0, v);
+              epilogue_store_regs<H16>(p, m, n0, v);
             }
           }
         }
@@ -1152,7 +1179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the next step's input, cast by the CTAs without a tile in this phase
     if (dbuf && phi == prog.cast_ahead_phase && step + 1 < prog.n_steps &&
         (int)blockIdx.x >= ph.tiles)
-      step_cast(prog, step + 1, ((step + 1) & 1) ? prog.cast_dst_alt : prog.cast_dst,
+      step_cast<H16>(prog, step + 1, ((step + 1) & 1) ? prog.cast_dst_alt : prog.cast_dst,
                 (int)blockIdx.x - ph.tiles, (int)gridDim.x - ph.tiles);
     if (it + 1 < n_total && sync_after) step_grid_sync(prog, s_abort, barriers_passed);
   }
@@ -1215,7 +1242,7 @@ struct Layout2 {
   static constexpr int SMEM = SMEM_BASE + STG_BYTES;
 };
 
-template <int STAGES>
+template <int STAGES, int H16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -1314,7 +1341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
-      const uint32_t idesc = ptx::idesc_bf16_f32(256, BN2, p.a_mn, p.b_mn);
+      const uint32_t idesc = ptx::idesc_16_f32<H16>(256, BN2, p.a_mn, p.b_mn);
       const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
       const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
       const uint32_t a_kstep = p.a_mn ? 2048u : 32u;
@@ -1416,7 +1443,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           if (m < p.M) {
             float v[32];
             epilogue_values(p, m, n0, r, sb, mp, v);
-            epilogue_store_regs(p, m, n0, v);
+            epilogue_store_regs<H16>(p, m, n0, v);
           }
         } else if (row0 < p.M) {  // warp-uniform; rows past M are clipped by TMA
           float v[32];
@@ -1430,7 +1457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             }
             __syncwarp();
           }
-          epilogue_stage_row(box, p.c_bf16, lane, v);
+          epilogue_stage_row<H16>(box, p.c_bf16, lane, v);
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -1498,19 +1525,21 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const TcParams p) {
       if (p.bias) o += p.bias[n];
       if (p.act == MLP_ACT_RELU) o = fmaxf(o, 0.f);
       if (p.mask) o = bf16_to_f32(p.mask[(size_t)m * p.ldm + n]) > 0.f ? o : 0.f;
-      if (p.c_bf16) static_cast<__nv_bfloat16*>(p.C)[(size_t)m * p.ldc + n] = f32_to_bf16(o);
+      if (p.c_bf16)
+        static_cast<uint16_t*>(p.C)[(size_t)m * p.ldc + n] =
+            f32_to_16_fmt(o, p.f16 ? MLP_DTYPE_F16 : MLP_DTYPE_BF16);
       else static_cast<float*>(p.C)[(size_t)m * p.ldc + n] = o;
     }
   }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int H16>
 mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                      const TcParams& p, cudaStream_t st) {
   using L = Layout<BN, STAGES>;
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES>,
+    if (cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, H16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
       return MLP_ERR_CUDA;
     configured = true;
@@ -1523,7 +1552,7 @@ mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
                                          "gemm_tc_splitk_bn256"};
     const int which = BN == 64 ? 0 : (BN == 128 ? 1 : 2);
     LaunchScope ls(p.splits > 1 ? split_names[which] : names[which], st, p.M, p.N, p.K);
-    launch_k(tc_gemm_kernel<BN, STAGES>, dim3(grid), dim3(kThreads),
+    launch_k(tc_gemm_kernel<BN, STAGES, H16>, dim3(grid), dim3(kThreads),
              p.tma_store || p.sgd_w ? L::SMEM : L::SMEM_BASE, st, ta, tb, tc, p);
   }
   MLP_CHECK(launch_status());
@@ -1538,14 +1567,14 @@ mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
   return MLP_OK;
 }
 
-template <int STAGES>
+template <int STAGES, int H16>
 mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                        const TcParams& p, cudaStream_t st) {
   using L = Layout2<STAGES>;
   static bool configured = false;
   static int max_pairs = 0;
   if (!configured) {
-    if (cudaFuncSetAttribute(tc_gemm_pair_kernel<STAGES>,
+    if (cudaFuncSetAttribute(tc_gemm_pair_kernel<STAGES, H16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
       return MLP_ERR_CUDA;
     // pairs that fit at once (a GPC with an odd number of free SMs leaves one over)
@@ -1554,7 +1583,7 @@ mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
     cfg.blockDim = dim3(kPairThreads);
     cfg.dynamicSmemBytes = L::SMEM;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<STAGES>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<STAGES, H16>, &cfg) != cudaSuccess ||
         n < 1) {
       cudaGetLastError();
       n = num_sms() / 2;
@@ -1566,7 +1595,7 @@ mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
   const int pairs = units < max_pairs ? units : max_pairs;
   {
     LaunchScope ls(p.splits > 1 ? "gemm_tc_pair_splitk" : "gemm_tc_pair", st, p.M, p.N, p.K);
-    launch_k(tc_gemm_pair_kernel<STAGES>, dim3(2 * pairs), dim3(kPairThreads),
+    launch_k(tc_gemm_pair_kernel<STAGES, H16>, dim3(2 * pairs), dim3(kPairThreads),
              p.tma_store ? L::SMEM : L::SMEM_BASE, st, ta, tb, tc, p);
   }
   MLP_CHECK(launch_status());
@@ -1652,6 +1681,7 @@ mlp_status prepare_tc(const GemmArgs& g, int tiles_m, int BN, int splits, int kb
   p.C = g.C;
   p.ldc = g.ldc;
   p.c_bf16 = g.c_bf16;
+  p.f16 = g.f16;
   p.wait_ns = wait_ns;
   p.splits = splits;
   p.kb_per_split = kb_per_split;
@@ -1705,13 +1735,15 @@ bool step_gemm_supported(const GemmArgs& g) {
 mlp_status launch_step_program(const StepSpec& s, unsigned* bar_words, unsigned long long wait_ns,
                                cudaStream_t st) {
   using L = Layout<STEP_BN, STEP_STAGES>;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(tc_step_kernel<STEP_BN, STEP_STAGES>,
+  static bool configured[2] = {false, false};
+  const int h16 = s.f16 ? 1 : 0;
+  if (!configured[h16]) {
+    if (cudaFuncSetAttribute(h16 ? tc_step_kernel<STEP_BN, STEP_STAGES, 1>
+                                 : tc_step_kernel<STEP_BN, STEP_STAGES, 0>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::SMEM + STEP_SGD_BYTES) != cudaSuccess)
       return MLP_ERR_CUDA;
-    configured = true;
+    configured[h16] = true;
   }
   if (s.n_gemm < 0 || s.n_gemm > kStepMaxGemms || !bar_words) return MLP_ERR_INVALID_ARG;
   StepProgram prog;  // ~12 KiB of kernel parameters
@@ -1800,8 +1832,10 @@ mlp_status launch_step_program(const StepSpec& s, unsigned* bar_words, unsigned 
   for (int g = 0; g < s.n_gemm; ++g)
     flops += 2ll * s.gemm[g].M * s.gemm[g].N * s.gemm[g].K;
   LaunchScope ls("step_program", st, s.n_steps, flops, s.n_gemm);
-  if (cudaLaunchKernelEx(&cfg, tc_step_kernel<STEP_BN, STEP_STAGES>, prog) != cudaSuccess)
-    return MLP_ERR_CUDA;
+  const cudaError_t e =
+      h16 ? cudaLaunchKernelEx(&cfg, tc_step_kernel<STEP_BN, STEP_STAGES, 1>, prog)
+          : cudaLaunchKernelEx(&cfg, tc_step_kernel<STEP_BN, STEP_STAGES, 0>, prog);
+  if (e != cudaSuccess) return MLP_ERR_CUDA;
   return launch_status();
 }
 
@@ -1809,6 +1843,20 @@ size_t gemm_tc_splitk_bytes(int M, int N, int K) {
   const GemmPlan pl = gemm_plan(M, N, K, false);
   if (pl.splits <= 1) return 0;
   return (size_t)pl.splits * M * ((N + 3) / 4 * 4) * sizeof(float);
+}
+
+// The tile kernel for a planned GEMM, instantiated for its 16-bit format.
+template <int H16>
+mlp_status launch_tiles(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                        const TcParams& p, bool pair, int BN, cudaStream_t st) {
+  if (pair) return launch_pair<6, H16>(ta, tb, tc, p, st);
+  // short, narrow problems (the 784-256-10 step) need few stages
+  if (BN == 64 && p.k_blocks <= 16) return launch_bn<64, 4, H16>(ta, tb, tc, p, st);
+  switch (BN) {
+    case 64: return launch_bn<64, 8, H16>(ta, tb, tc, p, st);
+    case 128: return launch_bn<128, 6, H16>(ta, tb, tc, p, st);
+    default: return launch_bn<256, 4, H16>(ta, tb, tc, p, st);
+  }
 }
 
 mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStream_t st) {
@@ -1860,14 +1908,8 @@ mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStr
       return MLP_ERR_CUDA;
     p.tma_store = 1;
   }
-  if (pl.pair) return launch_pair<6>(ta, tb, tc, p, st);
-  // short, narrow problems (the 784-256-10 step) need few stages
-  if (BN == 64 && p.k_blocks <= 16) return launch_bn<64, 4>(ta, tb, tc, p, st);
-  switch (BN) {
-    case 64: return launch_bn<64, 8>(ta, tb, tc, p, st);
-    case 128: return launch_bn<128, 6>(ta, tb, tc, p, st);
-    default: return launch_bn<256, 4>(ta, tb, tc, p, st);
-  }
+  return p.f16 ? launch_tiles<1>(ta, tb, tc, p, pl.pair, BN, st)
+               : launch_tiles<0>(ta, tb, tc, p, pl.pair, BN, st);
 }
 
 }  // namespace mlp

@@ -21,24 +21,27 @@ struct SgdSegments {
 };
 
 // k_elementwise.cu
-mlp_status launch_sgd(float* w, const float* g, float* v, __nv_bfloat16* wb, long long n,
+// 16-bit buffers are bf16 or fp16: their format arguments (wb_fmt, dst_dtype,
+// dl_dtype, dtype) take the MLP_DTYPE_* codes, MLP_DTYPE_F32 (0) meaning
+// fp32 where a buffer may also be fp32.
+mlp_status launch_sgd(float* w, const float* g, float* v, void* wb, int wb_fmt, long long n,
                       float lr, float mom, const SgdSegments& segs, cudaStream_t st);
-mlp_status launch_shadow(const float* w, __nv_bfloat16* wb, long long n, const SgdSegments& segs,
-                         cudaStream_t st);
-mlp_status launch_cast_rows(const void* src, int src_dtype, void* dst, int dst_bf16, int rows,
+mlp_status launch_shadow(const float* w, void* wb, int wb_fmt, long long n,
+                         const SgdSegments& segs, cudaStream_t st);
+mlp_status launch_cast_rows(const void* src, int src_dtype, void* dst, int dst_dtype, int rows,
                             int cols, int ld_dst, cudaStream_t st);
 size_t xent_workspace_bytes(int B);
 mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, int C,
-                       float* loss_out, void* dlog, int dl_bf16, int ldd, int* argmax, void* ws,
+                       float* loss_out, void* dlog, int dl_dtype, int ldd, int* argmax, void* ws,
                        cudaStream_t st);
 size_t colsum_workspace_bytes(int rows, int cols);
-mlp_status launch_colsum(const void* X, int bf16, int rows, int cols, int ld, float* out,
+mlp_status launch_colsum(const void* X, int dtype, int rows, int cols, int ld, float* out,
                          void* ws, cudaStream_t st);
 size_t mse_ws_bytes(long long n);
 mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out, void* dy,
                       void* ws, cudaStream_t st);
 mlp_status launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st);
-// Sets column `col` of rows [0, rows) of each listed bf16 or fp32 matrix to 1
+// Sets column `col` of rows [0, rows) of each listed fp32 / bf16 / fp16 matrix to 1
 // (and the columns after it, up to ld, to 0): the ones column that lets a
 // weight-gradient GEMM produce the bias gradient as its last row.
 struct OnesCols {
@@ -47,7 +50,7 @@ struct OnesCols {
   int ld[9];
   int col[9];
 };
-mlp_status launch_ones_cols(const OnesCols& oc, int rows, int bf16, cudaStream_t st);
+mlp_status launch_ones_cols(const OnesCols& oc, int rows, int dtype, cudaStream_t st);
 
 // k_gemm_simt.cu: fp32 (or bf16-input) SIMT GEMM with the fused epilogue.
 struct GemmArgs {
@@ -56,7 +59,10 @@ struct GemmArgs {
   const void* B; int ldb; int b_trans;
   const float* bias; int act;
   const void* mask; int ldm;
-  void* C; int ldc; int c_bf16;
+  void* C; int ldc; int c_bf16;  // c_bf16: C is 16-bit (bf16, or fp16 when f16 is set)
+  // tensor-core path: A, B, the 16-bit outputs (C, xent_dlog, sgd_shadow) and
+  // the ReLU mask are fp16 instead of bf16
+  int f16 = 0;
   // optional scratch for split-K partial sums (tensor-core path only)
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -87,7 +93,8 @@ struct GemmArgs {
 mlp_status launch_gemm_simt(const GemmArgs& g, int in_bf16, cudaStream_t st);
 size_t gemm_simt_scratch_bytes();
 
-// k_gemm_tc.cu: tcgen05 bf16 GEMM (TMA-fed, fp32 accumulation in tensor memory).
+// k_gemm_tc.cu: tcgen05 bf16 / fp16 GEMM (TMA-fed, fp32 accumulation in tensor
+// memory).
 mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStream_t st);
 // Scratch bytes a split-K launch of this shape would use (0: no split).
 size_t gemm_tc_splitk_bytes(int M, int N, int K);
@@ -101,7 +108,8 @@ constexpr int kStepMaxGemms = 24;
 struct StepSpec {
   const void* cast_src = nullptr;
   int cast_dtype = 0;
-  void* cast_dst = nullptr;  // bf16 rows of pitch cast_ld
+  void* cast_dst = nullptr;  // 16-bit rows of pitch cast_ld (fp16 when f16 is set)
+  int f16 = 0;
   // Optional second input buffer (same shape) for programs of several steps:
   // step s then reads buffer s % 2, and step s + 1's input is cast during
   // step s (by the CTAs idle in its smallest GEMM phase) instead of in a

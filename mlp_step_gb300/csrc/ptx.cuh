@@ -397,5 +397,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with A and B both fp16 (format fields 0).  A and B of one
+// kind::f16 MMA always share their type.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <int H16>
+__host__ __device__ constexpr uint32_t idesc_16_f32(int M, int N, int a_mn, int b_mn) {
+  return H16 ? idesc_f16_f32(M, N, a_mn, b_mn) : idesc_bf16_f32(M, N, a_mn, b_mn);
+}
+
 }  // namespace ptx
 }  // namespace mlp

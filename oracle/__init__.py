@@ -43,6 +43,8 @@ def lib():
         L.orc_max_threads.restype = ctypes.c_int
         L.orc_round_bf16.restype = ctypes.c_double
         L.orc_round_bf16.argtypes = [ctypes.c_double]
+        L.orc_round_f16.restype = ctypes.c_double
+        L.orc_round_f16.argtypes = [ctypes.c_double]
         L.orc_param_count.restype = ctypes.c_longlong
         L.orc_param_count.argtypes = [_I, ctypes.c_int]
         L.orc_matmul.argtypes = [_D, ctypes.c_int, _D, ctypes.c_int, ctypes.c_longlong,
@@ -117,6 +119,22 @@ def round_bf16(v: float) -> float:
     return lib().orc_round_bf16(float(v))
 
 
+def round_f16(v: float) -> float:
+    """Nearest IEEE binary16 value of v (ties to even, subnormals, overflow to
+    infinity), as a float."""
+    return lib().orc_round_f16(float(v))
+
+
+def _points(bf16_points=False, points=None):
+    """Rounding-points code of the oracle's MLP functions: 0 exact, 1 bf16
+    points, 2 fp16 points (points: None, 0/1/2, "bf16" or "f16")."""
+    if points is None:
+        return 1 if bf16_points else 0
+    if isinstance(points, str):
+        return {"exact": 0, "bf16": 1, "f16": 2, "fp16": 2}[points]
+    return int(points)
+
+
 def param_count(dims) -> int:
     d, n = _dims(dims)
     return lib().orc_param_count(d, n)
@@ -145,7 +163,7 @@ def matmul_entries(A, B, ii, jj, a_t=False, b_t=False):
     return out
 
 
-def mlp_forward(dims, params, X, bf16_points=False):
+def mlp_forward(dims, params, X, bf16_points=False, points=None):
     """Returns (list of hidden activations, logits Z)."""
     params, X = _d(params), _d(X)
     B = X.shape[0]
@@ -153,7 +171,7 @@ def mlp_forward(dims, params, X, bf16_points=False):
     acts = np.empty(max(n_act, 1))
     Z = np.empty((B, dims[-1]))
     d, n = _dims(dims)
-    lib().orc_mlp_forward(d, n, _p(params, _D), _p(X, _D), B, int(bf16_points),
+    lib().orc_mlp_forward(d, n, _p(params, _D), _p(X, _D), B, _points(bf16_points, points),
                           _p(acts, _D), _p(Z, _D))
     hs, off = [], 0
     for l in range(1, len(dims) - 1):
@@ -176,7 +194,7 @@ def softmax_xent(Z, y, B_norm=None):
     return loss[0], rl, dZ, am
 
 
-def mlp_backward(dims, params, X, hs, dZ, bf16_points=False, want_dx=False):
+def mlp_backward(dims, params, X, hs, dZ, bf16_points=False, want_dx=False, points=None):
     params, X, dZ = _d(params), _d(X), _d(dZ)
     B = X.shape[0]
     acts = _d(np.concatenate([h.ravel() for h in hs])) if hs else np.zeros(1)
@@ -184,7 +202,7 @@ def mlp_backward(dims, params, X, hs, dZ, bf16_points=False, want_dx=False):
     dX = np.empty_like(X) if want_dx else None
     d, n = _dims(dims)
     lib().orc_mlp_backward(d, n, _p(params, _D), _p(X, _D), B, _p(acts, _D), _p(dZ, _D),
-                           int(bf16_points), _p(g, _D), _p(dX, _D))
+                           _points(bf16_points, points), _p(g, _D), _p(dX, _D))
     return (g, dX) if want_dx else g
 
 
@@ -202,7 +220,7 @@ def sgd_momentum(w, g, v, lr, momentum):
     return w, v
 
 
-def mlp_train_step(dims, params, velocity, X, y, lr, momentum, bf16_points=False):
+def mlp_train_step(dims, params, velocity, X, y, lr, momentum, bf16_points=False, points=None):
     """One step; returns (loss, new params, new velocity, grads)."""
     p, v = _d(params).copy(), _d(velocity).copy()
     X = _d(X)
@@ -210,17 +228,18 @@ def mlp_train_step(dims, params, velocity, X, y, lr, momentum, bf16_points=False
     g = np.empty(p.size)
     d, n = _dims(dims)
     loss = lib().orc_mlp_train_step(d, n, _p(p, _D), _p(v, _D), _p(X, _D), _p(y, _I),
-                                    X.shape[0], lr, momentum, int(bf16_points), _p(g, _D))
+                                    X.shape[0], lr, momentum, _points(bf16_points, points),
+                                    _p(g, _D))
     return loss, p, v, g
 
 
-def mlp_forward_rows(dims, params, X, rows, bf16_points=False):
+def mlp_forward_rows(dims, params, X, rows, bf16_points=False, points=None):
     params, X = _f(params), _f(X)
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     Z = np.empty((len(rows), dims[-1]))
     d, n = _dims(dims)
     lib().orc_mlp_forward_rows_f32(d, n, _p(params, _F), _p(X, _F), _p(rows, _L), len(rows),
-                                   int(bf16_points), _p(Z, _D))
+                                   _points(bf16_points, points), _p(Z, _D))
     return Z
 
 

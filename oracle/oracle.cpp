@@ -30,10 +30,13 @@
 //   * flat stack parameter order per block: W_gate [d][h], then W_down [h][d];
 //   * MSE is the mean over all T*d elements.
 //
-// Optional "bf16 points" mode rounds (round-to-nearest-even to 8 significant
-// bits) exactly where a bf16 tensor-core path stores a bf16 operand: the input
-// X, the weights, the stored hidden activation H, and the gradients dZ / dH fed
-// to the backward matrix multiplies.  Everything else stays fp64.
+// Optional rounding-points modes round exactly where a tensor-core path stores
+// a 16-bit operand: the input X, the weights, the stored hidden activation H,
+// and the gradients dZ / dH fed to the backward matrix multiplies.  Everything
+// else stays fp64.  points = 1 ("bf16 points") rounds to nearest-even with 8
+// significant bits; points = 2 ("fp16 points", the FP16-operand choice of
+// [vk]) rounds to the nearest IEEE binary16 value (11 significant bits,
+// subnormals below 2^-14, overflow to infinity).  points = 0 is exact.
 
 #include <cmath>
 #include <cstdint>
@@ -61,7 +64,26 @@ double orc_round_bf16(double v) {
   return std::ldexp(q, e - 8);
 }
 
-static inline double maybe_bf16(double v, int on) { return on ? orc_round_bf16(v) : v; }
+// Round a double to the nearest IEEE 754 binary16 value, ties to even:
+// 11 significant bits for |v| >= 2^-14 (the smallest normal), a fixed step of
+// 2^-24 below it (subnormals), and +-infinity once the rounded magnitude
+// exceeds the largest finite value 65504.  Used only in fp16-points mode.
+double orc_round_f16(double v) {
+  if (v == 0.0 || !std::isfinite(v)) return v;
+  const double a = std::fabs(v);
+  int e = 0;
+  std::frexp(a, &e);                  // a = f * 2^e, 0.5 <= f < 1
+  int step = e - 11;                  // exponent of the spacing at a
+  if (step < -24) step = -24;         // subnormal spacing
+  const double r = std::ldexp(std::nearbyint(std::ldexp(a, -step)), step);
+  const double out = r > 65504.0 ? INFINITY : r;
+  return std::copysign(out, v);
+}
+
+// points: 0 exact, 1 bf16, 2 fp16 (see the header comment).
+static inline double maybe_round(double v, int points) {
+  return points == 1 ? orc_round_bf16(v) : (points == 2 ? orc_round_f16(v) : v);
+}
 
 // [cap] "Predict the profile": the 784-256-10 network has 203,530 parameters;
 // each layer holds an [in][out] weight and an [out] bias.
@@ -124,25 +146,25 @@ static long long weight_offset(const int* dims, int l) {
 // but the last applies ReLU (deeper MLPs repeat the hidden layer).
 // acts receives H_1 .. H_{L-1} back to back, each [B][dims[l]].
 void orc_mlp_forward(const int* dims, int n_dims, const double* params,
-                     const double* X, long long B, int bf16_points,
+                     const double* X, long long B, int points,
                      double* acts, double* Z) {
   const int L = n_dims - 1;
   std::vector<double> in((size_t)B * dims[0]);
-  for (size_t i = 0; i < in.size(); ++i) in[i] = maybe_bf16(X[i], bf16_points);
+  for (size_t i = 0; i < in.size(); ++i) in[i] = maybe_round(X[i], points);
   long long act_off = 0;
   for (int l = 0; l < L; ++l) {
     const int fi = dims[l], fo = dims[l + 1];
     const double* W = params + weight_offset(dims, l);
     const double* b = W + (long long)fi * fo;
     std::vector<double> Wr((size_t)fi * fo);
-    for (size_t i = 0; i < Wr.size(); ++i) Wr[i] = maybe_bf16(W[i], bf16_points);
+    for (size_t i = 0; i < Wr.size(); ++i) Wr[i] = maybe_round(W[i], points);
     std::vector<double> out((size_t)B * fo);
     orc_matmul(in.data(), 0, Wr.data(), 0, B, fo, fi, out.data());
     const bool last = (l == L - 1);
     for (long long r = 0; r < B; ++r)
       for (int c = 0; c < fo; ++c) {
         double v = out[r * fo + c] + b[c];
-        if (!last) v = maybe_bf16(v > 0.0 ? v : 0.0, bf16_points);
+        if (!last) v = maybe_round(v > 0.0 ? v : 0.0, points);
         out[r * fo + c] = v;
       }
     if (last) {
@@ -190,12 +212,12 @@ void orc_softmax_xent(const double* Z, const int* y, long long B, int C, long lo
 // grads has the flat parameter layout.  dX may be null.
 void orc_mlp_backward(const int* dims, int n_dims, const double* params,
                       const double* X, long long B, const double* acts,
-                      const double* dZ, int bf16_points, double* grads, double* dX) {
+                      const double* dZ, int points, double* grads, double* dX) {
   const int L = n_dims - 1;
   std::vector<long long> act_off(L, 0);
   for (int l = 1; l < L; ++l) act_off[l] = (l == 1 ? 0 : act_off[l - 1] + B * dims[l - 1]);
   std::vector<double> dY((size_t)B * dims[L]);
-  for (size_t i = 0; i < dY.size(); ++i) dY[i] = maybe_bf16(dZ[i], bf16_points);
+  for (size_t i = 0; i < dY.size(); ++i) dY[i] = maybe_round(dZ[i], points);
   for (int l = L - 1; l >= 0; --l) {
     const int fi = dims[l], fo = dims[l + 1];
     const double* W = params + weight_offset(dims, l);
@@ -203,7 +225,7 @@ void orc_mlp_backward(const int* dims, int n_dims, const double* params,
     double* db = dW + (long long)fi * fo;
     std::vector<double> in((size_t)B * fi);
     if (l == 0) {
-      for (size_t i = 0; i < in.size(); ++i) in[i] = maybe_bf16(X[i], bf16_points);
+      for (size_t i = 0; i < in.size(); ++i) in[i] = maybe_round(X[i], points);
     } else {
       std::memcpy(in.data(), acts + act_off[l], in.size() * sizeof(double));
     }
@@ -215,7 +237,7 @@ void orc_mlp_backward(const int* dims, int n_dims, const double* params,
     }
     if (l == 0 && dX == nullptr) break;
     std::vector<double> Wr((size_t)fi * fo);
-    for (size_t i = 0; i < Wr.size(); ++i) Wr[i] = maybe_bf16(W[i], bf16_points);
+    for (size_t i = 0; i < Wr.size(); ++i) Wr[i] = maybe_round(W[i], points);
     std::vector<double> dIn((size_t)B * fi);
     orc_matmul(dY.data(), 0, Wr.data(), 1, B, fi, fo, dIn.data());
     if (l == 0) {
@@ -224,7 +246,7 @@ void orc_mlp_backward(const int* dims, int n_dims, const double* params,
     }
     const double* H = acts + act_off[l];
     for (size_t i = 0; i < dIn.size(); ++i)
-      dIn[i] = maybe_bf16(H[i] > 0.0 ? dIn[i] : 0.0, bf16_points);
+      dIn[i] = maybe_round(H[i] > 0.0 ? dIn[i] : 0.0, points);
     dY.swap(dIn);
   }
 }
@@ -254,18 +276,18 @@ void orc_sgd_momentum(double* w, const double* g, double* v, long long n,
 // gradient; acts/Z/dZ are internal.
 double orc_mlp_train_step(const int* dims, int n_dims, double* params, double* velocity,
                           const double* X, const int* y, long long B, double lr,
-                          double momentum, int bf16_points, double* grads_out) {
+                          double momentum, int points, double* grads_out) {
   const int L = n_dims - 1;
   long long n_act = 0;
   for (int l = 1; l < L; ++l) n_act += B * dims[l];
   std::vector<double> acts((size_t)std::max<long long>(n_act, 1));
   std::vector<double> Z((size_t)B * dims[L]), dZ((size_t)B * dims[L]);
-  orc_mlp_forward(dims, n_dims, params, X, B, bf16_points, acts.data(), Z.data());
+  orc_mlp_forward(dims, n_dims, params, X, B, points, acts.data(), Z.data());
   double loss = 0.0;
   orc_softmax_xent(Z.data(), y, B, dims[L], B, &loss, nullptr, dZ.data(), nullptr);
   const long long P = orc_param_count(dims, n_dims);
   std::vector<double> g((size_t)P);
-  orc_mlp_backward(dims, n_dims, params, X, B, acts.data(), dZ.data(), bf16_points,
+  orc_mlp_backward(dims, n_dims, params, X, B, acts.data(), dZ.data(), points,
                    g.data(), nullptr);
   if (grads_out) std::memcpy(grads_out, g.data(), (size_t)P * sizeof(double));
   orc_sgd_momentum(params, g.data(), velocity, P, lr, momentum);
@@ -276,13 +298,13 @@ double orc_mlp_train_step(const int* dims, int n_dims, double* params, double* v
 // activations of the listed rows) for selected rows of a large batch.
 void orc_mlp_forward_rows_f32(const int* dims, int n_dims, const float* params,
                               const float* X, const long long* rows, long long n_rows,
-                              int bf16_points, double* Z_rows) {
+                              int points, double* Z_rows) {
   const int L = n_dims - 1;
 #pragma omp parallel for schedule(dynamic, 1)
   for (long long e = 0; e < n_rows; ++e) {
     std::vector<double> in(dims[0]);
     for (int i = 0; i < dims[0]; ++i)
-      in[i] = maybe_bf16((double)X[rows[e] * dims[0] + i], bf16_points);
+      in[i] = maybe_round((double)X[rows[e] * dims[0] + i], points);
     for (int l = 0; l < L; ++l) {
       const int fi = dims[l], fo = dims[l + 1];
       const float* W = params + weight_offset(dims, l);
@@ -290,11 +312,11 @@ void orc_mlp_forward_rows_f32(const int* dims, int n_dims, const float* params,
       std::vector<double> out(fo, 0.0);
       for (int c = 0; c < fo; ++c) {
         double acc = 0.0;
-        for (int k = 0; k < fi; ++k) acc += in[k] * maybe_bf16((double)W[(long long)k * fo + c], bf16_points);
+        for (int k = 0; k < fi; ++k) acc += in[k] * maybe_round((double)W[(long long)k * fo + c], points);
         out[c] = acc + (double)b[c];
       }
       if (l < L - 1)
-        for (int c = 0; c < fo; ++c) out[c] = maybe_bf16(out[c] > 0.0 ? out[c] : 0.0, bf16_points);
+        for (int c = 0; c < fo; ++c) out[c] = maybe_round(out[c] > 0.0 ? out[c] : 0.0, points);
       in.swap(out);
     }
     for (int c = 0; c < dims[L]; ++c) Z_rows[e * dims[L] + c] = in[c];

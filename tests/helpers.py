@@ -9,6 +9,17 @@ def bf16_values(a):
         .double().numpy()
 
 
+def f16_values(a):
+    """float64 copy of a float array after rounding to IEEE binary16."""
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.float16) \
+        .double().numpy()
+
+
+def values16(a, dtype):
+    """float64 copy of a float array after rounding to the 16-bit torch dtype."""
+    return f16_values(a) if dtype == torch.float16 else bf16_values(a)
+
+
 def to_dev(a, dtype=None):
     t = torch.from_numpy(np.ascontiguousarray(a))
     if dtype is not None:

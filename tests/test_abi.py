@@ -66,6 +66,12 @@ def test_create_rejects_bad_arguments(lib):
     need = M.mlp_workspace_bytes([784, 256, 10], 128, 0)
     bad = ctypes.c_void_p(0x10004)
     assert lib.mlp_create(d, 3, 1, 0, 128, bad, fake, fake, None, fake, need, ctypes.byref(h)) == 2
+    # the 16-bit tensor-core precisions need the weight shadow
+    need16 = M.mlp_workspace_bytes([784, 256, 10], 128, M.MLP_PREC_FP16)
+    assert need16 == M.mlp_workspace_bytes([784, 256, 10], 128, M.MLP_PREC_BF16) > 0
+    for prec in (M.MLP_PREC_BF16, M.MLP_PREC_FP16):
+        assert lib.mlp_create(d, 3, 1, prec, 128, fake, fake, fake, None, fake, need16,
+                              ctypes.byref(h)) == 1
     # unknown precision / activation
     assert lib.mlp_create(d, 3, 1, 7, 128, fake, fake, fake, None, fake, need, ctypes.byref(h)) == 1
     assert lib.mlp_create(d, 3, 9, 0, 128, fake, fake, fake, None, fake, need, ctypes.byref(h)) == 1
@@ -82,6 +88,15 @@ def test_gemm_rejects_bad_arguments(lib):
     assert lib.mlp_gemm(4, 8, 8, fake, 8, 0, fake, 8, 0, 1, None, 5, None, 0, fake, 8, 0, None) == 1
     # empty problem: OK, nothing launched
     assert lib.mlp_gemm(0, 8, 8, None, 8, 0, None, 8, 0, 1, None, 0, None, 0, None, 8, 0, None) == 0
+    # 16-bit outputs take the operands' 16-bit type: fp16 in -> bf16 out and
+    # bf16 in -> fp16 out are rejected; an fp16 row pitch must be 16-byte aligned
+    F16, BF16 = M.MLP_DTYPE_F16, M.MLP_DTYPE_BF16
+    assert lib.mlp_gemm(4, 8, 8, fake, 8, 0, fake, 8, 0, F16, None, 0, None, 0, fake, 8, BF16,
+                        None) == 1
+    assert lib.mlp_gemm(4, 8, 8, fake, 8, 0, fake, 8, 0, BF16, None, 0, None, 0, fake, 8, F16,
+                        None) == 1
+    assert lib.mlp_gemm(4, 8, 10, fake, 10, 0, fake, 8, 0, F16, None, 0, None, 0, fake, 8, F16,
+                        None) == 2
 
 
 def test_other_entry_points_reject_bad_arguments(lib):

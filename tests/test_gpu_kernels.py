@@ -8,7 +8,7 @@ import torch
 import oracle
 import mlp_step_gb300 as M
 from mlp_step_gb300 import synth
-from helpers import bf16_values, to_dev, rel_to_max, assert_elementwise, near_tie_rows
+from helpers import values16, bf16_values, to_dev, rel_to_max, assert_elementwise, near_tie_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -89,6 +89,16 @@ def test_xent_bf16_dlogits():
     assert rel_to_max(dl[:, :C], dZ_ref) <= 4e-3
 
 
+@pytest.mark.parametrize("B,C", [(128, 10), (300, 1000)])
+def test_xent_f16_dlogits(B, C):
+    Z = synth.normal_f32((B, C), synth.STREAM_GENERIC, std=3.0)
+    y = synth.labels(B, C, seed=17)
+    _, dl, _ = _xent_case(B, C, Z, y, torch.float16)
+    _, _, dZ_ref, _ = oracle.softmax_xent(Z.astype(np.float64), y)
+    # fp16: 11 significant bits, subnormal below 2^-14 (dZ carries 1 / B)
+    assert_elementwise(dl[:, :C], dZ_ref, 1e-3, 2.0 ** -24, "dZ")
+
+
 def test_xent_extreme_logits_pm60():
     # "Capstone 5", "Read the worked reference": logits at +/-60 must give
     # finite loss and gradients; closed forms per row (k entries at +60).
@@ -111,7 +121,8 @@ def test_xent_extreme_logits_pm60():
 
 @pytest.mark.parametrize("rows,cols,dtype", [(128, 10, torch.float32), (128, 256, torch.bfloat16),
                                              (16384, 1000, torch.bfloat16), (3, 5, torch.float32),
-                                             (1, 64, torch.bfloat16), (5000, 333, torch.float32)])
+                                             (1, 64, torch.bfloat16), (5000, 333, torch.float32),
+                                             (16384, 1000, torch.float16), (7, 13, torch.float16)])
 def test_colsum_matches_oracle(rows, cols, dtype):
     X = synth.normal_f32((rows, cols), synth.STREAM_GENERIC)
     Xd = to_dev(X, dtype)
@@ -148,23 +159,25 @@ def test_gemm_fp32_matches_oracle(shape, a_t, b_t):
 # ------------------------------------------------------------------ GEMM (bf16 tcgen05)
 
 def _tc_case(M_, N, K, a_t, b_t, bias=False, act=M.MLP_ACT_NONE, mask=False, out_bf16=False,
-             seed=0):
+             seed=0, h16=torch.bfloat16):
+    """One tensor-core GEMM with 16-bit operands of type h16 (bf16 or fp16);
+    out_bf16 selects a 16-bit output of the same type."""
     A, B = _operands(M_, N, K, a_t, b_t, seed)
-    Ad, Bd = to_dev(A, torch.bfloat16), to_dev(B, torch.bfloat16)
+    Ad, Bd = to_dev(A, h16), to_dev(B, h16)
     bvec = synth.normal_f32((N,), synth.STREAM_GENERIC + 5) if bias else None
     mk = synth.normal_f32((M_, N), synth.STREAM_GENERIC + 6) if mask else None
-    C = torch.full((M_, N), float("nan"), dtype=torch.bfloat16 if out_bf16 else torch.float32,
+    C = torch.full((M_, N), float("nan"), dtype=h16 if out_bf16 else torch.float32,
                    device="cuda")
     M.mlp_gemm(Ad, Bd, C, M_, N, K, a_trans=a_t, b_trans=b_t,
                bias=to_dev(bvec) if bias else None, act=act,
-               mask=to_dev(mk, torch.bfloat16) if mask else None)
-    ref = oracle.matmul(bf16_values(A), bf16_values(B), a_t=bool(a_t), b_t=bool(b_t))
+               mask=to_dev(mk, h16) if mask else None)
+    ref = oracle.matmul(values16(A, h16), values16(B, h16), a_t=bool(a_t), b_t=bool(b_t))
     if bias:
         ref = ref + bvec
     if act == M.MLP_ACT_RELU:
         ref = np.maximum(ref, 0.0)
     if mask:
-        ref = np.where(bf16_values(mk) > 0, ref, 0.0)
+        ref = np.where(values16(mk, h16) > 0, ref, 0.0)
     return C.float().cpu().numpy(), ref
 
 
@@ -208,6 +221,37 @@ def test_gemm_bf16_tc_large_ragged_outputs(shape, out_bf16):
     got, ref = _tc_case(M_, N, K, 0, 0, bias=True, act=M.MLP_ACT_RELU, out_bf16=out_bf16)
     assert np.all(np.isfinite(got)), "unwritten outputs"
     assert rel_to_max(got, ref) <= (8e-3 if out_bf16 else 1e-5)
+
+
+@pytest.mark.parametrize("a_t,b_t", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("shape", [(128, 256, 784), (300, 200, 136), (1, 16, 8), (256, 10, 128),
+                                   (2304, 1536, 200), (2100, 1803, 72)])
+def test_gemm_f16_tc_matches_oracle(shape, a_t, b_t):
+    """fp16 operands ("The Debugging Lesson Was Numerical": FP16 in, FP32
+    accumulate) through the same single-CTA and CTA-pair kernels."""
+    M_, N, K = shape
+    if (not a_t and K % 8) or (a_t and M_ % 8) or (not b_t and N % 8) or (b_t and K % 8):
+        pytest.skip("fp16 rows must be 16-byte aligned for TMA")
+    got, ref = _tc_case(M_, N, K, a_t, b_t, h16=torch.float16)
+    assert np.all(np.isfinite(got)), "unwritten outputs"
+    assert rel_to_max(got, ref) <= 1e-5, rel_to_max(got, ref)
+
+
+@pytest.mark.parametrize("bias,act,mask,out16", [(True, M.MLP_ACT_RELU, False, True),
+                                                 (False, M.MLP_ACT_NONE, True, True),
+                                                 (True, M.MLP_ACT_NONE, False, False)])
+def test_gemm_f16_tc_epilogues(bias, act, mask, out16):
+    got, ref = _tc_case(333, 520, 200, 0, 0, bias=bias, act=act, mask=mask, out_bf16=out16,
+                        h16=torch.float16)
+    # fp16 output: 11 significant bits
+    assert rel_to_max(got, ref) <= (1e-3 if out16 else 1e-5)
+    if mask:
+        mk = synth.normal_f32((333, 520), synth.STREAM_GENERIC + 6)
+        assert np.all(got[values16(mk, torch.float16) <= 0] == 0)
+    # large outputs leave through TMA bulk stores in the fp16 format
+    got, ref = _tc_case(2100, 1800, 72, 0, 0, bias=True, act=M.MLP_ACT_RELU, out_bf16=out16,
+                        h16=torch.float16)
+    assert rel_to_max(got, ref) <= (1e-3 if out16 else 1e-5)
 
 
 def test_gemm_bf16_tc_k_zero_gives_bias():

@@ -11,7 +11,7 @@ import torch
 import oracle
 import mlp_step_gb300 as M
 from mlp_step_gb300 import synth
-from helpers import bf16_values, to_dev, rel_to_max, assert_elementwise, near_tie_rows
+from helpers import bf16_values, f16_values, to_dev, rel_to_max, assert_elementwise, near_tie_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -111,6 +111,82 @@ def test_bf16_step_matches_oracle(B):
     W2 = net.params[200960:200960 + 2560].view(256, 10)
     S2 = net.shadow[784 * 256:].view(256, 16)
     assert torch.equal(S2[:, :10], W2.to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("B", [128, 112])
+def test_f16_step_matches_oracle(B):
+    """The fp16-operand variant ("The Debugging Lesson Was Numerical": FP16 in,
+    FP32 accumulate) against the oracle rounding at the same points to binary16."""
+    p0 = synth.mlp_flat_params(DIMS)
+    xb = synth.images_u8(B, 784)
+    y = synth.labels(B, 10)
+    net = M.MLP(DIMS, prec=M.MLP_PREC_FP16, max_batch=128, params=torch.from_numpy(p0))
+    loss = torch.zeros(1, device="cuda")
+    am = torch.empty(B, dtype=torch.int32, device="cuda")
+    net.train_step(to_dev(xb), to_dev(y), LR, MOM, loss_out=loss, argmax_out=am)
+    torch.cuda.synchronize()
+    Xh = f16_values(_x_values(xb))
+    l_ref, p_ref, v_ref, g_ref = oracle.mlp_train_step(DIMS, p0.astype(np.float64),
+                                                       np.zeros(p0.size), Xh, y, LR, MOM,
+                                                       points="f16")
+    assert abs(loss.item() - l_ref) <= 1e-3
+    for (name, got), (_, ref) in zip(_segments(DIMS, net.grads.cpu().numpy()),
+                                     _segments(DIMS, g_ref)):
+        assert rel_to_max(got, ref) <= 3e-2, name
+    assert rel_to_max(net.params.cpu().numpy() - p0, p_ref - p0) <= 3e-2
+    # predictions of the step's forward, where the top two logits are apart
+    hs, Z = oracle.mlp_forward(DIMS, p0.astype(np.float64), Xh, points="f16")
+    ok = ~near_tie_rows(Z, rel=1e-2)
+    assert np.array_equal(am.cpu().numpy()[ok], np.argmax(Z, 1)[ok])
+    # the fp16 shadow is the rounded fp32 master weight
+    W1 = net.params[:784 * 256].view(784, 256)
+    S1 = net.shadow[:784 * 256].view(784, 256)
+    assert S1.dtype == torch.float16 and torch.equal(S1, W1.to(torch.float16))
+    W2 = net.params[200960:200960 + 2560].view(256, 10)
+    S2 = net.shadow[784 * 256:].view(256, 16)
+    assert torch.equal(S2[:, :10], W2.to(torch.float16))
+
+
+def test_f16_step_matches_unfused_sequence_and_epoch():
+    """fp16 networks run the same step program; the separate calls (forward,
+    loss with fp16 dZ, backward, SGD) give the same step, and an epoch equals
+    its steps in sequence bit for bit."""
+    B, n = 128, 3 * 128 + 40
+    p0 = synth.mlp_flat_params(DIMS)
+    p0[200704:200960] = synth.normal_f32((256,), synth.STREAM_GENERIC, std=0.1)  # nonzero b1
+    xb = to_dev(synth.images_u8(n, 784))
+    y = to_dev(synth.labels(n, 10))
+    fused = M.MLP(DIMS, prec=M.MLP_PREC_FP16, max_batch=B, params=torch.from_numpy(p0))
+    loss_f = torch.zeros(4, device="cuda")
+    for _ in range(2):
+        fused.train_step(xb[:B], y[:B], LR, MOM, loss_out=loss_f)
+    seq = M.MLP(DIMS, prec=M.MLP_PREC_FP16, max_batch=B, params=torch.from_numpy(p0))
+    logits = torch.empty(B, 10, device="cuda")
+    dl = torch.empty(B, 16, dtype=torch.float16, device="cuda")
+    loss_s = torch.zeros(4, device="cuda")
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        seq.forward(xb[:B], logits)
+        M.softmax_xent_fwd_bwd(logits, y[:B], loss_s, dlogits=dl, workspace=ws)
+        seq.backward(dl, B)
+        seq.sgd_step(LR, MOM)
+    torch.cuda.synchronize()
+    assert abs(loss_f[0].item() - loss_s[0].item()) <= 1e-6 * abs(loss_s[0].item())
+    assert torch.allclose(fused.grads, seq.grads, rtol=1e-5, atol=1e-9)
+    assert torch.allclose(fused.params, seq.params, rtol=1e-6, atol=1e-8)
+    ep = M.MLP(DIMS, prec=M.MLP_PREC_FP16, max_batch=B, params=torch.from_numpy(p0))
+    losses = torch.zeros(4, device="cuda")
+    ep.train_epoch(xb, y, LR, MOM, B, losses_out=losses)
+    sq = M.MLP(DIMS, prec=M.MLP_PREC_FP16, max_batch=B, params=torch.from_numpy(p0))
+    loss_q = torch.zeros(4, 4, device="cuda")
+    for s_ in range(4):
+        a, b = s_ * B, min(n, (s_ + 1) * B)
+        sq.train_step(xb[a:b], y[a:b], LR, MOM, loss_out=loss_q[s_])
+    torch.cuda.synchronize()
+    assert torch.equal(losses, loss_q[:, 0])
+    for name in ("params", "velocity", "grads", "shadow"):
+        assert torch.equal(getattr(ep, name), getattr(sq, name)), name
+    assert M.get_device_status() == M.MLP_OK
 
 
 def test_bf16_fused_step_matches_unfused_sequence():

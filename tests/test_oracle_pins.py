@@ -36,6 +36,47 @@ def test_bf16_rounding_matches_library():
     assert oracle.round_bf16(1 + 3 * 2 ** -8) == 1 + 2 ** -6
 
 
+def test_f16_rounding_matches_library_and_binary16_edges():
+    # numpy converts float64 to IEEE binary16 in one correctly rounded step
+    mag = np.exp(4.0 * synth.normal(9, synth.STREAM_GENERIC + 1, 20000))
+    x = synth.normal(9, synth.STREAM_GENERIC, 20000) * mag
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).astype(np.float64)
+    got = np.array([oracle.round_f16(float(v)) for v in x])
+    assert np.array_equal(got, want)
+    assert np.isinf(got).any() and (np.abs(got[got != 0]) < 2.0 ** -14).any()  # both ends hit
+    # values fixed by the binary16 format: largest finite 65504 = (2 - 2^-10) 2^15;
+    # halfway to the next step (65520) rounds to infinity; subnormal step 2^-24
+    assert oracle.round_f16(65504.0) == 65504.0
+    assert oracle.round_f16(65519.99) == 65504.0
+    assert oracle.round_f16(65520.0) == math.inf
+    assert oracle.round_f16(-65520.0) == -math.inf
+    assert oracle.round_f16(2.0 ** -24) == 2.0 ** -24
+    assert oracle.round_f16(2.0 ** -25) == 0.0               # tie between 0 and 2^-24: even
+    assert oracle.round_f16(3 * 2.0 ** -25) == 2.0 ** -23    # tie between 2^-24 and 2^-23
+    assert oracle.round_f16(1 + 2.0 ** -11) == 1.0            # ties to even above 1
+    assert oracle.round_f16(1 + 3 * 2.0 ** -11) == 1 + 2.0 ** -9
+    assert oracle.round_f16(1.0 / 3.0) == 1365.0 / 4096.0     # 0x3555
+
+
+def test_rounding_points_modes_round_where_the_formats_differ():
+    """With identity weights the logits are the inputs.  1 + 2^-9 has 10
+    significant bits: binary16 holds it (fp16 points agree with exact mode),
+    bf16 does not (8 bits: it becomes 1).  1 + 2^-12 fits neither."""
+    dims = [2, 2, 2]
+    params = np.zeros(oracle.param_count(dims))
+    params[0:4] = [1, 0, 0, 1]        # W1 = I
+    params[6:10] = [1, 0, 0, 1]       # W2 = I
+    X = np.array([[1 + 2.0 ** -9, 1 + 2.0 ** -12]])
+    _, z_exact = oracle.mlp_forward(dims, params, X)
+    _, z_f16 = oracle.mlp_forward(dims, params, X, points="f16")
+    _, z_bf16 = oracle.mlp_forward(dims, params, X, points="bf16")
+    assert z_exact[0].tolist() == [1 + 2.0 ** -9, 1 + 2.0 ** -12]
+    assert z_f16[0].tolist() == [1 + 2.0 ** -9, 1.0]
+    assert z_bf16[0].tolist() == [1.0, 1.0]
+    assert oracle.mlp_forward(dims, params, X, bf16_points=True)[1].tolist() == z_bf16.tolist()
+
+
 # ------------------------------------------------------------ GEMM
 
 @pytest.mark.parametrize("a_t,b_t", [(0, 0), (1, 0), (0, 1), (1, 1)])
