@@ -17,15 +17,20 @@
  *         "What Worked", "What Didn't Work".
  *   [vk]  "The Work Moved Down a Layer" -- "Cooperation Beats Isolation",
  *         "Keep state resident", "The Debugging Lesson Was Numerical".
+ *   [hv]  "HIP + Vulkan backends -- Phase 3 (path to 100%)" -- "Vulkan /
+ *         SPIR-V", "Phase-3 bug hunt" (linear-order sums for bit parity
+ *         with a CPU oracle).
  *
  * Conventions for every call:
  *   - All tensors are caller-owned DEVICE memory (the library allocates
  *     nothing), row-major and contiguous along the last dimension, with the
  *     leading dimension given where one is taken.  Base pointers must be
  *     16-byte aligned (MLP_ERR_MISALIGNED otherwise); leading dimensions of
- *     bf16 operands of the tensor-core path must make rows 16-byte aligned.
+ *     bf16 / fp16 operands of the tensor-core path must make rows 16-byte
+ *     aligned.
  *   - Weights are [in][out] (the X * W orientation of [cap] "The minimum
- *     model").  bf16 means IEEE bfloat16 rounded to nearest even from fp32.
+ *     model").  bf16 means bfloat16 rounded to nearest even from fp32, fp16
+ *     IEEE binary16 rounded to nearest even.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
  *     enqueue work: no host synchronisation, no allocation, no host copies, so
  *     a whole step can be captured into a CUDA graph.
@@ -89,6 +94,26 @@ mlp_status mlp_get_device_status(void* stream);
  * the GPU's global timer (0 restores the default of 2 s, far above any
  * legitimate wait).  Host-side setting, passed to kernels at launch. */
 void mlp_set_wait_limit_ns(long long ns);
+
+/* Summation order of the fp32 reductions that the library controls (the
+ * linear-order sums of [hv] "Vulkan / SPIR-V" and "Phase-3 bug hunt": a
+ * fixed, plain left-to-right order, so that a CPU loop summing the same way
+ * reproduces the result bit for bit).
+ *   MLP_ORDER_FAST (default): fp32 SIMT GEMMs may split K over CTAs (partial
+ *     sums added in split order) and column sums reduce in chunks and trees;
+ *     results are deterministic run to run.
+ *   MLP_ORDER_LINEAR: every fp32 SIMT GEMM output is ONE fused-multiply-add
+ *     chain over k = 0, 1, ..., K-1 starting from 0, then + bias (one fp32
+ *     add), then the activation and mask; every column sum adds the rows
+ *     r = 0, 1, ... into one fp32 accumulator starting from 0.  Slower (no
+ *     split-K, one thread per column).
+ * The tensor-core MMAs accumulate in the hardware's order in either mode, and
+ * the loss uses IEEE exp and log; neither is covered.  Host-side setting,
+ * read at each launch. */
+#define MLP_ORDER_FAST 0
+#define MLP_ORDER_LINEAR 1
+mlp_status mlp_set_reduction_order(int order);
+int mlp_get_reduction_order(void);
 
 /* Self-test of the bounded-wait mechanism: launches one block that waits on a
  * shared-memory barrier nothing arrives at, for `limit_ns` nanoseconds, then

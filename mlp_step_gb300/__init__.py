@@ -18,7 +18,7 @@ __all__ = [
     "MlpError", "load", "lib_path",
     "MLP_ACT_NONE", "MLP_ACT_RELU", "MLP_ACT_LEAKY_RELU_SQ",
     "MLP_PREC_FP32", "MLP_PREC_BF16", "MLP_PREC_FP16", "MLP_DTYPE_F32", "MLP_DTYPE_BF16",
-    "MLP_DTYPE_U8", "MLP_DTYPE_F16",
+    "MLP_DTYPE_U8", "MLP_DTYPE_F16", "MLP_ORDER_FAST", "MLP_ORDER_LINEAR",
 ]
 
 MLP_OK = 0
@@ -39,6 +39,8 @@ MLP_DTYPE_F32 = 0
 MLP_DTYPE_BF16 = 1
 MLP_DTYPE_U8 = 2
 MLP_DTYPE_F16 = 3
+MLP_ORDER_FAST = 0
+MLP_ORDER_LINEAR = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_HERE, "libmlp_step.so")
@@ -55,6 +57,8 @@ SIGNATURES = {
     "mlp_status_string": (ctypes.c_char_p, [_i]),
     "mlp_get_device_status": (_i, [_vp]),
     "mlp_set_wait_limit_ns": (None, [_ll]),
+    "mlp_set_reduction_order": (_i, [_i]),
+    "mlp_get_reduction_order": (_i, []),
     "mlp_selftest_wait_timeout": (_i, [_ll, _vp]),
     "mlp_launch_count": (ctypes.c_ulonglong, []),
     "mlp_timing_enable": (_i, [_i]),
@@ -163,6 +167,15 @@ def get_device_status(stream=None) -> int:
 
 def set_wait_limit_ns(ns: int) -> None:
     load().mlp_set_wait_limit_ns(int(ns))
+
+
+def set_reduction_order(order: int) -> None:
+    """MLP_ORDER_FAST or MLP_ORDER_LINEAR (see mlp_step.h)."""
+    _check(load().mlp_set_reduction_order(int(order)), "mlp_set_reduction_order")
+
+
+def get_reduction_order() -> int:
+    return load().mlp_get_reduction_order()
 
 
 def selftest_wait_timeout(limit_ns: int, stream=None) -> None:

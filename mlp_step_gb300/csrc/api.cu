@@ -53,6 +53,9 @@ bool pdl_enabled() {
 static unsigned long long g_wait_limit_ns = 0;
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 
+static int g_reduction_order = MLP_ORDER_FAST;
+bool linear_order() { return g_reduction_order == MLP_ORDER_LINEAR; }
+
 unsigned long long wait_limit_ns() {
   return g_wait_limit_ns ? g_wait_limit_ns : kDefaultWaitNs;
 }
@@ -202,6 +205,14 @@ mlp_status mlp_get_device_status(void* stream) {
 }
 
 void mlp_set_wait_limit_ns(long long ns) { g_wait_limit_ns = ns > 0 ? (unsigned long long)ns : 0; }
+
+mlp_status mlp_set_reduction_order(int order) {
+  if (order != MLP_ORDER_FAST && order != MLP_ORDER_LINEAR) return MLP_ERR_INVALID_ARG;
+  g_reduction_order = order;
+  return MLP_OK;
+}
+
+int mlp_get_reduction_order(void) { return g_reduction_order; }
 
 mlp_status mlp_selftest_wait_timeout(long long limit_ns, void* stream) {
   if (limit_ns <= 0) return MLP_ERR_INVALID_ARG;

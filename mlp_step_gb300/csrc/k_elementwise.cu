@@ -658,6 +658,23 @@ __global__ void colsum_pass2_kernel(const float* __restrict__ partial, int chunk
   out[c] = t;
 }
 
+// Linear-order form (MLP_ORDER_LINEAR): thread c adds rows 0, 1, ..., rows-1
+// of column c into one fp32 accumulator, the plain loop a CPU would run; the
+// warp's 32 columns are read together, so each row step is one coalesced
+// load per warp.
+template <typename T>
+__global__ void __launch_bounds__(128) colsum_linear_kernel(const T* __restrict__ X, int rows,
+                                                            int cols, int ld,
+                                                            float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  float s = 0.f;
+  for (int r = 0; r < rows; ++r) s += ldf(X + (size_t)r * ld + c);
+  out[c] = s;
+}
+
 void colsum_plan(int rows, int cols, int* chunks, int* rows_per_chunk) {
   (void)cols;
   int ch = (rows + 511) / 512;
@@ -695,6 +712,20 @@ void launch_colsum_t(const T* X, int rows, int cols, int ld, int ch, int rpc, fl
 mlp_status launch_colsum(const void* X, int dtype, int rows, int cols, int ld, float* out,
                          void* ws, cudaStream_t st) {
   if (cols <= 0) return MLP_OK;
+  if (linear_order()) {
+    LaunchScope ls("colsum_linear", st, rows, cols);
+    const dim3 g((cols + 127) / 128);
+    if (dtype == MLP_DTYPE_BF16)
+      launch_k(colsum_linear_kernel<__nv_bfloat16>, g, dim3(128), 0, st,
+               static_cast<const __nv_bfloat16*>(X), rows, cols, ld, out);
+    else if (dtype == MLP_DTYPE_F16)
+      launch_k(colsum_linear_kernel<__half>, g, dim3(128), 0, st, static_cast<const __half*>(X),
+               rows, cols, ld, out);
+    else
+      launch_k(colsum_linear_kernel<float>, g, dim3(128), 0, st, static_cast<const float*>(X),
+               rows, cols, ld, out);
+    return launch_status();
+  }
   int ch, rpc;
   colsum_plan(rows, cols, &ch, &rpc);
   float* dst = ch > 1 ? static_cast<float*>(ws) : out;

@@ -276,8 +276,10 @@ size_t gemm_simt_scratch_bytes() {
 
 // K splits of an fp32 GEMM: when its tiles leave most SMs idle, K is cut so
 // that about one CTA per SM runs (each split at least two 16-deep steps);
-// needs the split-K scratch in g.ws (counters zero between launches).
+// needs the split-K scratch in g.ws (counters zero between launches).  Never
+// in the linear-order mode.
 static int simt_splits(const GemmArgs& g, int tiles) {
+  if (linear_order()) return 1;  // one FMA chain over all of K per output
   if (!g.ws || g.ws_bytes < gemm_simt_scratch_bytes() || (reinterpret_cast<uintptr_t>(g.ws) & 15))
     return 1;
   if (tiles >= num_sms() || tiles > kSimtCounters) return 1;

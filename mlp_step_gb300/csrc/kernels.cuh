@@ -145,6 +145,8 @@ mlp_status launch_rmsnorm_bwd(const void* dnp, const void* x, const void* dy, co
 
 // Host helpers (api.cu)
 unsigned long long wait_limit_ns();
+// MLP_ORDER_LINEAR in effect (mlp_set_reduction_order)?
+bool linear_order();
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, unsigned long long inner,
                          unsigned long long outer, unsigned long long row_stride_bytes,
                          unsigned box_inner, unsigned box_outer);

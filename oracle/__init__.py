@@ -45,6 +45,12 @@ def lib():
         L.orc_round_bf16.argtypes = [ctypes.c_double]
         L.orc_round_f16.restype = ctypes.c_double
         L.orc_round_f16.argtypes = [ctypes.c_double]
+        L.orc_matmul_f32_linear.argtypes = [_F, ctypes.c_int, _F, ctypes.c_int,
+                                            ctypes.c_longlong, ctypes.c_longlong,
+                                            ctypes.c_longlong, _F, ctypes.c_int, _F,
+                                            ctypes.c_longlong, _F]
+        L.orc_colsum_f32_linear.argtypes = [_F, ctypes.c_longlong, ctypes.c_longlong,
+                                            ctypes.c_longlong, _F]
         L.orc_param_count.restype = ctypes.c_longlong
         L.orc_param_count.argtypes = [_I, ctypes.c_int]
         L.orc_matmul.argtypes = [_D, ctypes.c_int, _D, ctypes.c_int, ctypes.c_longlong,
@@ -204,6 +210,30 @@ def mlp_backward(dims, params, X, hs, dZ, bf16_points=False, want_dx=False, poin
     lib().orc_mlp_backward(d, n, _p(params, _D), _p(X, _D), B, _p(acts, _D), _p(dZ, _D),
                            _points(bf16_points, points), _p(g, _D), _p(dX, _D))
     return (g, dX) if want_dx else g
+
+
+def matmul_f32_linear(A, B, a_t=False, b_t=False, bias=None, act=0, mask=None):
+    """fp32 C = act(chain + bias) with each chain one fused-multiply-add
+    sequence over ascending k (the linear-order mode); mask keeps C > 0 cells.
+    A is [M][K] (a_t False) or [K][M]; B is [K][N] (b_t False) or [N][K]."""
+    A, B = _f(A), _f(B)
+    Mr, K = (A.shape[1], A.shape[0]) if a_t else A.shape
+    N = B.shape[0] if b_t else B.shape[1]
+    C = np.empty((Mr, N), dtype=np.float32)
+    bias = None if bias is None else _f(bias)
+    mask = None if mask is None else _f(mask)
+    lib().orc_matmul_f32_linear(_p(A, _F), int(a_t), _p(B, _F), int(b_t), Mr, N, K,
+                                _p(bias, _F), int(act), _p(mask, _F),
+                                0 if mask is None else mask.shape[1], _p(C, _F))
+    return C
+
+
+def colsum_f32_linear(X):
+    """fp32 column sums, rows added in ascending order from 0."""
+    X = _f(X)
+    out = np.empty(X.shape[1], dtype=np.float32)
+    lib().orc_colsum_f32_linear(_p(X, _F), X.shape[0], X.shape[1], X.shape[1], _p(out, _F))
+    return out
 
 
 def colsum(X):

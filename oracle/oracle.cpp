@@ -261,6 +261,49 @@ void orc_colsum_f32(const float* X, long long rows, long long cols, long long ld
   }
 }
 
+// ---------------------------------------------------------------- linear order
+// The linear-order fp32 forms ([hv] "HIP + Vulkan backends -- Phase 3 (path
+// to 100%)", "Vulkan / SPIR-V" and "Phase-3 bug hunt": sum left to right, one
+// element after another, so that a device sum made in the same order agrees
+// bit for bit).  These two are fp32 by definition, not fp64: they state the
+// exact sequence of single-precision operations a linear-order sum performs.
+
+// C[m][n] = act(chain + bias[n]) where chain = fma(a_{K-1}, b_{K-1}, ... fma(a_0,
+// b_0, 0)), every step one correctly rounded single-precision fused
+// multiply-add; bias (nullable) is one fp32 add; act 1 = ReLU (max with 0);
+// mask (nullable, [M][ldm]) keeps C where mask > 0.  A is [M][K] (a_t = 0) or
+// [K][M]; B is [K][N] (b_t = 0) or [N][K].
+void orc_matmul_f32_linear(const float* A, int a_t, const float* B, int b_t, long long M,
+                           long long N, long long K, const float* bias, int act,
+                           const float* mask, long long ldm, float* C) {
+#pragma omp parallel for schedule(static)
+  for (long long m = 0; m < M; ++m) {
+    for (long long n = 0; n < N; ++n) {
+      float acc = 0.0f;
+      for (long long k = 0; k < K; ++k) {
+        const float a = a_t ? A[k * M + m] : A[m * K + k];
+        const float b = b_t ? B[n * K + k] : B[k * N + n];
+        acc = std::fma(a, b, acc);
+      }
+      float v = acc;
+      if (bias) v = v + bias[n];
+      if (act == 1) v = v > 0.0f ? v : 0.0f;
+      if (mask && !(mask[m * ldm + n] > 0.0f)) v = 0.0f;
+      C[m * N + n] = v;
+    }
+  }
+}
+
+// out[c] = ((X[0][c] + X[1][c]) + X[2][c]) + ... in fp32, starting from 0.
+void orc_colsum_f32_linear(const float* X, long long rows, long long cols, long long ld,
+                           float* out) {
+  for (long long c = 0; c < cols; ++c) {
+    float s = 0.0f;
+    for (long long r = 0; r < rows; ++r) s = s + X[r * ld + c];
+    out[c] = s;
+  }
+}
+
 // [cap] "Read the worked reference": momentum SGD over one flat buffer,
 // v <- momentum * v - lr * g;  w <- w + v.
 void orc_sgd_momentum(double* w, const double* g, double* v, long long n,

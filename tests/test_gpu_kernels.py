@@ -282,3 +282,44 @@ def test_bounded_wait_times_out_cleanly():
     assert M.get_device_status() == M.MLP_OK  # cleared, context still usable
     x = torch.ones(4, device="cuda")
     assert x.sum().item() == 4.0
+
+
+# ------------------------------------------------------------------ linear order
+
+@pytest.fixture
+def linear_order():
+    M.set_reduction_order(M.MLP_ORDER_LINEAR)
+    yield
+    M.set_reduction_order(M.MLP_ORDER_FAST)
+
+
+@pytest.mark.parametrize("a_t,b_t", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("shape", [(128, 256, 784), (67, 33, 129), (785, 256, 128), (1, 10, 256)])
+def test_gemm_fp32_linear_order_is_bit_exact(shape, a_t, b_t, linear_order):
+    """MLP_ORDER_LINEAR ("HIP + Vulkan backends -- Phase 3", "Phase-3 bug
+    hunt": linear-order sums for bit parity): each output is one fused
+    multiply-add chain over ascending k, + bias, ReLU, mask -- the oracle's
+    fp32 chain to the bit (these shapes split K in the default mode)."""
+    M_, N, K = shape
+    A, B = _operands(M_, N, K, a_t, b_t)
+    bias = synth.normal_f32((N,), synth.STREAM_GENERIC + 5)
+    mk = synth.normal_f32((M_, N), synth.STREAM_GENERIC + 6)
+    C = torch.full((M_, N), float("nan"), device="cuda")
+    M.mlp_gemm(to_dev(A), to_dev(B), C, M_, N, K, a_trans=a_t, b_trans=b_t, bias=to_dev(bias),
+               act=M.MLP_ACT_RELU, mask=to_dev(mk))
+    want = oracle.matmul_f32_linear(A, B, a_t=a_t, b_t=b_t, bias=bias, act=1, mask=mk)
+    got = C.cpu().numpy()
+    assert np.array_equal(got, want), np.abs(got - want).max()
+
+
+@pytest.mark.parametrize("rows,cols,dtype", [(16384, 1000, torch.float32), (5000, 333, torch.float32),
+                                             (128, 256, torch.bfloat16), (7, 13, torch.float16)])
+def test_colsum_linear_order_is_bit_exact(rows, cols, dtype, linear_order):
+    X = synth.normal_f32((rows, cols), synth.STREAM_GENERIC)
+    Xd = to_dev(X, dtype)
+    out = torch.empty(cols, device="cuda")
+    ws = torch.empty(max(M.mlp_colsum_workspace_bytes(rows, cols), 16), dtype=torch.uint8,
+                     device="cuda")
+    M.mlp_colsum(Xd, out, workspace=ws)
+    want = oracle.colsum_f32_linear(Xd.float().cpu().numpy())
+    assert np.array_equal(out.cpu().numpy(), want)

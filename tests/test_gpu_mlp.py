@@ -386,3 +386,38 @@ def test_overfit_32_on_gpu():
         final = torch.zeros(1, device="cuda")
         M.softmax_xent_fwd_bwd(logits, y, final, workspace=ws)
         assert final.item() < 0.01, (prec, final.item())
+
+
+def test_fp32_forward_backward_linear_order_is_bit_exact():
+    """In MLP_ORDER_LINEAR the fp32 path's forward logits and backward
+    gradients are chains of fp32 fused multiply-adds in ascending order, so
+    the oracle's linear-order GEMMs composed layer by layer give them to the
+    bit ("HIP + Vulkan backends -- Phase 3": bit parity through linear-order
+    sums)."""
+    B = 128
+    p0 = synth.mlp_flat_params(DIMS)
+    p0[200704:200960] = synth.normal_f32((256,), synth.STREAM_GENERIC, std=0.1)  # nonzero b1
+    xb = synth.images_u8(B, 784)
+    dZ = synth.normal_f32((B, 10), synth.STREAM_GENERIC + 3, std=0.01)
+    M.set_reduction_order(M.MLP_ORDER_LINEAR)
+    try:
+        net = M.MLP(DIMS, prec=M.MLP_PREC_FP32, max_batch=B, params=torch.from_numpy(p0))
+        logits = torch.empty(B, 10, device="cuda")
+        net.forward(to_dev(xb), logits)
+        net.backward(to_dev(dZ), B)
+        torch.cuda.synchronize()
+    finally:
+        M.set_reduction_order(M.MLP_ORDER_FAST)
+    X = _x_values(xb)
+    W1, b1 = p0[:200704].reshape(784, 256), p0[200704:200960]
+    W2, b2 = p0[200960:203520].reshape(256, 10), p0[203520:]
+    H = oracle.matmul_f32_linear(X, W1, bias=b1, act=1)
+    Z = oracle.matmul_f32_linear(H, W2, bias=b2)
+    assert np.array_equal(logits.cpu().numpy(), Z)
+    ones = np.ones((B, 1), dtype=np.float32)
+    g2 = oracle.matmul_f32_linear(np.hstack([H, ones]), dZ, a_t=1)          # [dW2; db2]
+    dH = oracle.matmul_f32_linear(dZ, W2, b_t=1, mask=H)                      # (dZ W2^T) * (H > 0)
+    g1 = oracle.matmul_f32_linear(np.hstack([X, ones]), dH, a_t=1)          # [dW1; db1]
+    g = net.grads.cpu().numpy()
+    assert np.array_equal(g[:200960].reshape(785, 256), g1)
+    assert np.array_equal(g[200960:].reshape(257, 10), g2)

@@ -79,6 +79,39 @@ def test_rounding_points_modes_round_where_the_formats_differ():
 
 # ------------------------------------------------------------ GEMM
 
+def test_linear_f32_matmul_is_one_fused_chain_per_output():
+    """The linear-order fp32 GEMM: one fused multiply-add chain over ascending
+    k per output.  With a = [1, 1 + 2^-12] and b = [-(1 + 2^-11), 1 + 2^-12]
+    the exact dot product is 2^-24; the chain's second step fma((1 + 2^-12)^2,
+    -(1 + 2^-11)) keeps it, while rounding the product first (a tie at half an
+    ulp of 1, to even) would give 0."""
+    a = np.array([[1.0, 1 + 2.0 ** -12]], dtype=np.float32)
+    b = np.array([[-(1 + 2.0 ** -11)], [1 + 2.0 ** -12]], dtype=np.float32)
+    assert oracle.matmul_f32_linear(a, b)[0, 0] == np.float32(2.0 ** -24)
+    # integer operands: every partial sum is an integer below 2^24, exact in
+    # fp32, so the chain equals the fp64 product for every operand layout
+    M_, N, K = 5, 7, 9
+    A = np.floor(synth.uniform01(3, synth.STREAM_GENERIC, M_ * K) * 19 - 9).reshape(M_, K)
+    B = np.floor(synth.uniform01(3, synth.STREAM_GENERIC + 1, K * N) * 19 - 9).reshape(K, N)
+    bias = np.floor(synth.uniform01(3, synth.STREAM_GENERIC + 2, N) * 9 - 4)
+    mask = np.floor(synth.uniform01(3, synth.STREAM_GENERIC + 3, M_ * N) * 3 - 1).reshape(M_, N)
+    want = np.where(mask > 0, np.maximum(A @ B + bias, 0.0), 0.0)
+    for a_t in (0, 1):
+        for b_t in (0, 1):
+            got = oracle.matmul_f32_linear(A.T if a_t else A, B.T if b_t else B, a_t=a_t,
+                                           b_t=b_t, bias=bias, act=1, mask=mask)
+            assert np.array_equal(got, want), (a_t, b_t)
+
+
+def test_linear_f32_colsum_adds_rows_in_ascending_order():
+    """1 + 1e8 rounds back to 1e8 in fp32 (ulp 8), so adding [1, 1e8, -1e8]
+    from the top gives 0 although the exact sum is 1 (from the bottom: 1)."""
+    X = np.array([[1.0, -3.0], [1e8, 2.0], [-1e8, 5.0]], dtype=np.float32)
+    assert oracle.colsum_f32_linear(X).tolist() == [0.0, 4.0]
+    Xi = np.floor(synth.uniform01(4, synth.STREAM_GENERIC, 300 * 7) * 201 - 100).reshape(300, 7)
+    assert np.array_equal(oracle.colsum_f32_linear(Xi), Xi.sum(0))
+
+
 @pytest.mark.parametrize("a_t,b_t", [(0, 0), (1, 0), (0, 1), (1, 1)])
 def test_matmul_matches_library(a_t, b_t):
     M, N, K = 7, 5, 11
