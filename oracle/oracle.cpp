@@ -7,7 +7,8 @@
 //
 // Every function is the plain definition of what it computes, written out with
 // explicit loops in fp64 (summation in index order; OpenMP splits only
-// independent outputs, never a sum).  Sources, by page and section:
+// independent outputs, never a sum), except the two linear-order functions,
+// which state an exact sequence of fp32 operations.  Sources, by page and section:
 //
 //   [cap]  "Capstone 5: train a network with your CUDA kernels" (Day 100):
 //          "The minimum model", "Work through the backward pass",
@@ -17,6 +18,8 @@
 //          "What Worked" (RMSNorm -> gate -> LeakyReLU^2 -> down -> residual).
 //   [vk]   "The Work Moved Down a Layer": "The Debugging Lesson Was Numerical"
 //          (bf16/fp16 operands, fp32 accumulation, fp32 epilogue).
+//   [hv]   "HIP + Vulkan backends -- Phase 3 (path to 100%)": "Vulkan /
+//          SPIR-V", "Phase-3 bug hunt" (left-to-right sums for bit parity).
 //
 // Readings where the pages are silent (each also listed in the design notes):
 //   * loss is the mean over the batch, so dZ carries 1/B;
