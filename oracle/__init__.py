@@ -51,6 +51,13 @@ def lib():
                                             ctypes.c_longlong, _F]
         L.orc_colsum_f32_linear.argtypes = [_F, ctypes.c_longlong, ctypes.c_longlong,
                                             ctypes.c_longlong, _F]
+        L.orc_attn_prep.argtypes = [_D, _D, _D, ctypes.c_longlong, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_longlong,
+                                    ctypes.c_double, ctypes.c_double, _D]
+        L.orc_attn_prep_rows_f32.argtypes = [_F, _F, _F, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_longlong, ctypes.c_double, ctypes.c_double,
+                                             _L, ctypes.c_longlong, _D]
         L.orc_param_count.restype = ctypes.c_longlong
         L.orc_param_count.argtypes = [_I, ctypes.c_int]
         L.orc_matmul.argtypes = [_D, ctypes.c_int, _D, ctypes.c_int, ctypes.c_longlong,
@@ -349,3 +356,27 @@ def stack_fwd_bwd(x0, params, n_blocks, d, h, eps, slope, target):
     loss = lib().orc_stack_fwd_bwd(_p(x0, _D), _p(params, _D), n_blocks, T, d, h, eps, slope,
                                    _p(target, _D), _p(g, _D), _p(dx0, _D))
     return loss, g, dx0
+
+
+def attn_prep(x, W, q_gain, n_q, n_kv, hd, rope_dims, seq_len, eps=1e-6, theta=10000.0):
+    """Fused attention preprocessing of every token: RMSNorm, QKV projection,
+    QK norm, partial RoPE, q gain; returns [T][(n_q + 2 n_kv) hd]."""
+    x, W, g = _d(x), _d(W), _d(q_gain)
+    T, d = x.shape
+    out = np.empty((T, (n_q + 2 * n_kv) * hd))
+    lib().orc_attn_prep(_p(x, _D), _p(W, _D), _p(g, _D), T, d, n_q, n_kv, hd, rope_dims,
+                        seq_len, eps, theta, _p(out, _D))
+    return out
+
+
+def attn_prep_rows(x, W, q_gain, rows, n_q, n_kv, hd, rope_dims, seq_len, eps=1e-6,
+                   theta=10000.0):
+    """attn_prep for the listed rows only (fp32 inputs as stored)."""
+    x, W, g = _f(x), _f(W), _f(q_gain)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((len(rows), (n_q + 2 * n_kv) * hd))
+    lib().orc_attn_prep_rows_f32(_p(x, _F), _p(W, _F), _p(g, _F), x.shape[1], n_q, n_kv, hd,
+                                 rope_dims, seq_len, eps, theta, _p(rows, _L), len(rows),
+                                 _p(out, _D))
+    return out
+

@@ -572,4 +572,77 @@ double orc_stack_fwd_bwd(const double* x0, const double* params, int n_blocks, l
   return loss;
 }
 
+// ---------------------------------------------------------------- attention prep
+// [mk] "What Worked" (attention preprocessing fusion) and "What Didn't Work"
+// (the fully fused form: RMSNorm -> QKV projection -> QK norm -> RoPE -> gain,
+// achievable in raw CUDA).  Per token t at position p = t mod seq_len:
+//   r = 1 / sqrt(mean_i x_i^2 + eps);  u = r (x W_qkv)      (RMSNorm, gain 1)
+//   u splits into n_q query heads, n_kv key heads, n_kv value heads of hd;
+//   query and key heads:  u_h <- u_h / sqrt(mean_j u_hj^2 + eps)   (QK norm)
+//                         partial RoPE on dims [0, R): for i < R/2,
+//                           a = p theta^(-2i/R),
+//                           (u_i, u_{i+R/2}) <- (u_i cos a - u_{i+R/2} sin a,
+//                                                u_{i+R/2} cos a + u_i sin a)
+//   query heads:          u_h <- q_gain[h] u_h
+//   value heads:          unchanged.
+// x [T][d], W [d][N] with N = (n_q + 2 n_kv) hd, out [T][N].
+static void attn_prep_token(const double* x, const double* W, const double* q_gain, int d,
+                            int n_q, int n_kv, int hd, int R, long long pos, double eps,
+                            double theta, double* out) {
+  const int N = (n_q + 2 * n_kv) * hd;
+  double ss = 0.0;
+  for (int i = 0; i < d; ++i) ss += x[i] * x[i];
+  const double r = 1.0 / std::sqrt(ss / d + eps);
+  for (int n = 0; n < N; ++n) {
+    double acc = 0.0;
+    for (int i = 0; i < d; ++i) acc += x[i] * W[(long long)i * N + n];
+    out[n] = r * acc;
+  }
+  for (int h = 0; h < n_q + n_kv; ++h) {
+    double* u = out + (long long)h * hd;
+    double hs = 0.0;
+    for (int j = 0; j < hd; ++j) hs += u[j] * u[j];
+    const double inv = 1.0 / std::sqrt(hs / hd + eps);
+    for (int j = 0; j < hd; ++j) u[j] *= inv;
+    for (int i = 0; i < R / 2; ++i) {
+      const double a = (double)pos * std::pow(theta, -2.0 * i / R);
+      const double c = std::cos(a), s = std::sin(a);
+      const double x1 = u[i], x2 = u[i + R / 2];
+      u[i] = x1 * c - x2 * s;
+      u[i + R / 2] = x2 * c + x1 * s;
+    }
+    if (h < n_q)
+      for (int j = 0; j < hd; ++j) u[j] *= q_gain[h];
+  }
+}
+
+void orc_attn_prep(const double* x, const double* W, const double* q_gain, long long T, int d,
+                   int n_q, int n_kv, int hd, int R, long long seq_len, double eps,
+                   double theta, double* out) {
+  const int N = (n_q + 2 * n_kv) * hd;
+#pragma omp parallel for schedule(static)
+  for (long long t = 0; t < T; ++t)
+    attn_prep_token(x + t * d, W, q_gain, d, n_q, n_kv, hd, R, t % seq_len, eps, theta,
+                    out + t * N);
+}
+
+// The same for the listed tokens only (x and W in fp32, as stored; outputs
+// fp64), for spot checks of large problems.
+void orc_attn_prep_rows_f32(const float* x, const float* W, const float* q_gain, int d, int n_q,
+                            int n_kv, int hd, int R, long long seq_len, double eps,
+                            double theta, const long long* rows, long long n_rows,
+                            double* out) {
+  const int N = (n_q + 2 * n_kv) * hd;
+  std::vector<double> Wd((size_t)d * N), g(n_q > 0 ? n_q : 1);
+  for (size_t i = 0; i < Wd.size(); ++i) Wd[i] = W[i];
+  for (int h = 0; h < n_q; ++h) g[h] = q_gain[h];
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long long e = 0; e < n_rows; ++e) {
+    std::vector<double> xr(d);
+    for (int i = 0; i < d; ++i) xr[i] = x[rows[e] * d + i];
+    attn_prep_token(xr.data(), Wd.data(), g.data(), d, n_q, n_kv, hd, R, rows[e] % seq_len, eps,
+                    theta, out + e * N);
+  }
+}
+
 }  // extern "C"

@@ -475,3 +475,71 @@ def test_stack_fd():
         xm = x0.copy(); xm[idx] -= hh
         fd = (L(params, xp) - L(params, xm)) / (2 * hh)
         assert abs(dx0[idx] - fd) <= 1e-8 + 1e-5 * abs(fd)
+
+
+# ------------------------------------------------------------ attention preprocessing
+
+def _attn_dims():
+    return dict(n_q=2, n_kv=1, hd=64, rope_dims=16, seq_len=5)
+
+
+def test_attn_prep_rope_closed_form():
+    """RMSNorm -> QKV -> QK norm -> partial RoPE -> q gain ("Full-Depth MLP
+    Megakernel + Fused Attention Preprocessing", "What Worked" / "What Didn't
+    Work") on a case with a closed form: x = ones(4) (r = 1 with eps 0), q head
+    u = e_0, k head u = e_1, v head u = 2 e_0.  The QK norm scales a unit
+    vector of a 64-wide head to 8; RoPE over R = 4 dims pairs (0, 2) at
+    frequency 1 and (1, 3) at frequency theta^(-1/2) = 0.01."""
+    d, hd, R = 4, 64, 4
+    W = np.zeros((d, 3 * hd))
+    W[:, 0] = 0.25             # q dim 0
+    W[:, hd + 1] = 0.25        # k dim 1
+    W[:, 2 * hd] = 0.5         # v dim 0
+    T = 4
+    x = np.ones((T, d))
+    out = oracle.attn_prep(x, W, np.array([1.5]), 1, 1, hd, R, seq_len=100, eps=0.0)
+    for p in range(T):
+        q, k, v = out[p, :hd], out[p, hd:2 * hd], out[p, 2 * hd:]
+        want_q = np.zeros(hd)
+        want_q[0], want_q[2] = 8 * math.cos(p), 8 * math.sin(p)
+        want_k = np.zeros(hd)
+        want_k[1], want_k[3] = 8 * math.cos(0.01 * p), 8 * math.sin(0.01 * p)
+        want_v = np.zeros(hd)
+        want_v[0] = 2.0
+        assert np.allclose(q, 1.5 * want_q, rtol=0, atol=1e-12)
+        assert np.allclose(k, want_k, rtol=0, atol=1e-12)
+        assert np.array_equal(v, want_v)
+
+
+def test_attn_prep_invariants_and_library_special_cases():
+    dm = _attn_dims()
+    n_q, n_kv, hd = dm["n_q"], dm["n_kv"], dm["hd"]
+    T, d = 11, 32
+    N = (n_q + 2 * n_kv) * hd
+    x = synth.normal(5, synth.STREAM_GENERIC, T * d).reshape(T, d)
+    W = synth.normal(5, synth.STREAM_GENERIC + 1, d * N).reshape(d, N) * 0.2
+    gain = np.array([0.5, 1.75])
+    out = oracle.attn_prep(x, W, gain, eps=0.0, **dm)
+    # RMSNorm makes the block invariant to a positive scale of x
+    assert np.allclose(oracle.attn_prep(3.0 * x, W, gain, eps=0.0, **dm), out, rtol=1e-12,
+                       atol=1e-12)
+    # value heads: r (x W)_v, a plain matrix product
+    r = 1.0 / np.sqrt((x * x).mean(1))
+    u = r[:, None] * (x @ W)
+    assert np.allclose(out[:, (n_q + n_kv) * hd:], u[:, (n_q + n_kv) * hd:], rtol=1e-12)
+    # RoPE rotates pairs, so every query head keeps RMS |gain| and every key head RMS 1
+    for h in range(n_q + n_kv):
+        rms = np.sqrt((out[:, h * hd:(h + 1) * hd] ** 2).mean(1))
+        assert np.allclose(rms, gain[h] if h < n_q else 1.0, rtol=1e-12)
+    # at position 0 (tokens 0 and seq_len) nothing rotates: normalised head x gain
+    for t in (0, dm["seq_len"], 2 * dm["seq_len"]):
+        for h in range(n_q + n_kv):
+            uh = u[t, h * hd:(h + 1) * hd]
+            want = uh / np.sqrt((uh * uh).mean()) * (gain[h] if h < n_q else 1.0)
+            assert np.allclose(out[t, h * hd:(h + 1) * hd], want, rtol=1e-12)
+    # the sampled-rows form (fp32 inputs as stored) agrees with the full form
+    rows = np.array([3, 7, 10])
+    got = oracle.attn_prep_rows(x.astype(np.float32), W.astype(np.float32), gain, rows, **dm)
+    ref = oracle.attn_prep(x.astype(np.float32).astype(np.float64),
+                           W.astype(np.float32).astype(np.float64), gain, eps=1e-6, **dm)[rows]
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
