@@ -13,6 +13,8 @@ Workloads (synthetic, seeded inputs; see synth.py):
   block         one RMSNorm -> gate -> LeakyReLU^2 -> down -> residual block, fwd + bwd,
                 65,536 tokens x 512
   stack         11 such blocks over 262,144 tokens, MSE loss, fwd + bwd + momentum SGD
+  attn_prep     fused attention preprocessing (RMSNorm -> QKV -> QK norm -> RoPE -> gain),
+                65,536 tokens x 512, 8 query / 4 key-value heads of 64
 
 A bench "step" is one pass of the whole training step of the workload over its
 batch (for mlp784_epoch: the whole epoch).  The timed region is K steps, each
@@ -155,6 +157,12 @@ def algorithmic_work(name):
     if base.startswith("block_bwd_act"):
         T, d, h = sh
         return "tensor", 2.0 * T * d * h      # dA = dY W_down^T; the u recompute is not credited
+    if base.startswith("attn_prep_gemm"):
+        M_, N, K = sh
+        return "tensor", 2.0 * M_ * N * K     # the QKV projection; the epilogue is not credited
+    if base == "row_rstd":
+        T, d = sh[0], sh[1]
+        return "hbm", 2.0 * T * d + 4.0 * T
     if base == "rmsnorm_bwd":
         return "hbm", 4100.0 * sh[0]          # per token: dn', x, dy, dx bf16 + rstd
     if base == "sgd":
@@ -609,6 +617,104 @@ class BlockStep(Workload):
         return done, dt, "%d oracle block fwd+bwd passes over %d tokens (fp64)" % (n, T)
 
 
+class AttnPrep(Workload):
+    """Fused attention preprocessing over 65,536 tokens: RMSNorm -> QKV
+    projection -> QK norm -> partial RoPE -> q gain."""
+    name = "attn_prep"
+    unit = "tokens/s"
+    dtype = "bf16"
+
+    def __init__(self, T=65536, seq_len=1024, n_q=8, n_kv=4, rope_dims=32):
+        self.T, self.d, self.L = T, 512, seq_len
+        self.n_q, self.n_kv, self.R = n_q, n_kv, rope_dims
+        self.N = (n_q + 2 * n_kv) * 64
+        self.samples_per_step = T
+        self.config = {"workload": "fused attention preprocessing: x[%d tokens, 512] bf16 N(0,1) "
+                                   "(%d sequences of %d), RMSNorm (eps 1e-6, gain 1) -> W_qkv "
+                                   "512x%d (%d query, %d key, %d value heads of 64, N(0, 512^-1/2)) "
+                                   "-> QK RMSNorm -> rotate-half RoPE on %d of 64 dims (base "
+                                   "10000) -> q gain U(0.5, 1.5); forward only"
+                                   % (T, T // seq_len, seq_len, self.N, n_q, n_kv, n_kv,
+                                      rope_dims),
+                       "tokens": T, "d": 512, "n_q_heads": n_q, "n_kv_heads": n_kv,
+                       "head_dim": 64, "rope_dims": rope_dims, "seq_len": seq_len,
+                       "cuda_graph": True, "l2": "flushed between timed steps (256 MiB write)"}
+
+    def setup(self):
+        import torch
+        import mlp_step_gb300 as M
+        from mlp_step_gb300 import synth
+        self.M = M
+        bf = torch.bfloat16
+        self.x_host = torch.from_numpy(synth.normal_f32((self.T, self.d),
+                                                        synth.STREAM_GENERIC + 40)).to(bf)
+        self.x_host = self.x_host.pin_memory()
+        self.x = self.x_host.cuda()
+        self.w = torch.from_numpy(synth.normal_f32((self.d, self.N), synth.STREAM_GENERIC + 41,
+                                                   std=self.d ** -0.5)).to(bf).cuda()
+        self.gain = torch.from_numpy(synth.uniform_f32((self.n_q,), synth.STREAM_GENERIC + 42,
+                                                       lo=0.5, hi=1.5)).cuda()
+        self.out = torch.empty(self.T, self.N, dtype=bf, device="cuda")
+        self.r = torch.empty(self.T, device="cuda")
+        self.out_host = torch.empty(4, dtype=bf).pin_memory()
+        self.h2d_bytes = self.T * self.d * 2
+        self.d2h_bytes = 8
+        self.step_eager()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        c0 = M.launch_count()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(self.graph, stream=s):
+                self.step_eager()
+        torch.cuda.current_stream().wait_stream(s)
+        self.launches_per_step = M.launch_count() - c0
+        torch.cuda.synchronize()
+
+    def step_eager(self):
+        self.M.mlp_attn_prep_fwd(self.x, self.w, self.gain, self.out, self.r, self.n_q,
+                                 self.n_kv, self.R, self.L)
+
+    def step(self):
+        self.graph.replay()
+
+    def step_e2e(self):
+        self.x.copy_(self.x_host, non_blocking=True)
+        self.graph.replay()
+        self.out_host.copy_(self.out[0, :4], non_blocking=True)
+
+    e2e_inputs = (("x_host", "x"),)
+
+    def e2e_result(self):
+        return self.out[0, :4], self.out_host
+
+    def check(self):
+        import torch
+        torch.cuda.synchronize()
+        assert torch.isfinite(self.out.float()).all(), "non-finite output"
+        assert self.M.get_device_status() == self.M.MLP_OK
+
+    def oracle_sample(self, budget_s):
+        import oracle
+        from mlp_step_gb300 import synth
+        T = 256
+        x = synth.normal_f32((T, self.d), synth.STREAM_GENERIC + 40).astype(np.float64)
+        w = synth.normal_f32((self.d, self.N), synth.STREAM_GENERIC + 41, std=self.d ** -0.5)
+        g = synth.uniform_f32((self.n_q,), synth.STREAM_GENERIC + 42, lo=0.5, hi=1.5)
+        t0 = time.perf_counter()
+        done = 0
+        n = 0
+        while True:
+            oracle.attn_prep(x, w, g, self.n_q, self.n_kv, 64, self.R, self.L)
+            done += T
+            n += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return done, dt, "%d oracle passes over %d tokens (fp64)" % (n, T)
+
+
 class StackStep(Workload):
     """11 blocks over 262,144 tokens, MSE loss, full fwd + bwd + momentum SGD."""
     name = "stack"
@@ -719,6 +825,7 @@ WORKLOADS = {
     "mlp_wide": WideMLP,
     "mlp_wide_f16": lambda: WideMLP(prec_name="fp16"),
     "block": BlockStep,
+    "attn_prep": AttnPrep,
     "stack": StackStep,
 }
 SIZED = {"block": lambda T: BlockStep(T=T), "stack": lambda T: StackStep(T=T),

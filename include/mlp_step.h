@@ -315,6 +315,31 @@ size_t mlp_colsum_workspace_bytes(int rows, int cols);
 mlp_status mlp_colsum(const void* X, int dtype, int rows, int cols, int ld, float* out,
                       void* workspace, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- attention prep
+ * The fused attention preprocessing of [mk] "What Worked" (QK RMSNorm +
+ * partial RoPE + q gain after the projection) in the fully fused form that
+ * [mk] "What Didn't Work" finds achievable in raw CUDA (RMSNorm -> QKV
+ * projection -> QK norm -> RoPE -> gain).  Per token t at position
+ * p = t mod seq_len:
+ *   r = 1 / sqrt(mean_i x_i^2 + eps);  u = r (x W_qkv)          (RMSNorm, gain 1)
+ *   u = [n_q query heads | n_kv key heads | n_kv value heads] of head_dim;
+ *   query and key heads: u_h <- u_h / sqrt(mean_j u_hj^2 + eps)  (QK norm, gain 1)
+ *     then for i < rope_dims / 2, with a = p * rope_theta^(-2i / rope_dims):
+ *     (u_i, u_{i+R/2}) <- (u_i cos a - u_{i+R/2} sin a, u_{i+R/2} cos a + u_i sin a)
+ *     (rotate-half RoPE on the first rope_dims dims of the head);
+ *   query heads: u_h <- q_gain[h] u_h;  value heads: unchanged.
+ * x bf16 [T][d]; w_qkv bf16 [d][N] with N = (n_q_heads + 2 n_kv_heads) *
+ * head_dim; q_gain fp32 [n_q_heads]; qkv_out bf16 [T][N]; rstd_out fp32 [T]
+ * receives r (it is also the kernels' scratch).  Two launches: the per-token
+ * r, then the tcgen05 projection whose epilogue applies r, the QK norm, RoPE
+ * and the gain to each head while it is in registers.
+ * Supported: head_dim 64, rope_dims 16, 32 or 64, d a multiple of 8.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED (16-byte base pointers). */
+mlp_status mlp_attn_prep_fwd(const void* x, const void* w_qkv, const float* q_gain, int T,
+                             int d, int n_q_heads, int n_kv_heads, int head_dim, int rope_dims,
+                             int seq_len, float eps, float rope_theta, void* qkv_out,
+                             float* rstd_out, void* stream);
+
 /* ---------------------------------------------------------------- block ----
  * Transformer MLP block ([mk] "What Worked"), per token t:
  *   r = 1 / sqrt(mean_i x_i^2 + eps);  n = r x          (RMSNorm, gain 1)

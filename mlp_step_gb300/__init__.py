@@ -58,6 +58,8 @@ SIGNATURES = {
     "mlp_get_device_status": (_i, [_vp]),
     "mlp_set_wait_limit_ns": (None, [_ll]),
     "mlp_set_reduction_order": (_i, [_i]),
+    "mlp_attn_prep_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, ctypes.c_float,
+                               ctypes.c_float, _vp, _vp, _vp]),
     "mlp_get_reduction_order": (_i, []),
     "mlp_selftest_wait_timeout": (_i, [_ll, _vp]),
     "mlp_launch_count": (ctypes.c_ulonglong, []),
@@ -382,6 +384,16 @@ def mlp_block_bwd(x, rstd, w_gate, w_down, dy, dx, dw_gate, dw_down, workspace, 
     _check(load().mlp_block_bwd(_ptr(x), _ptr(rstd), _ptr(w_gate), _ptr(w_down), _ptr(dy), T, d,
                                 h, eps, slope, _ptr(dx), _ptr(dw_gate), _ptr(dw_down),
                                 _ptr(workspace), wsb, _stream(stream)), "mlp_block_bwd")
+
+
+def mlp_attn_prep_fwd(x, w_qkv, q_gain, qkv_out, rstd_out, n_q_heads, n_kv_heads,
+                      rope_dims, seq_len, eps=1e-6, rope_theta=10000.0, head_dim=64, stream=None):
+    """Fused RMSNorm -> QKV projection -> QK norm -> partial RoPE -> q gain."""
+    T, d = x.shape
+    _check(load().mlp_attn_prep_fwd(_ptr(x), _ptr(w_qkv), _ptr(q_gain), T, d, n_q_heads,
+                                    n_kv_heads, head_dim, rope_dims, seq_len, eps, rope_theta,
+                                    _ptr(qkv_out), _ptr(rstd_out), _stream(stream)),
+           "mlp_attn_prep_fwd")
 
 
 def mlp_stack_param_count(n_blocks: int, d: int, hidden: int) -> int:

@@ -189,4 +189,32 @@ mlp_status mlp_stack_train_step(int n_blocks, int T, int d, int hidden, float ep
                     (long long)(per * n_blocks), lr, momentum, segs, st);
 }
 
+mlp_status mlp_attn_prep_fwd(const void* x, const void* w_qkv, const float* q_gain, int T,
+                             int d, int n_q_heads, int n_kv_heads, int head_dim, int rope_dims,
+                             int seq_len, float eps, float rope_theta, void* qkv_out,
+                             float* rstd_out, void* stream) {
+  if (T < 0 || d <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || seq_len <= 0 || !(eps >= 0.f) ||
+      !(rope_theta > 0.f))
+    return MLP_ERR_INVALID_ARG;
+  if (head_dim != 64 || (rope_dims != 16 && rope_dims != 32 && rope_dims != 64) || d % 8 != 0 ||
+      d > 65536 || (long long)(n_q_heads + 2 * n_kv_heads) * 64 > 65536)
+    return MLP_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return MLP_OK;
+  if (!x || !w_qkv || !q_gain || !qkv_out || !rstd_out) return MLP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(qkv_out) || !aligned16(rstd_out) ||
+      !aligned16(q_gain))
+    return MLP_ERR_MISALIGNED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MLP_CHECK(launch_row_rstd(x, T, d, eps, rstd_out, st));
+  const int N = (n_q_heads + 2 * n_kv_heads) * 64;
+  GemmArgs g{};
+  g.M = T; g.N = N; g.K = d;
+  g.A = x; g.lda = d; g.a_trans = 0;
+  g.B = w_qkv; g.ldb = N; g.b_trans = 0;
+  g.act = MLP_ACT_NONE;
+  g.C = qkv_out; g.ldc = N; g.c_bf16 = 1;
+  return launch_attn_prep_gemm(g, rstd_out, q_gain, n_q_heads, n_kv_heads, rope_dims, seq_len,
+                               eps, rope_theta, st);
+}
+
 }  // extern "C"

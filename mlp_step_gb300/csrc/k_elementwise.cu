@@ -827,6 +827,47 @@ mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out
   return MLP_OK;
 }
 
+// ------------------------------------------------------------------ row RMS
+// One warp per token: 16-byte loads of 8 bf16, the squares summed per lane in
+// index order and across lanes by a fixed butterfly, r = 1 / sqrt(ss / d + eps)
+// ("Full-Depth MLP Megakernel + Fused Attention Preprocessing", "What Worked":
+// the RMSNorm in front of the QKV projection, gain 1, folded into the
+// projection's epilogue as this per-token scale).
+
+__global__ void __launch_bounds__(256) row_rstd_kernel(const __nv_bfloat16* __restrict__ x,
+                                                       long long T, int d, float eps,
+                                                       float* __restrict__ rstd) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const long long t = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const uint4* row = reinterpret_cast<const uint4*>(x + t * d);
+  float ss = 0.f;
+  for (int q = lane; q < d / 8; q += 32) {
+    const uint4 v = __ldcs(row + q);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      ss = fmaf(f.x, f.x, ss);
+      ss = fmaf(f.y, f.y, ss);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) rstd[t] = 1.0f / sqrtf(ss / (float)d + eps);
+}
+
+mlp_status launch_row_rstd(const void* x, long long T, int d, float eps, float* rstd,
+                           cudaStream_t st) {
+  if (T <= 0) return MLP_OK;
+  LaunchScope ls("row_rstd", st, T, d);
+  launch_k(row_rstd_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, st,
+           static_cast<const __nv_bfloat16*>(x), T, d, eps, rstd);
+  return launch_status();
+}
+
 // ------------------------------------------------------------------ ones columns
 
 // dtype: MLP_DTYPE_F32, MLP_DTYPE_BF16 or MLP_DTYPE_F16.

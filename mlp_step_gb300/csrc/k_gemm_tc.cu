@@ -72,6 +72,59 @@ struct TcParams {
   int a_alt;      // step programs: odd steps read A through the alternate tensor map
 };
 
+// Epilogue of the fused attention preprocessing ("Full-Depth MLP Megakernel +
+// Fused Attention Preprocessing", "What Worked" and "What Didn't Work": QK
+// RMSNorm, partial RoPE and the q gain after the QKV projection, fused in raw
+// CUDA).  The accumulator row of a token holds its heads of 64 columns:
+// query heads [0, n_q), key heads [n_q, n_qk), then value heads.
+struct AttnEpi {
+  const float* rstd;    // [M] input RMSNorm scale of each token
+  const float* q_gain;  // [n_q]
+  int n_q, n_qk;
+  int seq_len;          // the position of token m is m % seq_len
+  float eps;            // of the QK norm
+  float theta;          // RoPE base
+};
+
+// One head of one token, 64 values (va: columns 0-31, vb: 32-63), already
+// scaled by the token's RMSNorm factor: divide by the head's RMS, rotate the
+// pairs (i, i + R/2) for i < R/2 by pos * theta^(-2i/R) (rotate-half RoPE on
+// the first R dims), multiply by gain.  R is a compile-time constant so the
+// partner of every element is a fixed register.
+template <int R>
+__device__ __forceinline__ void attn_head(float (&va)[32], float (&vb)[32], float gain, float pos,
+                                          float log2_theta, float eps) {
+  static_assert(R % 2 == 0 && R <= 64, "rope dims");
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) ss = fmaf(va[j], va[j], ss);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) ss = fmaf(vb[j], vb[j], ss);
+  const float inv = 1.0f / sqrtf(ss * (1.0f / 64.0f) + eps);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    va[j] *= inv;
+    vb[j] *= inv;
+  }
+#pragma unroll
+  for (int i = 0; i < R / 2; ++i) {
+    const float freq = exp2f(-(float)(2 * i) / (float)R * log2_theta);
+    float sn, cs;
+    sincosf(pos * freq, &sn, &cs);
+    constexpr int H = R / 2;
+    float& x1 = i < 32 ? va[i] : vb[i - 32];
+    float& x2 = i + H < 32 ? va[i + H] : vb[i + H - 32];
+    const float a = x1, b = x2;
+    x1 = a * cs - b * sn;
+    x2 = b * cs + a * sn;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    va[j] *= gain;
+    vb[j] *= gain;
+  }
+}
+
 template <int BN, int STAGES>
 struct Layout {
   static constexpr int A_BYTES = BM * BK * 2;
@@ -1242,11 +1295,14 @@ struct Layout2 {
   static constexpr int SMEM = SMEM_BASE + STG_BYTES;
 };
 
-template <int STAGES, int H16>
+// EPI = 0: the GEMM epilogue (bias, activation, mask, split-K partials);
+// EPI = R > 0: the fused attention preprocessing with R RoPE dims (ae).
+template <int STAGES, int H16, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+                        const __grid_constant__ CUtensorMap tmC, const TcParams p,
+                        const AttnEpi ae) {
   using L = Layout2<STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1406,65 +1462,117 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       float* part = p.splits > 1 ? p.partial + (size_t)(u % p.splits) * p.M * p.ldp : nullptr;
       const int row0 = tm * 256 + (int)rank * 128 + quarter * 32;  // this warp's first row
       const int m = row0 + lane;
-      // ReLU-mask pieces are fetched one piece ahead of their use
-      MaskPiece mp_next;
-      load_mask(p, m, tn * BN2 + c_half, mp_next);
-      for (int c0 = c_half; c0 < c_half + BN2 / 2; c0 += 32) {
-        const int n0 = tn * BN2 + c0;
-        if (n0 >= p.N) break;  // warp-uniform
-        const MaskPiece mp = mp_next;
-        if (c0 + 32 < c_half + BN2 / 2 && n0 + 32 < p.N) load_mask(p, m, n0 + 32, mp_next);
-        uint32_t r[32];
-        __syncwarp();
-        ptx::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                                    (uint32_t)(acc * BN2 + c0),
-                                r);
-        ptx::tmem_ld_wait();
-        const float* sb = stage_bias(p, n0, sbias + (warp - 2) * 32, lane);
-        if (part) {
-          if (m < p.M) {
-            float* prow = part + (size_t)m * p.ldp + n0;
-            if (n0 + 32 <= p.N) {
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                reinterpret_cast<float4*>(prow)[q] =
-                    make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-            } else {
-              // fully unrolled with a predicate: a loop with a data-dependent
-              // trip count would index r[] dynamically and put the whole
-              // accumulator piece in local memory on every path
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (n0 + j < p.N) prow[j] = __uint_as_float(r[j]);
+      if constexpr (EPI == 0) {
+        // ReLU-mask pieces are fetched one piece ahead of their use
+        MaskPiece mp_next;
+        load_mask(p, m, tn * BN2 + c_half, mp_next);
+        for (int c0 = c_half; c0 < c_half + BN2 / 2; c0 += 32) {
+          const int n0 = tn * BN2 + c0;
+          if (n0 >= p.N) break;  // warp-uniform
+          const MaskPiece mp = mp_next;
+          if (c0 + 32 < c_half + BN2 / 2 && n0 + 32 < p.N) load_mask(p, m, n0 + 32, mp_next);
+          uint32_t r[32];
+          __syncwarp();
+          ptx::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                      (uint32_t)(acc * BN2 + c0),
+                                  r);
+          ptx::tmem_ld_wait();
+          const float* sb = stage_bias(p, n0, sbias + (warp - 2) * 32, lane);
+          if (part) {
+            if (m < p.M) {
+              float* prow = part + (size_t)m * p.ldp + n0;
+              if (n0 + 32 <= p.N) {
+  #pragma unroll
+                for (int q = 0; q < 8; ++q)
+                  reinterpret_cast<float4*>(prow)[q] =
+                      make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                  __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+              } else {
+                // fully unrolled with a predicate: a loop with a data-dependent
+                // trip count would index r[] dynamically and put the whole
+                // accumulator piece in local memory on every path
+  #pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (n0 + j < p.N) prow[j] = __uint_as_float(r[j]);
+              }
             }
-          }
-        } else if (!p.tma_store) {
-          if (m < p.M) {
+          } else if (!p.tma_store) {
+            if (m < p.M) {
+              float v[32];
+              epilogue_values(p, m, n0, r, sb, mp, v);
+              epilogue_store_regs<H16>(p, m, n0, v);
+            }
+          } else if (row0 < p.M) {  // warp-uniform; rows past M are clipped by TMA
             float v[32];
             epilogue_values(p, m, n0, r, sb, mp, v);
-            epilogue_store_regs<H16>(p, m, n0, v);
-          }
-        } else if (row0 < p.M) {  // warp-uniform; rows past M are clipped by TMA
-          float v[32];
-          epilogue_values(p, m, n0, r, sb, mp, v);
-          // per warp 4 KiB: two 2 KiB bf16 boxes in turn, or one fp32 box
-          uint8_t* box = stg + (warp - 2) * 4096 + (p.c_bf16 ? (stg_count & 1) * 2048 : 0);
-          if (p.c_bf16 ? stg_count >= 2 : stg_count >= 1) {
-            if (lane == 0) {
-              if (p.c_bf16) ptx::bulk_wait_group_read<1>();
-              else ptx::bulk_wait_group_read<0>();
+            // per warp 4 KiB: two 2 KiB bf16 boxes in turn, or one fp32 box
+            uint8_t* box = stg + (warp - 2) * 4096 + (p.c_bf16 ? (stg_count & 1) * 2048 : 0);
+            if (p.c_bf16 ? stg_count >= 2 : stg_count >= 1) {
+              if (lane == 0) {
+                if (p.c_bf16) ptx::bulk_wait_group_read<1>();
+                else ptx::bulk_wait_group_read<0>();
+              }
+              __syncwarp();
             }
+            epilogue_stage_row<H16>(box, p.c_bf16, lane, v);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_2d(&tmC, box, n0, row0);
+              ptx::bulk_commit_group();
+            }
+            ++stg_count;
+          }
+        }
+      } else {
+        // fused attention preprocessing: one 64-column head per step
+        const float rs = m < p.M ? __ldg(ae.rstd + m) : 0.f;
+        const float pos = (float)(m < p.M ? m % ae.seq_len : 0);
+        const float l2t = log2f(ae.theta);
+        // a 32-column piece of bf16 / fp16 output, through the staging boxes
+        // and a TMA store for large outputs, else straight from registers
+        auto store_piece = [&](const float (&v)[32], int nn) {
+          if (!p.tma_store) {
+            if (m < p.M) epilogue_store_regs<H16>(p, m, nn, v);
+            return;
+          }
+          if (row0 >= p.M) return;  // warp-uniform; rows past M are clipped by TMA
+          uint8_t* box = stg + (warp - 2) * 4096 + (stg_count & 1) * 2048;
+          if (stg_count >= 2) {
+            if (lane == 0) ptx::bulk_wait_group_read<1>();
             __syncwarp();
           }
-          epilogue_stage_row<H16>(box, p.c_bf16, lane, v);
+          epilogue_stage_row<H16>(box, 1, lane, v);
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_2d(&tmC, box, n0, row0);
+            ptx::tma_store_2d(&tmC, box, nn, row0);
             ptx::bulk_commit_group();
           }
           ++stg_count;
+        };
+        for (int hc = c_half; hc < c_half + BN2 / 2; hc += 64) {
+          const int n0 = tn * BN2 + hc;
+          if (n0 >= p.N) break;  // warp-uniform
+          uint32_t ra[32], rb[32];
+          __syncwarp();
+          const uint32_t taddr =
+              tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN2 + hc);
+          ptx::tmem_ld_32x32b_x32(taddr, ra);
+          ptx::tmem_ld_32x32b_x32(taddr + 32, rb);
+          ptx::tmem_ld_wait();
+          float va[32], vb[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            va[j] = __uint_as_float(ra[j]) * rs;
+            vb[j] = __uint_as_float(rb[j]) * rs;
+          }
+          const int head = n0 >> 6;
+          if (head < ae.n_qk)  // warp-uniform: query and key heads
+            attn_head<EPI>(va, vb, head < ae.n_q ? __ldg(ae.q_gain + head) : 1.0f, pos, l2t,
+                           ae.eps);
+          store_piece(va, n0);
+          store_piece(vb, n0 + 32);
         }
       }
       ptx::tc_fence_before();
@@ -1567,14 +1675,14 @@ mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
   return MLP_OK;
 }
 
-template <int STAGES, int H16>
+template <int STAGES, int H16, int EPI = 0>
 mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                       const TcParams& p, cudaStream_t st) {
+                       const TcParams& p, cudaStream_t st, const AttnEpi& ae = AttnEpi{}) {
   using L = Layout2<STAGES>;
   static bool configured = false;
   static int max_pairs = 0;
   if (!configured) {
-    if (cudaFuncSetAttribute(tc_gemm_pair_kernel<STAGES, H16>,
+    if (cudaFuncSetAttribute(tc_gemm_pair_kernel<STAGES, H16, EPI>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
       return MLP_ERR_CUDA;
     // pairs that fit at once (a GPC with an odd number of free SMs leaves one over)
@@ -1583,7 +1691,7 @@ mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
     cfg.blockDim = dim3(kPairThreads);
     cfg.dynamicSmemBytes = L::SMEM;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<STAGES, H16>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<STAGES, H16, EPI>, &cfg) != cudaSuccess ||
         n < 1) {
       cudaGetLastError();
       n = num_sms() / 2;
@@ -1594,9 +1702,10 @@ mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
   const int units = p.num_tiles * p.splits;
   const int pairs = units < max_pairs ? units : max_pairs;
   {
-    LaunchScope ls(p.splits > 1 ? "gemm_tc_pair_splitk" : "gemm_tc_pair", st, p.M, p.N, p.K);
-    launch_k(tc_gemm_pair_kernel<STAGES, H16>, dim3(2 * pairs), dim3(kPairThreads),
-             p.tma_store ? L::SMEM : L::SMEM_BASE, st, ta, tb, tc, p);
+    LaunchScope ls(EPI ? "attn_prep_gemm" : (p.splits > 1 ? "gemm_tc_pair_splitk" : "gemm_tc_pair"),
+                   st, p.M, p.N, p.K);
+    launch_k(tc_gemm_pair_kernel<STAGES, H16, EPI>, dim3(2 * pairs), dim3(kPairThreads),
+             p.tma_store ? L::SMEM : L::SMEM_BASE, st, ta, tb, tc, p, ae);
   }
   MLP_CHECK(launch_status());
   if (p.splits > 1) {
@@ -1910,6 +2019,43 @@ mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStr
   }
   return p.f16 ? launch_tiles<1>(ta, tb, tc, p, pl.pair, BN, st)
                : launch_tiles<0>(ta, tb, tc, p, pl.pair, BN, st);
+}
+
+// QKV projection with the fused attention-preprocessing epilogue: CTA-pair
+// 256 x 256 tiles (each a whole number of 64-column heads), one pass over K,
+// bf16 operands and output.
+mlp_status launch_attn_prep_gemm(const GemmArgs& g, const float* rstd, const float* q_gain,
+                                 int n_q, int n_kv, int rope_dims, int seq_len, float eps,
+                                 float theta, cudaStream_t st) {
+  if (g.M <= 0 || g.N <= 0) return MLP_OK;
+  if (g.K <= 0 || !g.c_bf16 || g.f16 || g.bias || g.mask || g.act != MLP_ACT_NONE ||
+      (rope_dims != 16 && rope_dims != 32 && rope_dims != 64) || g.N != (n_q + 2 * n_kv) * 64)
+    return MLP_ERR_UNSUPPORTED_SHAPE;
+  CUtensorMap ta, tb, tc;
+  TcParams p;
+  const unsigned long long wait_ns = wait_limit_ns();
+  MLP_CHECK(prepare_tc(g, (g.M + 255) / 256, BN2, 1, (g.K + BK - 1) / BK, 128, wait_ns, &p, &ta,
+                       &tb));
+  memset(&tc, 0, sizeof(tc));
+  p.tma_store = 0;
+  if ((long long)g.M * g.N >= (1ll << 20) && ((long long)g.ldc * 2) % 16 == 0 && aligned16(g.C)) {
+    if (!encode_tmap_out_2d(&tc, g.C, 0, g.N, g.M, (unsigned long long)g.ldc * 2, 32, 32))
+      return MLP_ERR_CUDA;
+    p.tma_store = 1;
+  }
+  AttnEpi ae;
+  ae.rstd = rstd;
+  ae.q_gain = q_gain;
+  ae.n_q = n_q;
+  ae.n_qk = n_q + n_kv;
+  ae.seq_len = seq_len;
+  ae.eps = eps;
+  ae.theta = theta;
+  switch (rope_dims) {
+    case 16: return launch_pair<6, 0, 16>(ta, tb, tc, p, st, ae);
+    case 32: return launch_pair<6, 0, 32>(ta, tb, tc, p, st, ae);
+    default: return launch_pair<6, 0, 64>(ta, tb, tc, p, st, ae);
+  }
 }
 
 }  // namespace mlp

@@ -41,6 +41,10 @@ size_t mse_ws_bytes(long long n);
 mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out, void* dy,
                       void* ws, cudaStream_t st);
 mlp_status launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st);
+// rstd[t] = 1 / sqrt(mean_i x[t][i]^2 + eps) for bf16 rows x [T][d] (d a
+// multiple of 8, rows 16-byte aligned).
+mlp_status launch_row_rstd(const void* x, long long T, int d, float eps, float* rstd,
+                           cudaStream_t st);
 // Sets column `col` of rows [0, rows) of each listed fp32 / bf16 / fp16 matrix to 1
 // (and the columns after it, up to ld, to 0): the ones column that lets a
 // weight-gradient GEMM produce the bias gradient as its last row.
@@ -96,6 +100,13 @@ size_t gemm_simt_scratch_bytes();
 // k_gemm_tc.cu: tcgen05 bf16 / fp16 GEMM (TMA-fed, fp32 accumulation in tensor
 // memory).
 mlp_status launch_gemm_tc(const GemmArgs& g, unsigned long long wait_ns, cudaStream_t st);
+// k_gemm_tc.cu: the QKV projection of the fused attention preprocessing
+// (g: bf16 x [M][K] times W_qkv [K][N], N = (n_q + 2 n_kv) * 64, bf16 C), with
+// the per-token RMSNorm scale rstd, QK norm, partial RoPE over rope_dims (16,
+// 32 or 64) and the q gain in the epilogue.
+mlp_status launch_attn_prep_gemm(const GemmArgs& g, const float* rstd, const float* q_gain,
+                                 int n_q, int n_kv, int rope_dims, int seq_len, float eps,
+                                 float theta, cudaStream_t st);
 // Scratch bytes a split-K launch of this shape would use (0: no split).
 size_t gemm_tc_splitk_bytes(int M, int N, int K);
 

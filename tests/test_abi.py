@@ -186,3 +186,18 @@ def test_loss_and_update_entry_points_check_arguments(lib):
     assert lib.mlp_train_epoch(None, fake, 2, fake, 256, 128, f(0.1), f(0.9), None, None,
                                None) == 1
     assert lib.mlp_forward(None, fake, 2, 128, fake, None) == 1
+
+
+def test_attn_prep_entry_point_checks_arguments(lib):
+    fake = ctypes.c_void_p(0x10000)
+    f = ctypes.c_float
+    call = lambda T, d, nq, nkv, hd, R, L, x=fake, out=fake: lib.mlp_attn_prep_fwd(
+        x, fake, fake, T, d, nq, nkv, hd, R, L, f(1e-6), f(10000.0), out, fake, None)
+    assert call(0, 512, 8, 4, 64, 32, 1024) == 0                     # empty: nothing launched
+    assert call(-1, 512, 8, 4, 64, 32, 1024) == 1
+    assert call(16, 512, 0, 4, 64, 32, 1024) == 1                    # no query heads
+    assert call(16, 512, 8, 4, 128, 32, 1024) == 3                   # head_dim must be 64
+    assert call(16, 512, 8, 4, 64, 24, 1024) == 3                    # rope dims 16 / 32 / 64
+    assert call(16, 500, 8, 4, 64, 32, 1024) == 3                    # rows of 8 bf16
+    assert call(16, 512, 8, 4, 64, 32, 1024, x=None) == 1
+    assert call(16, 512, 8, 4, 64, 32, 1024, out=ctypes.c_void_p(0x10008)) == 2
