@@ -66,20 +66,26 @@ def test_wide_gemm_shapes_sampled(name):
     assert rel_to_max(got, ref) <= tol, rel_to_max(got, ref)
 
 
-def test_wide_train_step_full_size():
+@pytest.mark.parametrize("prec", ["bf16", "f16"])
+def test_wide_train_step_full_size(prec):
+    """The bench's wide step (batch 16,384) with bf16 operands and with the
+    fp16 variant ("The Debugging Lesson Was Numerical"), each against the
+    oracle rounding at the same points in its format."""
     lr, mom = 0.01, 0.9
     p0 = synth.mlp_flat_params(DIMS)
     X = synth.normal_f32((B, DIMS[0]), synth.STREAM_X)
     y = synth.labels(B, DIMS[-1])
-    net = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
-    Xd = to_dev(X, torch.bfloat16)
+    h16 = torch.float16 if prec == "f16" else torch.bfloat16
+    net = M.MLP(DIMS, prec=M.MLP_PREC_FP16 if prec == "f16" else M.MLP_PREC_BF16, max_batch=B,
+                params=torch.from_numpy(p0))
+    Xd = to_dev(X, h16)
     yd = to_dev(y)
-    # forward logits on sampled rows against the oracle (bf16 points)
+    # forward logits on sampled rows against the oracle (rounding points of the format)
     logits = torch.empty(B, DIMS[-1], device="cuda")
     net.forward(Xd, logits)
     rows = np.concatenate([synth.randint(1, synth.STREAM_GENERIC, 14, B), [0, B - 1]])
     Xb = Xd.float().cpu().numpy()
-    Z_ref = oracle.mlp_forward_rows(DIMS, p0, Xb, rows, bf16_points=True)
+    Z_ref = oracle.mlp_forward_rows(DIMS, p0, Xb, rows, points=prec)
     assert rel_to_max(logits.cpu().numpy()[rows], Z_ref) <= 3e-2
     # full step: loss is the mean of the per-row losses of those logits
     loss = torch.zeros(4, device="cuda")
