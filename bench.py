@@ -871,7 +871,9 @@ def recorded_traffic(kernel, workload):
     was captured on the kernel source that is built now (else None)."""
     import glob
     import hashlib
-    if kernel.startswith("gemm") or kernel == "step_program" or kernel.startswith("attn_prep"):
+    if kernel == "gemm_simt":
+        fname = "k_gemm_simt.cu"
+    elif kernel.startswith("gemm") or kernel == "step_program" or kernel.startswith("attn_prep"):
         fname = "k_gemm_tc.cu"
     elif kernel.startswith("block") or kernel.startswith("rmsnorm"):
         fname = "k_block.cu"
