@@ -86,6 +86,19 @@ struct AttnEpi {
   float theta;          // RoPE base
 };
 
+// sin and cos of an angle a of moderate size (|a| up to ~1e5): Cody-Waite
+// reduction to r = a - 2 pi k in [-pi, pi] with 2 pi split as 6.28125 (exact
+// times any k below 2^16) plus the fp32 rest of 2 pi, then the hardware
+// sine / cosine approximations on r, whose absolute error on [-pi, pi] is
+// about 2^-21.  The RoPE angles of a sequence of 1,024 positions are below
+// 1,024 rad, so the reduced angle carries an error of about 1e-10 rad.
+__device__ __forceinline__ void rope_sincos(float a, float& sn, float& cs) {
+  const float k = rintf(a * 0.15915494309189535f);  // a / (2 pi), rounded
+  float r = fmaf(-k, 6.28125f, a);
+  r = fmaf(-k, 0.0019353071693331003f, r);
+  __sincosf(r, &sn, &cs);
+}
+
 // One head of one token, 64 values (va: columns 0-31, vb: 32-63), already
 // scaled by the token's RMSNorm factor: divide by the head's RMS, rotate the
 // pairs (i, i + R/2) for i < R/2 by pos * theta^(-2i/R) (rotate-half RoPE on
@@ -110,7 +123,7 @@ __device__ __forceinline__ void attn_head(float (&va)[32], float (&vb)[32], floa
   for (int i = 0; i < R / 2; ++i) {
     const float freq = exp2f(-(float)(2 * i) / (float)R * log2_theta);
     float sn, cs;
-    sincosf(pos * freq, &sn, &cs);
+    rope_sincos(pos * freq, sn, cs);
     constexpr int H = R / 2;
     float& x1 = i < 32 ? va[i] : vb[i - 32];
     float& x2 = i + H < 32 ? va[i + H] : vb[i + H - 32];
