@@ -98,7 +98,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
         const float mk = ld_in(static_cast<const T*>(g.mask) + (size_t)m * g.ldm + n);
         v = mk > 0.f ? v : 0.f;
       }
-      if (g.c_bf16) static_cast<__nv_bfloat16*>(g.C)[(size_t)m * g.ldc + n] = f32_to_bf16(v);
+      // 16-bit outputs in the operands' format (fp16 when g.f16 is set)
+      if (g.c_bf16)
+        static_cast<uint16_t*>(g.C)[(size_t)m * g.ldc + n] =
+            f32_to_16_fmt(v, g.f16 ? MLP_DTYPE_F16 : MLP_DTYPE_BF16);
       else static_cast<float*>(g.C)[(size_t)m * g.ldc + n] = v;
     }
   }

@@ -264,6 +264,20 @@ def test_gemm_bf16_tc_k_zero_gives_bias():
     assert np.array_equal(C.cpu().numpy(), np.tile(bias, (5, 1)))
 
 
+@pytest.mark.parametrize("h16", [torch.bfloat16, torch.float16])
+def test_gemm_16bit_k_zero_writes_bias_in_the_operand_format(h16):
+    """K = 0 with a 16-bit output: the epilogue of a zero sum, stored in the
+    operands' 16-bit format (bf16 or fp16)."""
+    N = 24
+    bias = synth.normal_f32((N,), synth.STREAM_GENERIC + 5)
+    C = torch.full((5, N), float("nan"), dtype=h16, device="cuda")
+    A = torch.zeros(5, 8, dtype=h16, device="cuda")
+    B = torch.zeros(8, N, dtype=h16, device="cuda")
+    M.mlp_gemm(A, B, C, 5, N, 0, bias=to_dev(bias), act=M.MLP_ACT_RELU)
+    want = torch.from_numpy(np.tile(np.maximum(bias, 0.0), (5, 1))).to(h16)
+    assert torch.equal(C.cpu(), want)
+
+
 def test_gemm_bf16_tc_deterministic():
     A, B = _operands(1000, 1000, 1000, 0, 0)
     Ad, Bd = to_dev(A, torch.bfloat16), to_dev(B, torch.bfloat16)
