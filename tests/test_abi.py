@@ -201,3 +201,15 @@ def test_attn_prep_entry_point_checks_arguments(lib):
     assert call(16, 500, 8, 4, 64, 32, 1024) == 3                    # rows of 8 bf16
     assert call(16, 512, 8, 4, 64, 32, 1024, x=None) == 1
     assert call(16, 512, 8, 4, 64, 32, 1024, out=ctypes.c_void_p(0x10008)) == 2
+
+
+def test_reduction_order_switch(lib):
+    assert M.get_reduction_order() == M.MLP_ORDER_FAST
+    assert lib.mlp_set_reduction_order(7) == 1          # unknown order: rejected, unchanged
+    assert M.get_reduction_order() == M.MLP_ORDER_FAST
+    M.set_reduction_order(M.MLP_ORDER_LINEAR)
+    try:
+        assert M.get_reduction_order() == M.MLP_ORDER_LINEAR
+    finally:
+        M.set_reduction_order(M.MLP_ORDER_FAST)
+    assert M.get_reduction_order() == M.MLP_ORDER_FAST
