@@ -543,3 +543,26 @@ def test_attn_prep_invariants_and_library_special_cases():
     ref = oracle.attn_prep(x.astype(np.float32).astype(np.float64),
                            W.astype(np.float32).astype(np.float64), gain, eps=1e-6, **dm)[rows]
     assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_rounding_points_modes_round_the_backward_operands():
+    """dZ enters the backward matrix multiplies at a rounding point.  With
+    identity weights and H = [1, 1], dW2 = H^T dZ; dZ = 1 + 2^-9 survives
+    binary16 (fp16 points equal exact mode) but not bf16 (it becomes 1)."""
+    dims = [2, 2, 2]
+    params = np.zeros(oracle.param_count(dims))
+    params[0:4] = [1, 0, 0, 1]
+    params[6:10] = [1, 0, 0, 1]
+    X = np.array([[1.0, 1.0]])
+    dZ = np.array([[1 + 2.0 ** -9, 0.0]])
+    grads = {}
+    for name in ("exact", "f16", "bf16"):
+        hs, _ = oracle.mlp_forward(dims, params, X, points=name)
+        grads[name] = oracle.mlp_backward(dims, params, X, hs, dZ, points=name)
+    dw2 = lambda g: g[6:10].reshape(2, 2)
+    assert dw2(grads["exact"]).tolist() == [[1 + 2.0 ** -9, 0.0], [1 + 2.0 ** -9, 0.0]]
+    assert np.array_equal(dw2(grads["f16"]), dw2(grads["exact"]))
+    assert dw2(grads["bf16"]).tolist() == [[1.0, 0.0], [1.0, 0.0]]
+    # db2 is the column sum of dZ, taken through the same rounding point
+    assert grads["f16"][10:12].tolist() == [1 + 2.0 ** -9, 0.0]
+    assert grads["bf16"][10:12].tolist() == [1.0, 0.0]
