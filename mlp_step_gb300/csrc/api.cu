@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 
 #include "kernels.cuh"
+#include "trace.cuh"
 
 using namespace mlp;
 
@@ -791,6 +792,7 @@ mlp_status mlp_refresh_shadow(mlp_handle* h, void* stream) {
 
 mlp_status mlp_forward(mlp_handle* h, const void* x, int x_dtype, int batch, float* logits,
                        void* stream) {
+  NvtxRange nvtx_range("mlp_forward");
   if (!h || batch < 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
   if (x_dtype != MLP_DTYPE_F32 && x_dtype != MLP_DTYPE_BF16 && x_dtype != MLP_DTYPE_U8 &&
       x_dtype != MLP_DTYPE_F16)
@@ -809,6 +811,7 @@ mlp_status mlp_forward(mlp_handle* h, const void* x, int x_dtype, int batch, flo
 
 mlp_status mlp_backward(mlp_handle* h, const void* dlogits, int ld_dlogits, int batch, void* dx,
                         void* stream) {
+  NvtxRange nvtx_range("mlp_backward");
   if (!h || batch < 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
   if (batch == 0) return MLP_OK;
   if (!dlogits || !h->have_forward || ld_dlogits < h->dims[h->L]) return MLP_ERR_INVALID_ARG;
@@ -819,6 +822,7 @@ mlp_status mlp_backward(mlp_handle* h, const void* dlogits, int ld_dlogits, int 
 }
 
 mlp_status mlp_sgd_step(mlp_handle* h, float lr, float momentum, void* stream) {
+  NvtxRange nvtx_range("mlp_sgd_step");
   if (!h) return MLP_ERR_INVALID_ARG;
   return launch_sgd(h->params, h->grads, h->velocity, h->shadow, buf_dtype(h), h->n_params, lr,
                     momentum, h->segs, S(stream));
@@ -827,6 +831,7 @@ mlp_status mlp_sgd_step(mlp_handle* h, float lr, float momentum, void* stream) {
 mlp_status mlp_train_step(mlp_handle* h, const void* x, int x_dtype, const int32_t* labels,
                           int batch, float lr, float momentum, float* loss_out,
                           int32_t* argmax_out, void* stream) {
+  NvtxRange nvtx_range("mlp_train_step");
   if (!h || batch < 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
   if (x_dtype != MLP_DTYPE_F32 && x_dtype != MLP_DTYPE_BF16 && x_dtype != MLP_DTYPE_U8 &&
       x_dtype != MLP_DTYPE_F16)
@@ -843,6 +848,7 @@ mlp_status mlp_train_step(mlp_handle* h, const void* x, int x_dtype, const int32
 mlp_status mlp_train_epoch(mlp_handle* h, const void* x, int x_dtype, const int32_t* labels,
                            int n_samples, int batch, float lr, float momentum, float* losses_out,
                            int32_t* argmax_out, void* stream) {
+  NvtxRange nvtx_range("mlp_train_epoch");
   if (!h || n_samples < 0 || batch <= 0 || batch > h->max_batch) return MLP_ERR_INVALID_ARG;
   if (x_dtype != MLP_DTYPE_F32 && x_dtype != MLP_DTYPE_BF16 && x_dtype != MLP_DTYPE_U8 &&
       x_dtype != MLP_DTYPE_F16)

@@ -1,6 +1,7 @@
 // C-ABI entry points of the MLP block, the MSE loss and the block stack:
 // argument checks, workspace carving and the enqueue order.
 #include "kernels.cuh"
+#include "trace.cuh"
 
 using namespace mlp;
 
@@ -76,6 +77,7 @@ size_t mlp_block_workspace_bytes(int T, int d, int hidden) {
 mlp_status mlp_block_fwd(const void* x, const void* w_gate, const void* w_down, int T, int d,
                          int hidden, float eps, float slope, void* y, float* rstd_out,
                          void* stream) {
+  NvtxRange nvtx_range("mlp_block_fwd");
   if (!block_shape_ok(T, d, hidden)) return T < 0 ? MLP_ERR_INVALID_ARG : MLP_ERR_UNSUPPORTED_SHAPE;
   if (!(eps >= 0.f)) return MLP_ERR_INVALID_ARG;
   if (T == 0) return MLP_OK;
@@ -90,6 +92,7 @@ mlp_status mlp_block_bwd(const void* x, const float* rstd, const void* w_gate,
                          const void* w_down, const void* dy, int T, int d, int hidden, float eps,
                          float slope, void* dx, float* dw_gate, float* dw_down, void* workspace,
                          size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("mlp_block_bwd");
   (void)eps;  // rstd carries the forward's normalisation
   if (!block_shape_ok(T, d, hidden)) return T < 0 ? MLP_ERR_INVALID_ARG : MLP_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return MLP_OK;
@@ -137,6 +140,7 @@ mlp_status mlp_stack_train_step(int n_blocks, int T, int d, int hidden, float ep
                                 float* velocity, float* grads, void* params_bf16, float lr,
                                 float momentum, float* loss_out, void* workspace,
                                 size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("mlp_stack_train_step");
   if (n_blocks <= 0 || T < 0) return MLP_ERR_INVALID_ARG;
   if (!block_shape_ok(T, d, hidden)) return MLP_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return MLP_OK;
@@ -193,6 +197,7 @@ mlp_status mlp_attn_prep_fwd(const void* x, const void* w_qkv, const float* q_ga
                              int d, int n_q_heads, int n_kv_heads, int head_dim, int rope_dims,
                              int seq_len, float eps, float rope_theta, void* qkv_out,
                              float* rstd_out, void* stream) {
+  NvtxRange nvtx_range("mlp_attn_prep_fwd");
   if (T < 0 || d <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || seq_len <= 0 || !(eps >= 0.f) ||
       !(rope_theta > 0.f))
     return MLP_ERR_INVALID_ARG;

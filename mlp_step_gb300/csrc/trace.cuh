@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 namespace mlp {
 
@@ -21,6 +22,18 @@ class LaunchScope {
  private:
   cudaStream_t st_;
   int slot_;
+};
+
+// A named NVTX range over one library call (a training step, an epoch, a
+// block pass), so that a timeline profiler groups each call's kernels under
+// its name.  NVTX3 is header-only; without a profiler attached the push and
+// pop cost a branch.
+class NvtxRange {
+ public:
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
 }  // namespace mlp
