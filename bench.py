@@ -4,15 +4,16 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 Workloads (synthetic, seeded inputs; see synth.py):
+  stack         11 MLP blocks over 262,144 tokens, MSE loss, fwd + bwd + momentum SGD
+                (default: the largest single-GPU configuration)
   mlp784_epoch  784-256-10 MLP, ReLU hidden, bf16 tensor-core path, one epoch of 6,000
-                images = 46 steps of batch 128 + 1 of 112 (default)
+                images = 46 steps of batch 128 + 1 of 112
   mlp784_fp32   same network, fp32 SIMT path, one step of batch 128
   mlp_wide      1024-8192-8192-1000 MLP, batch 16,384, bf16 operands, fp32 master weights
   mlp784_epoch_f16, mlp_wide_f16
                 the same two workloads with fp16 operands (FP16 in, FP32 accumulate)
   block         one RMSNorm -> gate -> LeakyReLU^2 -> down -> residual block, fwd + bwd,
                 65,536 tokens x 512
-  stack         11 such blocks over 262,144 tokens, MSE loss, fwd + bwd + momentum SGD
   attn_prep     fused attention preprocessing (RMSNorm -> QKV -> QK norm -> RoPE -> gain),
                 65,536 tokens x 512, 8 query / 4 key-value heads of 64
 
@@ -188,6 +189,12 @@ class Workload:
     samples_per_step = 1
     dtype = "bf16"
     config = {}
+    # a step of tens of milliseconds, repeated back to back for seconds: the
+    # tensor-core roofline takes the sustained (power-capped) peak
+    sustained = False
+    # algorithmic (credited) GEMM flops of one bench step; recomputation is
+    # not credited
+    credited_flops_per_step = 0.0
 
     def setup(self):
         raise NotImplementedError
@@ -325,6 +332,12 @@ class MLP784Epoch(Workload):
         self.x = self.x_host.cuda()
         self.y = self.y_host.cuda()
         self.n_steps = (self.n_images + self.batch - 1) // self.batch
+        # per training step of b rows: forward and weight-gradient GEMMs of
+        # both layers, and the hidden layer's input gradient (the first
+        # layer's input gradient is not computed)
+        self.credited_flops_per_step = float(sum(
+            2.0 * min(self.batch, self.n_images - i * self.batch) * (
+                2 * (784 * 256 + 256 * 10) + 256 * 10) for i in range(self.n_steps)))
         self.losses = torch.zeros(self.n_steps, dtype=torch.float32, device="cuda")
         self.losses_host = torch.zeros(self.n_steps, dtype=torch.float32).pin_memory()
         self.h2d_bytes = xb.nbytes + y.nbytes
@@ -352,6 +365,37 @@ class MLP784Epoch(Workload):
                 self._e2e_eager()
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
+        self.train_step_launches = self._count_train_step_launches(dims, prec, p0, xb, y)
+
+    def _count_train_step_launches(self, dims, prec, p0, xb, y):
+        """Kernel launches of one training step of batch 128: the library's
+        train-step call (one step program where it fits) against the same step
+        through the separate public calls (forward, softmax cross entropy,
+        backward, momentum SGD)."""
+        import torch
+        M = self.M
+        if prec == M.MLP_PREC_FP32:
+            return None
+        net = M.MLP(dims, prec=prec, max_batch=self.batch, params=torch.from_numpy(p0))
+        x = torch.from_numpy(xb[:self.batch]).cuda()
+        lab = torch.from_numpy(y[:self.batch]).cuda()
+        loss = torch.zeros(1, device="cuda")
+        c0 = M.launch_count()
+        net.train_step(x, lab, 0.1, 0.9, loss_out=loss)
+        fused = M.launch_count() - c0
+        logits = torch.zeros(self.batch, 10, device="cuda")
+        dl = torch.zeros(self.batch, 16, dtype=net.shadow.dtype, device="cuda")
+        ws = torch.empty(M.softmax_xent_workspace_bytes(self.batch, 10), dtype=torch.uint8,
+                         device="cuda")
+        c0 = M.launch_count()
+        net.forward(x, logits)
+        M.softmax_xent_fwd_bwd(logits, lab, loss, dlogits=dl, workspace=ws)
+        net.backward(dl, self.batch)
+        net.sgd_step(0.1, 0.9)
+        unfused = M.launch_count() - c0
+        torch.cuda.synchronize()
+        return {"fused": fused, "unfused": unfused,
+                "unfused_calls": "mlp_forward, softmax_xent_fwd_bwd, mlp_backward, mlp_sgd_step"}
 
     def _e2e_eager(self):
         self.x.copy_(self.x_host, non_blocking=True)
@@ -426,6 +470,11 @@ class WideMLP(Workload):
             self.name = "mlp_wide_f16"
             self.dtype = "f16"
         self.samples_per_step = self.batch
+        self.sustained = True
+        d = self.dims
+        fwd = sum(2.0 * batch * d[i] * d[i + 1] for i in range(3))
+        dx = sum(2.0 * batch * d[i] * d[i + 1] for i in range(1, 3))
+        self.credited_flops_per_step = 2 * fwd + dx   # forward, dW, dX of layers 2 and 3
         self.config = {"workload": "1024-8192-8192-1000 MLP, ReLU, " + prec_name +
                                    " weights/activations, "
                                    "fp32 master weights and accumulation, batch 16384, inputs "
@@ -521,6 +570,8 @@ class BlockStep(Workload):
     def __init__(self, T=65536):
         self.T, self.d, self.h = T, 512, 1536
         self.samples_per_step = T
+        # six GEMMs of 2 T d h: gate and down forward; dA, dW_down, dW_gate, dn
+        self.credited_flops_per_step = 6 * 2.0 * T * 512 * 1536
         self.config = {"workload": "transformer MLP block fwd+bwd: x[%d tokens, 512] bf16 "
                                    "N(0,1), RMSNorm (eps 1e-6, gain 1) -> W_gate 512x1536 -> "
                                    "LeakyReLU(0.5)^2 -> W_down 1536x512 -> residual, weights "
@@ -629,6 +680,7 @@ class AttnPrep(Workload):
         self.n_q, self.n_kv, self.R = n_q, n_kv, rope_dims
         self.N = (n_q + 2 * n_kv) * 64
         self.samples_per_step = T
+        self.credited_flops_per_step = 2.0 * T * 512 * self.N
         self.config = {"workload": "fused attention preprocessing: x[%d tokens, 512] bf16 N(0,1) "
                                    "(%d sequences of %d), RMSNorm (eps 1e-6, gain 1) -> W_qkv "
                                    "512x%d (%d query, %d key, %d value heads of 64, N(0, 512^-1/2)) "
@@ -724,6 +776,8 @@ class StackStep(Workload):
     def __init__(self, n_blocks=11, T=262144):
         self.nb, self.T, self.d, self.h = n_blocks, T, 512, 1536
         self.samples_per_step = T
+        self.sustained = True
+        self.credited_flops_per_step = n_blocks * 6 * 2.0 * T * 512 * 1536
         self.config = {"workload": "stack of %d MLP blocks (d 512, hidden 1536, "
                                    "LeakyReLU(0.5)^2, RMSNorm pre-norm, residual) over %d tokens "
                                    "bf16, MSE loss vs N(0,1) targets, full fwd + bwd + "
@@ -1012,9 +1066,23 @@ def run_ours(args, wl):
 
     peaks, peaks_kind = load_peaks()
     rep = kernel_profile(wl, max(3, min(args.steps, 20)))
-    roof = roofline_entry(rep, peaks, peaks_kind, f16=wl.dtype == "f16")
+    roof = roofline_entry(rep, peaks, peaks_kind, sustained=wl.sustained, f16=wl.dtype == "f16")
     if roof is not None:
         roof["traffic"] = recorded_traffic(roof["kernel"], wl.name)
+    step_roof = None
+    if wl.credited_flops_per_step:
+        # the whole step against the tensor peak: credited GEMM flops per step
+        # over the device-timed step (every kernel of the step in the time)
+        alu = wl.dtype == "f32"
+        peak = round(fp32_alu_tflops(), 2) if alu else \
+            peaks["bf16_tflops_sustained" if wl.sustained else "bf16_tflops"]
+        ach = wl.credited_flops_per_step / (ms_per_step * 1e-3) / 1e12
+        step_roof = {"bound": "alu" if alu else "tensor", "achieved": round(ach, 3),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 5),
+                     "credited_flops_per_step": wl.credited_flops_per_step,
+                     "peak_kind": ("derived: SMs x 128 fp32 lanes x 2 flops x 2070 MHz" if alu
+                                   else peaks_kind + (" sustained" if wl.sustained
+                                                      else " burst"))}
 
     med = float(np.median(step_ms))
     cv = float(np.std(step_ms) / np.mean(step_ms)) if len(step_ms) > 1 else 0.0
@@ -1031,9 +1099,12 @@ def run_ours(args, wl):
                 "mode": e2e_mode},
         "gpu_launches": wl.launches_per_step * args.steps,
         "roofline": roof,
+        "step_roofline": step_roof,
         "kernels": {k: [n, round(ms / n, 6)] for k, (n, ms) in sorted(rep.items())},
         "wall_s_timed_region": round(wall, 4),
     }
+    if getattr(wl, "train_step_launches", None):
+        out["train_step_launches"] = wl.train_step_launches
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.set_threads(os.cpu_count())
@@ -1084,7 +1155,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mlp784_epoch", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="stack", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=1.0,

@@ -124,8 +124,17 @@ def load():
 # ------------------------------------------------------------------ helpers
 
 def _ptr(t):
+    """Device address of a tensor the library reads as row-major rows: the
+    last dimension must be unit-stride (rows may be padded, their pitch is
+    passed as the leading dimension), and tensors of more than two
+    dimensions must be contiguous."""
     if t is None:
         return None
+    if t.dim() >= 1 and t.numel() > 1 and t.stride(-1) != 1:
+        raise ValueError("the library reads row-major rows: last dimension must have stride 1 "
+                         "(got strides %s)" % (tuple(t.stride()),))
+    if t.dim() > 2 and not t.is_contiguous():
+        raise ValueError("tensors of more than two dimensions must be contiguous")
     return ctypes.c_void_p(t.data_ptr())
 
 
