@@ -27,7 +27,7 @@ def build(force: bool = False) -> str:
     """Compile the oracle with g++ (fp64, no fast-math, no FMA contraction)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + ".tmp%d" % os.getpid()
-        subprocess.check_call(["g++", "-std=c++17", "-O2", "-fopenmp", "-ffp-contract=off",
+        subprocess.check_call(["g++", "-std=c++17", "-O3", "-fopenmp", "-ffp-contract=off",
                                "-fno-fast-math", "-shared", "-fPIC", _SRC, "-o", tmp])
         os.replace(tmp, _LIB)
     return _LIB

@@ -102,19 +102,41 @@ long long orc_param_count(const int* dims, int n_dims) {
 //   b_t = 0: B stored [K][N];  b_t = 1: B stored [N][K]
 // [cap] "Work through the backward pass": the weight and input gradients are
 // matrix multiplies with one transposed input.
+// Every entry is acc = 0; acc = acc + A(m,k) * B(k,n) for k = 0, 1, ..., K-1
+// (each product and sum rounded to double, no contraction).  The loops visit
+// entries in blocks of rows and columns so that a row of B is reused across
+// several rows of C, but each entry still receives its K terms one at a time
+// in ascending k, so the result is the same as the plain triple loop.
 void orc_matmul(const double* A, int a_t, const double* B, int b_t,
                 long long M, long long N, long long K, double* C) {
-#pragma omp parallel for schedule(static)
-  for (long long m = 0; m < M; ++m) {
-    for (long long n = 0; n < N; ++n) {
-      double acc = 0.0;
-      for (long long k = 0; k < K; ++k) {
-        double a = a_t ? A[k * M + m] : A[m * K + k];
-        double b = b_t ? B[n * K + k] : B[k * N + n];
-        acc += a * b;
+  constexpr long long MB = 8, NB = 256;
+  // B as [K][N] rows (a plain copy of the transposed storage when b_t = 1)
+  std::vector<double> Bt;
+  const double* Bk = B;
+  if (b_t) {
+    Bt.resize((size_t)K * N);
+    for (long long n = 0; n < N; ++n)
+      for (long long k = 0; k < K; ++k) Bt[(size_t)k * N + n] = B[n * K + k];
+    Bk = Bt.data();
+  }
+  const long long mblocks = (M + MB - 1) / MB, nblocks = (N + NB - 1) / NB;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long long blk = 0; blk < mblocks * nblocks; ++blk) {
+    const long long m0 = (blk / nblocks) * MB, n0 = (blk % nblocks) * NB;
+    const long long mr = std::min(MB, M - m0), nr = std::min(NB, N - n0);
+    double acc[MB][NB];
+    for (long long i = 0; i < mr; ++i)
+      for (long long j = 0; j < nr; ++j) acc[i][j] = 0.0;
+    for (long long k = 0; k < K; ++k) {
+      const double* brow = Bk + k * N + n0;
+      for (long long i = 0; i < mr; ++i) {
+        const double a = a_t ? A[k * M + m0 + i] : A[(m0 + i) * K + k];
+        double* ci = acc[i];
+        for (long long j = 0; j < nr; ++j) ci[j] = ci[j] + a * brow[j];
       }
-      C[m * N + n] = acc;
     }
+    for (long long i = 0; i < mr; ++i)
+      for (long long j = 0; j < nr; ++j) C[(m0 + i) * N + n0 + j] = acc[i][j];
   }
 }
 

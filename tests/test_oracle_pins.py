@@ -127,6 +127,27 @@ def test_matmul_matches_library(a_t, b_t):
     assert np.allclose(ent, want32[ii, jj], rtol=1e-13, atol=1e-13)
 
 
+@pytest.mark.parametrize("a_t,b_t", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_matmul_sums_each_entry_in_ascending_k(a_t, b_t):
+    """Every entry is the K products added one at a time in ascending k from
+    0.0, as a plain triple loop does, at shapes that cross the row and column
+    blocks the oracle's loops visit (bit for bit)."""
+    for M, N, K in ((9, 257, 5), (17, 3, 13), (1, 513, 2)):
+        A = synth.normal(2, synth.STREAM_GENERIC, M * K).reshape((K, M) if a_t else (M, K))
+        B = synth.normal(2, synth.STREAM_GENERIC + 1, K * N).reshape((N, K) if b_t else (K, N))
+        Am = A.T if a_t else A
+        Bm = B.T if b_t else B
+        want = np.zeros((M, N))
+        for m in range(M):
+            for n in range(N):
+                acc = 0.0
+                for k in range(K):
+                    acc = acc + float(Am[m, k]) * float(Bm[k, n])
+                want[m, n] = acc
+        got = oracle.matmul(A, B, a_t=bool(a_t), b_t=bool(b_t))
+        assert np.array_equal(got, want), (M, N, K)
+
+
 def test_colsum_matches_library_and_bias_gradient():
     X = synth.normal(3, synth.STREAM_GENERIC, 37 * 13).reshape(37, 13).astype(np.float32)
     got = oracle.colsum(X)
