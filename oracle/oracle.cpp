@@ -416,19 +416,17 @@ static void block_fwd_token(const double* x, const double* Wg, const double* Wd,
                             int d, int h, double eps, double slope,
                             double* y, double* rstd, double* u_out, double* a_out) {
   const double r = rms_rstd(x, d, eps);
-  std::vector<double> n(d), u(h, 0.0), a(h);
+  std::vector<double> n(d), u(h, 0.0), a(h), z(d, 0.0);
   for (int i = 0; i < d; ++i) n[i] = x[i] * r;
-  for (int j = 0; j < h; ++j) {
-    double acc = 0.0;
-    for (int i = 0; i < d; ++i) acc += n[i] * Wg[(long long)i * h + j];
-    u[j] = acc;
-    a[j] = lrelu_sq(acc, slope);
-  }
-  for (int i = 0; i < d; ++i) {
-    double acc = 0.0;
-    for (int j = 0; j < h; ++j) acc += a[j] * Wd[(long long)j * d + i];
-    y[i] = x[i] + acc;
-  }
+  // u_j = sum_i n_i Wg[i][j], each u_j summing over ascending i from 0 (the
+  // loops run over i outside so that rows of W_gate are read in order)
+  for (int i = 0; i < d; ++i)
+    for (int j = 0; j < h; ++j) u[j] = u[j] + n[i] * Wg[(long long)i * h + j];
+  for (int j = 0; j < h; ++j) a[j] = lrelu_sq(u[j], slope);
+  // z_i = sum_j a_j Wd[j][i] over ascending j, then y = x + z
+  for (int j = 0; j < h; ++j)
+    for (int i = 0; i < d; ++i) z[i] = z[i] + a[j] * Wd[(long long)j * d + i];
+  for (int i = 0; i < d; ++i) y[i] = x[i] + z[i];
   if (rstd) *rstd = r;
   if (u_out) std::memcpy(u_out, u.data(), h * sizeof(double));
   if (a_out) std::memcpy(a_out, a.data(), h * sizeof(double));
