@@ -4,17 +4,16 @@
 // written to memory).
 //
 // Forward (block_fwd_kernel): one CTA pair (a 2-CTA cluster) per 128-token
-// tile.  Tensor memory of a CTA holds its half of the 128 x 512 fp32 output
-// (256 columns) and two 128-column gate-chunk accumulators.  The 12 hidden
-// chunks of 128 are split between the pair (CTA r computes chunks c with
-// c % 2 == r): the gate MMA U_c = x W_gate[:, c] runs in tensor memory, the
-// epilogue warps apply RMSNorm's row scale and LeakyReLU^2 in fp32, round to
-// bf16 and write the activation chunk A_c into the operand slot of BOTH CTAs'
-// shared memory (the peer's through distributed shared memory); both CTAs
-// then accumulate y_half += A_c W_down[c, half].  So no FLOP is recomputed and
-// the intermediate stays on chip (the page's design kept it in registers and
-// lost to one large library GEMM; here it lives in tensor memory and shared
-// memory and is fed to the tensor cores directly).
+// tile, the gate computed transposed (hidden units on tensor-memory lanes,
+// tokens on columns) by tcgen05.mma.cta_group::2, so each CTA keeps only its
+// 64 tokens of x in shared memory for the whole tile; the activation epilogue
+// writes each token's bf16 activations into the down MMA's operand slot of the
+// CTA that supplies that token (one of the two by distributed shared memory),
+// and the down projection accumulates Y^T in tensor memory.  No FLOP is
+// recomputed and the intermediate stays on chip (the page's design kept it in
+// registers and lost to one large library GEMM; here it lives in tensor memory
+// and shared memory and is fed to the tensor cores directly).  Details at the
+// kernel.
 //
 // RMSNorm with gain 1 is folded into the epilogue: u = r (x W_gate) with
 // r = 1 / sqrt(mean(x^2) + eps) per token, so the gate GEMM reads x as is.
@@ -35,15 +34,8 @@ namespace mlp {
 
 namespace {
 
-constexpr int TM = 128;                 // tokens per tile
+constexpr int TM = 128;                 // tokens per tile (forward: per CTA pair)
 constexpr int DM = 512;                 // model width
-constexpr int HC = 128;                 // hidden chunk
-constexpr int YH = 256;                 // output columns per CTA of the pair
-constexpr int F_STAGES = 3;
-constexpr int F_SLOTS = 2;                // one activation slot per CTA of the pair
-constexpr int F_STAGE_BYTES = 49152;      // x k-block + two W_gate chunks' k-blocks
-constexpr int F_SLOT_BYTES = TM * HC * 2;  // 32 KiB bf16 activation chunk
-constexpr int F_SMEM = 1024 + F_SLOTS * F_SLOT_BYTES + F_STAGES * F_STAGE_BYTES + 2 * TM * 4 + 512;
 
 __device__ __forceinline__ float lrelu_sq(float u, float slope) {
   const float t = u > 0.f ? u : slope * u;
@@ -52,41 +44,6 @@ __device__ __forceinline__ float lrelu_sq(float u, float slope) {
 
 __device__ __forceinline__ float lrelu_sq_grad(float u, float slope) {
   return u > 0.f ? 2.f * u : 2.f * slope * slope * u;
-}
-
-struct FwdParams {
-  int T, hidden, tiles, n_own;
-  float eps, slope;
-  const __nv_bfloat16* x;
-  __nv_bfloat16* y;
-  float* rstd;
-  unsigned long long wait_ns;
-  int* err;
-};
-
-constexpr int F_THREADS = 320;  // 10 warps
-
-// MMA issue order of one tile for a CTA that owns n_own gate chunks (its
-// chunks c = 2 j + rank, j = 0 .. n_own-1).  Gate chunks go in pairs: one
-// N = 256 pass computes chunks j = 2p and 2p+1 into the two adjacent gate
-// accumulators (operand reads per FLOP halve against two N = 128 passes),
-// followed by the four down chunks c = 4p .. 4p+3 that those pairs of both
-// CTAs feed.  An odd last chunk runs alone (N = 128).
-enum : int { OP_GATE_PAIR = 0, OP_GATE = 1, OP_DOWN = 2 };
-struct FwdOp {
-  int kind, idx;
-};
-__device__ __forceinline__ int fwd_n_ops(int n_own) { return 5 * (n_own / 2) + 3 * (n_own & 1); }
-__device__ __forceinline__ FwdOp fwd_op(int i, int n_own) {
-  const int n_gp = n_own / 2;
-  if (i < 5 * n_gp) {
-    const int pr = i / 5, r = i % 5;
-    if (r == 0) return {OP_GATE_PAIR, pr};
-    return {OP_DOWN, 4 * pr + r - 1};
-  }
-  const int r = i - 5 * n_gp;
-  if (r == 0) return {OP_GATE, n_own - 1};
-  return {OP_DOWN, 2 * (n_own - 1) + r - 1};
 }
 
 __device__ __forceinline__ float sumsq_bf16x8(const uint4& v) {
@@ -101,61 +58,93 @@ __device__ __forceinline__ float sumsq_bf16x8(const uint4& v) {
   return s;
 }
 
-// RMSNorm scale of the 32 token rows [row0, row0 + 32) of a tile, computed by
-// one warp with coalesced loads (each row: lanes read 2 x 16 B); lane i
-// returns the scale of row row0 + i (0 for rows past T).
-__device__ __forceinline__ float warp_rows_rstd(const __nv_bfloat16* x, int row0, int T, float eps,
-                                                int lane) {
-  float mine = 0.f;
-#pragma unroll 1
-  for (int rr = 0; rr < 32; rr += 8) {
-    uint4 v[8][2];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int m = row0 + rr + q;
-      if (m < T) {
-        const uint4* p = reinterpret_cast<const uint4*>(x + (size_t)m * DM);
-        v[q][0] = __ldg(p + lane);
-        v[q][1] = __ldg(p + 32 + lane);
-      } else {
-        v[q][0] = make_uint4(0, 0, 0, 0);
-        v[q][1] = make_uint4(0, 0, 0, 0);
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      float ss = sumsq_bf16x8(v[q][0]) + sumsq_bf16x8(v[q][1]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == rr + q) mine = ss;
-    }
-  }
-  return row0 + lane < T ? 1.0f / sqrtf(mine / (float)DM + eps) : 0.f;
+// ------------------------------------------------------------------ forward
+
+// Forward megakernel on CTA pairs with the gate computed transposed.  A pair
+// (2-CTA cluster) owns a tile of 128 tokens; CTA r supplies tokens
+// [64 r, 64 r + 64) of it as MMA operands and holds those tokens of x in
+// shared memory for the whole tile (read from memory once per tile).  For
+// each 256-wide hidden chunk c:
+//   gate:  G_c^T [256 hidden, 128 tokens] = W_gate[:, c]^T x^T   (K = 512)
+//          one tcgen05.mma.cta_group::2 of M = 256, N = 128: CTA r stages
+//          hidden rows [128 r, 128 r + 128) of the chunk (W_gate read as an
+//          M-major operand) and receives them in its tensor memory, lanes =
+//          hidden units, columns = the tile's 128 tokens;
+//   act:   eight epilogue warps per CTA read G_c^T, form a = f(r_t g) in fp32
+//          (RMSNorm's row scale r_t of token t, LeakyReLU^2), round to bf16
+//          and write each token's activations where the down MMA reads them:
+//          tokens [0, 64) into CTA 0's slot, [64, 128) into CTA 1's (one of
+//          the two by distributed shared memory);
+//   down:  Y^T [512 out, 128 tokens] += W_down[c, :]^T A_c^T     (K = 256)
+//          two M = 256 pair MMAs (output columns [0, 256) and [256, 512)),
+//          B = the activation slot (MN-major, tokens contiguous).
+// Tensor memory per CTA: Y^T (its 256 output columns x 128 tokens, 256
+// columns) and two 128-column gate accumulators, so the gate of chunk c + 1
+// runs while the epilogue converts chunk c; two activation slots let the down
+// MMAs of chunk c run while chunk c + 1's activations are written.  MMA order
+// per tile: G0 G1 D0 G2 D1 ... G_{n-1} D_{n-2} D_{n-1}.  Four output warps
+// per CTA compute the next tile's row scales from the resident x, then drain
+// Y^T (+ x, bf16) while the next tile's first two gates run.
+// The intermediate never leaves tensor and shared memory.
+constexpr int F2_TOK = 64;                   // tokens per CTA per tile
+constexpr int F2_HC = 256;                   // hidden per chunk (pair M)
+constexpr int F2_X_BYTES = F2_TOK * DM * 2;  // 64 KiB: 8 k-blocks of [64 tokens][128 B]
+constexpr int F2_SLOT_BYTES = F2_HC * F2_TOK * 2;  // 32 KiB: [256 hidden][64 tokens] bf16
+constexpr int F2_STAGES = 3;
+constexpr int F2_STAGE_BYTES = 32768;
+constexpr int F2_X = 0;
+constexpr int F2_SLOTS = F2_X + F2_X_BYTES;
+constexpr int F2_STG = F2_SLOTS + 2 * F2_SLOT_BYTES;
+constexpr int F2_RBUF = F2_STG + F2_STAGES * F2_STAGE_BYTES;  // float [2][128]
+constexpr int F2_BARS = F2_RBUF + 2 * TM * 4;
+constexpr int F2_SMEM = 1024 + F2_BARS + 256;
+constexpr int F2_THREADS = 448;  // producer, MMA, 4 output warps, 8 epilogue warps
+static_assert(F2_SMEM <= 232448, "forward kernel shared memory");
+
+struct Fwd2Params {
+  int T, n_chunks, tiles;
+  float eps, slope;
+  const __nv_bfloat16* x;
+  __nv_bfloat16* y;
+  float* rstd;
+  unsigned long long wait_ns;
+  int* err;
+};
+
+// MMA / weight-stream order of one tile: op i -> (is_down, chunk).
+__device__ __forceinline__ void f2_op(int i, int n, bool& down, int& c) {
+  // G0, then (G_j, D_{j-1}) for j = 1 .. n-1, then D_{n-1}
+  if (i == 0) { down = false; c = 0; return; }
+  if (i == 2 * n - 1) { down = true; c = n - 1; return; }
+  const int j = (i + 1) >> 1;
+  down = (i & 1) == 0;
+  c = down ? j - 1 : j;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F2_THREADS, 1)
     block_fwd_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmWg,
-                     const __grid_constant__ CUtensorMap tmWd, const FwdParams p) {
+                     const __grid_constant__ CUtensorMap tmWd, const Fwd2Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  // activation slots: chunk c lives in slot c % 2, the slot of its owner
-  uint8_t* slots = smem;                                   // F_SLOTS x 32 KiB
-  uint8_t* stages = smem + F_SLOTS * F_SLOT_BYTES;         // F_STAGES x 48 KiB
-  float* rbuf = reinterpret_cast<float*>(stages + F_STAGES * F_STAGE_BYTES);  // [2][TM]
-  uint64_t* full = reinterpret_cast<uint64_t*>(rbuf + 2 * TM);
-  uint64_t* empty = full + F_STAGES;
-  uint64_t* ufull = empty + F_STAGES;    // [2] gate accumulator ready
-  uint64_t* uempty = ufull + 2;          // [2] gate accumulator drained (128 arrivals)
-  uint64_t* afull = uempty + 2;          // [2] activation slot filled (1 arrival + copy bytes)
-  uint64_t* aempty = afull + F_SLOTS;    // [2] slot consumed by both CTAs (2 arrivals)
-  uint64_t* rready = aempty + F_SLOTS;   // [2] row scales of a tile in rbuf (128 arrivals)
-  uint64_t* yfull = rready + 2;
-  uint64_t* yempty = yfull + 1;          // 128 arrivals
+  uint8_t* xs = smem + F2_X;
+  uint8_t* slots = smem + F2_SLOTS;
+  uint8_t* stages = smem + F2_STG;
+  float* rbuf = reinterpret_cast<float*>(smem + F2_RBUF);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + F2_BARS);
+  uint64_t* empty = full + F2_STAGES;
+  uint64_t* gfull = empty + F2_STAGES;   // [2] gate accumulator ready (multicast commit)
+  uint64_t* gempty = gfull + 2;          // [2] drained (leader: 16 warp arrivals)
+  uint64_t* afull = gempty + 2;          // [2] slot written (leader: 512 thread arrivals)
+  uint64_t* aempty = afull + 2;          // [2] slot consumed (multicast commit)
+  uint64_t* xfull = aempty + 2;          // this CTA's x landed (tx bytes)
+  uint64_t* xempty = xfull + 1;          // last gate of the tile done (multicast commit)
+  uint64_t* rready = xempty + 1;         // [2] row scales of a tile in rbuf (256 arrivals)
+  uint64_t* yfull = rready + 2;          // Y^T complete (multicast commit)
+  uint64_t* yempty = yfull + 1;          // Y^T drained (leader: 8 warp arrivals)
   uint64_t* done = yempty + 1;
-  uint64_t* awritten = done + 1;         // chunk stored in this CTA's slot (128 arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(awritten + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -163,317 +152,348 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
   const uint32_t peer = rank ^ 1u;
   const int cluster = blockIdx.x >> 1;
   const int n_clusters = gridDim.x >> 1;
-  const int n_ops = fwd_n_ops(p.n_own);
+  const int n = p.n_chunks;
 
   if (warp == 0 && lane == 0) {
-    for (int s = 0; s < F_STAGES; ++s) {
+    for (int s = 0; s < F2_STAGES; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&ufull[b], 1);
-      ptx::mbar_init(&uempty[b], 128);
-      ptx::mbar_init(&rready[b], 128);
+      ptx::mbar_init(&gfull[b], 1);
+      ptx::mbar_init(&gempty[b], 16);
+      ptx::mbar_init(&afull[b], 512);
+      ptx::mbar_init(&aempty[b], 1);
+      ptx::mbar_init(&rready[b], 256);
     }
-    for (int s2 = 0; s2 < F_SLOTS; ++s2) {
-      ptx::mbar_init(&afull[s2], 1);
-      ptx::mbar_init(&aempty[s2], 2);
-    }
+    ptx::mbar_init(xfull, 1);
+    ptx::mbar_init(xempty, 1);
     ptx::mbar_init(yfull, 1);
-    ptx::mbar_init(yempty, 128);
+    ptx::mbar_init(yempty, 8);
     ptx::mbar_init(done, 1);
-    ptx::mbar_init(awritten, 128);
     *s_abort = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tensormap(&tmX);
     ptx::prefetch_tensormap(&tmWg);
     ptx::prefetch_tensormap(&tmWd);
   }
-  if (warp == 1) ptx::tmem_alloc(tmem_slot, 512);
+  if (warp == 1) ptx::tmem_alloc_pair(tmem_slot, 512);
   ptx::tc_fence_before();
   __syncthreads();
-  ptx::cluster_sync();  // the peer's barriers are initialised before any remote arrive
+  ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
   ptx::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // y half: cols [0,256); U buffers: [256,384), [384,512)
+  // Y^T: columns [0, 128) output half 0, [128, 256) half 1; gate buffers at
+  // 256 and 384
+  const uint32_t tmem = *tmem_slot;
   pdl_wait();
   pdl_launch_dependents();
 
-  int last_parity[F_STAGES];
+  int last_parity[F2_STAGES];
+  int x_parity = -1;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer
+    // ---------------------------------------------------------------- weights producer
     if (lane == 0) {
-      for (int s = 0; s < F_STAGES; ++s) last_parity[s] = -1;
+      for (int s = 0; s < F2_STAGES; ++s) last_parity[s] = -1;
+      const uint32_t full0 = ptx::mapa_shared(ptx::smem_u32(full), 0);  // the leader's full[]
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int t = cluster; t < p.tiles && ok && !*s_abort; t += n_clusters) {
-        for (int i = 0; i < n_ops && ok; ++i) {
-          const FwdOp op = fwd_op(i, p.n_own);
-          const int nkb = op.kind == OP_DOWN ? HC / 64 : DM / 64;
-          const uint32_t bytes = op.kind == OP_GATE_PAIR ? 49152u : 32768u;
-          for (int kb = 0; kb < nkb; ++kb) {
-            if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
-                                        DEVERR_TIMEOUT_PRODUCER)) {
+        for (int i = 0; i < 2 * n && ok; ++i) {
+          bool down;
+          int c;
+          f2_op(i, n, down, c);
+          for (int q = 0; q < 4; ++q) {
+            if (!ptx::mbar_wait_cluster_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
+                                                DEVERR_TIMEOUT_PRODUCER)) {
               *s_abort = 1;
               ok = false;
               break;
             }
-            ptx::mbar_arrive_expect_tx(&full[stage], bytes);
-            last_parity[stage] = (int)phase;
-            uint8_t* st = stages + stage * F_STAGE_BYTES;
-            if (op.kind == OP_DOWN) {
-              const int c = op.idx;
-#pragma unroll
-              for (int j = 0; j < YH / 64; ++j)
-                ptx::tma_load_2d(st + j * 8192, &tmWd, &full[stage], (int)rank * YH + j * 64,
-                                 c * HC + kb * 64);
-            } else {
-              ptx::tma_load_2d(st, &tmX, &full[stage], kb * 64, t * TM);
-              // chunk(s) c = 2 j + rank: one for a single gate, j = 2p, 2p+1 for a pair
-              const int j0 = op.kind == OP_GATE_PAIR ? 2 * op.idx : op.idx;
-              const int nch = op.kind == OP_GATE_PAIR ? 2 : 1;
-              for (int q = 0; q < nch; ++q) {
-                const int c = 2 * (j0 + q) + (int)rank;
-                ptx::tma_load_2d(st + 16384 + q * 16384, &tmWg, &full[stage], c * HC, kb * 64);
-                ptx::tma_load_2d(st + 24576 + q * 16384, &tmWg, &full[stage], c * HC + 64,
-                                 kb * 64);
-              }
+            if (rank == 0) {
+              ptx::mbar_arrive_expect_tx(&full[stage], 2 * F2_STAGE_BYTES);
+              last_parity[stage] = (int)phase;
             }
-            if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
+            const uint32_t bar = full0 + (uint32_t)stage * 8u;
+            uint8_t* st = stages + stage * F2_STAGE_BYTES;
+            if (!down) {
+              // W_gate^T rows (hidden) [c*256 + 128 r, +128) x d [128 q, +128): two
+              // 64-hidden boxes of 128 d rows
+              const int h0 = c * F2_HC + (int)rank * 128;
+              ptx::tma_load_2d_pair(st, &tmWg, bar, h0, q * 128);
+              ptx::tma_load_2d_pair(st + 16384, &tmWg, bar, h0 + 64, q * 128);
+            } else {
+              // W_down^T rows (output columns) of both halves x hidden [c*256 + 64 q, +64)
+              const int k0 = c * F2_HC + q * 64;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int b = 0; b < 2; ++b)
+                  ptx::tma_load_2d_pair(st + hh * 16384 + b * 8192, &tmWd, bar,
+                                        hh * 256 + (int)rank * 128 + b * 64, k0);
+            }
+            if (++stage == F2_STAGES) { stage = 0; phase ^= 1; }
           }
         }
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc_g = ptx::idesc_bf16_f32(TM, HC, 0, 1);
-      const uint32_t idesc_gp = ptx::idesc_bf16_f32(TM, 2 * HC, 0, 1);
-      const uint32_t idesc_d = ptx::idesc_bf16_f32(TM, YH, 0, 1);
+    // ---------------------------------------------------------------- MMA issuer (leader)
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc_g = ptx::idesc_bf16_f32(2 * TM, TM, 1, 0);  // A M-major, B K-major
+      const uint32_t idesc_d = ptx::idesc_bf16_f32(2 * TM, TM, 1, 1);  // A M-major, B MN-major
+      const uint32_t xs_a = ptx::smem_u32(xs);
+      const uint32_t slot_a = ptx::smem_u32(slots);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t ucount[2] = {0, 0}, acount[F_SLOTS] = {0, 0}, ycount = 0;
       bool ok = true;
-      for (int t = cluster; t < p.tiles && ok && !*s_abort; t += n_clusters) {
-        for (int i = 0; i < n_ops && ok; ++i) {
-          const FwdOp op = fwd_op(i, p.n_own);
-          if (op.kind != OP_DOWN) {
-            // gate accumulators: a pair fills both, a single gate fills j % 2
-            const bool pair = op.kind == OP_GATE_PAIR;
-            const int b0 = pair ? 0 : (op.idx & 1);
-            const int nb = pair ? 2 : 1;
-            for (int q = 0; q < nb && ok; ++q) {
-              const int b = b0 + q;
-              if (!ptx::mbar_wait_bounded(&uempty[b], (ucount[b] & 1) ^ 1, p.wait_ns, p.err,
-                                          DEVERR_TIMEOUT_MMA)) { ok = false; break; }
-              ++ucount[b];
-            }
-            if (!ok) break;
+      int it = 0;
+      for (int t = cluster; t < p.tiles && ok && !*s_abort; t += n_clusters, ++it) {
+        // both CTAs' x for this tile have landed (the row-scale warps arrive
+        // after seeing their own x)
+        if (!ptx::mbar_wait_cluster_bounded(&rready[it & 1], (it >> 1) & 1, p.wait_ns, p.err,
+                                            DEVERR_TIMEOUT_MMA)) { ok = false; break; }
+        for (int i = 0; i < 2 * n && ok; ++i) {
+          bool down;
+          int c;
+          f2_op(i, n, down, c);
+          const uint32_t g = (uint32_t)(it * n + c);  // running chunk index
+          const int b = (int)(g & 1);
+          if (!down) {
+            if (!ptx::mbar_wait_cluster_bounded(&gempty[b], ((g >> 1) & 1) ^ 1, p.wait_ns, p.err,
+                                                DEVERR_TIMEOUT_MMA)) { ok = false; break; }
             ptx::tc_fence_after();
-            const uint32_t d = tmem + 256 + b0 * HC;
-            const uint32_t idesc = pair ? idesc_gp : idesc_g;
-            for (int kb = 0; kb < DM / 64; ++kb) {
+            const uint32_t d = tmem + 256 + (uint32_t)b * 128;
+            for (int q = 0; q < 4; ++q) {
               if (!ptx::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err,
                                           DEVERR_TIMEOUT_MMA)) { ok = false; break; }
               ptx::tc_fence_after();
-              const uint32_t sa = ptx::smem_u32(stages + stage * F_STAGE_BYTES);
+              const uint32_t sa = ptx::smem_u32(stages + stage * F2_STAGE_BYTES);
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t ad = ptx::sw128_desc(sa + k * 32, 16, 1024);
-                const uint64_t bd = ptx::sw128_desc(sa + 16384 + k * 2048, 8192, 1024);
-                ptx::mma_bf16(d, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < 8; ++k) {
+                const int kk = q * 128 + k * 16;  // d index of this K step
+                const uint64_t ad = ptx::sw128_desc(sa + k * 2048, 16384, 1024);
+                const uint64_t bd =
+                    ptx::sw128_desc(xs_a + (kk >> 6) * 8192 + (kk & 63) * 2, 16, 1024);
+                ptx::mma_bf16_pair(d, ad, bd, idesc_g, (q > 0 || k > 0) ? 1u : 0u);
               }
-              ptx::mma_commit(&empty[stage]);
-              if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
+              ptx::mma_commit_pair_multicast(&empty[stage], 3);
+              if (++stage == F2_STAGES) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
-            for (int q = 0; q < nb; ++q) ptx::mma_commit(&ufull[b0 + q]);
+            ptx::mma_commit_pair_multicast(&gfull[b], 3);
+            if (c == n - 1) ptx::mma_commit_pair_multicast(xempty, 3);
           } else {
-            const int c = op.idx;
-            const int s = c & 1;
             if (c == 0) {
-              if (!ptx::mbar_wait_bounded(yempty, (ycount & 1) ^ 1, p.wait_ns, p.err,
-                                          DEVERR_TIMEOUT_MMA)) { ok = false; break; }
-              ++ycount;
+              if (!ptx::mbar_wait_cluster_bounded(yempty, (it & 1) ^ 1, p.wait_ns, p.err,
+                                                  DEVERR_TIMEOUT_MMA)) { ok = false; break; }
             }
-            if (!ptx::mbar_wait_cluster_bounded(&afull[s], acount[s] & 1, p.wait_ns, p.err,
+            if (!ptx::mbar_wait_cluster_bounded(&afull[b], (g >> 1) & 1, p.wait_ns, p.err,
                                                 DEVERR_TIMEOUT_PEER)) { ok = false; break; }
-            ++acount[s];
             ptx::tc_fence_after();
-            const uint32_t a_base = ptx::smem_u32(slots + s * F_SLOT_BYTES);
-            for (int kb = 0; kb < HC / 64; ++kb) {
+            const uint32_t sl = slot_a + (uint32_t)b * F2_SLOT_BYTES;
+            for (int q = 0; q < 4; ++q) {
               if (!ptx::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err,
                                           DEVERR_TIMEOUT_MMA)) { ok = false; break; }
               ptx::tc_fence_after();
-              const uint32_t sb = ptx::smem_u32(stages + stage * F_STAGE_BYTES);
+              const uint32_t sa = ptx::smem_u32(stages + stage * F2_STAGE_BYTES);
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const uint64_t ad = ptx::sw128_desc(a_base + kb * 16384 + k * 32, 16, 1024);
-                const uint64_t bd = ptx::sw128_desc(sb + k * 2048, 8192, 1024);
-                ptx::mma_bf16(tmem, ad, bd, idesc_d, (c > 0 || kb > 0 || k > 0) ? 1u : 0u);
+                const uint64_t bd = ptx::sw128_desc(sl + (q * 64 + k * 16) * 128, 8192, 1024);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  const uint64_t ad = ptx::sw128_desc(sa + hh * 16384 + k * 2048, 8192, 1024);
+                  ptx::mma_bf16_pair(tmem + (uint32_t)hh * 128, ad, bd, idesc_d,
+                                     (c > 0 || q > 0 || k > 0) ? 1u : 0u);
+                }
               }
-              ptx::mma_commit(&empty[stage]);
-              if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
+              ptx::mma_commit_pair_multicast(&empty[stage], 3);
+              if (++stage == F2_STAGES) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
-            // slot s is reusable once both CTAs' MMAs that read it are done;
-            // its owner (CTA s) waits for that
-            ptx::mma_commit_multicast(&aempty[s], (uint16_t)(1u << s));
-            if (c == 2 * p.n_own - 1) ptx::mma_commit(yfull);
+            ptx::mma_commit_pair_multicast(&aempty[b], 3);
+            if (c == n - 1) ptx::mma_commit_pair_multicast(yfull, 3);
           }
         }
       }
       if (!ok) *s_abort = 1;
-      ptx::mma_commit(done);
+      ptx::mma_commit_pair_multicast(done, 1);
       ptx::mbar_wait_bounded(done, 0, p.wait_ns, p.err, DEVERR_TIMEOUT_TEARDOWN);
     }
   } else if (warp < 6) {
-    // ---------------------------------------------------------------- activation warps
+    // ---------------------------------------------------------------- x, row scales, output
+    // Thread (quarter q, lane l) owns tensor-memory lane 32 q + l: output
+    // column 256 hh + 128 rank + 32 q + l of half hh.
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    uint32_t uc[2] = {0, 0}, ac = 0, wc = 0;
+    const uint32_t yempty0 = ptx::mapa_shared(ptx::smem_u32(yempty), 0);
+    const uint32_t rbuf_peer = ptx::mapa_shared(ptx::smem_u32(rbuf), peer);
+    const uint32_t rready_peer = ptx::mapa_shared(ptx::smem_u32(rready), peer);
+    // row scales: two threads per token, each summing half of the row
+    const int tok = (warp - 2) * 16 + (lane >> 1);
+    const int rhalf = lane & 1;
     bool ok = true;
     int it = 0;
-    for (int t = cluster; t < p.tiles && ok; t += n_clusters, ++it) {
-      if (*s_abort) break;
-      if (!ptx::mbar_wait_bounded(&rready[it & 1], (it >> 1) & 1, p.wait_ns, p.err,
-                                  DEVERR_TIMEOUT_EPILOGUE)) { ok = false; break; }
-      const float r = rbuf[(it & 1) * TM + row];
-      for (int j = 0; j < p.n_own && ok; ++j) {
-        const int b = j & 1;
-        if (!ptx::mbar_wait_bounded(&ufull[b], uc[b] & 1, p.wait_ns, p.err,
-                                    DEVERR_TIMEOUT_EPILOGUE)) { ok = false; break; }
-        ++uc[b];
-        // own chunk c = 2 j + rank goes to this CTA's slot
-        const int sl = (int)rank;
-        if (!ptx::mbar_wait_bounded(&aempty[sl], (ac & 1) ^ 1, p.wait_ns, p.err,
-                                    DEVERR_TIMEOUT_EPILOGUE)) { ok = false; break; }
-        ++ac;
-        const uint32_t my_slot_addr = ptx::smem_u32(slots + sl * F_SLOT_BYTES);
-        ptx::tc_fence_after();
+    int t_prev = -1;
+    auto drain = [&](int tp, int itp) -> bool {
+      if (!ptx::mbar_wait_bounded(yfull, itp & 1, p.wait_ns, p.err, DEVERR_TIMEOUT_EPILOGUE))
+        return false;
+      ptx::tc_fence_after();
+      const int odd = lane & 1;
 #pragma unroll 1
-        for (int cc = 0; cc < HC / 32; ++cc) {
+      for (int hh = 0; hh < 2; ++hh) {
+        // this lane's pair of output columns (even lane: o, o+1; odd: o-1, o)
+        const int col = hh * 256 + (int)rank * 128 + quarter * 32 + (lane & ~1);
+#pragma unroll 1
+        for (int tb = 0; tb < TM / 32; ++tb) {
           uint32_t v[32];
           __syncwarp();
-          ptx::tmem_ld_32x32b_x32(tmem + lane_off + 256 + b * HC + cc * 32, v);
+          ptx::tmem_ld_32x32b_x32(tmem + lane_off + (uint32_t)(hh * 128 + tb * 32), v);
           ptx::tmem_ld_wait();
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float a0 = lrelu_sq(__uint_as_float(v[2 * e]) * r, p.slope);
-            const float a1 = lrelu_sq(__uint_as_float(v[2 * e + 1]) * r, p.slope);
-            pk[e] = pack_bf16x2(a0, a1);
+          if (hh == 1 && tb == TM / 32 - 1) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (rank == 0) ptx::mbar_arrive(yempty);
+              else ptx::mbar_arrive_remote(yempty0);
+            }
           }
-          // K-major 128B-swizzled operand layout: 64-wide k blocks of
-          // [128 rows][128 B]; 16-byte chunk j of row `row` sits at
-          // chunk (j ^ (row & 7)).
-          const int kb = cc >> 1;
+          // token pairs (j, j+1): even lanes take token j, odd lanes j + 1
+          uint32_t xv[16];
+          const int m0 = tp * TM + tb * 32 + odd;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int j16 = (cc & 1) * 4 + q;
-            const uint32_t off =
-                (uint32_t)(kb * 16384 + row * 128 + ((j16 ^ (row & 7)) << 4));
-            ptx::st_shared_v4(my_slot_addr + off,
-                              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
+          for (int jj = 0; jj < 16; ++jj) {
+            const int m = m0 + 2 * jj;
+            xv[jj] = m < p.T ? __ldg(reinterpret_cast<const unsigned int*>(
+                                   p.x + (size_t)m * DM + col))
+                             : 0u;
+          }
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const float send = __uint_as_float(odd ? v[2 * jj] : v[2 * jj + 1]);
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const float lo = odd ? recv : __uint_as_float(v[2 * jj]);
+            const float hi = odd ? __uint_as_float(v[2 * jj + 1]) : recv;
+            const int m = m0 + 2 * jj;
+            if (m < p.T) {
+              const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv[jj]));
+              *reinterpret_cast<unsigned int*>(p.y + (size_t)m * DM + col) =
+                  pack_bf16x2(lo + xf.x, hi + xf.y);
+            }
           }
         }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&uempty[b]);
-        // the chunk is complete in this CTA once all 128 writers are past
-        // this point; one thread then publishes it locally and sends a copy
-        // to the peer's slot (the copy's bytes complete the peer's barrier)
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(awritten);
-        if (warp == 2 && lane == 0) {
-          // on a timeout the chunk is not published; the peer and the MMA
-          // warp then give up on their own bounded waits
-          if (!ptx::mbar_wait_bounded(awritten, wc & 1, p.wait_ns, p.err,
-                                      DEVERR_TIMEOUT_EPILOGUE)) {
-            *s_abort = 1;
-          } else {
-          ptx::mbar_arrive(&afull[sl]);
-          const uint32_t peer_bar = ptx::mapa_shared(ptx::smem_u32(&afull[sl]), peer);
-          ptx::mbar_arrive_expect_tx_remote(peer_bar, (uint32_t)F_SLOT_BYTES);
-          ptx::bulk_copy_to_peer(ptx::mapa_shared(my_slot_addr, peer), my_slot_addr,
-                                 (uint32_t)F_SLOT_BYTES, peer_bar);
-          }
-        }
-        ++wc;
       }
-    }
-    if (!ok) *s_abort = 1;
-  } else {
-    // ---------------------------------------------------------------- output warps
-    // Row scales for the next tile are computed one tile ahead.  The residual
-    // half-row of x streams through a ring of four 32-column chunks in
-    // registers, the first four in flight while the tile's MMAs run.  (Ten
-    // warps put three on some SM sub-partitions, which caps a thread at 168
-    // registers, so the whole half-row cannot be held at once.)
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    uint4 xq[4][4];
-    uint32_t yc = 0;
-    bool ok = true;
-    int it = 0;
-    auto publish_rstd = [&](int tile, int buf) {
-      const float r = warp_rows_rstd(p.x, tile * TM + quarter * 32, p.T, p.eps, lane);
-      rbuf[buf * TM + row] = r;
-      const int m = tile * TM + row;
-      if (rank == 0 && p.rstd && m < p.T) p.rstd[m] = r;
-      ptx::mbar_arrive(&rready[buf]);
+      return true;
     };
-    if (cluster < p.tiles) publish_rstd(cluster, 0);
     for (int t = cluster; t < p.tiles && ok; t += n_clusters, ++it) {
-      if (*s_abort) break;
-      const int tn = t + n_clusters;
-      if (tn < p.tiles) publish_rstd(tn, (it + 1) & 1);
-      const int m = t * TM + row;
-      const bool valid = m < p.T;
-      const uint4* xsrc = reinterpret_cast<const uint4*>(p.x + (size_t)m * DM + rank * YH);
-      if (valid) {
+      if (*s_abort) { ok = false; break; }
+      // this CTA's 64 tokens of x, once the last gate of the tile before has run
+      if (warp == 2 && lane == 0) {
+        if (it > 0 && !ptx::mbar_wait_bounded(xempty, (it - 1) & 1, p.wait_ns, p.err,
+                                               DEVERR_TIMEOUT_EPILOGUE)) {
+          *s_abort = 1;
+        } else {
+          ptx::mbar_arrive_expect_tx(xfull, (uint32_t)F2_X_BYTES);
+          x_parity = it & 1;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) xq[c][q] = __ldg(xsrc + c * 4 + q);
+          for (int kb = 0; kb < DM / 64; ++kb)
+            ptx::tma_load_2d(xs + kb * 8192, &tmX, xfull, kb * 64, t * TM + (int)rank * F2_TOK);
+        }
       }
-      if (!ptx::mbar_wait_bounded(yfull, yc & 1, p.wait_ns, p.err, DEVERR_TIMEOUT_EPILOGUE)) {
+      __syncwarp();
+      if (!ptx::mbar_wait_bounded(xfull, it & 1, p.wait_ns, p.err, DEVERR_TIMEOUT_EPILOGUE)) {
         ok = false;
         break;
       }
-      ++yc;
-      ptx::tc_fence_after();
-      uint4* yr = reinterpret_cast<uint4*>(p.y + (size_t)m * DM + rank * YH);
+      // row scale of token `tok`: sum of squares over this thread's four
+      // k-blocks, 16-byte chunks read in swizzled order (conflict-free)
+      float ss = 0.f;
 #pragma unroll
-      for (int cc = 0; cc < YH / 32; ++cc) {
-        uint32_t v[32];
-        __syncwarp();
-        ptx::tmem_ld_32x32b_x32(tmem + lane_off + cc * 32, v);
-        ptx::tmem_ld_wait();
-        if (valid) {
+      for (int kb = 0; kb < 4; ++kb) {
+        const uint8_t* row = xs + (rhalf * 4 + kb) * 8192 + tok * 128;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xq[cc & 3][q]);
-            uint4 o;
-            uint32_t* op = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 xf = __bfloat1622float2(xh[e]);
-              op[e] = pack_bf16x2(__uint_as_float(v[q * 8 + 2 * e]) + xf.x,
-                                  __uint_as_float(v[q * 8 + 2 * e + 1]) + xf.y);
-            }
-            yr[cc * 4 + q] = o;
-          }
-          if (cc + 4 < YH / 32) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) xq[cc & 3][q] = __ldg(xsrc + (cc + 4) * 4 + q);
-          }
-        }
+        for (int j = 0; j < 8; ++j)
+          ss += sumsq_bf16x8(*reinterpret_cast<const uint4*>(row + ((j ^ (tok & 7)) << 4)));
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(yempty);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      const int m = t * TM + (int)rank * F2_TOK + tok;
+      const float r = m < p.T ? 1.0f / sqrtf(ss / (float)DM + p.eps) : 0.f;
+      const int buf = it & 1;
+      if (rhalf == 0) {
+        const int idx = buf * TM + (int)rank * F2_TOK + tok;
+        rbuf[idx] = r;
+        ptx::st_cluster_f32(rbuf_peer + (uint32_t)idx * 4u, r);
+        if (p.rstd && m < p.T) p.rstd[m] = r;
+      }
+      ptx::mbar_arrive_cluster_local(&rready[buf]);
+      ptx::mbar_arrive_remote(rready_peer + (uint32_t)buf * 8u);
+      // output of the tile before, while this tile's first gates run
+      if (t_prev >= 0 && !drain(t_prev, it - 1)) { ok = false; break; }
+      t_prev = t;
+    }
+    if (ok && t_prev >= 0 && !*s_abort && !drain(t_prev, it - 1)) ok = false;
+    if (!ok) *s_abort = 1;
+  } else {
+    // ---------------------------------------------------------------- gate epilogue
+    // Warps 6-13: tensor-memory lane quarter warp % 4 (hidden units), token
+    // half th (columns [64 th, 64 th + 64)); the activations of those tokens
+    // go to CTA th's slot.
+    const int quarter = warp & 3;
+    const int th = (warp - 6) >> 2;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t gempty0 = ptx::mapa_shared(ptx::smem_u32(gempty), 0);
+    const uint32_t afull0 = ptx::mapa_shared(ptx::smem_u32(afull), 0);
+    const int k = (int)rank * 128 + quarter * 32 + lane;  // hidden row within the chunk
+    const uint32_t dst_slots = ptx::mapa_shared(ptx::smem_u32(slots), (uint32_t)th);
+    bool ok = true;
+    int it = 0;
+    for (int t = cluster; t < p.tiles && ok; t += n_clusters, ++it) {
+      const float* rt = rbuf + (it & 1) * TM + th * F2_TOK;
+      for (int c = 0; c < n && ok; ++c) {
+        if (*s_abort) { ok = false; break; }
+        const uint32_t g = (uint32_t)(it * n + c);
+        const int b = (int)(g & 1);
+        if (!ptx::mbar_wait_bounded(&gfull[b], (g >> 1) & 1, p.wait_ns, p.err,
+                                    DEVERR_TIMEOUT_EPILOGUE)) { ok = false; break; }
+        ptx::tc_fence_after();
+        uint32_t v[64];
+        __syncwarp();
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + 256 + (uint32_t)(b * 128 + th * 64),
+                                *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        ptx::tmem_ld_32x32b_x32(tmem + lane_off + 256 + (uint32_t)(b * 128 + th * 64 + 32),
+                                *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0) ptx::mbar_arrive(&gempty[b]);
+          else ptx::mbar_arrive_remote(gempty0 + (uint32_t)b * 8u);
+        }
+        if (c == 0 && !ptx::mbar_wait_cluster_bounded(&rready[it & 1], (it >> 1) & 1, p.wait_ns,
+                                                      p.err, DEVERR_TIMEOUT_EPILOGUE)) {
+          ok = false;
+          break;
+        }
+        if (!ptx::mbar_wait_bounded(&aempty[b], ((g >> 1) & 1) ^ 1, p.wait_ns, p.err,
+                                    DEVERR_TIMEOUT_EPILOGUE)) { ok = false; break; }
+        const uint32_t row = dst_slots + (uint32_t)(b * F2_SLOT_BYTES + k * 128);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 r0 = *reinterpret_cast<const float4*>(rt + 8 * j);
+          const float4 r1 = *reinterpret_cast<const float4*>(rt + 8 * j + 4);
+          const float* u = reinterpret_cast<const float*>(&v[8 * j]);
+          uint4 o;
+          o.x = pack_bf16x2(lrelu_sq(u[0] * r0.x, p.slope), lrelu_sq(u[1] * r0.y, p.slope));
+          o.y = pack_bf16x2(lrelu_sq(u[2] * r0.z, p.slope), lrelu_sq(u[3] * r0.w, p.slope));
+          o.z = pack_bf16x2(lrelu_sq(u[4] * r1.x, p.slope), lrelu_sq(u[5] * r1.y, p.slope));
+          o.w = pack_bf16x2(lrelu_sq(u[6] * r1.z, p.slope), lrelu_sq(u[7] * r1.w, p.slope));
+          ptx::st_cluster_v4(row + (uint32_t)((j ^ (k & 7)) << 4), o);
+        }
+        ptx::fence_proxy_async_cluster();
+        if (rank == 0) ptx::mbar_arrive_cluster_local(&afull[b]);
+        else ptx::mbar_arrive_remote(afull0 + (uint32_t)b * 8u);
+      }
     }
     if (!ok) *s_abort = 1;
   }
@@ -483,19 +503,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(F_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (*s_abort && warp == 0 && lane == 0) {
-    for (int s = 0; s < F_STAGES; ++s)
+    for (int s = 0; s < F2_STAGES; ++s)
       if (last_parity[s] >= 0)
         ptx::mbar_wait_bounded(&full[s], (uint32_t)last_parity[s], p.wait_ns, p.err,
                                DEVERR_TIMEOUT_TEARDOWN);
   }
+  if (*s_abort && warp == 2 && lane == 0 && x_parity >= 0)
+    ptx::mbar_wait_bounded(xfull, (uint32_t)x_parity, p.wait_ns, p.err, DEVERR_TIMEOUT_TEARDOWN);
   __syncwarp();
   __syncthreads();
-  __syncwarp();
-  // neither CTA leaves while the peer may still write into its shared memory
+  // neither CTA frees its tensor memory or leaves while the pair's MMAs,
+  // copies or signals may still reach it
   ptx::cluster_sync();
   if (warp == 1) {
     __syncwarp();
-    ptx::tmem_dealloc(tmem, 512);
+    ptx::tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -866,22 +888,32 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const __nv_bfloat16* _
 mlp_status launch_block_fwd(const void* x, const void* wg, const void* wd, int T, int hidden,
                             float eps, float slope, void* y, float* rstd, cudaStream_t st) {
   static bool configured = false;
+  static int max_clusters = 0;
   if (!configured) {
     if (cudaFuncSetAttribute(block_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             F_SMEM) != cudaSuccess)
+                             F2_SMEM) != cudaSuccess)
       return MLP_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    cfg.blockDim = dim3(F2_THREADS);
+    cfg.dynamicSmemBytes = F2_SMEM;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, block_fwd_kernel, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = num_sms() / 2;
+    }
+    max_clusters = n;
     configured = true;
   }
   CUtensorMap tx, tg, td;
-  if (!encode_tmap_bf16_2d(&tx, x, DM, T, DM * 2, 64, TM)) return MLP_ERR_CUDA;
-  if (!encode_tmap_bf16_2d(&tg, wg, hidden, DM, (unsigned long long)hidden * 2, 64, 64))
+  if (!encode_tmap_bf16_2d(&tx, x, DM, T, DM * 2, 64, F2_TOK)) return MLP_ERR_CUDA;
+  if (!encode_tmap_bf16_2d(&tg, wg, hidden, DM, (unsigned long long)hidden * 2, 64, 128))
     return MLP_ERR_CUDA;
   if (!encode_tmap_bf16_2d(&td, wd, DM, hidden, DM * 2, 64, 64)) return MLP_ERR_CUDA;
-  FwdParams p;
+  Fwd2Params p;
   p.T = T;
-  p.hidden = hidden;
+  p.n_chunks = hidden / F2_HC;
   p.tiles = (T + TM - 1) / TM;
-  p.n_own = hidden / (2 * HC);
   p.eps = eps;
   p.slope = slope;
   p.x = static_cast<const __nv_bfloat16*>(x);
@@ -890,11 +922,11 @@ mlp_status launch_block_fwd(const void* x, const void* wg, const void* wd, int T
   p.wait_ns = wait_limit_ns();
   p.err = device_error_word();
   if (!p.err) return MLP_ERR_CUDA;
-  int clusters = num_sms() / 2;
+  int clusters = max_clusters;
   if (clusters > p.tiles) clusters = p.tiles;
   if (clusters < 1) clusters = 1;
   LaunchScope ls("block_fwd", st, T, DM, hidden);
-  launch_k(block_fwd_kernel, dim3(2 * clusters), dim3(F_THREADS), F_SMEM, st, tx, tg, td, p);
+  launch_k(block_fwd_kernel, dim3(2 * clusters), dim3(F2_THREADS), F2_SMEM, st, tx, tg, td, p);
   return launch_status();
 }
 
