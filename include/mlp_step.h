@@ -59,7 +59,7 @@ typedef int mlp_status;
 #define MLP_ERR_UNSUPPORTED_SHAPE 3  /* a dimension outside what the kernels handle */
 #define MLP_ERR_CUDA 4               /* a CUDA runtime call or launch failed        */
 #define MLP_ERR_DEVICE_TIMEOUT 5     /* a kernel abandoned a bounded wait           */
-#define MLP_ERR_NUMERIC 6            /* non-finite loss                             */
+#define MLP_ERR_NUMERIC 6            /* a loss kernel produced a non-finite loss    */
 
 #define MLP_ACT_NONE 0
 #define MLP_ACT_RELU 1               /* [cap] "The minimum model"                    */
@@ -87,7 +87,11 @@ const char* mlp_status_string(mlp_status s);
 
 /* Synchronises `stream`, then reads and clears the device error word.
  * Returns MLP_ERR_DEVICE_TIMEOUT if a kernel abandoned a bounded wait since the
- * last call, MLP_ERR_CUDA if the stream reports an error, else MLP_OK. */
+ * last call, MLP_ERR_NUMERIC if a loss computed since the last call (softmax
+ * cross entropy, mean-squared loss, or the loss inside a training step) was
+ * not finite ([cap] "The independent submission gate": a run that exits
+ * cleanly is not yet a correct one), MLP_ERR_CUDA if the stream reports an
+ * error, else MLP_OK.  The first event recorded since the last call wins. */
 mlp_status mlp_get_device_status(void* stream);
 
 /* Sets the time limit of every bounded wait in the kernels, in nanoseconds of
@@ -269,7 +273,8 @@ mlp_status softmax_xent_fwd_bwd(const float* logits, int ld_logits, const int32_
  * loads the library holds until the process exits; batches above
  * softmax_xent_noalloc_max_batch() = 524,288 rows return
  * MLP_ERR_UNSUPPORTED_SHAPE.  The first call on a device looks up the array's
- * device address (cudaGetSymbolAddress) with that device current; make that
+ * device address (cudaGetSymbolAddress) with that device current and keeps it
+ * for the life of the process (a device reset invalidates it); make that
  * first call before any stream capture on the device.  The call allocates
  * nothing.  All calls share the one array and it keeps the last call's
  * contents (each call writes every partial it reads, so nothing needs

@@ -200,7 +200,7 @@ mlp_status mlp_get_device_status(void* stream) {
   if (err != 0) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return MLP_ERR_CUDA;
-    return MLP_ERR_DEVICE_TIMEOUT;
+    return err == DEVERR_NUMERIC ? MLP_ERR_NUMERIC : MLP_ERR_DEVICE_TIMEOUT;
   }
   return MLP_OK;
 }

@@ -27,10 +27,18 @@ enum : int {
   DEVERR_TIMEOUT_TEARDOWN = 0x104,
   DEVERR_TIMEOUT_PEER = 0x105,
   DEVERR_TIMEOUT_GRID = 0x106,
+  DEVERR_NUMERIC = 0x201,  // a loss kernel produced a non-finite loss
 };
 
 __device__ __forceinline__ void record_device_error(int* word, int code) {
   if (word) atomicCAS(word, 0, code);
+}
+
+// A loss that is not finite (an overflowing or NaN logit or output reached
+// the mean) is recorded for mlp_get_device_status (MLP_ERR_NUMERIC); the value
+// itself is still stored.
+__device__ __forceinline__ void check_loss_finite(float loss, int* err) {
+  if (!isfinite(loss)) record_device_error(err, DEVERR_NUMERIC);
 }
 
 __device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }

@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(256) xent_rows_regs_kernel(
 // forms the mean (warp w sums its rows in order, then warp sums in order).
 __global__ void __launch_bounds__(256) xent_single_block_kernel(
     const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
-    float* __restrict__ loss_out, void* dlog, int dl_dtype, int ldd, int* argmax) {
+    float* __restrict__ loss_out, void* dlog, int dl_dtype, int ldd, int* argmax, int* err) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float part[8];
@@ -389,7 +389,9 @@ __global__ void __launch_bounds__(256) xent_single_block_kernel(
   if (threadIdx.x == 0) {
     float t = 0.f;
     for (int w = 0; w < 8; ++w) t += part[w];
-    if (loss_out) *loss_out = t / (float)B;
+    const float loss = t / (float)B;
+    check_loss_finite(loss, err);
+    if (loss_out) *loss_out = loss;
   }
 }
 
@@ -422,7 +424,7 @@ __device__ __forceinline__ float xent_lane_row(const float* __restrict__ z_row, 
 
 __global__ void __launch_bounds__(512) xent_lane_rows_kernel(
     const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
-    float* __restrict__ loss_out, void* dlog, int dl_dtype, int ldd, int* argmax) {
+    float* __restrict__ loss_out, void* dlog, int dl_dtype, int ldd, int* argmax, int* err) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float red[512];
@@ -445,7 +447,11 @@ __global__ void __launch_bounds__(512) xent_lane_rows_kernel(
     if (r < w) red[r] += red[r + w];
     __syncthreads();
   }
-  if (r == 0 && loss_out) *loss_out = red[0] / (float)B;
+  if (r == 0) {
+    const float loss = red[0] / (float)B;
+    check_loss_finite(loss, err);
+    if (loss_out) *loss_out = loss;
+  }
 }
 
 // Large batches: one row per warp, one partial per block, then a one-block
@@ -476,9 +482,11 @@ __global__ void __launch_bounds__(256) xent_rows_kernel(
 }
 
 // Sum of `n` partials in a fixed order, times `scale`, into *out.
+// out = (sum of the n partials in a fixed order) / divisor: the mean of a
+// loss, so a non-finite result is recorded in the device error word.
 __global__ void __launch_bounds__(256) sum_partials_kernel(const float* __restrict__ partial,
                                                            long long n, float divisor,
-                                                           float* __restrict__ out) {
+                                                           float* __restrict__ out, int* err) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float red[256];
@@ -490,7 +498,11 @@ __global__ void __launch_bounds__(256) sum_partials_kernel(const float* __restri
     if ((int)threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
     __syncthreads();
   }
-  if (threadIdx.x == 0) *out = red[0] / divisor;
+  if (threadIdx.x == 0) {
+    const float loss = red[0] / divisor;
+    check_loss_finite(loss, err);
+    *out = loss;
+  }
 }
 
 size_t xent_workspace_bytes(int B) {
@@ -507,13 +519,13 @@ mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, i
     while (threads < B) threads *= 2;  // a power of two for the tree sum
     LaunchScope ls("xent", st, B, C);
     launch_k(xent_lane_rows_kernel, dim3(1), dim3(threads), 0, st, logits, ldl, labels, B, C,
-             loss_out, dlog, dl_dtype, ldd, argmax);
+             loss_out, dlog, dl_dtype, ldd, argmax, device_error_word());
     return launch_status();
   }
   if (B <= 256) {
     LaunchScope ls("xent", st, B, C);
-    launch_k(xent_single_block_kernel, dim3(1), dim3(256), 0, st, logits, ldl, labels, B, C, loss_out, dlog,
-                                                dl_dtype, ldd, argmax);
+    launch_k(xent_single_block_kernel, dim3(1), dim3(256), 0, st, logits, ldl, labels, B, C,
+             loss_out, dlog, dl_dtype, ldd, argmax, device_error_word());
     return launch_status();
   }
   const int blocks = (B + 7) / 8;
@@ -535,7 +547,8 @@ mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, i
   MLP_CHECK(launch_status());
   if (loss_out) {
     LaunchScope ls("sum_partials", st, blocks);
-    launch_k(sum_partials_kernel, dim3(1), dim3(256), 0, st, partial, blocks, (float)B, loss_out);
+    launch_k(sum_partials_kernel, dim3(1), dim3(256), 0, st, partial, blocks, (float)B, loss_out,
+             device_error_word());
     return launch_status();
   }
   return MLP_OK;
@@ -821,7 +834,8 @@ mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out
   MLP_CHECK(launch_status());
   if (loss_out) {
     LaunchScope ls("sum_partials", st, blocks);
-    launch_k(sum_partials_kernel, dim3(1), dim3(256), 0, st, partial, blocks, (float)n, loss_out);
+    launch_k(sum_partials_kernel, dim3(1), dim3(256), 0, st, partial, blocks, (float)n, loss_out,
+             device_error_word());
     return launch_status();
   }
   return MLP_OK;

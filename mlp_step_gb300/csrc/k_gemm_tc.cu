@@ -1231,9 +1231,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (warp == 2 && lane == 0 &&
               ptx::mbar_wait_bounded(xent_bar, (uint32_t)(xent_uses & 1), prog.wait_ns, prog.err,
-                                     DEVERR_TIMEOUT_EPILOGUE))
-            *loss_out = (((xent_part[0] + xent_part[1]) + xent_part[2]) + xent_part[3]) /
-                        (float)p.xent_norm;
+                                     DEVERR_TIMEOUT_EPILOGUE)) {
+            const float loss = (((xent_part[0] + xent_part[1]) + xent_part[2]) + xent_part[3]) /
+                               (float)p.xent_norm;
+            check_loss_finite(loss, prog.err);
+            *loss_out = loss;
+          }
           ++xent_uses;
         }
         ptx::tc_fence_before();

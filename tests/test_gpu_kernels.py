@@ -337,3 +337,37 @@ def test_colsum_linear_order_is_bit_exact(rows, cols, dtype, linear_order):
     M.mlp_colsum(Xd, out, workspace=ws)
     want = oracle.colsum_f32_linear(Xd.float().cpu().numpy())
     assert np.array_equal(out.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("B,C", [(100, 10), (200, 1000), (3000, 1000)])
+@pytest.mark.parametrize("bad", [float("inf"), float("nan")])
+def test_xent_nonfinite_logits_report_numeric(B, C, bad):
+    """Logits holding an infinity or a NaN give a non-finite loss; every path
+    of the loss kernel (one row per thread, one block, per-block partials)
+    records it for mlp_get_device_status as MLP_ERR_NUMERIC."""
+    Z = torch.from_numpy(synth.normal_f32((B, C), synth.STREAM_GENERIC + 9)).cuda()
+    Z[B // 2, 1] = bad
+    y = torch.from_numpy(synth.labels(B, C)).cuda()
+    loss = torch.zeros(4, device="cuda")
+    ws = torch.empty(max(M.softmax_xent_workspace_bytes(B, C), 16), dtype=torch.uint8,
+                     device="cuda")
+    M.softmax_xent_fwd_bwd(Z, y, loss, workspace=ws)
+    assert M.get_device_status() == M.MLP_ERR_NUMERIC
+    assert M.get_device_status() == M.MLP_OK
+    Z[B // 2, 1] = 0.0
+    M.softmax_xent_fwd_bwd(Z, y, loss, workspace=ws)
+    assert M.get_device_status() == M.MLP_OK
+    assert np.isfinite(loss[0].item())
+
+
+def test_mse_nonfinite_output_reports_numeric():
+    n = 512 * 64
+    yv = torch.from_numpy(synth.normal_f32((n,), synth.STREAM_BLOCK_X)).to(torch.bfloat16).cuda()
+    t = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    yv[77] = float("nan")
+    loss = torch.zeros(4, device="cuda")
+    dy = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(M.mse_workspace_bytes(n), dtype=torch.uint8, device="cuda")
+    M.mse_loss_fwd_bwd(yv, t, loss, dy, ws)
+    assert M.get_device_status() == M.MLP_ERR_NUMERIC
+    assert M.get_device_status() == M.MLP_OK
