@@ -8,13 +8,28 @@
 
 namespace {
 
-// Partial sums of the batch mean: one float per 8 rows (one block of 8 warps).
-constexpr int kMaxPartials = 65536;  // 256 KiB: batches up to 524,288 rows
+// Partial sums of the batch mean (as many floats as launch_xent's workspace
+// for the batch: one per 8 rows on the multi-block path).
+constexpr int kMaxPartials = 65536;  // 256 KiB
 static __device__ __align__(256) float g_xent_scratch[kMaxPartials];
+
+// Largest batch whose loss scratch fits g_xent_scratch, from the same
+// workspace function the workspace entry point uses (monotone in the batch).
+int max_batch() {
+  int lo = 0, hi = 1 << 30;
+  while (lo < hi) {
+    const int mid = lo + (hi - lo + 1) / 2;
+    if (mlp::xent_workspace_bytes(mid) <= sizeof(g_xent_scratch)) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
 
 // Device address of g_xent_scratch on the current device.  Host code only
 // sees a host-side stand-in under the array's name, so the address is looked
-// up once per device with cudaGetSymbolAddress (the device must be current).
+// up with cudaGetSymbolAddress (the device must be current) on the first call
+// on each device and kept for the life of the process; after a device reset
+// (cudaDeviceReset) the kept address is no longer valid.
 float* scratch_address(mlp_status* st) {
   static float* addr[64] = {};
   static std::mutex mu;
@@ -40,7 +55,10 @@ float* scratch_address(mlp_status* st) {
 
 extern "C" {
 
-int softmax_xent_noalloc_max_batch(void) { return kMaxPartials * 8; }
+int softmax_xent_noalloc_max_batch(void) {
+  static const int b = max_batch();
+  return b;
+}
 
 mlp_status softmax_xent_fwd_bwd_noalloc(const float* logits, int ld_logits,
                                         const int32_t* labels, int batch, int classes,
@@ -48,7 +66,7 @@ mlp_status softmax_xent_fwd_bwd_noalloc(const float* logits, int ld_logits,
                                         int ld_dlogits, int32_t* argmax_out, void* stream) {
   if (batch < 0 || classes <= 0) return MLP_ERR_INVALID_ARG;
   if (batch == 0) return MLP_OK;
-  if (batch > kMaxPartials * 8) return MLP_ERR_UNSUPPORTED_SHAPE;
+  if (mlp::xent_workspace_bytes(batch) > sizeof(g_xent_scratch)) return MLP_ERR_UNSUPPORTED_SHAPE;
   if (!logits || !labels || ld_logits < classes) return MLP_ERR_INVALID_ARG;
   if (dlogits && (ld_dlogits < classes ||
                   (dlogits_dtype != MLP_DTYPE_F32 && dlogits_dtype != MLP_DTYPE_BF16 &&
