@@ -196,6 +196,44 @@ def test_stack_step_matches_oracle_small():
     assert torch.equal(shadow, params.to(torch.bfloat16))
 
 
+def test_stack_eleven_blocks_matches_oracle():
+    """The 11-block stack over 6,144 tokens, the smallest token count at which
+    every kernel of the 262,144-token step runs in the same form: CTA-pair
+    forward, backward-activation and input-gradient kernels, and both
+    weight-gradient GEMMs split six ways over the tokens as at full size.
+    Loss, every block's W_gate and W_down gradients, the velocity and the
+    update against the fp64 oracle's stack and momentum step."""
+    nb, T, h = 11, 6144, 1536
+    x0 = bf16_values(synth.normal_f32((T, D), synth.STREAM_BLOCK_X)).astype(np.float32)
+    tgt = bf16_values(synth.normal_f32((T, D), synth.STREAM_TARGET)).astype(np.float32)
+    P = M.mlp_stack_param_count(nb, D, h)
+    p0 = bf16_values(synth.normal_f32((P,), synth.STREAM_BLOCK_WG, std=0.02)).astype(np.float32)
+    params = to_dev(p0)
+    vel = torch.zeros_like(params)
+    grads = torch.zeros_like(params)
+    shadow = params.to(torch.bfloat16)
+    ws = torch.empty(M.mlp_stack_workspace_bytes(nb, T, D, h), dtype=torch.uint8, device="cuda")
+    loss = torch.zeros(4, device="cuda")
+    lr, mom = 0.02, 0.95
+    M.mlp_stack_train_step(nb, T, D, h, to_dev(x0, torch.bfloat16), to_dev(tgt, torch.bfloat16),
+                           params, vel, grads, shadow, lr, mom, loss, ws, eps=EPS, slope=SLOPE)
+    torch.cuda.synchronize()
+    L_ref, g_ref, _ = oracle.stack_fwd_bwd(x0, p0, nb, D, h, EPS, SLOPE, tgt)
+    w_ref, v_ref = oracle.sgd_momentum(p0, g_ref, np.zeros(P), lr, mom)
+    assert abs(loss[0].item() - L_ref) <= 1e-3, (loss[0].item(), L_ref)
+    g = grads.cpu().numpy()
+    v = vel.cpu().numpy()
+    dw = params.cpu().numpy().astype(np.float64) - p0
+    per = 2 * D * h
+    for b in range(nb):
+        for part, sl in (("gate", slice(b * per, b * per + D * h)),
+                         ("down", slice(b * per + D * h, (b + 1) * per))):
+            assert rel_to_max(g[sl], g_ref[sl]) <= 3e-2, (b, part, rel_to_max(g[sl], g_ref[sl]))
+            assert rel_to_max(v[sl], v_ref[sl]) <= 3e-2, (b, part, "velocity")
+            assert rel_to_max(dw[sl], w_ref[sl] - p0[sl]) <= 3e-2, (b, part, "update")
+    assert torch.equal(shadow, params.to(torch.bfloat16))
+
+
 def test_stack_full_size_runs_finite():
     nb, T, h = 11, 262144, 1536
     P = M.mlp_stack_param_count(nb, D, h)
