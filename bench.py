@@ -16,6 +16,9 @@ Workloads (synthetic, seeded inputs; see synth.py):
                 65,536 tokens x 512
   attn_prep     fused attention preprocessing (RMSNorm -> QKV -> QK norm -> RoPE -> gain),
                 65,536 tokens x 512, 8 query / 4 key-value heads of 64
+  hbm           the memory-bound kernels (SGD, MSE, softmax cross entropy, column sum,
+                input cast) once each at full-config sizes; value = their total bytes
+                per second
 
 A bench "step" is one pass of the whole training step of the workload over its
 batch (for mlp784_epoch: the whole epoch).  The timed region is K steps, each
@@ -872,6 +875,116 @@ class StackStep(Workload):
                           % (n, T, self.nb))
 
 
+class HbmKernels(Workload):
+    """The step's memory-bound kernels, each at the size it runs at in the
+    largest configurations (every buffer above L2): momentum SGD over the
+    stack's 17,301,504 parameters with the bf16 shadow, the mean-squared loss
+    over 262,144 x 512, softmax cross entropy over 16,384 x 1000 with bf16 dZ,
+    a bf16 column sum over 16,384 x 8192 and the input cast of 262,144 images
+    of 1,024 bytes to bf16.  The bench step runs each once; the per-kernel
+    GB/s come from the library's event timing."""
+    name = "hbm"
+    unit = "GB/s"
+    dtype = "f32"
+
+    def __init__(self):
+        # algorithmic bytes of one step (GB): sgd 22 B per parameter; mse 6 B per
+        # element; xent 4 B read + 2 B written per logit, 8 B per row; column
+        # sum 2 B per element + 4 B per column; cast 1 B read + 2 B written per
+        # byte; the small net's two forward GEMMs read the cast input once and
+        # write their bf16 / fp32 outputs
+        nb = {"sgd": 22.0 * 17301504, "mse": 6.0 * 262144 * 512,
+              "xent": 6.0 * 16384 * 1000 + 8.0 * 16384, "colsum": 2.0 * 16384 * 8192 + 4 * 8192,
+              "cast": 3.0 * 262144 * 1024,
+              "gemm": 2.0 * 262144 * 1024 + 2.0 * 262144 * 16 * 2 + 4.0 * 262144 * 16}
+        self.samples_per_step = sum(nb.values()) / 1e9
+        self.config = {"workload": "memory-bound kernels at full-config sizes: sgd 17,301,504 "
+                                   "params (+bf16 shadow), mse 262144x512 bf16, softmax xent "
+                                   "16384x1000 fp32 -> bf16 dZ, column sum 16384x8192 bf16, "
+                                   "cast 262144x1024 u8 -> bf16 (+ the 1024-16-16 net's two "
+                                   "small forward GEMMs that read it); value = algorithmic "
+                                   "bytes of the step / step time",
+                       "algorithmic_bytes": nb,
+                       "cuda_graph": True, "l2": "every buffer above L2; flushed as well"}
+
+    def setup(self):
+        import torch
+        import mlp_step_gb300 as M
+        from mlp_step_gb300 import synth
+        self.M = M
+        bf = torch.bfloat16
+        n = 17301504
+        self.w = torch.from_numpy(synth.normal_f32((n,), synth.STREAM_BLOCK_WG, std=0.02)).cuda()
+        self.g = torch.from_numpy(synth.normal_f32((n,), synth.STREAM_GENERIC + 50,
+                                                   std=1e-3)).cuda()
+        self.v = torch.zeros_like(self.w)
+        self.wb = self.w.to(bf)
+        T, d = 262144, 512
+        self.y = torch.from_numpy(synth.normal_f32((T, d), synth.STREAM_BLOCK_X)).to(bf).cuda()
+        self.t = torch.from_numpy(synth.normal_f32((T, d), synth.STREAM_TARGET)).to(bf).cuda()
+        self.dy = torch.empty_like(self.y)
+        self.mse_ws = torch.empty(M.mse_workspace_bytes(T * d), dtype=torch.uint8, device="cuda")
+        self.loss = torch.zeros(4, device="cuda")
+        B, C = 16384, 1000
+        self.z = torch.from_numpy(synth.normal_f32((B, C), synth.STREAM_GENERIC + 51,
+                                                   std=3.0)).cuda()
+        self.lab = torch.from_numpy(synth.labels(B, C)).cuda()
+        self.dz = torch.empty(B, 1024, dtype=bf, device="cuda")
+        self.loss_xent = torch.zeros(4, device="cuda")
+        self.xent_ws = torch.empty(M.softmax_xent_workspace_bytes(B, C), dtype=torch.uint8,
+                                   device="cuda")
+        self.cs_x = torch.from_numpy(synth.uniform_f32((16384, 8192),
+                                                       synth.STREAM_GENERIC + 52)).to(bf).cuda()
+        self.cs_out = torch.empty(8192, device="cuda")
+        self.cs_ws = torch.empty(max(M.mlp_colsum_workspace_bytes(16384, 8192), 16),
+                                 dtype=torch.uint8, device="cuda")
+        self.net = M.MLP([1024, 16, 16], prec=M.MLP_PREC_BF16, max_batch=262144)
+        self.img = torch.from_numpy(synth.images_u8(262144, 1024)).cuda()
+        self.logits = torch.empty(262144, 16, device="cuda")
+        self.step_eager()
+        torch.cuda.synchronize()
+        self.graph = capture_graph(self)
+        c0 = M.launch_count()
+        self.step_eager()
+        self.launches_per_step = M.launch_count() - c0
+        torch.cuda.synchronize()
+
+    def step_eager(self):
+        M = self.M
+        M.sgd_momentum_step(self.w, self.g, self.v, 1e-3, 0.9, w_bf16=self.wb)
+        M.mse_loss_fwd_bwd(self.y, self.t, self.loss, self.dy, self.mse_ws)
+        M.softmax_xent_fwd_bwd(self.z, self.lab, self.loss_xent, dlogits=self.dz,
+                               workspace=self.xent_ws, classes=1000)
+        M.mlp_colsum(self.cs_x, self.cs_out, workspace=self.cs_ws)
+        self.net.forward(self.img, self.logits)
+
+    def step(self):
+        self.graph.replay()
+
+    def step_e2e(self):
+        self.graph.replay()
+
+    def check(self):
+        import torch
+        torch.cuda.synchronize()
+        assert self.M.get_device_status() == self.M.MLP_OK
+
+    def oracle_sample(self, budget_s):
+        import oracle
+        from mlp_step_gb300 import synth
+        n = 1 << 20
+        w = synth.normal_f32((n,), synth.STREAM_BLOCK_WG, std=0.02).astype(np.float64)
+        g = synth.normal_f32((n,), synth.STREAM_GENERIC + 50, std=1e-3).astype(np.float64)
+        v = np.zeros(n)
+        t0 = time.perf_counter()
+        done = 0
+        while time.perf_counter() - t0 < budget_s:
+            w, v = oracle.sgd_momentum(w, g, v, 1e-3, 0.9)
+            done += 22.0 * n
+        dt = time.perf_counter() - t0
+        return done / 1e9, dt, "oracle momentum SGD over 2^20 parameters (22 B each), fp64"
+
+
 WORKLOADS = {
     "mlp784_epoch": lambda: MLP784Epoch("bf16"),
     "mlp784_fp32": lambda: MLP784Epoch("fp32", n_images=128),
@@ -881,6 +994,7 @@ WORKLOADS = {
     "block": BlockStep,
     "attn_prep": AttnPrep,
     "stack": StackStep,
+    "hbm": HbmKernels,
 }
 SIZED = {"block": lambda T: BlockStep(T=T), "stack": lambda T: StackStep(T=T),
          "mlp_wide": lambda B: WideMLP(batch=B)}

@@ -250,6 +250,111 @@ def test_bf16_epoch_matches_step_sequence():
     assert M.get_device_status() == M.MLP_OK
 
 
+def _oracle_epoch(p0, X, y, B, perturb=0.0):
+    """Losses and final parameters of the oracle's epoch at the bf16 points,
+    the velocity carried from step to step; perturb scales the starting
+    weights by (1 + perturb * n_i) with n_i ~ N(0, 1) drawn once."""
+    p = p0.astype(np.float64)
+    if perturb:
+        p = p * (1.0 + perturb * synth.normal(9, synth.STREAM_GENERIC + 61, p.size))
+    v = np.zeros(p.size)
+    losses = []
+    for s in range((len(y) + B - 1) // B):
+        a, b = s * B, min(len(y), (s + 1) * B)
+        l, p, v, _ = oracle.mlp_train_step(DIMS, p, v, X[a:b], y[a:b], LR, MOM, bf16_points=True)
+        losses.append(l)
+    return np.array(losses), p
+
+
+def test_bf16_epoch_trajectory_matches_oracle():
+    """One epoch of 6,000 images ("Capstone 5", "Checked results, after the
+    prediction": 46 steps of batch 128 and one of 112, lr 0.1, momentum 0.9).
+
+    * Step by step: each of the 47 steps, run through the library, against the
+      oracle step (bf16 rounding points) started from the library's own
+      parameters and velocity before that step: loss within 1e-3, the update
+      and the new velocity within 3e-2 of their largest entry per tensor.
+    * mlp_train_epoch (all full steps in one launch) equals that step
+      sequence bit for bit.
+    * Free-running: the epoch against the oracle's own epoch.  At the bf16
+      points the method amplifies tiny changes of the weights (a 16-bit
+      rounding flips; measured: a 2^-24 relative change of the starting
+      weights moves the oracle's own loss by up to about 1e-2 within the
+      epoch), so the losses and the weights' change over the epoch are held
+      to 1e-3 (3e-2) plus four times that spread, measured here."""
+    B, n = 128, 6000
+    p0 = synth.mlp_flat_params(DIMS)
+    xb = synth.images_u8(n, 784)
+    y = synth.labels(n, 10)
+    X = bf16_values(_x_values(xb))
+    xd, yd = to_dev(xb), to_dev(y)
+    n_steps = (n + B - 1) // B
+    # the step sequence, state before every step kept
+    sq = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+    loss_s = torch.zeros(n_steps, 4, device="cuda")
+    states = []
+    for s in range(n_steps):
+        states.append((sq.params.double().cpu().numpy(), sq.velocity.double().cpu().numpy()))
+        a, b = s * B, min(n, (s + 1) * B)
+        sq.train_step(xd[a:b], yd[a:b], LR, MOM, loss_out=loss_s[s])
+    torch.cuda.synchronize()
+    states.append((sq.params.double().cpu().numpy(), sq.velocity.double().cpu().numpy()))
+    got_losses = loss_s[:, 0].double().cpu().numpy()
+    for s in range(n_steps):
+        a, b = s * B, min(n, (s + 1) * B)
+        (p_s, v_s), (p_n, v_n) = states[s], states[s + 1]
+        l_ref, p_ref, v_ref, _ = oracle.mlp_train_step(DIMS, p_s, v_s, X[a:b], y[a:b], LR, MOM,
+                                                       bf16_points=True)
+        assert abs(got_losses[s] - l_ref) <= 1e-3, (s, got_losses[s], l_ref)
+        for (name, g), (_, r) in zip(_segments(DIMS, p_n - p_s), _segments(DIMS, p_ref - p_s)):
+            assert rel_to_max(g, r) <= 3e-2, (s, "update", name, rel_to_max(g, r))
+        for (name, g), (_, r) in zip(_segments(DIMS, v_n), _segments(DIMS, v_ref)):
+            assert rel_to_max(g, r) <= 3e-2, (s, "velocity", name)
+    # the epoch call: bit for bit the step sequence
+    ep = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+    losses = torch.full((n_steps,), float("nan"), device="cuda")
+    ep.train_epoch(xd, yd, LR, MOM, B, losses_out=losses)
+    torch.cuda.synchronize()
+    assert torch.equal(losses, loss_s[:, 0])
+    for name in ("params", "velocity", "shadow"):
+        assert torch.equal(getattr(ep, name), getattr(sq, name)), name
+    # free-running, against the oracle's epoch and its own spread
+    ref_losses, p_ref = _oracle_epoch(p0, X, y, B)
+    pert_losses, p_pert = _oracle_epoch(p0, X, y, B, perturb=2.0 ** -24)
+    spread = np.abs(pert_losses - ref_losses).max()
+    assert np.abs(got_losses - ref_losses).max() <= 1e-3 + 4 * spread, (
+        np.abs(got_losses - ref_losses).max(), spread)
+    got = states[-1][0]
+    for (name, g), (_, r), (_, rp), (_, w0) in zip(_segments(DIMS, got), _segments(DIMS, p_ref),
+                                                   _segments(DIMS, p_pert),
+                                                   _segments(DIMS, p0)):
+        tol = 3e-2 + 4 * rel_to_max(rp - w0, r - w0)
+        assert rel_to_max(g - w0, r - w0) <= tol, (name, rel_to_max(g - w0, r - w0), tol)
+
+
+def test_nonfinite_loss_is_reported():
+    """A step whose loss is not finite returns MLP_OK from the call (the work
+    is enqueued) and MLP_ERR_NUMERIC from mlp_get_device_status ("Capstone
+    5", "The independent submission gate": exit code zero alone does not
+    prove the network is correct); the status is cleared by reading it."""
+    B = 128
+    p0 = synth.mlp_flat_params(DIMS)
+    x = torch.from_numpy(_x_values(synth.images_u8(B, 784))).cuda()
+    x[3, 100] = float("inf")
+    y = to_dev(synth.labels(B, 10))
+    for prec in (M.MLP_PREC_BF16, M.MLP_PREC_FP32):
+        net = M.MLP(DIMS, prec=prec, max_batch=B, params=torch.from_numpy(p0))
+        loss = torch.zeros(1, device="cuda")
+        net.train_step(x, y, LR, MOM, loss_out=loss)
+        assert M.get_device_status() == M.MLP_ERR_NUMERIC
+        assert not np.isfinite(loss.item())
+        assert M.get_device_status() == M.MLP_OK
+    # finite inputs leave the status clear
+    net = M.MLP(DIMS, prec=M.MLP_PREC_BF16, max_batch=B, params=torch.from_numpy(p0))
+    net.train_step(torch.from_numpy(_x_values(synth.images_u8(B, 784))).cuda(), y, LR, MOM)
+    assert M.get_device_status() == M.MLP_OK
+
+
 @pytest.mark.parametrize("rem", [0, 40])
 def test_bf16_epochs_with_even_step_counts_match_step_sequence(rem):
     """Epoch programs alternate two input buffers; after an even number of
