@@ -161,27 +161,73 @@ __device__ __forceinline__ float load_in(const void* src, int src_dtype, size_t 
 }
 
 // dst_dtype: MLP_DTYPE_F32, MLP_DTYPE_BF16 or MLP_DTYPE_F16.
+// byte / 255 for a 16-bit destination: the product with fp32(1/255) rounds to
+// the same bf16 and fp16 value as the IEEE quotient for every byte (checked
+// exhaustively by the host tests), and costs one multiply instead of a divide.
+__device__ __forceinline__ uint32_t bytes2_to_16(uint32_t w, int sh, int fmt) {
+  const float r = 1.0f / 255.0f;
+  return pack16x2_fmt((float)((w >> sh) & 0xffu) * r, (float)((w >> (sh + 8)) & 0xffu) * r, fmt);
+}
+
 __global__ void __launch_bounds__(256) cast_rows_kernel(const void* __restrict__ src,
                                                         int src_dtype, void* __restrict__ dst,
                                                         int dst_dtype, int rows, int cols,
                                                         int ld_dst) {
   pdl_wait();
   pdl_launch_dependents();
+  const bool d16 = dst_dtype != MLP_DTYPE_F32;
+  if (d16 && src_dtype == MLP_DTYPE_U8 && (cols & 15) == 0 && (ld_dst & 7) == 0) {
+    // the whole matrix as 16-byte input chunks: 16 bytes in, 32 bytes out per
+    // chunk, two chunks in flight per thread
+    const int cpr = cols >> 4;
+    const long long n = (long long)rows * cpr;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const uint8_t* s8 = static_cast<const uint8_t*>(src);
+    uint16_t* d16p = static_cast<uint16_t*>(dst);
+    for (long long q0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; q0 < n;
+         q0 += 2 * stride) {
+      uint4 in[2];
+      long long qq[2] = {q0, q0 + stride};
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (qq[k] < n) {
+          const long long r = qq[k] / cpr, c = qq[k] - r * cpr;
+          in[k] = __ldcs(reinterpret_cast<const uint4*>(s8 + r * cols) + c);
+        }
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (qq[k] < n) {
+          const long long r = qq[k] / cpr, c = qq[k] - r * cpr;
+          const uint32_t* w = reinterpret_cast<const uint32_t*>(&in[k]);
+          uint4 o0, o1;
+          o0.x = bytes2_to_16(w[0], 0, dst_dtype);
+          o0.y = bytes2_to_16(w[0], 16, dst_dtype);
+          o0.z = bytes2_to_16(w[1], 0, dst_dtype);
+          o0.w = bytes2_to_16(w[1], 16, dst_dtype);
+          o1.x = bytes2_to_16(w[2], 0, dst_dtype);
+          o1.y = bytes2_to_16(w[2], 16, dst_dtype);
+          o1.z = bytes2_to_16(w[3], 0, dst_dtype);
+          o1.w = bytes2_to_16(w[3], 16, dst_dtype);
+          uint4* dq = reinterpret_cast<uint4*>(d16p + r * ld_dst) + 2 * c;
+          dq[0] = o0;
+          dq[1] = o1;
+        }
+    }
+    return;
+  }
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const size_t si = (size_t)r * cols, di = (size_t)r * ld_dst;
-    const bool d16 = dst_dtype != MLP_DTYPE_F32;
     if (d16 && src_dtype == MLP_DTYPE_U8 && (cols & 7) == 0 && (ld_dst & 7) == 0) {
       // 8 bytes in, 8 16-bit values (16 bytes) out per thread
       const uint2* s8 = reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(src) + si);
       uint4* dq = reinterpret_cast<uint4*>(static_cast<uint16_t*>(dst) + di);
       for (int q = threadIdx.x; q < cols / 8; q += blockDim.x) {
         const uint2 b = s8[q];
-        const uint8_t* u = reinterpret_cast<const uint8_t*>(&b);
         uint4 o;
-        o.x = pack16x2_fmt((float)u[0] / 255.0f, (float)u[1] / 255.0f, dst_dtype);
-        o.y = pack16x2_fmt((float)u[2] / 255.0f, (float)u[3] / 255.0f, dst_dtype);
-        o.z = pack16x2_fmt((float)u[4] / 255.0f, (float)u[5] / 255.0f, dst_dtype);
-        o.w = pack16x2_fmt((float)u[6] / 255.0f, (float)u[7] / 255.0f, dst_dtype);
+        o.x = bytes2_to_16(b.x, 0, dst_dtype);
+        o.y = bytes2_to_16(b.x, 16, dst_dtype);
+        o.z = bytes2_to_16(b.y, 0, dst_dtype);
+        o.w = bytes2_to_16(b.y, 16, dst_dtype);
         dq[q] = o;
       }
     } else {
@@ -201,6 +247,15 @@ mlp_status launch_cast_rows(const void* src, int src_dtype, void* dst, int dst_d
   // destination rows, which the row-size checks there and 16-byte base
   // pointers (checked by the callers) guarantee
   int blocks = rows < num_sms() * 16 ? rows : num_sms() * 16;
+  if (dst_dtype != MLP_DTYPE_F32 && src_dtype == MLP_DTYPE_U8 && (cols & 15) == 0 &&
+      (ld_dst & 7) == 0) {
+    // flattened form: enough 256-thread blocks for two 16-byte chunks per
+    // thread, at most 8 per SM
+    const long long chunks = (long long)rows * (cols >> 4);
+    const long long want = (chunks + 511) / 512;
+    blocks = (int)(want < (long long)num_sms() * 8 ? want : (long long)num_sms() * 8);
+    if (blocks < 1) blocks = 1;
+  }
   LaunchScope ls("cast", st, (long long)rows * cols);
   launch_k(cast_rows_kernel, dim3(blocks), dim3(256), 0, st, src, src_dtype, dst, dst_dtype, rows,
            cols, ld_dst);
@@ -294,6 +349,14 @@ __device__ __forceinline__ float xent_row_regs(const float* __restrict__ z, int 
   }
   best = warp_argmax(best);
   const float m = best.v;
+  // the label's logit from the lane that holds it (no second read of the row)
+  float zy = 0.f;
+#pragma unroll
+  for (int g = 0; g < NSEG; ++g)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (g * 128 + lane * 4 + e == label) zy = v[g][e];
+  zy = __shfl_sync(0xffffffffu, zy, (label & 127) >> 2);
   float s = 0.f;
 #pragma unroll
   for (int g = 0; g < NSEG; ++g)
@@ -304,15 +367,17 @@ __device__ __forceinline__ float xent_row_regs(const float* __restrict__ z, int 
       s += v[g][e];
     }
   s = warp_sum(s);
-  const float loss = m + logf(s) - z[label];
+  const float loss = m + logf(s) - zy;
   if (dlog_row) {
+    // softmax as exp(z - m) times the row's 1/s (one division per row)
+    const float inv_s = 1.0f / s;
 #pragma unroll
     for (int g = 0; g < NSEG; ++g) {
       const int c0 = g * 128 + lane * 4;
       float d[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        d[e] = c0 + e < C ? (v[g][e] / s - (c0 + e == label ? 1.f : 0.f)) * inv_norm : 0.f;
+        d[e] = c0 + e < C ? (v[g][e] * inv_s - (c0 + e == label ? 1.f : 0.f)) * inv_norm : 0.f;
       if (c0 + 3 < ldd) {
         if (dl_dtype) {
           uint2 o;
@@ -340,22 +405,24 @@ __device__ __forceinline__ float xent_row_regs(const float* __restrict__ z, int 
   return loss;
 }
 
+// Warp w of block b takes rows b * 8 + w, then every 8 * gridDim.x-th row
+// after it (three blocks per SM)
+// and adds their losses in that order; partial[b] is the block's sum.
 template <int NSEG>
-__global__ void __launch_bounds__(256) xent_rows_regs_kernel(
+__global__ void __launch_bounds__(256, 3) xent_rows_regs_kernel(
     const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
     float* __restrict__ partial, void* dlog, int dl_dtype, int ldd, int* argmax) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ float part[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * 8 + warp;
   float li = 0.f;
-  if (r < B) {
+  for (int r = blockIdx.x * 8 + warp; r < B; r += gridDim.x * 8) {
     void* drow = nullptr;
     if (dlog) drow = dl_dtype ? (void*)(static_cast<uint16_t*>(dlog) + (size_t)r * ldd)
                              : (void*)(static_cast<float*>(dlog) + (size_t)r * ldd);
-    li = xent_row_regs<NSEG>(logits + (size_t)r * ldl, labels[r], C, 1.0f / (float)B, drow,
-                             dl_dtype, ldd, argmax ? argmax + r : nullptr, lane);
+    li += xent_row_regs<NSEG>(logits + (size_t)r * ldl, labels[r], C, 1.0f / (float)B, drow,
+                              dl_dtype, ldd, argmax ? argmax + r : nullptr, lane);
   }
   if (lane == 0) part[warp] = li;
   __syncthreads();
@@ -528,10 +595,13 @@ mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, i
              loss_out, dlog, dl_dtype, ldd, argmax, device_error_word());
     return launch_status();
   }
-  const int blocks = (B + 7) / 8;
+  int blocks = (B + 7) / 8;
   float* partial = static_cast<float*>(ws);
   const bool vec = C <= 1024 && (ldl % 4) == 0 && aligned16(logits) &&
                    (!dlog || ((ldd % 4) == 0 && aligned16(dlog)));
+  // the register-resident rows kernel loops over rows: one wave of blocks
+  // (at most as many partials as the workspace holds, one per 8 rows)
+  if (vec && blocks > num_sms() * 3) blocks = num_sms() * 3;
   {
   LaunchScope ls("xent", st, B, C);
   if (vec && C <= 256)

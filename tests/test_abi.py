@@ -213,3 +213,17 @@ def test_reduction_order_switch(lib):
     finally:
         M.set_reduction_order(M.MLP_ORDER_FAST)
     assert M.get_reduction_order() == M.MLP_ORDER_FAST
+
+
+def test_byte_scaling_by_reciprocal_rounds_like_division():
+    """The cast of image bytes to a 16-bit operand multiplies by fp32(1/255)
+    instead of dividing by 255: for every byte the product rounds to the same
+    bf16 and fp16 value as the IEEE fp32 quotient byte / 255 (the value the
+    oracle and the fp32 path use), so the shortcut changes no result."""
+    import numpy as np
+    import torch
+    b = np.arange(256, dtype=np.float32)
+    q = b / np.float32(255)
+    m = b * (np.float32(1) / np.float32(255))
+    for dt in (torch.bfloat16, torch.float16):
+        assert torch.equal(torch.from_numpy(q).to(dt), torch.from_numpy(m).to(dt)), dt
