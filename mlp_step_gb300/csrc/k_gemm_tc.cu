@@ -99,20 +99,50 @@ __device__ __forceinline__ void rope_sincos(float a, float& sn, float& cs) {
   __sincosf(r, &sn, &cs);
 }
 
+// The RoPE rotation of one token: sin and cos of pos * theta^(-2i/R) for the
+// R/2 pairs, the same for every query and key head of the token.  For R up to
+// 32 they are computed once per tile and kept in registers for the warp's
+// heads; for R = 64 (32 pairs) each head computes them again (keeping 64 more
+// registers live would spill).
+template <int R>
+struct RopeAngles {
+  static constexpr bool kept = R <= 32;
+  float sn[kept ? R / 2 : 1], cs[kept ? R / 2 : 1];
+  float pos, log2_theta;
+};
+
+__device__ __forceinline__ void rope_angle(int i, int R, float pos, float log2_theta, float& sn,
+                                           float& cs) {
+  const float freq = exp2f(-(float)(2 * i) / (float)R * log2_theta);
+  rope_sincos(pos * freq, sn, cs);
+}
+
+template <int R>
+__device__ __forceinline__ void rope_angles(float pos, float log2_theta, RopeAngles<R>& ra) {
+  ra.pos = pos;
+  ra.log2_theta = log2_theta;
+  if constexpr (RopeAngles<R>::kept) {
+#pragma unroll
+    for (int i = 0; i < R / 2; ++i) rope_angle(i, R, pos, log2_theta, ra.sn[i], ra.cs[i]);
+  }
+}
+
 // One head of one token, 64 values (va: columns 0-31, vb: 32-63), already
-// scaled by the token's RMSNorm factor: divide by the head's RMS, rotate the
-// pairs (i, i + R/2) for i < R/2 by pos * theta^(-2i/R) (rotate-half RoPE on
-// the first R dims), multiply by gain.  R is a compile-time constant so the
+// scaled by the token's RMSNorm factor: divide by the head's RMS (the sum of
+// squares in four interleaved partial sums, added pairwise), rotate the pairs
+// (i, i + R/2) for i < R/2 by the token's angles (rotate-half RoPE on the
+// first R dims), multiply by gain.  R is a compile-time constant so the
 // partner of every element is a fixed register.
 template <int R>
-__device__ __forceinline__ void attn_head(float (&va)[32], float (&vb)[32], float gain, float pos,
-                                          float log2_theta, float eps) {
+__device__ __forceinline__ void attn_head(float (&va)[32], float (&vb)[32], float gain,
+                                          const RopeAngles<R>& ra, float eps) {
   static_assert(R % 2 == 0 && R <= 64, "rope dims");
-  float ss = 0.f;
+  float ss4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < 32; ++j) ss = fmaf(va[j], va[j], ss);
+  for (int j = 0; j < 32; ++j) ss4[j & 3] = fmaf(va[j], va[j], ss4[j & 3]);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) ss = fmaf(vb[j], vb[j], ss);
+  for (int j = 0; j < 32; ++j) ss4[j & 3] = fmaf(vb[j], vb[j], ss4[j & 3]);
+  const float ss = (ss4[0] + ss4[1]) + (ss4[2] + ss4[3]);
   const float inv = 1.0f / sqrtf(ss * (1.0f / 64.0f) + eps);
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
@@ -121,12 +151,16 @@ __device__ __forceinline__ void attn_head(float (&va)[32], float (&vb)[32], floa
   }
 #pragma unroll
   for (int i = 0; i < R / 2; ++i) {
-    const float freq = exp2f(-(float)(2 * i) / (float)R * log2_theta);
-    float sn, cs;
-    rope_sincos(pos * freq, sn, cs);
     constexpr int H = R / 2;
     float& x1 = i < 32 ? va[i] : vb[i - 32];
     float& x2 = i + H < 32 ? va[i + H] : vb[i + H - 32];
+    float sn, cs;
+    if constexpr (RopeAngles<R>::kept) {
+      sn = ra.sn[i];
+      cs = ra.cs[i];
+    } else {
+      rope_angle(i, R, ra.pos, ra.log2_theta, sn, cs);
+    }
     const float a = x1, b = x2;
     x1 = a * cs - b * sn;
     x2 = b * cs + a * sn;
@@ -1567,6 +1601,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           }
           ++stg_count;
         };
+        // this token's rotation, computed once for the warp's heads of the tile
+        RopeAngles<EPI> angles;
+        if (tn * BN2 + c_half < ae.n_qk * 64) rope_angles<EPI>(pos, l2t, angles);
         for (int hc = c_half; hc < c_half + BN2 / 2; hc += 64) {
           const int n0 = tn * BN2 + hc;
           if (n0 >= p.N) break;  // warp-uniform
@@ -1585,7 +1622,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           }
           const int head = n0 >> 6;
           if (head < ae.n_qk)  // warp-uniform: query and key heads
-            attn_head<EPI>(va, vb, head < ae.n_q ? __ldg(ae.q_gain + head) : 1.0f, pos, l2t,
+            attn_head<EPI>(va, vb, head < ae.n_q ? __ldg(ae.q_gain + head) : 1.0f, angles,
                            ae.eps);
           store_piece(va, n0);
           store_piece(vb, n0 + 32);
