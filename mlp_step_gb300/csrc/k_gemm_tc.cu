@@ -1334,13 +1334,16 @@ constexpr int BN2 = 256;
 // lane quadrant, each draining 128 of the 256 accumulator columns)
 constexpr int kPairThreads = 320;
 
-template <int STAGES>
+// STG_WARP: staging bytes per epilogue warp: 4 KiB (two 32 x 32 bf16 boxes or
+// one fp32 box) for the GEMM epilogue, 8 KiB (two 32 x 64 bf16 boxes: a whole
+// head per store) for the attention epilogue.
+template <int STAGES, int STG_WARP = 4096>
 struct Layout2 {
   static constexpr int A_BYTES = 128 * BK * 2;
   static constexpr int B_BYTES = 128 * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int BAR_BYTES = 2048;        // barriers, then 8 x 32 bias floats at 512
-  static constexpr int STG_BYTES = 8 * 4096;    // per epilogue warp: 2 x 2 KiB (bf16) / 4 KiB (fp32)
+  static constexpr int STG_BYTES = 8 * STG_WARP;
   static constexpr int SMEM_BASE = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
   static constexpr int SMEM = SMEM_BASE + STG_BYTES;
 };
@@ -1353,7 +1356,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const TcParams p,
                         const AttnEpi ae) {
-  using L = Layout2<STAGES>;
+  using L = Layout2<STAGES, (EPI > 0 ? 8192 : 4096)>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -1579,20 +1582,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const float rs = m < p.M ? __ldg(ae.rstd + m) : 0.f;
         const float pos = (float)(m < p.M ? m % ae.seq_len : 0);
         const float l2t = log2f(ae.theta);
-        // a 32-column piece of bf16 / fp16 output, through the staging boxes
-        // and a TMA store for large outputs, else straight from registers
-        auto store_piece = [&](const float (&v)[32], int nn) {
+        // a head's 64 bf16 / fp16 outputs: one 32 x 64 staging box (128-byte
+        // rows, 128-byte swizzle) and one TMA store for large outputs, else
+        // straight from registers
+        auto store_head = [&](const float (&va)[32], const float (&vb)[32], int nn) {
           if (!p.tma_store) {
-            if (m < p.M) epilogue_store_regs<H16>(p, m, nn, v);
+            if (m < p.M) {
+              epilogue_store_regs<H16>(p, m, nn, va);
+              epilogue_store_regs<H16>(p, m, nn + 32, vb);
+            }
             return;
           }
           if (row0 >= p.M) return;  // warp-uniform; rows past M are clipped by TMA
-          uint8_t* box = stg + (warp - 2) * 4096 + (stg_count & 1) * 2048;
+          uint8_t* box = stg + (warp - 2) * 8192 + (stg_count & 1) * 4096;
           if (stg_count >= 2) {
             if (lane == 0) ptx::bulk_wait_group_read<1>();
             __syncwarp();
           }
-          epilogue_stage_row<H16>(box, 1, lane, v);
+          uint8_t* row = box + lane * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float* v = q < 4 ? &va[q * 8] : &vb[(q - 4) * 8];
+            uint4 o;
+            o.x = pack16x2<H16>(v[0], v[1]);
+            o.y = pack16x2<H16>(v[2], v[3]);
+            o.z = pack16x2<H16>(v[4], v[5]);
+            o.w = pack16x2<H16>(v[6], v[7]);
+            *reinterpret_cast<uint4*>(row + ((q ^ (lane & 7)) << 4)) = o;
+          }
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -1624,8 +1641,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           if (head < ae.n_qk)  // warp-uniform: query and key heads
             attn_head<EPI>(va, vb, head < ae.n_q ? __ldg(ae.q_gain + head) : 1.0f, angles,
                            ae.eps);
-          store_piece(va, n0);
-          store_piece(vb, n0 + 32);
+          store_head(va, vb, n0);
         }
       }
       ptx::tc_fence_before();
@@ -1731,7 +1747,8 @@ mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
 template <int STAGES, int H16, int EPI = 0>
 mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                        const TcParams& p, cudaStream_t st, const AttnEpi& ae = AttnEpi{}) {
-  using L = Layout2<STAGES>;
+  using L = Layout2<STAGES, (EPI > 0 ? 8192 : 4096)>;
+  static_assert(L::SMEM <= 232448, "pair kernel shared memory");
   static bool configured = false;
   static int max_pairs = 0;
   if (!configured) {
@@ -2092,11 +2109,12 @@ mlp_status launch_attn_prep_gemm(const GemmArgs& g, const float* rstd, const flo
   memset(&tc, 0, sizeof(tc));
   p.tma_store = 0;
   if ((long long)g.M * g.N >= (1ll << 20) && ((long long)g.ldc * 2) % 16 == 0 && aligned16(g.C)) {
-    if (!encode_tmap_out_2d(&tc, g.C, 0, g.N, g.M, (unsigned long long)g.ldc * 2, 32, 32))
+    // one head (64 columns) per store: 32 x 64 boxes, 128-byte swizzle
+    if (!encode_tmap_bf16_2d(&tc, g.C, g.N, g.M, (unsigned long long)g.ldc * 2, 64, 32))
       return MLP_ERR_CUDA;
     p.tma_store = 1;
   }
-  AttnEpi ae;
+  AttnEpi ae{};
   ae.rstd = rstd;
   ae.q_gain = q_gain;
   ae.n_q = n_q;
@@ -2105,9 +2123,9 @@ mlp_status launch_attn_prep_gemm(const GemmArgs& g, const float* rstd, const flo
   ae.eps = eps;
   ae.theta = theta;
   switch (rope_dims) {
-    case 16: return launch_pair<6, 0, 16>(ta, tb, tc, p, st, ae);
-    case 32: return launch_pair<6, 0, 32>(ta, tb, tc, p, st, ae);
-    default: return launch_pair<6, 0, 64>(ta, tb, tc, p, st, ae);
+    case 16: return launch_pair<5, 0, 16>(ta, tb, tc, p, st, ae);
+    case 32: return launch_pair<5, 0, 32>(ta, tb, tc, p, st, ae);
+    default: return launch_pair<5, 0, 64>(ta, tb, tc, p, st, ae);
   }
 }
 
