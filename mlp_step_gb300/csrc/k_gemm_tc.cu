@@ -99,43 +99,44 @@ __device__ __forceinline__ void rope_sincos(float a, float& sn, float& cs) {
   __sincosf(r, &sn, &cs);
 }
 
-// The RoPE rotation of one token: sin and cos of pos * theta^(-2i/R) for the
-// R/2 pairs, the same for every query and key head of the token.  For R up to
-// 32 they are computed once per tile and kept in registers for the warp's
-// heads; for R = 64 (32 pairs) each head computes them again (keeping 64 more
-// registers live would spill).
+// The RoPE rotation of one token: sin and cos of pos * f_i for the R/2 pairs,
+// f_i = theta^(-2i/R) (the same for every token: computed once per CTA into
+// shared memory), the same for every query and key head of the token.  For R
+// up to 32 they are computed once per tile and kept in registers for the
+// warp's heads; for R = 64 (32 pairs) each head computes them again (keeping
+// 64 more registers live would spill).
 template <int R>
 struct RopeAngles {
   static constexpr bool kept = R <= 32;
   float sn[kept ? R / 2 : 1], cs[kept ? R / 2 : 1];
-  float pos, log2_theta;
+  float pos;
+  const float* freq;  // shared memory, R/2 values
 };
 
-__device__ __forceinline__ void rope_angle(int i, int R, float pos, float log2_theta, float& sn,
-                                           float& cs) {
-  const float freq = exp2f(-(float)(2 * i) / (float)R * log2_theta);
-  rope_sincos(pos * freq, sn, cs);
+__device__ __forceinline__ float rope_freq(int i, int R, float log2_theta) {
+  return exp2f(-(float)(2 * i) / (float)R * log2_theta);
 }
 
 template <int R>
-__device__ __forceinline__ void rope_angles(float pos, float log2_theta, RopeAngles<R>& ra) {
+__device__ __forceinline__ void rope_angles(float pos, const float* freq, RopeAngles<R>& ra) {
   ra.pos = pos;
-  ra.log2_theta = log2_theta;
+  ra.freq = freq;
   if constexpr (RopeAngles<R>::kept) {
 #pragma unroll
-    for (int i = 0; i < R / 2; ++i) rope_angle(i, R, pos, log2_theta, ra.sn[i], ra.cs[i]);
+    for (int i = 0; i < R / 2; ++i) rope_sincos(pos * freq[i], ra.sn[i], ra.cs[i]);
   }
 }
 
-// One head of one token, 64 values (va: columns 0-31, vb: 32-63), already
-// scaled by the token's RMSNorm factor: divide by the head's RMS (the sum of
-// squares in four interleaved partial sums, added pairwise), rotate the pairs
-// (i, i + R/2) for i < R/2 by the token's angles (rotate-half RoPE on the
-// first R dims), multiply by gain.  R is a compile-time constant so the
-// partner of every element is a fixed register.
+// One head of one token, 64 accumulator values (va: columns 0-31, vb: 32-63)
+// before the token's RMSNorm factor rs: rotates the pairs (i, i + R/2) for
+// i < R/2 by the token's angles (rotate-half RoPE on the first R dims) in
+// place and returns the one factor that finishes the head, rs / RMS(rs v) *
+// gain (RoPE is a rotation, so scaling before or after it is the same).  The
+// sum of squares runs in four interleaved partial sums, added pairwise.  R is
+// a compile-time constant so the partner of every element is a fixed register.
 template <int R>
-__device__ __forceinline__ void attn_head(float (&va)[32], float (&vb)[32], float gain,
-                                          const RopeAngles<R>& ra, float eps) {
+__device__ __forceinline__ float attn_head(float (&va)[32], float (&vb)[32], float rs, float gain,
+                                           const RopeAngles<R>& ra, float eps) {
   static_assert(R % 2 == 0 && R <= 64, "rope dims");
   float ss4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -143,12 +144,7 @@ __device__ __forceinline__ void attn_head(float (&va)[32], float (&vb)[32], floa
 #pragma unroll
   for (int j = 0; j < 32; ++j) ss4[j & 3] = fmaf(vb[j], vb[j], ss4[j & 3]);
   const float ss = (ss4[0] + ss4[1]) + (ss4[2] + ss4[3]);
-  const float inv = 1.0f / sqrtf(ss * (1.0f / 64.0f) + eps);
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    va[j] *= inv;
-    vb[j] *= inv;
-  }
+  const float inv = 1.0f / sqrtf(rs * rs * ss * (1.0f / 64.0f) + eps);
 #pragma unroll
   for (int i = 0; i < R / 2; ++i) {
     constexpr int H = R / 2;
@@ -159,17 +155,13 @@ __device__ __forceinline__ void attn_head(float (&va)[32], float (&vb)[32], floa
       sn = ra.sn[i];
       cs = ra.cs[i];
     } else {
-      rope_angle(i, R, ra.pos, ra.log2_theta, sn, cs);
+      rope_sincos(ra.pos * ra.freq[i], sn, cs);
     }
     const float a = x1, b = x2;
     x1 = a * cs - b * sn;
     x2 = b * cs + a * sn;
   }
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    va[j] *= gain;
-    vb[j] *= gain;
-  }
+  return rs * inv * gain;
 }
 
 template <int BN, int STAGES>
@@ -1336,47 +1328,84 @@ constexpr int kPairThreads = 320;
 
 // STG_WARP: staging bytes per epilogue warp: 4 KiB (two 32 x 32 bf16 boxes or
 // one fp32 box) for the GEMM epilogue, 8 KiB (two 32 x 64 bf16 boxes: a whole
-// head per store) for the attention epilogue.
-template <int STAGES, int STG_WARP = 4096>
+// head per store) for the streamed attention epilogue, 4 KiB (one such box)
+// for the attention epilogue with resident weights.  B_RES: k-blocks of B held
+// for the whole tile column (0: B streams through the stages with A).
+template <int STAGES, int STG_WARP = 4096, int B_RES = 0>
 struct Layout2 {
   static constexpr int A_BYTES = 128 * BK * 2;
   static constexpr int B_BYTES = 128 * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int B_BLOCKS = B_RES > 0 ? B_RES : STAGES;
   static constexpr int BAR_BYTES = 2048;        // barriers, then 8 x 32 bias floats at 512
   static constexpr int STG_BYTES = 8 * STG_WARP;
-  static constexpr int SMEM_BASE = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int SMEM_BASE = 1024 + STAGES * A_BYTES + B_BLOCKS * B_BYTES + BAR_BYTES;
   static constexpr int SMEM = SMEM_BASE + STG_BYTES;
 };
 
+// Resident-B attention projection: K up to 8 k-blocks (512) of the CTA's 128
+// weight columns stay in shared memory while the pair walks down a column of
+// tiles, so only the token rows stream (half the operand bytes per tile).
+constexpr int kBResBlocks = 8;
+
+template <int STAGES, int EPI, bool BRES>
+using PairLayout = Layout2<STAGES, (EPI > 0 && !BRES ? 8192 : 4096), (BRES ? kBResBlocks : 0)>;
+
+// The units (tiles x splits) of one CTA pair: every n_pairs-th unit of the
+// grouped raster, or, with resident B, a contiguous run of the column-major
+// tile order (a run changes tile column at most a few times, and not at all
+// when the pair count is a multiple of the column count).
+struct PairUnits {
+  int begin, end, stride;
+};
+
+__device__ __forceinline__ PairUnits pair_units(int pair, int n_pairs, int units, bool bres) {
+  if (!bres) return {pair, units, n_pairs};
+  return {(int)((long long)pair * units / n_pairs), (int)((long long)(pair + 1) * units / n_pairs),
+          1};
+}
+
+__device__ __forceinline__ void pair_tile(const TcParams& p, int u, bool bres, int& tm, int& tn) {
+  if (bres) {
+    tn = u / p.tiles_m;
+    tm = u - tn * p.tiles_m;
+  } else {
+    tile_coords(u / p.splits, p.tiles_m, p.tiles_n, tm, tn);
+  }
+}
+
 // EPI = 0: the GEMM epilogue (bias, activation, mask, split-K partials);
 // EPI = R > 0: the fused attention preprocessing with R RoPE dims (ae).
-template <int STAGES, int H16, int EPI>
+template <int STAGES, int H16, int EPI, bool BRES = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const TcParams p,
                         const AttnEpi ae) {
-  using L = Layout2<STAGES, (EPI > 0 ? 8192 : 4096)>;
+  static_assert(!BRES || EPI > 0, "resident B is the attention projection's");
+  using L = PairLayout<STAGES, EPI, BRES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * L::A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * L::B_BYTES);
-  uint8_t* stg = sB + STAGES * L::B_BYTES + L::BAR_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + L::B_BLOCKS * L::B_BYTES);
+  uint8_t* stg = sB + L::B_BLOCKS * L::B_BYTES + L::BAR_BYTES;
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* bfree = done + 1;  // resident B: the MMAs reading it have completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bfree + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sbias = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);
+  float* sfreq = sbias;  // attention: the RoPE frequencies (no bias there)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
   const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
   const int units = p.num_tiles * p.splits;
+  const PairUnits ur = pair_units(pair, n_pairs, units, BRES);
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -1388,7 +1417,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       ptx::mbar_init(&tempty[a], 16);  // the pair's 16 epilogue warps
     }
     ptx::mbar_init(done, 1);
+    ptx::mbar_init(bfree, 1);
     *s_abort = 0;
+  }
+  if constexpr (EPI > 0) {
+    if (threadIdx.x < EPI / 2) sfreq[threadIdx.x] = rope_freq(threadIdx.x, EPI, log2f(ae.theta));
+  }
+  if (warp == 0 && lane == 0) {
     ptx::fence_mbar_init();
     ptx::prefetch_tensormap(&tmA);
     ptx::prefetch_tensormap(&tmB);
@@ -1411,13 +1446,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const uint32_t full0 = ptx::mapa_shared(ptx::smem_u32(full), 0);  // the even CTA's full[]
       int stage = 0;
       uint32_t phase = 0;
-      for (int u = pair; u < units && !*s_abort; u += n_pairs) {
+      int b_tn = -1, b_loads = 0;  // resident B: its tile column, and how often it was loaded
+      for (int u = ur.begin; u < ur.end && !*s_abort; u += ur.stride) {
         int tm, tn;
-        tile_coords(u / p.splits, p.tiles_m, p.tiles_n, tm, tn);
+        pair_tile(p, u, BRES, tm, tn);
         const int kb0 = (u % p.splits) * p.kb_per_split;
         const int kb1 = min(p.k_blocks, kb0 + p.kb_per_split);
         const int m0 = tm * 256 + (int)rank * 128;
         const int n0 = tn * BN2 + (int)rank * 128;
+        // resident B: a new tile column is loaded with this unit's A stages,
+        // once the pair's MMAs on the old one have completed
+        const bool load_b = !BRES || tn != b_tn;
+        if constexpr (BRES) {
+          // the next unit's token rows into L2 while this unit's stream:
+          // their loads then wait on L2 rather than on DRAM
+          if (u + 1 < ur.end && !p.a_mn) {
+            const int m_next = ((u + 1) % p.tiles_m) * 256 + (int)rank * 128;
+            for (int kb = kb0; kb < kb1; ++kb) ptx::tma_prefetch_2d(&tmA, kb * BK, m_next);
+          }
+        }
+        if (BRES && load_b) {
+          if (b_loads > 0 &&
+              !ptx::mbar_wait_cluster_bounded(bfree, (uint32_t)((b_loads - 1) & 1), p.wait_ns,
+                                              p.err, DEVERR_TIMEOUT_PRODUCER)) {
+            *s_abort = 1;
+            break;
+          }
+          b_tn = tn;
+          ++b_loads;
+        }
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait_cluster_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err,
                                               DEVERR_TIMEOUT_PRODUCER)) {
@@ -1425,20 +1482,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             break;
           }
           if (rank == 0) {
-            ptx::mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
+            ptx::mbar_arrive_expect_tx(&full[stage],
+                                       2 * (L::A_BYTES + (load_b ? L::B_BYTES : 0)));
             last_parity[stage] = (int)phase;
           }
           const uint32_t bar = full0 + (uint32_t)stage * 8u;
           const int k0 = kb * BK;
           uint8_t* a_dst = sA + stage * L::A_BYTES;
-          uint8_t* b_dst = sB + stage * L::B_BYTES;
+          uint8_t* b_dst = sB + (BRES ? kb : stage) * L::B_BYTES;
           if (!p.a_mn) {
             ptx::tma_load_2d_pair(a_dst, &tmA, bar, k0, m0);
           } else {
             ptx::tma_load_2d_pair(a_dst, &tmA, bar, m0, k0);
             ptx::tma_load_2d_pair(a_dst + 8192, &tmA, bar, m0 + 64, k0);
           }
-          if (!p.b_mn) {
+          if (!load_b) {
+          } else if (!p.b_mn) {
             ptx::tma_load_2d_pair(b_dst, &tmB, bar, k0, n0);
           } else {
             ptx::tma_load_2d_pair(b_dst, &tmB, bar, n0, k0);
@@ -1459,7 +1518,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int u = pair; u < units && !*s_abort; u += n_pairs) {
+      for (int u = ur.begin; u < ur.end && !*s_abort; u += ur.stride) {
         if (!ptx::mbar_wait_cluster_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err,
                                             DEVERR_TIMEOUT_MMA)) {
           *s_abort = 1;
@@ -1478,7 +1537,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           }
           ptx::tc_fence_after();
           const uint32_t a_base = ptx::smem_u32(sA + stage * L::A_BYTES);
-          const uint32_t b_base = ptx::smem_u32(sB + stage * L::B_BYTES);
+          const uint32_t b_base = ptx::smem_u32(sB + (BRES ? kb : stage) * L::B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = ptx::sw128_desc(a_base + k * a_kstep, a_lbo, 1024);
@@ -1491,6 +1550,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         if (!ok) break;
         ptx::mma_commit_pair_multicast(&tfull[acc], 3);
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        if constexpr (BRES) {
+          // the next unit starts a new tile column: both producers may
+          // overwrite their B once these MMAs have completed
+          if (u + 1 < ur.end && (u + 1) / p.tiles_m != u / p.tiles_m)
+            ptx::mma_commit_pair_multicast(bfree, 3);
+        }
       }
       ptx::mma_commit_pair_multicast(done, 1);
       ptx::mbar_wait_bounded(done, 0, p.wait_ns, p.err, DEVERR_TIMEOUT_TEARDOWN);
@@ -1502,7 +1567,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int stg_count = 0;
-    for (int u = pair; u < units; u += n_pairs) {
+    for (int u = ur.begin; u < ur.end; u += ur.stride) {
       if (*s_abort) break;
       if (!ptx::mbar_wait_cluster_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err,
                                           DEVERR_TIMEOUT_EPILOGUE)) {
@@ -1511,7 +1576,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       }
       ptx::tc_fence_after();
       int tm, tn;
-      tile_coords(u / p.splits, p.tiles_m, p.tiles_n, tm, tn);
+      pair_tile(p, u, BRES, tm, tn);
       float* part = p.splits > 1 ? p.partial + (size_t)(u % p.splits) * p.M * p.ldp : nullptr;
       const int row0 = tm * 256 + (int)rank * 128 + quarter * 32;  // this warp's first row
       const int m = row0 + lane;
@@ -1581,22 +1646,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         // fused attention preprocessing: one 64-column head per step
         const float rs = m < p.M ? __ldg(ae.rstd + m) : 0.f;
         const float pos = (float)(m < p.M ? m % ae.seq_len : 0);
-        const float l2t = log2f(ae.theta);
         // a head's 64 bf16 / fp16 outputs: one 32 x 64 staging box (128-byte
         // rows, 128-byte swizzle) and one TMA store for large outputs, else
         // straight from registers
-        auto store_head = [&](const float (&va)[32], const float (&vb)[32], int nn) {
+        auto store_head = [&](float (&va)[32], float (&vb)[32], float sc, int nn) {
           if (!p.tma_store) {
             if (m < p.M) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                va[j] *= sc;
+                vb[j] *= sc;
+              }
               epilogue_store_regs<H16>(p, m, nn, va);
               epilogue_store_regs<H16>(p, m, nn + 32, vb);
             }
             return;
           }
           if (row0 >= p.M) return;  // warp-uniform; rows past M are clipped by TMA
-          uint8_t* box = stg + (warp - 2) * 8192 + (stg_count & 1) * 4096;
-          if (stg_count >= 2) {
-            if (lane == 0) ptx::bulk_wait_group_read<1>();
+          // two boxes per warp in turn (streamed weights), or one (resident)
+          constexpr int kBoxes = BRES ? 1 : 2;
+          uint8_t* box = stg + (warp - 2) * (kBoxes * 4096) + (stg_count % kBoxes) * 4096;
+          if (stg_count >= kBoxes) {
+            if (lane == 0) ptx::bulk_wait_group_read<kBoxes - 1>();
             __syncwarp();
           }
           uint8_t* row = box + lane * 128;
@@ -1604,10 +1675,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           for (int q = 0; q < 8; ++q) {
             const float* v = q < 4 ? &va[q * 8] : &vb[(q - 4) * 8];
             uint4 o;
-            o.x = pack16x2<H16>(v[0], v[1]);
-            o.y = pack16x2<H16>(v[2], v[3]);
-            o.z = pack16x2<H16>(v[4], v[5]);
-            o.w = pack16x2<H16>(v[6], v[7]);
+            o.x = pack16x2<H16>(v[0] * sc, v[1] * sc);
+            o.y = pack16x2<H16>(v[2] * sc, v[3] * sc);
+            o.z = pack16x2<H16>(v[4] * sc, v[5] * sc);
+            o.w = pack16x2<H16>(v[6] * sc, v[7] * sc);
             *reinterpret_cast<uint4*>(row + ((q ^ (lane & 7)) << 4)) = o;
           }
           ptx::fence_proxy_async_smem();
@@ -1620,7 +1691,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         };
         // this token's rotation, computed once for the warp's heads of the tile
         RopeAngles<EPI> angles;
-        if (tn * BN2 + c_half < ae.n_qk * 64) rope_angles<EPI>(pos, l2t, angles);
+        if (tn * BN2 + c_half < ae.n_qk * 64) rope_angles<EPI>(pos, sfreq, angles);
         for (int hc = c_half; hc < c_half + BN2 / 2; hc += 64) {
           const int n0 = tn * BN2 + hc;
           if (n0 >= p.N) break;  // warp-uniform
@@ -1634,14 +1705,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           float va[32], vb[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            va[j] = __uint_as_float(ra[j]) * rs;
-            vb[j] = __uint_as_float(rb[j]) * rs;
+            va[j] = __uint_as_float(ra[j]);
+            vb[j] = __uint_as_float(rb[j]);
           }
           const int head = n0 >> 6;
+          float sc = rs;  // value heads: the token's RMSNorm factor only
           if (head < ae.n_qk)  // warp-uniform: query and key heads
-            attn_head<EPI>(va, vb, head < ae.n_q ? __ldg(ae.q_gain + head) : 1.0f, angles,
-                           ae.eps);
-          store_head(va, vb, n0);
+            sc = attn_head<EPI>(va, vb, rs, head < ae.n_q ? __ldg(ae.q_gain + head) : 1.0f,
+                                angles, ae.eps);
+          store_head(va, vb, sc, n0);
         }
       }
       ptx::tc_fence_before();
@@ -1744,15 +1816,15 @@ mlp_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
   return MLP_OK;
 }
 
-template <int STAGES, int H16, int EPI = 0>
+template <int STAGES, int H16, int EPI = 0, bool BRES = false>
 mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                        const TcParams& p, cudaStream_t st, const AttnEpi& ae = AttnEpi{}) {
-  using L = Layout2<STAGES, (EPI > 0 ? 8192 : 4096)>;
+  using L = PairLayout<STAGES, EPI, BRES>;
   static_assert(L::SMEM <= 232448, "pair kernel shared memory");
   static bool configured = false;
   static int max_pairs = 0;
   if (!configured) {
-    if (cudaFuncSetAttribute(tc_gemm_pair_kernel<STAGES, H16, EPI>,
+    if (cudaFuncSetAttribute(tc_gemm_pair_kernel<STAGES, H16, EPI, BRES>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
       return MLP_ERR_CUDA;
     // pairs that fit at once (a GPC with an odd number of free SMs leaves one over)
@@ -1761,7 +1833,8 @@ mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
     cfg.blockDim = dim3(kPairThreads);
     cfg.dynamicSmemBytes = L::SMEM;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<STAGES, H16, EPI>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<STAGES, H16, EPI, BRES>, &cfg) !=
+            cudaSuccess ||
         n < 1) {
       cudaGetLastError();
       n = num_sms() / 2;
@@ -1774,7 +1847,7 @@ mlp_status launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
   {
     LaunchScope ls(EPI ? "attn_prep_gemm" : (p.splits > 1 ? "gemm_tc_pair_splitk" : "gemm_tc_pair"),
                    st, p.M, p.N, p.K);
-    launch_k(tc_gemm_pair_kernel<STAGES, H16, EPI>, dim3(2 * pairs), dim3(kPairThreads),
+    launch_k(tc_gemm_pair_kernel<STAGES, H16, EPI, BRES>, dim3(2 * pairs), dim3(kPairThreads),
              p.tma_store ? L::SMEM : L::SMEM_BASE, st, ta, tb, tc, p, ae);
   }
   MLP_CHECK(launch_status());
@@ -2122,6 +2195,14 @@ mlp_status launch_attn_prep_gemm(const GemmArgs& g, const float* rstd, const flo
   ae.seq_len = seq_len;
   ae.eps = eps;
   ae.theta = theta;
+  // K up to 512: the weights stay resident and only the token rows stream
+  if (p.k_blocks <= kBResBlocks) {
+    switch (rope_dims) {
+      case 16: return launch_pair<4, 0, 16, true>(ta, tb, tc, p, st, ae);
+      case 32: return launch_pair<4, 0, 32, true>(ta, tb, tc, p, st, ae);
+      default: return launch_pair<4, 0, 64, true>(ta, tb, tc, p, st, ae);
+    }
+  }
   switch (rope_dims) {
     case 16: return launch_pair<5, 0, 16>(ta, tb, tc, p, st, ae);
     case 32: return launch_pair<5, 0, 32>(ta, tb, tc, p, st, ae);

@@ -51,7 +51,8 @@ def _check(got, ref, n_q, n_kv):
 @pytest.mark.parametrize("T,d,n_q,n_kv,R,seq_len", [(1000, 512, 8, 4, 32, 128),
                                                     (300, 136, 2, 1, 16, 7),
                                                     (513, 512, 4, 4, 64, 1024),
-                                                    (1, 64, 1, 1, 32, 1)])
+                                                    (1, 64, 1, 1, 32, 1),
+                                                    (300, 1024, 2, 1, 32, 64)])
 def test_attn_prep_matches_oracle(T, d, n_q, n_kv, R, seq_len):
     x, W, gain = _inputs(T, d, n_q, n_kv)
     got, rstd = _run(x, W, gain, n_q, n_kv, R, seq_len)
@@ -71,6 +72,24 @@ def test_attn_prep_full_size_sampled_rows():
     got, _ = _run(x, W, gain, n_q, n_kv, R, L)
     rows = np.unique(np.concatenate([[0, 1, L - 1, L, 2 * L + 5, T - 1],
                                      synth.randint(11, synth.STREAM_GENERIC, 40, T)]))
+    ref = oracle.attn_prep_rows(bf16_values(x).astype(np.float32),
+                                bf16_values(W).astype(np.float32), gain, rows, n_q, n_kv, 64, R, L)
+    _check(got[rows], ref, n_q, n_kv)
+
+
+def test_attn_prep_weights_reloaded_across_tile_columns():
+    """K up to 512 keeps a CTA pair's 256 weight columns resident while it
+    walks a run of token tiles down one column; with three columns (N = 640,
+    the last one ragged) over 79 token tiles, some runs cross into the next
+    column and load its weights mid-run.  Two rows of every 256-token tile,
+    one from each CTA of the pair, against the oracle."""
+    T, d, n_q, n_kv, R, L = 20000, 512, 6, 2, 32, 1000
+    x, W, gain = _inputs(T, d, n_q, n_kv, seed=5)
+    got, _ = _run(x, W, gain, n_q, n_kv, R, L)
+    tiles = np.arange((T + 255) // 256)
+    rows = np.unique(np.minimum(np.concatenate([tiles * 256 + (tiles * 37) % 128,
+                                                tiles * 256 + 128 + (tiles * 53) % 128,
+                                                [T - 1]]), T - 1))
     ref = oracle.attn_prep_rows(bf16_values(x).astype(np.float32),
                                 bf16_values(W).astype(np.float32), gain, rows, n_q, n_kv, 64, R, L)
     _check(got[rows], ref, n_q, n_kv)
