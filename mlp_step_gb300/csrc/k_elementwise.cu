@@ -912,11 +912,16 @@ mlp_status launch_mse(const void* y, const void* t, long long n, float* loss_out
 }
 
 // ------------------------------------------------------------------ row RMS
-// One warp per token: 16-byte loads of 8 bf16, the squares summed per lane in
-// index order and across lanes by a fixed butterfly, r = 1 / sqrt(ss / d + eps)
-// ("Full-Depth MLP Megakernel + Fused Attention Preprocessing", "What Worked":
-// the RMSNorm in front of the QKV projection, gain 1, folded into the
-// projection's epilogue as this per-token scale).
+// r = 1 / sqrt(ss / d + eps) per token, ss its squares summed per lane in
+// index order (16-byte loads of 8 bf16) and across the lanes by a fixed
+// butterfly ("Full-Depth MLP Megakernel + Fused Attention Preprocessing",
+// "What Worked": the RMSNorm in front of the QKV projection, gain 1, folded
+// into the projection's epilogue as this per-token scale).  A warp takes 4
+// consecutive tokens and requests the first 2 x 32 chunks of all four rows
+// (rows of up to 512 values whole) before summing any: 4 KiB in flight per
+// warp.  The loads leave the rows in L2 for the projection that reads them
+// next.
+constexpr int kRstdTok = 4, kRstdAhead = 2;
 
 __global__ void __launch_bounds__(256) row_rstd_kernel(const __nv_bfloat16* __restrict__ x,
                                                        long long T, int d, float eps,
@@ -924,31 +929,57 @@ __global__ void __launch_bounds__(256) row_rstd_kernel(const __nv_bfloat16* __re
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
-  const long long t = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const uint4* row = reinterpret_cast<const uint4*>(x + t * d);
-  float ss = 0.f;
-  for (int q = lane; q < d / 8; q += 32) {
-    const uint4 v = __ldcs(row + q);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+  const long long t0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kRstdTok;
+  if (t0 >= T) return;
+  const int chunks = d / 8;
+  uint4 v[kRstdTok][kRstdAhead];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(h[e]);
-      ss = fmaf(f.x, f.x, ss);
-      ss = fmaf(f.y, f.y, ss);
+  for (int j = 0; j < kRstdTok; ++j) {
+    const uint4* row = reinterpret_cast<const uint4*>(x + (t0 + j) * d);
+#pragma unroll
+    for (int i = 0; i < kRstdAhead; ++i)
+      v[j][i] = t0 + j < T && lane + 32 * i < chunks ? __ldg(row + lane + 32 * i)
+                                                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float ss[kRstdTok];
+#pragma unroll
+  for (int j = 0; j < kRstdTok; ++j) {
+    ss[j] = 0.f;
+    auto add = [&](const uint4& c) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&c);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        ss[j] = fmaf(f.x, f.x, ss[j]);
+        ss[j] = fmaf(f.y, f.y, ss[j]);
+      }
+    };
+#pragma unroll
+    for (int i = 0; i < kRstdAhead; ++i) add(v[j][i]);
+    if (t0 + j < T) {
+      const uint4* row = reinterpret_cast<const uint4*>(x + (t0 + j) * d);
+      for (int q = lane + 32 * kRstdAhead; q < chunks; q += 32) add(__ldg(row + q));
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (lane == 0) rstd[t] = 1.0f / sqrtf(ss / (float)d + eps);
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int j = 0; j < kRstdTok; ++j) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], o);
+  if (lane < kRstdTok && t0 + lane < T) {
+    float s = ss[0];
+#pragma unroll
+    for (int j = 1; j < kRstdTok; ++j)
+      if (lane == j) s = ss[j];
+    rstd[t0 + lane] = 1.0f / sqrtf(s / (float)d + eps);
+  }
 }
 
 mlp_status launch_row_rstd(const void* x, long long T, int d, float eps, float* rstd,
                            cudaStream_t st) {
   if (T <= 0) return MLP_OK;
   LaunchScope ls("row_rstd", st, T, d);
-  launch_k(row_rstd_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, st,
-           static_cast<const __nv_bfloat16*>(x), T, d, eps, rstd);
+  launch_k(row_rstd_kernel, dim3((unsigned)((T + 8 * kRstdTok - 1) / (8 * kRstdTok))), dim3(256),
+           0, st, static_cast<const __nv_bfloat16*>(x), T, d, eps, rstd);
   return launch_status();
 }
 
