@@ -293,6 +293,12 @@ __device__ __forceinline__ float warp_sum(float s) {
   return s;
 }
 
+__device__ __forceinline__ float warp_max(float m) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
 __device__ __forceinline__ float xent_row(const float* __restrict__ z, int label, int C,
                                           float inv_norm, void* dlog_row, int dl_dtype, int ldd,
                                           int* argmax_out, int lane) {
@@ -321,15 +327,12 @@ __device__ __forceinline__ float xent_row(const float* __restrict__ z, int label
 }
 
 // Rows of up to 1024 classes whose logits start on 16-byte boundaries: the
-// warp reads the row once (float4 per lane per 128-class segment), keeps the
-// values and their exponentials in registers, and writes dZ from them.
+// warp reads the row once (float4 per lane per 128-class segment, classes
+// past C as -inf), keeps the values and their exponentials in registers, and
+// writes dZ from them.
 template <int NSEG>
-__device__ __forceinline__ float xent_row_regs(const float* __restrict__ z, int label, int C,
-                                               float inv_norm, void* dlog_row, int dl_dtype,
-                                               int ldd, int* argmax_out, int lane) {
-  label = label < 0 ? 0 : (label >= C ? C - 1 : label);
-  float v[NSEG][4];
-  MaxIdx best{-INFINITY, 0x7fffffff};
+__device__ __forceinline__ void xent_load_row(const float* __restrict__ z, int C, int lane,
+                                              float (&v)[NSEG][4]) {
 #pragma unroll
   for (int g = 0; g < NSEG; ++g) {
     const int c0 = g * 128 + lane * 4;
@@ -340,44 +343,71 @@ __device__ __forceinline__ float xent_row_regs(const float* __restrict__ z, int 
 #pragma unroll
       for (int e = 0; e < 4; ++e) v[g][e] = c0 + e < C ? z[c0 + e] : -INFINITY;
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (v[g][e] > best.v || (v[g][e] == best.v && c0 + e < best.i)) {
-        best.v = v[g][e];
-        best.i = c0 + e;
-      }
   }
-  best = warp_argmax(best);
-  const float m = best.v;
-  // the label's logit from the lane that holds it (no second read of the row)
-  float zy = 0.f;
+}
+
+template <int NSEG>
+__device__ __forceinline__ float xent_row_regs(float (&v)[NSEG][4], float zy, int label, int C,
+                                               float inv_norm, void* dlog_row, int dl_dtype,
+                                               int ldd, int* argmax_out, int lane) {
+  // the row maximum; its first index only when the caller asks for it
+  float m;
+  int best_i = 0;
+  if (argmax_out) {
+    MaxIdx best{-INFINITY, 0x7fffffff};
 #pragma unroll
-  for (int g = 0; g < NSEG; ++g)
+    for (int g = 0; g < NSEG; ++g) {
+      const int c0 = g * 128 + lane * 4;
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (g * 128 + lane * 4 + e == label) zy = v[g][e];
-  zy = __shfl_sync(0xffffffffu, zy, (label & 127) >> 2);
+      for (int e = 0; e < 4; ++e)
+        if (v[g][e] > best.v || (v[g][e] == best.v && c0 + e < best.i)) {
+          best.v = v[g][e];
+          best.i = c0 + e;
+        }
+    }
+    best = warp_argmax(best);
+    m = best.v;
+    best_i = best.i;
+  } else {
+    m = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < NSEG; ++g)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) m = fmaxf(m, v[g][e]);
+    m = warp_max(m);
+  }
+  // e^(z - m) as the base-2 exponential of (z - m) log2(e): the rounding of
+  // the product adds |z - m| 2^-24 relative error (about 2e-6 for logits
+  // 30 apart), well inside the fp32 dZ and loss tolerances
+  constexpr float kLog2e = 1.4426950408889634f;
   float s = 0.f;
 #pragma unroll
   for (int g = 0; g < NSEG; ++g)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int c = g * 128 + lane * 4 + e;
-      v[g][e] = c < C ? expf(v[g][e] - m) : 0.f;
+      v[g][e] = c < C ? exp2f((v[g][e] - m) * kLog2e) : 0.f;
       s += v[g][e];
     }
   s = warp_sum(s);
   const float loss = m + logf(s) - zy;
   if (dlog_row) {
-    // softmax as exp(z - m) times the row's 1/s (one division per row)
-    const float inv_s = 1.0f / s;
+    // dZ = (softmax - onehot) / B: exp(z - m) times the row's one factor
+    // 1 / (s B) (zero past C, where the exponentials are zero), and 1 / B off
+    // the label's entry in the lane and segment that hold it
+    const float a = inv_norm / s;
+    const int lab_lane = (label & 127) >> 2, lab_seg = label >> 7, lab_e = label & 3;
 #pragma unroll
     for (int g = 0; g < NSEG; ++g) {
       const int c0 = g * 128 + lane * 4;
       float d[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        d[e] = c0 + e < C ? (v[g][e] * inv_s - (c0 + e == label ? 1.f : 0.f)) * inv_norm : 0.f;
+      for (int e = 0; e < 4; ++e) d[e] = v[g][e] * a;
+      if (g == lab_seg && lane == lab_lane) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (e == lab_e) d[e] -= inv_norm;
+      }
       if (c0 + 3 < ldd) {
         if (dl_dtype) {
           uint2 o;
@@ -401,28 +431,104 @@ __device__ __forceinline__ float xent_row_regs(const float* __restrict__ z, int 
       else static_cast<float*>(dlog_row)[c] = 0.f;
     }
   }
-  if (argmax_out && lane == 0) *argmax_out = best.i;
+  if (argmax_out && lane == 0) *argmax_out = best_i;
   return loss;
 }
 
 // Warp w of block b takes rows b * 8 + w, then every 8 * gridDim.x-th row
-// after it (three blocks per SM)
-// and adds their losses in that order; partial[b] is the block's sum.
+// after it (two blocks per SM) and adds their losses in that order;
+// partial[b] is the block's sum.  Each warp keeps its next kXentDepth rows in
+// flight: bulk copies into its own shared-memory row buffers, completing on
+// one mbarrier per buffer, issued as soon as the buffer's row has been read
+// into registers.  The labels of those rows are loaded as the copies are
+// issued.  Waits are bounded; a warp that gives up records the timeout and
+// waits (bounded again) for its copies still in flight before the block exits.
+constexpr int kXentDepth = 3;
+
 template <int NSEG>
-__global__ void __launch_bounds__(256, 3) xent_rows_regs_kernel(
+constexpr size_t xent_rows_smem() {
+  return (size_t)8 * kXentDepth * NSEG * 128 * sizeof(float);
+}
+
+template <int NSEG>
+__global__ void __launch_bounds__(256, 2) xent_rows_regs_kernel(
     const float* __restrict__ logits, int ldl, const int* __restrict__ labels, int B, int C,
-    float* __restrict__ partial, void* dlog, int dl_dtype, int ldd, int* argmax) {
+    float* __restrict__ partial, void* dlog, int dl_dtype, int ldd, int* argmax,
+    unsigned long long wait_ns, int* err) {
   pdl_wait();
   pdl_launch_dependents();
+  constexpr int ROWF = NSEG * 128;
+  extern __shared__ __align__(128) float xent_rows[];
+  __shared__ __align__(8) uint64_t bars[8][kXentDepth];
   __shared__ float part[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* buf = xent_rows + warp * kXentDepth * ROWF;
+  const int stride = gridDim.x * 8;
+  const int first = blockIdx.x * 8 + warp;
+  const uint32_t bytes = ((uint32_t)C * 4u + 15u) & ~15u;  // within the row pitch (ldl % 4 == 0)
+  if (lane == 0) {
+    for (int d = 0; d < kXentDepth; ++d) ptx::mbar_init(&bars[warp][d], 1);
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
+  // the first rows of this warp, and their labels
+  int lab[kXentDepth];
+#pragma unroll
+  for (int d = 0; d < kXentDepth; ++d) {
+    const int r = first + d * stride;
+    lab[d] = r < B ? labels[r] : 0;
+    if (lane == 0 && r < B) {
+      ptx::mbar_arrive_expect_tx(&bars[warp][d], bytes);
+      ptx::bulk_load_global(buf + d * ROWF, logits + (size_t)r * ldl, bytes, &bars[warp][d]);
+    }
+  }
   float li = 0.f;
-  for (int r = blockIdx.x * 8 + warp; r < B; r += gridDim.x * 8) {
+  int k = 0;
+  bool ok = true;
+  for (int r = first; r < B; r += stride, ++k) {
+    const int d = k % kXentDepth;
+    if (!ptx::mbar_wait_bounded(&bars[warp][d], (uint32_t)((k / kXentDepth) & 1), wait_ns, err,
+                                DEVERR_TIMEOUT_PRODUCER)) {
+      ok = false;
+      break;
+    }
+    const float* row = buf + d * ROWF;
+    float v[NSEG][4];
+#pragma unroll
+    for (int g = 0; g < NSEG; ++g) {
+      const int c0 = g * 128 + lane * 4;
+      if (c0 + 3 < C) {
+        const float4 q = *reinterpret_cast<const float4*>(row + c0);
+        v[g][0] = q.x; v[g][1] = q.y; v[g][2] = q.z; v[g][3] = q.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[g][e] = c0 + e < C ? row[c0 + e] : -INFINITY;
+      }
+    }
+    const int label = lab[0] < 0 ? 0 : (lab[0] >= C ? C - 1 : lab[0]);
+    const float zy = row[label];
+#pragma unroll
+    for (int j = 0; j + 1 < kXentDepth; ++j) lab[j] = lab[j + 1];
+    // every lane has read the buffer: refill it with the row kXentDepth ahead
+    __syncwarp();
+    const int rn = r + kXentDepth * stride;
+    lab[kXentDepth - 1] = rn < B ? labels[rn] : 0;
+    if (lane == 0 && rn < B) {
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive_expect_tx(&bars[warp][d], bytes);
+      ptx::bulk_load_global(buf + d * ROWF, logits + (size_t)rn * ldl, bytes, &bars[warp][d]);
+    }
     void* drow = nullptr;
     if (dlog) drow = dl_dtype ? (void*)(static_cast<uint16_t*>(dlog) + (size_t)r * ldd)
                              : (void*)(static_cast<float*>(dlog) + (size_t)r * ldd);
-    li += xent_row_regs<NSEG>(logits + (size_t)r * ldl, labels[r], C, 1.0f / (float)B, drow,
-                              dl_dtype, ldd, argmax ? argmax + r : nullptr, lane);
+    li += xent_row_regs<NSEG>(v, zy, label, C, 1.0f / (float)B, drow, dl_dtype, ldd,
+                              argmax ? argmax + r : nullptr, lane);
+  }
+  if (!ok && lane == 0) {
+    // copies issued and not yet consumed: rows k, k + 1, ... of this warp
+    for (int j = k; j < k + kXentDepth && first + j * stride < B; ++j)
+      ptx::mbar_wait_bounded(&bars[warp][j % kXentDepth], (uint32_t)((j / kXentDepth) & 1),
+                             wait_ns, err, DEVERR_TIMEOUT_TEARDOWN);
   }
   if (lane == 0) part[warp] = li;
   __syncthreads();
@@ -601,15 +707,27 @@ mlp_status launch_xent(const float* logits, int ldl, const int* labels, int B, i
                    (!dlog || ((ldd % 4) == 0 && aligned16(dlog)));
   // the register-resident rows kernel loops over rows: one wave of blocks
   // (at most as many partials as the workspace holds, one per 8 rows)
-  if (vec && blocks > num_sms() * 3) blocks = num_sms() * 3;
+  if (vec && blocks > num_sms() * 2) blocks = num_sms() * 2;
   {
   LaunchScope ls("xent", st, B, C);
+  static bool configured = false;
+  if (vec && !configured) {
+    if (cudaFuncSetAttribute(xent_rows_regs_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)xent_rows_smem<2>()) != cudaSuccess ||
+        cudaFuncSetAttribute(xent_rows_regs_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)xent_rows_smem<8>()) != cudaSuccess)
+      return MLP_ERR_CUDA;
+    configured = true;
+  }
+  const unsigned long long wait_ns = wait_limit_ns();
   if (vec && C <= 256)
-    launch_k(xent_rows_regs_kernel<2>, dim3(blocks), dim3(256), 0, st, logits, ldl, labels, B, C, partial, dlog,
-                                                     dl_dtype, ldd, argmax);
+    launch_k(xent_rows_regs_kernel<2>, dim3(blocks), dim3(256), xent_rows_smem<2>(), st, logits,
+             ldl, labels, B, C, partial, dlog, dl_dtype, ldd, argmax, wait_ns,
+             device_error_word());
   else if (vec)
-    launch_k(xent_rows_regs_kernel<8>, dim3(blocks), dim3(256), 0, st, logits, ldl, labels, B, C, partial, dlog,
-                                                     dl_dtype, ldd, argmax);
+    launch_k(xent_rows_regs_kernel<8>, dim3(blocks), dim3(256), xent_rows_smem<8>(), st, logits,
+             ldl, labels, B, C, partial, dlog, dl_dtype, ldd, argmax, wait_ns,
+             device_error_word());
   else
     launch_k(xent_rows_kernel, dim3(blocks), dim3(256), 0, st, logits, ldl, labels, B, C, partial, dlog, dl_dtype,
                                              ldd, argmax);

@@ -147,15 +147,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_ad
       : "memory");
 }
 
-// Asynchronous bulk copy of `bytes` (multiple of 16) from this CTA's shared
-// memory into another CTA's shared memory; completes as transaction bytes on
-// the destination CTA's mbarrier.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster_addr, uint32_t src_addr,
-                                                  uint32_t bytes, uint32_t mbar_cluster_addr) {
+// Asynchronous bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global memory into this CTA's shared memory; completes as
+// transaction bytes on the CTA's mbarrier.
+__device__ __forceinline__ void bulk_load_global(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                                 uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-      "[%3];" ::"r"(dst_cluster_addr),
-      "r"(src_addr), "r"(bytes), "r"(mbar_cluster_addr)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 
