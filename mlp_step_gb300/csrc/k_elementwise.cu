@@ -326,26 +326,10 @@ __device__ __forceinline__ float xent_row(const float* __restrict__ z, int label
   return loss;
 }
 
-// Rows of up to 1024 classes whose logits start on 16-byte boundaries: the
-// warp reads the row once (float4 per lane per 128-class segment, classes
-// past C as -inf), keeps the values and their exponentials in registers, and
-// writes dZ from them.
-template <int NSEG>
-__device__ __forceinline__ void xent_load_row(const float* __restrict__ z, int C, int lane,
-                                              float (&v)[NSEG][4]) {
-#pragma unroll
-  for (int g = 0; g < NSEG; ++g) {
-    const int c0 = g * 128 + lane * 4;
-    if (c0 + 3 < C) {
-      const float4 q = __ldcs(reinterpret_cast<const float4*>(z + c0));
-      v[g][0] = q.x; v[g][1] = q.y; v[g][2] = q.z; v[g][3] = q.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[g][e] = c0 + e < C ? z[c0 + e] : -INFINITY;
-    }
-  }
-}
-
+// Rows of up to 1024 classes whose logits start on 16-byte boundaries: one
+// warp holds the row in registers (4 values per lane per 128-class segment,
+// classes past C as -inf), keeps their exponentials there and writes dZ from
+// them.  zy is the label's logit.
 template <int NSEG>
 __device__ __forceinline__ float xent_row_regs(float (&v)[NSEG][4], float zy, int label, int C,
                                                float inv_norm, void* dlog_row, int dl_dtype,
@@ -379,14 +363,14 @@ __device__ __forceinline__ float xent_row_regs(float (&v)[NSEG][4], float zy, in
   // e^(z - m) as the base-2 exponential of (z - m) log2(e): the rounding of
   // the product adds |z - m| 2^-24 relative error (about 2e-6 for logits
   // 30 apart), well inside the fp32 dZ and loss tolerances
+  // (classes past C hold -inf, whose exponential is 0)
   constexpr float kLog2e = 1.4426950408889634f;
   float s = 0.f;
 #pragma unroll
   for (int g = 0; g < NSEG; ++g)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int c = g * 128 + lane * 4 + e;
-      v[g][e] = c < C ? exp2f((v[g][e] - m) * kLog2e) : 0.f;
+      v[g][e] = exp2f((v[g][e] - m) * kLog2e);
       s += v[g][e];
     }
   s = warp_sum(s);
@@ -466,10 +450,14 @@ __global__ void __launch_bounds__(256, 2) xent_rows_regs_kernel(
   const int stride = gridDim.x * 8;
   const int first = blockIdx.x * 8 + warp;
   const uint32_t bytes = ((uint32_t)C * 4u + 15u) & ~15u;  // within the row pitch (ldl % 4 == 0)
+  const int c_pad = (C + 3) & ~3;  // classes [C, c_pad) arrive with the row and are masked
   if (lane == 0) {
     for (int d = 0; d < kXentDepth; ++d) ptx::mbar_init(&bars[warp][d], 1);
     ptx::fence_mbar_init();
   }
+  // the buffers' classes past the copied bytes hold -inf for the whole launch
+  for (int d = 0; d < kXentDepth; ++d)
+    for (int c = c_pad + lane; c < ROWF; c += 32) buf[d * ROWF + c] = -INFINITY;
   __syncwarp();
   // the first rows of this warp, and their labels
   int lab[kXentDepth];
@@ -492,18 +480,16 @@ __global__ void __launch_bounds__(256, 2) xent_rows_regs_kernel(
       ok = false;
       break;
     }
-    const float* row = buf + d * ROWF;
+    float* row = buf + d * ROWF;
+    if (c_pad != C) {  // the copied row's padding past C
+      if (lane < c_pad - C) row[C + lane] = -INFINITY;
+      __syncwarp();
+    }
     float v[NSEG][4];
 #pragma unroll
     for (int g = 0; g < NSEG; ++g) {
-      const int c0 = g * 128 + lane * 4;
-      if (c0 + 3 < C) {
-        const float4 q = *reinterpret_cast<const float4*>(row + c0);
-        v[g][0] = q.x; v[g][1] = q.y; v[g][2] = q.z; v[g][3] = q.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) v[g][e] = c0 + e < C ? row[c0 + e] : -INFINITY;
-      }
+      const float4 q = *reinterpret_cast<const float4*>(row + g * 128 + lane * 4);
+      v[g][0] = q.x; v[g][1] = q.y; v[g][2] = q.z; v[g][3] = q.w;
     }
     const int label = lab[0] < 0 ? 0 : (lab[0] >= C ? C - 1 : lab[0]);
     const float zy = row[label];
