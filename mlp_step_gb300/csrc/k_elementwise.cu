@@ -326,6 +326,39 @@ __device__ __forceinline__ float xent_row(const float* __restrict__ z, int label
   return loss;
 }
 
+// Two fp32 values in one 64-bit register for the paired fp32 instructions of
+// sm_100 and later (two independent round-to-nearest operations each).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// The hardware base-2 exponential (PTX ex2.approx, results below 2^-126
+// flushed to zero).
+__device__ __forceinline__ float ex2_hw(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Rows of up to 1024 classes whose logits start on 16-byte boundaries: one
 // warp holds the row in registers (4 values per lane per 128-class segment,
 // classes past C as -inf), keeps their exponentials there and writes dZ from
@@ -360,33 +393,43 @@ __device__ __forceinline__ float xent_row_regs(float (&v)[NSEG][4], float zy, in
       for (int e = 0; e < 4; ++e) m = fmaxf(m, v[g][e]);
     m = warp_max(m);
   }
-  // e^(z - m) as the base-2 exponential of (z - m) log2(e): the rounding of
-  // the product adds |z - m| 2^-24 relative error (about 2e-6 for logits
-  // 30 apart), well inside the fp32 dZ and loss tolerances
-  // (classes past C hold -inf, whose exponential is 0)
+  // e^(z - m) as 2^(z log2(e) - m log2(e)): the argument as one fused
+  // multiply-add per element (two per paired instruction), whose roundings
+  // (of m log2(e) and of the result) shift it by about |m| 2^-23, a relative
+  // error near 1e-6 of each exponential, common to the row for the m part;
+  // well inside the fp32 dZ and loss tolerances.  Classes past C hold -inf,
+  // whose exponential is 0.  The row sum runs in two interleaved halves.
   constexpr float kLog2e = 1.4426950408889634f;
-  float s = 0.f;
+  const uint64_t l2 = f2_pack(kLog2e, kLog2e);
+  const uint64_t ml2 = f2_pack(-m * kLog2e, -m * kLog2e);
+  uint64_t s2 = f2_pack(0.f, 0.f);
 #pragma unroll
   for (int g = 0; g < NSEG; ++g)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      v[g][e] = exp2f((v[g][e] - m) * kLog2e);
-      s += v[g][e];
+    for (int h = 0; h < 2; ++h) {
+      float t0, t1;
+      f2_unpack(f2_fma(f2_pack(v[g][2 * h], v[g][2 * h + 1]), l2, ml2), t0, t1);
+      v[g][2 * h] = ex2_hw(t0);
+      v[g][2 * h + 1] = ex2_hw(t1);
+      s2 = f2_add(s2, f2_pack(v[g][2 * h], v[g][2 * h + 1]));
     }
-  s = warp_sum(s);
+  float s_lo, s_hi;
+  f2_unpack(s2, s_lo, s_hi);
+  const float s = warp_sum(s_lo + s_hi);
   const float loss = m + logf(s) - zy;
   if (dlog_row) {
     // dZ = (softmax - onehot) / B: exp(z - m) times the row's one factor
     // 1 / (s B) (zero past C, where the exponentials are zero), and 1 / B off
     // the label's entry in the lane and segment that hold it
     const float a = inv_norm / s;
+    const uint64_t a2 = f2_pack(a, a);
     const int lab_lane = (label & 127) >> 2, lab_seg = label >> 7, lab_e = label & 3;
 #pragma unroll
     for (int g = 0; g < NSEG; ++g) {
       const int c0 = g * 128 + lane * 4;
       float d[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) d[e] = v[g][e] * a;
+      f2_unpack(f2_mul(f2_pack(v[g][0], v[g][1]), a2), d[0], d[1]);
+      f2_unpack(f2_mul(f2_pack(v[g][2], v[g][3]), a2), d[2], d[3]);
       if (g == lab_seg && lane == lab_lane) {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
