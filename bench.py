@@ -788,7 +788,10 @@ class StackStep(Workload):
         self.nb, self.T, self.d, self.h = n_blocks, T, 512, 1536
         self.samples_per_step = T
         self.sustained = True
-        self.credited_flops_per_step = n_blocks * 6 * 2.0 * T * 512 * 1536
+        # six 2 T d h GEMMs per block, less the first block's input-gradient
+        # GEMM, which the step does not run (the stack input's gradient is
+        # not an output)
+        self.credited_flops_per_step = (n_blocks * 6 - 1) * 2.0 * T * 512 * 1536
         self.config = {"workload": "stack of %d MLP blocks (d 512, hidden 1536, "
                                    "LeakyReLU(0.5)^2, RMSNorm pre-norm, residual) over %d tokens "
                                    "bf16, MSE loss vs N(0,1) targets, full fwd + bwd + "

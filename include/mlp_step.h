@@ -379,8 +379,9 @@ mlp_status mse_loss_fwd_bwd(const void* y, const void* t, size_t n, float* loss_
 
 /* One training step of a stack of n_blocks blocks over T tokens with the
  * mean-squared loss on the last output: block forwards (saving each block
- * input and rstd in the workspace), MSE, block backwards in reverse order,
- * then momentum SGD with the bf16 shadow refresh.
+ * input and rstd in the workspace), MSE, block backwards in reverse order
+ * (the first block's without its input gradient, which the step does not
+ * return), then momentum SGD with the bf16 shadow refresh.
  * params, velocity, grads: fp32, per block W_gate [d][hidden] then
  * W_down [hidden][d]; params_bf16: bf16 shadow in the same layout.
  * x0, target: bf16 [T][d].  loss_out: device fp32 scalar. */

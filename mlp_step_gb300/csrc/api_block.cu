@@ -44,6 +44,8 @@ mlp_status gemm(int M, int N, int K, const void* A, int lda, int a_trans, const 
   return launch_gemm_tc(g, wait_limit_ns(), st);
 }
 
+// dx == nullptr: the weight gradients only (the input gradient of a stack's
+// first block feeds nothing).
 mlp_status block_bwd_impl(const void* x, const float* rstd, const void* wg, const void* wd,
                           const void* dy, int T, int d, int hidden, float slope, void* dx,
                           float* dwg, float* dwd, void* ws, cudaStream_t st) {
@@ -59,6 +61,7 @@ mlp_status block_bwd_impl(const void* x, const float* rstd, const void* wg, cons
   MLP_CHECK(gemm(hidden, d, T, a_ws, hidden, 1, dy, d, 0, dwd, d, st, split_ws, w.split));
   // dW_gate = x^T (r du) = n^T du   [d][hidden]
   MLP_CHECK(gemm(d, hidden, T, x, d, 1, du_ws, hidden, 0, dwg, hidden, st, split_ws, w.split));
+  if (!dx) return MLP_OK;
   // dn' = (r du) W_gate^T   [T][d], rounded to bf16 (it only feeds dx)
   MLP_CHECK(gemm(T, d, hidden, du_ws, hidden, 0, wg, hidden, 1, dn_ws, d, st, nullptr, 0, 1));
   // dx = dy + dn' - r^2 x mean(dn' x)
@@ -176,9 +179,11 @@ mlp_status mlp_stack_train_step(int n_blocks, int T, int d, int hidden, float ep
   MLP_CHECK(launch_mse(cur, target, (long long)td, loss, dy, mse, st));
   for (int l = n_blocks - 1; l >= 0; --l) {
     const void* xin = l == 0 ? x0 : (const void*)(xs + (l - 1) * td);
+    // the first block's input gradient is not an output of the step
     MLP_CHECK(block_bwd_impl(xin, rstd + (size_t)l * T, wb + l * per,
-                             wb + l * per + (size_t)d * hidden, dy, T, d, hidden, slope, dx,
-                             grads + l * per, grads + l * per + (size_t)d * hidden, blk, st));
+                             wb + l * per + (size_t)d * hidden, dy, T, d, hidden, slope,
+                             l == 0 ? nullptr : dx, grads + l * per,
+                             grads + l * per + (size_t)d * hidden, blk, st));
     void* t = dy;
     dy = dx;
     dx = t;
