@@ -117,6 +117,39 @@ def test_xent_extreme_logits_pm60():
     assert np.array_equal(am, am_ref)
 
 
+@pytest.mark.parametrize("B,C,ld", [(1000, 250, 256), (600, 1001, 1008), (700, 130, 132)])
+def test_xent_rows_ragged_classes_in_padded_pitch(B, C, ld):
+    """Batches above 256 rows take the row-buffered warp kernel (rows of up to
+    256 or 1,024 classes).  Rows of C classes in a wider pitch whose padding
+    holds huge logits: the classes past C must not reach the max, the sum or
+    dZ (C not a multiple of 4 exercises the masking of the copied padding).
+    The call without argmax (plain row max) gives the same loss and dZ bit
+    for bit."""
+    Z = synth.normal_f32((B, C), synth.STREAM_GENERIC + 7, std=3.0)
+    y = synth.labels(B, C, seed=23)
+    Zp = np.full((B, ld), 1e30, dtype=np.float32)
+    Zp[:, :C] = Z
+    Zd, yd = to_dev(Zp), to_dev(y)
+    ldd = (C + 7) // 8 * 8
+    ws = torch.empty(max(M.softmax_xent_workspace_bytes(B, C), 16), dtype=torch.uint8,
+                     device="cuda")
+    outs = []
+    for with_argmax in (True, False):
+        loss = torch.zeros(1, device="cuda")
+        dl = torch.full((B, ldd), 7.0, dtype=torch.float32, device="cuda")
+        am = torch.empty(B, dtype=torch.int32, device="cuda") if with_argmax else None
+        M.softmax_xent_fwd_bwd(Zd, yd, loss, dlogits=dl, argmax_out=am, workspace=ws, classes=C)
+        outs.append((loss.item(), dl.cpu().numpy(), am.cpu().numpy() if with_argmax else None))
+    l_ref, _, dZ_ref, am_ref = oracle.softmax_xent(Z.astype(np.float64), y)
+    loss, dl, am = outs[0]
+    assert abs(loss - l_ref) <= 2e-6 * max(1.0, abs(l_ref))
+    assert_elementwise(dl[:, :C], dZ_ref, 1e-5, 1e-7 / B, "dZ")
+    assert np.all(dl[:, C:] == 0.0)
+    ok = ~near_tie_rows(Z)
+    assert np.array_equal(am[ok], am_ref[ok])
+    assert outs[1][0] == loss and np.array_equal(outs[1][1], dl)
+
+
 # ------------------------------------------------------------------ column sums
 
 @pytest.mark.parametrize("rows,cols,dtype", [(128, 10, torch.float32), (128, 256, torch.bfloat16),
