@@ -1457,14 +1457,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         // resident B: a new tile column is loaded with this unit's A stages,
         // once the pair's MMAs on the old one have completed
         const bool load_b = !BRES || tn != b_tn;
-        if constexpr (BRES) {
-          // the next unit's token rows into L2 while this unit's stream:
-          // their loads then wait on L2 rather than on DRAM
-          if (u + 1 < ur.end && !p.a_mn) {
-            const int m_next = ((u + 1) % p.tiles_m) * 256 + (int)rank * 128;
-            for (int kb = kb0; kb < kb1; ++kb) ptx::tma_prefetch_2d(&tmA, kb * BK, m_next);
-          }
-        }
         if (BRES && load_b) {
           if (b_loads > 0 &&
               !ptx::mbar_wait_cluster_bounded(bfree, (uint32_t)((b_loads - 1) & 1), p.wait_ns,
