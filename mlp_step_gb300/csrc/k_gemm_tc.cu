@@ -1684,6 +1684,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         // this token's rotation, computed once for the warp's heads of the tile
         RopeAngles<EPI> angles;
         if (tn * BN2 + c_half < ae.n_qk * 64) rope_angles<EPI>(pos, sfreq, angles);
+        // the accumulator goes back to the MMA issuer as soon as this warp's
+        // last head of the tile is in registers
+        auto release = [&] {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (rank == 0) ptx::mbar_arrive(&tempty[acc]);
+            else ptx::mbar_arrive_remote(tempty0 + (uint32_t)acc * 8u);
+          }
+        };
+        bool released = false;
         for (int hc = c_half; hc < c_half + BN2 / 2; hc += 64) {
           const int n0 = tn * BN2 + hc;
           if (n0 >= p.N) break;  // warp-uniform
@@ -1694,6 +1705,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           ptx::tmem_ld_32x32b_x32(taddr, ra);
           ptx::tmem_ld_32x32b_x32(taddr + 32, rb);
           ptx::tmem_ld_wait();
+          if (hc + 64 >= c_half + BN2 / 2 || n0 + 64 >= p.N) {
+            release();
+            released = true;
+          }
           float va[32], vb[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -1707,12 +1722,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                                 angles, ae.eps);
           store_head(va, vb, sc, n0);
         }
+        if (!released) release();
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (rank == 0) ptx::mbar_arrive(&tempty[acc]);
-        else ptx::mbar_arrive_remote(tempty0 + (uint32_t)acc * 8u);
+      if constexpr (EPI == 0) {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0) ptx::mbar_arrive(&tempty[acc]);
+          else ptx::mbar_arrive_remote(tempty0 + (uint32_t)acc * 8u);
+        }
       }
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
