@@ -86,17 +86,14 @@ struct AttnEpi {
   float theta;          // RoPE base
 };
 
-// sin and cos of an angle a of moderate size (|a| up to ~1e5): Cody-Waite
-// reduction to r = a - 2 pi k in [-pi, pi] with 2 pi split as 6.28125 (exact
-// times any k below 2^16) plus the fp32 rest of 2 pi, then the hardware
-// sine / cosine approximations on r, whose absolute error on [-pi, pi] is
-// about 2^-21.  The RoPE angles of a sequence of 1,024 positions are below
-// 1,024 rad, so the reduced angle carries an error of about 1e-10 rad.
+// sin and cos of a RoPE angle a = pos * f, through the hardware sine and
+// cosine approximations directly.  Their reduction of the argument (a scaled
+// by 1 / (2 pi) in fp32) loses about |a| 2^-24 rad, some 1e-4 rad for the
+// angles below 1,024 rad of sequences of 1,024 positions: the same order as
+// the fp32 rounding of the product pos * f itself, and far below the bf16
+// rounding of the rotated outputs.
 __device__ __forceinline__ void rope_sincos(float a, float& sn, float& cs) {
-  const float k = rintf(a * 0.15915494309189535f);  // a / (2 pi), rounded
-  float r = fmaf(-k, 6.28125f, a);
-  r = fmaf(-k, 0.0019353071693331003f, r);
-  __sincosf(r, &sn, &cs);
+  __sincosf(a, &sn, &cs);
 }
 
 // The RoPE rotation of one token: sin and cos of pos * f_i for the R/2 pairs,
