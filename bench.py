@@ -174,10 +174,10 @@ def algorithmic_work(name):
     if base == "cast":
         return "hbm", 3.0 * sh[0]         # byte in, bf16 out
     if base == "xent":
-        B, C = sh
+        B, C = sh[0], sh[1]
         return "hbm", B * C * (4.0 + 2.0) + 8.0 * B
     if base == "colsum":
-        r, c = sh
+        r, c = sh[0], sh[1]
         return "hbm", 2.0 * r * c + 4.0 * c
     if base == "mse":
         return "hbm", 6.0 * sh[0]
